@@ -1,0 +1,290 @@
+"""Plain CPU oracle of the DFlash draft pass (test infrastructure only).
+
+This module is the independent checker for the CUDA library in
+``block_diffusion_speculative_fc_gb300``.  Only ``tests/``,
+``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` may
+import it; the product path never does.  It shares no code, tables or
+constants with the CUDA path and imports nothing from it.
+
+Everything is numpy in float64: inputs (weights, target features, which may
+have been rounded to bf16 by the input generator) are widened to float64 and
+every intermediate stays float64.  Contractions use ``numpy`` matmul; there is
+no blocking, fusion or reordering beyond the definitions below.
+
+Sources (three web pages on the method):
+  [P1] "Inside SGLang: DFlash and DFlash 2 Implementation" (blog walkthrough).
+  [P2] "[Feature] Spec V2 DFlash Support", sgl-project/sglang PR #23000.
+  [P3] CSDN article "DFlash基本原理 / DFlash推理流程" (z-lab generate loop,
+       Kimi-K2.6 draft config, SGLang flow, fused_kv_materialize).
+
+Readings taken where the pages are silent (each is also pinned by a test):
+  * RMSNorm: y = x / sqrt(mean(x^2) + eps) * g over the last axis.
+  * q/k norm: RMSNorm per head over head_dim with one gain vector [D]
+    shared by all heads.
+  * RoPE: neox ("rotate half") on the full head_dim, frequency
+    f_i = theta^(-2i/D) for i < D/2, pair (i, i + D/2).
+  * attention: scale 1/sqrt(D); query head h reads KV head h // (n_h/KVH).
+  * sliding window W > 0: a context key at position pk is visible to a
+    query at position pq iff pq - pk < W; block keys are always visible.
+  * no biases anywhere; argmax returns the lowest index among equal maxima.
+
+Parity status: every function below is pinned by ``tests/test_oracle_pins.py``
+(worked examples printed on the pages, closed forms, invariants, brute force).
+The composition ``draft_forward`` has no printed numeric example on the pages;
+it is pinned through its pinned parts and through an independent loop-level
+restatement in the test suite ("parity unpinned by the pages" for the
+composite as a whole).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+F64 = np.float64
+
+
+def _f64(a):
+    return np.asarray(a, dtype=F64)
+
+
+# ---------------------------------------------------------------------------
+# Step 1: context features.  [P3] "target model prefill": the feature of layer
+# id j is hidden_states[j + 1] (index 0 holds the embedding output), and the
+# selected states are concatenated along the feature axis in list order.
+# ---------------------------------------------------------------------------
+def extract_context_feature(hidden_states, layer_ids):
+    """hidden_states: list (embedding output first) of [rows, H_t] arrays."""
+    picked = [_f64(hidden_states[j + 1]) for j in layer_ids]
+    return np.concatenate(picked, axis=-1)
+
+
+def rms_norm(x, g, eps):
+    """RMSNorm over the last axis."""
+    x = _f64(x)
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    return x / np.sqrt(ms + eps) * _f64(g)
+
+
+def head_rms_norm(x, g, eps):
+    """Per-head RMSNorm: x [..., heads, D], one gain g [D] for all heads."""
+    return rms_norm(x, g, eps)
+
+
+def rope_frequencies(head_dim, theta):
+    i = np.arange(head_dim // 2, dtype=F64)
+    return np.power(F64(theta), -2.0 * i / head_dim)
+
+
+def rope_neox(x, positions, theta):
+    """Rotate-half RoPE.  x [n, heads, D]; positions [n] (integers).
+
+    Component i (i < D/2) and component i + D/2 form one plane, rotated by
+    the angle positions * f_i.
+    """
+    x = _f64(x)
+    d = x.shape[-1]
+    half = d // 2
+    ang = np.asarray(positions, dtype=F64)[:, None] * rope_frequencies(d, theta)[None, :]
+    c = np.cos(ang)[:, None, :]
+    s = np.sin(ang)[:, None, :]
+    lo, hi = x[..., :half], x[..., half:]
+    return np.concatenate([lo * c - hi * s, hi * c + lo * s], axis=-1)
+
+
+def linear(x, w):
+    """y = x w^T with w in [out, in] layout (no bias)."""
+    return _f64(x) @ _f64(w).T
+
+
+# [P1] Step 1 ("project_target_hidden(): fc + hidden_norm"); [P3] "target_hidden
+# = self.hidden_norm(self.fc(target_hidden))".
+def project_target_hidden(feats, fc_w, hidden_norm_g, eps):
+    """feats: list of n_sel arrays [rows, H_t] in target_layer_ids order."""
+    x = np.concatenate([_f64(f) for f in feats], axis=-1)
+    return rms_norm(linear(x, fc_w), hidden_norm_g, eps)
+
+
+def split_qkv(w_qkv, cfg):
+    """Rows of the fused projection: q (n_h*D), then k (KVH*D), then v."""
+    nq = cfg.n_heads * cfg.head_dim
+    nk = cfg.n_kv_heads * cfg.head_dim
+    return w_qkv[:nq], w_qkv[nq:nq + nk], w_qkv[nq + nk:nq + 2 * nk]
+
+
+# [P1] Step 1 (kv_proj_only -> apply_k_norm -> apply_k_rope -> set_kv_buffer,
+# once per draft layer); [P3] "fused_kv_materialize" computes the same thing.
+def context_kv(y_hat, layer_w, positions, cfg):
+    """K/V of projected context rows for one draft layer.
+
+    Returns K, V of shape [rows, KVH, D]; K is k-normed then rotated.
+    """
+    _, wk, wv = split_qkv(layer_w["qkv"], cfg)
+    rows = y_hat.shape[0]
+    k = linear(y_hat, wk).reshape(rows, cfg.n_kv_heads, cfg.head_dim)
+    v = linear(y_hat, wv).reshape(rows, cfg.n_kv_heads, cfg.head_dim)
+    k = head_rms_norm(k, layer_w["k_norm"], cfg.rms_eps)
+    k = rope_neox(k, positions, cfg.rope_theta)
+    return k, v
+
+
+def block_attention(q, k_ctx, v_ctx, k_blk, v_blk, q_pos, ctx_pos, window):
+    """Non-causal block attention ([P1] Step 4; [P3] is_causal=False).
+
+    q [S, n_h, D]; context keys/values [T, KVH, D] at positions ctx_pos [T];
+    block keys/values [S, KVH, D], always visible to every block query.
+    window > 0 keeps a context key only when q_pos - ctx_pos < window.
+    """
+    S, n_h, D = q.shape
+    kvh = k_blk.shape[1]
+    group = n_h // kvh
+    keys = np.concatenate([_f64(k_ctx), _f64(k_blk)], axis=0)      # [T+S, KVH, D]
+    vals = np.concatenate([_f64(v_ctx), _f64(v_blk)], axis=0)
+    T, n_blk = k_ctx.shape[0], k_blk.shape[0]
+    visible = np.ones((S, T + n_blk), dtype=bool)
+    if window and window > 0 and T > 0:
+        dist = np.asarray(q_pos, dtype=np.int64)[:, None] - np.asarray(ctx_pos, dtype=np.int64)[None, :]
+        visible[:, :T] = dist < window
+    out = np.empty((S, n_h, D), dtype=F64)
+    scale = 1.0 / np.sqrt(F64(D))
+    for h in range(n_h):
+        kv = h // group
+        scores = (_f64(q[:, h, :]) @ keys[:, kv, :].T) * scale     # [S, T+n_blk]
+        scores = np.where(visible, scores, -np.inf)
+        m = scores.max(axis=1, keepdims=True)
+        p = np.exp(scores - m)
+        p = p / p.sum(axis=1, keepdims=True)
+        out[:, h, :] = p @ vals[:, kv, :]
+    return out
+
+
+def silu(x):
+    return x / (1.0 + np.exp(-x))
+
+
+def draft_layer(x, layer_w, k_ctx, v_ctx, positions, window, cfg):
+    """One DFlashDecoderLayer on the block rows of one request.
+
+    x [S, H] residual stream; returns the updated residual stream.  The
+    block K/V computed here live only for this pass and are never committed.
+    """
+    S = x.shape[0]
+    D = cfg.head_dim
+    h = rms_norm(x, layer_w["in_norm"], cfg.rms_eps)
+    wq, wk, wv = split_qkv(layer_w["qkv"], cfg)
+    q = linear(h, wq).reshape(S, cfg.n_heads, D)
+    k = linear(h, wk).reshape(S, cfg.n_kv_heads, D)
+    v = linear(h, wv).reshape(S, cfg.n_kv_heads, D)
+    q = rope_neox(head_rms_norm(q, layer_w["q_norm"], cfg.rms_eps), positions, cfg.rope_theta)
+    k = rope_neox(head_rms_norm(k, layer_w["k_norm"], cfg.rms_eps), positions, cfg.rope_theta)
+    ctx_pos = np.arange(k_ctx.shape[0], dtype=np.int64)
+    a = block_attention(q, k_ctx, v_ctx, k, v, positions, ctx_pos, window)
+    x = x + linear(a.reshape(S, cfg.n_heads * D), layer_w["o"])
+    h2 = rms_norm(x, layer_w["post_norm"], cfg.rms_eps)
+    gu = linear(h2, layer_w["gate_up"])
+    gate, up = gu[:, :cfg.intermediate], gu[:, cfg.intermediate:]
+    x = x + linear(silu(gate) * up, layer_w["down"])
+    return x
+
+
+# [P1] Step 3 (block_ids = [anchor, MASK...], positions = prefix + j) and
+# Step 4 (backbone, final norm); [P3] "draft model predict".
+def draft_forward(cfg, W, anchor, ctx_kv_layers, kv_len):
+    """Draft backbone for one request.
+
+    ctx_kv_layers: per layer (K [kv_len, KVH, D], V) of the committed context.
+    Returns the final-normed hidden states [S, H].
+    """
+    S = cfg.block_size
+    ids = np.full(S, cfg.mask_token_id, dtype=np.int64)
+    ids[0] = anchor
+    x = _f64(W["embed"])[ids]
+    positions = kv_len + np.arange(S, dtype=np.int64)
+    for l in range(cfg.n_layers):
+        kc, vc = ctx_kv_layers[l]
+        x = draft_layer(x, W["layers"][l], kc[:kv_len], vc[:kv_len], positions,
+                        cfg.sliding_window[l], cfg)
+    return rms_norm(x, W["final_norm"], cfg.rms_eps)
+
+
+# [P1] Step 4 ("selects from draft_hidden[:, 1:, :] using the target vocabulary
+# head"); plain DFlash proposes argmax tokens ([P1] Sampling).
+def lm_head_argmax(hidden_rows, lm_head):
+    """Greedy ids and the top-2 logit margin of each row.
+
+    Ties resolve to the lowest index (numpy argmax convention).
+    """
+    logits = _f64(hidden_rows) @ _f64(lm_head).T
+    ids = np.argmax(logits, axis=1)
+    srt = np.sort(logits, axis=1)
+    margin = srt[:, -1] - srt[:, -2] if logits.shape[1] > 1 else np.full(len(ids), np.inf)
+    return ids.astype(np.int64), margin
+
+
+def draft_block(cfg, W, anchor, ctx_kv_layers, kv_len):
+    """Full draft pass for one request: ids [S] (col 0 = anchor), hidden [S, H], margins [S-1]."""
+    hid = draft_forward(cfg, W, anchor, ctx_kv_layers, kv_len)
+    ids, margin = lm_head_argmax(hid[1:], W["lm_head"])
+    out = np.empty(cfg.block_size, dtype=np.int64)
+    out[0] = anchor
+    out[1:] = ids
+    return out, hid, margin
+
+
+# ---------------------------------------------------------------------------
+# Step 3: verification.  [P3] "target model verify":
+#   acceptance_length = sum(cumprod(block[1:] == posterior[:-1]))
+# [P1] Step 6: commit_lens = accept_len + 1, bonus = posterior[accept_len],
+# out_tokens = accepted drafts, then bonus, then padding.
+# ---------------------------------------------------------------------------
+def accept_block(draft, posterior):
+    draft = np.asarray(draft, dtype=np.int64)
+    posterior = np.asarray(posterior, dtype=np.int64)
+    S = draft.shape[0]
+    matches = (draft[1:] == posterior[:-1]).astype(np.int64)
+    acc = int(np.cumprod(matches).sum()) if S > 1 else 0
+    bonus = int(posterior[acc])
+    out = np.zeros(S, dtype=np.int64)
+    out[:acc] = draft[1:acc + 1]
+    out[acc] = bonus
+    return acc, bonus, acc + 1, out
+
+
+def commit_output(output_ids, start, draft, acc, bonus):
+    """[P3] verify step: output_ids[start:start+acc+1] = block[:acc+1];
+    output_ids[start+acc+1] = bonus; the new start (crop index) is start+acc+1."""
+    output_ids = np.array(output_ids, copy=True)
+    output_ids[start:start + acc + 1] = np.asarray(draft, dtype=np.int64)[:acc + 1]
+    output_ids[start + acc + 1] = bonus
+    return output_ids, start + acc + 1
+
+
+class DraftContext:
+    """Committed draft K/V of one request: per layer K, V [rows, KVH, D].
+
+    Context row i sits at position i: rows are appended at positions
+    kv_len .. kv_len + n - 1 and nothing is ever overwritten.
+    """
+
+    def __init__(self, cfg):
+        self.cfg = cfg
+        shape = (0, cfg.n_kv_heads, cfg.head_dim)
+        self.k = [np.zeros(shape, F64) for _ in range(cfg.n_layers)]
+        self.v = [np.zeros(shape, F64) for _ in range(cfg.n_layers)]
+
+    @property
+    def kv_len(self):
+        return self.k[0].shape[0]
+
+    def layers(self):
+        return list(zip(self.k, self.v))
+
+    # [P1] Step 7: only the committed prefix rows of the verify features become
+    # context (prefix-valid writes).
+    def inject(self, feats, W):
+        cfg = self.cfg
+        y_hat = project_target_hidden(feats, W["fc"], W["hidden_norm"], cfg.rms_eps)
+        pos = self.kv_len + np.arange(y_hat.shape[0], dtype=np.int64)
+        for l in range(cfg.n_layers):
+            k, v = context_kv(y_hat, W["layers"][l], pos, cfg)
+            self.k[l] = np.concatenate([self.k[l], k], axis=0)
+            self.v[l] = np.concatenate([self.v[l], v], axis=0)
+        return y_hat

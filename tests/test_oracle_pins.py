@@ -1,0 +1,452 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+No check here re-types an oracle formula: each one uses a worked example
+printed on the pages (tests/golden/), a closed form, an invariant, a special
+case with a known answer, or brute force over tiny inputs.
+"""
+import itertools
+import json
+import math
+import os
+from types import SimpleNamespace
+
+import numpy as np
+import pytest
+
+from oracle import dflash_oracle as O
+from tests.loop_restatement import draft_forward_loops
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def tiny_cfg(**over):
+    base = dict(hidden=32, n_heads=4, n_kv_heads=2, head_dim=8, intermediate=48, vocab=40,
+                mask_token_id=39, block_size=4, n_layers=2, sliding_window=(0, 0),
+                rms_eps=1e-6, rope_theta=10000.0, target_hidden=16, target_layer_ids=(0, 2, 4))
+    base.update(over)
+    c = SimpleNamespace(**base)
+    c.n_sel = len(c.target_layer_ids)
+    return c
+
+
+def tiny_weights(cfg, rng, gains=True):
+    H, D = cfg.hidden, cfg.head_dim
+    g = (lambda n: rng.uniform(0.5, 1.5, n)) if gains else (lambda n: np.ones(n))
+    W = {"fc": rng.normal(0, 0.2, (H, cfg.n_sel * cfg.target_hidden)),
+         "hidden_norm": g(H), "final_norm": g(H),
+         "embed": rng.normal(0, 1.0, (cfg.vocab, H)),
+         "lm_head": rng.normal(0, 0.3, (cfg.vocab, H)), "layers": []}
+    for _ in range(cfg.n_layers):
+        W["layers"].append({
+            "qkv": rng.normal(0, 0.3, ((cfg.n_heads + 2 * cfg.n_kv_heads) * D, H)),
+            "o": rng.normal(0, 0.2, (H, cfg.n_heads * D)),
+            "gate_up": rng.normal(0, 0.2, (2 * cfg.intermediate, H)),
+            "down": rng.normal(0, 0.2, (H, cfg.intermediate)),
+            "in_norm": g(H), "post_norm": g(H), "q_norm": g(D), "k_norm": g(D)})
+    return W
+
+
+# ----------------------------------------------------------------- acceptance
+def test_accept_worked_example_p1():
+    gd = _golden("accept_worked_example_p1.json")
+    voc, ex = gd["vocab"], gd["expected"]
+    draft = [voc[t] for t in gd["block"]]
+    post = [voc[t] for t in gd["target_choices"]]
+    acc, bonus, commit, out = O.accept_block(draft, post)
+    assert acc == ex["accept_len"] and commit == ex["commit_len"]
+    assert bonus == voc[ex["bonus"]]
+    assert list(out[:commit]) == [voc[t] for t in ex["out_tokens_valid"]]
+    L = gd["prefix_len"]
+    assert list(L + np.arange(len(draft))) == ex["block_positions"]
+    output_ids = np.full(32, -1)
+    output_ids[L] = voc["of"]
+    new_ids, new_start = O.commit_output(output_ids, L, draft, acc, bonus)
+    assert new_start == ex["new_seq_len"] == ex["next_anchor_position"]
+    # inputs whose target state became valid, and the emitted tokens, at their positions
+    assert [new_ids[p] for p in ex["computed_positions"]] == [voc[t] for t in ex["computed_inputs"]]
+    assert [new_ids[p] for p in ex["emitted_positions"]] == [voc[t] for t in ex["out_tokens_valid"]]
+    assert new_ids[new_start] == voc[ex["next_anchor"]]
+
+
+def test_accept_block5_example_p3():
+    gd = _golden("accept_block5_example_p3.json")
+    voc, ex = gd["vocab"], gd["expected"]
+    acc, bonus, commit, out = O.accept_block([voc[t] for t in gd["candidates"]],
+                                             [voc[t] for t in gd["target"]])
+    assert commit == ex["accept_lens"]
+    assert bonus == voc[ex["verified_id"]]
+    assert list(out) == [voc[t] if isinstance(t, str) else t for t in ex["out_tokens"]]
+
+
+def test_accept_zero_and_full():
+    # zero survivors: one correction is emitted, the old anchor's state commits
+    acc, bonus, commit, out = O.accept_block([7, 1, 2, 3], [9, 1, 2, 3])
+    assert (acc, bonus, commit) == (0, 9, 1) and list(out) == [9, 0, 0, 0]
+    # all survive: S-1 drafts plus a bonus from the last target row
+    acc, bonus, commit, out = O.accept_block([7, 1, 2, 3], [1, 2, 3, 5])
+    assert (acc, bonus, commit) == (3, 5, 4) and list(out) == [1, 2, 3, 5]
+
+
+@pytest.mark.parametrize("S", [2, 3, 4, 8, 16])
+def test_accept_bruteforce_all_patterns(S):
+    rng = np.random.default_rng(S)
+    for bits in itertools.product([0, 1], repeat=S - 1):
+        draft = rng.integers(0, 100, S)
+        post = rng.integers(100, 200, S)           # never equal to a draft
+        for i, b in enumerate(bits):
+            if b:
+                post[i] = draft[i + 1]
+        n = 0                                       # explicit first-mismatch loop
+        while n < S - 1 and bits[n]:
+            n += 1
+        acc, bonus, commit, out = O.accept_block(draft, post)
+        assert acc == n and commit == n + 1 and bonus == post[n]
+        assert list(out[:n]) == list(draft[1:n + 1]) and out[n] == post[n]
+        assert all(v == 0 for v in out[n + 1:])
+
+
+def test_commit_crop_accumulates():
+    # the z-lab loop advances start by acceptance_length + 1 every cycle
+    ids = np.zeros(64, dtype=np.int64)
+    start = 5
+    for acc in [0, 3, 1, 3]:
+        draft = np.arange(100, 104)
+        ids, new_start = O.commit_output(ids, start, draft, acc, 999)
+        assert new_start == start + acc + 1
+        assert ids[new_start] == 999
+        assert list(ids[start:start + acc + 1]) == list(draft[:acc + 1])
+        start = new_start
+
+
+# ------------------------------------------------------- context feature concat
+def test_extract_context_feature_offset_and_order():
+    # hidden_states[k] is the constant k: the embedding output is index 0
+    hs = [np.full((3, 4), float(k)) for k in range(8)]
+    f = O.extract_context_feature(hs, [0, 2, 4])
+    assert f.shape == (3, 12)
+    for j, lid in enumerate([0, 2, 4]):
+        assert np.all(f[:, 4 * j:4 * (j + 1)] == lid + 1)
+
+
+def test_concat_column_blocks_reach_fc_in_list_order():
+    rows, Ht, n_sel, H = 3, 5, 3, 15
+    feats = [np.full((rows, Ht), j + 1.0) + np.arange(Ht) * 0.01 for j in range(n_sel)]
+    # fc rows are one-hot selectors: output r reads concat column r
+    fc = np.eye(H, n_sel * Ht)
+    y = O.linear(np.concatenate(feats, -1), fc)
+    for j in range(n_sel):
+        assert np.allclose(y[:, j * Ht:(j + 1) * Ht], feats[j])
+    # with a unit gain the norm of the projection only rescales rows
+    yh = O.project_target_hidden(feats, fc, np.ones(H), 0.0)
+    assert np.allclose(yh / yh[:, :1], y / y[:, :1])
+
+
+# ----------------------------------------------------------------- RMSNorm
+def test_rms_norm_hand_vector_and_invariants():
+    y = O.rms_norm(np.array([[3.0, 4.0]]), np.ones(2), 0.0)
+    assert np.allclose(y, [[3 / math.sqrt(12.5), 4 / math.sqrt(12.5)]])
+    rng = np.random.default_rng(0)
+    x = rng.normal(size=(5, 64))
+    eps = 1e-6
+    y = O.rms_norm(x, np.ones(64), eps)
+    ms = np.mean(x * x, axis=1)
+    assert np.allclose(np.sqrt(np.mean(y * y, axis=1)), np.sqrt(ms / (ms + eps)))
+    assert np.allclose(O.rms_norm(7.0 * x, np.ones(64), 0.0), O.rms_norm(x, np.ones(64), 0.0))
+    g = rng.uniform(0.5, 1.5, 64)
+    assert np.allclose(O.rms_norm(x, g, eps), O.rms_norm(x, np.ones(64), eps) * g)
+
+
+def test_head_rms_norm_is_per_head():
+    rng = np.random.default_rng(1)
+    x = rng.normal(size=(3, 4, 8))
+    x[:, 2] *= 100.0                     # one loud head must not affect the others
+    y = O.head_rms_norm(x, np.ones(8), 0.0)
+    assert np.allclose(np.sqrt(np.mean(y * y, axis=-1)), 1.0)
+
+
+# --------------------------------------------------------------------- RoPE
+def test_rope_position_zero_is_identity():
+    x = np.random.default_rng(2).normal(size=(3, 2, 16))
+    assert np.allclose(O.rope_neox(x, [0, 0, 0], 1e6), x)
+
+
+def test_rope_planes_are_i_and_i_plus_half():
+    D, theta = 16, 10000.0
+    for i in (0, 1, 5):
+        e = np.zeros((1, 1, D))
+        e[0, 0, i] = 1.0
+        p = 7
+        y = O.rope_neox(e, [p], theta)[0, 0]
+        ang = p * theta ** (-2.0 * i / D)            # frequency of plane i
+        expect = np.zeros(D)
+        expect[i], expect[i + D // 2] = math.cos(ang), math.sin(ang)
+        assert np.allclose(y, expect)
+
+
+def test_rope_norm_relative_and_composition():
+    rng = np.random.default_rng(3)
+    D, theta = 32, 1e6
+    q = rng.normal(size=(1, 1, D))
+    k = rng.normal(size=(1, 1, D))
+    qr = O.rope_neox(q, [11], theta)
+    assert np.allclose(np.linalg.norm(qr), np.linalg.norm(q))
+    dots = [float(np.sum(O.rope_neox(q, [m], theta) * O.rope_neox(k, [m - 4], theta)))
+            for m in (4, 9, 1000, 32000)]
+    assert np.allclose(dots, dots[0], atol=1e-9)
+    two = O.rope_neox(O.rope_neox(q, [5], theta), [9], theta)
+    assert np.allclose(two, O.rope_neox(q, [14], theta))
+
+
+# ---------------------------------------------------------------- projections
+def test_linear_matches_triple_loop():
+    rng = np.random.default_rng(4)
+    x, w = rng.normal(size=(3, 5)), rng.normal(size=(4, 5))
+    y = O.linear(x, w)
+    for i in range(3):
+        for o in range(4):
+            assert math.isclose(y[i, o], sum(x[i, k] * w[o, k] for k in range(5)), rel_tol=1e-12)
+
+
+def test_split_qkv_row_order():
+    cfg = tiny_cfg()
+    D = cfg.head_dim
+    w = np.arange((cfg.n_heads + 2 * cfg.n_kv_heads) * D)[:, None] * np.ones((1, 3))
+    q, k, v = O.split_qkv(w, cfg)
+    assert q[0, 0] == 0 and k[0, 0] == cfg.n_heads * D
+    assert v[0, 0] == (cfg.n_heads + cfg.n_kv_heads) * D and v.shape[0] == cfg.n_kv_heads * D
+
+
+def test_silu_closed_form():
+    assert O.silu(np.array(0.0)) == 0.0
+    assert math.isclose(float(O.silu(np.array(1.0))), 1 / (1 + math.exp(-1)))
+    assert math.isclose(float(O.silu(np.array(40.0))), 40.0, rel_tol=1e-12)
+
+
+# ---------------------------------------------------------------- attention
+def _attn_loops(q, kc, vc, kb, vb, q_pos, ctx_pos, window):
+    S, nh, D = q.shape
+    grp = nh // kb.shape[1]
+    out = np.zeros_like(q)
+    for j in range(S):
+        for h in range(nh):
+            g = h // grp
+            keys, vals = [], []
+            for t in range(kc.shape[0]):
+                if window == 0 or q_pos[j] - ctx_pos[t] < window:
+                    keys.append(kc[t, g]); vals.append(vc[t, g])
+            for t in range(S):
+                keys.append(kb[t, g]); vals.append(vb[t, g])
+            sc = [float(np.dot(q[j, h], kk)) / math.sqrt(D) for kk in keys]
+            m = max(sc)
+            e = [math.exp(s - m) for s in sc]
+            out[j, h] = sum(ei * vv for ei, vv in zip(e, vals)) / sum(e)
+    return out
+
+
+@pytest.mark.parametrize("window", [0, 1, 3, 6])
+def test_attention_bruteforce(window):
+    rng = np.random.default_rng(5 + window)
+    S, nh, kvh, D, T = 4, 4, 2, 8, 7
+    q = rng.normal(size=(S, nh, D))
+    kc, vc = rng.normal(size=(T, kvh, D)), rng.normal(size=(T, kvh, D))
+    kb, vb = rng.normal(size=(S, kvh, D)), rng.normal(size=(S, kvh, D))
+    q_pos, ctx_pos = T + np.arange(S), np.arange(T)
+    got = O.block_attention(q, kc, vc, kb, vb, q_pos, ctx_pos, window)
+    assert np.allclose(got, _attn_loops(q, kc, vc, kb, vb, q_pos, ctx_pos, window), atol=1e-12)
+
+
+def test_attention_special_cases():
+    rng = np.random.default_rng(6)
+    S, nh, kvh, D, T = 3, 2, 1, 4, 5
+    q = rng.normal(size=(S, nh, D))
+    # identical keys: uniform weights, so the output is the mean of the values
+    k = np.tile(rng.normal(size=(1, kvh, D)), (T, 1, 1))
+    kb = np.tile(k[:1], (S, 1, 1))
+    vc, vb = rng.normal(size=(T, kvh, D)), rng.normal(size=(S, kvh, D))
+    out = O.block_attention(q, k, vc, kb, vb, T + np.arange(S), np.arange(T), 0)
+    mean_v = np.concatenate([vc, vb])[:, 0].mean(axis=0)
+    assert np.allclose(out, mean_v[None, None, :])
+    # one block row, window 1: no context key is visible, the output is that row's value
+    out = O.block_attention(q[:1], rng.normal(size=(T, kvh, D)), vc, kb[:1], vb[:1],
+                            [T], np.arange(T), 1)
+    assert np.allclose(out[0], vb[0, 0])
+
+
+def test_attention_window_edges():
+    # a context key at distance W-1 is visible, at distance W it is not
+    D = 4
+    W = 3
+    q = np.zeros((1, 1, D)); q[0, 0, 0] = 50.0          # strongly prefers key direction e0
+    kc = np.zeros((4, 1, D)); vc = np.zeros((4, 1, D))
+    q_pos = [10]
+    ctx_pos = np.array([7, 8, 2, 3])                    # distances 3, 2, 8, 7
+    kc[1, 0, 0] = 1.0; vc[1, 0, 1] = 1.0                # distance 2 = W-1: visible, wins
+    kc[0, 0, 0] = 2.0; vc[0, 0, 2] = 1.0                # distance 3 = W: hidden although larger
+    kb = np.zeros((1, 1, D)); vb = np.zeros((1, 1, D))
+    out = O.block_attention(q, kc, vc, kb, vb, q_pos, ctx_pos, W)
+    assert out[0, 0, 1] > 0.99 and out[0, 0, 2] == 0.0
+
+
+def test_attention_is_non_causal_and_gqa_grouped():
+    rng = np.random.default_rng(7)
+    S, nh, kvh, D, T = 4, 4, 2, 8, 3
+    q = rng.normal(size=(S, nh, D))
+    kc, vc = rng.normal(size=(T, kvh, D)), rng.normal(size=(T, kvh, D))
+    kb, vb = rng.normal(size=(S, kvh, D)), rng.normal(size=(S, kvh, D))
+    args = (T + np.arange(S), np.arange(T), 0)
+    base = O.block_attention(q, kc, vc, kb, vb, *args)
+    vb2 = vb.copy(); vb2[S - 1] += 1.0                  # last block row changes row 0
+    assert not np.allclose(O.block_attention(q, kc, vc, kb, vb2, *args)[0], base[0])
+    vc2 = vc.copy(); vc2[:, 1] += 1.0                   # KV head 1 feeds query heads 2,3 only
+    alt = O.block_attention(q, kc, vc2, kb, vb, *args)
+    assert np.allclose(alt[:, :2], base[:, :2]) and not np.allclose(alt[:, 2:], base[:, 2:])
+
+
+# ----------------------------------------------------------------- lm head
+def test_lm_head_argmax_planted_and_ties():
+    H, V = 6, 9
+    w = np.zeros((V, H))
+    for v in range(V):
+        w[v, v % H] = 1.0                               # logit v = x[v % H]
+    x = np.array([[0, 0, 5.0, 0, 0, 0], [0, 1.0, 0, 0, 0, 0.5]])
+    ids, margin = O.lm_head_argmax(x, w)
+    assert list(ids) == [2, 1]                          # 2 ties with 8 and 1 with 7: lowest index
+    assert margin[0] == 0.0 and margin[1] == 0.0
+    x = np.array([[0, 0, 0, 3.0, 1.0, 0]])
+    ids, margin = O.lm_head_argmax(x, w[:6])
+    assert ids[0] == 3 and margin[0] == 2.0
+
+
+# ------------------------------------------------------ injection and context
+def test_inject_positions_continue_across_calls():
+    cfg = tiny_cfg()
+    rng = np.random.default_rng(8)
+    W = tiny_weights(cfg, rng)
+    feats = [rng.normal(size=(6, cfg.target_hidden)) for _ in range(cfg.n_sel)]
+    a = O.DraftContext(cfg)
+    a.inject(feats, W)
+    b = O.DraftContext(cfg)
+    b.inject([f[:2] for f in feats], W)
+    b.inject([f[2:] for f in feats], W)
+    assert a.kv_len == b.kv_len == 6
+    for l in range(cfg.n_layers):
+        assert np.allclose(a.k[l], b.k[l]) and np.allclose(a.v[l], b.v[l])
+    # un-rotating row i by its position gives back a unit-RMS head
+    k0 = O.rope_neox(a.k[0], -np.arange(6), cfg.rope_theta)
+    gk = W["layers"][0]["k_norm"]
+    assert np.allclose(np.sqrt(np.mean((k0 / gk) ** 2, axis=-1)), 1.0, atol=1e-5)
+
+
+def test_context_rows_are_rotated_by_their_positions():
+    cfg = tiny_cfg()
+    rng = np.random.default_rng(9)
+    W = tiny_weights(cfg, rng)
+    y = rng.normal(size=(3, cfg.hidden))
+    k0, v0 = O.context_kv(y, W["layers"][0], np.array([0, 0, 0]), cfg)
+    k5, v5 = O.context_kv(y, W["layers"][0], np.array([5, 6, 7]), cfg)
+    assert np.allclose(v0, v5)
+    assert np.allclose(O.rope_neox(k0, [5, 6, 7], cfg.rope_theta), k5)
+
+
+# --------------------------------------------------- composition (loop level)
+def _to_lists(W):
+    out = {k: np.asarray(v).tolist() for k, v in W.items() if k != "layers"}
+    out["layers"] = [{k: np.asarray(v).tolist() for k, v in L.items()} for L in W["layers"]]
+    return out
+
+
+@pytest.mark.parametrize("window", [(0, 0), (3, 0)])
+def test_draft_forward_matches_loop_restatement(window):
+    cfg = tiny_cfg(sliding_window=window)
+    rng = np.random.default_rng(10)
+    W = tiny_weights(cfg, rng)
+    ctx = O.DraftContext(cfg)
+    feats = [rng.normal(size=(6, cfg.target_hidden)) for _ in range(cfg.n_sel)]
+    ctx.inject(feats, W)
+    got = O.draft_forward(cfg, W, 5, ctx.layers(), ctx.kv_len)
+    ref = draft_forward_loops(cfg, _to_lists(W), 5, [k.tolist() for k in ctx.k],
+                              [v.tolist() for v in ctx.v], ctx.kv_len)
+    assert np.allclose(got, np.array(ref), rtol=1e-10, atol=1e-10)
+
+
+def test_draft_block_ids_layout():
+    cfg = tiny_cfg()
+    rng = np.random.default_rng(11)
+    W = tiny_weights(cfg, rng)
+    ctx = O.DraftContext(cfg)
+    ctx.inject([rng.normal(size=(4, cfg.target_hidden)) for _ in range(cfg.n_sel)], W)
+    ids, hid, margin = O.draft_block(cfg, W, 17, ctx.layers(), ctx.kv_len)
+    assert ids[0] == 17 and len(ids) == cfg.block_size and len(margin) == cfg.block_size - 1
+    logits = hid[1:] @ W["lm_head"].T
+    assert list(ids[1:]) == [int(np.argmax(r)) for r in logits]
+
+
+def test_draft_block_does_not_depend_on_cache_rows_past_kv_len():
+    cfg = tiny_cfg()
+    rng = np.random.default_rng(12)
+    W = tiny_weights(cfg, rng)
+    ctx = O.DraftContext(cfg)
+    ctx.inject([rng.normal(size=(5, cfg.target_hidden)) for _ in range(cfg.n_sel)], W)
+    a = O.draft_forward(cfg, W, 3, ctx.layers(), 3)
+    junk = [(np.concatenate([k[:3], 9 + k[3:]]), v) for k, v in ctx.layers()]
+    assert np.allclose(a, O.draft_forward(cfg, W, 3, junk, 3))
+
+
+# ------------------------------------- planted mistakes must trip these pins
+def test_pins_catch_planted_mistakes(monkeypatch):
+    """Plant plausible mistakes in the oracle (CPU only) and check a pin fails."""
+    # 1. interleaved (GPT-J) RoPE pairs instead of rotate-half
+    def rope_interleaved(x, positions, theta):
+        x = np.asarray(x, float)
+        d = x.shape[-1]
+        ang = np.asarray(positions, float)[:, None] * O.rope_frequencies(d, theta)[None]
+        c, s = np.cos(ang)[:, None], np.sin(ang)[:, None]
+        ev, od = x[..., 0::2], x[..., 1::2]
+        out = np.empty_like(x)
+        out[..., 0::2], out[..., 1::2] = ev * c - od * s, od * c + ev * s
+        return out
+    monkeypatch.setattr(O, "rope_neox", rope_interleaved)
+    with pytest.raises(AssertionError):
+        test_rope_planes_are_i_and_i_plus_half()
+    monkeypatch.undo()
+    # 2. causal mask inside the block
+    orig = O.block_attention
+
+    def causal(q, kc, vc, kb, vb, q_pos, ctx_pos, window):
+        out = np.empty_like(np.asarray(q, float))
+        for j in range(q.shape[0]):
+            out[j:j + 1] = orig(q[j:j + 1], kc, vc, kb[:j + 1], vb[:j + 1], q_pos[j:j + 1],
+                                ctx_pos, window)
+        return out
+    monkeypatch.setattr(O, "block_attention", causal)
+    with pytest.raises(AssertionError):
+        test_attention_is_non_causal_and_gqa_grouped()
+    monkeypatch.undo()
+    # 3. off-by-one acceptance (count the first mismatch as accepted)
+    orig_acc = O.accept_block
+
+    def acc_plus_one(d, p):
+        a, b, c, o = orig_acc(d, p)
+        a = min(a + 1, len(d) - 1)
+        return a, int(np.asarray(p)[a]), a + 1, o
+    monkeypatch.setattr(O, "accept_block", acc_plus_one)
+    with pytest.raises(AssertionError):
+        test_accept_worked_example_p1()
+    monkeypatch.undo()
+    # 4. hidden-state offset forgotten
+    monkeypatch.setattr(O, "extract_context_feature",
+                        lambda hs, ids: np.concatenate([hs[j] for j in ids], -1))
+    with pytest.raises(AssertionError):
+        test_extract_context_feature_offset_and_order()
+    monkeypatch.undo()
+    # 5. RMSNorm gain dropped
+    monkeypatch.setattr(O, "rms_norm", lambda x, g, eps: np.asarray(x, float) / np.sqrt(
+        np.mean(np.asarray(x, float) ** 2, -1, keepdims=True) + eps))
+    with pytest.raises(AssertionError):
+        test_rms_norm_hand_vector_and_invariants()
+    monkeypatch.undo()
