@@ -1,0 +1,447 @@
+// C-ABI runtime of the DFlash draft-pass library: handle, validation,
+// workspace plan and the launch sequence of each entry point.
+#include <algorithm>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/dflash.h"
+#include "kernels.h"
+
+using namespace dflash;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int st, const std::string &msg) {
+  g_last_error = msg;
+  return st;
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct Layout {
+  size_t err, rope, x, h, qb, kb, vb, attn, act, row_pos, keys, y, yh, slot, rpos, total;
+};
+
+}  // namespace
+
+struct dflash_handle {
+  dflash_config cfg;
+  std::vector<int32_t> window;
+  const void *fc_w, *hidden_norm_g, *final_norm_g, *embed, *lm_head;
+  std::vector<const void *> qkv_w, o_w, gate_up_w, down_w, in_norm_g, post_norm_g, q_norm_g,
+      k_norm_g;
+  Layout L;
+  char *ws = nullptr;
+  size_t ws_bytes = 0;
+  int store;      // ST_F32 / ST_BF16
+  size_t es;      // element size of the configured dtype
+};
+
+namespace {
+
+Layout plan(const dflash_config &c, size_t es) {
+  Layout L{};
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align_up(o + std::max<size_t>(bytes, 1), 256);
+    return at;
+  };
+  const size_t M = (size_t)c.max_batch * c.block_size;
+  const size_t R = (size_t)c.max_rows;
+  const size_t H = c.hidden, D = c.head_dim;
+  L.err = take(256);
+  L.rope = take(sizeof(float) * 2 * (size_t)c.max_position * (D / 2));
+  L.x = take(4 * M * H);
+  L.h = take(es * M * H);
+  L.qb = take(es * M * c.n_heads * D);
+  L.kb = take(es * M * c.n_kv_heads * D);
+  L.vb = take(es * M * c.n_kv_heads * D);
+  L.attn = take(es * M * c.n_heads * D);
+  L.act = take(es * M * c.intermediate);
+  L.row_pos = take(4 * M);
+  L.keys = take(8 * M);
+  L.y = take(4 * R * H);
+  L.yh = take(es * R * H);
+  L.slot = take(4 * R);
+  L.rpos = take(4 * R);
+  L.total = o;
+  return L;
+}
+
+template <typename P> P *at(dflash_handle *h, size_t off) { return (P *)(h->ws + off); }
+
+int check_cuda(cudaError_t e, const char *what) {
+  if (e == cudaSuccess) return DFLASH_OK;
+  return fail(DFLASH_ECUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+cudaError_t run_gemm(dflash_handle *h, const GemmProblem &P, cudaStream_t s) {
+  return launch_gemm_simt(h->store, P, s);
+}
+
+EpiParams epi_base(const dflash_handle *h, int op) {
+  EpiParams e;
+  std::memset(&e, 0, sizeof(e));
+  e.op = op;
+  e.n_heads = h->cfg.n_heads;
+  e.n_kv_heads = h->cfg.n_kv_heads;
+  e.head_dim = h->cfg.head_dim;
+  e.eps = h->cfg.rms_eps;
+  return e;
+}
+
+GemmProblem problem_1src(const void *A, int64_t lda, int M, int K) {
+  GemmProblem P;
+  std::memset(&P, 0, sizeof(P));
+  P.A.ptr[0] = A;
+  P.A.ld = lda;
+  P.A.k_per_src = K;
+  P.A.n_src = 1;
+  P.M = M;
+  P.K = K;
+  return P;
+}
+
+void add_seg(GemmProblem &P, const void *W, int64_t ldw, int N, const EpiParams &e) {
+  GemmSeg &s = P.seg[P.nseg++];
+  s.W = W;
+  s.ldw = ldw;
+  s.N = N;
+  s.epi = e;
+}
+
+int check_kv(const dflash_handle *h, const dflash_kv *kv) {
+  if (!kv) return fail(DFLASH_EINVAL, "kv is NULL");
+  if (!kv->k_pages || !kv->v_pages || !kv->page_table || !kv->kv_len)
+    return fail(DFLASH_EINVAL, "kv: k_pages, v_pages, page_table and kv_len must be non-NULL");
+  if (kv->pages_per_req <= 0 || kv->n_pages <= 0)
+    return fail(DFLASH_EINVAL, "kv: pages_per_req and n_pages must be positive");
+  for (int l = 0; l < h->cfg.n_layers; ++l)
+    if (!kv->k_pages[l] || !kv->v_pages[l])
+      return fail(DFLASH_EINVAL, "kv: NULL page pointer for layer " + std::to_string(l));
+  return DFLASH_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *dflash_status_string(int st) {
+  switch (st) {
+    case DFLASH_OK: return "ok";
+    case DFLASH_EINVAL: return "invalid argument";
+    case DFLASH_EUNSUPPORTED: return "unsupported shape";
+    case DFLASH_ECAPACITY: return "capacity exceeded";
+    case DFLASH_ECUDA: return "CUDA error";
+    case DFLASH_EDEVICE: return "device-side error flagged";
+    case DFLASH_ESTATE: return "no workspace bound";
+    default: return "unknown status";
+  }
+}
+
+const char *dflash_last_error(void) { return g_last_error.c_str(); }
+
+int dflash_create(const dflash_config *cfg, const dflash_weights *w, dflash_handle **out) {
+  if (!out) return fail(DFLASH_EINVAL, "out is NULL");
+  *out = nullptr;
+  if (!cfg || !w) return fail(DFLASH_EINVAL, "cfg and weights must be non-NULL");
+  const dflash_config &c = *cfg;
+  if (c.dtype != DFLASH_F32 && c.dtype != DFLASH_BF16) return fail(DFLASH_EUNSUPPORTED, "dtype");
+  if (c.target_hidden <= 0 || c.n_sel <= 0 || c.hidden <= 0 || c.n_layers <= 0 || c.n_heads <= 0 ||
+      c.n_kv_heads <= 0 || c.head_dim <= 0 || c.intermediate <= 0 || c.vocab <= 1 ||
+      c.block_size <= 0 || c.max_batch <= 0 || c.max_rows <= 0 || c.max_position <= 0)
+    return fail(DFLASH_EINVAL, "every size in the config must be positive");
+  if (c.n_sel > kMaxSrc) return fail(DFLASH_EUNSUPPORTED, "n_sel must be <= 8");
+  if (c.head_dim != 64 && c.head_dim != 128) return fail(DFLASH_EUNSUPPORTED, "head_dim must be 64 or 128");
+  if (c.n_heads % c.n_kv_heads) return fail(DFLASH_EUNSUPPORTED, "n_heads must be a multiple of n_kv_heads");
+  if (c.hidden % 128 || c.target_hidden % 128 || c.intermediate % 128 || (c.n_heads * c.head_dim) % 128 ||
+      (c.n_kv_heads * c.head_dim) % 64)
+    return fail(DFLASH_EUNSUPPORTED, "hidden, target_hidden, intermediate, n_heads*head_dim must be multiples of 128");
+  if (c.block_size < 2 || c.block_size > 32) return fail(DFLASH_EUNSUPPORTED, "block_size must be in [2, 32]");
+  if ((c.n_heads / c.n_kv_heads) * c.block_size > 128)
+    return fail(DFLASH_EUNSUPPORTED, "(n_heads/n_kv_heads)*block_size must be <= 128");
+  if (c.page_size != 64) return fail(DFLASH_EUNSUPPORTED, "page_size must be 64");
+  if (c.mask_token_id < 0 || c.mask_token_id >= c.vocab) return fail(DFLASH_EINVAL, "mask_token_id outside the vocabulary");
+  if (!(c.rms_eps >= 0.f) || !(c.rope_theta > 0.f)) return fail(DFLASH_EINVAL, "rms_eps >= 0 and rope_theta > 0 required");
+  if (c.max_position < c.block_size) return fail(DFLASH_EINVAL, "max_position < block_size");
+  if (!c.sliding_window) return fail(DFLASH_EINVAL, "sliding_window array is NULL");
+  for (int l = 0; l < c.n_layers; ++l)
+    if (c.sliding_window[l] < 0) return fail(DFLASH_EINVAL, "negative sliding_window");
+  if (!w->fc_w || !w->hidden_norm_g || !w->final_norm_g || !w->embed || !w->lm_head || !w->qkv_w ||
+      !w->o_w || !w->gate_up_w || !w->down_w || !w->in_norm_g || !w->post_norm_g || !w->q_norm_g ||
+      !w->k_norm_g)
+    return fail(DFLASH_EINVAL, "a weight pointer is NULL");
+  for (int l = 0; l < c.n_layers; ++l)
+    if (!w->qkv_w[l] || !w->o_w[l] || !w->gate_up_w[l] || !w->down_w[l] || !w->in_norm_g[l] ||
+        !w->post_norm_g[l] || !w->q_norm_g[l] || !w->k_norm_g[l])
+      return fail(DFLASH_EINVAL, "a per-layer weight pointer is NULL (layer " + std::to_string(l) + ")");
+
+  dflash_handle *h = new dflash_handle();
+  h->cfg = c;
+  h->window.assign(c.sliding_window, c.sliding_window + c.n_layers);
+  h->cfg.sliding_window = h->window.data();
+  h->fc_w = w->fc_w;
+  h->hidden_norm_g = w->hidden_norm_g;
+  h->final_norm_g = w->final_norm_g;
+  h->embed = w->embed;
+  h->lm_head = w->lm_head;
+  const int L = c.n_layers;
+  h->qkv_w.assign(w->qkv_w, w->qkv_w + L);
+  h->o_w.assign(w->o_w, w->o_w + L);
+  h->gate_up_w.assign(w->gate_up_w, w->gate_up_w + L);
+  h->down_w.assign(w->down_w, w->down_w + L);
+  h->in_norm_g.assign(w->in_norm_g, w->in_norm_g + L);
+  h->post_norm_g.assign(w->post_norm_g, w->post_norm_g + L);
+  h->q_norm_g.assign(w->q_norm_g, w->q_norm_g + L);
+  h->k_norm_g.assign(w->k_norm_g, w->k_norm_g + L);
+  h->store = c.dtype == DFLASH_F32 ? ST_F32 : ST_BF16;
+  h->es = c.dtype == DFLASH_F32 ? 4 : 2;
+  h->L = plan(h->cfg, h->es);
+  *out = h;
+  g_last_error.clear();
+  return DFLASH_OK;
+}
+
+void dflash_destroy(dflash_handle *h) { delete h; }
+
+int dflash_workspace_size(const dflash_handle *h, size_t *bytes) {
+  if (!h || !bytes) return fail(DFLASH_EINVAL, "handle and bytes must be non-NULL");
+  *bytes = h->L.total;
+  return DFLASH_OK;
+}
+
+int dflash_bind_workspace(dflash_handle *h, void *dev_ptr, size_t bytes, dflash_stream_t stream) {
+  if (!h || !dev_ptr) return fail(DFLASH_EINVAL, "handle and workspace must be non-NULL");
+  if ((uintptr_t)dev_ptr % 256) return fail(DFLASH_EINVAL, "workspace must be 256-byte aligned");
+  if (bytes < h->L.total)
+    return fail(DFLASH_ECAPACITY, "workspace too small: need " + std::to_string(h->L.total) + " bytes");
+  cudaStream_t s = (cudaStream_t)stream;
+  h->ws = (char *)dev_ptr;
+  h->ws_bytes = bytes;
+  int st = check_cuda(cudaMemsetAsync(h->ws + h->L.err, 0, 256, s), "clear error word");
+  if (st) return st;
+  st = check_cuda(launch_rope_table(at<float2>(h, h->L.rope), h->cfg.max_position, h->cfg.head_dim,
+                                    h->cfg.rope_theta, s), "rope table");
+  if (st) return st;
+  return check_cuda(prepare_kernels(), "kernel attributes");
+}
+
+int dflash_get_error(dflash_handle *h, dflash_stream_t stream, uint32_t *word) {
+  if (!h) return fail(DFLASH_EINVAL, "handle is NULL");
+  if (!h->ws) return fail(DFLASH_ESTATE, "no workspace bound");
+  cudaStream_t s = (cudaStream_t)stream;
+  uint32_t v = 0;
+  int st = check_cuda(cudaMemcpyAsync(&v, h->ws + h->L.err, sizeof(v), cudaMemcpyDeviceToHost, s), "read error word");
+  if (st) return st;
+  st = check_cuda(cudaMemsetAsync(h->ws + h->L.err, 0, sizeof(v), s), "clear error word");
+  if (st) return st;
+  st = check_cuda(cudaStreamSynchronize(s), "synchronize");
+  if (st) return st;
+  if (word) *word = v;
+  return v ? DFLASH_EDEVICE : DFLASH_OK;
+}
+
+int dflash_inject_context(dflash_handle *h, const dflash_kv *kv, int32_t batch, int32_t total_rows,
+                          const void *const *target_feats, const int32_t *row_offset,
+                          const int32_t *n_rows, dflash_stream_t stream) {
+  if (!h) return fail(DFLASH_EINVAL, "handle is NULL");
+  if (!h->ws) return fail(DFLASH_ESTATE, "no workspace bound");
+  const dflash_config &c = h->cfg;
+  if (int st = check_kv(h, kv)) return st;
+  if (batch < 0 || total_rows < 0) return fail(DFLASH_EINVAL, "negative batch or total_rows");
+  if (batch > c.max_batch) return fail(DFLASH_ECAPACITY, "batch > max_batch");
+  if (batch == 0) return DFLASH_OK;
+  if (!target_feats || !row_offset || !n_rows)
+    return fail(DFLASH_EINVAL, "target_feats, row_offset and n_rows must be non-NULL");
+  for (int j = 0; j < c.n_sel; ++j)
+    if (!target_feats[j]) return fail(DFLASH_EINVAL, "NULL feature pointer " + std::to_string(j));
+  cudaStream_t s = (cudaStream_t)stream;
+  unsigned int *err = at<unsigned int>(h, h->L.err);
+  const int H = c.hidden, D = c.head_dim;
+  const int kvd = c.n_kv_heads * D;
+  const int q_rows = c.n_heads * D;
+  int *slot = at<int>(h, h->L.slot), *rpos = at<int>(h, h->L.rpos);
+  float *y = at<float>(h, h->L.y);
+  void *yh = h->ws + h->L.yh;
+  const float2 *rope = at<const float2>(h, h->L.rope);
+
+  for (int64_t r0 = 0; r0 < total_rows; r0 += c.max_rows) {
+    const int rows = (int)std::min<int64_t>(c.max_rows, total_rows - r0);
+    int st = check_cuda(launch_inject_prep(batch, (int)r0, rows, row_offset, n_rows, kv->kv_len,
+                                           kv->page_table, kv->pages_per_req, kv->n_pages,
+                                           c.page_size, c.max_position, slot, rpos, err, s),
+                        "inject row map");
+    if (st) return st;
+    // a1: concat (K-split over the selected layers) + fc
+    GemmProblem P;
+    std::memset(&P, 0, sizeof(P));
+    for (int j = 0; j < c.n_sel; ++j)
+      P.A.ptr[j] = (const char *)target_feats[j] + (size_t)r0 * c.target_hidden * h->es;
+    P.A.ld = c.target_hidden;
+    P.A.k_per_src = c.target_hidden;
+    P.A.n_src = c.n_sel;
+    P.M = rows;
+    P.K = c.n_sel * c.target_hidden;
+    EpiParams e = epi_base(h, EPI_STORE_F32);
+    e.N = H;
+    e.ld = H;
+    e.out_f32 = y;
+    add_seg(P, h->fc_w, P.K, H, e);
+    if ((st = check_cuda(run_gemm(h, P, s), "fc GEMM"))) return st;
+    // a2: hidden_norm
+    if ((st = check_cuda(launch_rmsnorm(1, h->store, y, h->hidden_norm_g, rows, H, c.rms_eps, yh,
+                                        nullptr, s), "hidden_norm")))
+      return st;
+    // a3: every layer's K/V projection + k-norm + RoPE + paged scatter
+    for (int l0 = 0; l0 < c.n_layers; l0 += kMaxSeg) {
+      GemmProblem Q = problem_1src(yh, H, rows, H);
+      for (int l = l0; l < std::min(c.n_layers, l0 + kMaxSeg); ++l) {
+        EpiParams k = epi_base(h, EPI_KV_CACHE);
+        k.N = 2 * kvd;
+        k.k_cache = kv->k_pages[l];
+        k.v_cache = kv->v_pages[l];
+        k.k_gain = h->k_norm_g[l];
+        k.row_pos = rpos;
+        k.row_slot = slot;
+        k.rope = rope;
+        add_seg(Q, (const char *)h->qkv_w[l] + (size_t)q_rows * H * h->es, H, 2 * kvd, k);
+      }
+      if ((st = check_cuda(run_gemm(h, Q, s), "context K/V GEMM"))) return st;
+    }
+  }
+  return check_cuda(launch_inject_finalize(batch, total_rows, row_offset, n_rows, kv->kv_len,
+                                           kv->pages_per_req * c.page_size, err, s),
+                    "inject finalize");
+}
+
+int dflash_draft_block(dflash_handle *h, const dflash_kv *kv, int32_t batch, const int32_t *anchor,
+                       int32_t *draft_ids, void *hidden_out, dflash_stream_t stream) {
+  if (!h) return fail(DFLASH_EINVAL, "handle is NULL");
+  if (!h->ws) return fail(DFLASH_ESTATE, "no workspace bound");
+  const dflash_config &c = h->cfg;
+  if (int st = check_kv(h, kv)) return st;
+  if (batch < 0) return fail(DFLASH_EINVAL, "negative batch");
+  if (batch > c.max_batch) return fail(DFLASH_ECAPACITY, "batch > max_batch");
+  if (batch == 0) return DFLASH_OK;
+  if (!anchor || !draft_ids) return fail(DFLASH_EINVAL, "anchor and draft_ids must be non-NULL");
+  cudaStream_t s = (cudaStream_t)stream;
+  unsigned int *err = at<unsigned int>(h, h->L.err);
+  const int S = c.block_size, M = batch * S, H = c.hidden, D = c.head_dim;
+  const int qd = c.n_heads * D, kvd = c.n_kv_heads * D;
+  float *x = at<float>(h, h->L.x);
+  void *hb = h->ws + h->L.h;
+  void *qb = h->ws + h->L.qb, *kb = h->ws + h->L.kb, *vb = h->ws + h->L.vb;
+  void *attn = h->ws + h->L.attn, *act = h->ws + h->L.act;
+  int *row_pos = at<int>(h, h->L.row_pos);
+  unsigned long long *keys = at<unsigned long long>(h, h->L.keys);
+  const float2 *rope = at<const float2>(h, h->L.rope);
+  int st;
+
+  // a4: block embedding [anchor, MASK x (S-1)] at positions kv_len + j
+  if ((st = check_cuda(launch_embed(h->store, h->embed, anchor, kv->kv_len, batch, S, H, c.vocab,
+                                    c.mask_token_id, c.max_position, x, row_pos, keys, err, s),
+                       "embed")))
+    return st;
+  for (int l = 0; l < c.n_layers; ++l) {
+    // a5: RMSNorm + QKV GEMM + q/k-norm + RoPE
+    if ((st = check_cuda(launch_rmsnorm(1, h->store, x, h->in_norm_g[l], M, H, c.rms_eps, hb,
+                                        nullptr, s), "input norm")))
+      return st;
+    GemmProblem P = problem_1src(hb, H, M, H);
+    EpiParams e = epi_base(h, EPI_QKV);
+    e.N = qd + 2 * kvd;
+    e.q_out = qb;
+    e.k_out = kb;
+    e.v_out = vb;
+    e.q_gain = h->q_norm_g[l];
+    e.k_gain = h->k_norm_g[l];
+    e.row_pos = row_pos;
+    e.rope = rope;
+    add_seg(P, h->qkv_w[l], H, qd + 2 * kvd, e);
+    if ((st = check_cuda(run_gemm(h, P, s), "QKV GEMM"))) return st;
+    // a6: non-causal block attention over [context ; block]
+    AttnParams a;
+    std::memset(&a, 0, sizeof(a));
+    a.q = qb;
+    a.kb = kb;
+    a.vb = vb;
+    a.k_cache = kv->k_pages[l];
+    a.v_cache = kv->v_pages[l];
+    a.page_table = kv->page_table;
+    a.kv_len = kv->kv_len;
+    a.out = attn;
+    a.B = batch;
+    a.S = S;
+    a.n_heads = c.n_heads;
+    a.n_kv_heads = c.n_kv_heads;
+    a.head_dim = D;
+    a.page_size = c.page_size;
+    a.pages_per_req = kv->pages_per_req;
+    a.n_pages = kv->n_pages;
+    a.window = h->window[l];
+    a.scale = 1.0f / sqrtf((float)D);
+    a.err = err;
+    if ((st = check_cuda(launch_attention_simt(h->store, a, s), "attention"))) return st;
+    // a7: O projection + residual
+    GemmProblem O = problem_1src(attn, qd, M, qd);
+    EpiParams eo = epi_base(h, EPI_RESID);
+    eo.N = H;
+    eo.ld = H;
+    eo.out_f32 = x;
+    add_seg(O, h->o_w[l], qd, H, eo);
+    if ((st = check_cuda(run_gemm(h, O, s), "O GEMM"))) return st;
+    // a8: RMSNorm + gate/up GEMM with SwiGLU + down GEMM + residual
+    if ((st = check_cuda(launch_rmsnorm(1, h->store, x, h->post_norm_g[l], M, H, c.rms_eps, hb,
+                                        nullptr, s), "post-attention norm")))
+      return st;
+    GemmProblem G = problem_1src(hb, H, M, H);
+    EpiParams eg = epi_base(h, EPI_SWIGLU);
+    eg.N = 2 * c.intermediate;
+    eg.ld = c.intermediate;
+    eg.out_act = act;
+    add_seg(G, h->gate_up_w[l], H, 2 * c.intermediate, eg);
+    if ((st = check_cuda(run_gemm(h, G, s), "gate/up GEMM"))) return st;
+    GemmProblem Dn = problem_1src(act, c.intermediate, M, c.intermediate);
+    EpiParams ed = epi_base(h, EPI_RESID);
+    ed.N = H;
+    ed.ld = H;
+    ed.out_f32 = x;
+    add_seg(Dn, h->down_w[l], c.intermediate, H, ed);
+    if ((st = check_cuda(run_gemm(h, Dn, s), "down GEMM"))) return st;
+  }
+  // a9: final norm + lm_head + argmax (logits never stored)
+  if ((st = check_cuda(launch_rmsnorm(1, h->store, x, h->final_norm_g, M, H, c.rms_eps, hb,
+                                      hidden_out, s), "final norm")))
+    return st;
+  GemmProblem P = problem_1src(hb, H, M, H);
+  EpiParams e = epi_base(h, EPI_ARGMAX);
+  e.N = c.vocab;
+  e.argmax_keys = keys;
+  add_seg(P, h->lm_head, H, c.vocab, e);
+  if ((st = check_cuda(run_gemm(h, P, s), "lm_head GEMM"))) return st;
+  return check_cuda(launch_argmax_finalize(keys, anchor, batch, S, draft_ids, s), "argmax finalize");
+}
+
+int dflash_accept_commit(dflash_handle *h, int32_t batch, const int32_t *draft_ids,
+                         const int32_t *posterior, int32_t *seq_len, int32_t *accept_len,
+                         int32_t *commit_len, int32_t *bonus, int32_t *out_tokens,
+                         int32_t *output_ids, int32_t out_stride, dflash_stream_t stream) {
+  if (!h) return fail(DFLASH_EINVAL, "handle is NULL");
+  if (!h->ws) return fail(DFLASH_ESTATE, "no workspace bound");
+  if (batch < 0) return fail(DFLASH_EINVAL, "negative batch");
+  if (batch > h->cfg.max_batch) return fail(DFLASH_ECAPACITY, "batch > max_batch");
+  if (batch == 0) return DFLASH_OK;
+  if (!draft_ids || !posterior || !seq_len || !accept_len || !commit_len || !bonus || !out_tokens)
+    return fail(DFLASH_EINVAL, "a required pointer is NULL");
+  if (output_ids && out_stride <= 0) return fail(DFLASH_EINVAL, "out_stride must be positive");
+  return check_cuda(launch_accept(batch, h->cfg.block_size, h->cfg.vocab, draft_ids, posterior,
+                                  seq_len, accept_len, commit_len, bonus, out_tokens, output_ids,
+                                  out_stride, at<unsigned int>(h, h->L.err), (cudaStream_t)stream),
+                    "accept");
+}
+
+}  // extern "C"

@@ -1,0 +1,105 @@
+// Internal launch interface between the C-ABI runtime (dflash_api.cu) and the
+// kernels.  Host-side declarations only; no torch types anywhere.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dflash {
+
+enum StoreType { ST_F32 = 0, ST_BF16 = 1 };
+
+// What the GEMM epilogue does with the fp32 tile Y[m, n] = sum_k A[m,k] W[n,k].
+enum EpiOp {
+  EPI_STORE_F32 = 0,  // out_f32[m*ld + n] = y
+  EPI_RESID = 1,      // out_f32[m*ld + n] += y                (residual stream)
+  EPI_SWIGLU = 2,     // out_act[m*ld + n] = silu(y_gate) * y_up (paired tiles)
+  EPI_ARGMAX = 3,     // argmax_keys[m] = max(key(y, n))
+  EPI_QKV = 4,        // per-head RMSNorm (q, k) + RoPE -> q/k/v block buffers
+  EPI_KV_CACHE = 5,   // k-norm + RoPE (k), plain v -> paged cache rows (slot)
+  EPI_STORE_ACT = 6,  // out_act[m*ld + n] = y
+};
+
+struct EpiParams {
+  int op;
+  int N;                         // valid output features of this segment
+  int ld;                        // row stride of the output (elements)
+  float *out_f32;
+  void *out_act;
+  unsigned long long *argmax_keys;
+  // per-head epilogues
+  void *q_out, *k_out, *v_out;   // EPI_QKV: [M, n_heads*D], [M, kvh*D], [M, kvh*D]
+  void *k_cache, *v_cache;       // EPI_KV_CACHE: [n_pages*page, kvh, D]
+  const void *q_gain, *k_gain;   // [D]
+  const int *row_pos;            // [M] RoPE position of each row
+  const int *row_slot;           // [M] cache row of each row, -1 = skip
+  const float2 *rope;            // [max_position, D/2] (cos, sin)
+  int n_heads, n_kv_heads, head_dim;
+  float eps;
+};
+
+constexpr int kMaxSrc = 8;   // sources of the K-split A operand (selected layers)
+constexpr int kMaxSeg = 8;   // weight segments of a grouped launch
+
+struct GemmA {
+  const void *ptr[kMaxSrc];  // each [M, k_per_src], row stride ld
+  int64_t ld;
+  int k_per_src;
+  int n_src;
+};
+
+struct GemmSeg {
+  const void *W;   // [N, K] row-major (row stride ldw)
+  int64_t ldw;
+  int N;           // rows of W used by this segment (for EPI_SWIGLU: 2 * I)
+  EpiParams epi;
+};
+
+struct GemmProblem {
+  GemmA A;
+  int M, K;
+  int nseg;
+  GemmSeg seg[kMaxSeg];
+};
+
+struct AttnParams {
+  const void *q;       // [B*S, n_heads*D]
+  const void *kb, *vb; // [B*S, kvh*D] block keys / values
+  const void *k_cache, *v_cache;  // [n_pages*page, kvh, D]
+  const int *page_table;
+  const int *kv_len;
+  void *out;           // [B*S, n_heads*D]
+  int B, S, n_heads, n_kv_heads, head_dim, page_size, pages_per_req, n_pages;
+  int window;          // 0 = full
+  float scale;
+  unsigned int *err;
+};
+
+// ---- launchers (return cudaGetLastError()) ----
+cudaError_t launch_gemm_simt(int store, const GemmProblem &P, cudaStream_t s);
+cudaError_t launch_attention_simt(int store, const AttnParams &p, cudaStream_t s);
+
+cudaError_t launch_embed(int store, const void *embed, const int *anchor, const int *kv_len,
+                         int B, int S, int H, int vocab, int mask_id, int max_position,
+                         float *x, int *row_pos, unsigned long long *keys, unsigned int *err,
+                         cudaStream_t s);
+cudaError_t launch_rmsnorm(int in_f32, int store, const void *x, const void *gain, int M, int H,
+                           float eps, void *out, void *out2, cudaStream_t s);
+cudaError_t launch_argmax_finalize(const unsigned long long *keys, const int *anchor, int B, int S,
+                                   int *draft_ids, cudaStream_t s);
+cudaError_t launch_inject_prep(int B, int row0, int rows, const int *row_offset, const int *n_rows,
+                               const int *kv_len, const int *page_table, int pages_per_req,
+                               int n_pages, int page_size, int max_position, int *row_slot,
+                               int *row_pos, unsigned int *err, cudaStream_t s);
+cudaError_t launch_inject_finalize(int B, int total_rows, const int *row_offset,
+                                   const int *n_rows, int *kv_len, int capacity,
+                                   unsigned int *err, cudaStream_t s);
+// One-time kernel attribute setup (dynamic shared memory limits).
+cudaError_t prepare_kernels();
+cudaError_t launch_rope_table(float2 *table, int max_position, int head_dim, float theta,
+                              cudaStream_t s);
+cudaError_t launch_accept(int B, int S, int vocab, const int *draft, const int *post,
+                          int *seq_len, int *accept_len, int *commit_len, int *bonus,
+                          int *out_tokens, int *output_ids, int out_stride, unsigned int *err,
+                          cudaStream_t s);
+
+}  // namespace dflash

@@ -1,0 +1,239 @@
+// Row-wise kernels around the GEMMs: block embedding, RMSNorm, argmax
+// finalisation, injection row mapping and the RoPE table.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace dflash {
+
+// ---------------------------------------------------------------------------
+// Block embedding ("Inside SGLang", Step 3: input id = anchor at j = 0, else
+// mask_token_id; logical position = prefix length + j).  Writes the fp32
+// residual stream, the RoPE position of every block row and clears the
+// argmax keys of the lm_head pass.
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void embed_kernel(const T *__restrict__ embed, const int *__restrict__ anchor,
+                             const int *__restrict__ kv_len, int S, int H, int vocab, int mask_id,
+                             int max_position, float *__restrict__ x, int *__restrict__ row_pos,
+                             unsigned long long *__restrict__ keys, unsigned int *err) {
+  const int m = blockIdx.x;
+  const int b = m / S, j = m % S;
+  int id = j == 0 ? anchor[b] : mask_id;
+  const bool bad_id = id < 0 || id >= vocab;
+  const int pos = kv_len[b] + j;
+  const bool bad_pos = pos < 0 || pos >= max_position;
+  if (threadIdx.x == 0) {
+    if (bad_id) raise_error(err, DFLASH_DERR_TOKEN_RANGE);
+    if (bad_pos) raise_error(err, DFLASH_DERR_POSITION);
+    row_pos[m] = bad_pos ? 0 : pos;
+    keys[m] = 0ull;
+  }
+  const T *src = embed + (int64_t)(bad_id ? 0 : id) * H;
+  float *dst = x + (int64_t)m * H;
+  for (int c = threadIdx.x; c < H; c += blockDim.x) dst[c] = bad_id ? 0.f : to_f32(src[c]);
+}
+
+cudaError_t launch_embed(int store, const void *embed, const int *anchor, const int *kv_len, int B,
+                         int S, int H, int vocab, int mask_id, int max_position, float *x,
+                         int *row_pos, unsigned long long *keys, unsigned int *err,
+                         cudaStream_t s) {
+  const int M = B * S;
+  if (M <= 0) return cudaSuccess;
+  if (store == ST_F32)
+    embed_kernel<float><<<M, 256, 0, s>>>((const float *)embed, anchor, kv_len, S, H, vocab,
+                                          mask_id, max_position, x, row_pos, keys, err);
+  else
+    embed_kernel<bf16><<<M, 256, 0, s>>>((const bf16 *)embed, anchor, kv_len, S, H, vocab, mask_id,
+                                         max_position, x, row_pos, keys, err);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// RMSNorm y = x / sqrt(mean(x^2) + eps) * g, one CTA per row, fp32 math.
+// out2 (optional) receives a second copy (the hidden_out of the draft pass).
+// ---------------------------------------------------------------------------
+template <typename Tin, typename Tout>
+__global__ void rmsnorm_kernel(const Tin *__restrict__ x, const Tout *__restrict__ g, int H,
+                               float eps, Tout *__restrict__ out, Tout *__restrict__ out2) {
+  const int m = blockIdx.x;
+  const Tin *row = x + (int64_t)m * H;
+  float ss = 0.f;
+  for (int c = threadIdx.x; c < H; c += blockDim.x) {
+    const float v = to_f32(row[c]);
+    ss += v * v;
+  }
+  __shared__ float red[32];
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+    v = warp_sum(v);
+    if (threadIdx.x == 0) red[0] = v;
+  }
+  __syncthreads();
+  const float r = rsqrtf(red[0] / (float)H + eps);
+  Tout *o = out + (int64_t)m * H;
+  Tout *o2 = out2 ? out2 + (int64_t)m * H : nullptr;
+  for (int c = threadIdx.x; c < H; c += blockDim.x) {
+    const Tout y = from_f32<Tout>(to_f32(row[c]) * r * to_f32(g[c]));
+    o[c] = y;
+    if (o2) o2[c] = y;
+  }
+}
+
+cudaError_t launch_rmsnorm(int in_f32, int store, const void *x, const void *gain, int M, int H,
+                           float eps, void *out, void *out2, cudaStream_t s) {
+  if (M <= 0) return cudaSuccess;
+  const int thr = 256;
+  if (store == ST_F32) {
+    if (in_f32)
+      rmsnorm_kernel<float, float><<<M, thr, 0, s>>>((const float *)x, (const float *)gain, H, eps,
+                                                     (float *)out, (float *)out2);
+    else
+      return cudaErrorInvalidValue;
+  } else {
+    if (in_f32)
+      rmsnorm_kernel<float, bf16><<<M, thr, 0, s>>>((const float *)x, (const bf16 *)gain, H, eps,
+                                                    (bf16 *)out, (bf16 *)out2);
+    else
+      rmsnorm_kernel<bf16, bf16><<<M, thr, 0, s>>>((const bf16 *)x, (const bf16 *)gain, H, eps,
+                                                   (bf16 *)out, (bf16 *)out2);
+  }
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// draft_ids[b, 0] = anchor, draft_ids[b, j] = argmax of block row j (j >= 1).
+// ---------------------------------------------------------------------------
+__global__ void argmax_finalize_kernel(const unsigned long long *__restrict__ keys,
+                                       const int *__restrict__ anchor, int M, int S,
+                                       int *__restrict__ draft_ids) {
+  const int m = blockIdx.x * blockDim.x + threadIdx.x;
+  if (m >= M) return;
+  const int j = m % S;
+  draft_ids[m] = j == 0 ? anchor[m / S] : argmax_key_index(keys[m]);
+}
+
+cudaError_t launch_argmax_finalize(const unsigned long long *keys, const int *anchor, int B, int S,
+                                   int *draft_ids, cudaStream_t s) {
+  const int M = B * S;
+  if (M <= 0) return cudaSuccess;
+  argmax_finalize_kernel<<<(M + 127) / 128, 128, 0, s>>>(keys, anchor, M, S, draft_ids);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Injection row map ("Inside SGLang", Step 7: prefix-valid writes).  For the
+// feature rows row0 .. row0+rows-1 of this chunk: the owning request b is the
+// one with row_offset[b] <= r < row_offset[b] + n_rows[b]; its position is
+// kv_len[b] + (r - row_offset[b]) and its cache row is
+// page_table[b][pos / page] * page + pos % page.  Rows owned by no request,
+// or failing a capacity / page-range / position check, get slot -1.
+// ---------------------------------------------------------------------------
+__global__ void inject_prep_kernel(int B, int row0, int rows, const int *__restrict__ row_offset,
+                                   const int *__restrict__ n_rows, const int *__restrict__ kv_len,
+                                   const int *__restrict__ page_table, int pages_per_req,
+                                   int n_pages, int page_size, int max_position,
+                                   int *__restrict__ row_slot, int *__restrict__ row_pos,
+                                   unsigned int *err) {
+  extern __shared__ int sm[];
+  int *s_off = sm, *s_n = sm + B, *s_len = sm + 2 * B;
+  for (int b = threadIdx.x; b < B; b += blockDim.x) {
+    s_off[b] = row_offset[b];
+    s_n[b] = n_rows[b];
+    s_len[b] = kv_len[b];
+  }
+  __syncthreads();
+  const int local = blockIdx.x * blockDim.x + threadIdx.x;
+  if (local >= rows) return;
+  const int r = row0 + local;
+  int slot = -1, pos = 0;
+  for (int b = 0; b < B; ++b) {
+    const int i = r - s_off[b];
+    if (i < 0 || i >= s_n[b]) continue;
+    pos = s_len[b] + i;
+    const int64_t cap = (int64_t)pages_per_req * page_size;
+    if (pos >= cap || pos < 0) {
+      raise_error(err, DFLASH_DERR_KV_CAPACITY);
+    } else if (pos >= max_position) {
+      raise_error(err, DFLASH_DERR_POSITION);
+    } else {
+      const int page = page_table[(int64_t)b * pages_per_req + pos / page_size];
+      if (page < 0 || page >= n_pages)
+        raise_error(err, DFLASH_DERR_PAGE_RANGE);
+      else
+        slot = page * page_size + pos % page_size;
+    }
+    break;
+  }
+  row_slot[local] = slot;
+  row_pos[local] = slot < 0 ? 0 : pos;
+}
+
+cudaError_t launch_inject_prep(int B, int row0, int rows, const int *row_offset, const int *n_rows,
+                               const int *kv_len, const int *page_table, int pages_per_req,
+                               int n_pages, int page_size, int max_position, int *row_slot,
+                               int *row_pos, unsigned int *err, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  const int thr = 256;
+  inject_prep_kernel<<<(rows + thr - 1) / thr, thr, 3 * B * sizeof(int), s>>>(
+      B, row0, rows, row_offset, n_rows, kv_len, page_table, pages_per_req, n_pages, page_size,
+      max_position, row_slot, row_pos, err);
+  return cudaGetLastError();
+}
+
+// kv_len[b] += n_rows[b].  A request whose rows do not lie inside the feature
+// buffers, or whose new length passes the page table's capacity, is flagged
+// and its length is not advanced past what was actually written.
+__global__ void inject_finalize_kernel(int B, int total_rows, const int *__restrict__ row_offset,
+                                       const int *__restrict__ n_rows, int *kv_len, int capacity,
+                                       unsigned int *err) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= B) return;
+  const int n = n_rows[b], off = row_offset[b];
+  if (n <= 0) {
+    if (n < 0) raise_error(err, DFLASH_DERR_ROW_RANGE);
+    return;
+  }
+  if (off < 0 || (int64_t)off + n > total_rows) {
+    raise_error(err, DFLASH_DERR_ROW_RANGE);
+    return;
+  }
+  const int64_t v = (int64_t)kv_len[b] + n;
+  kv_len[b] = (int)(v > capacity ? capacity : v);
+}
+
+cudaError_t launch_inject_finalize(int B, int total_rows, const int *row_offset, const int *n_rows,
+                                   int *kv_len, int capacity, unsigned int *err, cudaStream_t s) {
+  if (B <= 0) return cudaSuccess;
+  inject_finalize_kernel<<<(B + 127) / 128, 128, 0, s>>>(B, total_rows, row_offset, n_rows, kv_len,
+                                                         capacity, err);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// RoPE table (cos, sin) of angle p * theta^(-2i/D), i < D/2, for every
+// position p < max_position.  Angles are formed and reduced in double
+// precision so that large positions keep full fp32 accuracy.
+// ---------------------------------------------------------------------------
+__global__ void rope_table_kernel(float2 *table, int max_position, int half, double theta) {
+  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (int64_t)max_position * half) return;
+  const int p = (int)(idx / half), i = (int)(idx % half);
+  const double freq = pow(theta, -2.0 * (double)i / (double)(2 * half));
+  double sn, cs;
+  sincos((double)p * freq, &sn, &cs);
+  table[idx] = make_float2((float)cs, (float)sn);
+}
+
+cudaError_t launch_rope_table(float2 *table, int max_position, int head_dim, float theta,
+                              cudaStream_t s) {
+  const int half = head_dim / 2;
+  const int64_t n = (int64_t)max_position * half;
+  rope_table_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(table, max_position, half,
+                                                                (double)theta);
+  return cudaGetLastError();
+}
+
+}  // namespace dflash

@@ -1,0 +1,117 @@
+"""Owner of one libdflash handle and its torch-allocated device buffers.
+
+PyTorch only provides device memory and the current CUDA stream here; every
+computation is a call into libdflash.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import (DFLASH_BF16, DFLASH_F32, DflashConfig, DflashKV, DflashWeights, _ptr_array,
+               dflash_accept_commit, dflash_bind_workspace, dflash_create, dflash_destroy,
+               dflash_draft_block, dflash_get_error, dflash_inject_context, dflash_workspace_size)
+
+
+def _stream():
+    return torch.cuda.current_stream().cuda_stream
+
+
+class KVCache:
+    """Paged draft KV cache: per layer K and V pages [n_pages, 64, KVH, D]."""
+
+    def __init__(self, cfg, batch, pages_per_req, page_table, dtype, device="cuda"):
+        self.batch = batch
+        self.pages_per_req = pages_per_req
+        self.page_table = torch.as_tensor(page_table, dtype=torch.int32).to(device).contiguous()
+        self.n_pages = int(self.page_table.max().item()) + 1 if self.page_table.numel() else 1
+        shape = (self.n_pages, cfg.page_size, cfg.n_kv_heads, cfg.head_dim)
+        self.k = [torch.zeros(shape, dtype=dtype, device=device) for _ in range(cfg.n_layers)]
+        self.v = [torch.zeros(shape, dtype=dtype, device=device) for _ in range(cfg.n_layers)]
+        self.kv_len = torch.zeros(batch, dtype=torch.int32, device=device)
+        self._kp = _ptr_array(self.k)
+        self._vp = _ptr_array(self.v)
+        self.struct = DflashKV(ctypes.cast(self._kp, ctypes.POINTER(ctypes.c_void_p)),
+                               ctypes.cast(self._vp, ctypes.POINTER(ctypes.c_void_p)),
+                               self.page_table.data_ptr(), pages_per_req, self.n_pages,
+                               self.kv_len.data_ptr())
+
+    def gather(self, layer, b, n=None):
+        """Host copy of the first n committed rows of request b: (K, V) [n, KVH, D]."""
+        n = int(self.kv_len[b].item()) if n is None else n
+        pos = torch.arange(n, device=self.page_table.device)
+        rows = self.page_table[b, pos // 64].long() * 64 + pos % 64
+        kf = self.k[layer].reshape(-1, *self.k[layer].shape[2:])[rows]
+        vf = self.v[layer].reshape(-1, *self.v[layer].shape[2:])[rows]
+        return kf.float().cpu(), vf.float().cpu()
+
+
+class DraftSession:
+    """One draft model bound to libdflash.
+
+    cfg: object with the DraftConfig attributes; W: dict of device tensors in
+    the layout of include/dflash.h (see synth.make_weights).
+    """
+
+    def __init__(self, cfg, W, max_batch, max_rows, max_position):
+        self.cfg = cfg
+        self.W = W
+        self.dtype = torch.float32 if cfg.dtype == "f32" else torch.bfloat16
+        self._win = (ctypes.c_int32 * cfg.n_layers)(*cfg.sliding_window)
+        self.c = DflashConfig(DFLASH_F32 if cfg.dtype == "f32" else DFLASH_BF16, cfg.target_hidden,
+                              cfg.n_sel, cfg.hidden, cfg.n_layers, cfg.n_heads, cfg.n_kv_heads,
+                              cfg.head_dim, cfg.intermediate, cfg.vocab, cfg.mask_token_id,
+                              cfg.block_size, cfg.page_size,
+                              ctypes.cast(self._win, ctypes.POINTER(ctypes.c_int32)),
+                              cfg.rms_eps, cfg.rope_theta, max_batch, max_rows, max_position)
+        Ls = W["layers"]
+        self._arrs = {k: _ptr_array([L[k] for L in Ls]) for k in
+                      ["qkv", "o", "gate_up", "down", "in_norm", "post_norm", "q_norm", "k_norm"]}
+        cast = lambda a: ctypes.cast(a, ctypes.POINTER(ctypes.c_void_p))  # noqa: E731
+        A = self._arrs
+        self.w = DflashWeights(W["fc"].data_ptr(), W["hidden_norm"].data_ptr(),
+                               W["final_norm"].data_ptr(), W["embed"].data_ptr(),
+                               W["lm_head"].data_ptr(), cast(A["qkv"]), cast(A["o"]),
+                               cast(A["gate_up"]), cast(A["down"]), cast(A["in_norm"]),
+                               cast(A["post_norm"]), cast(A["q_norm"]), cast(A["k_norm"]))
+        self.h = dflash_create(self.c, self.w)
+        self.ws_bytes = dflash_workspace_size(self.h)
+        self.ws = torch.empty(self.ws_bytes + 256, dtype=torch.uint8, device="cuda")
+        base = self.ws.data_ptr()
+        self.ws_ptr = (base + 255) // 256 * 256
+        dflash_bind_workspace(self.h, self.ws_ptr, self.ws_bytes, _stream())
+
+    def close(self):
+        if self.h is not None:
+            dflash_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def new_kv(self, batch, pages_per_req, page_table):
+        return KVCache(self.cfg, batch, pages_per_req, page_table, self.dtype)
+
+    def inject(self, kv, feats, row_offset, n_rows, batch=None):
+        """feats: [n_sel, rows, H_t] device tensor (or a list of n_sel [rows, H_t])."""
+        batch = kv.batch if batch is None else batch
+        fl = [feats[j] for j in range(self.cfg.n_sel)]
+        rows = fl[0].shape[0]
+        dflash_inject_context(self.h, kv.struct, batch, rows, fl, row_offset, n_rows, _stream())
+
+    def draft(self, kv, anchor, draft_ids, hidden_out=None, batch=None):
+        batch = kv.batch if batch is None else batch
+        dflash_draft_block(self.h, kv.struct, batch, anchor, draft_ids, hidden_out, _stream())
+
+    def accept(self, batch, draft_ids, posterior, seq_len, accept_len, commit_len, bonus,
+               out_tokens, output_ids=None):
+        stride = output_ids.shape[1] if output_ids is not None else 0
+        dflash_accept_commit(self.h, batch, draft_ids, posterior, seq_len, accept_len, commit_len,
+                             bonus, out_tokens, output_ids, stride, _stream())
+
+    def error(self):
+        return dflash_get_error(self.h, _stream())

@@ -1,0 +1,162 @@
+"""Lock-step runner of the CUDA path and the CPU oracle over draft-verify cycles.
+
+Both sides get the same seeded inputs (weights, target features, anchors,
+posteriors).  Posteriors are built from the oracle's draft ids, so the two
+sides stay in lock-step even when a near-tie argmax differs.  Comparisons:
+  * KV cache contents and hidden states: relative L2 within `tol`;
+  * draft ids: identical except where the oracle's top-2 margin < 1e-2;
+  * acceptance, commit, bonus, out_tokens, output_ids, seq_len, kv_len:
+    bit-exact.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import block_diffusion_speculative_fc_gb300 as pkg
+from oracle import dflash_oracle as O
+from synth import make_anchor, make_features, make_page_table, make_posterior, \
+    make_posterior_with_commit, make_commit_lengths, make_weights
+
+MARGIN = 1e-2
+
+
+def to_numpy_weights(W):
+    """Host copies for the oracle.  float32 holds every bf16 value exactly; the
+    oracle widens to float64 at each use."""
+    f = lambda t: t.float().cpu().numpy()  # noqa: E731
+    out = {k: f(v) for k, v in W.items() if k != "layers"}
+    out["layers"] = [{k: f(v) for k, v in L.items()} for L in W["layers"]]
+    return out
+
+
+def rel_l2(a, b):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    den = np.linalg.norm(b)
+    return float(np.linalg.norm(a - b) / (den if den > 0 else 1.0))
+
+
+def i32(a):
+    return torch.as_tensor(np.asarray(a), dtype=torch.int32, device="cuda")
+
+
+class CycleRun:
+    def __init__(self, cfg, batch, ctx_lens, cycles, seed=0, gains="unit", permuted=False,
+                 check=None, match=("bernoulli", 0.85), tol=None, max_rows=None,
+                 extra_pages=2, W=None, Wn=None):
+        self.cfg, self.B, self.cycles, self.seed = cfg, batch, cycles, seed
+        self.ctx_lens = np.asarray(ctx_lens, dtype=np.int64)
+        self.check = list(range(batch)) if check is None else list(check)
+        self.match = match
+        self.tol = tol if tol is not None else (1e-4 if cfg.dtype == "f32" else 2e-2)
+        S = cfg.block_size
+        self.W = W if W is not None else make_weights(cfg, seed=seed, device="cuda", gains=gains)
+        self.Wn = Wn if Wn is not None else to_numpy_weights(self.W)
+        max_ctx = int(self.ctx_lens.max()) + (cycles + 1) * S
+        self.ppr = (max_ctx + 63) // 64 + extra_pages
+        self.page_table = make_page_table(batch, self.ppr, permuted, seed)
+        rows_total = int(self.ctx_lens.sum())
+        self.sess = pkg.DraftSession(cfg, self.W, max_batch=batch,
+                                     max_rows=max_rows or max(rows_total, batch * S),
+                                     max_position=self.ppr * 64 + S)
+        self.kv = self.sess.new_kv(batch, self.ppr, self.page_table)
+        self.ctx = {b: O.DraftContext(cfg) for b in self.check}
+        self.stats = {"hidden_rel": [], "kv_rel": [], "id_mismatch_near_tie": 0, "ids": 0,
+                      "accept": []}
+
+    # ------------------------------------------------------------- helpers
+    def _feat_rows(self, feats, rows):
+        return [feats[j][rows].double().cpu().numpy() for j in range(self.cfg.n_sel)]
+
+    def prefill(self):
+        cfg = self.cfg
+        T = self.ctx_lens
+        offs = np.concatenate([[0], np.cumsum(T)[:-1]])
+        feats = make_features(cfg, int(T.sum()), self.seed, "prefill", device="cuda")
+        self.sess.inject(self.kv, feats, i32(offs), i32(T))
+        for b in self.check:
+            self.ctx[b].inject(self._feat_rows(feats, slice(int(offs[b]), int(offs[b] + T[b]))),
+                               self.Wn)
+        assert np.array_equal(self.kv.kv_len.cpu().numpy(), T)
+        self.compare_kv()
+
+    def compare_kv(self, layers=None):
+        for b in self.check:
+            for l in (range(self.cfg.n_layers) if layers is None else layers):
+                k, v = self.kv.gather(l, b)
+                rk = rel_l2(k.numpy(), self.ctx[b].k[l])
+                rv = rel_l2(v.numpy(), self.ctx[b].v[l])
+                self.stats["kv_rel"].append(max(rk, rv))
+                assert rk <= self.tol and rv <= self.tol, (b, l, rk, rv)
+
+    def run(self):
+        cfg, B, S = self.cfg, self.B, self.cfg.block_size
+        self.prefill()
+        anchor = make_anchor(B, cfg, self.seed)
+        seq = self.ctx_lens.copy()
+        seq_d = i32(seq)
+        out_stride = int(seq.max()) + (self.cycles + 2) * S
+        output_ids = torch.full((B, out_stride), cfg.mask_token_id, dtype=torch.int32, device="cuda")
+        out_ref = np.full((B, out_stride), cfg.mask_token_id, dtype=np.int64)
+        for b in range(B):
+            out_ref[b, seq[b]] = anchor[b]
+        output_ids[:, :] = torch.as_tensor(out_ref, dtype=torch.int32)
+        draft_d = torch.zeros((B, S), dtype=torch.int32, device="cuda")
+        hid_d = torch.zeros((B, S, cfg.hidden), dtype=self.sess.dtype, device="cuda")
+        for c in range(self.cycles):
+            self.sess.draft(self.kv, i32(anchor), draft_d, hid_d)
+            got = draft_d.cpu().numpy().astype(np.int64)
+            draft_used = got.copy()
+            for b in self.check:
+                ids, hid, margin = O.draft_block(cfg, self.Wn, int(anchor[b]), self.ctx[b].layers(),
+                                                 self.ctx[b].kv_len)
+                r = rel_l2(hid_d[b].double().cpu().numpy(), hid)
+                self.stats["hidden_rel"].append(r)
+                assert r <= self.tol, (c, b, r)
+                assert got[b, 0] == anchor[b]
+                for j in range(1, S):
+                    self.stats["ids"] += 1
+                    if got[b, j] != ids[j]:
+                        assert margin[j - 1] < MARGIN, (c, b, j, got[b, j], ids[j], margin[j - 1])
+                        self.stats["id_mismatch_near_tie"] += 1
+                draft_used[b] = ids
+            # synthetic target verify
+            if self.match[0] == "geometric":
+                commit = make_commit_lengths(B, S, self.match[1], self.seed, c)
+                post = make_posterior_with_commit(draft_used, commit, cfg.vocab, self.seed, c)
+            else:
+                p = self.match[1] if self.match[0] == "bernoulli" else \
+                    np.random.default_rng(self.seed).uniform(self.match[1], self.match[2], B)
+                post = make_posterior(draft_used, np.broadcast_to(p, (B,)), cfg.vocab, self.seed, c)
+            acc_d = torch.zeros(B, dtype=torch.int32, device="cuda")
+            com_d = torch.zeros_like(acc_d)
+            bon_d = torch.zeros_like(acc_d)
+            tok_d = torch.zeros((B, S), dtype=torch.int32, device="cuda")
+            self.sess.accept(B, i32(draft_used), i32(post), seq_d, acc_d, com_d, bon_d, tok_d,
+                             output_ids)
+            acc_g, com_g, bon_g = acc_d.cpu().numpy(), com_d.cpu().numpy(), bon_d.cpu().numpy()
+            tok_g = tok_d.cpu().numpy()
+            seq_g = seq_d.cpu().numpy()
+            ids_g = output_ids.cpu().numpy()
+            for b in self.check:      # oracle inputs are synthetic or the oracle's own ids
+                a, bonus, commit, out = O.accept_block(draft_used[b], post[b])
+                assert (acc_g[b], com_g[b], bon_g[b]) == (a, commit, bonus), (c, b)
+                assert np.array_equal(tok_g[b], out), (c, b)
+                out_ref[b], seq[b] = O.commit_output(out_ref[b], seq[b], draft_used[b], a, bonus)
+                self.stats["accept"].append(a)
+                assert seq_g[b] == seq[b] and np.array_equal(ids_g[b], out_ref[b]), (c, b)
+            # commit the verified feature rows of the block (prefix-valid)
+            feats = make_features(cfg, B * S, self.seed, ("verify", c), device="cuda")
+            self.sess.inject(self.kv, feats, i32(np.arange(B) * S), com_d)
+            for b in self.check:
+                self.ctx[b].inject(self._feat_rows(feats, slice(b * S, b * S + int(com_g[b]))),
+                                   self.Wn)
+            kvl = self.kv.kv_len.cpu().numpy()
+            assert all(kvl[b] == seq[b] for b in self.check)
+            assert np.array_equal(kvl, seq_g)          # kv_len == crop index after the commit
+            anchor = bon_g.astype(np.int64)
+        self.compare_kv()
+        err = self.sess.error()
+        assert err == 0, pkg.decode_error(err)
+        return self.stats

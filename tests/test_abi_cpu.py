@@ -1,0 +1,104 @@
+"""CPU-only checks of the C-ABI library: it loads, exports every declared
+symbol, and its host-side validation refuses bad arguments without touching
+a GPU (dflash_create and dflash_workspace_size make no CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import block_diffusion_speculative_fc_gb300 as pkg
+from block_diffusion_speculative_fc_gb300 import _build
+from synth import WORKLOADS
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return pkg.load_library()
+
+
+def declared_functions():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for f in os.listdir(inc):
+        if f.endswith(".h"):
+            src = open(os.path.join(inc, f)).read()
+            names |= set(re.findall(r"^[A-Za-z_][\w \*]*?\b(dflash_\w+)\s*\(", src, re.M))
+    return sorted(names)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert {"dflash_inject_context", "dflash_draft_block", "dflash_accept_commit"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(pkg.EXPORTED) <= set(names)
+
+
+def _session_structs(cfg, **over):
+    win = (ctypes.c_int32 * cfg.n_layers)(*cfg.sliding_window)
+    c = pkg.DflashConfig(pkg.DFLASH_F32 if cfg.dtype == "f32" else pkg.DFLASH_BF16,
+                         cfg.target_hidden, cfg.n_sel, cfg.hidden, cfg.n_layers, cfg.n_heads,
+                         cfg.n_kv_heads, cfg.head_dim, cfg.intermediate, cfg.vocab,
+                         cfg.mask_token_id, cfg.block_size, cfg.page_size,
+                         ctypes.cast(win, ctypes.POINTER(ctypes.c_int32)), cfg.rms_eps,
+                         cfg.rope_theta, 4, 256, 4096)
+    for k, v in over.items():
+        setattr(c, k, v)
+    fake = 0x10000  # never dereferenced by host-side code
+    arr = (ctypes.c_void_p * cfg.n_layers)(*([fake] * cfg.n_layers))
+    P = ctypes.cast(arr, ctypes.POINTER(ctypes.c_void_p))
+    w = pkg.DflashWeights(fake, fake, fake, fake, fake, P, P, P, P, P, P, P, P)
+    return c, w, (win, arr)
+
+
+def test_create_validates_config(lib):
+    cfg = WORKLOADS["tiny"].cfg
+    c, w, keep = _session_structs(cfg)
+    h = pkg.dflash_create(c, w)
+    n = pkg.dflash_workspace_size(h)
+    assert n > 0
+    pkg.dflash_destroy(h)
+    for field, bad in [("head_dim", 96), ("page_size", 32), ("block_size", 1), ("block_size", 40),
+                       ("n_kv_heads", 3), ("hidden", 200), ("mask_token_id", 5000),
+                       ("max_batch", 0), ("dtype", 7), ("n_sel", 9)]:
+        c2, w2, keep2 = _session_structs(cfg, **{field: bad})
+        with pytest.raises(pkg.DFlashError) as ei:
+            pkg.dflash_create(c2, w2)
+        assert ei.value.status in (-1, -2), (field, ei.value.status)
+
+
+def test_calls_before_workspace_are_refused(lib):
+    cfg = WORKLOADS["tiny"].cfg
+    c, w, keep = _session_structs(cfg)
+    h = pkg.dflash_create(c, w)
+    kvarr = (ctypes.c_void_p * cfg.n_layers)(*([0x10000] * cfg.n_layers))
+    P = ctypes.cast(kvarr, ctypes.POINTER(ctypes.c_void_p))
+    kv = pkg.DflashKV(P, P, 0x10000, 4, 16, 0x10000)
+    with pytest.raises(pkg.DFlashError) as ei:
+        pkg.dflash_draft_block(h, kv, 1, 0x10000, 0x10000, None, None)
+    assert ei.value.status == -6
+    with pytest.raises(pkg.DFlashError) as ei:
+        pkg.dflash_accept_commit(h, 1, 1, 1, 1, 1, 1, 1, 1, None, 0, None)
+    assert ei.value.status == -6
+    with pytest.raises(pkg.DFlashError):
+        pkg.dflash_bind_workspace(h, None, 1 << 20, None)
+    with pytest.raises(pkg.DFlashError) as ei:
+        pkg.dflash_bind_workspace(h, 0x10001, 1 << 40, None)   # misaligned
+    assert ei.value.status == -1
+    with pytest.raises(pkg.DFlashError) as ei:
+        pkg.dflash_bind_workspace(h, 0x10000, 16, None)        # too small
+    assert ei.value.status == -3
+    pkg.dflash_destroy(h)
+
+
+def test_null_arguments_are_refused(lib):
+    with pytest.raises(pkg.DFlashError):
+        pkg.dflash_create(pkg.DflashConfig(), pkg.DflashWeights())
+    assert lib.dflash_status_string(-3) == b"capacity exceeded"
+    assert lib.dflash_workspace_size(None, None) == -1
+    assert lib.dflash_inject_context(None, None, 0, 0, None, None, None, None) == -1
+    pkg.dflash_destroy(None)
