@@ -1,0 +1,485 @@
+#!/usr/bin/env python
+"""Throughput of the DFlash draft pass on one GB300: drafted tokens/s.
+
+One step = one draft-verify cycle of the whole hot path on one batch:
+  dflash_draft_block -> (synthetic target verify) -> dflash_accept_commit
+  -> dflash_inject_context(commit rows)
+metric = batch * (block_size - 1) / (device time of the three calls), the
+synthetic verify (a torch.where over pre-drawn randoms) being excluded.
+Before every cycle kv_len / seq_len are restored to the workload's context
+length, so every timed cycle drafts against exactly that context.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Under torchrun (N > 1) each rank runs an independent replica (requests are
+independent; no collective is on the path) and rank 0 prints the line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from synth import WORKLOADS, make_anchor, make_context_lengths, make_features, \
+    make_page_table, make_weights  # noqa: E402
+
+METRIC = "DFlash draft-pass drafted tokens/s on 1 GB300; % of BF16/HBM roofline"
+UNIT = "drafted tokens/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="qwen8b-b1")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-cycles", type=int, default=2)
+    ap.add_argument("--reference-budget-s", type=float, default=120.0)
+    return ap.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p["hbm_gbs"], p["bf16_tflops"], p["bf16_tflops_sustained"], "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ------------------------------------------------------------- roofline model
+def algorithmic(cfg, B, ctx_mean, commit_mean):
+    """Per-launch algorithmic bytes and flops of each kernel family."""
+    S, H, D = cfg.block_size, cfg.hidden, cfg.head_dim
+    M = B * S
+    es = 2 if cfg.dtype == "bf16" else 4
+    qkv = cfg.qkv_rows
+    qd, kvd, I, V = cfg.n_heads * D, cfg.n_kv_heads * D, cfg.intermediate, cfg.vocab
+    K_fc = cfg.n_sel * cfg.target_hidden
+    rows = B * S  # dense verify block; commit rows are written
+    keys = B * (ctx_mean + S)
+    fam = {
+        "gemm_qkv": (es * (qkv * H + M * H + M * qkv), 2 * M * qkv * H),
+        "gemm_o": (es * (H * qd + M * qd) + 8 * M * H, 2 * M * H * qd),
+        "gemm_gate_up": (es * (2 * I * H + M * H + M * I), 2 * M * 2 * I * H),
+        "gemm_down": (es * (H * I + M * I) + 8 * M * H, 2 * M * H * I),
+        "gemm_lm_head_argmax": (es * (V * H + M * H) + 8 * M, 2 * M * V * H),
+        "attention": (es * (2 * keys * kvd + 2 * M * qd), 4 * M * qd * (ctx_mean + S)),
+        "gemm_fc": (es * (H * K_fc + rows * K_fc) + 4 * rows * H, 2 * rows * H * K_fc),
+        "gemm_kv_inject": (es * (cfg.n_layers * 2 * kvd * H + rows * H
+                                 + B * commit_mean * cfg.n_layers * 2 * kvd),
+                           2 * rows * cfg.n_layers * 2 * kvd * H),
+        "accept": (4 * (2 * B * S + B * (S + 4)), 0),
+    }
+    return fam
+
+
+def source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "block_diffusion_speculative_fc_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel, workload):
+    """DRAM bytes per launch from a committed ncu summary, if it matches the source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            t = json.load(f)
+    except Exception:
+        return None
+    e = t.get(workload, {}).get(kernel)
+    if not e or e.get("source_hash") != source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------- clock sampling
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.p = None
+
+    def start(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.p = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.p.terminate()
+        self.p.wait()
+        self.f.flush()
+        self.f.seek(0)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.f.read().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.f.name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------- our arm
+class Bench:
+    def __init__(self, wl, seed=0):
+        import torch
+        import block_diffusion_speculative_fc_gb300 as pkg
+        self.torch, self.pkg = torch, pkg
+        self.wl, self.cfg = wl, wl.cfg
+        cfg = self.cfg
+        B, S = wl.batch, cfg.block_size
+        self.B, self.S = B, S
+        self.T = make_context_lengths(wl, seed)
+        self.W = make_weights(cfg, seed=seed, device="cuda")
+        self.ppr = (int(self.T.max()) + 2 * S + 63) // 64 + 1
+        self.page_table = make_page_table(B, self.ppr, wl.permuted_pages, seed)
+        self.sess = pkg.DraftSession(cfg, self.W, max_batch=B,
+                                     max_rows=max(B * S, min(int(self.T.sum()), 65536)),
+                                     max_position=self.ppr * 64 + S)
+        self.kv = self.sess.new_kv(B, self.ppr, self.page_table)
+        i32 = lambda a: torch.as_tensor(np.asarray(a), dtype=torch.int32, device="cuda")  # noqa
+        self.i32 = i32
+        offs = np.concatenate([[0], np.cumsum(self.T)[:-1]])
+        # prefill in slices so that feature buffers stay moderate
+        for b0 in range(0, B, 8):
+            bs = list(range(b0, min(B, b0 + 8)))
+            rows = int(self.T[bs].sum())
+            feats = make_features(cfg, rows, seed, ("prefill", b0), device="cuda")
+            ro = np.zeros(B, dtype=np.int64)
+            nr = np.zeros(B, dtype=np.int64)
+            acc = 0
+            for b in bs:
+                ro[b] = acc
+                nr[b] = self.T[b]
+                acc += self.T[b]
+            self.sess.inject(self.kv, feats, i32(ro), i32(nr))
+            del feats
+        torch.cuda.synchronize()
+        assert self.sess.error() == 0
+        self.base_len = i32(self.T)
+        self.anchor = i32(make_anchor(B, cfg, seed))
+        self.seq = i32(self.T)
+        self.draft = torch.zeros((B, S), dtype=torch.int32, device="cuda")
+        self.acc = torch.zeros(B, dtype=torch.int32, device="cuda")
+        self.com, self.bon = torch.zeros_like(self.acc), torch.zeros_like(self.acc)
+        self.tok = torch.zeros((B, S), dtype=torch.int32, device="cuda")
+        self.row_off = i32(np.arange(B) * S)
+        self.pool = [make_features(cfg, B * S, seed, ("verify", i), device="cuda") for i in range(4)]
+        g = torch.Generator(device="cuda")
+        g.manual_seed(seed + 17)
+        self.gen = g
+        if wl.match[0] == "bernoulli":
+            self.p = torch.full((B, 1), wl.match[1], device="cuda")
+        elif wl.match[0] == "bernoulli_per_req":
+            r = np.random.default_rng(seed).uniform(wl.match[1], wl.match[2], B)
+            self.p = torch.as_tensor(r, dtype=torch.float32, device="cuda")[:, None]
+        else:
+            self.p = None
+
+    def posterior_randoms(self, n):
+        torch, B, S, V = self.torch, self.B, self.S, self.cfg.vocab
+        u = torch.rand((n, B, S - 1), generator=self.gen, device="cuda")
+        r = torch.randint(0, V, (n, B, S), generator=self.gen, device="cuda", dtype=torch.int32)
+        if self.p is None:  # geometric commit lengths: accept = commit - 1
+            c = torch.distributions.Geometric(probs=torch.tensor(1.0 / self.wl.match[1]))
+            k = c.sample((n, B)).to("cuda").clamp(max=S - 1)       # failures before success
+            return u, r, k
+        return u, r, None
+
+    def make_post(self, u, r, k):
+        torch = self.torch
+        post = r.clone()
+        nxt = self.draft[:, 1:]
+        if k is None:
+            post[:, :-1] = torch.where(u < self.p, nxt, r[:, :-1])
+        else:
+            idx = torch.arange(self.S - 1, device="cuda")[None, :]
+            take = idx < k[:, None]
+            miss = (nxt + 1) % self.cfg.vocab
+            post[:, :-1] = torch.where(take, nxt, torch.where(idx == k[:, None], miss, r[:, :-1]))
+        return post
+
+    def cycle(self, c, u, r, k, ev=None):
+        torch = self.torch
+        self.kv.kv_len.copy_(self.base_len)
+        self.seq.copy_(self.base_len)
+        anchor = self.anchor if c == 0 else self.bon
+        if ev:
+            ev[0].record()
+        self.sess.draft(self.kv, anchor, self.draft)
+        if ev:
+            ev[1].record()
+        post = self.make_post(u, r, k)
+        if ev:
+            ev[2].record()
+        self.sess.accept(self.B, self.draft, post, self.seq, self.acc, self.com, self.bon, self.tok)
+        self.sess.inject(self.kv, self.pool[c % len(self.pool)], self.row_off, self.com)
+        if ev:
+            ev[3].record()
+
+    def run(self, warmup, steps):
+        torch = self.torch
+        u, r, k = self.posterior_randoms(warmup + steps)
+        for c in range(warmup):
+            self.cycle(c, u[c], r[c], None if k is None else k[c])
+        torch.cuda.synchronize()
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+        per_cycle_launches = 12 * self.cfg.n_layers + 16
+        self.pkg.dflash_profile_enable(self.sess.h, steps * per_cycle_launches + 64)
+        acc_sum = torch.zeros((), dtype=torch.int64, device="cuda")
+        for i in range(steps):
+            c = warmup + i
+            self.cycle(c, u[c], r[c], None if k is None else k[c], evs[i])
+            acc_sum += self.com.sum()
+        torch.cuda.synchronize()
+        prof = self.pkg.dflash_profile_collect(self.sess.h)
+        self.pkg.dflash_profile_disable(self.sess.h)
+        ms = [e[0].elapsed_time(e[1]) + e[2].elapsed_time(e[3]) for e in evs]
+        assert self.sess.error() == 0
+        mean_commit = float(acc_sum.item()) / (steps * self.B)
+        return sum(ms), ms, prof, mean_commit
+
+    def run_e2e(self, steps):
+        """Same cycles through the public API with host buffers: verify features
+        and verify randoms copied host->device each step, results device->host."""
+        torch, B, S, cfg = self.torch, self.B, self.S, self.cfg
+        u, r, k = self.posterior_randoms(steps)
+        u_h, r_h = u.cpu().pin_memory(), r.cpu().pin_memory()
+        k_h = k.cpu().pin_memory() if k is not None else None
+        feats_h = [p.cpu().pin_memory() for p in self.pool]
+        feat_d = torch.empty_like(self.pool[0])
+        u_d, r_d = torch.empty_like(u[0]), torch.empty_like(r[0])
+        k_d = torch.empty_like(k[0]) if k is not None else None
+        out_h = torch.empty((B, S + 3), dtype=torch.int32).pin_memory()
+        out_d = torch.empty((B, S + 3), dtype=torch.int32, device="cuda")
+        h2d = feats_h[0].numel() * feats_h[0].element_size() + u_h[0].numel() * 4 + r_h[0].numel() * 4
+        if k_h is not None:
+            h2d += k_h[0].numel() * k_h.element_size()
+        d2h = out_h.numel() * 4
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record()
+        for c in range(steps):
+            feat_d.copy_(feats_h[c % len(feats_h)], non_blocking=True)
+            u_d.copy_(u_h[c], non_blocking=True)
+            r_d.copy_(r_h[c], non_blocking=True)
+            if k_d is not None:
+                k_d.copy_(k_h[c], non_blocking=True)
+            self.kv.kv_len.copy_(self.base_len)
+            self.seq.copy_(self.base_len)
+            anchor = self.anchor if c == 0 else self.bon
+            self.sess.draft(self.kv, anchor, self.draft)
+            post = self.make_post(u_d, r_d, k_d)
+            self.sess.accept(B, self.draft, post, self.seq, self.acc, self.com, self.bon, self.tok)
+            self.sess.inject(self.kv, feat_d, self.row_off, self.com)
+            out_d[:, :S].copy_(self.tok)
+            out_d[:, S].copy_(self.acc)
+            out_d[:, S + 1].copy_(self.bon)
+            out_d[:, S + 2].copy_(self.seq)
+            out_h.copy_(out_d, non_blocking=True)
+        t1.record()
+        torch.cuda.synchronize()
+        ms = t0.elapsed_time(t1)
+        return ms, h2d, d2h
+
+
+def cpu_baseline(bench, cycles):
+    """The oracle, as it stands, timed on this host's cores for `cycles` cycles
+    of the same workload (request 0 only, scaled by batch)."""
+    import torch
+    from oracle import dflash_oracle as O
+    from synth import make_posterior
+    cfg, T = bench.cfg, int(bench.T[0])
+    f = lambda t: t.float().cpu().numpy()  # noqa: E731
+    W = {k: f(v) for k, v in bench.W.items() if k != "layers"}
+    W["layers"] = [{k: f(v) for k, v in L.items()} for L in bench.W["layers"]]
+    feats = make_features(cfg, T, 99, "cpu-prefill", device="cuda")
+    ctx = O.DraftContext(cfg)
+    ctx.inject([feats[j].double().cpu().numpy() for j in range(cfg.n_sel)], W)
+    vfe = make_features(cfg, cfg.block_size, 99, "cpu-verify", device="cuda")
+    vf = [vfe[j].double().cpu().numpy() for j in range(cfg.n_sel)]
+    anchor = 5
+    t0 = time.perf_counter()
+    for c in range(cycles):
+        ids, hid, margin = O.draft_block(cfg, W, anchor, ctx.layers(), ctx.kv_len)
+        post = make_posterior(ids[None], [0.85], cfg.vocab, 0, c)[0]
+        acc, bonus, commit, out = O.accept_block(ids, post)
+        ctx.inject([v[:commit] for v in vf], W)
+        anchor = bonus
+    dt = time.perf_counter() - t0
+    try:
+        import threadpoolctl
+        blas = max((p.get("num_threads", 0) for p in threadpoolctl.threadpool_info()), default=None)
+    except Exception:
+        blas = None
+    cores = len(os.sched_getaffinity(0))
+    value = cycles * (cfg.block_size - 1) / dt      # one request's drafted tokens per second
+    return {"value": value, "unit": UNIT, "cores": blas or cores, "kind": "oracle",
+            "sample": f"{cycles} full cycles (draft_block + accept + inject of the commit rows) "
+                      f"of request 0 at context {T}, float64 numpy, {cores} host cores"}, W
+
+
+def dominant_roofline(bench, prof, mean_commit, wl_name):
+    hbm, tf, tf_sus, src = peaks()
+    fam = algorithmic(bench.cfg, bench.B, float(np.mean(bench.T)), mean_commit)
+    total = sum(v[1] for v in prof.values())
+    name = max(prof, key=lambda n: prof[n][1])
+    launches, ms = prof[name]
+    avg_s = ms / launches / 1e3
+    bytes_, flops = fam.get(name, (0, 0))
+    ai = flops / bytes_ if bytes_ else 0
+    ridge = tf * 1e12 / (hbm * 1e9)
+    if ai > ridge:
+        out = {"bound": "tensor", "achieved": flops / avg_s / 1e12, "peak": tf_sus,
+               "unit": "TFLOP/s"}
+    else:
+        out = {"bound": "hbm", "achieved": bytes_ / avg_s / 1e9, "peak": hbm, "unit": "GB/s"}
+    out["frac"] = out["achieved"] / out["peak"]
+    out["traffic"] = traffic_for(name, wl_name)
+    out["kernel"] = name
+    out["share"] = ms / total if total else None
+    out["peak_source"] = src
+    return out
+
+
+def main():
+    a = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    wl = WORKLOADS[a.workload]
+    if a.impl == "reference":
+        return reference_arm(a, wl, rank, world)
+    import torch
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    bench = Bench(wl)
+    cs = ClockSampler(local)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    cs.start()
+    total_ms, ms, prof, mean_commit = bench.run(a.warmup, a.steps)
+    clocks = cs.stop()
+    t = torch.tensor([total_ms], device="cuda")
+    if dist:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms = float(t.item())
+    tokens = world * a.steps * bench.B * (bench.S - 1)
+    value = tokens / (total_ms / 1e3)
+    e2e = None
+    if not a.no_e2e:
+        e_ms, h2d, d2h = bench.run_e2e(a.steps)
+        te = torch.tensor([e_ms], device="cuda")
+        if dist:
+            dist.all_reduce(te, op=dist.ReduceOp.MAX)
+        e2e = {"value": tokens / (float(te.item()) / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    roof = dominant_roofline(bench, prof, mean_commit, a.workload)
+    cpu = None
+    if rank == 0 and world == 1 and not a.no_cpu_baseline:
+        cpu, _ = cpu_baseline(bench, a.cpu_cycles)
+    launches = sum(v[0] for v in prof.values())
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": a.steps,
+            "warmup": a.warmup, "ms_per_step": total_ms / a.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": bench.cfg.dtype, "data": "synthetic",
+            "config": {"workload": a.workload, "batch": bench.B, "block_size": bench.S,
+                       "context": int(bench.T[0]) if len(set(bench.T.tolist())) == 1 else
+                       f"{int(bench.T.min())}..{int(bench.T.max())}",
+                       "layers": bench.cfg.n_layers, "hidden": bench.cfg.hidden,
+                       "vocab": bench.cfg.vocab, "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2 (weights streamed every step)",
+                       "kv_len_reset_each_cycle": True,
+                       "mean_commit_len": mean_commit},
+            "clocks": clocks, "e2e": e2e, "gpu_launches": launches,
+            "roofline": roof, "cpu_baseline": cpu,
+            "kernels_ms_per_step": {k: v[1] / a.steps for k, v in sorted(prof.items())},
+        }
+        print(json.dumps(line))
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def reference_arm(a, wl, rank, world):
+    """The oracle as it stands on the host cores: same workload, metric, unit."""
+    if rank != 0:
+        return
+    import torch
+    torch.cuda.set_device(0)
+    bench_like = Bench(wl)
+    steps = max(1, a.steps)
+    per = []
+    from oracle import dflash_oracle as O  # noqa: F401
+    t_start = time.perf_counter()
+    cb, _ = cpu_baseline(bench_like, 1)       # warm-up / setup sample
+    done = 0
+    for _ in range(steps):
+        r, _ = cpu_baseline(bench_like, 1)
+        per.append(r["value"])
+        done += 1
+        if time.perf_counter() - t_start > a.reference_budget_s:
+            break
+    value = float(np.mean(per)) * wl.batch          # one request measured, scaled by batch
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": done,
+            "steps_requested": a.steps, "warmup": a.warmup, "higher_is_better": True,
+            "impl": "reference", "dtype": "f64", "data": "synthetic",
+            "config": {"workload": a.workload, "batch": wl.batch,
+                       "block_size": wl.cfg.block_size},
+            "cpu_baseline": {"kind": "oracle", "cores": cb["cores"], "sample": cb["sample"]
+                             + f"; request 0 timed, value scaled by batch {wl.batch}",
+                             "value": value},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

@@ -23,7 +23,8 @@ DERR_BITS = {0x1: "KV_CAPACITY", 0x2: "PAGE_RANGE", 0x4: "TOKEN_RANGE", 0x8: "PO
              0x10: "OUTPUT_ROW", 0x20: "TIMEOUT", 0x40: "ROW_RANGE"}
 EXPORTED = ["dflash_create", "dflash_destroy", "dflash_workspace_size", "dflash_bind_workspace",
             "dflash_inject_context", "dflash_draft_block", "dflash_accept_commit",
-            "dflash_get_error", "dflash_status_string", "dflash_last_error"]
+            "dflash_get_error", "dflash_status_string", "dflash_last_error",
+            "dflash_profile_enable", "dflash_profile_disable", "dflash_profile_collect"]
 
 
 class DflashConfig(ctypes.Structure):
@@ -46,6 +47,10 @@ class DflashWeights(ctypes.Structure):
 class DflashKV(ctypes.Structure):
     _fields_ = [("k_pages", P_VOID), ("v_pages", P_VOID), ("page_table", c_void_p),
                 ("pages_per_req", c_int32), ("n_pages", c_int32), ("kv_len", c_void_p)]
+
+
+class DflashProfileEntry(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 32), ("launches", c_int32), ("total_ms", c_float)]
 
 
 class DFlashError(RuntimeError):
@@ -78,13 +83,18 @@ def load_library(path=LIB_PATH):
     lib.dflash_accept_commit.argtypes = [c_void_p, c_int32, c_void_p, c_void_p, c_void_p, c_void_p,
                                          c_void_p, c_void_p, c_void_p, c_void_p, c_int32, c_void_p]
     lib.dflash_get_error.argtypes = [c_void_p, c_void_p, ctypes.POINTER(ctypes.c_uint32)]
+    lib.dflash_profile_enable.argtypes = [c_void_p, c_int32]
+    lib.dflash_profile_disable.argtypes = [c_void_p]
+    lib.dflash_profile_collect.argtypes = [c_void_p, ctypes.POINTER(DflashProfileEntry), c_int32,
+                                           ctypes.POINTER(c_int32)]
     lib.dflash_status_string.argtypes = [ctypes.c_int]
     lib.dflash_status_string.restype = ctypes.c_char_p
     lib.dflash_last_error.argtypes = []
     lib.dflash_last_error.restype = ctypes.c_char_p
     for name in ["dflash_create", "dflash_workspace_size", "dflash_bind_workspace",
                  "dflash_inject_context", "dflash_draft_block", "dflash_accept_commit",
-                 "dflash_get_error"]:
+                 "dflash_get_error", "dflash_profile_enable", "dflash_profile_disable",
+                 "dflash_profile_collect"]:
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -157,6 +167,22 @@ def dflash_get_error(h, stream):
     if st not in (0, -5):
         _check(st)
     return w.value
+
+
+def dflash_profile_enable(h, max_records):
+    _check(load_library().dflash_profile_enable(h, max_records))
+
+
+def dflash_profile_disable(h):
+    _check(load_library().dflash_profile_disable(h))
+
+
+def dflash_profile_collect(h, cap=64):
+    """{kernel name: (launches, total_ms)} of the launches recorded since enable."""
+    arr = (DflashProfileEntry * cap)()
+    n = c_int32()
+    _check(load_library().dflash_profile_collect(h, arr, cap, ctypes.byref(n)))
+    return {arr[i].name.decode(): (arr[i].launches, arr[i].total_ms) for i in range(n.value)}
 
 
 def decode_error(word):

@@ -38,6 +38,15 @@ struct dflash_handle {
   size_t ws_bytes = 0;
   int store;      // ST_F32 / ST_BF16
   size_t es;      // element size of the configured dtype
+  // optional per-launch event timing
+  struct ProfRec {
+    const char *name;
+    cudaEvent_t a, b;
+  };
+  bool prof_on = false;
+  size_t prof_cap = 0;
+  std::vector<cudaEvent_t> ev;
+  std::vector<ProfRec> recs;
 };
 
 namespace {
@@ -79,8 +88,25 @@ int check_cuda(cudaError_t e, const char *what) {
   return fail(DFLASH_ECUDA, std::string(what) + ": " + cudaGetErrorString(e));
 }
 
+// Runs one launch; when profiling is on, brackets it with a pair of events.
+template <class F> int timed(dflash_handle *h, const char *name, cudaStream_t s, F &&launch) {
+  int idx = -1;
+  if (h->prof_on && h->recs.size() < h->prof_cap) {
+    idx = (int)h->recs.size();
+    h->recs.push_back({name, h->ev[2 * idx], h->ev[2 * idx + 1]});
+    cudaEventRecord(h->ev[2 * idx], s);
+  }
+  const cudaError_t e = launch();
+  if (idx >= 0) cudaEventRecord(h->ev[2 * idx + 1], s);
+  return check_cuda(e, name);
+}
+
 cudaError_t run_gemm(dflash_handle *h, const GemmProblem &P, cudaStream_t s) {
   return launch_gemm_simt(h->store, P, s);
+}
+
+cudaError_t run_attention(dflash_handle *h, const AttnParams &a, cudaStream_t s) {
+  return launch_attention_simt(h->store, a, s);
 }
 
 EpiParams epi_base(const dflash_handle *h, int op) {
@@ -206,7 +232,55 @@ int dflash_create(const dflash_config *cfg, const dflash_weights *w, dflash_hand
   return DFLASH_OK;
 }
 
-void dflash_destroy(dflash_handle *h) { delete h; }
+void dflash_destroy(dflash_handle *h) {
+  if (!h) return;
+  for (cudaEvent_t e : h->ev) cudaEventDestroy(e);
+  delete h;
+}
+
+int dflash_profile_enable(dflash_handle *h, int32_t max_records) {
+  if (!h || max_records <= 0) return fail(DFLASH_EINVAL, "handle NULL or max_records <= 0");
+  while (h->ev.size() < 2 * (size_t)max_records) {
+    cudaEvent_t e;
+    if (int st = check_cuda(cudaEventCreate(&e), "cudaEventCreate")) return st;
+    h->ev.push_back(e);
+  }
+  h->prof_cap = (size_t)max_records;
+  h->recs.clear();
+  h->prof_on = true;
+  return DFLASH_OK;
+}
+
+int dflash_profile_disable(dflash_handle *h) {
+  if (!h) return fail(DFLASH_EINVAL, "handle is NULL");
+  h->prof_on = false;
+  return DFLASH_OK;
+}
+
+int dflash_profile_collect(dflash_handle *h, dflash_profile_entry *out, int32_t cap, int32_t *n) {
+  if (!h || !out || !n || cap < 0) return fail(DFLASH_EINVAL, "NULL argument");
+  std::vector<dflash_profile_entry> agg;
+  for (const auto &r : h->recs) {
+    if (int st = check_cuda(cudaEventSynchronize(r.b), "cudaEventSynchronize")) return st;
+    float ms = 0.f;
+    if (int st = check_cuda(cudaEventElapsedTime(&ms, r.a, r.b), "cudaEventElapsedTime")) return st;
+    auto it = std::find_if(agg.begin(), agg.end(),
+                           [&](const dflash_profile_entry &e) { return !std::strcmp(e.name, r.name); });
+    if (it == agg.end()) {
+      dflash_profile_entry e;
+      std::memset(&e, 0, sizeof(e));
+      std::strncpy(e.name, r.name, sizeof(e.name) - 1);
+      agg.push_back(e);
+      it = agg.end() - 1;
+    }
+    it->launches += 1;
+    it->total_ms += ms;
+  }
+  h->recs.clear();
+  *n = (int32_t)std::min<size_t>(agg.size(), (size_t)cap);
+  for (int i = 0; i < *n; ++i) out[i] = agg[i];
+  return DFLASH_OK;
+}
 
 int dflash_workspace_size(const dflash_handle *h, size_t *bytes) {
   if (!h || !bytes) return fail(DFLASH_EINVAL, "handle and bytes must be non-NULL");
@@ -271,10 +345,11 @@ int dflash_inject_context(dflash_handle *h, const dflash_kv *kv, int32_t batch, 
 
   for (int64_t r0 = 0; r0 < total_rows; r0 += c.max_rows) {
     const int rows = (int)std::min<int64_t>(c.max_rows, total_rows - r0);
-    int st = check_cuda(launch_inject_prep(batch, (int)r0, rows, row_offset, n_rows, kv->kv_len,
-                                           kv->page_table, kv->pages_per_req, kv->n_pages,
-                                           c.page_size, c.max_position, slot, rpos, err, s),
-                        "inject row map");
+    int st = timed(h, "inject_prep", s, [&] {
+      return launch_inject_prep(batch, (int)r0, rows, row_offset, n_rows, kv->kv_len,
+                                kv->page_table, kv->pages_per_req, kv->n_pages, c.page_size,
+                                c.max_position, slot, rpos, err, s);
+    });
     if (st) return st;
     // a1: concat (K-split over the selected layers) + fc
     GemmProblem P;
@@ -291,10 +366,11 @@ int dflash_inject_context(dflash_handle *h, const dflash_kv *kv, int32_t batch, 
     e.ld = H;
     e.out_f32 = y;
     add_seg(P, h->fc_w, P.K, H, e);
-    if ((st = check_cuda(run_gemm(h, P, s), "fc GEMM"))) return st;
+    if ((st = timed(h, "gemm_fc", s, [&] { return run_gemm(h, P, s); }))) return st;
     // a2: hidden_norm
-    if ((st = check_cuda(launch_rmsnorm(1, h->store, y, h->hidden_norm_g, rows, H, c.rms_eps, yh,
-                                        nullptr, s), "hidden_norm")))
+    if ((st = timed(h, "rmsnorm_hidden", s, [&] {
+           return launch_rmsnorm(1, h->store, y, h->hidden_norm_g, rows, H, c.rms_eps, yh, nullptr, s);
+         })))
       return st;
     // a3: every layer's K/V projection + k-norm + RoPE + paged scatter
     for (int l0 = 0; l0 < c.n_layers; l0 += kMaxSeg) {
@@ -310,12 +386,13 @@ int dflash_inject_context(dflash_handle *h, const dflash_kv *kv, int32_t batch, 
         k.rope = rope;
         add_seg(Q, (const char *)h->qkv_w[l] + (size_t)q_rows * H * h->es, H, 2 * kvd, k);
       }
-      if ((st = check_cuda(run_gemm(h, Q, s), "context K/V GEMM"))) return st;
+      if ((st = timed(h, "gemm_kv_inject", s, [&] { return run_gemm(h, Q, s); }))) return st;
     }
   }
-  return check_cuda(launch_inject_finalize(batch, total_rows, row_offset, n_rows, kv->kv_len,
-                                           kv->pages_per_req * c.page_size, err, s),
-                    "inject finalize");
+  return timed(h, "inject_finalize", s, [&] {
+    return launch_inject_finalize(batch, total_rows, row_offset, n_rows, kv->kv_len,
+                                  kv->pages_per_req * c.page_size, err, s);
+  });
 }
 
 int dflash_draft_block(dflash_handle *h, const dflash_kv *kv, int32_t batch, const int32_t *anchor,
@@ -342,14 +419,16 @@ int dflash_draft_block(dflash_handle *h, const dflash_kv *kv, int32_t batch, con
   int st;
 
   // a4: block embedding [anchor, MASK x (S-1)] at positions kv_len + j
-  if ((st = check_cuda(launch_embed(h->store, h->embed, anchor, kv->kv_len, batch, S, H, c.vocab,
-                                    c.mask_token_id, c.max_position, x, row_pos, keys, err, s),
-                       "embed")))
+  if ((st = timed(h, "embed", s, [&] {
+         return launch_embed(h->store, h->embed, anchor, kv->kv_len, batch, S, H, c.vocab,
+                             c.mask_token_id, c.max_position, x, row_pos, keys, err, s);
+       })))
     return st;
   for (int l = 0; l < c.n_layers; ++l) {
     // a5: RMSNorm + QKV GEMM + q/k-norm + RoPE
-    if ((st = check_cuda(launch_rmsnorm(1, h->store, x, h->in_norm_g[l], M, H, c.rms_eps, hb,
-                                        nullptr, s), "input norm")))
+    if ((st = timed(h, "rmsnorm", s, [&] {
+           return launch_rmsnorm(1, h->store, x, h->in_norm_g[l], M, H, c.rms_eps, hb, nullptr, s);
+         })))
       return st;
     GemmProblem P = problem_1src(hb, H, M, H);
     EpiParams e = epi_base(h, EPI_QKV);
@@ -362,7 +441,7 @@ int dflash_draft_block(dflash_handle *h, const dflash_kv *kv, int32_t batch, con
     e.row_pos = row_pos;
     e.rope = rope;
     add_seg(P, h->qkv_w[l], H, qd + 2 * kvd, e);
-    if ((st = check_cuda(run_gemm(h, P, s), "QKV GEMM"))) return st;
+    if ((st = timed(h, "gemm_qkv", s, [&] { return run_gemm(h, P, s); }))) return st;
     // a6: non-causal block attention over [context ; block]
     AttnParams a;
     std::memset(&a, 0, sizeof(a));
@@ -385,7 +464,7 @@ int dflash_draft_block(dflash_handle *h, const dflash_kv *kv, int32_t batch, con
     a.window = h->window[l];
     a.scale = 1.0f / sqrtf((float)D);
     a.err = err;
-    if ((st = check_cuda(launch_attention_simt(h->store, a, s), "attention"))) return st;
+    if ((st = timed(h, "attention", s, [&] { return run_attention(h, a, s); }))) return st;
     // a7: O projection + residual
     GemmProblem O = problem_1src(attn, qd, M, qd);
     EpiParams eo = epi_base(h, EPI_RESID);
@@ -393,10 +472,11 @@ int dflash_draft_block(dflash_handle *h, const dflash_kv *kv, int32_t batch, con
     eo.ld = H;
     eo.out_f32 = x;
     add_seg(O, h->o_w[l], qd, H, eo);
-    if ((st = check_cuda(run_gemm(h, O, s), "O GEMM"))) return st;
+    if ((st = timed(h, "gemm_o", s, [&] { return run_gemm(h, O, s); }))) return st;
     // a8: RMSNorm + gate/up GEMM with SwiGLU + down GEMM + residual
-    if ((st = check_cuda(launch_rmsnorm(1, h->store, x, h->post_norm_g[l], M, H, c.rms_eps, hb,
-                                        nullptr, s), "post-attention norm")))
+    if ((st = timed(h, "rmsnorm", s, [&] {
+           return launch_rmsnorm(1, h->store, x, h->post_norm_g[l], M, H, c.rms_eps, hb, nullptr, s);
+         })))
       return st;
     GemmProblem G = problem_1src(hb, H, M, H);
     EpiParams eg = epi_base(h, EPI_SWIGLU);
@@ -404,26 +484,28 @@ int dflash_draft_block(dflash_handle *h, const dflash_kv *kv, int32_t batch, con
     eg.ld = c.intermediate;
     eg.out_act = act;
     add_seg(G, h->gate_up_w[l], H, 2 * c.intermediate, eg);
-    if ((st = check_cuda(run_gemm(h, G, s), "gate/up GEMM"))) return st;
+    if ((st = timed(h, "gemm_gate_up", s, [&] { return run_gemm(h, G, s); }))) return st;
     GemmProblem Dn = problem_1src(act, c.intermediate, M, c.intermediate);
     EpiParams ed = epi_base(h, EPI_RESID);
     ed.N = H;
     ed.ld = H;
     ed.out_f32 = x;
     add_seg(Dn, h->down_w[l], c.intermediate, H, ed);
-    if ((st = check_cuda(run_gemm(h, Dn, s), "down GEMM"))) return st;
+    if ((st = timed(h, "gemm_down", s, [&] { return run_gemm(h, Dn, s); }))) return st;
   }
   // a9: final norm + lm_head + argmax (logits never stored)
-  if ((st = check_cuda(launch_rmsnorm(1, h->store, x, h->final_norm_g, M, H, c.rms_eps, hb,
-                                      hidden_out, s), "final norm")))
+  if ((st = timed(h, "rmsnorm", s, [&] {
+         return launch_rmsnorm(1, h->store, x, h->final_norm_g, M, H, c.rms_eps, hb, hidden_out, s);
+       })))
     return st;
   GemmProblem P = problem_1src(hb, H, M, H);
   EpiParams e = epi_base(h, EPI_ARGMAX);
   e.N = c.vocab;
   e.argmax_keys = keys;
   add_seg(P, h->lm_head, H, c.vocab, e);
-  if ((st = check_cuda(run_gemm(h, P, s), "lm_head GEMM"))) return st;
-  return check_cuda(launch_argmax_finalize(keys, anchor, batch, S, draft_ids, s), "argmax finalize");
+  if ((st = timed(h, "gemm_lm_head_argmax", s, [&] { return run_gemm(h, P, s); }))) return st;
+  return timed(h, "argmax_finalize", s,
+               [&] { return launch_argmax_finalize(keys, anchor, batch, S, draft_ids, s); });
 }
 
 int dflash_accept_commit(dflash_handle *h, int32_t batch, const int32_t *draft_ids,
@@ -438,10 +520,12 @@ int dflash_accept_commit(dflash_handle *h, int32_t batch, const int32_t *draft_i
   if (!draft_ids || !posterior || !seq_len || !accept_len || !commit_len || !bonus || !out_tokens)
     return fail(DFLASH_EINVAL, "a required pointer is NULL");
   if (output_ids && out_stride <= 0) return fail(DFLASH_EINVAL, "out_stride must be positive");
-  return check_cuda(launch_accept(batch, h->cfg.block_size, h->cfg.vocab, draft_ids, posterior,
-                                  seq_len, accept_len, commit_len, bonus, out_tokens, output_ids,
-                                  out_stride, at<unsigned int>(h, h->L.err), (cudaStream_t)stream),
-                    "accept");
+  cudaStream_t s = (cudaStream_t)stream;
+  return timed(h, "accept", s, [&] {
+    return launch_accept(batch, h->cfg.block_size, h->cfg.vocab, draft_ids, posterior, seq_len,
+                         accept_len, commit_len, bonus, out_tokens, output_ids, out_stride,
+                         at<unsigned int>(h, h->L.err), s);
+  });
 }
 
 }  // extern "C"

@@ -245,6 +245,25 @@ int dflash_accept_commit(dflash_handle *h, int32_t batch, const int32_t *draft_i
  * not. */
 int dflash_get_error(dflash_handle *h, dflash_stream_t stream, uint32_t *word);
 
+/*
+ * Optional per-kernel timing (off by default).  While enabled, every launch
+ * of the three entry points is bracketed by a pair of CUDA events recorded on
+ * the launching stream (at most max_records launches; later ones are not
+ * recorded).  dflash_profile_collect waits for the recorded events, sums the
+ * durations per kernel name into out[0..*n) and forgets the records.
+ * Creating the events is a host-side runtime call; no device memory is
+ * allocated.
+ */
+typedef struct {
+  char name[32];
+  int32_t launches;
+  float total_ms;
+} dflash_profile_entry;
+
+int dflash_profile_enable(dflash_handle *h, int32_t max_records);
+int dflash_profile_disable(dflash_handle *h);
+int dflash_profile_collect(dflash_handle *h, dflash_profile_entry *out, int32_t cap, int32_t *n);
+
 /* Static description of a status code. */
 const char *dflash_status_string(int status);
 

@@ -106,5 +106,11 @@ def get_workload(name):
 
 
 def shrink(cfg: DraftConfig, **over) -> DraftConfig:
-    """A smaller variant of a config (same structure, fewer features)."""
-    return DraftConfig(**{**cfg.__dict__, **over})
+    """A smaller variant of a config (same structure, fewer features).  With
+    fewer layers and no explicit windows, the per-layer windows are cut to
+    the new layer count."""
+    d = {**cfg.__dict__, **over}
+    if "sliding_window" not in over and len(d["sliding_window"]) != d["n_layers"]:
+        w = tuple(d["sliding_window"])
+        d["sliding_window"] = (w + (0,) * d["n_layers"])[:d["n_layers"]]
+    return DraftConfig(**d)
