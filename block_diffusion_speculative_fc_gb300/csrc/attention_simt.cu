@@ -147,6 +147,9 @@ cudaError_t prepare_attention_simt() {
                               smem);
 }
 
-cudaError_t prepare_kernels() { return prepare_attention_simt(); }
+cudaError_t prepare_kernels() {
+  const cudaError_t e = prepare_attention_simt();
+  return e != cudaSuccess ? e : prepare_gemm_tc();
+}
 
 }  // namespace dflash

@@ -22,7 +22,10 @@ int fail(int st, const std::string &msg) {
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct Layout {
-  size_t err, rope, x, h, qb, kb, vb, attn, act, row_pos, keys, y, yh, slot, rpos, total;
+  size_t err, rope, x, h, qb, kb, vb, attn, act, row_pos, keys, y, yh, slot, rpos;
+  size_t tc_partials, tc_counters;
+  int tc_max_tiles;
+  size_t total;
 };
 
 }  // namespace
@@ -77,6 +80,21 @@ Layout plan(const dflash_config &c, size_t es) {
   L.yh = take(es * R * H);
   L.slot = take(4 * R);
   L.rpos = take(4 * R);
+  if (es == 2) {
+    // tensor-core GEMM scratch: stream-K partial tiles and per-tile tickets
+    const int Mb = (int)M, Mr = c.max_rows;
+    auto t128 = [](long long n) { return (int)((n + 127) / 128); };
+    int mt = 0;
+    mt = std::max(mt, gemm_tc_tiles(t128((long long)c.n_heads * D + 2LL * c.n_kv_heads * D), Mb, false));
+    mt = std::max(mt, gemm_tc_tiles(t128(H), Mb, false));
+    mt = std::max(mt, gemm_tc_tiles(t128(c.intermediate), Mb, true));
+    mt = std::max(mt, gemm_tc_tiles(t128(c.vocab), Mb, false));
+    mt = std::max(mt, gemm_tc_tiles(t128(H), Mr, false));
+    mt = std::max(mt, gemm_tc_tiles(std::min(c.n_layers, kMaxSeg) * t128(2LL * c.n_kv_heads * D), Mr, false));
+    L.tc_max_tiles = mt;
+    L.tc_partials = take(gemm_tc_partials_bytes());
+    L.tc_counters = take(4 * (size_t)mt);
+  }
   L.total = o;
   return L;
 }
@@ -102,7 +120,9 @@ template <class F> int timed(dflash_handle *h, const char *name, cudaStream_t s,
 }
 
 cudaError_t run_gemm(dflash_handle *h, const GemmProblem &P, cudaStream_t s) {
-  return launch_gemm_simt(h->store, P, s);
+  if (h->store == ST_F32) return launch_gemm_simt(ST_F32, P, s);
+  return launch_gemm_tc(P, at<float>(h, h->L.tc_partials), at<int>(h, h->L.tc_counters),
+                        h->L.tc_max_tiles, at<unsigned int>(h, h->L.err), s);
 }
 
 cudaError_t run_attention(dflash_handle *h, const AttnParams &a, cudaStream_t s) {
@@ -298,6 +318,10 @@ int dflash_bind_workspace(dflash_handle *h, void *dev_ptr, size_t bytes, dflash_
   h->ws_bytes = bytes;
   int st = check_cuda(cudaMemsetAsync(h->ws + h->L.err, 0, 256, s), "clear error word");
   if (st) return st;
+  if (h->L.tc_max_tiles > 0 &&
+      (st = check_cuda(cudaMemsetAsync(h->ws + h->L.tc_counters, 0, 4 * (size_t)h->L.tc_max_tiles, s),
+                       "clear GEMM tickets")))
+    return st;
   st = check_cuda(launch_rope_table(at<float2>(h, h->L.rope), h->cfg.max_position, h->cfg.head_dim,
                                     h->cfg.rope_theta, s), "rope table");
   if (st) return st;

@@ -28,6 +28,9 @@
 // DFLASH_DERR_TIMEOUT and the CTA winds down instead of hanging.
 #include <cuda.h>
 
+#include <algorithm>
+#include <cstring>
+
 #include "common.cuh"
 #include "epilogue.cuh"
 #include "kernels.h"
@@ -156,6 +159,19 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Named-barrier AND-reduction over the 128 epilogue threads (uniform result).
+__device__ __forceinline__ bool epi_all(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v)
+      : "memory");
+  return r != 0;
+}
 
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
 // 128 bytes, 8-row core groups 1024 bytes apart.
@@ -215,7 +231,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
   uint64_t *bars = (uint64_t *)(smem + C::STAGES * C::STAGE_BYTES + C::STAGING_BYTES);
   uint64_t *full = bars, *empty = bars + C::STAGES;
   uint64_t *acc_full = bars + 2 * C::STAGES, *acc_empty = acc_full + 2;
-  uint32_t *tmem_slot = (uint32_t *)(acc_empty + 2);
+  uint64_t *mma_done = acc_empty + 2;
+  uint32_t *tmem_slot = (uint32_t *)(mma_done + 1);
   int *flag = (int *)(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -231,6 +248,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
       mbar_init(&acc_full[i], 1);
       mbar_init(&acc_empty[i], 4);
     }
+    mbar_init(mma_done, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
@@ -261,7 +279,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
       for (long long i = R.b; i < R.e && ok;) {
         const int tile = (int)(i / p.KB);
         const int kb0 = (int)(i % p.KB);
-        const int kb1 = (int)min<long long>(p.KB, kb0 + (R.e - i));
+        const int kb1 = (int)(kb0 + (R.e - i) < p.KB ? kb0 + (R.e - i) : p.KB);
         int seg, n0, m0;
         locate(tile, seg, n0, m0);
         for (int kb = kb0; kb < kb1; ++kb, ++it) {
@@ -282,10 +300,10 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
         i += kb1 - kb0;
       }
       if (!ok) raise_error(p.err, DFLASH_DERR_TIMEOUT);
-      // drain: wait until the MMA warp has consumed every issued stage
+      // drain: no TMA write may still be in flight when the CTA winds down
       for (int j = 0; j < C::STAGES && j < it; ++j) {
         const int q = it - 1 - j;
-        mbar_wait(&empty[q % C::STAGES], (q / C::STAGES) & 1);
+        mbar_wait(&full[q % C::STAGES], (q / C::STAGES) & 1);
       }
     }
   } else if (warp == 1) {
@@ -296,7 +314,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
       bool ok = true;
       for (long long i = R.b; i < R.e && ok; ++seg_i) {
         const int kb0 = (int)(i % p.KB);
-        const int kb1 = (int)min<long long>(p.KB, kb0 + (R.e - i));
+        const int kb1 = (int)(kb0 + (R.e - i) < p.KB ? kb0 + (R.e - i) : p.KB);
         const int buf = seg_i & 1;
         const uint32_t aph = (seg_i >> 1) & 1;
         if (!mbar_wait(&acc_empty[buf], aph ^ 1)) {
@@ -326,6 +344,9 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
         i += kb1 - kb0;
       }
       if (!ok) raise_error(p.err, DFLASH_DERR_TIMEOUT);
+      // every MMA issued by this thread must be complete before TMEM is freed
+      umma_commit(mma_done);
+      mbar_wait(mma_done, 0);
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -338,7 +359,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
     for (long long i = R.b; i < R.e; ++seg_i) {
       const int tile = (int)(i / p.KB);
       const int kb0 = (int)(i % p.KB);
-      const int kb1 = (int)min<long long>(p.KB, kb0 + (R.e - i));
+      const int kb1 = (int)(kb0 + (R.e - i) < p.KB ? kb0 + (R.e - i) : p.KB);
       i += kb1 - kb0;
       int seg, n0, m0;
       locate(tile, seg, n0, m0);
@@ -346,7 +367,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
       const int rows = min(BN, p.M - m0);
       const int buf = seg_i & 1;
       const uint32_t aph = (seg_i >> 1) & 1;
-      const bool ok = mbar_wait(&acc_full[buf], aph);
+      const bool ok = epi_all(mbar_wait(&acc_full[buf], aph));
       if (!ok) {
         if (tid == 0) raise_error(p.err, DFLASH_DERR_TIMEOUT);
         break;
@@ -499,7 +520,14 @@ cudaError_t set_attr() {
 
 }  // namespace
 
-size_t gemm_tc_partials_bytes(int num_sms) { return (size_t)num_sms * 2 * 2 * 256 * 128 * 4; }
+// Partial-tile scratch: per CTA two slots of (pair ? 2 : 1) * BN * 128 fp32, at most 256 * 128.
+size_t gemm_tc_partials_bytes() { return (size_t)kTcMaxCtas * 2 * 256 * 128 * 4; }
+
+int gemm_tc_tiles(int n_tiles, int M, bool pair) {
+  int BN = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
+  if (pair && BN > 128) BN = 128;
+  return n_tiles * ((M + BN - 1) / BN);
+}
 
 int gemm_tc_num_sms() {
   if (!g_num_sms) {
@@ -557,7 +585,7 @@ cudaError_t launch_gemm_tc(const GemmProblem &P, float *partials, int *counters,
   p.partials = partials;
   p.counters = counters;
   p.err = err;
-  const int G = (int)std::min<long long>(gemm_tc_num_sms(), p.total_iters);
+  const int G = (int)std::min<long long>(std::min(gemm_tc_num_sms(), kTcMaxCtas), p.total_iters);
   switch (BN | (pair ? 1 : 0)) {
     case 16: return launch_cfg<16, false>(p, G, s);
     case 32: return launch_cfg<32, false>(p, G, s);

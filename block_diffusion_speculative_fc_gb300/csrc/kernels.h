@@ -74,7 +74,14 @@ struct AttnParams {
   unsigned int *err;
 };
 
+constexpr int kTcMaxCtas = 160;   // persistent tensor-core GEMM grid cap (>= SM count)
+
 // ---- launchers (return cudaGetLastError()) ----
+cudaError_t launch_gemm_tc(const GemmProblem &P, float *partials, int *counters, int max_tiles,
+                           unsigned int *err, cudaStream_t s);
+size_t gemm_tc_partials_bytes();
+int gemm_tc_tiles(int n_tiles, int M, bool pair);
+cudaError_t prepare_gemm_tc();
 cudaError_t launch_gemm_simt(int store, const GemmProblem &P, cudaStream_t s);
 cudaError_t launch_attention_simt(int store, const AttnParams &p, cudaStream_t s);
 

@@ -1,0 +1,55 @@
+// Test-only entry point: the tensor-core GEMM on its own (include/dflash_testing.h).
+#include <cstring>
+
+#include "../../include/dflash_testing.h"
+#include "kernels.h"
+
+using namespace dflash;
+
+extern "C" size_t dflash_test_gemm_scratch(int32_t M, int32_t N) {
+  const int tiles = gemm_tc_tiles((N + 127) / 128, M > 0 ? M : 1, false);
+  return gemm_tc_partials_bytes() + 4 * (size_t)tiles + 256;
+}
+
+extern "C" int dflash_test_gemm(int32_t M, int32_t N, int32_t K, int32_t n_src,
+                                const void *const *A, int32_t lda, const void *W, int32_t ldw,
+                                int32_t op, void *out, void *act_out, void *scratch,
+                                size_t scratch_bytes, dflash_stream_t stream) {
+  if (M <= 0 || N <= 0 || K <= 0 || n_src <= 0 || n_src > kMaxSrc || !A || !W || !scratch)
+    return DFLASH_EINVAL;
+  if (K % n_src || (K / n_src) % 64) return DFLASH_EUNSUPPORTED;
+  if (scratch_bytes < dflash_test_gemm_scratch(M, N)) return DFLASH_ECAPACITY;
+  if (op != EPI_STORE_F32 && op != EPI_SWIGLU && op != EPI_ARGMAX) return DFLASH_EINVAL;
+  if (op == EPI_SWIGLU && (N % 2 || !act_out)) return DFLASH_EINVAL;
+  if (op != EPI_SWIGLU && !out) return DFLASH_EINVAL;
+  cudaStream_t s = (cudaStream_t)stream;
+  GemmProblem P;
+  std::memset(&P, 0, sizeof(P));
+  for (int j = 0; j < n_src; ++j) P.A.ptr[j] = A[j];
+  P.A.ld = lda;
+  P.A.k_per_src = K / n_src;
+  P.A.n_src = n_src;
+  P.M = M;
+  P.K = K;
+  GemmSeg &g = P.seg[P.nseg++];
+  g.W = W;
+  g.ldw = ldw;
+  g.N = N;
+  std::memset(&g.epi, 0, sizeof(g.epi));
+  g.epi.op = op;
+  g.epi.N = N;
+  g.epi.ld = op == EPI_SWIGLU ? N / 2 : N;
+  g.epi.out_f32 = (float *)out;
+  g.epi.out_act = act_out;
+  g.epi.argmax_keys = (unsigned long long *)out;
+  char *base = (char *)scratch;
+  unsigned int *err = (unsigned int *)base;
+  float *partials = (float *)(base + 256);
+  int *counters = (int *)(base + 256 + gemm_tc_partials_bytes());
+  const int tiles = gemm_tc_tiles((N + 127) / 128, M, false);
+  if (cudaMemsetAsync(base, 0, 256, s) != cudaSuccess) return DFLASH_ECUDA;
+  if (cudaMemsetAsync(counters, 0, 4 * (size_t)tiles, s) != cudaSuccess) return DFLASH_ECUDA;
+  if (prepare_gemm_tc() != cudaSuccess) return DFLASH_ECUDA;
+  if (launch_gemm_tc(P, partials, counters, tiles, err, s) != cudaSuccess) return DFLASH_ECUDA;
+  return DFLASH_OK;
+}

@@ -1,0 +1,36 @@
+/*
+ * dflash_testing.h -- test-only entry point of libdflash.
+ *
+ * Runs the tensor-core GEMM of the library on its own so that it can be
+ * compared with a plain matrix product; the draft pass never calls it.
+ */
+#ifndef DFLASH_TESTING_H
+#define DFLASH_TESTING_H
+
+#include "dflash.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * Y[m, n] = sum_k A[m, k] * W[n, k] with bf16 inputs and fp32 accumulation.
+ *   A       HOST array [n_src] of device pointers, each [M, K / n_src] bf16
+ *           with row stride lda elements (the K-split operand of the fc step)
+ *   W       device [N, K] bf16, row stride ldw
+ *   op      0: out = Y as fp32 [M, N];
+ *           2: act_out = silu(Y[:, :N/2]) * Y[:, N/2:] as bf16 [M, N/2];
+ *           3: argmax keys of each row into ((uint64_t*)out)[M] (caller zeroes them)
+ *   scratch device workspace of at least dflash_test_gemm_scratch(M, N) bytes
+ * Returns a dflash_status.
+ */
+size_t dflash_test_gemm_scratch(int32_t M, int32_t N);
+int dflash_test_gemm(int32_t M, int32_t N, int32_t K, int32_t n_src, const void *const *A,
+                     int32_t lda, const void *W, int32_t ldw, int32_t op, void *out,
+                     void *act_out, void *scratch, size_t scratch_bytes, dflash_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DFLASH_TESTING_H */

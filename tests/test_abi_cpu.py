@@ -36,6 +36,7 @@ def test_library_exports_every_declared_symbol(lib):
     for n in names:
         assert hasattr(lib, n), n
     assert set(pkg.EXPORTED) <= set(names)
+    assert "dflash_test_gemm" in names
 
 
 def _session_structs(cfg, **over):
