@@ -1,0 +1,505 @@
+// bf16 block attention on the tensor cores, paged KV staged by TMA.
+//
+// Non-causal attention of the S block queries over [committed context ; the S
+// block keys] ("Inside SGLang: DFlash and DFlash 2 Implementation", Step 4:
+// two K/V sources inside draft attention; CSDN DFlash article, "draft model
+// predict", is_causal=False), with the optional sliding window of the
+// Kimi-K2.6 draft card (a context key at pk is visible to a query at pq iff
+// pq - pk < W).
+//
+// Work split (flash-decoding): every (request b, KV head g) owns the R = G*S
+// query rows of its query-head group.  Its context pages are cut into splits of
+// `pps` pages; the last split also takes the S block keys.  A prep kernel
+// sizes the splits from the device-side kv_len so that the whole batch makes
+// about two work items per SM, and a persistent kernel walks the item list.
+// Per item: one 64-key tile at a time (one KV page of one head: two TMA boxes
+// of 64 rows x 64 dims for K and two for V, 128-byte swizzle, 3-stage ring),
+// S = Q K^T and O += P V with mma.sync m16n8k16 (bf16 in, fp32 accumulate),
+// online softmax in registers with quad shuffles.  A split that is not alone
+// writes (O, m, l) to scratch; the last split of a (b, g) to finish (atomic
+// ticket) merges the splits in split order and writes the output.
+#include <cuda.h>
+
+#include <algorithm>
+#include <cstring>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace dflash {
+namespace att {
+
+constexpr int KT = 64;          // keys per tile (one page)
+constexpr int STAGES = 3;
+constexpr int TILE_BYTES = KT * 128 * 2;   // K (or V) tile: 64 keys x 128 dims
+constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 64;
+constexpr uint32_t WAIT_LIMIT = 1u << 22;
+
+struct Params {
+  CUtensorMap tmK, tmV;          // cache: dims {D, KVH, n_pages*64}, box {64, 1, 64}
+  CUtensorMap tmKb, tmVb;        // block keys: dims {D, KVH, B*S}, box {64, 1, 64}
+  const bf16 *q;                 // [B*S, n_heads, D]
+  bf16 *out;                     // [B*S, n_heads, D]
+  const int *page_table;
+  const int *kv_len;
+  const int *item_start;         // [B*KVH + 1] prefix of splits per (b, g)
+  const int *pps_ptr;            // pages per split (device scalar)
+  float *part_o;                 // [max_items][R][D]
+  float2 *part_ml;               // [max_items][R]
+  int *tickets;                  // [B*KVH]
+  unsigned int *err;
+  int B, S, n_heads, kvh, pages_per_req, n_pages, window, R, max_items;
+  float scale_log2;              // log2(e) / sqrt(D)
+};
+
+__device__ __forceinline__ uint32_t su32(const void *p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ bool mbar_try(uint64_t *b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(su32(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity) {
+  for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
+    if (mbar_try(b, parity)) return true;
+    if (i > 64) __nanosleep(64);
+  }
+  return false;
+}
+__device__ __forceinline__ void tma3(void *dst, const CUtensorMap *tm, uint64_t *bar, int x, int y,
+                                     int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(su32(dst)),
+      "l"((uint64_t)tm), "r"(su32(bar)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                        uint32_t &r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                          uint32_t &r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma16816(float *c, const uint32_t *a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+// Byte address of (row, 16-byte chunk c) in a tile of rows of 128 bytes with
+// the 128-byte swizzle TMA applies (chunk index XOR row % 8).
+__device__ __forceinline__ uint32_t swz(uint32_t base, int row, int c) {
+  return base + row * 128 + (((c ^ row) & 7) << 4);
+}
+
+// ---------------------------------------------------------------- work list
+__global__ void attn_prep_kernel(const int *__restrict__ kv_len, int B, int kvh, int cap,
+                                 int window, int target_items, int max_items, int *item_start,
+                                 int *pps_out, unsigned int *err) {
+  __shared__ int s_total;
+  if (threadIdx.x == 0) s_total = 0;
+  __syncthreads();
+  int local = 0;
+  for (int b = threadIdx.x; b < B; b += blockDim.x) {
+    int kv = kv_len[b];
+    kv = kv < 0 ? 0 : (kv > cap ? cap : kv);
+    const int lo = window > 0 ? max(0, kv - window + 1) : 0;
+    const int pages = kv > lo ? (kv - 1) / KT - lo / KT + 1 : 0;
+    local += pages;
+  }
+  atomicAdd(&s_total, local * kvh);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int total = s_total;
+    int pps = max(1, (total + target_items - 1) / target_items);
+    // keep the item count within the scratch: B*kvh + total/pps <= max_items
+    while (B * kvh + total / pps + 1 > max_items) ++pps;
+    *pps_out = pps;
+    int acc = 0;
+    for (int b = 0; b < B; ++b) {
+      int kv = kv_len[b];
+      if (kv < 0 || kv > cap) raise_error(err, DFLASH_DERR_KV_CAPACITY);
+      kv = kv < 0 ? 0 : (kv > cap ? cap : kv);
+      const int lo = window > 0 ? max(0, kv - window + 1) : 0;
+      const int pages = kv > lo ? (kv - 1) / KT - lo / KT + 1 : 0;
+      const int nsplit = max(1, (pages + pps - 1) / pps);
+      for (int g = 0; g < kvh; ++g) {
+        item_start[b * kvh + g] = acc;
+        acc += nsplit;
+      }
+    }
+    item_start[B * kvh] = acc;
+  }
+}
+
+// ---------------------------------------------------------------- main kernel
+__global__ void __launch_bounds__(256) attn_mma_kernel(const __grid_constant__ Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint64_t *full = (uint64_t *)(smem + STAGES * STAGE_BYTES);
+  int *s_flag = (int *)(full + STAGES);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nwarps = blockDim.x >> 5;
+  const int grp = lane >> 2, tig = lane & 3;
+  const int S = p.S, R = p.R, G = p.n_heads / p.kvh;
+  const int pps = *p.pps_ptr;
+  const int n_bg = p.B * p.kvh;
+  const int total_items = p.item_start[n_bg];
+  const int cap = p.pages_per_req * KT;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&full[i])));
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  uint32_t use = 0;   // stage uses so far (ring position and phase)
+
+  for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
+    // item -> (b, g, split)
+    int lo_i = 0, hi_i = n_bg - 1;
+    while (lo_i < hi_i) {
+      const int mid = (lo_i + hi_i + 1) >> 1;
+      if (p.item_start[mid] <= item) lo_i = mid; else hi_i = mid - 1;
+    }
+    const int bg = lo_i, b = bg / p.kvh, g = bg % p.kvh;
+    const int split = item - p.item_start[bg];
+    const int nsplit = p.item_start[bg + 1] - p.item_start[bg];
+    int kv = p.kv_len[b];
+    kv = kv < 0 ? 0 : (kv > cap ? cap : kv);
+    const int lo = p.window > 0 ? max(0, kv - p.window + 1) : 0;
+    const int first_page = lo / KT;
+    const int pages = kv > lo ? (kv - 1) / KT - first_page + 1 : 0;
+    const int pg0 = split * pps, pg1 = min(pages, pg0 + pps);
+    const bool has_block = split == nsplit - 1;
+    const int ntiles = max(0, pg1 - pg0) + (has_block ? 1 : 0);
+
+    // query rows of this warp: r = warp*16 + grp (+8); row r -> head g*G + r/S, position j = r%S
+    const int r0 = warp * 16 + grp, r1 = r0 + 8;
+    uint32_t qa[8][4];
+    {
+      const bf16 *q = p.q;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int r = hh ? r1 : r0;
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const int d = ks * 16 + half * 8 + tig * 2;
+            uint32_t v = 0;
+            if (r < R) {
+              const int h = g * G + r / S, j = r % S;
+              v = *reinterpret_cast<const uint32_t *>(q + ((size_t)(b * S + j) * p.n_heads + h) * 128 + d);
+            }
+            qa[ks][half * 2 + hh] = v;
+          }
+        }
+      }
+    }
+    float o[16][4];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    const int j0 = r0 % S, j1 = r1 % S;
+    const int lo0 = p.window > 0 ? kv + j0 - p.window + 1 : 0;   // first visible ctx position
+    const int lo1 = p.window > 0 ? kv + j1 - p.window + 1 : 0;
+
+    auto issue = [&](int t, uint32_t u) {
+      uint8_t *st = smem + (u % STAGES) * STAGE_BYTES;
+      uint64_t *bar = &full[u % STAGES];
+      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(bar)),
+                   "r"(STAGE_BYTES)
+                   : "memory");
+      if (t < pg1 - pg0) {
+        const int lp = first_page + pg0 + t;
+        int page = p.page_table[(size_t)b * p.pages_per_req + lp];
+        if (page < 0 || page >= p.n_pages) {
+          raise_error(p.err, DFLASH_DERR_PAGE_RANGE);
+          page = 0;
+        }
+        tma3(st, &p.tmK, bar, 0, g, page * KT);
+        tma3(st + TILE_BYTES / 2, &p.tmK, bar, 64, g, page * KT);
+        tma3(st + TILE_BYTES, &p.tmV, bar, 0, g, page * KT);
+        tma3(st + TILE_BYTES + TILE_BYTES / 2, &p.tmV, bar, 64, g, page * KT);
+      } else {
+        tma3(st, &p.tmKb, bar, 0, g, b * S);
+        tma3(st + TILE_BYTES / 2, &p.tmKb, bar, 64, g, b * S);
+        tma3(st + TILE_BYTES, &p.tmVb, bar, 0, g, b * S);
+        tma3(st + TILE_BYTES + TILE_BYTES / 2, &p.tmVb, bar, 64, g, b * S);
+      }
+    };
+    if (threadIdx.x == 0)
+      for (int t = 0; t < STAGES && t < ntiles; ++t) issue(t, use + t);
+
+    bool ok = true;
+    for (int t = 0; t < ntiles; ++t) {
+      const uint32_t u = use + t;
+      const bool got = mbar_wait(&full[u % STAGES], (u / STAGES) & 1);
+      if (!got) ok = false;
+      const uint32_t kbase = su32(smem + (u % STAGES) * STAGE_BYTES);
+      const uint32_t vbase = kbase + TILE_BYTES;
+      const bool blk = t >= pg1 - pg0;
+      const int pos0 = (first_page + pg0 + t) * KT;   // position of key 0 of a context tile
+      // ---- S = Q K^T (16 rows x 64 keys per warp)
+      float s[8][4];
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+        for (int kc = 0; kc < 4; ++kc) {          // 32 dims per ldmatrix.x4
+          const int key = nt * 8 + (lane & 7);
+          const int d = kc * 32 + (lane >> 3) * 8;
+          const uint32_t addr = swz(kbase + (d >> 6) * (TILE_BYTES / 2), key, (d & 63) >> 3);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(addr, b0, b1, b2, b3);
+          mma16816(s[nt], qa[kc * 2], b0, b1);
+          mma16816(s[nt], qa[kc * 2 + 1], b2, b3);
+        }
+      }
+      // ---- mask, online softmax
+      float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int key = nt * 8 + tig * 2 + (e & 1);
+          const bool row1 = e >= 2;
+          bool vis;
+          if (blk) {
+            vis = key < S;
+          } else {
+            const int pos = pos0 + key;
+            vis = pos < kv && pos >= (row1 ? lo1 : lo0);
+          }
+          if ((row1 ? r1 : r0) >= R) vis = false;
+          const float v = vis ? s[nt][e] * p.scale_log2 : -INFINITY;
+          s[nt][e] = v;
+          if (row1) mx1 = fmaxf(mx1, v); else mx0 = fmaxf(mx0, v);
+        }
+      }
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      const float a0 = mn0 == -INFINITY ? 1.f : exp2f(m0 - mn0);
+      const float a1 = mn1 == -INFINITY ? 1.f : exp2f(m1 - mn1);
+      m0 = mn0;
+      m1 = mn1;
+      float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+        s[nt][0] = s[nt][0] == -INFINITY ? 0.f : exp2f(s[nt][0] - mn0);
+        s[nt][1] = s[nt][1] == -INFINITY ? 0.f : exp2f(s[nt][1] - mn0);
+        s[nt][2] = s[nt][2] == -INFINITY ? 0.f : exp2f(s[nt][2] - mn1);
+        s[nt][3] = s[nt][3] == -INFINITY ? 0.f : exp2f(s[nt][3] - mn1);
+        ps0 += s[nt][0] + s[nt][1];
+        ps1 += s[nt][2] + s[nt][3];
+      }
+      l0 = l0 * a0 + ps0;
+      l1 = l1 * a1 + ps1;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        o[i][0] *= a0;
+        o[i][1] *= a0;
+        o[i][2] *= a1;
+        o[i][3] *= a1;
+      }
+      // ---- O += P V (P from the S accumulators, V via transposed ldmatrix)
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {              // 16 keys per step
+        uint32_t pa[4];
+        pa[0] = pack_bf16(s[2 * kk][0], s[2 * kk][1]);
+        pa[1] = pack_bf16(s[2 * kk][2], s[2 * kk][3]);
+        pa[2] = pack_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1]);
+        pa[3] = pack_bf16(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+#pragma unroll
+        for (int np = 0; np < 8; ++np) {            // pairs of 8-dim n-tiles
+          const int key = kk * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+          const int d = np * 16 + (lane >> 4) * 8;
+          const uint32_t addr = swz(vbase + (d >> 6) * (TILE_BYTES / 2), key, (d & 63) >> 3);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(addr, b0, b1, b2, b3);
+          mma16816(o[2 * np], pa, b0, b1);
+          mma16816(o[2 * np + 1], pa, b2, b3);
+        }
+      }
+      __syncthreads();   // every warp is done with this stage
+      if (threadIdx.x == 0 && t + STAGES < ntiles) issue(t + STAGES, u + STAGES);
+    }
+    use += ntiles;
+    if (!ok && lane == 0) raise_error(p.err, DFLASH_DERR_TIMEOUT);
+
+    // ---- finish: row sums across the quad
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    if (nsplit == 1) {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int r = hh ? r1 : r0;
+        if (r >= R) continue;
+        const float inv = 1.f / (hh ? l1 : l0);
+        const int h = g * G + r / S, j = r % S;
+        bf16 *dst = p.out + ((size_t)(b * S + j) * p.n_heads + h) * 128;
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt) {
+          const int d = nt * 8 + tig * 2;
+          *reinterpret_cast<__nv_bfloat162 *>(dst + d) =
+              __floats2bfloat162_rn(o[nt][hh * 2] * inv, o[nt][hh * 2 + 1] * inv);
+        }
+      }
+      continue;
+    }
+    float *po = p.part_o + (size_t)item * R * 128;
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int r = hh ? r1 : r0;
+      if (r >= R) continue;
+#pragma unroll
+      for (int nt = 0; nt < 16; ++nt) {
+        const int d = nt * 8 + tig * 2;
+        *reinterpret_cast<float2 *>(po + r * 128 + d) = make_float2(o[nt][hh * 2], o[nt][hh * 2 + 1]);
+      }
+      if (tig == 0) p.part_ml[(size_t)item * R + r] = make_float2(hh ? m1 : m0, hh ? l1 : l0);
+    }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) *s_flag = atomicAdd(&p.tickets[bg], 1) == nsplit - 1;
+    __syncthreads();
+    if (*s_flag) {
+      __threadfence();
+      const int base = p.item_start[bg];
+      for (int idx = threadIdx.x; idx < R * 128; idx += blockDim.x) {
+        const int r = idx >> 7, d = idx & 127;
+        float mstar = -INFINITY;
+        for (int sp = 0; sp < nsplit; ++sp) mstar = fmaxf(mstar, __ldcg(&p.part_ml[(size_t)(base + sp) * R + r].x));
+        float num = 0.f, den = 0.f;
+        for (int sp = 0; sp < nsplit; ++sp) {
+          const float2 ml = __ldcg(&p.part_ml[(size_t)(base + sp) * R + r]);
+          const float w = ml.x == -INFINITY ? 0.f : exp2f(ml.x - mstar);
+          num += w * __ldcg(&p.part_o[((size_t)(base + sp) * R + r) * 128 + d]);
+          den += w * ml.y;
+        }
+        const int h = g * G + r / S, j = r % S;
+        p.out[((size_t)(b * S + j) * p.n_heads + h) * 128 + d] = __float2bfloat16_rn(num / den);
+      }
+      if (threadIdx.x == 0) p.tickets[bg] = 0;
+    }
+    __syncthreads();
+  }
+  (void)nwarps;
+}
+
+}  // namespace att
+
+namespace {
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn att_encoder() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (EncodeTiledFn)ptr;
+  }
+  return fn;
+}
+// [rows, kvh, 128] bf16 viewed as dims {128, kvh, rows}; box {64, 1, 64}.
+bool encode_kv(CUtensorMap *tm, const void *base, uint64_t rows, int kvh) {
+  EncodeTiledFn fn = att_encoder();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {128, (cuuint64_t)kvh, rows};
+  cuuint64_t strides[2] = {128 * 2, (cuuint64_t)kvh * 128 * 2};
+  cuuint32_t box[3] = {64, 1, 64};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+}  // namespace
+
+size_t attention_mma_scratch_items(int max_batch, int kvh) {
+  return (size_t)max_batch * kvh + 2 * (size_t)kTcMaxCtas + 8;
+}
+
+cudaError_t prepare_attention_mma() {
+  return cudaFuncSetAttribute(att::attn_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              att::SMEM);
+}
+
+cudaError_t launch_attention_mma(const AttnParams &a, const AttnScratch &w, cudaStream_t s) {
+  if (a.B <= 0) return cudaSuccess;
+  if (a.head_dim != 128 || a.page_size != att::KT) return cudaErrorInvalidValue;
+  const int R = (a.n_heads / a.n_kv_heads) * a.S;
+  const int warps = (R + 15) / 16;
+  if (warps > 8) return cudaErrorInvalidValue;
+  att::Params p;
+  memset(&p, 0, sizeof(p));
+  if (!encode_kv(&p.tmK, a.k_cache, (uint64_t)a.n_pages * att::KT, a.n_kv_heads) ||
+      !encode_kv(&p.tmV, a.v_cache, (uint64_t)a.n_pages * att::KT, a.n_kv_heads) ||
+      !encode_kv(&p.tmKb, a.kb, (uint64_t)a.B * a.S, a.n_kv_heads) ||
+      !encode_kv(&p.tmVb, a.vb, (uint64_t)a.B * a.S, a.n_kv_heads))
+    return cudaErrorInvalidValue;
+  int sms = 0, dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (sms <= 0) sms = 1;
+  const int max_items = (int)attention_mma_scratch_items(a.B, a.n_kv_heads);
+  att::attn_prep_kernel<<<1, 256, 0, s>>>(a.kv_len, a.B, a.n_kv_heads, a.pages_per_req * att::KT,
+                                           a.window, 2 * sms, max_items, w.item_start, w.pps,
+                                           a.err);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  p.q = (const bf16 *)a.q;
+  p.out = (bf16 *)a.out;
+  p.page_table = a.page_table;
+  p.kv_len = a.kv_len;
+  p.item_start = w.item_start;
+  p.pps_ptr = w.pps;
+  p.part_o = w.part_o;
+  p.part_ml = (float2 *)w.part_ml;
+  p.tickets = w.tickets;
+  p.err = a.err;
+  p.B = a.B;
+  p.S = a.S;
+  p.n_heads = a.n_heads;
+  p.kvh = a.n_kv_heads;
+  p.pages_per_req = a.pages_per_req;
+  p.n_pages = a.n_pages;
+  p.window = a.window;
+  p.R = R;
+  p.max_items = max_items;
+  p.scale_log2 = 1.4426950408889634f * a.scale;
+  att::attn_mma_kernel<<<2 * sms, warps * 32, att::SMEM, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace dflash

@@ -148,8 +148,10 @@ cudaError_t prepare_attention_simt() {
 }
 
 cudaError_t prepare_kernels() {
-  const cudaError_t e = prepare_attention_simt();
-  return e != cudaSuccess ? e : prepare_gemm_tc();
+  cudaError_t e = prepare_attention_simt();
+  if (e == cudaSuccess) e = prepare_gemm_tc();
+  if (e == cudaSuccess) e = prepare_attention_mma();
+  return e;
 }
 
 }  // namespace dflash

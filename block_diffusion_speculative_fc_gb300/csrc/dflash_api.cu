@@ -25,6 +25,8 @@ struct Layout {
   size_t err, rope, x, h, qb, kb, vb, attn, act, row_pos, keys, y, yh, slot, rpos;
   size_t tc_partials, tc_counters;
   int tc_max_tiles;
+  size_t att_item_start, att_pps, att_part_o, att_part_ml, att_tickets;
+  int att_bg;
   size_t total;
 };
 
@@ -94,6 +96,15 @@ Layout plan(const dflash_config &c, size_t es) {
     L.tc_max_tiles = mt;
     L.tc_partials = take(gemm_tc_partials_bytes());
     L.tc_counters = take(4 * (size_t)mt);
+    // attention split scratch
+    const size_t R = (size_t)(c.n_heads / c.n_kv_heads) * c.block_size;
+    const size_t items = attention_mma_scratch_items(c.max_batch, c.n_kv_heads);
+    L.att_bg = c.max_batch * c.n_kv_heads;
+    L.att_item_start = take(4 * ((size_t)L.att_bg + 1));
+    L.att_pps = take(4);
+    L.att_part_o = take(4 * items * R * 128);
+    L.att_part_ml = take(8 * items * R);
+    L.att_tickets = take(4 * (size_t)L.att_bg);
   }
   L.total = o;
   return L;
@@ -126,7 +137,14 @@ cudaError_t run_gemm(dflash_handle *h, const GemmProblem &P, cudaStream_t s) {
 }
 
 cudaError_t run_attention(dflash_handle *h, const AttnParams &a, cudaStream_t s) {
-  return launch_attention_simt(h->store, a, s);
+  if (h->store == ST_F32) return launch_attention_simt(ST_F32, a, s);
+  AttnScratch w;
+  w.item_start = at<int>(h, h->L.att_item_start);
+  w.pps = at<int>(h, h->L.att_pps);
+  w.part_o = at<float>(h, h->L.att_part_o);
+  w.part_ml = at<float>(h, h->L.att_part_ml);
+  w.tickets = at<int>(h, h->L.att_tickets);
+  return launch_attention_mma(a, w, s);
 }
 
 EpiParams epi_base(const dflash_handle *h, int op) {
@@ -211,6 +229,8 @@ int dflash_create(const dflash_config *cfg, const dflash_weights *w, dflash_hand
   if ((c.n_heads / c.n_kv_heads) * c.block_size > 128)
     return fail(DFLASH_EUNSUPPORTED, "(n_heads/n_kv_heads)*block_size must be <= 128");
   if (c.page_size != 64) return fail(DFLASH_EUNSUPPORTED, "page_size must be 64");
+  if (c.dtype == DFLASH_BF16 && c.head_dim != 128)
+    return fail(DFLASH_EUNSUPPORTED, "bf16 configurations need head_dim 128");
   if (c.mask_token_id < 0 || c.mask_token_id >= c.vocab) return fail(DFLASH_EINVAL, "mask_token_id outside the vocabulary");
   if (!(c.rms_eps >= 0.f) || !(c.rope_theta > 0.f)) return fail(DFLASH_EINVAL, "rms_eps >= 0 and rope_theta > 0 required");
   if (c.max_position < c.block_size) return fail(DFLASH_EINVAL, "max_position < block_size");
@@ -321,6 +341,10 @@ int dflash_bind_workspace(dflash_handle *h, void *dev_ptr, size_t bytes, dflash_
   if (h->L.tc_max_tiles > 0 &&
       (st = check_cuda(cudaMemsetAsync(h->ws + h->L.tc_counters, 0, 4 * (size_t)h->L.tc_max_tiles, s),
                        "clear GEMM tickets")))
+    return st;
+  if (h->L.att_bg > 0 &&
+      (st = check_cuda(cudaMemsetAsync(h->ws + h->L.att_tickets, 0, 4 * (size_t)h->L.att_bg, s),
+                       "clear attention tickets")))
     return st;
   st = check_cuda(launch_rope_table(at<float2>(h, h->L.rope), h->cfg.max_position, h->cfg.head_dim,
                                     h->cfg.rope_theta, s), "rope table");

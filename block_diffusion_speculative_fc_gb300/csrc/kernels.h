@@ -74,6 +74,14 @@ struct AttnParams {
   unsigned int *err;
 };
 
+struct AttnScratch {
+  int *item_start;   // [max_batch * kvh + 1]
+  int *pps;          // [1]
+  float *part_o;     // [max_items][R][128]
+  float *part_ml;    // [max_items][R][2]
+  int *tickets;      // [max_batch * kvh], zero between launches
+};
+
 constexpr int kTcMaxCtas = 160;   // persistent tensor-core GEMM grid cap (>= SM count)
 
 // ---- launchers (return cudaGetLastError()) ----
@@ -82,6 +90,9 @@ cudaError_t launch_gemm_tc(const GemmProblem &P, float *partials, int *counters,
 size_t gemm_tc_partials_bytes();
 int gemm_tc_tiles(int n_tiles, int M, bool pair);
 cudaError_t prepare_gemm_tc();
+cudaError_t launch_attention_mma(const AttnParams &p, const AttnScratch &w, cudaStream_t s);
+size_t attention_mma_scratch_items(int max_batch, int kvh);
+cudaError_t prepare_attention_mma();
 cudaError_t launch_gemm_simt(int store, const GemmProblem &P, cudaStream_t s);
 cudaError_t launch_attention_simt(int store, const AttnParams &p, cudaStream_t s);
 

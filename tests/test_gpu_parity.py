@@ -73,3 +73,17 @@ def test_prefill_chunked_equals_single_chunk():
     """max_rows smaller than the prefill: the chunked injection must match."""
     run = CycleRun(QWEN_MINI, 2, [150, 90], cycles=1, max_rows=64, permuted=True)
     _report(run.run())
+
+
+def test_qwen_mini_long_contexts_multi_page_splits():
+    """Contexts of thousands of rows: attention splits span several pages and
+    are merged across splits."""
+    run = CycleRun(QWEN_MINI, 4, [1500, 2100, 700, 3000], cycles=2, permuted=True,
+                   check=[0, 3], max_rows=2048)
+    _report(run.run())
+
+
+def test_kimi_mini_long_context_window_edge():
+    """Window 64 against contexts far longer than the window."""
+    run = CycleRun(KIMI_MINI, 2, [1000, 130], cycles=3, permuted=True)
+    _report(run.run())
