@@ -33,7 +33,8 @@ constexpr int KT = 64;          // keys per tile (one page)
 constexpr int STAGES = 3;
 constexpr int TILE_BYTES = KT * 128 * 2;   // K (or V) tile: 64 keys x 128 dims
 constexpr int STAGE_BYTES = 2 * TILE_BYTES;
-constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 64;
+constexpr int MAX_SPLITS = 16;  // splits of one (request, KV head) at most
+constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 64 + (MAX_SPLITS + 1) * 128 * 4;
 constexpr uint32_t WAIT_LIMIT = 1u << 22;
 
 struct Params {
@@ -127,12 +128,23 @@ __global__ void attn_prep_kernel(const int *__restrict__ kv_len, int B, int kvh,
     local += pages;
   }
   atomicAdd(&s_total, local * kvh);
+  __shared__ int s_maxpages;
+  if (threadIdx.x == 0) s_maxpages = 0;
+  __syncthreads();
+  for (int b = threadIdx.x; b < B; b += blockDim.x) {
+    int kv = kv_len[b];
+    kv = kv < 0 ? 0 : (kv > cap ? cap : kv);
+    const int lo = window > 0 ? max(0, kv - window + 1) : 0;
+    atomicMax(&s_maxpages, kv > lo ? (kv - 1) / KT - lo / KT + 1 : 0);
+  }
   __syncthreads();
   if (threadIdx.x == 0) {
     const int total = s_total;
-    int pps = max(1, (total + target_items - 1) / target_items);
-    // keep the item count within the scratch: B*kvh + total/pps <= max_items
+    // about one item per SM, at least two pages per split, at most MAX_SPLITS
+    // splits per (request, head), and never more items than the scratch holds
+    int pps = max(2, (total + target_items - 1) / target_items);
     while (B * kvh + total / pps + 1 > max_items) ++pps;
+    pps = max(pps, (s_maxpages + MAX_SPLITS - 1) / MAX_SPLITS);
     *pps_out = pps;
     int acc = 0;
     for (int b = 0; b < B; ++b) {
@@ -157,6 +169,7 @@ __global__ void __launch_bounds__(256) attn_mma_kernel(const __grid_constant__ P
   uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t *full = (uint64_t *)(smem + STAGES * STAGE_BYTES);
   int *s_flag = (int *)(full + STAGES);
+  float *s_w = (float *)(smem + STAGES * STAGE_BYTES + 64);   // [MAX_SPLITS + 1][R]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nwarps = blockDim.x >> 5;
   const int grp = lane >> 2, tig = lane & 3;
@@ -392,19 +405,39 @@ __global__ void __launch_bounds__(256) attn_mma_kernel(const __grid_constant__ P
     if (*s_flag) {
       __threadfence();
       const int base = p.item_start[bg];
-      for (int idx = threadIdx.x; idx < R * 128; idx += blockDim.x) {
-        const int r = idx >> 7, d = idx & 127;
+      // per-row merge weights of the splits, then a float4 sweep over O
+      for (int r = threadIdx.x; r < R; r += blockDim.x) {
         float mstar = -INFINITY;
-        for (int sp = 0; sp < nsplit; ++sp) mstar = fmaxf(mstar, __ldcg(&p.part_ml[(size_t)(base + sp) * R + r].x));
-        float num = 0.f, den = 0.f;
+        for (int sp = 0; sp < nsplit; ++sp)
+          mstar = fmaxf(mstar, __ldcg(&p.part_ml[(size_t)(base + sp) * R + r].x));
+        float den = 0.f;
         for (int sp = 0; sp < nsplit; ++sp) {
           const float2 ml = __ldcg(&p.part_ml[(size_t)(base + sp) * R + r]);
           const float w = ml.x == -INFINITY ? 0.f : exp2f(ml.x - mstar);
-          num += w * __ldcg(&p.part_o[((size_t)(base + sp) * R + r) * 128 + d]);
+          s_w[sp * R + r] = w;
           den += w * ml.y;
         }
+        s_w[MAX_SPLITS * R + r] = 1.f / den;
+      }
+      __syncthreads();
+#pragma unroll 4
+      for (int idx = threadIdx.x; idx < R * 32; idx += blockDim.x) {
+        const int r = idx >> 5, d = (idx & 31) * 4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int sp = 0; sp < nsplit; ++sp) {
+          const float w = s_w[sp * R + r];
+          const float4 v = __ldcg(reinterpret_cast<const float4 *>(
+              &p.part_o[((size_t)(base + sp) * R + r) * 128 + d]));
+          acc.x += w * v.x;
+          acc.y += w * v.y;
+          acc.z += w * v.z;
+          acc.w += w * v.w;
+        }
+        const float inv = s_w[MAX_SPLITS * R + r];
         const int h = g * G + r / S, j = r % S;
-        p.out[((size_t)(b * S + j) * p.n_heads + h) * 128 + d] = __float2bfloat16_rn(num / den);
+        bf16 *dst = p.out + ((size_t)(b * S + j) * p.n_heads + h) * 128 + d;
+        *reinterpret_cast<__nv_bfloat162 *>(dst) = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+        *reinterpret_cast<__nv_bfloat162 *>(dst + 2) = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
       }
       if (threadIdx.x == 0) p.tickets[bg] = 0;
     }
