@@ -1,4 +1,5 @@
-// CUDA-core block attention: the fp32 path of the library.
+// CUDA-core block attention: the fp32 path of the library (tcgen05 and
+// mma.sync have no exact-fp32 kind; bf16 configurations use attention_mma.cu).
 //
 // Non-causal attention of the S block queries of every query head over
 // [committed context keys ; all S block keys] ("Inside SGLang", Step 4: two
@@ -131,19 +132,14 @@ cudaError_t launch_attention_simt(int store, const AttnParams &p, cudaStream_t s
   if (p.B <= 0) return cudaSuccess;
   const int R = (p.n_heads / p.n_kv_heads) * p.S;
   const size_t smem = attention_simt_smem(R, p.head_dim);
-  if (store == ST_F32)
-    attn_simt_kernel<float><<<p.B * p.n_kv_heads, THREADS, smem, s>>>(p);
-  else
-    attn_simt_kernel<bf16><<<p.B * p.n_kv_heads, THREADS, smem, s>>>(p);
+  if (store != ST_F32) return cudaErrorInvalidValue;   // bf16 runs on the tensor cores
+  attn_simt_kernel<float><<<p.B * p.n_kv_heads, THREADS, smem, s>>>(p);
   return cudaGetLastError();
 }
 
 cudaError_t prepare_attention_simt() {
   const int smem = (int)attention_simt_smem(128, 128);
-  cudaError_t e = cudaFuncSetAttribute(attn_simt_kernel<float>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(attn_simt_kernel<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(attn_simt_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               smem);
 }
 

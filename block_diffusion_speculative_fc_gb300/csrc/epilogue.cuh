@@ -1,8 +1,8 @@
 // GEMM epilogues shared by every GEMM kernel of the library.
 //
 // A GEMM hands over an fp32 tile Y[r][c] (r = token row m0 + r, c = output
-// feature n0 + c, 128 features wide) staged in shared memory; the epilogue
-// turns it into the step's output:
+// feature n0 + c, 128 features wide, at most 32 rows) staged in shared
+// memory; the epilogue turns it into the step's output:
 //   EPI_QKV       per-head RMSNorm of q and k, RoPE of q and k, plain v
 //                 ("Inside SGLang", Step 4: DFlashAttention computes block
 //                 Q/K/V, normalizes Q/K, applies RoPE).
@@ -13,50 +13,120 @@
 //   EPI_SWIGLU    silu(gate) * up of a paired gate/up tile.
 //   EPI_ARGMAX    greedy token choice without materialising logits.
 //   EPI_RESID / EPI_STORE_*  residual add / plain stores.
+// The tile is tiny and sits on the critical path of short launches, so every
+// op issues its global loads in batches before using them (one memory round
+// trip per batch rather than one per element).
 #pragma once
 #include "common.cuh"
 #include "kernels.h"
 
 namespace dflash {
 
+constexpr int kEpiMaxRows = 32;
+
 // Rotate-half RoPE on one head held by a warp (component i pairs with
-// i + D/2), optionally preceded by a per-head RMSNorm with gain g[D].
-template <typename T>
+// i + D/2), optionally preceded by a per-head RMSNorm.  g_lo/g_hi: this lane's
+// gains for i = lane + 32k and i + D/2; cs: this lane's (cos, sin).
+template <typename T, int NP>
 __device__ __forceinline__ void head_epilogue(const float *src, int D, bool norm, bool rope,
-                                              const T *gain, float eps, const float2 *rope_row,
-                                              T *dst, int lane) {
+                                              const float *g_lo, const float *g_hi, float eps,
+                                              const float2 *cs, T *dst, int lane) {
   const int half = D >> 1;
+  float lo[NP], hi[NP];
+  float ss = 0.f;
+#pragma unroll
+  for (int k = 0; k < NP; ++k) {
+    const int i = lane + 32 * k;
+    lo[k] = i < half ? src[i] : 0.f;
+    hi[k] = i < half ? src[i + half] : 0.f;
+    ss += lo[k] * lo[k] + hi[k] * hi[k];
+  }
   float rstd = 1.f;
   if (norm) {
-    float ss = 0.f;
-    for (int i = lane; i < D; i += 32) ss += src[i] * src[i];
     ss = warp_sum(ss);
     rstd = rsqrtf(ss / (float)D + eps);
   }
-  for (int i = lane; i < half; i += 32) {
-    float lo = src[i], hi = src[i + half];
+#pragma unroll
+  for (int k = 0; k < NP; ++k) {
+    const int i = lane + 32 * k;
+    if (i >= half) continue;
+    float a = lo[k], b = hi[k];
     if (norm) {
-      lo *= rstd * to_f32(gain[i]);
-      hi *= rstd * to_f32(gain[i + half]);
+      a *= rstd * g_lo[k];
+      b *= rstd * g_hi[k];
     }
     if (rope) {
-      const float2 cs = rope_row[i];
-      const float a = lo * cs.x - hi * cs.y;
-      const float b = hi * cs.x + lo * cs.y;
-      lo = a;
-      hi = b;
+      const float x = a * cs[k].x - b * cs[k].y;
+      const float y = b * cs[k].x + a * cs[k].y;
+      a = x;
+      b = y;
     }
-    dst[i] = from_f32<T>(lo);
-    dst[i + half] = from_f32<T>(hi);
+    dst[i] = from_f32<T>(a);
+    dst[i + half] = from_f32<T>(b);
   }
 }
 
+// Per-head epilogues for D = 64 * NP.  One warp per (row, head) item; row
+// positions / cache slots come from shared memory, gains are loaded once.
+template <typename T, int NP, class Sync>
+__device__ void head_ops(const EpiParams &e, const float *t0, int ldt, int m0, int rows, int n0,
+                         int lane, int warp, int nwarps, const int *s_pos, const int *s_slot,
+                         Sync sync) {
+  const int D = e.head_dim;
+  const int hpt = 128 / D;
+  const int kvd = e.n_kv_heads * D;
+  const bool qkv = e.op == EPI_QKV;
+  for (int item = warp; item < rows * hpt; item += nwarps) {
+    const int r = item / hpt, hh = item % hpt;
+    const int f0 = n0 + hh * D;
+    if (f0 >= e.N) continue;
+    const int m = m0 + r;
+    const int hg = f0 / D;
+    // kind: 0 = q, 1 = k, 2 = v
+    int kind, head;
+    if (qkv) {
+      kind = hg < e.n_heads ? 0 : (hg < e.n_heads + e.n_kv_heads ? 1 : 2);
+      head = kind == 0 ? hg : (kind == 1 ? hg - e.n_heads : hg - e.n_heads - e.n_kv_heads);
+    } else {
+      kind = hg < e.n_kv_heads ? 1 : 2;
+      head = kind == 1 ? hg : hg - e.n_kv_heads;
+    }
+    T *dst;
+    if (qkv) {
+      dst = kind == 0 ? (T *)e.q_out + (int64_t)m * e.n_heads * D + head * D
+                      : (T *)(kind == 1 ? e.k_out : e.v_out) + (int64_t)m * kvd + head * D;
+    } else {
+      const int slot = s_slot[r];
+      if (slot < 0) continue;
+      dst = (T *)(kind == 1 ? e.k_cache : e.v_cache) + (int64_t)slot * kvd + head * D;
+    }
+    const bool nr = kind != 2;
+    float g_lo[NP], g_hi[NP];
+    float2 cs[NP];
+    if (nr) {
+      const T *gain = (const T *)(kind == 0 ? e.q_gain : e.k_gain);
+      const float2 *rope_row = e.rope + (int64_t)s_pos[r] * (D >> 1);
+#pragma unroll
+      for (int k = 0; k < NP; ++k) {
+        const int i = lane + 32 * k;
+        g_lo[k] = to_f32(gain[i]);
+        g_hi[k] = to_f32(gain[i + (D >> 1)]);
+        cs[k] = rope_row[i];
+      }
+    }
+    head_epilogue<T, NP>(t0 + r * ldt + hh * D, D, nr, nr, g_lo, g_hi, e.eps, cs, dst, lane);
+  }
+  (void)sync;
+}
+
 // t0: fp32 tile [rows][ldt] (features n0 .. n0+127); t1: the "up" tile of a
-// SwiGLU pair.  All `nthreads` threads of the caller take part; the caller
-// synchronises before (tile complete) and after (tile reuse).
-template <typename T>
+// SwiGLU pair.  All `nthreads` threads of the caller take part (a multiple of
+// 128); the caller synchronises before (tile complete) and after (tile reuse).
+// s_int: shared scratch of at least 2 * kEpiMaxRows ints; sync(): barrier over
+// the participating threads.
+template <typename T, class Sync>
 __device__ void run_epilogue(const EpiParams &e, const float *t0, const float *t1, int ldt, int m0,
-                             int rows, int n0, int tid, int nthreads) {
+                             int rows, int n0, int tid, int nthreads, int *s_int, Sync sync) {
   const int lane = tid & 31, warp = tid >> 5, nwarps = nthreads >> 5;
   switch (e.op) {
     case EPI_STORE_F32:
@@ -64,30 +134,55 @@ __device__ void run_epilogue(const EpiParams &e, const float *t0, const float *t
     case EPI_STORE_ACT:
     case EPI_SWIGLU: {
       const int nvalid = e.op == EPI_SWIGLU ? e.N / 2 : e.N;
-      for (int idx = tid; idx < rows * 128; idx += nthreads) {
-        const int r = idx >> 7, c = idx & 127, n = n0 + c;
-        if (n >= nvalid) continue;
-        const int64_t o = (int64_t)(m0 + r) * e.ld + n;
-        const float y = t0[r * ldt + c];
-        if (e.op == EPI_STORE_F32)
-          e.out_f32[o] = y;
-        else if (e.op == EPI_RESID)
-          e.out_f32[o] += y;
-        else if (e.op == EPI_STORE_ACT)
-          ((T *)e.out_act)[o] = from_f32<T>(y);
-        else
-          ((T *)e.out_act)[o] = from_f32<T>(silu(y) * t1[r * ldt + c]);
+      const int c = tid & 127, rg = tid >> 7, ng = nthreads >> 7;
+      const int n = n0 + c;
+      if (n >= nvalid) break;
+      constexpr int BATCH = 16;
+      for (int rb = rg; rb < rows; rb += BATCH * ng) {
+        float y[BATCH];
+#pragma unroll
+        for (int k = 0; k < BATCH; ++k) {
+          const int r = rb + k * ng;
+          y[k] = r < rows ? t0[r * ldt + c] : 0.f;
+        }
+        if (e.op == EPI_RESID) {
+          float old[BATCH];
+#pragma unroll
+          for (int k = 0; k < BATCH; ++k) {
+            const int r = rb + k * ng;
+            old[k] = r < rows ? e.out_f32[(int64_t)(m0 + r) * e.ld + n] : 0.f;
+          }
+#pragma unroll
+          for (int k = 0; k < BATCH; ++k) {
+            const int r = rb + k * ng;
+            if (r < rows) e.out_f32[(int64_t)(m0 + r) * e.ld + n] = old[k] + y[k];
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < BATCH; ++k) {
+            const int r = rb + k * ng;
+            if (r >= rows) continue;
+            const int64_t o = (int64_t)(m0 + r) * e.ld + n;
+            if (e.op == EPI_STORE_F32)
+              e.out_f32[o] = y[k];
+            else if (e.op == EPI_STORE_ACT)
+              ((T *)e.out_act)[o] = from_f32<T>(y[k]);
+            else
+              ((T *)e.out_act)[o] = from_f32<T>(silu(y[k]) * t1[r * ldt + c]);
+          }
+        }
       }
       break;
     }
     case EPI_ARGMAX: {
       for (int r = warp; r < rows; r += nwarps) {
         unsigned long long best = 0ull;
-        for (int c = lane; c < 128; c += 32) {
-          const int n = n0 + c;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int c = lane + 32 * k, n = n0 + c;
           if (n < e.N) {
-            const unsigned long long k = argmax_key(t0[r * ldt + c], n);
-            best = k > best ? k : best;
+            const unsigned long long key = argmax_key(t0[r * ldt + c], n);
+            best = key > best ? key : best;
           }
         }
 #pragma unroll
@@ -101,40 +196,17 @@ __device__ void run_epilogue(const EpiParams &e, const float *t0, const float *t
     }
     case EPI_QKV:
     case EPI_KV_CACHE: {
-      const int D = e.head_dim;
-      const int hpt = 128 / D;  // heads per 128-feature tile
-      const int kvd = e.n_kv_heads * D;
-      for (int item = warp; item < rows * hpt; item += nwarps) {
-        const int r = item / hpt, hh = item % hpt;
-        const int f0 = n0 + hh * D;
-        if (f0 >= e.N) continue;
-        const int m = m0 + r;
-        const int hg = f0 / D;
-        const float *src = t0 + r * ldt + hh * D;
-        const float2 *rope_row = e.rope + (int64_t)e.row_pos[m] * (D >> 1);
-        if (e.op == EPI_QKV) {
-          if (hg < e.n_heads) {
-            T *dst = (T *)e.q_out + (int64_t)m * e.n_heads * D + hg * D;
-            head_epilogue<T>(src, D, true, true, (const T *)e.q_gain, e.eps, rope_row, dst, lane);
-          } else if (hg < e.n_heads + e.n_kv_heads) {
-            T *dst = (T *)e.k_out + (int64_t)m * kvd + (hg - e.n_heads) * D;
-            head_epilogue<T>(src, D, true, true, (const T *)e.k_gain, e.eps, rope_row, dst, lane);
-          } else {
-            T *dst = (T *)e.v_out + (int64_t)m * kvd + (hg - e.n_heads - e.n_kv_heads) * D;
-            head_epilogue<T>(src, D, false, false, (const T *)nullptr, e.eps, rope_row, dst, lane);
-          }
-        } else {
-          const int slot = e.row_slot[m];
-          if (slot < 0) continue;
-          if (hg < e.n_kv_heads) {
-            T *dst = (T *)e.k_cache + (int64_t)slot * kvd + hg * D;
-            head_epilogue<T>(src, D, true, true, (const T *)e.k_gain, e.eps, rope_row, dst, lane);
-          } else {
-            T *dst = (T *)e.v_cache + (int64_t)slot * kvd + (hg - e.n_kv_heads) * D;
-            head_epilogue<T>(src, D, false, false, (const T *)nullptr, e.eps, rope_row, dst, lane);
-          }
-        }
+      int *s_pos = s_int, *s_slot = s_int + kEpiMaxRows;
+      for (int r = tid; r < rows; r += nthreads) {
+        s_pos[r] = e.row_pos[m0 + r];
+        s_slot[r] = e.op == EPI_KV_CACHE ? e.row_slot[m0 + r] : 0;
       }
+      sync();
+      if (e.head_dim == 128)
+        head_ops<T, 2>(e, t0, ldt, m0, rows, n0, lane, warp, nwarps, s_pos, s_slot, sync);
+      else
+        head_ops<T, 1>(e, t0, ldt, m0, rows, n0, lane, warp, nwarps, s_pos, s_slot, sync);
+      sync();
       break;
     }
     default:

@@ -97,7 +97,9 @@ __global__ void __launch_bounds__(THREADS) gemm_simt_kernel(const __grid_constan
       for (int j = 0; j < 4; ++j) (p ? t1 : t0)[(tm * 4 + j) * TLD + tf + 32 * i] = acc[p][i][j];
   __syncthreads();
   const int rows = min(BM, P.M - m0);
-  run_epilogue<T>(seg.epi, t0, PAIR ? t1 : nullptr, TLD, m0, rows, n0, tid, THREADS);
+  __shared__ int s_int[2 * kEpiMaxRows];
+  run_epilogue<T>(seg.epi, t0, PAIR ? t1 : nullptr, TLD, m0, rows, n0, tid, THREADS, s_int,
+                  [] { __syncthreads(); });
 }
 
 cudaError_t launch_gemm_simt(int store, const GemmProblem &P, cudaStream_t s) {
@@ -109,13 +111,9 @@ cudaError_t launch_gemm_simt(int store, const GemmProblem &P, cudaStream_t s) {
     tiles += (n + BN - 1) / BN;
   }
   dim3 grid(tiles, (P.M + BM - 1) / BM);
-  if (store == ST_F32) {
-    if (pair) gemm_simt_kernel<float, true><<<grid, THREADS, 0, s>>>(P);
-    else gemm_simt_kernel<float, false><<<grid, THREADS, 0, s>>>(P);
-  } else {
-    if (pair) gemm_simt_kernel<bf16, true><<<grid, THREADS, 0, s>>>(P);
-    else gemm_simt_kernel<bf16, false><<<grid, THREADS, 0, s>>>(P);
-  }
+  if (store != ST_F32) return cudaErrorInvalidValue;   // bf16 runs on the tensor cores
+  if (pair) gemm_simt_kernel<float, true><<<grid, THREADS, 0, s>>>(P);
+  else gemm_simt_kernel<float, false><<<grid, THREADS, 0, s>>>(P);
   return cudaGetLastError();
 }
 

@@ -209,7 +209,7 @@ struct Cfg {
   static constexpr int STAGE_BYTES = P * W_BYTES + A_BYTES;
   static constexpr int CH = BN < 32 ? BN : 32;          // epilogue token chunk
   static constexpr int STAGING_BYTES = P * CH * 128 * 4;
-  static constexpr int BAR_BYTES = 256;
+  static constexpr int BAR_BYTES = 512;   // mbarriers, TMEM slot, flag, epilogue row info
   static constexpr int BUDGET = 225 * 1024;
   static constexpr int STAGES_RAW = (BUDGET - 1024 - STAGING_BYTES - BAR_BYTES) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 12 ? 12 : STAGES_RAW;
@@ -234,6 +234,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
   uint64_t *mma_done = acc_empty + 2;
   uint32_t *tmem_slot = (uint32_t *)(mma_done + 1);
   int *flag = (int *)(tmem_slot + 1);
+  int *s_int = (int *)((uint8_t *)bars + 256);   // 2 * kEpiMaxRows ints
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x, cta = blockIdx.x;
@@ -389,7 +390,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
           epi_bar();
           if (c0 < rows)
             run_epilogue<T>(e, st0, PAIR ? st1 : nullptr, 128, m0 + c0, min(C::CH, rows - c0), n0,
-                            tid, 128);
+                            tid, 128, s_int, [] { epi_bar(); });
           epi_bar();
         }
         tc_fence_before();
@@ -432,12 +433,29 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
               float acc[32];
 #pragma unroll
               for (int t = 0; t < C::CH; ++t) acc[t] = 0.f;
-              for (int c = c_first; c <= c_last; ++c) {
+              // contributors in CTA order, two at a time so that twice the
+              // loads are in flight; the summation order stays fixed
+              auto slot_of = [&](int c) {
                 const long long cfirst_tile = (p.total_iters * c / G) / p.KB;
                 const int w = tile == cfirst_tile ? 0 : 1;
-                const float *src = p.partials + ((size_t)c * 2 + w) * (C::P * BN * 128);
+                return p.partials + ((size_t)c * 2 + w) * (C::P * BN * 128) + (q * BN + c0) * 128 + f;
+              };
+              int c = c_first;
+              for (; c < c_last; c += 2) {
+                const float *a = slot_of(c), *b2 = slot_of(c + 1);
+                float va[32], vb[32];
 #pragma unroll
-                for (int t = 0; t < C::CH; ++t) acc[t] += __ldcg(&src[(q * BN + c0 + t) * 128 + f]);
+                for (int t = 0; t < C::CH; ++t) {
+                  va[t] = __ldcg(a + t * 128);
+                  vb[t] = __ldcg(b2 + t * 128);
+                }
+#pragma unroll
+                for (int t = 0; t < C::CH; ++t) acc[t] = (acc[t] + va[t]) + vb[t];
+              }
+              if (c == c_last) {
+                const float *a = slot_of(c);
+#pragma unroll
+                for (int t = 0; t < C::CH; ++t) acc[t] += __ldcg(a + t * 128);
               }
               float *dst = q ? st1 : st0;
 #pragma unroll
@@ -446,7 +464,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
             epi_bar();
             if (c0 < rows)
               run_epilogue<T>(e, st0, PAIR ? st1 : nullptr, 128, m0 + c0, min(C::CH, rows - c0),
-                              n0, tid, 128);
+                              n0, tid, 128, s_int, [] { epi_bar(); });
             epi_bar();
           }
           if (tid == 0) p.counters[tile] = 0;   // ready for the next launch

@@ -55,28 +55,37 @@ cudaError_t launch_embed(int store, const void *embed, const int *anchor, const 
 template <typename Tin, typename Tout>
 __global__ void rmsnorm_kernel(const Tin *__restrict__ x, const Tout *__restrict__ g, int H,
                                float eps, Tout *__restrict__ out, Tout *__restrict__ out2) {
+  // one CTA per row; each thread keeps up to 32 values in registers so the
+  // row is read once with all loads in flight
+  constexpr int MAXV = 32;
   const int m = blockIdx.x;
   const Tin *row = x + (int64_t)m * H;
+  float v[MAXV];
   float ss = 0.f;
-  for (int c = threadIdx.x; c < H; c += blockDim.x) {
-    const float v = to_f32(row[c]);
-    ss += v * v;
+#pragma unroll
+  for (int k = 0; k < MAXV; ++k) {
+    const int c = threadIdx.x + k * blockDim.x;
+    v[k] = c < H ? to_f32(row[c]) : 0.f;
+    ss += v[k] * v[k];
   }
   __shared__ float red[32];
   ss = warp_sum(ss);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
   __syncthreads();
   if (threadIdx.x < 32) {
-    float v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
-    v = warp_sum(v);
-    if (threadIdx.x == 0) red[0] = v;
+    float t = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0.f;
+    t = warp_sum(t);
+    if (threadIdx.x == 0) red[0] = t;
   }
   __syncthreads();
   const float r = rsqrtf(red[0] / (float)H + eps);
   Tout *o = out + (int64_t)m * H;
   Tout *o2 = out2 ? out2 + (int64_t)m * H : nullptr;
-  for (int c = threadIdx.x; c < H; c += blockDim.x) {
-    const Tout y = from_f32<Tout>(to_f32(row[c]) * r * to_f32(g[c]));
+#pragma unroll
+  for (int k = 0; k < MAXV; ++k) {
+    const int c = threadIdx.x + k * blockDim.x;
+    if (c >= H) continue;
+    const Tout y = from_f32<Tout>(v[k] * r * to_f32(g[c]));
     o[c] = y;
     if (o2) o2[c] = y;
   }
@@ -85,7 +94,8 @@ __global__ void rmsnorm_kernel(const Tin *__restrict__ x, const Tout *__restrict
 cudaError_t launch_rmsnorm(int in_f32, int store, const void *x, const void *gain, int M, int H,
                            float eps, void *out, void *out2, cudaStream_t s) {
   if (M <= 0) return cudaSuccess;
-  const int thr = 256;
+  const int thr = H <= 8192 ? 256 : 1024;   // rows up to 32 values per thread
+  if (H > 32 * thr) return cudaErrorInvalidValue;
   if (store == ST_F32) {
     if (in_f32)
       rmsnorm_kernel<float, float><<<M, thr, 0, s>>>((const float *)x, (const float *)gain, H, eps,
