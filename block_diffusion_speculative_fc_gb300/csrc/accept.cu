@@ -19,6 +19,8 @@ __global__ void __launch_bounds__(128) accept_kernel(
     int B, int S, int vocab, const int *__restrict__ draft, const int *__restrict__ post,
     int *seq_len, int *accept_len, int *commit_len, int *bonus, int *out_tokens,
     int *output_ids, int out_stride, unsigned int *err) {
+  pdl_trigger();
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (b >= B) return;
@@ -60,10 +62,9 @@ cudaError_t launch_accept(int B, int S, int vocab, const int *draft, const int *
                           int *output_ids, int out_stride, unsigned int *err, cudaStream_t s) {
   if (B <= 0) return cudaSuccess;
   const int warps = 4;
-  accept_kernel<<<(B + warps - 1) / warps, warps * 32, 0, s>>>(
-      B, S, vocab, draft, post, seq_len, accept_len, commit_len, bonus, out_tokens, output_ids,
-      out_stride, err);
-  return cudaGetLastError();
+  return launch_pdl(accept_kernel, dim3((B + warps - 1) / warps), dim3(warps * 32), 0, s, B, S,
+                    vocab, draft, post, seq_len, accept_len, commit_len, bonus, out_tokens,
+                    output_ids, out_stride, err);
 }
 
 }  // namespace dflash

@@ -116,6 +116,8 @@ __device__ __forceinline__ uint32_t swz(uint32_t base, int row, int c) {
 __global__ void attn_prep_kernel(const int *__restrict__ kv_len, int B, int kvh, int cap,
                                  int window, int target_items, int max_items, int *item_start,
                                  int *pps_out, unsigned int *err) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ int s_total;
   if (threadIdx.x == 0) s_total = 0;
   __syncthreads();
@@ -165,6 +167,8 @@ __global__ void attn_prep_kernel(const int *__restrict__ kv_len, int B, int kvh,
 
 // ---------------------------------------------------------------- main kernel
 __global__ void __launch_bounds__(256) attn_mma_kernel(const __grid_constant__ Params p) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t *full = (uint64_t *)(smem + STAGES * STAGE_BYTES);
@@ -506,10 +510,9 @@ cudaError_t launch_attention_mma(const AttnParams &a, const AttnScratch &w, cuda
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (sms <= 0) sms = 1;
   const int max_items = (int)attention_mma_scratch_items(a.B, a.n_kv_heads);
-  att::attn_prep_kernel<<<1, 256, 0, s>>>(a.kv_len, a.B, a.n_kv_heads, a.pages_per_req * att::KT,
-                                           a.window, 2 * sms, max_items, w.item_start, w.pps,
-                                           a.err);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(att::attn_prep_kernel, dim3(1), dim3(256), 0, s, a.kv_len, a.B,
+                             a.n_kv_heads, a.pages_per_req * att::KT, a.window, 2 * sms,
+                             max_items, w.item_start, w.pps, a.err);
   if (e != cudaSuccess) return e;
   p.q = (const bf16 *)a.q;
   p.out = (bf16 *)a.out;
@@ -531,8 +534,7 @@ cudaError_t launch_attention_mma(const AttnParams &a, const AttnScratch &w, cuda
   p.R = R;
   p.max_items = max_items;
   p.scale_log2 = 1.4426950408889634f * a.scale;
-  att::attn_mma_kernel<<<2 * sms, warps * 32, att::SMEM, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(att::attn_mma_kernel, dim3(2 * sms), dim3(warps * 32), att::SMEM, s, p);
 }
 
 }  // namespace dflash

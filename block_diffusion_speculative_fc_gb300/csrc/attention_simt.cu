@@ -26,6 +26,8 @@ size_t attention_simt_smem(int R, int D) {
 
 template <typename T>
 __global__ void __launch_bounds__(THREADS) attn_simt_kernel(const __grid_constant__ AttnParams p) {
+  pdl_trigger();
+  pdl_wait();
   const int b = blockIdx.x / p.n_kv_heads, g = blockIdx.x % p.n_kv_heads;
   const int G = p.n_heads / p.n_kv_heads, S = p.S, R = G * S, D = p.head_dim;
   const int kvd = p.n_kv_heads * D;
@@ -133,8 +135,7 @@ cudaError_t launch_attention_simt(int store, const AttnParams &p, cudaStream_t s
   const int R = (p.n_heads / p.n_kv_heads) * p.S;
   const size_t smem = attention_simt_smem(R, p.head_dim);
   if (store != ST_F32) return cudaErrorInvalidValue;   // bf16 runs on the tensor cores
-  attn_simt_kernel<float><<<p.B * p.n_kv_heads, THREADS, smem, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(attn_simt_kernel<float>, dim3(p.B * p.n_kv_heads), dim3(THREADS), smem, s, p);
 }
 
 cudaError_t prepare_attention_simt() {

@@ -4,6 +4,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/dflash.h"
 
 namespace dflash {
@@ -47,5 +49,32 @@ __device__ __forceinline__ int argmax_key_index(unsigned long long k) {
 }
 
 __device__ __forceinline__ float silu(float x) { return x / (1.0f + expf(-x)); }
+
+// Programmatic dependent launch: every kernel of the library lets the next
+// kernel of the stream be scheduled as soon as all of its own CTAs have
+// started (trigger), and waits for its predecessor to finish and flush memory
+// only right before it reads what the predecessor wrote (wait).  Work that
+// does not depend on the predecessor -- above all streaming GEMM weights into
+// shared memory -- overlaps the predecessor's tail.
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 }  // namespace dflash

@@ -24,6 +24,8 @@ __device__ __forceinline__ int seg_tiles(const GemmSeg &s, bool pair) {
 
 template <typename T, bool PAIR>
 __global__ void __launch_bounds__(THREADS) gemm_simt_kernel(const __grid_constant__ GemmProblem P) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float smem[(PAIR ? 2 : 1) * BN * WLD + BM * WLD];
   float *Ws = smem;                              // [PAIR?2:1][BN][WLD]
   float *As = smem + (PAIR ? 2 : 1) * BN * WLD;  // [BM][WLD]
@@ -112,9 +114,8 @@ cudaError_t launch_gemm_simt(int store, const GemmProblem &P, cudaStream_t s) {
   }
   dim3 grid(tiles, (P.M + BM - 1) / BM);
   if (store != ST_F32) return cudaErrorInvalidValue;   // bf16 runs on the tensor cores
-  if (pair) gemm_simt_kernel<float, true><<<grid, THREADS, 0, s>>>(P);
-  else gemm_simt_kernel<float, false><<<grid, THREADS, 0, s>>>(P);
-  return cudaGetLastError();
+  if (pair) return launch_pdl(gemm_simt_kernel<float, true>, grid, dim3(THREADS), 0, s, P);
+  return launch_pdl(gemm_simt_kernel<float, false>, grid, dim3(THREADS), 0, s, P);
 }
 
 }  // namespace dflash

@@ -224,6 +224,7 @@ struct Cfg {
 template <int BN, bool PAIR, typename T>
 __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_constant__ Params p) {
   using C = Cfg<BN, PAIR>;
+  pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t *stages = smem;
@@ -275,30 +276,49 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first(), pol_a = policy_evict_last();
-      int it = 0;
-      bool ok = true;
-      for (long long i = R.b; i < R.e && ok;) {
-        const int tile = (int)(i / p.KB);
-        const int kb0 = (int)(i % p.KB);
-        const int kb1 = (int)(kb0 + (R.e - i) < p.KB ? kb0 + (R.e - i) : p.KB);
-        int seg, n0, m0;
+      long long cur = R.b;
+      int seg = 0, n0 = 0, m0 = 0, k = 0;
+      auto next = [&]() -> bool {
+        if (cur >= R.e) return false;
+        const int tile = (int)(cur / p.KB);
+        k = (int)(cur % p.KB) * BK;
         locate(tile, seg, n0, m0);
-        for (int kb = kb0; kb < kb1; ++kb, ++it) {
-          const int s = it % C::STAGES;
-          const uint32_t ph = (it / C::STAGES) & 1;
-          if (!mbar_wait(&empty[s], ph ^ 1)) {
-            ok = false;
-            break;
-          }
-          uint8_t *st = stages + s * C::STAGE_BYTES;
-          mbar_expect_tx(&full[s], C::STAGE_BYTES);
-          const int k = kb * BK;
-          tma_load_2d(st, &p.tmW[seg], &full[s], k, n0, pol_w);
-          if (PAIR) tma_load_2d(st + C::W_BYTES, &p.tmW[seg], &full[s], k, p.seg_half[seg] + n0, pol_w);
-          const int src = k / p.k_per_src;
-          tma_load_2d(st + C::P * C::W_BYTES, &p.tmA[src], &full[s], k - src * p.k_per_src, m0, pol_a);
+        ++cur;
+        return true;
+      };
+      auto load_w = [&](int s) {
+        uint8_t *st = stages + s * C::STAGE_BYTES;
+        mbar_expect_tx(&full[s], C::STAGE_BYTES);
+        tma_load_2d(st, &p.tmW[seg], &full[s], k, n0, pol_w);
+        if (PAIR) tma_load_2d(st + C::W_BYTES, &p.tmW[seg], &full[s], k, p.seg_half[seg] + n0, pol_w);
+      };
+      auto load_a = [&](int s, int kk, int mm) {
+        const int src = kk / p.k_per_src;
+        tma_load_2d(stages + s * C::STAGE_BYTES + C::P * C::W_BYTES, &p.tmA[src], &full[s],
+                    kk - src * p.k_per_src, mm, pol_a);
+      };
+      // Weights do not depend on the previous kernel: fill the whole ring with
+      // them first, then wait for the predecessor and add the activations.
+      int it = 0;
+      int pend_k[C::STAGES], pend_m[C::STAGES];
+      while (it < C::STAGES && next()) {
+        load_w(it);
+        pend_k[it] = k;
+        pend_m[it] = m0;
+        ++it;
+      }
+      pdl_wait();
+      for (int j = 0; j < it; ++j) load_a(j, pend_k[j], pend_m[j]);
+      bool ok = true;
+      while (next()) {
+        const int s = it % C::STAGES;
+        if (!mbar_wait(&empty[s], ((it / C::STAGES) & 1) ^ 1)) {
+          ok = false;
+          break;
         }
-        i += kb1 - kb0;
+        load_w(s);
+        load_a(s, k, m0);
+        ++it;
       }
       if (!ok) raise_error(p.err, DFLASH_DERR_TIMEOUT);
       // drain: no TMA write may still be in flight when the CTA winds down
@@ -351,6 +371,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
     }
   } else {
     // ------------------------------------------------------------ epilogue
+    pdl_wait();                                      // reads the predecessor's outputs
     const int ew = warp - EPI_WARP0;                 // 0..3
     const int tid = ew * 32 + lane;                  // 0..127
     const int quarter = warp & 3;                    // TMEM lane quarter this warp may access
@@ -524,9 +545,7 @@ template <int BN, bool PAIR>
 cudaError_t launch_cfg(tc::Params &p, int G, cudaStream_t s) {
   using C = tc::Cfg<BN, PAIR>;
   auto kern = tc::gemm_tc_kernel<BN, PAIR, bf16>;
-  tc::gemm_tc_kernel<BN, PAIR, bf16><<<G, tc::THREADS, C::SMEM, s>>>(p);
-  (void)kern;
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(G), dim3(tc::THREADS), C::SMEM, s, p);
 }
 
 template <int BN, bool PAIR>

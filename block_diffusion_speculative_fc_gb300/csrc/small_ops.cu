@@ -16,6 +16,8 @@ __global__ void embed_kernel(const T *__restrict__ embed, const int *__restrict_
                              const int *__restrict__ kv_len, int S, int H, int vocab, int mask_id,
                              int max_position, float *__restrict__ x, int *__restrict__ row_pos,
                              unsigned long long *__restrict__ keys, unsigned int *err) {
+  pdl_trigger();
+  pdl_wait();
   const int m = blockIdx.x;
   const int b = m / S, j = m % S;
   int id = j == 0 ? anchor[b] : mask_id;
@@ -40,12 +42,10 @@ cudaError_t launch_embed(int store, const void *embed, const int *anchor, const 
   const int M = B * S;
   if (M <= 0) return cudaSuccess;
   if (store == ST_F32)
-    embed_kernel<float><<<M, 256, 0, s>>>((const float *)embed, anchor, kv_len, S, H, vocab,
-                                          mask_id, max_position, x, row_pos, keys, err);
-  else
-    embed_kernel<bf16><<<M, 256, 0, s>>>((const bf16 *)embed, anchor, kv_len, S, H, vocab, mask_id,
-                                         max_position, x, row_pos, keys, err);
-  return cudaGetLastError();
+    return launch_pdl(embed_kernel<float>, dim3(M), dim3(256), 0, s, (const float *)embed, anchor,
+                      kv_len, S, H, vocab, mask_id, max_position, x, row_pos, keys, err);
+  return launch_pdl(embed_kernel<bf16>, dim3(M), dim3(256), 0, s, (const bf16 *)embed, anchor,
+                    kv_len, S, H, vocab, mask_id, max_position, x, row_pos, keys, err);
 }
 
 // ---------------------------------------------------------------------------
@@ -58,6 +58,8 @@ __global__ void rmsnorm_kernel(const Tin *__restrict__ x, const Tout *__restrict
   // one CTA per row; each thread keeps up to 32 values in registers so the
   // row is read once with all loads in flight
   constexpr int MAXV = 32;
+  pdl_trigger();
+  pdl_wait();
   const int m = blockIdx.x;
   const Tin *row = x + (int64_t)m * H;
   float v[MAXV];
@@ -96,21 +98,12 @@ cudaError_t launch_rmsnorm(int in_f32, int store, const void *x, const void *gai
   if (M <= 0) return cudaSuccess;
   const int thr = H <= 8192 ? 256 : 1024;   // rows up to 32 values per thread
   if (H > 32 * thr) return cudaErrorInvalidValue;
-  if (store == ST_F32) {
-    if (in_f32)
-      rmsnorm_kernel<float, float><<<M, thr, 0, s>>>((const float *)x, (const float *)gain, H, eps,
-                                                     (float *)out, (float *)out2);
-    else
-      return cudaErrorInvalidValue;
-  } else {
-    if (in_f32)
-      rmsnorm_kernel<float, bf16><<<M, thr, 0, s>>>((const float *)x, (const bf16 *)gain, H, eps,
-                                                    (bf16 *)out, (bf16 *)out2);
-    else
-      rmsnorm_kernel<bf16, bf16><<<M, thr, 0, s>>>((const bf16 *)x, (const bf16 *)gain, H, eps,
-                                                   (bf16 *)out, (bf16 *)out2);
-  }
-  return cudaGetLastError();
+  if (!in_f32) return cudaErrorInvalidValue;
+  if (store == ST_F32)
+    return launch_pdl(rmsnorm_kernel<float, float>, dim3(M), dim3(thr), 0, s, (const float *)x,
+                      (const float *)gain, H, eps, (float *)out, (float *)out2);
+  return launch_pdl(rmsnorm_kernel<float, bf16>, dim3(M), dim3(thr), 0, s, (const float *)x,
+                    (const bf16 *)gain, H, eps, (bf16 *)out, (bf16 *)out2);
 }
 
 // ---------------------------------------------------------------------------
@@ -119,6 +112,8 @@ cudaError_t launch_rmsnorm(int in_f32, int store, const void *x, const void *gai
 __global__ void argmax_finalize_kernel(const unsigned long long *__restrict__ keys,
                                        const int *__restrict__ anchor, int M, int S,
                                        int *__restrict__ draft_ids) {
+  pdl_trigger();
+  pdl_wait();
   const int m = blockIdx.x * blockDim.x + threadIdx.x;
   if (m >= M) return;
   const int j = m % S;
@@ -129,8 +124,8 @@ cudaError_t launch_argmax_finalize(const unsigned long long *keys, const int *an
                                    int *draft_ids, cudaStream_t s) {
   const int M = B * S;
   if (M <= 0) return cudaSuccess;
-  argmax_finalize_kernel<<<(M + 127) / 128, 128, 0, s>>>(keys, anchor, M, S, draft_ids);
-  return cudaGetLastError();
+  return launch_pdl(argmax_finalize_kernel, dim3((M + 127) / 128), dim3(128), 0, s, keys, anchor, M,
+                    S, draft_ids);
 }
 
 // ---------------------------------------------------------------------------
@@ -147,6 +142,8 @@ __global__ void inject_prep_kernel(int B, int row0, int rows, const int *__restr
                                    int n_pages, int page_size, int max_position,
                                    int *__restrict__ row_slot, int *__restrict__ row_pos,
                                    unsigned int *err) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ int sm[];
   int *s_off = sm, *s_n = sm + B, *s_len = sm + 2 * B;
   for (int b = threadIdx.x; b < B; b += blockDim.x) {
@@ -187,10 +184,9 @@ cudaError_t launch_inject_prep(int B, int row0, int rows, const int *row_offset,
                                int *row_pos, unsigned int *err, cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
   const int thr = 256;
-  inject_prep_kernel<<<(rows + thr - 1) / thr, thr, 3 * B * sizeof(int), s>>>(
-      B, row0, rows, row_offset, n_rows, kv_len, page_table, pages_per_req, n_pages, page_size,
-      max_position, row_slot, row_pos, err);
-  return cudaGetLastError();
+  return launch_pdl(inject_prep_kernel, dim3((rows + thr - 1) / thr), dim3(thr),
+                    3 * B * sizeof(int), s, B, row0, rows, row_offset, n_rows, kv_len, page_table,
+                    pages_per_req, n_pages, page_size, max_position, row_slot, row_pos, err);
 }
 
 // kv_len[b] += n_rows[b].  A request whose rows do not lie inside the feature
@@ -199,6 +195,8 @@ cudaError_t launch_inject_prep(int B, int row0, int rows, const int *row_offset,
 __global__ void inject_finalize_kernel(int B, int total_rows, const int *__restrict__ row_offset,
                                        const int *__restrict__ n_rows, int *kv_len, int capacity,
                                        unsigned int *err) {
+  pdl_trigger();
+  pdl_wait();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= B) return;
   const int n = n_rows[b], off = row_offset[b];
@@ -217,9 +215,8 @@ __global__ void inject_finalize_kernel(int B, int total_rows, const int *__restr
 cudaError_t launch_inject_finalize(int B, int total_rows, const int *row_offset, const int *n_rows,
                                    int *kv_len, int capacity, unsigned int *err, cudaStream_t s) {
   if (B <= 0) return cudaSuccess;
-  inject_finalize_kernel<<<(B + 127) / 128, 128, 0, s>>>(B, total_rows, row_offset, n_rows, kv_len,
-                                                         capacity, err);
-  return cudaGetLastError();
+  return launch_pdl(inject_finalize_kernel, dim3((B + 127) / 128), dim3(128), 0, s, B, total_rows,
+                    row_offset, n_rows, kv_len, capacity, err);
 }
 
 // ---------------------------------------------------------------------------
