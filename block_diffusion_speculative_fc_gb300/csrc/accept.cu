@@ -19,7 +19,6 @@ __global__ void __launch_bounds__(128) accept_kernel(
     int B, int S, int vocab, const int *__restrict__ draft, const int *__restrict__ post,
     int *seq_len, int *accept_len, int *commit_len, int *bonus, int *out_tokens,
     int *output_ids, int out_stride, unsigned int *err) {
-  pdl_trigger();
   pdl_wait();
   const int lane = threadIdx.x & 31;
   const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);

@@ -116,7 +116,6 @@ __device__ __forceinline__ uint32_t swz(uint32_t base, int row, int c) {
 __global__ void attn_prep_kernel(const int *__restrict__ kv_len, int B, int kvh, int cap,
                                  int window, int target_items, int max_items, int *item_start,
                                  int *pps_out, unsigned int *err) {
-  pdl_trigger();
   pdl_wait();
   __shared__ int s_total;
   if (threadIdx.x == 0) s_total = 0;
@@ -167,7 +166,6 @@ __global__ void attn_prep_kernel(const int *__restrict__ kv_len, int B, int kvh,
 
 // ---------------------------------------------------------------- main kernel
 __global__ void __launch_bounds__(256) attn_mma_kernel(const __grid_constant__ Params p) {
-  pdl_trigger();
   pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -447,6 +445,7 @@ __global__ void __launch_bounds__(256) attn_mma_kernel(const __grid_constant__ P
     }
     __syncthreads();
   }
+  pdl_trigger();
   (void)nwarps;
 }
 

@@ -26,7 +26,6 @@ size_t attention_simt_smem(int R, int D) {
 
 template <typename T>
 __global__ void __launch_bounds__(THREADS) attn_simt_kernel(const __grid_constant__ AttnParams p) {
-  pdl_trigger();
   pdl_wait();
   const int b = blockIdx.x / p.n_kv_heads, g = blockIdx.x % p.n_kv_heads;
   const int G = p.n_heads / p.n_kv_heads, S = p.S, R = G * S, D = p.head_dim;

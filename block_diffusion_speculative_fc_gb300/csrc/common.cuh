@@ -50,12 +50,14 @@ __device__ __forceinline__ int argmax_key_index(unsigned long long k) {
 
 __device__ __forceinline__ float silu(float x) { return x / (1.0f + expf(-x)); }
 
-// Programmatic dependent launch: every kernel of the library lets the next
-// kernel of the stream be scheduled as soon as all of its own CTAs have
-// started (trigger), and waits for its predecessor to finish and flush memory
-// only right before it reads what the predecessor wrote (wait).  Work that
-// does not depend on the predecessor -- above all streaming GEMM weights into
-// shared memory -- overlaps the predecessor's tail.
+// Programmatic dependent launch.  Every kernel is launched so that it may be
+// scheduled before its predecessor in the stream has exited.  A kernel waits
+// for its predecessor (griddepcontrol.wait) right before it first reads what
+// the predecessor wrote; only writes a CTA made before it signals its
+// dependents (griddepcontrol.launch_dependents) are covered by that wait, so
+// each kernel signals only after its last global write (or not at all, which
+// signals at exit).  Work that does not depend on the predecessor -- above
+// all the GEMM weight stream -- runs before the wait.
 __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }

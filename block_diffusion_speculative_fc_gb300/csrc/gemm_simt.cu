@@ -24,7 +24,6 @@ __device__ __forceinline__ int seg_tiles(const GemmSeg &s, bool pair) {
 
 template <typename T, bool PAIR>
 __global__ void __launch_bounds__(THREADS) gemm_simt_kernel(const __grid_constant__ GemmProblem P) {
-  pdl_trigger();
   pdl_wait();
   __shared__ float smem[(PAIR ? 2 : 1) * BN * WLD + BM * WLD];
   float *Ws = smem;                              // [PAIR?2:1][BN][WLD]

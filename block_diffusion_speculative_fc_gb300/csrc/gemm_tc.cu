@@ -224,7 +224,6 @@ struct Cfg {
 template <int BN, bool PAIR, typename T>
 __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_constant__ Params p) {
   using C = Cfg<BN, PAIR>;
-  pdl_trigger();
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t *stages = smem;
@@ -276,14 +275,21 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first(), pol_a = policy_evict_last();
-      long long cur = R.b;
+      // walk this CTA's (tile, k-block) range incrementally: one division up
+      // front, a tile lookup only when the tile changes
+      long long left = R.e - R.b;
+      int tile = (int)(R.b / p.KB), kb = (int)(R.b % p.KB) - 1;
       int seg = 0, n0 = 0, m0 = 0, k = 0;
+      locate(tile, seg, n0, m0);
       auto next = [&]() -> bool {
-        if (cur >= R.e) return false;
-        const int tile = (int)(cur / p.KB);
-        k = (int)(cur % p.KB) * BK;
-        locate(tile, seg, n0, m0);
-        ++cur;
+        if (left <= 0) return false;
+        --left;
+        if (++kb == p.KB) {
+          kb = 0;
+          ++tile;
+          locate(tile, seg, n0, m0);
+        }
+        k = kb * BK;
         return true;
       };
       auto load_w = [&](int s) {
@@ -496,6 +502,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
   }
   tc_fence_before();
   __syncthreads();
+  pdl_trigger();   // every global write of this CTA is done
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);

@@ -16,7 +16,6 @@ __global__ void embed_kernel(const T *__restrict__ embed, const int *__restrict_
                              const int *__restrict__ kv_len, int S, int H, int vocab, int mask_id,
                              int max_position, float *__restrict__ x, int *__restrict__ row_pos,
                              unsigned long long *__restrict__ keys, unsigned int *err) {
-  pdl_trigger();
   pdl_wait();
   const int m = blockIdx.x;
   const int b = m / S, j = m % S;
@@ -58,7 +57,6 @@ __global__ void rmsnorm_kernel(const Tin *__restrict__ x, const Tout *__restrict
   // one CTA per row; each thread keeps up to 32 values in registers so the
   // row is read once with all loads in flight
   constexpr int MAXV = 32;
-  pdl_trigger();
   pdl_wait();
   const int m = blockIdx.x;
   const Tin *row = x + (int64_t)m * H;
@@ -91,6 +89,8 @@ __global__ void rmsnorm_kernel(const Tin *__restrict__ x, const Tout *__restrict
     o[c] = y;
     if (o2) o2[c] = y;
   }
+  __syncthreads();
+  pdl_trigger();
 }
 
 cudaError_t launch_rmsnorm(int in_f32, int store, const void *x, const void *gain, int M, int H,
@@ -112,7 +112,6 @@ cudaError_t launch_rmsnorm(int in_f32, int store, const void *x, const void *gai
 __global__ void argmax_finalize_kernel(const unsigned long long *__restrict__ keys,
                                        const int *__restrict__ anchor, int M, int S,
                                        int *__restrict__ draft_ids) {
-  pdl_trigger();
   pdl_wait();
   const int m = blockIdx.x * blockDim.x + threadIdx.x;
   if (m >= M) return;
@@ -142,7 +141,6 @@ __global__ void inject_prep_kernel(int B, int row0, int rows, const int *__restr
                                    int n_pages, int page_size, int max_position,
                                    int *__restrict__ row_slot, int *__restrict__ row_pos,
                                    unsigned int *err) {
-  pdl_trigger();
   pdl_wait();
   extern __shared__ int sm[];
   int *s_off = sm, *s_n = sm + B, *s_len = sm + 2 * B;
@@ -195,7 +193,6 @@ cudaError_t launch_inject_prep(int B, int row0, int rows, const int *row_offset,
 __global__ void inject_finalize_kernel(int B, int total_rows, const int *__restrict__ row_offset,
                                        const int *__restrict__ n_rows, int *kv_len, int capacity,
                                        unsigned int *err) {
-  pdl_trigger();
   pdl_wait();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= B) return;
