@@ -22,7 +22,7 @@ int fail(int st, const std::string &msg) {
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct Layout {
-  size_t err, rope, x, h, qb, kb, vb, attn, act, row_pos, keys, y, yh, slot, rpos;
+  size_t err, rope, x, h, xg, ssq, qb, kb, vb, attn, act, row_pos, keys, yg, ssq_y, slot, rpos;
   size_t tc_partials, tc_counters;
   int tc_max_tiles;
   size_t att_item_start, att_pps, att_part_o, att_part_ml, att_tickets;
@@ -71,6 +71,8 @@ Layout plan(const dflash_config &c, size_t es) {
   L.rope = take(sizeof(float) * 2 * (size_t)c.max_position * (D / 2));
   L.x = take(4 * M * H);
   L.h = take(es * M * H);
+  L.xg = take(es * M * H);                       // x * g of the next RMSNorm (GEMM operand)
+  L.ssq = take(4 * (H / 128) * M);               // per-128-feature sums of squares of x
   L.qb = take(es * M * c.n_heads * D);
   L.kb = take(es * M * c.n_kv_heads * D);
   L.vb = take(es * M * c.n_kv_heads * D);
@@ -78,8 +80,8 @@ Layout plan(const dflash_config &c, size_t es) {
   L.act = take(es * M * c.intermediate);
   L.row_pos = take(4 * M);
   L.keys = take(8 * M);
-  L.y = take(4 * R * H);
-  L.yh = take(es * R * H);
+  L.yg = take(es * R * H);                       // fc output * hidden_norm gain
+  L.ssq_y = take(4 * (H / 128) * R);
   L.slot = take(4 * R);
   L.rpos = take(4 * R);
   if (es == 2) {
@@ -156,6 +158,16 @@ EpiParams epi_base(const dflash_handle *h, int op) {
   e.head_dim = h->cfg.head_dim;
   e.eps = h->cfg.rms_eps;
   return e;
+}
+
+// The GEMM's A operand is x * g of an RMSNorm whose row scale is applied in
+// the epilogue from the per-tile sums of squares `ssq` (row stride ld).
+void set_norm_in(const dflash_handle *h, EpiParams &e, const float *ssq, int ld) {
+  e.ssq_in = ssq;
+  e.ssq_parts = h->cfg.hidden / 128;
+  e.ssq_ld = ld;
+  e.norm_eps = h->cfg.rms_eps;
+  e.inv_h = 1.0f / (float)h->cfg.hidden;
 }
 
 GemmProblem problem_1src(const void *A, int64_t lda, int M, int K) {
@@ -387,8 +399,8 @@ int dflash_inject_context(dflash_handle *h, const dflash_kv *kv, int32_t batch, 
   const int kvd = c.n_kv_heads * D;
   const int q_rows = c.n_heads * D;
   int *slot = at<int>(h, h->L.slot), *rpos = at<int>(h, h->L.rpos);
-  float *y = at<float>(h, h->L.y);
-  void *yh = h->ws + h->L.yh;
+  void *yg = h->ws + h->L.yg;
+  float *ssq_y = at<float>(h, h->L.ssq_y);
   const float2 *rope = at<const float2>(h, h->L.rope);
 
   for (int64_t r0 = 0; r0 < total_rows; r0 += c.max_rows) {
@@ -399,7 +411,8 @@ int dflash_inject_context(dflash_handle *h, const dflash_kv *kv, int32_t batch, 
                                 c.max_position, slot, rpos, err, s);
     });
     if (st) return st;
-    // a1: concat (K-split over the selected layers) + fc
+    // a1 + a2: concat (K-split over the selected layers) + fc; the epilogue
+    // writes y * hidden_norm gain and the row sums of squares of y
     GemmProblem P;
     std::memset(&P, 0, sizeof(P));
     for (int j = 0; j < c.n_sel; ++j)
@@ -409,20 +422,18 @@ int dflash_inject_context(dflash_handle *h, const dflash_kv *kv, int32_t batch, 
     P.A.n_src = c.n_sel;
     P.M = rows;
     P.K = c.n_sel * c.target_hidden;
-    EpiParams e = epi_base(h, EPI_STORE_F32);
+    EpiParams e = epi_base(h, EPI_STORE_NORM);
     e.N = H;
     e.ld = H;
-    e.out_f32 = y;
+    e.out_act = yg;
+    e.norm_gain = h->hidden_norm_g;
+    e.ssq_out = ssq_y;
+    e.ssq_ld = c.max_rows;
     add_seg(P, h->fc_w, P.K, H, e);
     if ((st = timed(h, "gemm_fc", s, [&] { return run_gemm(h, P, s); }))) return st;
-    // a2: hidden_norm
-    if ((st = timed(h, "rmsnorm_hidden", s, [&] {
-           return launch_rmsnorm(1, h->store, y, h->hidden_norm_g, rows, H, c.rms_eps, yh, nullptr, s);
-         })))
-      return st;
-    // a3: every layer's K/V projection + k-norm + RoPE + paged scatter
+    // a3: every layer's K/V projection of hidden_norm(y) + k-norm + RoPE + paged scatter
     for (int l0 = 0; l0 < c.n_layers; l0 += kMaxSeg) {
-      GemmProblem Q = problem_1src(yh, H, rows, H);
+      GemmProblem Q = problem_1src(yg, H, rows, H);
       for (int l = l0; l < std::min(c.n_layers, l0 + kMaxSeg); ++l) {
         EpiParams k = epi_base(h, EPI_KV_CACHE);
         k.N = 2 * kvd;
@@ -432,6 +443,7 @@ int dflash_inject_context(dflash_handle *h, const dflash_kv *kv, int32_t batch, 
         k.row_pos = rpos;
         k.row_slot = slot;
         k.rope = rope;
+        set_norm_in(h, k, ssq_y, c.max_rows);
         add_seg(Q, (const char *)h->qkv_w[l] + (size_t)q_rows * H * h->es, H, 2 * kvd, k);
       }
       if ((st = timed(h, "gemm_kv_inject", s, [&] { return run_gemm(h, Q, s); }))) return st;
@@ -457,8 +469,10 @@ int dflash_draft_block(dflash_handle *h, const dflash_kv *kv, int32_t batch, con
   unsigned int *err = at<unsigned int>(h, h->L.err);
   const int S = c.block_size, M = batch * S, H = c.hidden, D = c.head_dim;
   const int qd = c.n_heads * D, kvd = c.n_kv_heads * D;
+  const int ldq = c.max_batch * S;                 // row stride of the sums of squares
   float *x = at<float>(h, h->L.x);
-  void *hb = h->ws + h->L.h;
+  void *xg = h->ws + h->L.xg;
+  float *ssq = at<float>(h, h->L.ssq);
   void *qb = h->ws + h->L.qb, *kb = h->ws + h->L.kb, *vb = h->ws + h->L.vb;
   void *attn = h->ws + h->L.attn, *act = h->ws + h->L.act;
   int *row_pos = at<int>(h, h->L.row_pos);
@@ -466,19 +480,17 @@ int dflash_draft_block(dflash_handle *h, const dflash_kv *kv, int32_t batch, con
   const float2 *rope = at<const float2>(h, h->L.rope);
   int st;
 
-  // a4: block embedding [anchor, MASK x (S-1)] at positions kv_len + j
+  // a4: block embedding [anchor, MASK x (S-1)] at positions kv_len + j, with the
+  // first layer's input RMSNorm deferred into its QKV GEMM
   if ((st = timed(h, "embed", s, [&] {
          return launch_embed(h->store, h->embed, anchor, kv->kv_len, batch, S, H, c.vocab,
-                             c.mask_token_id, c.max_position, x, row_pos, keys, err, s);
+                             c.mask_token_id, c.max_position, x, h->in_norm_g[0], xg, ssq, ldq,
+                             row_pos, keys, err, s);
        })))
     return st;
   for (int l = 0; l < c.n_layers; ++l) {
     // a5: RMSNorm + QKV GEMM + q/k-norm + RoPE
-    if ((st = timed(h, "rmsnorm", s, [&] {
-           return launch_rmsnorm(1, h->store, x, h->in_norm_g[l], M, H, c.rms_eps, hb, nullptr, s);
-         })))
-      return st;
-    GemmProblem P = problem_1src(hb, H, M, H);
+    GemmProblem P = problem_1src(xg, H, M, H);
     EpiParams e = epi_base(h, EPI_QKV);
     e.N = qd + 2 * kvd;
     e.q_out = qb;
@@ -488,6 +500,7 @@ int dflash_draft_block(dflash_handle *h, const dflash_kv *kv, int32_t batch, con
     e.k_gain = h->k_norm_g[l];
     e.row_pos = row_pos;
     e.rope = rope;
+    set_norm_in(h, e, ssq, ldq);
     add_seg(P, h->qkv_w[l], H, qd + 2 * kvd, e);
     if ((st = timed(h, "gemm_qkv", s, [&] { return run_gemm(h, P, s); }))) return st;
     // a6: non-causal block attention over [context ; block]
@@ -513,40 +526,50 @@ int dflash_draft_block(dflash_handle *h, const dflash_kv *kv, int32_t batch, con
     a.scale = 1.0f / sqrtf((float)D);
     a.err = err;
     if ((st = timed(h, "attention", s, [&] { return run_attention(h, a, s); }))) return st;
-    // a7: O projection + residual
+    // a7: O projection + residual (+ deferred post-attention RMSNorm)
     GemmProblem O = problem_1src(attn, qd, M, qd);
-    EpiParams eo = epi_base(h, EPI_RESID);
+    EpiParams eo = epi_base(h, EPI_RESID_NORM);
     eo.N = H;
     eo.ld = H;
     eo.out_f32 = x;
+    eo.out_act = xg;
+    eo.norm_gain = h->post_norm_g[l];
+    eo.ssq_out = ssq;
+    eo.ssq_ld = ldq;
     add_seg(O, h->o_w[l], qd, H, eo);
     if ((st = timed(h, "gemm_o", s, [&] { return run_gemm(h, O, s); }))) return st;
     // a8: RMSNorm + gate/up GEMM with SwiGLU + down GEMM + residual
-    if ((st = timed(h, "rmsnorm", s, [&] {
-           return launch_rmsnorm(1, h->store, x, h->post_norm_g[l], M, H, c.rms_eps, hb, nullptr, s);
-         })))
-      return st;
-    GemmProblem G = problem_1src(hb, H, M, H);
+    GemmProblem G = problem_1src(xg, H, M, H);
     EpiParams eg = epi_base(h, EPI_SWIGLU);
     eg.N = 2 * c.intermediate;
     eg.ld = c.intermediate;
     eg.out_act = act;
+    set_norm_in(h, eg, ssq, ldq);
     add_seg(G, h->gate_up_w[l], H, 2 * c.intermediate, eg);
     if ((st = timed(h, "gemm_gate_up", s, [&] { return run_gemm(h, G, s); }))) return st;
     GemmProblem Dn = problem_1src(act, c.intermediate, M, c.intermediate);
-    EpiParams ed = epi_base(h, EPI_RESID);
+    EpiParams ed = epi_base(h, EPI_RESID_NORM);
     ed.N = H;
     ed.ld = H;
     ed.out_f32 = x;
+    ed.out_act = xg;
+    ed.norm_gain = l + 1 < c.n_layers ? h->in_norm_g[l + 1] : h->final_norm_g;
+    ed.ssq_out = ssq;
+    ed.ssq_ld = ldq;
     add_seg(Dn, h->down_w[l], c.intermediate, H, ed);
     if ((st = timed(h, "gemm_down", s, [&] { return run_gemm(h, Dn, s); }))) return st;
   }
-  // a9: final norm + lm_head + argmax (logits never stored)
-  if ((st = timed(h, "rmsnorm", s, [&] {
-         return launch_rmsnorm(1, h->store, x, h->final_norm_g, M, H, c.rms_eps, hb, hidden_out, s);
+  // a9: final norm + lm_head + argmax (logits never stored).  The argmax of a
+  // row is unchanged by the row's positive RMSNorm scale, so the lm_head runs
+  // on x * final gain directly; the normalised hidden states are only formed
+  // when the caller asks for them.
+  if (hidden_out &&
+      (st = timed(h, "rmsnorm_hidden_out", s, [&] {
+         return launch_rmsnorm(1, h->store, x, h->final_norm_g, M, H, c.rms_eps, hidden_out,
+                               nullptr, s);
        })))
     return st;
-  GemmProblem P = problem_1src(hb, H, M, H);
+  GemmProblem P = problem_1src(xg, H, M, H);
   EpiParams e = epi_base(h, EPI_ARGMAX);
   e.N = c.vocab;
   e.argmax_keys = keys;

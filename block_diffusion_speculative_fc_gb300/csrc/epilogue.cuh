@@ -122,54 +122,112 @@ __device__ void head_ops(const EpiParams &e, const float *t0, int ldt, int m0, i
 // t0: fp32 tile [rows][ldt] (features n0 .. n0+127); t1: the "up" tile of a
 // SwiGLU pair.  All `nthreads` threads of the caller take part (a multiple of
 // 128); the caller synchronises before (tile complete) and after (tile reuse).
-// s_int: shared scratch of at least 2 * kEpiMaxRows ints; sync(): barrier over
-// the participating threads.
+// The tiles may be modified in place.  s_int: shared scratch of at least
+// kEpiScratchInts ints; sync(): barrier over the participating threads.
+constexpr int kEpiScratchInts = 3 * kEpiMaxRows;
+
 template <typename T, class Sync>
-__device__ void run_epilogue(const EpiParams &e, const float *t0, const float *t1, int ldt, int m0,
-                             int rows, int n0, int tid, int nthreads, int *s_int, Sync sync) {
+__device__ void run_epilogue(const EpiParams &e, float *t0, float *t1, int ldt, int m0, int rows,
+                             int n0, int tid, int nthreads, int *s_int, Sync sync) {
   const int lane = tid & 31, warp = tid >> 5, nwarps = nthreads >> 5;
+  if (e.ssq_in) {
+    // deferred RMSNorm of the A operand: scale every row by its rstd first
+    float *s_rstd = reinterpret_cast<float *>(s_int + 2 * kEpiMaxRows);
+    constexpr int RPW = kEpiMaxRows / 4;   // rows per warp with >= 4 warps
+    float acc[RPW];
+#pragma unroll
+    for (int k = 0; k < RPW; ++k) {
+      const int r = warp + k * nwarps;
+      acc[k] = 0.f;
+      if (r < rows)
+        for (int q = lane; q < e.ssq_parts; q += 32) acc[k] += e.ssq_in[(int64_t)q * e.ssq_ld + m0 + r];
+    }
+#pragma unroll
+    for (int k = 0; k < RPW; ++k) {
+      const int r = warp + k * nwarps;
+      const float t = warp_sum(acc[k]);
+      if (lane == 0 && r < rows) s_rstd[r] = rsqrtf(t * e.inv_h + e.norm_eps);
+    }
+    sync();
+    for (int idx = tid; idx < rows * 128; idx += nthreads) {
+      const int r = idx >> 7, c = idx & 127;
+      t0[r * ldt + c] *= s_rstd[r];
+      if (t1) t1[r * ldt + c] *= s_rstd[r];
+    }
+    sync();
+  }
   switch (e.op) {
     case EPI_STORE_F32:
     case EPI_RESID:
     case EPI_STORE_ACT:
-    case EPI_SWIGLU: {
+    case EPI_SWIGLU:
+    case EPI_RESID_NORM:
+    case EPI_STORE_NORM: {
       const int nvalid = e.op == EPI_SWIGLU ? e.N / 2 : e.N;
       const int c = tid & 127, rg = tid >> 7, ng = nthreads >> 7;
       const int n = n0 + c;
-      if (n >= nvalid) break;
+      const bool norm_out = e.op == EPI_RESID_NORM || e.op == EPI_STORE_NORM;
+      const float g = (norm_out && n < nvalid) ? to_f32(((const T *)e.norm_gain)[n]) : 0.f;
       constexpr int BATCH = 16;
-      for (int rb = rg; rb < rows; rb += BATCH * ng) {
-        float y[BATCH];
-#pragma unroll
-        for (int k = 0; k < BATCH; ++k) {
-          const int r = rb + k * ng;
-          y[k] = r < rows ? t0[r * ldt + c] : 0.f;
-        }
-        if (e.op == EPI_RESID) {
-          float old[BATCH];
+      if (n < nvalid) {
+        for (int rb = rg; rb < rows; rb += BATCH * ng) {
+          float y[BATCH];
 #pragma unroll
           for (int k = 0; k < BATCH; ++k) {
             const int r = rb + k * ng;
-            old[k] = r < rows ? e.out_f32[(int64_t)(m0 + r) * e.ld + n] : 0.f;
+            y[k] = r < rows ? t0[r * ldt + c] : 0.f;
           }
+          if (e.op == EPI_RESID || e.op == EPI_RESID_NORM) {
+            float old[BATCH];
 #pragma unroll
-          for (int k = 0; k < BATCH; ++k) {
-            const int r = rb + k * ng;
-            if (r < rows) e.out_f32[(int64_t)(m0 + r) * e.ld + n] = old[k] + y[k];
+            for (int k = 0; k < BATCH; ++k) {
+              const int r = rb + k * ng;
+              old[k] = r < rows ? e.out_f32[(int64_t)(m0 + r) * e.ld + n] : 0.f;
+            }
+#pragma unroll
+            for (int k = 0; k < BATCH; ++k) y[k] += old[k];
           }
-        } else {
 #pragma unroll
           for (int k = 0; k < BATCH; ++k) {
             const int r = rb + k * ng;
             if (r >= rows) continue;
             const int64_t o = (int64_t)(m0 + r) * e.ld + n;
-            if (e.op == EPI_STORE_F32)
-              e.out_f32[o] = y[k];
-            else if (e.op == EPI_STORE_ACT)
-              ((T *)e.out_act)[o] = from_f32<T>(y[k]);
-            else
-              ((T *)e.out_act)[o] = from_f32<T>(silu(y[k]) * t1[r * ldt + c]);
+            switch (e.op) {
+              case EPI_STORE_F32:
+              case EPI_RESID:
+                e.out_f32[o] = y[k];
+                break;
+              case EPI_STORE_ACT:
+                ((T *)e.out_act)[o] = from_f32<T>(y[k]);
+                break;
+              case EPI_SWIGLU:
+                ((T *)e.out_act)[o] = from_f32<T>(silu(y[k]) * t1[r * ldt + c]);
+                break;
+              case EPI_RESID_NORM:
+                e.out_f32[o] = y[k];
+                ((T *)e.out_act)[o] = from_f32<T>(y[k] * g);
+                t0[r * ldt + c] = y[k] * y[k];
+                break;
+              case EPI_STORE_NORM:
+                ((T *)e.out_act)[o] = from_f32<T>(y[k] * g);
+                t0[r * ldt + c] = y[k] * y[k];
+                break;
+            }
           }
+        }
+      }
+      if (norm_out) {
+        // per-row sum of squares of the 128 features of this tile
+        sync();
+        for (int r = warp; r < rows; r += nwarps) {
+          float v = 0.f;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int cc = lane + 32 * k;
+            v += (n0 + cc < nvalid) ? t0[r * ldt + cc] : 0.f;
+          }
+          v = warp_sum(v);
+          if (lane == 0) e.ssq_out[(int64_t)(n0 >> 7) * e.ssq_ld + m0 + r] = v;
         }
       }
       break;
@@ -196,7 +254,7 @@ __device__ void run_epilogue(const EpiParams &e, const float *t0, const float *t
     }
     case EPI_QKV:
     case EPI_KV_CACHE: {
-      int *s_pos = s_int, *s_slot = s_int + kEpiMaxRows;
+      int *s_pos = s_int, *s_slot = s_int + kEpiMaxRows;   // after s_rstd was consumed
       for (int r = tid; r < rows; r += nthreads) {
         s_pos[r] = e.row_pos[m0 + r];
         s_slot[r] = e.op == EPI_KV_CACHE ? e.row_slot[m0 + r] : 0;

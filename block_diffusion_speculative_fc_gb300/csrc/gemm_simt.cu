@@ -98,7 +98,7 @@ __global__ void __launch_bounds__(THREADS) gemm_simt_kernel(const __grid_constan
       for (int j = 0; j < 4; ++j) (p ? t1 : t0)[(tm * 4 + j) * TLD + tf + 32 * i] = acc[p][i][j];
   __syncthreads();
   const int rows = min(BM, P.M - m0);
-  __shared__ int s_int[2 * kEpiMaxRows];
+  __shared__ int s_int[kEpiScratchInts];
   run_epilogue<T>(seg.epi, t0, PAIR ? t1 : nullptr, TLD, m0, rows, n0, tid, THREADS, s_int,
                   [] { __syncthreads(); });
 }

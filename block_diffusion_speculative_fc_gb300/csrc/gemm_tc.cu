@@ -209,7 +209,7 @@ struct Cfg {
   static constexpr int STAGE_BYTES = P * W_BYTES + A_BYTES;
   static constexpr int CH = BN < 32 ? BN : 32;          // epilogue token chunk
   static constexpr int STAGING_BYTES = P * CH * 128 * 4;
-  static constexpr int BAR_BYTES = 512;   // mbarriers, TMEM slot, flag, epilogue row info
+  static constexpr int BAR_BYTES = 768;   // mbarriers, TMEM slot, flag, epilogue scratch
   static constexpr int BUDGET = 225 * 1024;
   static constexpr int STAGES_RAW = (BUDGET - 1024 - STAGING_BYTES - BAR_BYTES) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 12 ? 12 : STAGES_RAW;
@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
   uint64_t *mma_done = acc_empty + 2;
   uint32_t *tmem_slot = (uint32_t *)(mma_done + 1);
   int *flag = (int *)(tmem_slot + 1);
-  int *s_int = (int *)((uint8_t *)bars + 256);   // 2 * kEpiMaxRows ints
+  int *s_int = (int *)((uint8_t *)bars + 256);   // kEpiScratchInts ints
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x, cta = blockIdx.x;

@@ -17,7 +17,18 @@ enum EpiOp {
   EPI_QKV = 4,        // per-head RMSNorm (q, k) + RoPE -> q/k/v block buffers
   EPI_KV_CACHE = 5,   // k-norm + RoPE (k), plain v -> paged cache rows (slot)
   EPI_STORE_ACT = 6,  // out_act[m*ld + n] = y
+  EPI_RESID_NORM = 7, // x = out_f32 += y; out_act = x * norm_gain; ssq_out += x^2 per row
+  EPI_STORE_NORM = 8, // out_act = y * norm_gain; ssq_out = y^2 per row
 };
+
+// Deferred RMSNorm.  A producer of a tensor that feeds a normalised GEMM
+// (EPI_RESID_NORM / EPI_STORE_NORM, or the block embedding) writes
+//   out_act[m, n] = x[m, n] * g[n]                      (the GEMM's A operand)
+//   ssq[n / 128][m] = sum over its 128 features of x^2   (one slot per tile)
+// and the consuming GEMM multiplies row m of its result by
+//   rstd[m] = 1 / sqrt(sum_t ssq[t][m] / H + eps)
+// before its own epilogue: RMSNorm(x) W^T = rstd * ((x * g) W^T) because the
+// projection is linear.  Slots are summed in a fixed order (deterministic).
 
 struct EpiParams {
   int op;
@@ -35,6 +46,14 @@ struct EpiParams {
   const float2 *rope;            // [max_position, D/2] (cos, sin)
   int n_heads, n_kv_heads, head_dim;
   float eps;
+  // deferred RMSNorm of the A operand (NULL: the operand is already final)
+  const float *ssq_in;           // [ssq_parts][ssq_ld]
+  int ssq_parts, ssq_ld;
+  float norm_eps;                // eps of that RMSNorm
+  float inv_h;                   // 1 / (normalised width)
+  // EPI_RESID_NORM / EPI_STORE_NORM outputs
+  const void *norm_gain;         // [N] gain of the next RMSNorm
+  float *ssq_out;                // [N / 128][ssq_ld]
 };
 
 constexpr int kMaxSrc = 8;   // sources of the K-split A operand (selected layers)
@@ -98,7 +117,8 @@ cudaError_t launch_attention_simt(int store, const AttnParams &p, cudaStream_t s
 
 cudaError_t launch_embed(int store, const void *embed, const int *anchor, const int *kv_len,
                          int B, int S, int H, int vocab, int mask_id, int max_position,
-                         float *x, int *row_pos, unsigned long long *keys, unsigned int *err,
+                         float *x, const void *norm_gain, void *xg, float *ssq, int ssq_ld,
+                         int *row_pos, unsigned long long *keys, unsigned int *err,
                          cudaStream_t s);
 cudaError_t launch_rmsnorm(int in_f32, int store, const void *x, const void *gain, int M, int H,
                            float eps, void *out, void *out2, cudaStream_t s);

@@ -14,9 +14,14 @@ namespace dflash {
 template <typename T>
 __global__ void embed_kernel(const T *__restrict__ embed, const int *__restrict__ anchor,
                              const int *__restrict__ kv_len, int S, int H, int vocab, int mask_id,
-                             int max_position, float *__restrict__ x, int *__restrict__ row_pos,
-                             unsigned long long *__restrict__ keys, unsigned int *err) {
+                             int max_position, float *__restrict__ x, const T *__restrict__ gain,
+                             T *__restrict__ xg, float *__restrict__ ssq, int ssq_ld,
+                             int *__restrict__ row_pos, unsigned long long *__restrict__ keys,
+                             unsigned int *err) {
+  // one CTA of 256 threads per block row; also the deferred RMSNorm of the
+  // first layer's input (x * g and per-128-feature sums of squares)
   pdl_wait();
+  __shared__ float s_ws[64][4];
   const int m = blockIdx.x;
   const int b = m / S, j = m % S;
   int id = j == 0 ? anchor[b] : mask_id;
@@ -30,21 +35,37 @@ __global__ void embed_kernel(const T *__restrict__ embed, const int *__restrict_
     keys[m] = 0ull;
   }
   const T *src = embed + (int64_t)(bad_id ? 0 : id) * H;
-  float *dst = x + (int64_t)m * H;
-  for (int c = threadIdx.x; c < H; c += blockDim.x) dst[c] = bad_id ? 0.f : to_f32(src[c]);
+  const int warp = threadIdx.x >> 5;
+  for (int c0 = 0; c0 < H; c0 += blockDim.x) {
+    const int c = c0 + threadIdx.x;   // H is a multiple of 128: a warp stays inside one part
+    float v = 0.f;
+    if (c < H) {
+      v = bad_id ? 0.f : to_f32(src[c]);
+      x[(int64_t)m * H + c] = v;
+      xg[(int64_t)m * H + c] = from_f32<T>(v * to_f32(gain[c]));
+    }
+    const float t = warp_sum(v * v);
+    if ((threadIdx.x & 31) == 0 && c < H) s_ws[c >> 7][warp & 3] = t;
+  }
+  __syncthreads();
+  for (int q = threadIdx.x; q < (H >> 7); q += blockDim.x)
+    ssq[(int64_t)q * ssq_ld + m] = ((s_ws[q][0] + s_ws[q][1]) + s_ws[q][2]) + s_ws[q][3];
 }
 
 cudaError_t launch_embed(int store, const void *embed, const int *anchor, const int *kv_len, int B,
                          int S, int H, int vocab, int mask_id, int max_position, float *x,
-                         int *row_pos, unsigned long long *keys, unsigned int *err,
-                         cudaStream_t s) {
+                         const void *norm_gain, void *xg, float *ssq, int ssq_ld, int *row_pos,
+                         unsigned long long *keys, unsigned int *err, cudaStream_t s) {
   const int M = B * S;
   if (M <= 0) return cudaSuccess;
+  if (H % 128 || H > 64 * 128) return cudaErrorInvalidValue;
   if (store == ST_F32)
     return launch_pdl(embed_kernel<float>, dim3(M), dim3(256), 0, s, (const float *)embed, anchor,
-                      kv_len, S, H, vocab, mask_id, max_position, x, row_pos, keys, err);
+                      kv_len, S, H, vocab, mask_id, max_position, x, (const float *)norm_gain,
+                      (float *)xg, ssq, ssq_ld, row_pos, keys, err);
   return launch_pdl(embed_kernel<bf16>, dim3(M), dim3(256), 0, s, (const bf16 *)embed, anchor,
-                    kv_len, S, H, vocab, mask_id, max_position, x, row_pos, keys, err);
+                    kv_len, S, H, vocab, mask_id, max_position, x, (const bf16 *)norm_gain,
+                    (bf16 *)xg, ssq, ssq_ld, row_pos, keys, err);
 }
 
 // ---------------------------------------------------------------------------
