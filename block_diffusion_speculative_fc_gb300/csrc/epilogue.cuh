@@ -126,33 +126,49 @@ __device__ void head_ops(const EpiParams &e, const float *t0, int ldt, int m0, i
 // kEpiScratchInts ints; sync(): barrier over the participating threads.
 constexpr int kEpiScratchInts = 3 * kEpiMaxRows;
 
-template <typename T, class Sync>
-__device__ void run_epilogue(const EpiParams &e, float *t0, float *t1, int ldt, int m0, int rows,
-                             int n0, int tid, int nthreads, int *s_int, Sync sync) {
-  const int lane = tid & 31, warp = tid >> 5, nwarps = nthreads >> 5;
-  if (e.ssq_in) {
-    // deferred RMSNorm of the A operand: scale every row by its rstd first
-    float *s_rstd = reinterpret_cast<float *>(s_int + 2 * kEpiMaxRows);
-    constexpr int RPW = kEpiMaxRows / 4;   // rows per warp with >= 4 warps
-    float acc[RPW];
+// Row scales 1/sqrt(sum_t ssq[t][m] / H + eps) of the deferred RMSNorm for
+// rows m0 .. m0+rows-1 into rstd[0..rows): one warp per row, lanes over the
+// slots, every load of a warp issued before the reductions.
+__device__ __forceinline__ void compute_rstd(const EpiParams &e, int m0, int rows, float *rstd,
+                                             int lane, int warp, int nwarps) {
+  constexpr int U = 8;
+  for (int r0 = warp; r0 < rows; r0 += U * nwarps) {
+    float acc[U];
 #pragma unroll
-    for (int k = 0; k < RPW; ++k) {
-      const int r = warp + k * nwarps;
+    for (int k = 0; k < U; ++k) {
+      const int r = r0 + k * nwarps;
       acc[k] = 0.f;
       if (r < rows)
         for (int q = lane; q < e.ssq_parts; q += 32) acc[k] += e.ssq_in[(int64_t)q * e.ssq_ld + m0 + r];
     }
 #pragma unroll
-    for (int k = 0; k < RPW; ++k) {
-      const int r = warp + k * nwarps;
+    for (int k = 0; k < U; ++k) {
+      const int r = r0 + k * nwarps;
       const float t = warp_sum(acc[k]);
-      if (lane == 0 && r < rows) s_rstd[r] = rsqrtf(t * e.inv_h + e.norm_eps);
+      if (lane == 0 && r < rows) rstd[r] = rsqrtf(t * e.inv_h + e.norm_eps);
     }
-    sync();
+  }
+}
+
+template <typename T, class Sync>
+__device__ void run_epilogue(const EpiParams &e, float *t0, float *t1, int ldt, int m0, int rows,
+                             int n0, int tid, int nthreads, int *s_int, Sync sync,
+                             const float *rstd_pre = nullptr) {
+  const int lane = tid & 31, warp = tid >> 5, nwarps = nthreads >> 5;
+  if (e.ssq_in) {
+    // deferred RMSNorm of the A operand: scale every row by its rstd first
+    // (rstd_pre: row scales the caller already computed, indexed from m0)
+    const float *rs = rstd_pre;
+    if (!rs) {
+      float *s_rstd = reinterpret_cast<float *>(s_int + 2 * kEpiMaxRows);
+      compute_rstd(e, m0, rows, s_rstd, lane, warp, nwarps);
+      sync();
+      rs = s_rstd;
+    }
     for (int idx = tid; idx < rows * 128; idx += nthreads) {
       const int r = idx >> 7, c = idx & 127;
-      t0[r * ldt + c] *= s_rstd[r];
-      if (t1) t1[r * ldt + c] *= s_rstd[r];
+      t0[r * ldt + c] *= rs[r];
+      if (t1) t1[r * ldt + c] *= rs[r];
     }
     sync();
   }

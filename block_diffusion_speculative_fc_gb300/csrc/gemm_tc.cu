@@ -209,7 +209,7 @@ struct Cfg {
   static constexpr int STAGE_BYTES = P * W_BYTES + A_BYTES;
   static constexpr int CH = BN < 32 ? BN : 32;          // epilogue token chunk
   static constexpr int STAGING_BYTES = P * CH * 128 * 4;
-  static constexpr int BAR_BYTES = 768;   // mbarriers, TMEM slot, flag, epilogue scratch
+  static constexpr int BAR_BYTES = 768 + 1024;   // mbarriers, TMEM slot, flag, epilogue scratch, row scales
   static constexpr int BUDGET = 225 * 1024;
   static constexpr int STAGES_RAW = (BUDGET - 1024 - STAGING_BYTES - BAR_BYTES) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 12 ? 12 : STAGES_RAW;
@@ -235,6 +235,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
   uint32_t *tmem_slot = (uint32_t *)(mma_done + 1);
   int *flag = (int *)(tmem_slot + 1);
   int *s_int = (int *)((uint8_t *)bars + 256);   // kEpiScratchInts ints
+  float *s_rstd = (float *)((uint8_t *)bars + 768);   // [BN] deferred-norm row scales
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x, cta = blockIdx.x;
@@ -384,6 +385,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
     const int f = quarter * 32 + lane;               // output feature row of this thread
     float *st0 = staging, *st1 = staging + C::CH * 128;
     int seg_i = 0;
+    int rstd_m0 = -1, rstd_seg = -1;   // rows whose deferred-norm scales are in s_rstd
     for (long long i = R.b; i < R.e; ++seg_i) {
       const int tile = (int)(i / p.KB);
       const int kb0 = (int)(i % p.KB);
@@ -395,6 +397,14 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
       const int rows = min(BN, p.M - m0);
       const int buf = seg_i & 1;
       const uint32_t aph = (seg_i >> 1) & 1;
+      // row scales of a deferred RMSNorm, computed while the MMAs still run
+      const bool need_rstd = e.ssq_in != nullptr && (m0 != rstd_m0 || seg != rstd_seg);
+      if (need_rstd) {
+        epi_bar();   // the previous tile's epilogue is done with s_rstd
+        compute_rstd(e, m0, rows, s_rstd, lane, ew, 4);
+        rstd_m0 = m0;
+        rstd_seg = seg;
+      }
       const bool ok = epi_all(mbar_wait(&acc_full[buf], aph));
       if (!ok) {
         if (tid == 0) raise_error(p.err, DFLASH_DERR_TIMEOUT);
@@ -417,7 +427,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
           epi_bar();
           if (c0 < rows)
             run_epilogue<T>(e, st0, PAIR ? st1 : nullptr, 128, m0 + c0, min(C::CH, rows - c0), n0,
-                            tid, 128, s_int, [] { epi_bar(); });
+                            tid, 128, s_int, [] { epi_bar(); }, s_rstd + c0);
           epi_bar();
         }
         tc_fence_before();
@@ -491,7 +501,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
             epi_bar();
             if (c0 < rows)
               run_epilogue<T>(e, st0, PAIR ? st1 : nullptr, 128, m0 + c0, min(C::CH, rows - c0),
-                              n0, tid, 128, s_int, [] { epi_bar(); });
+                              n0, tid, 128, s_int, [] { epi_bar(); }, s_rstd + c0);
             epi_bar();
           }
           if (tid == 0) p.counters[tile] = 0;   // ready for the next launch

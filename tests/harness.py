@@ -19,6 +19,13 @@ from synth import make_anchor, make_features, make_page_table, make_posterior, \
     make_posterior_with_commit, make_commit_lengths, make_weights
 
 MARGIN = 1e-2
+# A drafted id may differ from the oracle's only where the choice is within
+# the arithmetic error of the two logits: the oracle's margin is below MARGIN,
+# or the GPU picked a token whose oracle logit trails the top one by less
+# than TIE_SIGMAS standard deviations of the logit-difference error implied by
+# the measured hidden-state error dh (a vector of norm |dh| in a random
+# direction moves <h, w_a - w_b> by about |dh| |w_a - w_b| / sqrt(H)).
+TIE_SIGMAS = 4.0
 
 
 def to_numpy_weights(W):
@@ -111,14 +118,21 @@ class CycleRun:
             for b in self.check:
                 ids, hid, margin = O.draft_block(cfg, self.Wn, int(anchor[b]), self.ctx[b].layers(),
                                                  self.ctx[b].kv_len)
-                r = rel_l2(hid_d[b].double().cpu().numpy(), hid)
+                h_gpu = hid_d[b].double().cpu().numpy()
+                r = rel_l2(h_gpu, hid)
                 self.stats["hidden_rel"].append(r)
                 assert r <= self.tol, (c, b, r)
                 assert got[b, 0] == anchor[b]
                 for j in range(1, S):
                     self.stats["ids"] += 1
                     if got[b, j] != ids[j]:
-                        assert margin[j - 1] < MARGIN, (c, b, j, got[b, j], ids[j], margin[j - 1])
+                        w2 = self.Wn["lm_head"][[ids[j], got[b, j]]].astype(np.float64)
+                        lg = np.asarray(hid[j], dtype=np.float64) @ w2.T
+                        gap = float(lg[0] - lg[1])     # oracle logit of its pick minus the GPU's pick
+                        dh = float(np.linalg.norm(h_gpu[j] - hid[j]))
+                        bound = TIE_SIGMAS * dh * float(np.linalg.norm(w2[0] - w2[1])) / np.sqrt(cfg.hidden)
+                        self.stats.setdefault("mismatch", []).append(
+                            (c, b, j, float(margin[j - 1]), gap, bound))
                         self.stats["id_mismatch_near_tie"] += 1
                 draft_used[b] = ids
             # synthetic target verify
@@ -159,4 +173,6 @@ class CycleRun:
         self.compare_kv()
         err = self.sess.error()
         assert err == 0, pkg.decode_error(err)
+        bad = [m for m in self.stats.get("mismatch", []) if m[3] >= MARGIN and m[4] > m[5]]
+        assert not bad, ("argmax differs beyond the near-tie allowance", bad)
         return self.stats

@@ -30,7 +30,7 @@ KIMI_MINI = shrink(KIMI, name="kimi-mini", target_hidden=256, target_layer_ids=(
 
 
 def _report(stats):
-    print({k: (max(v) if isinstance(v, list) and v and k != "accept" else v)
+    print({k: (max(v) if isinstance(v, list) and v and k not in ("accept", "mismatch") else v)
            for k, v in stats.items() if k != "accept"},
           "mean accept", float(np.mean(stats["accept"])) if stats["accept"] else None)
 
