@@ -23,8 +23,12 @@
 #include <algorithm>
 #include <cstring>
 
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "kernels.h"
+
+namespace cg = cooperative_groups;
 
 namespace dflash {
 namespace att {
@@ -164,6 +168,193 @@ __global__ void attn_prep_kernel(const int *__restrict__ kv_len, int B, int kvh,
   }
 }
 
+// Attention of the R query rows of (request b, KV head g) over context pages
+// [pg0, pg1) of its visible range (first_page = first visible page) and, when
+// has_block, the S block keys.  Leaves the unnormalised output, row maxima and
+// row sums (already summed over the quad) in `a`.  `use` counts stage uses of
+// the CTA's ring across calls.  All threads of the CTA take part.
+struct Acc {
+  float o[16][4];
+  float m0, m1, l0, l1;
+};
+
+__device__ __forceinline__ bool attend(const Params &p, uint8_t *smem, uint64_t *full, uint32_t &use,
+                                       int b, int g, int kv, int first_page, int pg0, int pg1,
+                                       bool has_block, Acc &a) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int grp = lane >> 2, tig = lane & 3;
+  const int S = p.S, R = p.R, G = p.n_heads / p.kvh;
+  const int ntiles = max(0, pg1 - pg0) + (has_block ? 1 : 0);
+  float(&o)[16][4] = a.o;
+  float &m0 = a.m0, &m1 = a.m1, &l0 = a.l0, &l1 = a.l1;
+  // query rows of this warp: r = warp*16 + grp (+8); row r -> head g*G + r/S, position j = r%S
+  const int r0 = warp * 16 + grp, r1 = r0 + 8;
+  uint32_t qa[8][4];
+  {
+    const bf16 *q = p.q;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int r = hh ? r1 : r0;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const int d = ks * 16 + half * 8 + tig * 2;
+          uint32_t v = 0;
+          if (r < R) {
+            const int h = g * G + r / S, j = r % S;
+            v = *reinterpret_cast<const uint32_t *>(q + ((size_t)(b * S + j) * p.n_heads + h) * 128 + d);
+          }
+          qa[ks][half * 2 + hh] = v;
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  m0 = -INFINITY;
+  m1 = -INFINITY;
+  l0 = 0.f;
+  l1 = 0.f;
+  const int j0 = r0 % S, j1 = r1 % S;
+  const int lo0 = p.window > 0 ? kv + j0 - p.window + 1 : 0;   // first visible ctx position
+  const int lo1 = p.window > 0 ? kv + j1 - p.window + 1 : 0;
+
+  auto issue = [&](int t, uint32_t u) {
+    uint8_t *st = smem + (u % STAGES) * STAGE_BYTES;
+    uint64_t *bar = &full[u % STAGES];
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(bar)),
+                 "r"(STAGE_BYTES)
+                 : "memory");
+    if (t < pg1 - pg0) {
+      const int lp = first_page + pg0 + t;
+      int page = p.page_table[(size_t)b * p.pages_per_req + lp];
+      if (page < 0 || page >= p.n_pages) {
+        raise_error(p.err, DFLASH_DERR_PAGE_RANGE);
+        page = 0;
+      }
+      tma3(st, &p.tmK, bar, 0, g, page * KT);
+      tma3(st + TILE_BYTES / 2, &p.tmK, bar, 64, g, page * KT);
+      tma3(st + TILE_BYTES, &p.tmV, bar, 0, g, page * KT);
+      tma3(st + TILE_BYTES + TILE_BYTES / 2, &p.tmV, bar, 64, g, page * KT);
+    } else {
+      tma3(st, &p.tmKb, bar, 0, g, b * S);
+      tma3(st + TILE_BYTES / 2, &p.tmKb, bar, 64, g, b * S);
+      tma3(st + TILE_BYTES, &p.tmVb, bar, 0, g, b * S);
+      tma3(st + TILE_BYTES + TILE_BYTES / 2, &p.tmVb, bar, 64, g, b * S);
+    }
+  };
+  if (threadIdx.x == 0)
+    for (int t = 0; t < STAGES && t < ntiles; ++t) issue(t, use + t);
+
+  bool ok = true;
+  for (int t = 0; t < ntiles; ++t) {
+    const uint32_t u = use + t;
+    const bool got = mbar_wait(&full[u % STAGES], (u / STAGES) & 1);
+    if (!got) ok = false;
+    const uint32_t kbase = su32(smem + (u % STAGES) * STAGE_BYTES);
+    const uint32_t vbase = kbase + TILE_BYTES;
+    const bool blk = t >= pg1 - pg0;
+    const int pos0 = (first_page + pg0 + t) * KT;   // position of key 0 of a context tile
+    // ---- S = Q K^T (16 rows x 64 keys per warp)
+    float s[8][4];
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+      for (int kc = 0; kc < 4; ++kc) {          // 32 dims per ldmatrix.x4
+        const int key = nt * 8 + (lane & 7);
+        const int d = kc * 32 + (lane >> 3) * 8;
+        const uint32_t addr = swz(kbase + (d >> 6) * (TILE_BYTES / 2), key, (d & 63) >> 3);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(addr, b0, b1, b2, b3);
+        mma16816(s[nt], qa[kc * 2], b0, b1);
+        mma16816(s[nt], qa[kc * 2 + 1], b2, b3);
+      }
+    }
+    // ---- mask, online softmax
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int key = nt * 8 + tig * 2 + (e & 1);
+        const bool row1 = e >= 2;
+        bool vis;
+        if (blk) {
+          vis = key < S;
+        } else {
+          const int pos = pos0 + key;
+          vis = pos < kv && pos >= (row1 ? lo1 : lo0);
+        }
+        if ((row1 ? r1 : r0) >= R) vis = false;
+        const float v = vis ? s[nt][e] * p.scale_log2 : -INFINITY;
+        s[nt][e] = v;
+        if (row1) mx1 = fmaxf(mx1, v); else mx0 = fmaxf(mx0, v);
+      }
+    }
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    const float a0 = mn0 == -INFINITY ? 1.f : exp2f(m0 - mn0);
+    const float a1 = mn1 == -INFINITY ? 1.f : exp2f(m1 - mn1);
+    m0 = mn0;
+    m1 = mn1;
+    float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      s[nt][0] = s[nt][0] == -INFINITY ? 0.f : exp2f(s[nt][0] - mn0);
+      s[nt][1] = s[nt][1] == -INFINITY ? 0.f : exp2f(s[nt][1] - mn0);
+      s[nt][2] = s[nt][2] == -INFINITY ? 0.f : exp2f(s[nt][2] - mn1);
+      s[nt][3] = s[nt][3] == -INFINITY ? 0.f : exp2f(s[nt][3] - mn1);
+      ps0 += s[nt][0] + s[nt][1];
+      ps1 += s[nt][2] + s[nt][3];
+    }
+    l0 = l0 * a0 + ps0;
+    l1 = l1 * a1 + ps1;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      o[i][0] *= a0;
+      o[i][1] *= a0;
+      o[i][2] *= a1;
+      o[i][3] *= a1;
+    }
+    // ---- O += P V (P from the S accumulators, V via transposed ldmatrix)
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {              // 16 keys per step
+      uint32_t pa[4];
+      pa[0] = pack_bf16(s[2 * kk][0], s[2 * kk][1]);
+      pa[1] = pack_bf16(s[2 * kk][2], s[2 * kk][3]);
+      pa[2] = pack_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1]);
+      pa[3] = pack_bf16(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+#pragma unroll
+      for (int np = 0; np < 8; ++np) {            // pairs of 8-dim n-tiles
+        const int key = kk * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+        const int d = np * 16 + (lane >> 4) * 8;
+        const uint32_t addr = swz(vbase + (d >> 6) * (TILE_BYTES / 2), key, (d & 63) >> 3);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(addr, b0, b1, b2, b3);
+        mma16816(o[2 * np], pa, b0, b1);
+        mma16816(o[2 * np + 1], pa, b2, b3);
+      }
+    }
+    __syncthreads();   // every warp is done with this stage
+    if (threadIdx.x == 0 && t + STAGES < ntiles) issue(t + STAGES, u + STAGES);
+  }
+  use += ntiles;
+  if (!ok && lane == 0) raise_error(p.err, DFLASH_DERR_TIMEOUT);
+
+  // ---- finish: row sums across the quad
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+  return ok;
+}
+
 // ---------------------------------------------------------------- main kernel
 __global__ void __launch_bounds__(256) attn_mma_kernel(const __grid_constant__ Params p) {
   pdl_wait();
@@ -206,171 +397,12 @@ __global__ void __launch_bounds__(256) attn_mma_kernel(const __grid_constant__ P
     const int pages = kv > lo ? (kv - 1) / KT - first_page + 1 : 0;
     const int pg0 = split * pps, pg1 = min(pages, pg0 + pps);
     const bool has_block = split == nsplit - 1;
-    const int ntiles = max(0, pg1 - pg0) + (has_block ? 1 : 0);
 
-    // query rows of this warp: r = warp*16 + grp (+8); row r -> head g*G + r/S, position j = r%S
+    Acc acc;
+    attend(p, smem, full, use, b, g, kv, first_page, pg0, pg1, has_block, acc);
     const int r0 = warp * 16 + grp, r1 = r0 + 8;
-    uint32_t qa[8][4];
-    {
-      const bf16 *q = p.q;
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int r = hh ? r1 : r0;
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            const int d = ks * 16 + half * 8 + tig * 2;
-            uint32_t v = 0;
-            if (r < R) {
-              const int h = g * G + r / S, j = r % S;
-              v = *reinterpret_cast<const uint32_t *>(q + ((size_t)(b * S + j) * p.n_heads + h) * 128 + d);
-            }
-            qa[ks][half * 2 + hh] = v;
-          }
-        }
-      }
-    }
-    float o[16][4];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    const int j0 = r0 % S, j1 = r1 % S;
-    const int lo0 = p.window > 0 ? kv + j0 - p.window + 1 : 0;   // first visible ctx position
-    const int lo1 = p.window > 0 ? kv + j1 - p.window + 1 : 0;
-
-    auto issue = [&](int t, uint32_t u) {
-      uint8_t *st = smem + (u % STAGES) * STAGE_BYTES;
-      uint64_t *bar = &full[u % STAGES];
-      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(bar)),
-                   "r"(STAGE_BYTES)
-                   : "memory");
-      if (t < pg1 - pg0) {
-        const int lp = first_page + pg0 + t;
-        int page = p.page_table[(size_t)b * p.pages_per_req + lp];
-        if (page < 0 || page >= p.n_pages) {
-          raise_error(p.err, DFLASH_DERR_PAGE_RANGE);
-          page = 0;
-        }
-        tma3(st, &p.tmK, bar, 0, g, page * KT);
-        tma3(st + TILE_BYTES / 2, &p.tmK, bar, 64, g, page * KT);
-        tma3(st + TILE_BYTES, &p.tmV, bar, 0, g, page * KT);
-        tma3(st + TILE_BYTES + TILE_BYTES / 2, &p.tmV, bar, 64, g, page * KT);
-      } else {
-        tma3(st, &p.tmKb, bar, 0, g, b * S);
-        tma3(st + TILE_BYTES / 2, &p.tmKb, bar, 64, g, b * S);
-        tma3(st + TILE_BYTES, &p.tmVb, bar, 0, g, b * S);
-        tma3(st + TILE_BYTES + TILE_BYTES / 2, &p.tmVb, bar, 64, g, b * S);
-      }
-    };
-    if (threadIdx.x == 0)
-      for (int t = 0; t < STAGES && t < ntiles; ++t) issue(t, use + t);
-
-    bool ok = true;
-    for (int t = 0; t < ntiles; ++t) {
-      const uint32_t u = use + t;
-      const bool got = mbar_wait(&full[u % STAGES], (u / STAGES) & 1);
-      if (!got) ok = false;
-      const uint32_t kbase = su32(smem + (u % STAGES) * STAGE_BYTES);
-      const uint32_t vbase = kbase + TILE_BYTES;
-      const bool blk = t >= pg1 - pg0;
-      const int pos0 = (first_page + pg0 + t) * KT;   // position of key 0 of a context tile
-      // ---- S = Q K^T (16 rows x 64 keys per warp)
-      float s[8][4];
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
-#pragma unroll
-        for (int kc = 0; kc < 4; ++kc) {          // 32 dims per ldmatrix.x4
-          const int key = nt * 8 + (lane & 7);
-          const int d = kc * 32 + (lane >> 3) * 8;
-          const uint32_t addr = swz(kbase + (d >> 6) * (TILE_BYTES / 2), key, (d & 63) >> 3);
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(addr, b0, b1, b2, b3);
-          mma16816(s[nt], qa[kc * 2], b0, b1);
-          mma16816(s[nt], qa[kc * 2 + 1], b2, b3);
-        }
-      }
-      // ---- mask, online softmax
-      float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int key = nt * 8 + tig * 2 + (e & 1);
-          const bool row1 = e >= 2;
-          bool vis;
-          if (blk) {
-            vis = key < S;
-          } else {
-            const int pos = pos0 + key;
-            vis = pos < kv && pos >= (row1 ? lo1 : lo0);
-          }
-          if ((row1 ? r1 : r0) >= R) vis = false;
-          const float v = vis ? s[nt][e] * p.scale_log2 : -INFINITY;
-          s[nt][e] = v;
-          if (row1) mx1 = fmaxf(mx1, v); else mx0 = fmaxf(mx0, v);
-        }
-      }
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-      const float a0 = mn0 == -INFINITY ? 1.f : exp2f(m0 - mn0);
-      const float a1 = mn1 == -INFINITY ? 1.f : exp2f(m1 - mn1);
-      m0 = mn0;
-      m1 = mn1;
-      float ps0 = 0.f, ps1 = 0.f;
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
-        s[nt][0] = s[nt][0] == -INFINITY ? 0.f : exp2f(s[nt][0] - mn0);
-        s[nt][1] = s[nt][1] == -INFINITY ? 0.f : exp2f(s[nt][1] - mn0);
-        s[nt][2] = s[nt][2] == -INFINITY ? 0.f : exp2f(s[nt][2] - mn1);
-        s[nt][3] = s[nt][3] == -INFINITY ? 0.f : exp2f(s[nt][3] - mn1);
-        ps0 += s[nt][0] + s[nt][1];
-        ps1 += s[nt][2] + s[nt][3];
-      }
-      l0 = l0 * a0 + ps0;
-      l1 = l1 * a1 + ps1;
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        o[i][0] *= a0;
-        o[i][1] *= a0;
-        o[i][2] *= a1;
-        o[i][3] *= a1;
-      }
-      // ---- O += P V (P from the S accumulators, V via transposed ldmatrix)
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {              // 16 keys per step
-        uint32_t pa[4];
-        pa[0] = pack_bf16(s[2 * kk][0], s[2 * kk][1]);
-        pa[1] = pack_bf16(s[2 * kk][2], s[2 * kk][3]);
-        pa[2] = pack_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-        pa[3] = pack_bf16(s[2 * kk + 1][2], s[2 * kk + 1][3]);
-#pragma unroll
-        for (int np = 0; np < 8; ++np) {            // pairs of 8-dim n-tiles
-          const int key = kk * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
-          const int d = np * 16 + (lane >> 4) * 8;
-          const uint32_t addr = swz(vbase + (d >> 6) * (TILE_BYTES / 2), key, (d & 63) >> 3);
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(addr, b0, b1, b2, b3);
-          mma16816(o[2 * np], pa, b0, b1);
-          mma16816(o[2 * np + 1], pa, b2, b3);
-        }
-      }
-      __syncthreads();   // every warp is done with this stage
-      if (threadIdx.x == 0 && t + STAGES < ntiles) issue(t + STAGES, u + STAGES);
-    }
-    use += ntiles;
-    if (!ok && lane == 0) raise_error(p.err, DFLASH_DERR_TIMEOUT);
-
-    // ---- finish: row sums across the quad
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    float(&o)[16][4] = acc.o;
+    const float m0 = acc.m0, m1 = acc.m1, l0 = acc.l0, l1 = acc.l1;
     if (nsplit == 1) {
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
@@ -449,6 +481,97 @@ __global__ void __launch_bounds__(256) attn_mma_kernel(const __grid_constant__ P
   (void)nwarps;
 }
 
+// ---------------------------------------------------------------- small batches
+// One thread-block cluster of C CTAs per (request, KV head): CTA rank r takes
+// the r-th of C equal slices of the context pages (the last rank also the
+// block keys), then the C partial results are merged through distributed
+// shared memory -- no scratch in global memory, no tickets, no prep kernel.
+__global__ void __launch_bounds__(256) attn_cluster_kernel(const __grid_constant__ Params p) {
+  pdl_wait();
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint64_t *full = (uint64_t *)(smem + STAGES * STAGE_BYTES);
+  cg::cluster_group cl = cg::this_cluster();
+  const int C = (int)cl.num_blocks();
+  const int rank = (int)cl.block_rank();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int grp = lane >> 2, tig = lane & 3;
+  const int S = p.S, R = p.R, G = p.n_heads / p.kvh;
+  const int bg = blockIdx.x / C, b = bg / p.kvh, g = bg % p.kvh;
+  const int cap = p.pages_per_req * KT;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&full[i])));
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  int kv = p.kv_len[b];
+  if (kv < 0 || kv > cap) {
+    if (threadIdx.x == 0 && rank == 0) raise_error(p.err, DFLASH_DERR_KV_CAPACITY);
+    kv = kv < 0 ? 0 : cap;
+  }
+  const int lo = p.window > 0 ? max(0, kv - p.window + 1) : 0;
+  const int first_page = lo / KT;
+  const int pages = kv > lo ? (kv - 1) / KT - first_page + 1 : 0;
+  const int pg0 = pages * rank / C, pg1 = pages * (rank + 1) / C;
+  uint32_t use = 0;
+  Acc acc;
+  attend(p, smem, full, use, b, g, kv, first_page, pg0, pg1, rank == C - 1, acc);
+  // this CTA's partial (unnormalised O, row max, row sum) into its own shared memory;
+  // the stage ring is free: attend() ends every tile with a CTA barrier
+  float *po = reinterpret_cast<float *>(smem);                    // [R][128]
+  float2 *pml = reinterpret_cast<float2 *>(smem + R * 128 * 4);   // [R]
+  const int r0 = warp * 16 + grp, r1 = r0 + 8;
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    const int r = hh ? r1 : r0;
+    if (r >= R) continue;
+#pragma unroll
+    for (int nt = 0; nt < 16; ++nt)
+      *reinterpret_cast<float2 *>(po + r * 128 + nt * 8 + tig * 2) =
+          make_float2(acc.o[nt][hh * 2], acc.o[nt][hh * 2 + 1]);
+    if (tig == 0) pml[r] = make_float2(hh ? acc.m1 : acc.m0, hh ? acc.l1 : acc.l0);
+  }
+  cl.sync();
+  // rank r merges rows [R*r/C, R*(r+1)/C) from every CTA of the cluster
+  const int rb = R * rank / C, re = R * (rank + 1) / C;
+  const int nthr = blockDim.x;
+  for (int idx = threadIdx.x; idx < (re - rb) * 32; idx += nthr) {
+    const int r = rb + idx / 32, d = (idx % 32) * 4;
+    float ms[8], ls[8];
+    float mstar = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      if (c >= C) break;
+      const float2 ml = cl.map_shared_rank(pml, c)[r];
+      ms[c] = ml.x;
+      ls[c] = ml.y;
+      mstar = fmaxf(mstar, ml.x);
+    }
+    float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+    float den = 0.f;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      if (c >= C) break;
+      const float w = ms[c] == -INFINITY ? 0.f : exp2f(ms[c] - mstar);
+      const float4 v = *reinterpret_cast<const float4 *>(cl.map_shared_rank(po, c) + r * 128 + d);
+      num.x += w * v.x;
+      num.y += w * v.y;
+      num.z += w * v.z;
+      num.w += w * v.w;
+      den += w * ls[c];
+    }
+    const float inv = 1.f / den;
+    const int h = g * G + r / S, j = r % S;
+    bf16 *dst = p.out + ((size_t)(b * S + j) * p.n_heads + h) * 128 + d;
+    *reinterpret_cast<__nv_bfloat162 *>(dst) = __floats2bfloat162_rn(num.x * inv, num.y * inv);
+    *reinterpret_cast<__nv_bfloat162 *>(dst + 2) = __floats2bfloat162_rn(num.z * inv, num.w * inv);
+  }
+  cl.sync();   // peers may still be reading this CTA's shared memory
+  __syncthreads();
+  pdl_trigger();
+}
+
 }  // namespace att
 
 namespace {
@@ -487,8 +610,13 @@ size_t attention_mma_scratch_items(int max_batch, int kvh) {
 }
 
 cudaError_t prepare_attention_mma() {
-  return cudaFuncSetAttribute(att::attn_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              att::SMEM);
+  cudaError_t e = cudaFuncSetAttribute(att::attn_mma_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, att::SMEM);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(att::attn_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           att::SMEM);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(att::attn_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
 }
 
 cudaError_t launch_attention_mma(const AttnParams &a, const AttnScratch &w, cudaStream_t s) {
@@ -508,20 +636,10 @@ cudaError_t launch_attention_mma(const AttnParams &a, const AttnScratch &w, cuda
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (sms <= 0) sms = 1;
-  const int max_items = (int)attention_mma_scratch_items(a.B, a.n_kv_heads);
-  cudaError_t e = launch_pdl(att::attn_prep_kernel, dim3(1), dim3(256), 0, s, a.kv_len, a.B,
-                             a.n_kv_heads, a.pages_per_req * att::KT, a.window, 2 * sms,
-                             max_items, w.item_start, w.pps, a.err);
-  if (e != cudaSuccess) return e;
   p.q = (const bf16 *)a.q;
   p.out = (bf16 *)a.out;
   p.page_table = a.page_table;
   p.kv_len = a.kv_len;
-  p.item_start = w.item_start;
-  p.pps_ptr = w.pps;
-  p.part_o = w.part_o;
-  p.part_ml = (float2 *)w.part_ml;
-  p.tickets = w.tickets;
   p.err = a.err;
   p.B = a.B;
   p.S = a.S;
@@ -531,8 +649,39 @@ cudaError_t launch_attention_mma(const AttnParams &a, const AttnScratch &w, cuda
   p.n_pages = a.n_pages;
   p.window = a.window;
   p.R = R;
-  p.max_items = max_items;
   p.scale_log2 = 1.4426950408889634f * a.scale;
+  // Few (request, head) pairs: a cluster of C CTAs per pair, merged on chip.
+  const int pairs = a.B * a.n_kv_heads;
+  if (4 * pairs <= 2 * sms) {
+    int C = 8;
+    while (C > 4 && C * pairs > 2 * sms) C >>= 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(pairs * C);
+    cfg.blockDim = dim3(warps * 32);
+    cfg.dynamicSmemBytes = att::SMEM;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = C;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, att::attn_cluster_kernel, p);
+  }
+  const int max_items = (int)attention_mma_scratch_items(a.B, a.n_kv_heads);
+  cudaError_t e = launch_pdl(att::attn_prep_kernel, dim3(1), dim3(256), 0, s, a.kv_len, a.B,
+                             a.n_kv_heads, a.pages_per_req * att::KT, a.window, 2 * sms,
+                             max_items, w.item_start, w.pps, a.err);
+  if (e != cudaSuccess) return e;
+  p.item_start = w.item_start;
+  p.pps_ptr = w.pps;
+  p.part_o = w.part_o;
+  p.part_ml = (float2 *)w.part_ml;
+  p.tickets = w.tickets;
+  p.max_items = max_items;
   return launch_pdl(att::attn_mma_kernel, dim3(2 * sms), dim3(warps * 32), att::SMEM, s, p);
 }
 

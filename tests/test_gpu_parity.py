@@ -87,3 +87,12 @@ def test_kimi_mini_long_context_window_edge():
     """Window 64 against contexts far longer than the window."""
     run = CycleRun(KIMI_MINI, 2, [1000, 130], cycles=3, permuted=True)
     _report(run.run())
+
+
+def test_many_request_heads_use_the_split_attention():
+    """80 (request, KV head) pairs: more than the cluster path takes, so the
+    persistent split kernel with ticketed merges runs (windowed layer too)."""
+    cfg = shrink(QWEN_MINI, name="many-pairs", sliding_window=(100, 0))
+    lens = np.random.default_rng(5).integers(20, 700, 40)
+    run = CycleRun(cfg, 40, lens, cycles=2, permuted=True, check=[0, 17, 39])
+    _report(run.run())
