@@ -109,6 +109,12 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *tm, ui
       "l"((uint64_t)tm), "r"(su32(bar)), "r"(x), "r"(y), "l"(policy)
       : "memory");
 }
+// Bring one weight box into L2 (no shared memory, no completion tracking).
+__device__ __forceinline__ void prefetch_l2(const CUtensorMap *tm, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"((uint64_t)tm),
+               "r"(x), "r"(y)
+               : "memory");
+}
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *tm) {
   asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)tm) : "memory");
 }
@@ -213,6 +219,8 @@ struct Cfg {
   static constexpr int BUDGET = 225 * 1024;
   static constexpr int STAGES_RAW = (BUDGET - 1024 - STAGING_BYTES - BAR_BYTES) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 12 ? 12 : STAGES_RAW;
+  // k-blocks of weights kept in flight to L2 beyond the ring (about 256 KB)
+  static constexpr int PF = (256 * 1024) / (P * W_BYTES);
   static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + STAGING_BYTES + BAR_BYTES;
   static constexpr int ACC_COLS = P * BN;                // one accumulator buffer
   static constexpr int TMEM_COLS = 2 * ACC_COLS <= 32 ? 32 : (2 * ACC_COLS <= 64 ? 64 :
@@ -278,21 +286,39 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
       const uint64_t pol_w = policy_evict_first(), pol_a = policy_evict_last();
       // walk this CTA's (tile, k-block) range incrementally: one division up
       // front, a tile lookup only when the tile changes
-      long long left = R.e - R.b;
-      int tile = (int)(R.b / p.KB), kb = (int)(R.b % p.KB) - 1;
-      int seg = 0, n0 = 0, m0 = 0, k = 0;
-      locate(tile, seg, n0, m0);
-      auto next = [&]() -> bool {
-        if (left <= 0) return false;
-        --left;
-        if (++kb == p.KB) {
-          kb = 0;
-          ++tile;
-          locate(tile, seg, n0, m0);
+      struct Walker {
+        long long left;
+        int tile, kb, seg, n0, m0, k;
+      };
+      auto start = [&](Walker &w, long long at) {
+        w.left = R.e - at;
+        w.tile = (int)(at / p.KB);
+        w.kb = (int)(at % p.KB) - 1;
+        locate(w.tile, w.seg, w.n0, w.m0);
+      };
+      auto advance = [&](Walker &w) -> bool {
+        if (w.left <= 0) return false;
+        --w.left;
+        if (++w.kb == p.KB) {
+          w.kb = 0;
+          ++w.tile;
+          locate(w.tile, w.seg, w.n0, w.m0);
         }
-        k = kb * BK;
+        w.k = w.kb * BK;
         return true;
       };
+      Walker ld, pf;
+      start(ld, R.b);
+      // L2 prefetch cursor: runs C::PF k-blocks beyond what the ring holds,
+      // so more weight bytes are in flight than shared memory can stage
+      start(pf, min(R.b + (long long)C::STAGES, R.e));
+      auto prefetch_one = [&]() {
+        if (!advance(pf)) return;
+        prefetch_l2(&p.tmW[pf.seg], pf.k, pf.n0);
+        if (PAIR) prefetch_l2(&p.tmW[pf.seg], pf.k, p.seg_half[pf.seg] + pf.n0);
+      };
+      int &seg = ld.seg, &n0 = ld.n0, &m0 = ld.m0, &k = ld.k;
+      auto next = [&]() -> bool { return advance(ld); };
       auto load_w = [&](int s) {
         uint8_t *st = stages + s * C::STAGE_BYTES;
         mbar_expect_tx(&full[s], C::STAGE_BYTES);
@@ -305,7 +331,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
                     kk - src * p.k_per_src, mm, pol_a);
       };
       // Weights do not depend on the previous kernel: fill the whole ring with
-      // them first, then wait for the predecessor and add the activations.
+      // them first (and start the L2 prefetch), then wait for the predecessor
+      // and add the activations.
       int it = 0;
       int pend_k[C::STAGES], pend_m[C::STAGES];
       while (it < C::STAGES && next()) {
@@ -314,6 +341,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
         pend_m[it] = m0;
         ++it;
       }
+      for (int j = 0; j < C::PF; ++j) prefetch_one();
       pdl_wait();
       for (int j = 0; j < it; ++j) load_a(j, pend_k[j], pend_m[j]);
       bool ok = true;
@@ -325,6 +353,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
         }
         load_w(s);
         load_a(s, k, m0);
+        prefetch_one();
         ++it;
       }
       if (!ok) raise_error(p.err, DFLASH_DERR_TIMEOUT);

@@ -36,15 +36,24 @@ __global__ void embed_kernel(const T *__restrict__ embed, const int *__restrict_
   }
   const T *src = embed + (int64_t)(bad_id ? 0 : id) * H;
   const int warp = threadIdx.x >> 5;
-  for (int c0 = 0; c0 < H; c0 += blockDim.x) {
-    const int c = c0 + threadIdx.x;   // H is a multiple of 128: a warp stays inside one part
-    float v = 0.f;
+  // every load of the row is issued before any use (H <= 64 * 128 = 32 x 256)
+  constexpr int MAXV = 32;
+  float v[MAXV], gv[MAXV];
+#pragma unroll
+  for (int k = 0; k < MAXV; ++k) {
+    const int c = k * blockDim.x + threadIdx.x;
+    v[k] = (c < H && !bad_id) ? to_f32(src[c]) : 0.f;
+    gv[k] = c < H ? to_f32(gain[c]) : 0.f;
+  }
+#pragma unroll
+  for (int k = 0; k < MAXV; ++k) {
+    const int c = k * blockDim.x + threadIdx.x;   // H is a multiple of 128: a warp stays in one part
+    if (k * (int)blockDim.x >= H) break;
     if (c < H) {
-      v = bad_id ? 0.f : to_f32(src[c]);
-      x[(int64_t)m * H + c] = v;
-      xg[(int64_t)m * H + c] = from_f32<T>(v * to_f32(gain[c]));
+      x[(int64_t)m * H + c] = v[k];
+      xg[(int64_t)m * H + c] = from_f32<T>(v[k] * gv[k]);
     }
-    const float t = warp_sum(v * v);
+    const float t = warp_sum(v[k] * v[k]);
     if ((threadIdx.x & 31) == 0 && c < H) s_ws[c >> 7][warp & 3] = t;
   }
   __syncthreads();
