@@ -109,12 +109,6 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *tm, ui
       "l"((uint64_t)tm), "r"(su32(bar)), "r"(x), "r"(y), "l"(policy)
       : "memory");
 }
-// Bring one weight box into L2 (no shared memory, no completion tracking).
-__device__ __forceinline__ void prefetch_l2(const CUtensorMap *tm, int x, int y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"((uint64_t)tm),
-               "r"(x), "r"(y)
-               : "memory");
-}
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *tm) {
   asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)tm) : "memory");
 }
@@ -219,8 +213,6 @@ struct Cfg {
   static constexpr int BUDGET = 225 * 1024;
   static constexpr int STAGES_RAW = (BUDGET - 1024 - STAGING_BYTES - BAR_BYTES) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 12 ? 12 : STAGES_RAW;
-  // k-blocks of weights kept in flight to L2 beyond the ring (about 256 KB)
-  static constexpr int PF = (256 * 1024) / (P * W_BYTES);
   static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + STAGING_BYTES + BAR_BYTES;
   static constexpr int ACC_COLS = P * BN;                // one accumulator buffer
   static constexpr int TMEM_COLS = 2 * ACC_COLS <= 32 ? 32 : (2 * ACC_COLS <= 64 ? 64 :
@@ -307,16 +299,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
         w.k = w.kb * BK;
         return true;
       };
-      Walker ld, pf;
+      Walker ld;
       start(ld, R.b);
-      // L2 prefetch cursor: runs C::PF k-blocks beyond what the ring holds,
-      // so more weight bytes are in flight than shared memory can stage
-      start(pf, min(R.b + (long long)C::STAGES, R.e));
-      auto prefetch_one = [&]() {
-        if (!advance(pf)) return;
-        prefetch_l2(&p.tmW[pf.seg], pf.k, pf.n0);
-        if (PAIR) prefetch_l2(&p.tmW[pf.seg], pf.k, p.seg_half[pf.seg] + pf.n0);
-      };
       int &seg = ld.seg, &n0 = ld.n0, &m0 = ld.m0, &k = ld.k;
       auto next = [&]() -> bool { return advance(ld); };
       auto load_w = [&](int s) {
@@ -331,8 +315,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
                     kk - src * p.k_per_src, mm, pol_a);
       };
       // Weights do not depend on the previous kernel: fill the whole ring with
-      // them first (and start the L2 prefetch), then wait for the predecessor
-      // and add the activations.
+      // them first, then wait for the predecessor and add the activations.
       int it = 0;
       int pend_k[C::STAGES], pend_m[C::STAGES];
       while (it < C::STAGES && next()) {
@@ -341,7 +324,6 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
         pend_m[it] = m0;
         ++it;
       }
-      for (int j = 0; j < C::PF; ++j) prefetch_one();
       pdl_wait();
       for (int j = 0; j < it; ++j) load_a(j, pend_k[j], pend_m[j]);
       bool ok = true;
@@ -353,7 +335,6 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
         }
         load_w(s);
         load_a(s, k, m0);
-        prefetch_one();
         ++it;
       }
       if (!ok) raise_error(p.err, DFLASH_DERR_TIMEOUT);
