@@ -204,6 +204,19 @@ int check_kv(const dflash_handle *h, const dflash_kv *kv) {
 
 }  // namespace
 
+namespace dflash {
+int handle_lm_head(const dflash_handle *h, const void **lm_head, int *hidden, int *vocab,
+                   int *dtype) {
+  if (!h) return DFLASH_EINVAL;
+  *lm_head = h->lm_head;
+  *hidden = h->cfg.hidden;
+  *vocab = h->cfg.vocab;
+  *dtype = h->cfg.dtype;
+  return DFLASH_OK;
+}
+void set_last_error(const char *msg) { g_last_error = msg; }
+}  // namespace dflash
+
 extern "C" {
 
 const char *dflash_status_string(int st) {

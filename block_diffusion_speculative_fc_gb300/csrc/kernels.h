@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/dflash.h"
+
 namespace dflash {
 
 enum StoreType { ST_F32 = 0, ST_BF16 = 1 };
@@ -139,5 +141,10 @@ cudaError_t launch_accept(int B, int S, int vocab, const int *draft, const int *
                           int *seq_len, int *accept_len, int *commit_len, int *bonus,
                           int *out_tokens, int *output_ids, int out_stride, unsigned int *err,
                           cudaStream_t s);
+
+// Host-side helpers implemented next to the handle (dflash_api.cu).
+int handle_lm_head(const dflash_handle *h, const void **lm_head, int *hidden, int *vocab,
+                   int *dtype);
+void set_last_error(const char *msg);
 
 }  // namespace dflash

@@ -264,6 +264,30 @@ int dflash_profile_enable(dflash_handle *h, int32_t max_records);
 int dflash_profile_disable(dflash_handle *h);
 int dflash_profile_collect(dflash_handle *h, dflash_profile_entry *out, int32_t cap, int32_t *n);
 
+/*
+ * Token selection that allocates nothing (no counterpart on the pages: it
+ * exists for callers that cannot give this library device memory, e.g. a
+ * plugin inside a serving engine whose caching allocator owns all device
+ * memory, or code that may not call cudaMalloc at all).
+ *   ids[r] = argmax_v <hidden[r], lm_head[v]>   (lowest id among equal maxima)
+ *   rows    1 .. 32
+ *   hidden  device [rows, hidden] in the configured dtype (bf16 only), e.g.
+ *           rows 1..S-1 of dflash_draft_block's hidden_out
+ *   ids     device int32 [rows]
+ * Needs a handle (host memory) but no bound workspace.  Its scratch (argmax
+ * keys, GEMM partial tiles and tickets, about 5.3 MB) is one static device
+ * array of the library, held by every GPU that loads it until the process
+ * exits.  The first call on a device sets that device up (looks up the
+ * array's address, sets kernel attributes, zeroes the tickets on `stream`):
+ * make that first call before any stream capture.  All calls share the one
+ * array, so calls that may overlap on the GPU (other streams, other threads)
+ * race; serialise them.  No cudaMalloc/cudaFree is made.
+ * Returns DFLASH_ECAPACITY for rows > 32 or vocab > 262144,
+ * DFLASH_EUNSUPPORTED for fp32 handles.
+ */
+int dflash_select_tokens_noalloc(dflash_handle *h, int32_t rows, const void *hidden, int32_t *ids,
+                                 dflash_stream_t stream);
+
 /* Static description of a status code. */
 const char *dflash_status_string(int status);
 
