@@ -282,9 +282,13 @@ class DraftContext:
     def inject(self, feats, W):
         cfg = self.cfg
         y_hat = project_target_hidden(feats, W["fc"], W["hidden_norm"], cfg.rms_eps)
+        self.append_projected(y_hat, W)
+        return y_hat
+
+    def append_projected(self, y_hat, W):
+        """Append rows whose fc + hidden_norm projection is already known."""
         pos = self.kv_len + np.arange(y_hat.shape[0], dtype=np.int64)
-        for l in range(cfg.n_layers):
-            k, v = context_kv(y_hat, W["layers"][l], pos, cfg)
+        for l in range(self.cfg.n_layers):
+            k, v = context_kv(y_hat, W["layers"][l], pos, self.cfg)
             self.k[l] = np.concatenate([self.k[l], k], axis=0)
             self.v[l] = np.concatenate([self.v[l], v], axis=0)
-        return y_hat

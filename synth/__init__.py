@@ -9,5 +9,5 @@ from .configs import DraftConfig, Workload, WORKLOADS, get_workload  # noqa: F40
 from .generate import (  # noqa: F401
     make_weights, make_features, make_context_lengths, make_page_table,
     make_posterior, make_posterior_with_commit, make_commit_lengths,
-    make_anchor, tensor_seed,
+    make_anchor, tensor_seed, make_pooled_features, make_match_probs,
 )

@@ -83,6 +83,16 @@ def make_features(cfg, rows, seed, tag, device="cpu"):
     return _normal((cfg.n_sel, rows, cfg.target_hidden), 1.0, cfg, device, seed, "feat", tag)
 
 
+def make_pooled_features(cfg, rows, pool, seed, tag, device="cpu"):
+    """Target features whose rows are drawn (seeded, uniformly) from `pool`
+    distinct N(0, 1) rows: [n_sel, rows, H_t] and the row -> pool index map.
+    Long contexts keep their full size on the device while a row-wise checker
+    only has to project each distinct row once."""
+    base = _normal((cfg.n_sel, pool, cfg.target_hidden), 1.0, cfg, device, seed, "pool", tag)
+    idx = _rng(seed, "pool_idx", tag).integers(0, pool, size=rows)
+    return base[:, torch.as_tensor(idx, device=device)], base, idx
+
+
 def make_context_lengths(wl, seed=0):
     kind = wl.context[0]
     B = wl.batch

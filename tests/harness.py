@@ -16,7 +16,7 @@ import torch
 import block_diffusion_speculative_fc_gb300 as pkg
 from oracle import dflash_oracle as O
 from synth import make_anchor, make_features, make_page_table, make_posterior, \
-    make_posterior_with_commit, make_commit_lengths, make_weights
+    make_posterior_with_commit, make_commit_lengths, make_weights, make_pooled_features
 
 MARGIN = 1e-2
 # A drafted id may differ from the oracle's only where the choice is within
@@ -51,8 +51,9 @@ def i32(a):
 class CycleRun:
     def __init__(self, cfg, batch, ctx_lens, cycles, seed=0, gains="unit", permuted=False,
                  check=None, match=("bernoulli", 0.85), tol=None, max_rows=None,
-                 extra_pages=2, W=None, Wn=None):
+                 extra_pages=2, W=None, Wn=None, pool=None):
         self.cfg, self.B, self.cycles, self.seed = cfg, batch, cycles, seed
+        self.pool = pool   # prefill rows drawn from this many distinct feature rows
         self.ctx_lens = np.asarray(ctx_lens, dtype=np.int64)
         self.check = list(range(batch)) if check is None else list(check)
         self.match = match
@@ -80,11 +81,26 @@ class CycleRun:
         cfg = self.cfg
         T = self.ctx_lens
         offs = np.concatenate([[0], np.cumsum(T)[:-1]])
-        feats = make_features(cfg, int(T.sum()), self.seed, "prefill", device="cuda")
+        if self.pool:
+            feats, base, idx = make_pooled_features(cfg, int(T.sum()), self.pool, self.seed,
+                                                    "prefill", device="cuda")
+        else:
+            feats = make_features(cfg, int(T.sum()), self.seed, "prefill", device="cuda")
         self.sess.inject(self.kv, feats, i32(offs), i32(T))
-        for b in self.check:
-            self.ctx[b].inject(self._feat_rows(feats, slice(int(offs[b]), int(offs[b] + T[b]))),
-                               self.Wn)
+        if self.pool:
+            # project each distinct row once; rows of a request are copies
+            y_pool = O.project_target_hidden(
+                [base[j].double().cpu().numpy() for j in range(cfg.n_sel)], self.Wn["fc"],
+                self.Wn["hidden_norm"], cfg.rms_eps)
+            del feats
+            for b in self.check:
+                rows = idx[int(offs[b]):int(offs[b] + T[b])]
+                self.ctx[b].append_projected(y_pool[rows], self.Wn)
+        else:
+            for b in self.check:
+                self.ctx[b].inject(self._feat_rows(feats, slice(int(offs[b]), int(offs[b] + T[b]))),
+                                   self.Wn)
+        torch.cuda.empty_cache()
         assert np.array_equal(self.kv.kv_len.cpu().numpy(), T)
         self.compare_kv()
 
