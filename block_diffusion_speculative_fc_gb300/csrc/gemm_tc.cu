@@ -56,6 +56,7 @@ struct Params {
   float *partials;                // [gridDim.x][2][P][BN][128]
   int *counters;                  // [tiles]
   unsigned int *err;
+  unsigned long long *trace;      // optional [gridDim.x][8] phase timestamps (ns), test builds only
 };
 
 // ------------------------------------------------------------------ PTX
@@ -158,6 +159,13 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
+__device__ __forceinline__ void stamp(const Params &p, int slot) {
+  if (p.trace) {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    p.trace[blockIdx.x * 8 + slot] = t;
+  }
+}
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 // Named-barrier AND-reduction over the 128 epilogue threads (uniform result).
 __device__ __forceinline__ bool epi_all(bool v) {
@@ -241,6 +249,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
   const int G = gridDim.x, cta = blockIdx.x;
   const Range R = cta_range(p.total_iters, G, cta);
 
+  if (threadIdx.x == 0) stamp(p, 0);
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::STAGES; ++i) {
       mbar_init(&full[i], 1);
@@ -262,6 +271,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (threadIdx.x == 0) stamp(p, 1);
 
   // tile -> (segment, feature tile, token tile)
   auto locate = [&](int tile, int &seg, int &n0, int &m0) {
@@ -324,7 +334,9 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
         pend_m[it] = m0;
         ++it;
       }
+      stamp(p, 2);
       pdl_wait();
+      stamp(p, 3);
       for (int j = 0; j < it; ++j) load_a(j, pend_k[j], pend_m[j]);
       bool ok = true;
       while (next()) {
@@ -367,6 +379,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
             ok = false;
             break;
           }
+          if (it == 0) stamp(p, 4);
           tc_fence_after();
           const uint32_t st = su32(stages + s * C::STAGE_BYTES);
           const uint64_t bdesc = sw128_desc(st + C::P * C::W_BYTES);
@@ -385,6 +398,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
       // every MMA issued by this thread must be complete before TMEM is freed
       umma_commit(mma_done);
       mbar_wait(mma_done, 0);
+      stamp(p, 5);
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -421,6 +435,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
         break;
       }
       tc_fence_after();
+      if (tid == 0 && seg_i == 0) stamp(p, 6);
       const uint32_t tacc = tmem + ((uint32_t)(quarter * 32) << 16) + buf * C::ACC_COLS;
       const bool whole = kb0 == 0 && kb1 == p.KB;
       if (whole) {
@@ -520,6 +535,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
       }
     }
   }
+  if (warp == EPI_WARP0 && lane == 0) stamp(p, 7);
   tc_fence_before();
   __syncthreads();
   pdl_trigger();   // every global write of this CTA is done
@@ -615,7 +631,7 @@ cudaError_t prepare_gemm_tc() {
 }
 
 cudaError_t launch_gemm_tc(const GemmProblem &P, float *partials, int *counters, int max_tiles,
-                           unsigned int *err, cudaStream_t s) {
+                           unsigned int *err, cudaStream_t s, unsigned long long *trace) {
   if (P.M <= 0 || P.nseg <= 0) return cudaSuccess;
   if (P.K % tc::BK) return cudaErrorInvalidValue;
   const bool pair = P.seg[0].epi.op == EPI_SWIGLU;
@@ -649,6 +665,7 @@ cudaError_t launch_gemm_tc(const GemmProblem &P, float *partials, int *counters,
   p.partials = partials;
   p.counters = counters;
   p.err = err;
+  p.trace = trace;
   const int G = (int)std::min<long long>(std::min(gemm_tc_num_sms(), kTcMaxCtas), p.total_iters);
   switch (BN | (pair ? 1 : 0)) {
     case 16: return launch_cfg<16, false>(p, G, s);

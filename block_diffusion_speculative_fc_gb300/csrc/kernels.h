@@ -107,7 +107,7 @@ constexpr int kTcMaxCtas = 160;   // persistent tensor-core GEMM grid cap (>= SM
 
 // ---- launchers (return cudaGetLastError()) ----
 cudaError_t launch_gemm_tc(const GemmProblem &P, float *partials, int *counters, int max_tiles,
-                           unsigned int *err, cudaStream_t s);
+                           unsigned int *err, cudaStream_t s, unsigned long long *trace = nullptr);
 size_t gemm_tc_partials_bytes();
 int gemm_tc_tiles(int n_tiles, int M, bool pair);
 cudaError_t prepare_gemm_tc();

@@ -15,6 +15,15 @@ extern "C" int dflash_test_gemm(int32_t M, int32_t N, int32_t K, int32_t n_src,
                                 const void *const *A, int32_t lda, const void *W, int32_t ldw,
                                 int32_t op, void *out, void *act_out, void *scratch,
                                 size_t scratch_bytes, dflash_stream_t stream) {
+  return dflash_test_gemm_traced(M, N, K, n_src, A, lda, W, ldw, op, out, act_out, scratch,
+                                 scratch_bytes, nullptr, stream);
+}
+
+extern "C" int dflash_test_gemm_traced(int32_t M, int32_t N, int32_t K, int32_t n_src,
+                                       const void *const *A, int32_t lda, const void *W,
+                                       int32_t ldw, int32_t op, void *out, void *act_out,
+                                       void *scratch, size_t scratch_bytes,
+                                       unsigned long long *trace, dflash_stream_t stream) {
   if (M <= 0 || N <= 0 || K <= 0 || n_src <= 0 || n_src > kMaxSrc || !A || !W || !scratch)
     return DFLASH_EINVAL;
   if (K % n_src || (K / n_src) % 64) return DFLASH_EUNSUPPORTED;
@@ -50,6 +59,6 @@ extern "C" int dflash_test_gemm(int32_t M, int32_t N, int32_t K, int32_t n_src,
   if (cudaMemsetAsync(base, 0, 256, s) != cudaSuccess) return DFLASH_ECUDA;
   if (cudaMemsetAsync(counters, 0, 4 * (size_t)tiles, s) != cudaSuccess) return DFLASH_ECUDA;
   if (prepare_gemm_tc() != cudaSuccess) return DFLASH_ECUDA;
-  if (launch_gemm_tc(P, partials, counters, tiles, err, s) != cudaSuccess) return DFLASH_ECUDA;
+  if (launch_gemm_tc(P, partials, counters, tiles, err, s, trace) != cudaSuccess) return DFLASH_ECUDA;
   return DFLASH_OK;
 }

@@ -29,6 +29,17 @@ int dflash_test_gemm(int32_t M, int32_t N, int32_t K, int32_t n_src, const void 
                      int32_t lda, const void *W, int32_t ldw, int32_t op, void *out,
                      void *act_out, void *scratch, size_t scratch_bytes, dflash_stream_t stream);
 
+/* As dflash_test_gemm; when trace is non-NULL each CTA of the (persistent)
+ * GEMM writes 8 %globaltimer stamps (ns) to trace[cta * 8 + slot]: 0 entry,
+ * 1 set-up done, 2 weight ring issued, 3 predecessor wait returned, 4 first
+ * stage consumed by the MMA warp, 5 last MMA complete, 6 first accumulator
+ * received by the epilogue, 7 epilogue done.  Caller provides
+ * 8 * (number of SMs) slots (the grid never exceeds 160 CTAs). */
+int dflash_test_gemm_traced(int32_t M, int32_t N, int32_t K, int32_t n_src, const void *const *A,
+                            int32_t lda, const void *W, int32_t ldw, int32_t op, void *out,
+                            void *act_out, void *scratch, size_t scratch_bytes,
+                            unsigned long long *trace, dflash_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
