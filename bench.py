@@ -86,6 +86,10 @@ def algorithmic(cfg, B, ctx_mean, commit_mean):
                            2 * rows * cfg.n_layers * 2 * kvd * H),
         "accept": (4 * (2 * B * S + B * (S + 4)), 0),
     }
+    add = lambda *names: tuple(sum(fam[n][i] for n in names) for i in range(2))  # noqa: E731
+    fam["gemm_layer_program"] = add("gemm_o", "gemm_gate_up", "gemm_down", "gemm_qkv")
+    fam["gemm_last_program"] = add("gemm_o", "gemm_gate_up", "gemm_down", "gemm_lm_head_argmax")
+    fam["gemm_inject_program"] = add("gemm_fc", "gemm_kv_inject")
     return fam
 
 

@@ -23,7 +23,7 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct Layout {
   size_t err, rope, x, h, xg, ssq, qb, kb, vb, attn, act, row_pos, keys, yg, ssq_y, slot, rpos;
-  size_t tc_partials, tc_counters;
+  size_t tc_partials, tc_counters, tc_grid_bar;
   int tc_max_tiles;
   size_t att_item_start, att_pps, att_part_o, att_part_ml, att_tickets;
   int att_bg;
@@ -95,9 +95,10 @@ Layout plan(const dflash_config &c, size_t es) {
     mt = std::max(mt, gemm_tc_tiles(t128(c.vocab), Mb, false));
     mt = std::max(mt, gemm_tc_tiles(t128(H), Mr, false));
     mt = std::max(mt, gemm_tc_tiles(std::min(c.n_layers, kMaxSeg) * t128(2LL * c.n_kv_heads * D), Mr, false));
-    L.tc_max_tiles = mt;
+    L.tc_max_tiles = kMaxPhases * mt;   // tickets of every phase of a fused launch
     L.tc_partials = take(gemm_tc_partials_bytes());
-    L.tc_counters = take(4 * (size_t)mt);
+    L.tc_counters = take(4 * (size_t)L.tc_max_tiles);
+    L.tc_grid_bar = take(8);
     // attention split scratch
     const size_t R = (size_t)(c.n_heads / c.n_kv_heads) * c.block_size;
     const size_t items = attention_mma_scratch_items(c.max_batch, c.n_kv_heads);
@@ -136,6 +137,21 @@ cudaError_t run_gemm(dflash_handle *h, const GemmProblem &P, cudaStream_t s) {
   if (h->store == ST_F32) return launch_gemm_simt(ST_F32, P, s);
   return launch_gemm_tc(P, at<float>(h, h->L.tc_partials), at<int>(h, h->L.tc_counters),
                         h->L.tc_max_tiles, at<unsigned int>(h, h->L.err), s);
+}
+
+// Dependent GEMMs of equal row count in one launch (bf16); fp32 runs them one
+// after the other on the CUDA cores.
+cudaError_t run_program(dflash_handle *h, const GemmProblem *P, int n, cudaStream_t s) {
+  if (h->store == ST_F32) {
+    for (int i = 0; i < n; ++i) {
+      const cudaError_t e = launch_gemm_simt(ST_F32, P[i], s);
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+  }
+  return launch_gemm_program(P, n, at<float>(h, h->L.tc_partials), at<int>(h, h->L.tc_counters),
+                             h->L.tc_max_tiles, at<unsigned int>(h, h->L.tc_grid_bar),
+                             at<unsigned int>(h, h->L.err), s);
 }
 
 cudaError_t run_attention(dflash_handle *h, const AttnParams &a, cudaStream_t s) {
@@ -367,6 +383,9 @@ int dflash_bind_workspace(dflash_handle *h, void *dev_ptr, size_t bytes, dflash_
       (st = check_cuda(cudaMemsetAsync(h->ws + h->L.tc_counters, 0, 4 * (size_t)h->L.tc_max_tiles, s),
                        "clear GEMM tickets")))
     return st;
+  if (h->L.tc_max_tiles > 0 &&
+      (st = check_cuda(cudaMemsetAsync(h->ws + h->L.tc_grid_bar, 0, 8, s), "clear grid barrier")))
+    return st;
   if (h->L.att_bg > 0 &&
       (st = check_cuda(cudaMemsetAsync(h->ws + h->L.att_tickets, 0, 4 * (size_t)h->L.att_bg, s),
                        "clear attention tickets")))
@@ -426,7 +445,8 @@ int dflash_inject_context(dflash_handle *h, const dflash_kv *kv, int32_t batch, 
     if (st) return st;
     // a1 + a2: concat (K-split over the selected layers) + fc; the epilogue
     // writes y * hidden_norm gain and the row sums of squares of y
-    GemmProblem P;
+    GemmProblem prog[2];
+    GemmProblem &P = prog[0];
     std::memset(&P, 0, sizeof(P));
     for (int j = 0; j < c.n_sel; ++j)
       P.A.ptr[j] = (const char *)target_feats[j] + (size_t)r0 * c.target_hidden * h->es;
@@ -443,9 +463,8 @@ int dflash_inject_context(dflash_handle *h, const dflash_kv *kv, int32_t batch, 
     e.ssq_out = ssq_y;
     e.ssq_ld = c.max_rows;
     add_seg(P, h->fc_w, P.K, H, e);
-    if ((st = timed(h, "gemm_fc", s, [&] { return run_gemm(h, P, s); }))) return st;
     // a3: every layer's K/V projection of hidden_norm(y) + k-norm + RoPE + paged scatter
-    for (int l0 = 0; l0 < c.n_layers; l0 += kMaxSeg) {
+    auto kv_problem = [&](int l0) {
       GemmProblem Q = problem_1src(yg, H, rows, H);
       for (int l = l0; l < std::min(c.n_layers, l0 + kMaxSeg); ++l) {
         EpiParams k = epi_base(h, EPI_KV_CACHE);
@@ -459,6 +478,14 @@ int dflash_inject_context(dflash_handle *h, const dflash_kv *kv, int32_t batch, 
         set_norm_in(h, k, ssq_y, c.max_rows);
         add_seg(Q, (const char *)h->qkv_w[l] + (size_t)q_rows * H * h->es, H, 2 * kvd, k);
       }
+      return Q;
+    };
+    prog[1] = kv_problem(0);
+    // fc and the first group of layers' K/V in one launch
+    if ((st = timed(h, "gemm_inject_program", s, [&] { return run_program(h, prog, 2, s); })))
+      return st;
+    for (int l0 = kMaxSeg; l0 < c.n_layers; l0 += kMaxSeg) {
+      GemmProblem Q = kv_problem(l0);
       if ((st = timed(h, "gemm_kv_inject", s, [&] { return run_gemm(h, Q, s); }))) return st;
     }
   }
@@ -501,8 +528,8 @@ int dflash_draft_block(dflash_handle *h, const dflash_kv *kv, int32_t batch, con
                              row_pos, keys, err, s);
        })))
     return st;
-  for (int l = 0; l < c.n_layers; ++l) {
-    // a5: RMSNorm + QKV GEMM + q/k-norm + RoPE
+  // a5 of layer l: RMSNorm + QKV GEMM + q/k-norm + RoPE
+  auto qkv_problem = [&](int l) {
     GemmProblem P = problem_1src(xg, H, M, H);
     EpiParams e = epi_base(h, EPI_QKV);
     e.N = qd + 2 * kvd;
@@ -515,7 +542,13 @@ int dflash_draft_block(dflash_handle *h, const dflash_kv *kv, int32_t batch, con
     e.rope = rope;
     set_norm_in(h, e, ssq, ldq);
     add_seg(P, h->qkv_w[l], H, qd + 2 * kvd, e);
+    return P;
+  };
+  {
+    GemmProblem P = qkv_problem(0);
     if ((st = timed(h, "gemm_qkv", s, [&] { return run_gemm(h, P, s); }))) return st;
+  }
+  for (int l = 0; l < c.n_layers; ++l) {
     // a6: non-causal block attention over [context ; block]
     AttnParams a;
     std::memset(&a, 0, sizeof(a));
@@ -539,8 +572,12 @@ int dflash_draft_block(dflash_handle *h, const dflash_kv *kv, int32_t batch, con
     a.scale = 1.0f / sqrtf((float)D);
     a.err = err;
     if ((st = timed(h, "attention", s, [&] { return run_attention(h, a, s); }))) return st;
-    // a7: O projection + residual (+ deferred post-attention RMSNorm)
-    GemmProblem O = problem_1src(attn, qd, M, qd);
+    // One launch for the rest of the layer and the start of the next:
+    // a7 O-proj + residual (+ deferred post-attention norm), a8 gate/up with
+    // SwiGLU, down + residual (+ deferred next norm), then the next layer's
+    // QKV (a5) or, after the last layer, the lm_head with argmax (a9).
+    GemmProblem prog[4];
+    prog[0] = problem_1src(attn, qd, M, qd);
     EpiParams eo = epi_base(h, EPI_RESID_NORM);
     eo.N = H;
     eo.ld = H;
@@ -549,18 +586,15 @@ int dflash_draft_block(dflash_handle *h, const dflash_kv *kv, int32_t batch, con
     eo.norm_gain = h->post_norm_g[l];
     eo.ssq_out = ssq;
     eo.ssq_ld = ldq;
-    add_seg(O, h->o_w[l], qd, H, eo);
-    if ((st = timed(h, "gemm_o", s, [&] { return run_gemm(h, O, s); }))) return st;
-    // a8: RMSNorm + gate/up GEMM with SwiGLU + down GEMM + residual
-    GemmProblem G = problem_1src(xg, H, M, H);
+    add_seg(prog[0], h->o_w[l], qd, H, eo);
+    prog[1] = problem_1src(xg, H, M, H);
     EpiParams eg = epi_base(h, EPI_SWIGLU);
     eg.N = 2 * c.intermediate;
     eg.ld = c.intermediate;
     eg.out_act = act;
     set_norm_in(h, eg, ssq, ldq);
-    add_seg(G, h->gate_up_w[l], H, 2 * c.intermediate, eg);
-    if ((st = timed(h, "gemm_gate_up", s, [&] { return run_gemm(h, G, s); }))) return st;
-    GemmProblem Dn = problem_1src(act, c.intermediate, M, c.intermediate);
+    add_seg(prog[1], h->gate_up_w[l], H, 2 * c.intermediate, eg);
+    prog[2] = problem_1src(act, c.intermediate, M, c.intermediate);
     EpiParams ed = epi_base(h, EPI_RESID_NORM);
     ed.N = H;
     ed.ld = H;
@@ -569,25 +603,31 @@ int dflash_draft_block(dflash_handle *h, const dflash_kv *kv, int32_t batch, con
     ed.norm_gain = l + 1 < c.n_layers ? h->in_norm_g[l + 1] : h->final_norm_g;
     ed.ssq_out = ssq;
     ed.ssq_ld = ldq;
-    add_seg(Dn, h->down_w[l], c.intermediate, H, ed);
-    if ((st = timed(h, "gemm_down", s, [&] { return run_gemm(h, Dn, s); }))) return st;
+    add_seg(prog[2], h->down_w[l], c.intermediate, H, ed);
+    if (l + 1 < c.n_layers) {
+      prog[3] = qkv_problem(l + 1);
+      if ((st = timed(h, "gemm_layer_program", s, [&] { return run_program(h, prog, 4, s); })))
+        return st;
+    } else {
+      // a9: lm_head + argmax (logits never stored).  The argmax of a row is
+      // unchanged by the row's positive RMSNorm scale, so the lm_head runs on
+      // x * final gain directly.
+      prog[3] = problem_1src(xg, H, M, H);
+      EpiParams ea = epi_base(h, EPI_ARGMAX);
+      ea.N = c.vocab;
+      ea.argmax_keys = keys;
+      add_seg(prog[3], h->lm_head, H, c.vocab, ea);
+      if ((st = timed(h, "gemm_last_program", s, [&] { return run_program(h, prog, 4, s); })))
+        return st;
+    }
   }
-  // a9: final norm + lm_head + argmax (logits never stored).  The argmax of a
-  // row is unchanged by the row's positive RMSNorm scale, so the lm_head runs
-  // on x * final gain directly; the normalised hidden states are only formed
-  // when the caller asks for them.
+  // the normalised hidden states are formed only when the caller asks for them
   if (hidden_out &&
       (st = timed(h, "rmsnorm_hidden_out", s, [&] {
          return launch_rmsnorm(1, h->store, x, h->final_norm_g, M, H, c.rms_eps, hidden_out,
                                nullptr, s);
        })))
     return st;
-  GemmProblem P = problem_1src(xg, H, M, H);
-  EpiParams e = epi_base(h, EPI_ARGMAX);
-  e.N = c.vocab;
-  e.argmax_keys = keys;
-  add_seg(P, h->lm_head, H, c.vocab, e);
-  if ((st = timed(h, "gemm_lm_head_argmax", s, [&] { return run_gemm(h, P, s); }))) return st;
   return timed(h, "argmax_finalize", s,
                [&] { return launch_argmax_finalize(keys, anchor, batch, S, draft_ids, s); });
 }

@@ -11,15 +11,22 @@
 //
 // Structure (one CTA per SM, persistent):
 //   warp 0      TMA producer: W and A tiles (128B-swizzled, K-major) into a
-//               ring of shared-memory stages, mbarrier transaction counts.
+//               ring of shared-memory slots (one k-block of one 128-row weight
+//               tile plus its activation tile; a paired gate/up k-block uses
+//               two consecutive slots), mbarrier transaction counts.
 //   warp 1      TMEM allocator and MMA issuer: tcgen05.mma kind::f16 (bf16 in,
 //               fp32 accumulate), tcgen05.commit frees a stage / publishes an
 //               accumulator.  Two accumulator buffers let the epilogue of one
 //               tile overlap the MMAs of the next.
 //   warps 2..5  epilogue: tcgen05.ld to registers, shared-memory staging, the
 //               shared epilogue ops (norm/RoPE/scatter, SwiGLU, argmax, ...).
-// Work split (stream-K): the flattened (tile, k-block) iteration space is cut
-// into gridDim.x equal contiguous ranges.  A tile covered by one CTA is
+// A launch runs a *program* of up to kMaxPhases dependent GEMMs (e.g. O-proj,
+// gate/up, down, the next layer's QKV): between phases all CTAs meet at a
+// grid barrier (the launch is cooperative, so every CTA is resident), and the
+// producer streams the next phase's weights into free ring slots before it
+// waits -- the weight stream does not stop at a GEMM boundary.
+// Work split (stream-K): per phase, the flattened (tile, k-block) iteration
+// space is cut into gridDim.x equal contiguous ranges.  A tile covered by one CTA is
 // finished directly; a tile shared by several CTAs has each write an fp32
 // partial, and the last to arrive (atomic ticket, no waiting on other CTAs)
 // sums the partials in CTA order -- a fixed order, so results are
@@ -43,18 +50,26 @@ constexpr int THREADS = 192;
 constexpr int EPI_WARP0 = 2;
 constexpr uint32_t WAIT_LIMIT = 1u << 22;
 
-struct Params {
+// One GEMM of a program: its operands, epilogues and stream-K schedule.
+struct Phase {
   CUtensorMap tmA[kMaxSrc];       // activations, box {BK, BN}
   CUtensorMap tmW[kMaxSeg];       // weights, box {BK, 128}
   EpiParams epi[kMaxSeg];
   int seg_ntiles[kMaxSeg];        // 128-feature tiles per segment (pairs count once)
   int seg_half[kMaxSeg];          // pair: row offset of the "up" half
-  int nseg;
+  int nseg, pair;
   int M, K, KB, m_tiles, tiles;
   int k_per_src;
+  int counter_off;                // this phase's tickets start here
   long long total_iters;
-  float *partials;                // [gridDim.x][2][P][BN][128]
-  int *counters;                  // [tiles]
+};
+
+struct Params {
+  Phase ph[kMaxPhases];
+  int nph;
+  float *partials;                // [gridDim.x][2][<= 2*BN][128]
+  int *counters;                  // tickets of every phase, zero between launches
+  unsigned int *grid_bar;         // [2] phase arrivals, exits; zero between launches
   unsigned int *err;
   unsigned long long *trace;      // optional [gridDim.x][8] phase timestamps (ns), test builds only
 };
@@ -209,49 +224,65 @@ __device__ __forceinline__ int cta_of_iter(long long it, long long total, int G)
   return (int)(((it + 1) * G - 1) / total);
 }
 
-template <int BN, bool PAIR>
+template <int BN, bool PAIRABLE>
 struct Cfg {
-  static constexpr int P = PAIR ? 2 : 1;
+  static constexpr int P = PAIRABLE ? 2 : 1;              // accumulators per tile
   static constexpr int W_BYTES = 128 * BK * 2;
   static constexpr int A_BYTES = BN * BK * 2;
-  static constexpr int STAGE_BYTES = P * W_BYTES + A_BYTES;
-  static constexpr int CH = BN < 32 ? BN : 32;          // epilogue token chunk
+  static constexpr int SLOT_BYTES = W_BYTES + A_BYTES;
+  static constexpr int CH = BN < 32 ? BN : 32;            // epilogue token chunk
   static constexpr int STAGING_BYTES = P * CH * 128 * 4;
-  static constexpr int BAR_BYTES = 768 + 1024;   // mbarriers, TMEM slot, flag, epilogue scratch, row scales
+  static constexpr int BAR_BYTES = 2048;   // mbarriers, TMEM slot, flag, epilogue scratch, row scales
   static constexpr int BUDGET = 225 * 1024;
-  static constexpr int STAGES_RAW = (BUDGET - 1024 - STAGING_BYTES - BAR_BYTES) / STAGE_BYTES;
-  static constexpr int STAGES = STAGES_RAW > 12 ? 12 : STAGES_RAW;
-  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + STAGING_BYTES + BAR_BYTES;
-  static constexpr int ACC_COLS = P * BN;                // one accumulator buffer
+  static constexpr int SLOTS_RAW = (BUDGET - 1024 - STAGING_BYTES - BAR_BYTES) / SLOT_BYTES;
+  static constexpr int SLOTS = SLOTS_RAW > 24 ? 24 : SLOTS_RAW;
+  static constexpr int SMEM = 1024 + SLOTS * SLOT_BYTES + STAGING_BYTES + BAR_BYTES;
+  static constexpr int ACC_COLS = P * BN;                 // one accumulator buffer
   static constexpr int TMEM_COLS = 2 * ACC_COLS <= 32 ? 32 : (2 * ACC_COLS <= 64 ? 64 :
                                    (2 * ACC_COLS <= 128 ? 128 : (2 * ACC_COLS <= 256 ? 256 : 512)));
-  static_assert(STAGES >= 2, "not enough shared memory for two stages");
+  static_assert(SLOTS >= 4, "a paired k-block needs two slots and two k-blocks must fit");
   static_assert(2 * ACC_COLS <= 512, "accumulators exceed TMEM");
+  static_assert(2 * SLOTS * 8 + 5 * 8 + 8 <= 512, "barrier region");
 };
 
-template <int BN, bool PAIR, typename T>
+// Bounded acquire-spin on a grid barrier word; false = gave up.
+__device__ __forceinline__ bool grid_wait(const unsigned int *bar, unsigned int target) {
+  for (uint32_t i = 0; i < 4 * WAIT_LIMIT; ++i) {
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(bar) : "memory");
+    if (v >= target) return true;
+    __nanosleep(100);
+  }
+  return false;
+}
+// Later bulk-async (TMA) reads must observe what generic stores made visible.
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+template <int BN, bool PAIRABLE, typename T>
 __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_constant__ Params p) {
-  using C = Cfg<BN, PAIR>;
+  using C = Cfg<BN, PAIRABLE>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  uint8_t *stages = smem;
-  float *staging = (float *)(smem + C::STAGES * C::STAGE_BYTES);
-  uint64_t *bars = (uint64_t *)(smem + C::STAGES * C::STAGE_BYTES + C::STAGING_BYTES);
-  uint64_t *full = bars, *empty = bars + C::STAGES;
-  uint64_t *acc_full = bars + 2 * C::STAGES, *acc_empty = acc_full + 2;
+  uint8_t *slots = smem;
+  float *staging = (float *)(smem + C::SLOTS * C::SLOT_BYTES);
+  uint8_t *barbase = smem + C::SLOTS * C::SLOT_BYTES + C::STAGING_BYTES;
+  uint64_t *bars = (uint64_t *)barbase;
+  uint64_t *full = bars, *empty = bars + C::SLOTS;
+  uint64_t *acc_full = bars + 2 * C::SLOTS, *acc_empty = acc_full + 2;
   uint64_t *mma_done = acc_empty + 2;
-  uint32_t *tmem_slot = (uint32_t *)(mma_done + 1);
-  int *flag = (int *)(tmem_slot + 1);
-  int *s_int = (int *)((uint8_t *)bars + 256);   // kEpiScratchInts ints
-  float *s_rstd = (float *)((uint8_t *)bars + 768);   // [BN] deferred-norm row scales
+  uint32_t *tmem_slot = (uint32_t *)(barbase + 496);
+  int *flag = (int *)(barbase + 500);
+  int *s_int = (int *)(barbase + 512);        // kEpiScratchInts ints
+  float *s_rstd = (float *)(barbase + 1024);  // [BN] deferred-norm row scales
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x, cta = blockIdx.x;
-  const Range R = cta_range(p.total_iters, G, cta);
 
   if (threadIdx.x == 0) stamp(p, 0);
   if (threadIdx.x == 0) {
-    for (int i = 0; i < C::STAGES; ++i) {
+    for (int i = 0; i < C::SLOTS; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
     }
@@ -264,8 +295,11 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
   }
   if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
   if (warp == 0 && lane == 0) {
-    for (int i = 0; i < p.nseg; ++i) prefetch_tmap(&p.tmW[i]);
-    for (int i = 0; i < kMaxSrc && i * p.k_per_src < p.K; ++i) prefetch_tmap(&p.tmA[i]);
+    for (int k = 0; k < p.nph; ++k) {
+      for (int i = 0; i < p.ph[k].nseg; ++i) prefetch_tmap(&p.ph[k].tmW[i]);
+      for (int i = 0; i < kMaxSrc && i * p.ph[k].k_per_src < p.ph[k].K; ++i)
+        prefetch_tmap(&p.ph[k].tmA[i]);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -273,12 +307,12 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
   const uint32_t tmem = *tmem_slot;
   if (threadIdx.x == 0) stamp(p, 1);
 
-  // tile -> (segment, feature tile, token tile)
-  auto locate = [&](int tile, int &seg, int &n0, int &m0) {
-    int nt = tile / p.m_tiles;
-    m0 = (tile % p.m_tiles) * BN;
+  // tile -> (segment, feature tile, token tile) within a phase
+  auto locate = [&](const Phase &ph, int tile, int &seg, int &n0, int &m0) {
+    int nt = tile / ph.m_tiles;
+    m0 = (tile % ph.m_tiles) * BN;
     seg = 0;
-    while (seg < p.nseg - 1 && nt >= p.seg_ntiles[seg]) nt -= p.seg_ntiles[seg++];
+    while (seg < ph.nseg - 1 && nt >= ph.seg_ntiles[seg]) nt -= ph.seg_ntiles[seg++];
     n0 = nt * 128;
   };
 
@@ -286,113 +320,129 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first(), pol_a = policy_evict_last();
-      // walk this CTA's (tile, k-block) range incrementally: one division up
-      // front, a tile lookup only when the tile changes
-      struct Walker {
-        long long left;
-        int tile, kb, seg, n0, m0, k;
-      };
-      auto start = [&](Walker &w, long long at) {
-        w.left = R.e - at;
-        w.tile = (int)(at / p.KB);
-        w.kb = (int)(at % p.KB) - 1;
-        locate(w.tile, w.seg, w.n0, w.m0);
-      };
-      auto advance = [&](Walker &w) -> bool {
-        if (w.left <= 0) return false;
-        --w.left;
-        if (++w.kb == p.KB) {
-          w.kb = 0;
-          ++w.tile;
-          locate(w.tile, w.seg, w.n0, w.m0);
-        }
-        w.k = w.kb * BK;
-        return true;
-      };
-      Walker ld;
-      start(ld, R.b);
-      int &seg = ld.seg, &n0 = ld.n0, &m0 = ld.m0, &k = ld.k;
-      auto next = [&]() -> bool { return advance(ld); };
-      auto load_w = [&](int s) {
-        uint8_t *st = stages + s * C::STAGE_BYTES;
-        mbar_expect_tx(&full[s], C::STAGE_BYTES);
-        tma_load_2d(st, &p.tmW[seg], &full[s], k, n0, pol_w);
-        if (PAIR) tma_load_2d(st + C::W_BYTES, &p.tmW[seg], &full[s], k, p.seg_half[seg] + n0, pol_w);
-      };
-      auto load_a = [&](int s, int kk, int mm) {
-        const int src = kk / p.k_per_src;
-        tma_load_2d(stages + s * C::STAGE_BYTES + C::P * C::W_BYTES, &p.tmA[src], &full[s],
-                    kk - src * p.k_per_src, mm, pol_a);
-      };
-      // Weights do not depend on the previous kernel: fill the whole ring with
-      // them first, then wait for the predecessor and add the activations.
-      int it = 0;
-      int pend_k[C::STAGES], pend_m[C::STAGES];
-      while (it < C::STAGES && next()) {
-        load_w(it);
-        pend_k[it] = k;
-        pend_m[it] = m0;
-        ++it;
-      }
-      stamp(p, 2);
-      pdl_wait();
-      stamp(p, 3);
-      for (int j = 0; j < it; ++j) load_a(j, pend_k[j], pend_m[j]);
+      uint32_t it = 0;   // slot uses so far
       bool ok = true;
-      while (next()) {
-        const int s = it % C::STAGES;
-        if (!mbar_wait(&empty[s], ((it / C::STAGES) & 1) ^ 1)) {
-          ok = false;
-          break;
+      int pend_s[C::SLOTS], pend_k[C::SLOTS], pend_m[C::SLOTS];
+      for (int ph_i = 0; ph_i < p.nph && ok; ++ph_i) {
+        const Phase &ph = p.ph[ph_i];
+        const Range R = cta_range(ph.total_iters, G, cta);
+        auto load_a = [&](int s, int kk, int mm) {
+          const int src = kk / ph.k_per_src;
+          tma_load_2d(slots + s * C::SLOT_BYTES + C::W_BYTES, &ph.tmA[src], &full[s],
+                      kk - src * ph.k_per_src, mm, pol_a);
+        };
+        // The weights never depend on earlier work: they go out as soon as a
+        // slot is free.  Activations wait for this phase's inputs (the
+        // previous kernel, or every CTA's previous phase).
+        bool ready = false;
+        int npend = 0;
+        auto make_ready = [&]() {
+          if (ph_i == 0) {
+            stamp(p, 2);
+            pdl_wait();
+            stamp(p, 3);
+          } else if (!grid_wait(p.grid_bar, (unsigned)(ph_i * G))) {
+            ok = false;
+          }
+          fence_proxy_async();
+          for (int j = 0; j < npend; ++j) load_a(pend_s[j], pend_k[j], pend_m[j]);
+          npend = 0;
+          ready = true;
+        };
+        const int ns = ph.pair ? 2 : 1;
+        long long left = R.e - R.b;
+        int tile = (int)(R.b / ph.KB), kb = (int)(R.b % ph.KB) - 1;
+        int seg = 0, n0 = 0, m0 = 0;
+        if (left > 0) locate(ph, tile, seg, n0, m0);
+        while (left > 0 && ok) {
+          --left;
+          if (++kb == ph.KB) {
+            kb = 0;
+            ++tile;
+            locate(ph, tile, seg, n0, m0);
+          }
+          const int k = kb * BK;
+          for (int j = 0; j < ns && ok; ++j) {
+            const uint32_t u = it + j;
+            const uint32_t par = ((u / C::SLOTS) & 1) ^ 1;
+            if (!ready && !mbar_try(&empty[u % C::SLOTS], par)) make_ready();
+            if (!mbar_wait(&empty[u % C::SLOTS], par)) ok = false;
+          }
+          if (!ok) break;
+          const int s0 = it % C::SLOTS, s1 = (it + 1) % C::SLOTS;
+          mbar_expect_tx(&full[s0], ns * C::W_BYTES + C::A_BYTES);
+          tma_load_2d(slots + s0 * C::SLOT_BYTES, &ph.tmW[seg], &full[s0], k, n0, pol_w);
+          if (ns == 2) {
+            tma_load_2d(slots + s1 * C::SLOT_BYTES, &ph.tmW[seg], &full[s0], k,
+                        ph.seg_half[seg] + n0, pol_w);
+            mbar_arrive(&full[s1]);   // keeps the second slot's phase count in step
+          }
+          if (ready) {
+            load_a(s0, k, m0);
+          } else {
+            pend_s[npend] = s0;
+            pend_k[npend] = k;
+            pend_m[npend] = m0;
+            ++npend;
+          }
+          it += ns;
         }
-        load_w(s);
-        load_a(s, k, m0);
-        ++it;
+        if (ok && !ready) make_ready();
       }
       if (!ok) raise_error(p.err, DFLASH_DERR_TIMEOUT);
       // drain: no TMA write may still be in flight when the CTA winds down
-      for (int j = 0; j < C::STAGES && j < it; ++j) {
-        const int q = it - 1 - j;
-        mbar_wait(&full[q % C::STAGES], (q / C::STAGES) & 1);
+      for (uint32_t j = 0; j < (uint32_t)C::SLOTS && j < it; ++j) {
+        const uint32_t q = it - 1 - j;
+        mbar_wait(&full[q % C::SLOTS], (q / C::SLOTS) & 1);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16(128, BN);
-      int it = 0, seg_i = 0;
+      uint32_t it = 0;
+      int seg_i = 0;
       bool ok = true;
-      for (long long i = R.b; i < R.e && ok; ++seg_i) {
-        const int kb0 = (int)(i % p.KB);
-        const int kb1 = (int)(kb0 + (R.e - i) < p.KB ? kb0 + (R.e - i) : p.KB);
-        const int buf = seg_i & 1;
-        const uint32_t aph = (seg_i >> 1) & 1;
-        if (!mbar_wait(&acc_empty[buf], aph ^ 1)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t d0 = tmem + buf * C::ACC_COLS;
-        for (int kb = kb0; kb < kb1; ++kb, ++it) {
-          const int s = it % C::STAGES;
-          if (!mbar_wait(&full[s], (it / C::STAGES) & 1)) {
+      for (int ph_i = 0; ph_i < p.nph && ok; ++ph_i) {
+        const Phase &ph = p.ph[ph_i];
+        const Range R = cta_range(ph.total_iters, G, cta);
+        const int ns = ph.pair ? 2 : 1;
+        for (long long i = R.b; i < R.e && ok; ++seg_i) {
+          const int kb0 = (int)(i % ph.KB);
+          const int kb1 = (int)(kb0 + (R.e - i) < ph.KB ? kb0 + (R.e - i) : ph.KB);
+          const int buf = seg_i & 1;
+          const uint32_t aph = (seg_i >> 1) & 1;
+          if (!mbar_wait(&acc_empty[buf], aph ^ 1)) {
             ok = false;
             break;
           }
-          if (it == 0) stamp(p, 4);
           tc_fence_after();
-          const uint32_t st = su32(stages + s * C::STAGE_BYTES);
-          const uint64_t bdesc = sw128_desc(st + C::P * C::W_BYTES);
+          const uint32_t d0 = tmem + buf * C::ACC_COLS;
+          for (int kb = kb0; kb < kb1; ++kb) {
+            const int s0 = it % C::SLOTS, s1 = (it + 1) % C::SLOTS;
+            if (!mbar_wait(&full[s0], (it / C::SLOTS) & 1)) {
+              ok = false;
+              break;
+            }
+            if (it == 0) stamp(p, 4);
+            tc_fence_after();
+            const uint32_t st0 = su32(slots + s0 * C::SLOT_BYTES);
+            const uint64_t adesc = sw128_desc(st0 + C::W_BYTES);
+            const uint64_t wdesc0 = sw128_desc(st0);
+            const uint64_t wdesc1 = sw128_desc(su32(slots + s1 * C::SLOT_BYTES));
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
-            umma_bf16(d0, sw128_desc(st) + 2 * kk, bdesc + 2 * kk, idesc, acc);
-            if (PAIR) umma_bf16(d0 + BN, sw128_desc(st + C::W_BYTES) + 2 * kk, bdesc + 2 * kk, idesc, acc);
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
+              umma_bf16(d0, wdesc0 + 2 * kk, adesc + 2 * kk, idesc, acc);
+              if (ns == 2) umma_bf16(d0 + BN, wdesc1 + 2 * kk, adesc + 2 * kk, idesc, acc);
+            }
+            umma_commit(&empty[s0]);
+            if (ns == 2) umma_commit(&empty[s1]);
+            it += ns;
           }
-          umma_commit(&empty[s]);
+          umma_commit(&acc_full[buf]);
+          i += kb1 - kb0;
         }
-        umma_commit(&acc_full[buf]);
-        i += kb1 - kb0;
       }
       if (!ok) raise_error(p.err, DFLASH_DERR_TIMEOUT);
       // every MMA issued by this thread must be complete before TMEM is freed
@@ -402,142 +452,170 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    pdl_wait();                                      // reads the predecessor's outputs
     const int ew = warp - EPI_WARP0;                 // 0..3
     const int tid = ew * 32 + lane;                  // 0..127
     const int quarter = warp & 3;                    // TMEM lane quarter this warp may access
     const int f = quarter * 32 + lane;               // output feature row of this thread
     float *st0 = staging, *st1 = staging + C::CH * 128;
     int seg_i = 0;
-    int rstd_m0 = -1, rstd_seg = -1;   // rows whose deferred-norm scales are in s_rstd
-    for (long long i = R.b; i < R.e; ++seg_i) {
-      const int tile = (int)(i / p.KB);
-      const int kb0 = (int)(i % p.KB);
-      const int kb1 = (int)(kb0 + (R.e - i) < p.KB ? kb0 + (R.e - i) : p.KB);
-      i += kb1 - kb0;
-      int seg, n0, m0;
-      locate(tile, seg, n0, m0);
-      const EpiParams &e = p.epi[seg];
-      const int rows = min(BN, p.M - m0);
-      const int buf = seg_i & 1;
-      const uint32_t aph = (seg_i >> 1) & 1;
-      // row scales of a deferred RMSNorm, computed while the MMAs still run
-      const bool need_rstd = e.ssq_in != nullptr && (m0 != rstd_m0 || seg != rstd_seg);
-      if (need_rstd) {
-        epi_bar();   // the previous tile's epilogue is done with s_rstd
-        compute_rstd(e, m0, rows, s_rstd, lane, ew, 4);
-        rstd_m0 = m0;
-        rstd_seg = seg;
-      }
-      const bool ok = epi_all(mbar_wait(&acc_full[buf], aph));
-      if (!ok) {
+    bool alive = true;
+    for (int ph_i = 0; ph_i < p.nph && alive; ++ph_i) {
+      const Phase &ph = p.ph[ph_i];
+      const int np = ph.pair ? 2 : 1;
+      // this phase reads what the previous kernel / every CTA's previous phase wrote
+      if (ph_i == 0) {
+        pdl_wait();
+      } else if (!epi_all(grid_wait(p.grid_bar, (unsigned)(ph_i * G)))) {
         if (tid == 0) raise_error(p.err, DFLASH_DERR_TIMEOUT);
+        alive = false;
         break;
       }
-      tc_fence_after();
-      if (tid == 0 && seg_i == 0) stamp(p, 6);
-      const uint32_t tacc = tmem + ((uint32_t)(quarter * 32) << 16) + buf * C::ACC_COLS;
-      const bool whole = kb0 == 0 && kb1 == p.KB;
-      if (whole) {
-        for (int c0 = 0; c0 < BN; c0 += C::CH) {
-          float v[32];
-#pragma unroll
-          for (int q = 0; q < C::P; ++q) {
-            tmem_ld16(tacc + q * BN + c0, v);
-            if (C::CH == 32) tmem_ld16(tacc + q * BN + c0 + 16, v + 16);
-            float *dst = q ? st1 : st0;
-#pragma unroll
-            for (int t = 0; t < C::CH; ++t) dst[t * 128 + f] = v[t];
-          }
-          epi_bar();
-          if (c0 < rows)
-            run_epilogue<T>(e, st0, PAIR ? st1 : nullptr, 128, m0 + c0, min(C::CH, rows - c0), n0,
-                            tid, 128, s_int, [] { epi_bar(); }, s_rstd + c0);
-          epi_bar();
+      int rstd_m0 = -1, rstd_seg = -1;   // rows whose deferred-norm scales are in s_rstd
+      const Range R = cta_range(ph.total_iters, G, cta);
+      for (long long i = R.b; i < R.e; ++seg_i) {
+        const int tile = (int)(i / ph.KB);
+        const int kb0 = (int)(i % ph.KB);
+        const int kb1 = (int)(kb0 + (R.e - i) < ph.KB ? kb0 + (R.e - i) : ph.KB);
+        i += kb1 - kb0;
+        int seg, n0, m0;
+        locate(ph, tile, seg, n0, m0);
+        const EpiParams &e = ph.epi[seg];
+        const int rows = min(BN, ph.M - m0);
+        const int buf = seg_i & 1;
+        const uint32_t aph = (seg_i >> 1) & 1;
+        // row scales of a deferred RMSNorm, computed while the MMAs still run
+        if (e.ssq_in != nullptr && (m0 != rstd_m0 || seg != rstd_seg)) {
+          epi_bar();   // the previous tile's epilogue is done with s_rstd
+          compute_rstd(e, m0, rows, s_rstd, lane, ew, 4);
+          rstd_m0 = m0;
+          rstd_seg = seg;
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&acc_empty[buf]);
-      } else {
-        // partial tile: publish this CTA's share, last arriver finishes the tile
-        const long long first_tile = R.b / p.KB;
-        const int which = tile == first_tile ? 0 : 1;
-        float *mine = p.partials + ((size_t)cta * 2 + which) * (C::P * BN * 128);
-        for (int c0 = 0; c0 < BN; c0 += C::CH) {
-          float v[32];
-#pragma unroll
-          for (int q = 0; q < C::P; ++q) {
-            tmem_ld16(tacc + q * BN + c0, v);
-            if (C::CH == 32) tmem_ld16(tacc + q * BN + c0 + 16, v + 16);
-#pragma unroll
-            for (int t = 0; t < C::CH; ++t) mine[(q * BN + c0 + t) * 128 + f] = v[t];
-          }
+        const bool ok = epi_all(mbar_wait(&acc_full[buf], aph));
+        if (!ok) {
+          if (tid == 0) raise_error(p.err, DFLASH_DERR_TIMEOUT);
+          alive = false;
+          break;
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&acc_empty[buf]);
-        __threadfence();
-        epi_bar();
-        const long long kb_total = p.total_iters;
-        const int c_first = cta_of_iter((long long)tile * p.KB, kb_total, G);
-        const int c_last = cta_of_iter((long long)(tile + 1) * p.KB - 1, kb_total, G);
-        if (tid == 0) {
-          const int old = atomicAdd(&p.counters[tile], 1);
-          *flag = old == c_last - c_first;
-        }
-        epi_bar();
-        const bool last = *flag != 0;
-        if (last) {
-          __threadfence();
+        tc_fence_after();
+        if (tid == 0 && seg_i == 0) stamp(p, 6);
+        const uint32_t tacc = tmem + ((uint32_t)(quarter * 32) << 16) + buf * C::ACC_COLS;
+        const bool whole = kb0 == 0 && kb1 == ph.KB;
+        if (whole) {
           for (int c0 = 0; c0 < BN; c0 += C::CH) {
-#pragma unroll
-            for (int q = 0; q < C::P; ++q) {
-              float acc[32];
-#pragma unroll
-              for (int t = 0; t < C::CH; ++t) acc[t] = 0.f;
-              // contributors in CTA order, two at a time so that twice the
-              // loads are in flight; the summation order stays fixed
-              auto slot_of = [&](int c) {
-                const long long cfirst_tile = (p.total_iters * c / G) / p.KB;
-                const int w = tile == cfirst_tile ? 0 : 1;
-                return p.partials + ((size_t)c * 2 + w) * (C::P * BN * 128) + (q * BN + c0) * 128 + f;
-              };
-              int c = c_first;
-              for (; c < c_last; c += 2) {
-                const float *a = slot_of(c), *b2 = slot_of(c + 1);
-                float va[32], vb[32];
-#pragma unroll
-                for (int t = 0; t < C::CH; ++t) {
-                  va[t] = __ldcg(a + t * 128);
-                  vb[t] = __ldcg(b2 + t * 128);
-                }
-#pragma unroll
-                for (int t = 0; t < C::CH; ++t) acc[t] = (acc[t] + va[t]) + vb[t];
-              }
-              if (c == c_last) {
-                const float *a = slot_of(c);
-#pragma unroll
-                for (int t = 0; t < C::CH; ++t) acc[t] += __ldcg(a + t * 128);
-              }
+            float v[32];
+            for (int q = 0; q < np; ++q) {
+              tmem_ld16(tacc + q * BN + c0, v);
+              if (C::CH == 32) tmem_ld16(tacc + q * BN + c0 + 16, v + 16);
               float *dst = q ? st1 : st0;
 #pragma unroll
-              for (int t = 0; t < C::CH; ++t) dst[t * 128 + f] = acc[t];
+              for (int t = 0; t < C::CH; ++t) dst[t * 128 + f] = v[t];
             }
             epi_bar();
             if (c0 < rows)
-              run_epilogue<T>(e, st0, PAIR ? st1 : nullptr, 128, m0 + c0, min(C::CH, rows - c0),
+              run_epilogue<T>(e, st0, np == 2 ? st1 : nullptr, 128, m0 + c0, min(C::CH, rows - c0),
                               n0, tid, 128, s_int, [] { epi_bar(); }, s_rstd + c0);
             epi_bar();
           }
-          if (tid == 0) p.counters[tile] = 0;   // ready for the next launch
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[buf]);
+        } else {
+          // partial tile: publish this CTA's share, last arriver finishes the tile
+          const long long first_tile = R.b / ph.KB;
+          const int which = tile == first_tile ? 0 : 1;
+          float *mine = p.partials + ((size_t)cta * 2 + which) * (C::P * BN * 128);
+          for (int c0 = 0; c0 < BN; c0 += C::CH) {
+            float v[32];
+            for (int q = 0; q < np; ++q) {
+              tmem_ld16(tacc + q * BN + c0, v);
+              if (C::CH == 32) tmem_ld16(tacc + q * BN + c0 + 16, v + 16);
+#pragma unroll
+              for (int t = 0; t < C::CH; ++t) mine[(q * BN + c0 + t) * 128 + f] = v[t];
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[buf]);
+          __threadfence();
+          epi_bar();
+          const int c_first = cta_of_iter((long long)tile * ph.KB, ph.total_iters, G);
+          const int c_last = cta_of_iter((long long)(tile + 1) * ph.KB - 1, ph.total_iters, G);
+          int *ticket = p.counters + ph.counter_off + tile;
+          if (tid == 0) {
+            const int old = atomicAdd(ticket, 1);
+            *flag = old == c_last - c_first;
+          }
+          epi_bar();
+          const bool last = *flag != 0;
+          if (last) {
+            __threadfence();
+            for (int c0 = 0; c0 < BN; c0 += C::CH) {
+              for (int q = 0; q < np; ++q) {
+                float acc[32];
+#pragma unroll
+                for (int t = 0; t < C::CH; ++t) acc[t] = 0.f;
+                // contributors in CTA order, two at a time so that twice the
+                // loads are in flight; the summation order stays fixed
+                auto slot_of = [&](int c) {
+                  const long long cfirst_tile = (ph.total_iters * c / G) / ph.KB;
+                  const int w = tile == cfirst_tile ? 0 : 1;
+                  return p.partials + ((size_t)c * 2 + w) * (C::P * BN * 128) + (q * BN + c0) * 128 + f;
+                };
+                int c = c_first;
+                for (; c < c_last; c += 2) {
+                  const float *a = slot_of(c), *b2 = slot_of(c + 1);
+                  float va[32], vb[32];
+#pragma unroll
+                  for (int t = 0; t < C::CH; ++t) {
+                    va[t] = __ldcg(a + t * 128);
+                    vb[t] = __ldcg(b2 + t * 128);
+                  }
+#pragma unroll
+                  for (int t = 0; t < C::CH; ++t) acc[t] = (acc[t] + va[t]) + vb[t];
+                }
+                if (c == c_last) {
+                  const float *a = slot_of(c);
+#pragma unroll
+                  for (int t = 0; t < C::CH; ++t) acc[t] += __ldcg(a + t * 128);
+                }
+                float *dst = q ? st1 : st0;
+#pragma unroll
+                for (int t = 0; t < C::CH; ++t) dst[t * 128 + f] = acc[t];
+              }
+              epi_bar();
+              if (c0 < rows)
+                run_epilogue<T>(e, st0, np == 2 ? st1 : nullptr, 128, m0 + c0,
+                                min(C::CH, rows - c0), n0, tid, 128, s_int, [] { epi_bar(); },
+                                s_rstd + c0);
+              epi_bar();
+            }
+            if (tid == 0) *ticket = 0;   // ready for the next launch
+          }
+          epi_bar();
         }
+      }
+      if (!alive) break;
+      if (ph_i + 1 < p.nph) {
+        // this CTA's share of the phase is written: count it in the grid barrier
+        __threadfence();
         epi_bar();
+        if (tid == 0) atomicAdd(&p.grid_bar[0], 1u);
       }
     }
   }
   if (warp == EPI_WARP0 && lane == 0) stamp(p, 7);
   tc_fence_before();
   __syncthreads();
+  if (p.nph > 1 && threadIdx.x == 0) {
+    // the last CTA out clears the barrier words for the next program
+    __threadfence();
+    const unsigned int old = atomicAdd(&p.grid_bar[1], 1u);
+    if (old == (unsigned int)G - 1) {
+      p.grid_bar[0] = 0;
+      p.grid_bar[1] = 0;
+      __threadfence();
+    }
+  }
   pdl_trigger();   // every global write of this CTA is done
   if (warp == 1) {
     tc_fence_after();
@@ -584,18 +662,67 @@ bool encode_2d(CUtensorMap *tm, const void *base, uint64_t rows, uint64_t cols, 
 
 int g_num_sms = 0;
 
-template <int BN, bool PAIR>
-cudaError_t launch_cfg(tc::Params &p, int G, cudaStream_t s) {
-  using C = tc::Cfg<BN, PAIR>;
-  auto kern = tc::gemm_tc_kernel<BN, PAIR, bf16>;
-  return launch_pdl(kern, dim3(G), dim3(tc::THREADS), C::SMEM, s, p);
+template <int BN, bool PAIRABLE>
+cudaError_t launch_cfg(tc::Params &p, int G, bool coop, cudaStream_t s) {
+  using C = tc::Cfg<BN, PAIRABLE>;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(G);
+  cfg.blockDim = dim3(tc::THREADS);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeCooperative;
+  attr[1].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = coop ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, tc::gemm_tc_kernel<BN, PAIRABLE, bf16>, p);
 }
 
-template <int BN, bool PAIR>
+template <int BN, bool PAIRABLE>
 cudaError_t set_attr() {
-  using C = tc::Cfg<BN, PAIR>;
-  return cudaFuncSetAttribute(tc::gemm_tc_kernel<BN, PAIR, bf16>,
+  using C = tc::Cfg<BN, PAIRABLE>;
+  return cudaFuncSetAttribute(tc::gemm_tc_kernel<BN, PAIRABLE, bf16>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+}
+
+int pick_bn(int M, bool pair) {
+  int BN = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
+  if (pair && BN > 128) BN = 128;
+  return BN;
+}
+
+// One phase of a program from a problem description; returns its tile count.
+bool build_phase(tc::Phase &ph, const GemmProblem &P, int BN, int counter_off) {
+  memset(&ph, 0, sizeof(ph));
+  if (P.K % tc::BK || P.A.k_per_src % tc::BK) return false;
+  const bool pair = P.seg[0].epi.op == EPI_SWIGLU;
+  for (int j = 0; j < P.A.n_src; ++j)
+    if (!encode_2d(&ph.tmA[j], P.A.ptr[j], (uint64_t)P.M, (uint64_t)P.A.k_per_src, (uint64_t)P.A.ld, BN))
+      return false;
+  int ntiles = 0;
+  for (int i = 0; i < P.nseg; ++i) {
+    const GemmSeg &g = P.seg[i];
+    if (!encode_2d(&ph.tmW[i], g.W, (uint64_t)g.N, (uint64_t)P.K, (uint64_t)g.ldw, 128))
+      return false;
+    ph.epi[i] = g.epi;
+    const int n = pair ? g.N / 2 : g.N;
+    ph.seg_ntiles[i] = (n + 127) / 128;
+    ph.seg_half[i] = pair ? g.N / 2 : 0;
+    ntiles += ph.seg_ntiles[i];
+  }
+  ph.nseg = P.nseg;
+  ph.pair = pair ? 1 : 0;
+  ph.M = P.M;
+  ph.K = P.K;
+  ph.KB = P.K / tc::BK;
+  ph.m_tiles = (P.M + BN - 1) / BN;
+  ph.tiles = ntiles * ph.m_tiles;
+  ph.k_per_src = P.A.k_per_src;
+  ph.counter_off = counter_off;
+  ph.total_iters = (long long)ph.tiles * ph.KB;
+  return true;
 }
 
 }  // namespace
@@ -604,8 +731,7 @@ cudaError_t set_attr() {
 size_t gemm_tc_partials_bytes() { return (size_t)kTcMaxCtas * 2 * 256 * 128 * 4; }
 
 int gemm_tc_tiles(int n_tiles, int M, bool pair) {
-  int BN = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
-  if (pair && BN > 128) BN = 128;
+  const int BN = pick_bn(M, pair);
   return n_tiles * ((M + BN - 1) / BN);
 }
 
@@ -630,55 +756,60 @@ cudaError_t prepare_gemm_tc() {
   return cudaSuccess;
 }
 
+cudaError_t launch_gemm_program(const GemmProblem *probs, int n, float *partials, int *counters,
+                                int max_tiles, unsigned int *grid_bar, unsigned int *err,
+                                cudaStream_t s, unsigned long long *trace) {
+  if (n <= 0 || n > kMaxPhases) return cudaErrorInvalidValue;
+  if (n > 1 && !grid_bar) return cudaErrorInvalidValue;
+  const int M = probs[0].M;
+  if (M <= 0) return cudaSuccess;
+  bool any_pair = false;
+  for (int i = 0; i < n; ++i) {
+    if (probs[i].M != M || probs[i].nseg <= 0) return cudaErrorInvalidValue;
+    any_pair |= probs[i].seg[0].epi.op == EPI_SWIGLU;
+  }
+  const int BN = pick_bn(M, any_pair);
+  tc::Params p;
+  memset(&p, 0, sizeof(p));
+  int off = 0;
+  long long most = 0;
+  for (int i = 0; i < n; ++i) {
+    if (!build_phase(p.ph[i], probs[i], BN, off)) return cudaErrorInvalidValue;
+    off += p.ph[i].tiles;
+    most = std::max(most, p.ph[i].total_iters);
+  }
+  if (off > max_tiles) return cudaErrorInvalidValue;
+  p.nph = n;
+  p.partials = partials;
+  p.counters = counters;
+  p.grid_bar = grid_bar;
+  p.err = err;
+  p.trace = trace;
+  const int G = (int)std::min<long long>(std::min(gemm_tc_num_sms(), kTcMaxCtas), most);
+  const bool coop = n > 1;
+  if (any_pair) {
+    switch (BN) {
+      case 16: return launch_cfg<16, true>(p, G, coop, s);
+      case 32: return launch_cfg<32, true>(p, G, coop, s);
+      case 64: return launch_cfg<64, true>(p, G, coop, s);
+      case 128: return launch_cfg<128, true>(p, G, coop, s);
+    }
+  } else {
+    switch (BN) {
+      case 16: return launch_cfg<16, false>(p, G, coop, s);
+      case 32: return launch_cfg<32, false>(p, G, coop, s);
+      case 64: return launch_cfg<64, false>(p, G, coop, s);
+      case 128: return launch_cfg<128, false>(p, G, coop, s);
+      case 256: return launch_cfg<256, false>(p, G, coop, s);
+    }
+  }
+  return cudaErrorInvalidValue;
+}
+
 cudaError_t launch_gemm_tc(const GemmProblem &P, float *partials, int *counters, int max_tiles,
                            unsigned int *err, cudaStream_t s, unsigned long long *trace) {
   if (P.M <= 0 || P.nseg <= 0) return cudaSuccess;
-  if (P.K % tc::BK) return cudaErrorInvalidValue;
-  const bool pair = P.seg[0].epi.op == EPI_SWIGLU;
-  int BN = P.M <= 16 ? 16 : P.M <= 32 ? 32 : P.M <= 64 ? 64 : P.M <= 128 ? 128 : 256;
-  if (pair && BN > 128) BN = 128;
-  tc::Params p;
-  memset(&p, 0, sizeof(p));
-  for (int j = 0; j < P.A.n_src; ++j)
-    if (!encode_2d(&p.tmA[j], P.A.ptr[j], (uint64_t)P.M, (uint64_t)P.A.k_per_src, (uint64_t)P.A.ld, BN))
-      return cudaErrorInvalidValue;
-  int ntiles = 0;
-  for (int i = 0; i < P.nseg; ++i) {
-    const GemmSeg &g = P.seg[i];
-    if (!encode_2d(&p.tmW[i], g.W, (uint64_t)g.N, (uint64_t)P.K, (uint64_t)g.ldw, 128))
-      return cudaErrorInvalidValue;
-    p.epi[i] = g.epi;
-    const int n = pair ? g.N / 2 : g.N;
-    p.seg_ntiles[i] = (n + 127) / 128;
-    p.seg_half[i] = pair ? g.N / 2 : 0;
-    ntiles += p.seg_ntiles[i];
-  }
-  p.nseg = P.nseg;
-  p.M = P.M;
-  p.K = P.K;
-  p.KB = P.K / tc::BK;
-  p.m_tiles = (P.M + BN - 1) / BN;
-  p.tiles = ntiles * p.m_tiles;
-  if (p.tiles > max_tiles) return cudaErrorInvalidValue;
-  p.k_per_src = P.A.k_per_src;
-  p.total_iters = (long long)p.tiles * p.KB;
-  p.partials = partials;
-  p.counters = counters;
-  p.err = err;
-  p.trace = trace;
-  const int G = (int)std::min<long long>(std::min(gemm_tc_num_sms(), kTcMaxCtas), p.total_iters);
-  switch (BN | (pair ? 1 : 0)) {
-    case 16: return launch_cfg<16, false>(p, G, s);
-    case 32: return launch_cfg<32, false>(p, G, s);
-    case 64: return launch_cfg<64, false>(p, G, s);
-    case 128: return launch_cfg<128, false>(p, G, s);
-    case 256: return launch_cfg<256, false>(p, G, s);
-    case 17: return launch_cfg<16, true>(p, G, s);
-    case 33: return launch_cfg<32, true>(p, G, s);
-    case 65: return launch_cfg<64, true>(p, G, s);
-    case 129: return launch_cfg<128, true>(p, G, s);
-  }
-  return cudaErrorInvalidValue;
+  return launch_gemm_program(&P, 1, partials, counters, max_tiles, nullptr, err, s, trace);
 }
 
 }  // namespace dflash
