@@ -29,7 +29,8 @@ def sources():
 
 def _deps_mtime():
     files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
-    files.append(os.path.join(os.path.dirname(HERE), "include", "dflash.h"))
+    inc = os.path.join(os.path.dirname(HERE), "include")
+    files += [os.path.join(inc, f) for f in os.listdir(inc)]
     return max(os.path.getmtime(f) for f in files)
 
 

@@ -6,6 +6,7 @@
 #include <vector>
 
 #include "../../include/dflash.h"
+#include "../../include/dflash_testing.h"
 #include "kernels.h"
 
 using namespace dflash;
@@ -42,6 +43,7 @@ struct dflash_handle {
   char *ws = nullptr;
   size_t ws_bytes = 0;
   int store;      // ST_F32 / ST_BF16
+  bool fuse = true;   // dependent bf16 GEMMs as one cooperative launch
   size_t es;      // element size of the configured dtype
   // optional per-launch event timing
   struct ProfRec {
@@ -145,6 +147,13 @@ cudaError_t run_program(dflash_handle *h, const GemmProblem *P, int n, cudaStrea
   if (h->store == ST_F32) {
     for (int i = 0; i < n; ++i) {
       const cudaError_t e = launch_gemm_simt(ST_F32, P[i], s);
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+  }
+  if (!h->fuse) {
+    for (int i = 0; i < n; ++i) {
+      const cudaError_t e = run_gemm(h, P[i], s);
       if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
@@ -630,6 +639,12 @@ int dflash_draft_block(dflash_handle *h, const dflash_kv *kv, int32_t batch, con
     return st;
   return timed(h, "argmax_finalize", s,
                [&] { return launch_argmax_finalize(keys, anchor, batch, S, draft_ids, s); });
+}
+
+int dflash_test_set_fusion(dflash_handle *h, int32_t on) {
+  if (!h) return fail(DFLASH_EINVAL, "handle is NULL");
+  h->fuse = on != 0;
+  return DFLASH_OK;
 }
 
 int dflash_accept_commit(dflash_handle *h, int32_t batch, const int32_t *draft_ids,

@@ -61,6 +61,7 @@ struct Phase {
   int M, K, KB, m_tiles, tiles;
   int k_per_src;
   int counter_off;                // this phase's tickets start here
+  int G;                          // CTAs sharing this phase (<= gridDim.x, <= total_iters)
   long long total_iters;
 };
 
@@ -217,11 +218,51 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
 struct Range {
   long long b, e;
 };
+// CTA c's share of a phase spread over its first G CTAs (G <= total, so
+// every share of a participating CTA is non-empty); other CTAs sit it out.
 __device__ __forceinline__ Range cta_range(long long total, int G, int c) {
+  if (c >= G) return {0, 0};
   return {total * c / G, total * (c + 1) / G};
 }
 __device__ __forceinline__ int cta_of_iter(long long it, long long total, int G) {
   return (int)(((it + 1) * G - 1) / total);
+}
+
+// The scalars of a phase that the inner loops use, read once per phase into
+// registers.
+struct PhaseScalars {
+  int KB, k_per_src, m_tiles, nseg, pair, M, G;
+  long long total;
+  int seg_ntiles[kMaxSeg];
+};
+__device__ __forceinline__ PhaseScalars load_scalars(const Phase &ph) {
+  PhaseScalars ps;
+  ps.KB = ph.KB;
+  ps.k_per_src = ph.k_per_src;
+  ps.m_tiles = ph.m_tiles;
+  ps.nseg = ph.nseg;
+  ps.pair = ph.pair;
+  ps.M = ph.M;
+  ps.G = ph.G;
+  ps.total = ph.total_iters;
+#pragma unroll
+  for (int i = 0; i < kMaxSeg; ++i) ps.seg_ntiles[i] = ph.seg_ntiles[i];
+  return ps;
+}
+// tile -> (segment, feature tile, token tile), with register-only indexing
+template <int BN>
+__device__ __forceinline__ void locate(const PhaseScalars &ps, int tile, int &seg, int &n0, int &m0) {
+  int nt = tile / ps.m_tiles;
+  m0 = (tile - nt * ps.m_tiles) * BN;
+  seg = 0;
+#pragma unroll
+  for (int i = 0; i < kMaxSeg - 1; ++i) {
+    if (seg == i && i < ps.nseg - 1 && nt >= ps.seg_ntiles[i]) {
+      nt -= ps.seg_ntiles[i];
+      seg = i + 1;
+    }
+  }
+  n0 = nt * 128;
 }
 
 template <int BN, bool PAIRABLE>
@@ -258,6 +299,140 @@ __device__ __forceinline__ bool grid_wait(const unsigned int *bar, unsigned int 
 // Later bulk-async (TMA) reads must observe what generic stores made visible.
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// MMAs of k-blocks kb0..kb1-1 of one tile into the accumulator at d0; NS
+// slots per k-block (2: a gate/up pair sharing the activation tile).  The
+// pair count is a compile-time constant so that the MMAs of a k-block issue
+// back to back (a run-time choice here measurably slowed every GEMM).
+template <class C, int NS, int BN>
+__device__ __forceinline__ bool mma_kblocks(uint32_t &it, int kb0, int kb1, uint32_t d0,
+                                            uint8_t *slots, uint64_t *full, uint64_t *empty,
+                                            const Params &p) {
+  constexpr uint32_t idesc = idesc_bf16(128, BN);
+  for (int kb = kb0; kb < kb1; ++kb) {
+    const int s0 = it % C::SLOTS;
+    if (!mbar_wait(&full[s0], (it / C::SLOTS) & 1)) return false;
+    if (it == 0) stamp(p, 4);
+    tc_fence_after();
+    const uint32_t st0 = su32(slots + s0 * C::SLOT_BYTES);
+    const uint64_t adesc = sw128_desc(st0 + C::W_BYTES);
+    const uint64_t wdesc0 = sw128_desc(st0);
+    int s1 = 0;
+    uint64_t wdesc1 = 0;
+    if (NS == 2) {
+      s1 = (it + 1) % C::SLOTS;
+      wdesc1 = sw128_desc(su32(slots + s1 * C::SLOT_BYTES));
+    }
+#pragma unroll
+    for (int kk = 0; kk < BK / 16; ++kk) {
+      const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
+      umma_bf16(d0, wdesc0 + 2 * kk, adesc + 2 * kk, idesc, acc);
+      if (NS == 2) umma_bf16(d0 + BN, wdesc1 + 2 * kk, adesc + 2 * kk, idesc, acc);
+    }
+    umma_commit(&empty[s0]);
+    if (NS == 2) umma_commit(&empty[s1]);
+    it += NS;
+  }
+  return true;
+}
+// Activation tile of one k-block into slot s (K-split over the A sources).
+template <class C>
+__device__ __forceinline__ void issue_a(const Phase &ph, const PhaseScalars &ps, uint8_t *slots,
+                                        int s, int k, int m0, uint64_t *full, uint64_t pol) {
+  const int src = k / ps.k_per_src;
+  tma_load_2d(slots + s * C::SLOT_BYTES + C::W_BYTES, &ph.tmA[src], &full[s],
+              k - src * ps.k_per_src, m0, pol);
+}
+// The activations of phase ph_i may be read: the preceding kernel (phase 0)
+// or every CTA's previous phase has written them.  false = the grid barrier
+// wait gave up.
+__device__ __forceinline__ bool phase_inputs_ready(const Params &p, int ph_i, int G) {
+  if (ph_i == 0) {
+    stamp(p, 2);
+    pdl_wait();
+    stamp(p, 3);
+    return true;
+  }
+  const bool ok = grid_wait(p.grid_bar, (unsigned)(ph_i * G));
+  fence_proxy_async();   // later TMA reads see the other CTAs' generic stores
+  return ok;
+}
+
+// TMA producer of one phase: this CTA's (tile, k-block) range, NS slots per
+// k-block.  The weights never depend on earlier work: they go out as soon as a
+// slot is free.  Activations wait for the phase's inputs (the previous kernel,
+// or every CTA's previous phase), at the latest when the next slot to fill
+// still holds a weight-only k-block of this phase (waiting for it would never
+// end); until then their (slot, k, row) wait in pend_*.  false = a wait gave up.
+template <class C, int NS, int BN>
+__device__ __forceinline__ bool produce_phase(const Params &p, const Phase &ph,
+                                              const PhaseScalars &ps, int ph_i, int cta,
+                                              uint32_t &it, uint8_t *slots, uint64_t *full,
+                                              uint64_t *empty, int *pend_s, int *pend_k,
+                                              int *pend_m, uint64_t pol_w, uint64_t pol_a) {
+  const Range R = cta_range(ps.total, ps.G, cta);
+  const uint32_t it0 = it;
+  bool ready = false;
+  int npend = 0;
+  long long left = R.e - R.b;
+  int tile = (int)(R.b / ps.KB), kb = (int)(R.b - (long long)tile * ps.KB) - 1;
+  int seg = 0, n0 = 0, m0 = 0, half = 0;
+  const CUtensorMap *tmw = &ph.tmW[0];
+  if (left > 0) {
+    locate<BN>(ps, tile, seg, n0, m0);
+    tmw = &ph.tmW[seg];
+    if (NS == 2) half = ph.seg_half[seg];
+  }
+  while (left > 0) {
+    --left;
+    if (++kb == ps.KB) {
+      kb = 0;
+      ++tile;
+      locate<BN>(ps, tile, seg, n0, m0);
+      tmw = &ph.tmW[seg];
+      if (NS == 2) half = ph.seg_half[seg];
+    }
+    const int k = kb * BK;
+    if (!ready && it + NS - it0 > (uint32_t)C::SLOTS) {
+      const bool ok = phase_inputs_ready(p, ph_i, gridDim.x);
+      for (int j = 0; j < npend; ++j)
+        issue_a<C>(ph, ps, slots, pend_s[j], pend_k[j], pend_m[j], full, pol_a);
+      npend = 0;
+      ready = true;
+      if (!ok) return false;
+    }
+    // slot uses below SLOTS find a never-used slot: nothing to wait for
+    if (it >= (uint32_t)C::SLOTS && !mbar_wait(&empty[it % C::SLOTS], ((it / C::SLOTS) & 1) ^ 1))
+      return false;
+    if (NS == 2 && it + 1 >= (uint32_t)C::SLOTS &&
+        !mbar_wait(&empty[(it + 1) % C::SLOTS], (((it + 1) / C::SLOTS) & 1) ^ 1))
+      return false;
+    const int s0 = it % C::SLOTS;
+    mbar_expect_tx(&full[s0], NS * C::W_BYTES + C::A_BYTES);
+    tma_load_2d(slots + s0 * C::SLOT_BYTES, tmw, &full[s0], k, n0, pol_w);
+    if (NS == 2) {
+      const int s1 = (it + 1) % C::SLOTS;
+      tma_load_2d(slots + s1 * C::SLOT_BYTES, tmw, &full[s0], k, half + n0, pol_w);
+      mbar_arrive(&full[s1]);   // keeps the second slot's phase count in step
+    }
+    if (ready) {
+      issue_a<C>(ph, ps, slots, s0, k, m0, full, pol_a);
+    } else {
+      pend_s[npend] = s0;
+      pend_k[npend] = k;
+      pend_m[npend] = m0;
+      ++npend;
+    }
+    it += NS;
+  }
+  if (!ready) {
+    const bool ok = phase_inputs_ready(p, ph_i, gridDim.x);
+    for (int j = 0; j < npend; ++j)
+      issue_a<C>(ph, ps, slots, pend_s[j], pend_k[j], pend_m[j], full, pol_a);
+    if (!ok) return false;
+  }
+  return true;
 }
 
 template <int BN, bool PAIRABLE, typename T>
@@ -307,87 +482,26 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
   const uint32_t tmem = *tmem_slot;
   if (threadIdx.x == 0) stamp(p, 1);
 
-  // tile -> (segment, feature tile, token tile) within a phase
-  auto locate = [&](const Phase &ph, int tile, int &seg, int &n0, int &m0) {
-    int nt = tile / ph.m_tiles;
-    m0 = (tile % ph.m_tiles) * BN;
-    seg = 0;
-    while (seg < ph.nseg - 1 && nt >= ph.seg_ntiles[seg]) nt -= ph.seg_ntiles[seg++];
-    n0 = nt * 128;
-  };
-
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first(), pol_a = policy_evict_last();
       uint32_t it = 0;   // slot uses so far
       bool ok = true;
+      // k-blocks whose weights went out before their activations could:
+      // (slot, k, token row), at most one ring's worth
       int pend_s[C::SLOTS], pend_k[C::SLOTS], pend_m[C::SLOTS];
       for (int ph_i = 0; ph_i < p.nph && ok; ++ph_i) {
         const Phase &ph = p.ph[ph_i];
-        const Range R = cta_range(ph.total_iters, G, cta);
-        auto load_a = [&](int s, int kk, int mm) {
-          const int src = kk / ph.k_per_src;
-          tma_load_2d(slots + s * C::SLOT_BYTES + C::W_BYTES, &ph.tmA[src], &full[s],
-                      kk - src * ph.k_per_src, mm, pol_a);
-        };
-        // The weights never depend on earlier work: they go out as soon as a
-        // slot is free.  Activations wait for this phase's inputs (the
-        // previous kernel, or every CTA's previous phase).
-        bool ready = false;
-        int npend = 0;
-        auto make_ready = [&]() {
-          if (ph_i == 0) {
-            stamp(p, 2);
-            pdl_wait();
-            stamp(p, 3);
-          } else if (!grid_wait(p.grid_bar, (unsigned)(ph_i * G))) {
-            ok = false;
-          }
-          fence_proxy_async();
-          for (int j = 0; j < npend; ++j) load_a(pend_s[j], pend_k[j], pend_m[j]);
-          npend = 0;
-          ready = true;
-        };
-        const int ns = ph.pair ? 2 : 1;
-        long long left = R.e - R.b;
-        int tile = (int)(R.b / ph.KB), kb = (int)(R.b % ph.KB) - 1;
-        int seg = 0, n0 = 0, m0 = 0;
-        if (left > 0) locate(ph, tile, seg, n0, m0);
-        while (left > 0 && ok) {
-          --left;
-          if (++kb == ph.KB) {
-            kb = 0;
-            ++tile;
-            locate(ph, tile, seg, n0, m0);
-          }
-          const int k = kb * BK;
-          for (int j = 0; j < ns && ok; ++j) {
-            const uint32_t u = it + j;
-            const uint32_t par = ((u / C::SLOTS) & 1) ^ 1;
-            if (!ready && !mbar_try(&empty[u % C::SLOTS], par)) make_ready();
-            if (!mbar_wait(&empty[u % C::SLOTS], par)) ok = false;
-          }
-          if (!ok) break;
-          const int s0 = it % C::SLOTS, s1 = (it + 1) % C::SLOTS;
-          mbar_expect_tx(&full[s0], ns * C::W_BYTES + C::A_BYTES);
-          tma_load_2d(slots + s0 * C::SLOT_BYTES, &ph.tmW[seg], &full[s0], k, n0, pol_w);
-          if (ns == 2) {
-            tma_load_2d(slots + s1 * C::SLOT_BYTES, &ph.tmW[seg], &full[s0], k,
-                        ph.seg_half[seg] + n0, pol_w);
-            mbar_arrive(&full[s1]);   // keeps the second slot's phase count in step
-          }
-          if (ready) {
-            load_a(s0, k, m0);
-          } else {
-            pend_s[npend] = s0;
-            pend_k[npend] = k;
-            pend_m[npend] = m0;
-            ++npend;
-          }
-          it += ns;
-        }
-        if (ok && !ready) make_ready();
+        const PhaseScalars ps = load_scalars(ph);
+        if constexpr (PAIRABLE)
+          ok = ps.pair ? produce_phase<C, 2, BN>(p, ph, ps, ph_i, cta, it, slots, full, empty,
+                                                 pend_s, pend_k, pend_m, pol_w, pol_a)
+                       : produce_phase<C, 1, BN>(p, ph, ps, ph_i, cta, it, slots, full, empty,
+                                                 pend_s, pend_k, pend_m, pol_w, pol_a);
+        else
+          ok = produce_phase<C, 1, BN>(p, ph, ps, ph_i, cta, it, slots, full, empty, pend_s,
+                                       pend_k, pend_m, pol_w, pol_a);
       }
       if (!ok) raise_error(p.err, DFLASH_DERR_TIMEOUT);
       // drain: no TMA write may still be in flight when the CTA winds down
@@ -399,17 +513,16 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(128, BN);
       uint32_t it = 0;
       int seg_i = 0;
       bool ok = true;
       for (int ph_i = 0; ph_i < p.nph && ok; ++ph_i) {
-        const Phase &ph = p.ph[ph_i];
-        const Range R = cta_range(ph.total_iters, G, cta);
-        const int ns = ph.pair ? 2 : 1;
+        const PhaseScalars ps = load_scalars(p.ph[ph_i]);
+        const Range R = cta_range(ps.total, ps.G, cta);
+        const int ns = ps.pair ? 2 : 1;
         for (long long i = R.b; i < R.e && ok; ++seg_i) {
-          const int kb0 = (int)(i % ph.KB);
-          const int kb1 = (int)(kb0 + (R.e - i) < ph.KB ? kb0 + (R.e - i) : ph.KB);
+          const int kb0 = (int)(i % ps.KB);
+          const int kb1 = (int)(kb0 + (R.e - i) < ps.KB ? kb0 + (R.e - i) : ps.KB);
           const int buf = seg_i & 1;
           const uint32_t aph = (seg_i >> 1) & 1;
           if (!mbar_wait(&acc_empty[buf], aph ^ 1)) {
@@ -418,28 +531,12 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
           }
           tc_fence_after();
           const uint32_t d0 = tmem + buf * C::ACC_COLS;
-          for (int kb = kb0; kb < kb1; ++kb) {
-            const int s0 = it % C::SLOTS, s1 = (it + 1) % C::SLOTS;
-            if (!mbar_wait(&full[s0], (it / C::SLOTS) & 1)) {
-              ok = false;
-              break;
-            }
-            if (it == 0) stamp(p, 4);
-            tc_fence_after();
-            const uint32_t st0 = su32(slots + s0 * C::SLOT_BYTES);
-            const uint64_t adesc = sw128_desc(st0 + C::W_BYTES);
-            const uint64_t wdesc0 = sw128_desc(st0);
-            const uint64_t wdesc1 = sw128_desc(su32(slots + s1 * C::SLOT_BYTES));
-#pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk) {
-              const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
-              umma_bf16(d0, wdesc0 + 2 * kk, adesc + 2 * kk, idesc, acc);
-              if (ns == 2) umma_bf16(d0 + BN, wdesc1 + 2 * kk, adesc + 2 * kk, idesc, acc);
-            }
-            umma_commit(&empty[s0]);
-            if (ns == 2) umma_commit(&empty[s1]);
-            it += ns;
-          }
+          if constexpr (PAIRABLE)
+            ok = ns == 2 ? mma_kblocks<C, 2, BN>(it, kb0, kb1, d0, slots, full, empty, p)
+                         : mma_kblocks<C, 1, BN>(it, kb0, kb1, d0, slots, full, empty, p);
+          else
+            ok = mma_kblocks<C, 1, BN>(it, kb0, kb1, d0, slots, full, empty, p);
+          if (!ok) break;
           umma_commit(&acc_full[buf]);
           i += kb1 - kb0;
         }
@@ -461,26 +558,29 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
     bool alive = true;
     for (int ph_i = 0; ph_i < p.nph && alive; ++ph_i) {
       const Phase &ph = p.ph[ph_i];
-      const int np = ph.pair ? 2 : 1;
-      // this phase reads what the previous kernel / every CTA's previous phase wrote
+      const PhaseScalars ps = load_scalars(ph);
+      const int np = ps.pair ? 2 : 1;
+      // this phase reads what the previous kernel / every CTA's previous phase
+      // wrote; for the latter one thread spins with acquire semantics and the
+      // named barrier orders the other epilogue threads after it
       if (ph_i == 0) {
         pdl_wait();
-      } else if (!epi_all(grid_wait(p.grid_bar, (unsigned)(ph_i * G)))) {
+      } else if (!epi_all(tid == 0 ? grid_wait(p.grid_bar, (unsigned)(ph_i * G)) : true)) {
         if (tid == 0) raise_error(p.err, DFLASH_DERR_TIMEOUT);
         alive = false;
         break;
       }
       int rstd_m0 = -1, rstd_seg = -1;   // rows whose deferred-norm scales are in s_rstd
-      const Range R = cta_range(ph.total_iters, G, cta);
+      const Range R = cta_range(ps.total, ps.G, cta);
       for (long long i = R.b; i < R.e; ++seg_i) {
-        const int tile = (int)(i / ph.KB);
-        const int kb0 = (int)(i % ph.KB);
-        const int kb1 = (int)(kb0 + (R.e - i) < ph.KB ? kb0 + (R.e - i) : ph.KB);
+        const int tile = (int)(i / ps.KB);
+        const int kb0 = (int)(i - (long long)tile * ps.KB);
+        const int kb1 = (int)(kb0 + (R.e - i) < ps.KB ? kb0 + (R.e - i) : ps.KB);
         i += kb1 - kb0;
         int seg, n0, m0;
-        locate(ph, tile, seg, n0, m0);
-        const EpiParams &e = ph.epi[seg];
-        const int rows = min(BN, ph.M - m0);
+        locate<BN>(ps, tile, seg, n0, m0);
+        const EpiParams e = ph.epi[seg];
+        const int rows = min(BN, ps.M - m0);
         const int buf = seg_i & 1;
         const uint32_t aph = (seg_i >> 1) & 1;
         // row scales of a deferred RMSNorm, computed while the MMAs still run
@@ -499,7 +599,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
         tc_fence_after();
         if (tid == 0 && seg_i == 0) stamp(p, 6);
         const uint32_t tacc = tmem + ((uint32_t)(quarter * 32) << 16) + buf * C::ACC_COLS;
-        const bool whole = kb0 == 0 && kb1 == ph.KB;
+        const bool whole = kb0 == 0 && kb1 == ps.KB;
         if (whole) {
           for (int c0 = 0; c0 < BN; c0 += C::CH) {
             float v[32];
@@ -521,7 +621,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
           if (lane == 0) mbar_arrive(&acc_empty[buf]);
         } else {
           // partial tile: publish this CTA's share, last arriver finishes the tile
-          const long long first_tile = R.b / ph.KB;
+          const long long first_tile = R.b / ps.KB;
           const int which = tile == first_tile ? 0 : 1;
           float *mine = p.partials + ((size_t)cta * 2 + which) * (C::P * BN * 128);
           for (int c0 = 0; c0 < BN; c0 += C::CH) {
@@ -538,8 +638,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
           if (lane == 0) mbar_arrive(&acc_empty[buf]);
           __threadfence();
           epi_bar();
-          const int c_first = cta_of_iter((long long)tile * ph.KB, ph.total_iters, G);
-          const int c_last = cta_of_iter((long long)(tile + 1) * ph.KB - 1, ph.total_iters, G);
+          const int c_first = cta_of_iter((long long)tile * ps.KB, ps.total, ps.G);
+          const int c_last = cta_of_iter((long long)(tile + 1) * ps.KB - 1, ps.total, ps.G);
           int *ticket = p.counters + ph.counter_off + tile;
           if (tid == 0) {
             const int old = atomicAdd(ticket, 1);
@@ -557,7 +657,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
                 // contributors in CTA order, two at a time so that twice the
                 // loads are in flight; the summation order stays fixed
                 auto slot_of = [&](int c) {
-                  const long long cfirst_tile = (ph.total_iters * c / G) / ph.KB;
+                  const long long cfirst_tile = (ps.total * c / ps.G) / ps.KB;
                   const int w = tile == cfirst_tile ? 0 : 1;
                   return p.partials + ((size_t)c * 2 + w) * (C::P * BN * 128) + (q * BN + c0) * 128 + f;
                 };
@@ -786,6 +886,7 @@ cudaError_t launch_gemm_program(const GemmProblem *probs, int n, float *partials
   p.err = err;
   p.trace = trace;
   const int G = (int)std::min<long long>(std::min(gemm_tc_num_sms(), kTcMaxCtas), most);
+  for (int i = 0; i < n; ++i) p.ph[i].G = (int)std::max<long long>(1, std::min<long long>(G, p.ph[i].total_iters));
   const bool coop = n > 1;
   if (any_pair) {
     switch (BN) {

@@ -62,3 +62,73 @@ extern "C" int dflash_test_gemm_traced(int32_t M, int32_t N, int32_t K, int32_t 
   if (launch_gemm_tc(P, partials, counters, tiles, err, s, trace) != cudaSuccess) return DFLASH_ECUDA;
   return DFLASH_OK;
 }
+
+// ---------------------------------------------------------------- programs
+namespace {
+int program_tiles(int n, int32_t M, const int32_t *N, const int32_t *op) {
+  int t = 0;
+  bool pair = false;
+  for (int i = 0; i < n; ++i) pair |= op[i] == 2;
+  for (int i = 0; i < n; ++i) {
+    const int feats = op[i] == 2 ? N[i] / 2 : N[i];
+    t += gemm_tc_tiles((feats + 127) / 128, M, pair);
+  }
+  return t;
+}
+}  // namespace
+
+extern "C" size_t dflash_test_program_scratch(int32_t n_phases, int32_t M, const int32_t *N,
+                                              const int32_t *op) {
+  if (n_phases <= 0 || n_phases > kMaxPhases || M <= 0 || !N || !op) return 0;
+  return 256 + gemm_tc_partials_bytes() + 4 * (size_t)program_tiles(n_phases, M, N, op) + 256;
+}
+
+extern "C" int dflash_test_gemm_program(int32_t n_phases, int32_t M, const int32_t *N,
+                                        const int32_t *K, const void *const *A,
+                                        const void *const *W, const int32_t *op,
+                                        void *const *out, void *scratch, size_t scratch_bytes,
+                                        dflash_stream_t stream) {
+  if (n_phases <= 0 || n_phases > kMaxPhases || M <= 0 || !N || !K || !A || !W || !op || !out ||
+      !scratch)
+    return DFLASH_EINVAL;
+  for (int i = 0; i < n_phases; ++i) {
+    if (N[i] <= 0 || K[i] <= 0 || !A[i] || !W[i] || !out[i]) return DFLASH_EINVAL;
+    if (op[i] != 0 && op[i] != 1 && op[i] != 2) return DFLASH_EINVAL;
+    if (op[i] == 2 && N[i] % 2) return DFLASH_EINVAL;
+    if (K[i] % 64) return DFLASH_EUNSUPPORTED;
+  }
+  if (scratch_bytes < dflash_test_program_scratch(n_phases, M, N, op)) return DFLASH_ECAPACITY;
+  cudaStream_t s = (cudaStream_t)stream;
+  GemmProblem P[kMaxPhases];
+  for (int i = 0; i < n_phases; ++i) {
+    std::memset(&P[i], 0, sizeof(P[i]));
+    P[i].A.ptr[0] = A[i];
+    P[i].A.ld = K[i];
+    P[i].A.k_per_src = K[i];
+    P[i].A.n_src = 1;
+    P[i].M = M;
+    P[i].K = K[i];
+    GemmSeg &g = P[i].seg[P[i].nseg++];
+    g.W = W[i];
+    g.ldw = K[i];
+    g.N = N[i];
+    std::memset(&g.epi, 0, sizeof(g.epi));
+    g.epi.op = op[i] == 0 ? EPI_STORE_F32 : op[i] == 1 ? EPI_STORE_ACT : EPI_SWIGLU;
+    g.epi.N = N[i];
+    g.epi.ld = op[i] == 2 ? N[i] / 2 : N[i];
+    g.epi.out_f32 = (float *)out[i];
+    g.epi.out_act = out[i];
+  }
+  const int tiles = program_tiles(n_phases, M, N, op);
+  char *base = (char *)scratch;
+  unsigned int *err = (unsigned int *)base;
+  float *partials = (float *)(base + 256);
+  int *counters = (int *)(base + 256 + gemm_tc_partials_bytes());
+  unsigned int *grid_bar = (unsigned int *)((char *)counters + 4 * (size_t)tiles);
+  if (cudaMemsetAsync(base, 0, 256, s) != cudaSuccess) return DFLASH_ECUDA;
+  if (cudaMemsetAsync(counters, 0, 4 * (size_t)tiles + 256, s) != cudaSuccess) return DFLASH_ECUDA;
+  if (prepare_gemm_tc() != cudaSuccess) return DFLASH_ECUDA;
+  if (launch_gemm_program(P, n_phases, partials, counters, tiles, grid_bar, err, s) != cudaSuccess)
+    return DFLASH_ECUDA;
+  return DFLASH_OK;
+}

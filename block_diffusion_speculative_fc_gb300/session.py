@@ -11,7 +11,8 @@ import torch
 
 from . import (DFLASH_BF16, DFLASH_F32, DflashConfig, DflashKV, DflashWeights, _ptr_array,
                dflash_accept_commit, dflash_bind_workspace, dflash_create, dflash_destroy,
-               dflash_draft_block, dflash_get_error, dflash_inject_context, dflash_workspace_size)
+               dflash_draft_block, dflash_get_error, dflash_inject_context, dflash_workspace_size,
+               _check, load_library)
 
 
 def _stream():
@@ -112,6 +113,13 @@ class DraftSession:
         stride = output_ids.shape[1] if output_ids is not None else 0
         dflash_accept_commit(self.h, batch, draft_ids, posterior, seq_len, accept_len, commit_len,
                              bonus, out_tokens, output_ids, stride, _stream())
+
+    def set_fusion(self, on):
+        """Dependent GEMMs as one fused launch (True) or one launch each (False)."""
+        lib = load_library()
+        lib.dflash_test_set_fusion.argtypes = [ctypes.c_void_p, ctypes.c_int32]
+        lib.dflash_test_set_fusion.restype = ctypes.c_int
+        _check(lib.dflash_test_set_fusion(self.h, 1 if on else 0))
 
     def error(self):
         return dflash_get_error(self.h, _stream())

@@ -40,6 +40,27 @@ int dflash_test_gemm_traced(int32_t M, int32_t N, int32_t K, int32_t n_src, cons
                             void *act_out, void *scratch, size_t scratch_bytes,
                             unsigned long long *trace, dflash_stream_t stream);
 
+/*
+ * A chain of up to 4 dependent GEMMs run as one fused tensor-core launch (the
+ * form the draft pass uses for a layer's O-proj / gate-up / down / next-QKV).
+ * Phase i computes Y_i = A_i W_i^T with A_i device bf16 [M, K[i]] (row stride
+ * K[i]) and W_i device bf16 [N[i], K[i]]; op[i] 0 stores Y_i as fp32 [M, N[i]]
+ * into out[i], 1 as bf16 [M, N[i]], 2 stores silu(Y[:, :N/2]) * Y[:, N/2:] as
+ * bf16 [M, N[i]/2].  A later phase may read an earlier phase's bf16 output
+ * (A[i] == out[j], j < i).  N, K, A, W, op, out are HOST arrays of n_phases
+ * entries; scratch: device, at least dflash_test_program_scratch() bytes.
+ */
+size_t dflash_test_program_scratch(int32_t n_phases, int32_t M, const int32_t *N,
+                                   const int32_t *op);
+int dflash_test_gemm_program(int32_t n_phases, int32_t M, const int32_t *N, const int32_t *K,
+                             const void *const *A, const void *const *W, const int32_t *op,
+                             void *const *out, void *scratch, size_t scratch_bytes,
+                             dflash_stream_t stream);
+
+/* Fused launches of dependent GEMMs in the draft pass on (1) or off (0, one
+ * launch per GEMM) for this handle. */
+int dflash_test_set_fusion(dflash_handle *h, int32_t on);
+
 #ifdef __cplusplus
 }
 #endif

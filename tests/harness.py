@@ -51,7 +51,7 @@ def i32(a):
 class CycleRun:
     def __init__(self, cfg, batch, ctx_lens, cycles, seed=0, gains="unit", permuted=False,
                  check=None, match=("bernoulli", 0.85), tol=None, max_rows=None,
-                 extra_pages=2, W=None, Wn=None, pool=None):
+                 extra_pages=2, W=None, Wn=None, pool=None, fused=None):
         self.cfg, self.B, self.cycles, self.seed = cfg, batch, cycles, seed
         self.pool = pool   # prefill rows drawn from this many distinct feature rows
         self.ctx_lens = np.asarray(ctx_lens, dtype=np.int64)
@@ -68,6 +68,8 @@ class CycleRun:
         self.sess = pkg.DraftSession(cfg, self.W, max_batch=batch,
                                      max_rows=max_rows or max(rows_total, batch * S),
                                      max_position=self.ppr * 64 + S)
+        if fused is not None:
+            self.sess.set_fusion(fused)
         self.kv = self.sess.new_kv(batch, self.ppr, self.page_table)
         self.ctx = {b: O.DraftContext(cfg) for b in self.check}
         self.stats = {"hidden_rel": [], "kv_rel": [], "id_mismatch_near_tie": 0, "ids": 0,

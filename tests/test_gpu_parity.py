@@ -96,3 +96,17 @@ def test_many_request_heads_use_the_split_attention():
     lens = np.random.default_rng(5).integers(20, 700, 40)
     run = CycleRun(cfg, 40, lens, cycles=2, permuted=True, check=[0, 17, 39])
     _report(run.run())
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_qwen_mini_fused_and_split_launches(fused):
+    """The per-layer GEMM chain and the injection as one fused launch each, or
+    as one launch per GEMM: both must match the oracle."""
+    run = CycleRun(QWEN_MINI, 3, [100, 37, 260], cycles=3, gains="random", permuted=True,
+                   fused=fused)
+    _report(run.run())
+
+
+def test_kimi_mini_fused_launches():
+    run = CycleRun(KIMI_MINI, 2, [150, 64], cycles=3, gains="random", permuted=True, fused=True)
+    _report(run.run())
