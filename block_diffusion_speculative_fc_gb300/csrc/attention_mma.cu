@@ -11,9 +11,9 @@
 // query rows of its query-head group.  Its context pages are cut into splits of
 // `pps` pages; the last split also takes the S block keys.  A prep kernel
 // sizes the splits from the device-side kv_len so that the whole batch makes
-// about two work items per SM, and a persistent kernel walks the item list.
+// about one work item per resident CTA, and a persistent kernel walks the item list.
 // Per item: one 64-key tile at a time (one KV page of one head: two TMA boxes
-// of 64 rows x 64 dims for K and two for V, 128-byte swizzle, 3-stage ring),
+// of 64 rows x 64 dims for K and two for V, 128-byte swizzle, 2-stage ring),
 // S = Q K^T and O += P V with mma.sync m16n8k16 (bf16 in, fp32 accumulate),
 // online softmax in registers with quad shuffles.  A split that is not alone
 // writes (O, m, l) to scratch; the last split of a (b, g) to finish (atomic
@@ -34,12 +34,13 @@ namespace dflash {
 namespace att {
 
 constexpr int KT = 64;          // keys per tile (one page)
-constexpr int STAGES = 3;
+constexpr int STAGES = 2;       // 2 x 32 KB: three CTAs of <= 128 threads fit on an SM
 constexpr int TILE_BYTES = KT * 128 * 2;   // K (or V) tile: 64 keys x 128 dims
 constexpr int STAGE_BYTES = 2 * TILE_BYTES;
 constexpr int MAX_SPLITS = 16;  // splits of one (request, KV head) at most
 constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 64 + (MAX_SPLITS + 1) * 128 * 4;
 constexpr uint32_t WAIT_LIMIT = 1u << 22;
+constexpr int kMaxCluster = 16;  // CTAs per (request, KV head) in the cluster kernel
 
 struct Params {
   CUtensorMap tmK, tmV;          // cache: dims {D, KVH, n_pages*64}, box {64, 1, 64}
@@ -145,7 +146,7 @@ __global__ void attn_prep_kernel(const int *__restrict__ kv_len, int B, int kvh,
   __syncthreads();
   if (threadIdx.x == 0) {
     const int total = s_total;
-    // about one item per SM, at least two pages per split, at most MAX_SPLITS
+    // about one item per resident CTA, at least two pages per split, at most MAX_SPLITS
     // splits per (request, head), and never more items than the scratch holds
     int pps = max(2, (total + target_items - 1) / target_items);
     while (B * kvh + total / pps + 1 > max_items) ++pps;
@@ -178,9 +179,38 @@ struct Acc {
   float m0, m1, l0, l1;
 };
 
+// One 64-key tile into ring stage u: context page `lp` of request b, head g
+// (its cache page looked up in the page table), or the S block keys.
+__device__ __forceinline__ void issue_tile(const Params &p, uint8_t *smem, uint64_t *full,
+                                           uint32_t u, int b, int g, int lp, bool block) {
+  uint8_t *st = smem + (u % STAGES) * STAGE_BYTES;
+  uint64_t *bar = &full[u % STAGES];
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(bar)),
+               "r"(STAGE_BYTES)
+               : "memory");
+  if (!block) {
+    int page = p.page_table[(size_t)b * p.pages_per_req + lp];
+    if (page < 0 || page >= p.n_pages) {
+      raise_error(p.err, DFLASH_DERR_PAGE_RANGE);
+      page = 0;
+    }
+    tma3(st, &p.tmK, bar, 0, g, page * KT);
+    tma3(st + TILE_BYTES / 2, &p.tmK, bar, 64, g, page * KT);
+    tma3(st + TILE_BYTES, &p.tmV, bar, 0, g, page * KT);
+    tma3(st + TILE_BYTES + TILE_BYTES / 2, &p.tmV, bar, 64, g, page * KT);
+  } else {
+    tma3(st, &p.tmKb, bar, 0, g, b * p.S);
+    tma3(st + TILE_BYTES / 2, &p.tmKb, bar, 64, g, b * p.S);
+    tma3(st + TILE_BYTES, &p.tmVb, bar, 0, g, b * p.S);
+    tma3(st + TILE_BYTES + TILE_BYTES / 2, &p.tmVb, bar, 64, g, b * p.S);
+  }
+}
+
+// `pre`: tiles 0..pre-1 were already issued by the caller (context tiles,
+// issued before the predecessor kernel finished).
 __device__ __forceinline__ bool attend(const Params &p, uint8_t *smem, uint64_t *full, uint32_t &use,
                                        int b, int g, int kv, int first_page, int pg0, int pg1,
-                                       bool has_block, Acc &a) {
+                                       bool has_block, Acc &a, int pre = 0) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int grp = lane >> 2, tig = lane & 3;
   const int S = p.S, R = p.R, G = p.n_heads / p.kvh;
@@ -221,31 +251,10 @@ __device__ __forceinline__ bool attend(const Params &p, uint8_t *smem, uint64_t 
   const int lo1 = p.window > 0 ? kv + j1 - p.window + 1 : 0;
 
   auto issue = [&](int t, uint32_t u) {
-    uint8_t *st = smem + (u % STAGES) * STAGE_BYTES;
-    uint64_t *bar = &full[u % STAGES];
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(bar)),
-                 "r"(STAGE_BYTES)
-                 : "memory");
-    if (t < pg1 - pg0) {
-      const int lp = first_page + pg0 + t;
-      int page = p.page_table[(size_t)b * p.pages_per_req + lp];
-      if (page < 0 || page >= p.n_pages) {
-        raise_error(p.err, DFLASH_DERR_PAGE_RANGE);
-        page = 0;
-      }
-      tma3(st, &p.tmK, bar, 0, g, page * KT);
-      tma3(st + TILE_BYTES / 2, &p.tmK, bar, 64, g, page * KT);
-      tma3(st + TILE_BYTES, &p.tmV, bar, 0, g, page * KT);
-      tma3(st + TILE_BYTES + TILE_BYTES / 2, &p.tmV, bar, 64, g, page * KT);
-    } else {
-      tma3(st, &p.tmKb, bar, 0, g, b * S);
-      tma3(st + TILE_BYTES / 2, &p.tmKb, bar, 64, g, b * S);
-      tma3(st + TILE_BYTES, &p.tmVb, bar, 0, g, b * S);
-      tma3(st + TILE_BYTES + TILE_BYTES / 2, &p.tmVb, bar, 64, g, b * S);
-    }
+    issue_tile(p, smem, full, u, b, g, first_page + pg0 + t, t >= pg1 - pg0);
   };
   if (threadIdx.x == 0)
-    for (int t = 0; t < STAGES && t < ntiles; ++t) issue(t, use + t);
+    for (int t = pre; t < STAGES && t < ntiles; ++t) issue(t, use + t);
 
   bool ok = true;
   for (int t = 0; t < ntiles; ++t) {
@@ -273,25 +282,40 @@ __device__ __forceinline__ bool attend(const Params &p, uint8_t *smem, uint64_t 
         mma16816(s[nt], qa[kc * 2 + 1], b2, b3);
       }
     }
-    // ---- mask, online softmax
+    // ---- mask, online softmax.  A context tile that every row of the warp
+    // sees whole (all but the last tile and the window edge) needs no mask.
     float mx0 = -INFINITY, mx1 = -INFINITY;
+    const bool whole = __all_sync(0xffffffffu, !blk && pos0 + KT <= kv && pos0 >= lo0 &&
+                                                   pos0 >= lo1 && r1 < R);
+    if (whole) {
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
+      for (int nt = 0; nt < 8; ++nt) {
+        s[nt][0] *= p.scale_log2;
+        s[nt][1] *= p.scale_log2;
+        s[nt][2] *= p.scale_log2;
+        s[nt][3] *= p.scale_log2;
+        mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
+        mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
+      }
+    } else {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int key = nt * 8 + tig * 2 + (e & 1);
-        const bool row1 = e >= 2;
-        bool vis;
-        if (blk) {
-          vis = key < S;
-        } else {
-          const int pos = pos0 + key;
-          vis = pos < kv && pos >= (row1 ? lo1 : lo0);
+      for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int key = nt * 8 + tig * 2 + (e & 1);
+          const bool row1 = e >= 2;
+          bool vis;
+          if (blk) {
+            vis = key < S;
+          } else {
+            const int pos = pos0 + key;
+            vis = pos < kv && pos >= (row1 ? lo1 : lo0);
+          }
+          if ((row1 ? r1 : r0) >= R) vis = false;
+          const float v = vis ? s[nt][e] * p.scale_log2 : -INFINITY;
+          s[nt][e] = v;
+          if (row1) mx1 = fmaxf(mx1, v); else mx0 = fmaxf(mx0, v);
         }
-        if ((row1 ? r1 : r0) >= R) vis = false;
-        const float v = vis ? s[nt][e] * p.scale_log2 : -INFINITY;
-        s[nt][e] = v;
-        if (row1) mx1 = fmaxf(mx1, v); else mx0 = fmaxf(mx0, v);
       }
     }
     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
@@ -356,7 +380,11 @@ __device__ __forceinline__ bool attend(const Params &p, uint8_t *smem, uint64_t 
 }
 
 // ---------------------------------------------------------------- main kernel
-__global__ void __launch_bounds__(256) attn_mma_kernel(const __grid_constant__ Params p) {
+// MAXT: threads per CTA this instantiation is built for; up to 128 threads
+// (G*S <= 64 query rows) three CTAs share an SM, which is what hides the
+// latency of the per-tile MMA/softmax chain.
+template <int MAXT>
+__global__ void __launch_bounds__(MAXT, MAXT <= 128 ? 3 : 1) attn_mma_kernel(const __grid_constant__ Params p) {
   pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -487,7 +515,6 @@ __global__ void __launch_bounds__(256) attn_mma_kernel(const __grid_constant__ P
 // block keys), then the C partial results are merged through distributed
 // shared memory -- no scratch in global memory, no tickets, no prep kernel.
 __global__ void __launch_bounds__(256) attn_cluster_kernel(const __grid_constant__ Params p) {
-  pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t *full = (uint64_t *)(smem + STAGES * STAGE_BYTES);
@@ -514,9 +541,16 @@ __global__ void __launch_bounds__(256) attn_cluster_kernel(const __grid_constant
   const int first_page = lo / KT;
   const int pages = kv > lo ? (kv - 1) / KT - first_page + 1 : 0;
   const int pg0 = pages * rank / C, pg1 = pages * (rank + 1) / C;
+  // The context pages, kv_len and the page table were written before the
+  // previous kernel started (only Q and the block K/V come from it): their
+  // first tiles go out before waiting for it.
+  const int pre = min(STAGES, pg1 - pg0);
+  if (threadIdx.x == 0)
+    for (int t = 0; t < pre; ++t) issue_tile(p, smem, full, t, b, g, first_page + pg0 + t, false);
+  pdl_wait();
   uint32_t use = 0;
   Acc acc;
-  attend(p, smem, full, use, b, g, kv, first_page, pg0, pg1, rank == C - 1, acc);
+  attend(p, smem, full, use, b, g, kv, first_page, pg0, pg1, rank == C - 1, acc, pre);
   // this CTA's partial (unnormalised O, row max, row sum) into its own shared memory;
   // the stage ring is free: attend() ends every tile with a CTA barrier
   float *po = reinterpret_cast<float *>(smem);                    // [R][128]
@@ -533,33 +567,37 @@ __global__ void __launch_bounds__(256) attn_cluster_kernel(const __grid_constant
     if (tig == 0) pml[r] = make_float2(hh ? acc.m1 : acc.m0, hh ? acc.l1 : acc.l0);
   }
   cl.sync();
-  // rank r merges rows [R*r/C, R*(r+1)/C) from every CTA of the cluster
+  // rank r merges rows [R*r/C, R*(r+1)/C) from every CTA of the cluster; all
+  // remote loads of an item go out before any arithmetic
   const int rb = R * rank / C, re = R * (rank + 1) / C;
   const int nthr = blockDim.x;
   for (int idx = threadIdx.x; idx < (re - rb) * 32; idx += nthr) {
     const int r = rb + idx / 32, d = (idx % 32) * 4;
-    float ms[8], ls[8];
+    float2 ml[kMaxCluster];
+    float4 v[kMaxCluster];
+#pragma unroll
+    for (int c = 0; c < kMaxCluster; ++c) {
+      if (c >= C) break;
+      ml[c] = cl.map_shared_rank(pml, c)[r];
+      v[c] = *reinterpret_cast<const float4 *>(cl.map_shared_rank(po, c) + r * 128 + d);
+    }
     float mstar = -INFINITY;
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
+    for (int c = 0; c < kMaxCluster; ++c) {
       if (c >= C) break;
-      const float2 ml = cl.map_shared_rank(pml, c)[r];
-      ms[c] = ml.x;
-      ls[c] = ml.y;
-      mstar = fmaxf(mstar, ml.x);
+      mstar = fmaxf(mstar, ml[c].x);
     }
     float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
     float den = 0.f;
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
+    for (int c = 0; c < kMaxCluster; ++c) {
       if (c >= C) break;
-      const float w = ms[c] == -INFINITY ? 0.f : exp2f(ms[c] - mstar);
-      const float4 v = *reinterpret_cast<const float4 *>(cl.map_shared_rank(po, c) + r * 128 + d);
-      num.x += w * v.x;
-      num.y += w * v.y;
-      num.z += w * v.z;
-      num.w += w * v.w;
-      den += w * ls[c];
+      const float w = ml[c].x == -INFINITY ? 0.f : exp2f(ml[c].x - mstar);
+      num.x += w * v[c].x;
+      num.y += w * v[c].y;
+      num.z += w * v[c].z;
+      num.w += w * v[c].w;
+      den += w * ml[c].y;
     }
     const float inv = 1.f / den;
     const int h = g * G + r / S, j = r % S;
@@ -606,18 +644,48 @@ bool encode_kv(CUtensorMap *tm, const void *base, uint64_t rows, int kvh) {
 }  // namespace
 
 size_t attention_mma_scratch_items(int max_batch, int kvh) {
-  return (size_t)max_batch * kvh + 2 * (size_t)kTcMaxCtas + 8;
+  return (size_t)max_batch * kvh + 3 * (size_t)kTcMaxCtas + 8;
 }
 
 cudaError_t prepare_attention_mma() {
-  cudaError_t e = cudaFuncSetAttribute(att::attn_mma_kernel,
+  cudaError_t e = cudaFuncSetAttribute(att::attn_mma_kernel<128>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, att::SMEM);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(att::attn_mma_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           att::SMEM);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(att::attn_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            att::SMEM);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(att::attn_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+  return cudaFuncSetAttribute(att::attn_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
 }
+
+namespace {
+// Whether clusters of C CTAs of the cluster kernel (warps warps each) can be
+// placed on this device at all; answered once per (C, warps).
+bool cluster_fits(int C, int warps) {
+  static int known[att::kMaxCluster + 1][9] = {};
+  int &k = known[C][warps];
+  if (k == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(C);
+    cfg.blockDim = dim3(warps * 32);
+    cfg.dynamicSmemBytes = att::SMEM;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = C;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    k = (cudaOccupancyMaxActiveClusters(&n, att::attn_cluster_kernel, &cfg) == cudaSuccess && n > 0)
+            ? 1 : -1;
+    cudaGetLastError();
+  }
+  return k > 0;
+}
+}  // namespace
 
 cudaError_t launch_attention_mma(const AttnParams &a, const AttnScratch &w, cudaStream_t s) {
   if (a.B <= 0) return cudaSuccess;
@@ -653,8 +721,10 @@ cudaError_t launch_attention_mma(const AttnParams &a, const AttnScratch &w, cuda
   // Few (request, head) pairs: a cluster of C CTAs per pair, merged on chip.
   const int pairs = a.B * a.n_kv_heads;
   if (4 * pairs <= 2 * sms) {
-    int C = 8;
-    while (C > 4 && C * pairs > 2 * sms) C >>= 1;
+    // as many CTAs per pair as fit in one wave (two clusters' CTAs share an SM)
+    int C = 16;
+    while (C > 4 && (C * pairs > 2 * sms || (C > 8 && (C * pairs > sms || !cluster_fits(C, warps)))))
+      C >>= 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(pairs * C);
     cfg.blockDim = dim3(warps * 32);
@@ -672,8 +742,9 @@ cudaError_t launch_attention_mma(const AttnParams &a, const AttnScratch &w, cuda
     return cudaLaunchKernelEx(&cfg, att::attn_cluster_kernel, p);
   }
   const int max_items = (int)attention_mma_scratch_items(a.B, a.n_kv_heads);
+  const int per_sm = warps <= 4 ? 3 : 1;   // resident CTAs per SM (shared memory / registers)
   cudaError_t e = launch_pdl(att::attn_prep_kernel, dim3(1), dim3(256), 0, s, a.kv_len, a.B,
-                             a.n_kv_heads, a.pages_per_req * att::KT, a.window, 2 * sms,
+                             a.n_kv_heads, a.pages_per_req * att::KT, a.window, per_sm * sms,
                              max_items, w.item_start, w.pps, a.err);
   if (e != cudaSuccess) return e;
   p.item_start = w.item_start;
@@ -682,7 +753,9 @@ cudaError_t launch_attention_mma(const AttnParams &a, const AttnScratch &w, cuda
   p.part_ml = (float2 *)w.part_ml;
   p.tickets = w.tickets;
   p.max_items = max_items;
-  return launch_pdl(att::attn_mma_kernel, dim3(2 * sms), dim3(warps * 32), att::SMEM, s, p);
+  if (warps <= 4)
+    return launch_pdl(att::attn_mma_kernel<128>, dim3(per_sm * sms), dim3(warps * 32), att::SMEM, s, p);
+  return launch_pdl(att::attn_mma_kernel<256>, dim3(per_sm * sms), dim3(warps * 32), att::SMEM, s, p);
 }
 
 }  // namespace dflash

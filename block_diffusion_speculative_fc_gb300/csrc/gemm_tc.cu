@@ -26,11 +26,14 @@
 // producer streams the next phase's weights into free ring slots before it
 // waits -- the weight stream does not stop at a GEMM boundary.
 // Work split (stream-K): per phase, the flattened (tile, k-block) iteration
-// space is cut into gridDim.x equal contiguous ranges.  A tile covered by one CTA is
-// finished directly; a tile shared by several CTAs has each write an fp32
-// partial, and the last to arrive (atomic ticket, no waiting on other CTAs)
-// sums the partials in CTA order -- a fixed order, so results are
-// deterministic -- and runs the epilogue.
+// space is cut into equal contiguous ranges, one per CTA.  A tile covered by
+// one CTA is finished directly.  A tile shared by several CTAs is finished by
+// its owner, the CTA holding its first k-block -- for that CTA the tile is
+// the last segment of its range, so the owner merges after all its other
+// work.  The other contributors publish fp32 shares and a count; the owner
+// waits for the count (every CTA is resident), pulls the shares into shared
+// memory by bulk copy, adds them to its own share in CTA order -- a fixed
+// order, so results are deterministic -- and runs the epilogue.
 // Every mbarrier wait is bounded; a wait that gives up raises
 // DFLASH_DERR_TIMEOUT and the CTA winds down instead of hanging.
 #include <cuda.h>
@@ -49,6 +52,9 @@ constexpr int BK = 64;            // k elements per stage: one 128-byte swizzle 
 constexpr int THREADS = 192;
 constexpr int EPI_WARP0 = 2;
 constexpr uint32_t WAIT_LIMIT = 1u << 22;
+// Trace slots per CTA: 0..7 launch-level stamps, then 4 per phase (inputs
+// ready at the producer, first MMA, last MMA, epilogue done).
+constexpr int kTraceSlots = 8 + 4 * kMaxPhases;
 
 // One GEMM of a program: its operands, epilogues and stream-K schedule.
 struct Phase {
@@ -72,7 +78,7 @@ struct Params {
   int *counters;                  // tickets of every phase, zero between launches
   unsigned int *grid_bar;         // [2] phase arrivals, exits; zero between launches
   unsigned int *err;
-  unsigned long long *trace;      // optional [gridDim.x][8] phase timestamps (ns), test builds only
+  unsigned long long *trace;      // optional [gridDim.x][kTraceSlots] timestamps (ns), test entries only
 };
 
 // ------------------------------------------------------------------ PTX
@@ -124,6 +130,14 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *tm, ui
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
       " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(su32(dst)),
       "l"((uint64_t)tm), "r"(su32(bar)), "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
+// Untiled bulk copy global -> shared (16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          su32(dst)),
+      "l"((uint64_t)src), "r"(bytes), "r"(su32(bar))
       : "memory");
 }
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *tm) {
@@ -179,7 +193,7 @@ __device__ __forceinline__ void stamp(const Params &p, int slot) {
   if (p.trace) {
     unsigned long long t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    p.trace[blockIdx.x * 8 + slot] = t;
+    p.trace[blockIdx.x * kTraceSlots + slot] = t;
   }
 }
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
@@ -273,17 +287,24 @@ struct Cfg {
   static constexpr int SLOT_BYTES = W_BYTES + A_BYTES;
   static constexpr int CH = BN < 32 ? BN : 32;            // epilogue token chunk
   static constexpr int STAGING_BYTES = P * CH * 128 * 4;
-  static constexpr int BAR_BYTES = 2048;   // mbarriers, TMEM slot, flag, epilogue scratch, row scales
+  // stream-K merge area: shares of a (row chunk, half) of a split tile, one
+  // bulk copy each
+  static constexpr int CHUNK_BYTES = CH * 128 * 4;
+  static constexpr int MERGE_BYTES = BN >= 256 ? 16 * 1024 : 48 * 1024;
+  static constexpr int MERGE_SLOTS = MERGE_BYTES / CHUNK_BYTES;
+  static constexpr int BAR_BYTES = 2048;   // mbarriers, TMEM slot, epilogue scratch, row scales
   static constexpr int BUDGET = 225 * 1024;
-  static constexpr int SLOTS_RAW = (BUDGET - 1024 - STAGING_BYTES - BAR_BYTES) / SLOT_BYTES;
+  static constexpr int SLOTS_RAW =
+      (BUDGET - 1024 - STAGING_BYTES - MERGE_BYTES - BAR_BYTES) / SLOT_BYTES;
   static constexpr int SLOTS = SLOTS_RAW > 24 ? 24 : SLOTS_RAW;
-  static constexpr int SMEM = 1024 + SLOTS * SLOT_BYTES + STAGING_BYTES + BAR_BYTES;
+  static constexpr int SMEM = 1024 + SLOTS * SLOT_BYTES + STAGING_BYTES + MERGE_BYTES + BAR_BYTES;
   static constexpr int ACC_COLS = P * BN;                 // one accumulator buffer
   static constexpr int TMEM_COLS = 2 * ACC_COLS <= 32 ? 32 : (2 * ACC_COLS <= 64 ? 64 :
                                    (2 * ACC_COLS <= 128 ? 128 : (2 * ACC_COLS <= 256 ? 256 : 512)));
-  static_assert(SLOTS >= 4, "a paired k-block needs two slots and two k-blocks must fit");
+  static_assert(SLOTS >= (PAIRABLE ? 4 : 3), "two k-blocks (paired: two slots each) must fit");
+  static_assert(MERGE_SLOTS >= 1, "merge area");
   static_assert(2 * ACC_COLS <= 512, "accumulators exceed TMEM");
-  static_assert(2 * SLOTS * 8 + 5 * 8 + 8 <= 512, "barrier region");
+  static_assert(2 * SLOTS * 8 + 6 * 8 <= 496, "barrier region");
 };
 
 // Bounded acquire-spin on a grid barrier word; false = gave up.
@@ -293,6 +314,16 @@ __device__ __forceinline__ bool grid_wait(const unsigned int *bar, unsigned int 
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(bar) : "memory");
     if (v >= target) return true;
     __nanosleep(100);
+  }
+  return false;
+}
+// Bounded acquire-spin until a counter reaches `target`; false = gave up.
+__device__ __forceinline__ bool counter_wait(const int *ctr, int target) {
+  for (uint32_t i = 0; i < 4 * WAIT_LIMIT; ++i) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+    if (v >= target) return true;
+    __nanosleep(64);
   }
   return false;
 }
@@ -352,10 +383,12 @@ __device__ __forceinline__ bool phase_inputs_ready(const Params &p, int ph_i, in
     stamp(p, 2);
     pdl_wait();
     stamp(p, 3);
+    stamp(p, 8);
     return true;
   }
   const bool ok = grid_wait(p.grid_bar, (unsigned)(ph_i * G));
   fence_proxy_async();   // later TMA reads see the other CTAs' generic stores
+  stamp(p, 8 + 4 * ph_i);
   return ok;
 }
 
@@ -442,13 +475,14 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
   uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t *slots = smem;
   float *staging = (float *)(smem + C::SLOTS * C::SLOT_BYTES);
-  uint8_t *barbase = smem + C::SLOTS * C::SLOT_BYTES + C::STAGING_BYTES;
+  float *merge = (float *)(smem + C::SLOTS * C::SLOT_BYTES + C::STAGING_BYTES);
+  uint8_t *barbase = smem + C::SLOTS * C::SLOT_BYTES + C::STAGING_BYTES + C::MERGE_BYTES;
   uint64_t *bars = (uint64_t *)barbase;
   uint64_t *full = bars, *empty = bars + C::SLOTS;
   uint64_t *acc_full = bars + 2 * C::SLOTS, *acc_empty = acc_full + 2;
   uint64_t *mma_done = acc_empty + 2;
+  uint64_t *merge_bar = mma_done + 1;
   uint32_t *tmem_slot = (uint32_t *)(barbase + 496);
-  int *flag = (int *)(barbase + 500);
   int *s_int = (int *)(barbase + 512);        // kEpiScratchInts ints
   float *s_rstd = (float *)(barbase + 1024);  // [BN] deferred-norm row scales
 
@@ -466,6 +500,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
       mbar_init(&acc_empty[i], 4);
     }
     mbar_init(mma_done, 1);
+    mbar_init(merge_bar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
@@ -538,8 +573,10 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
             ok = mma_kblocks<C, 1, BN>(it, kb0, kb1, d0, slots, full, empty, p);
           if (!ok) break;
           umma_commit(&acc_full[buf]);
+          if (i == R.b) stamp(p, 9 + 4 * ph_i);   // first segment's MMAs issued
           i += kb1 - kb0;
         }
+        if (R.e > R.b) stamp(p, 10 + 4 * ph_i);
       }
       if (!ok) raise_error(p.err, DFLASH_DERR_TIMEOUT);
       // every MMA issued by this thread must be complete before TMEM is freed
@@ -555,6 +592,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
     const int f = quarter * 32 + lane;               // output feature row of this thread
     float *st0 = staging, *st1 = staging + C::CH * 128;
     int seg_i = 0;
+    uint32_t merge_phase = 0;   // completed phases of merge_bar
     bool alive = true;
     for (int ph_i = 0; ph_i < p.nph && alive; ++ph_i) {
       const Phase &ph = p.ph[ph_i];
@@ -620,63 +658,72 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
           __syncwarp();
           if (lane == 0) mbar_arrive(&acc_empty[buf]);
         } else {
-          // partial tile: publish this CTA's share, last arriver finishes the tile
-          const long long first_tile = R.b / ps.KB;
-          const int which = tile == first_tile ? 0 : 1;
-          float *mine = p.partials + ((size_t)cta * 2 + which) * (C::P * BN * 128);
-          for (int c0 = 0; c0 < BN; c0 += C::CH) {
-            float v[32];
-            for (int q = 0; q < np; ++q) {
-              tmem_ld16(tacc + q * BN + c0, v);
-              if (C::CH == 32) tmem_ld16(tacc + q * BN + c0 + 16, v + 16);
-#pragma unroll
-              for (int t = 0; t < C::CH; ++t) mine[(q * BN + c0 + t) * 128 + f] = v[t];
-            }
-          }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&acc_empty[buf]);
-          __threadfence();
-          epi_bar();
+          // Split tile.  Its owner is the CTA holding the tile's first k-block:
+          // the tile is the last segment of that CTA's range, so the owner
+          // merges after all its other work.  Every other contributor
+          // publishes its fp32 share and moves on.
           const int c_first = cta_of_iter((long long)tile * ps.KB, ps.total, ps.G);
           const int c_last = cta_of_iter((long long)(tile + 1) * ps.KB - 1, ps.total, ps.G);
-          int *ticket = p.counters + ph.counter_off + tile;
-          if (tid == 0) {
-            const int old = atomicAdd(ticket, 1);
-            *flag = old == c_last - c_first;
-          }
-          epi_bar();
-          const bool last = *flag != 0;
-          if (last) {
-            __threadfence();
+          int *ticket = p.counters + ph.counter_off + tile;   // shares published so far
+          if (cta != c_first) {
+            const long long first_tile = R.b / ps.KB;
+            const int which = tile == first_tile ? 0 : 1;
+            float *mine = p.partials + ((size_t)cta * 2 + which) * (C::P * BN * 128);
+            for (int c0 = 0; c0 < BN; c0 += C::CH) {
+              float v[32];
+              for (int q = 0; q < np; ++q) {
+                tmem_ld16(tacc + q * BN + c0, v);
+                if (C::CH == 32) tmem_ld16(tacc + q * BN + c0 + 16, v + 16);
+#pragma unroll
+                for (int t = 0; t < C::CH; ++t) mine[(q * BN + c0 + t) * 128 + f] = v[t];
+              }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[buf]);
+            // publish: the barrier orders every thread's share before thread
+            // 0's fence (cumulative), the count goes out after it
+            epi_bar();
+            if (tid == 0) {
+              __threadfence();
+              atomicAdd(ticket, 1);
+            }
+          } else {
+            // Owner: the other shares (every CTA is resident) come into the
+            // merge area by bulk copy -- one memory round trip for up to
+            // MERGE_SLOTS shares -- and are added to the owner's own share,
+            // read from TMEM, in CTA order (a fixed order: deterministic).
+            const int others = c_last - c_first;
+            if (!epi_all(tid == 0 ? counter_wait(ticket, others) : true) && tid == 0)
+              raise_error(p.err, DFLASH_DERR_TIMEOUT);
             for (int c0 = 0; c0 < BN; c0 += C::CH) {
               for (int q = 0; q < np; ++q) {
                 float acc[32];
-#pragma unroll
-                for (int t = 0; t < C::CH; ++t) acc[t] = 0.f;
-                // contributors in CTA order, two at a time so that twice the
-                // loads are in flight; the summation order stays fixed
-                auto slot_of = [&](int c) {
-                  const long long cfirst_tile = (ps.total * c / ps.G) / ps.KB;
-                  const int w = tile == cfirst_tile ? 0 : 1;
-                  return p.partials + ((size_t)c * 2 + w) * (C::P * BN * 128) + (q * BN + c0) * 128 + f;
-                };
-                int c = c_first;
-                for (; c < c_last; c += 2) {
-                  const float *a = slot_of(c), *b2 = slot_of(c + 1);
-                  float va[32], vb[32];
-#pragma unroll
-                  for (int t = 0; t < C::CH; ++t) {
-                    va[t] = __ldcg(a + t * 128);
-                    vb[t] = __ldcg(b2 + t * 128);
+                tmem_ld16(tacc + q * BN + c0, acc);
+                if (C::CH == 32) tmem_ld16(tacc + q * BN + c0 + 16, acc + 16);
+                for (int k0 = 0; k0 < others; k0 += C::MERGE_SLOTS) {
+                  const int kn = min(C::MERGE_SLOTS, others - k0);
+                  if (tid == 0) {
+                    fence_proxy_async();   // the shares were written by generic stores
+                    mbar_expect_tx(merge_bar, kn * C::CHUNK_BYTES);
+                    for (int k = 0; k < kn; ++k) {
+                      const int c = c_first + 1 + k0 + k;
+                      const long long cfirst_tile = (ps.total * c / ps.G) / ps.KB;
+                      const int w = tile == cfirst_tile ? 0 : 1;
+                      bulk_g2s(merge + k * (C::CHUNK_BYTES / 4),
+                               p.partials + ((size_t)c * 2 + w) * (C::P * BN * 128) +
+                                   (size_t)(q * BN + c0) * 128,
+                               C::CHUNK_BYTES, merge_bar);
+                    }
                   }
+                  if (!epi_all(mbar_wait(merge_bar, merge_phase & 1)) && tid == 0)
+                    raise_error(p.err, DFLASH_DERR_TIMEOUT);
+                  ++merge_phase;
+                  for (int k = 0; k < kn; ++k) {
 #pragma unroll
-                  for (int t = 0; t < C::CH; ++t) acc[t] = (acc[t] + va[t]) + vb[t];
-                }
-                if (c == c_last) {
-                  const float *a = slot_of(c);
-#pragma unroll
-                  for (int t = 0; t < C::CH; ++t) acc[t] += __ldcg(a + t * 128);
+                    for (int t = 0; t < C::CH; ++t) acc[t] += merge[k * (C::CHUNK_BYTES / 4) + t * 128 + f];
+                  }
+                  epi_bar();   // the merge area may be refilled
                 }
                 float *dst = q ? st1 : st0;
 #pragma unroll
@@ -689,17 +736,24 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
                                 s_rstd + c0);
               epi_bar();
             }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[buf]);
             if (tid == 0) *ticket = 0;   // ready for the next launch
           }
           epi_bar();
         }
       }
       if (!alive) break;
+      if (tid == 0) stamp(p, 11 + 4 * ph_i);
       if (ph_i + 1 < p.nph) {
-        // this CTA's share of the phase is written: count it in the grid barrier
-        __threadfence();
+        // this CTA's share of the phase is written: count it in the grid
+        // barrier (same publication pattern as a split tile's share)
         epi_bar();
-        if (tid == 0) atomicAdd(&p.grid_bar[0], 1u);
+        if (tid == 0) {
+          __threadfence();
+          atomicAdd(&p.grid_bar[0], 1u);
+        }
       }
     }
   }
@@ -828,6 +882,8 @@ bool build_phase(tc::Phase &ph, const GemmProblem &P, int BN, int counter_off) {
 }  // namespace
 
 // Partial-tile scratch: per CTA two slots of (pair ? 2 : 1) * BN * 128 fp32, at most 256 * 128.
+int gemm_tc_trace_slots() { return tc::kTraceSlots; }
+
 size_t gemm_tc_partials_bytes() { return (size_t)kTcMaxCtas * 2 * 256 * 128 * 4; }
 
 int gemm_tc_tiles(int n_tiles, int M, bool pair) {

@@ -103,8 +103,8 @@ struct AttnScratch {
   int *tickets;      // [max_batch * kvh], zero between launches
 };
 
-constexpr int kTcMaxCtas = 160;
-constexpr int kMaxPhases = 4;     // dependent GEMMs fused into one tensor-core launch   // persistent tensor-core GEMM grid cap (>= SM count)
+constexpr int kTcMaxCtas = 160;   // persistent tensor-core GEMM grid cap (>= SM count)
+constexpr int kMaxPhases = 4;     // dependent GEMMs fused into one tensor-core launch
 
 // ---- launchers (return cudaGetLastError()) ----
 cudaError_t launch_gemm_tc(const GemmProblem &P, float *partials, int *counters, int max_tiles,
@@ -115,6 +115,7 @@ cudaError_t launch_gemm_program(const GemmProblem *probs, int n, float *partials
                                 int max_tiles, unsigned int *grid_bar, unsigned int *err,
                                 cudaStream_t s, unsigned long long *trace = nullptr);
 size_t gemm_tc_partials_bytes();
+int gemm_tc_trace_slots();   // timestamps per CTA written by a traced launch
 int gemm_tc_tiles(int n_tiles, int M, bool pair);
 cudaError_t prepare_gemm_tc();
 cudaError_t launch_attention_mma(const AttnParams &p, const AttnScratch &w, cudaStream_t s);

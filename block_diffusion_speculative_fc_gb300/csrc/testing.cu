@@ -88,6 +88,18 @@ extern "C" int dflash_test_gemm_program(int32_t n_phases, int32_t M, const int32
                                         const void *const *W, const int32_t *op,
                                         void *const *out, void *scratch, size_t scratch_bytes,
                                         dflash_stream_t stream) {
+  return dflash_test_gemm_program_traced(n_phases, M, N, K, A, W, op, out, scratch, scratch_bytes,
+                                         nullptr, stream);
+}
+
+extern "C" int32_t dflash_test_trace_slots(void) { return gemm_tc_trace_slots(); }
+
+extern "C" int dflash_test_gemm_program_traced(int32_t n_phases, int32_t M, const int32_t *N,
+                                               const int32_t *K, const void *const *A,
+                                               const void *const *W, const int32_t *op,
+                                               void *const *out, void *scratch,
+                                               size_t scratch_bytes, unsigned long long *trace,
+                                               dflash_stream_t stream) {
   if (n_phases <= 0 || n_phases > kMaxPhases || M <= 0 || !N || !K || !A || !W || !op || !out ||
       !scratch)
     return DFLASH_EINVAL;
@@ -128,7 +140,8 @@ extern "C" int dflash_test_gemm_program(int32_t n_phases, int32_t M, const int32
   if (cudaMemsetAsync(base, 0, 256, s) != cudaSuccess) return DFLASH_ECUDA;
   if (cudaMemsetAsync(counters, 0, 4 * (size_t)tiles + 256, s) != cudaSuccess) return DFLASH_ECUDA;
   if (prepare_gemm_tc() != cudaSuccess) return DFLASH_ECUDA;
-  if (launch_gemm_program(P, n_phases, partials, counters, tiles, grid_bar, err, s) != cudaSuccess)
+  if (launch_gemm_program(P, n_phases, partials, counters, tiles, grid_bar, err, s, trace) !=
+      cudaSuccess)
     return DFLASH_ECUDA;
   return DFLASH_OK;
 }

@@ -30,11 +30,16 @@ int dflash_test_gemm(int32_t M, int32_t N, int32_t K, int32_t n_src, const void 
                      void *act_out, void *scratch, size_t scratch_bytes, dflash_stream_t stream);
 
 /* As dflash_test_gemm; when trace is non-NULL each CTA of the (persistent)
- * GEMM writes 8 %globaltimer stamps (ns) to trace[cta * 8 + slot]: 0 entry,
- * 1 set-up done, 2 weight ring issued, 3 predecessor wait returned, 4 first
- * stage consumed by the MMA warp, 5 last MMA complete, 6 first accumulator
- * received by the epilogue, 7 epilogue done.  Caller provides
- * 8 * (number of SMs) slots (the grid never exceeds 160 CTAs). */
+ * GEMM writes %globaltimer stamps (ns) to trace[cta * dflash_test_trace_slots()
+ * + slot]: 0 entry, 1 set-up done, 2 weight ring issued, 3 predecessor wait
+ * returned, 4 first stage consumed by the MMA warp, 5 last MMA complete, 6
+ * first accumulator received by the epilogue, 7 epilogue done; then per GEMM
+ * phase i (a program has up to 4): 8+4i inputs ready at the producer, 9+4i
+ * first segment's MMAs issued, 10+4i last MMA of the phase issued, 11+4i
+ * epilogue done with the phase.  Slots a CTA never reaches stay untouched.
+ * Caller provides dflash_test_trace_slots() * 160 entries (the grid never
+ * exceeds 160 CTAs). */
+int32_t dflash_test_trace_slots(void);
 int dflash_test_gemm_traced(int32_t M, int32_t N, int32_t K, int32_t n_src, const void *const *A,
                             int32_t lda, const void *W, int32_t ldw, int32_t op, void *out,
                             void *act_out, void *scratch, size_t scratch_bytes,
@@ -56,6 +61,12 @@ int dflash_test_gemm_program(int32_t n_phases, int32_t M, const int32_t *N, cons
                              const void *const *A, const void *const *W, const int32_t *op,
                              void *const *out, void *scratch, size_t scratch_bytes,
                              dflash_stream_t stream);
+
+/* As dflash_test_gemm_program, with the timestamps of dflash_test_gemm_traced. */
+int dflash_test_gemm_program_traced(int32_t n_phases, int32_t M, const int32_t *N, const int32_t *K,
+                                    const void *const *A, const void *const *W, const int32_t *op,
+                                    void *const *out, void *scratch, size_t scratch_bytes,
+                                    unsigned long long *trace, dflash_stream_t stream);
 
 /* Fused launches of dependent GEMMs in the draft pass on (1) or off (0, one
  * launch per GEMM) for this handle. */
