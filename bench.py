@@ -90,6 +90,9 @@ def algorithmic(cfg, B, ctx_mean, commit_mean):
     fam["gemm_layer_program"] = add("gemm_o", "gemm_gate_up", "gemm_down", "gemm_qkv")
     fam["gemm_last_program"] = add("gemm_o", "gemm_gate_up", "gemm_down", "gemm_lm_head_argmax")
     fam["gemm_inject_program"] = add("gemm_fc", "gemm_kv_inject")
+    # block embedding (table rows read; x fp32, x*g bf16 and row sums of squares written)
+    fam["embed"] = (es * M * H + (4 + es) * M * H + 4 * M * (H // 128), 0)
+    fam["gemm_embed_qkv_program"] = add("embed", "gemm_qkv")
     return fam
 
 

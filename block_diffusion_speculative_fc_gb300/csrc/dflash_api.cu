@@ -143,7 +143,9 @@ cudaError_t run_gemm(dflash_handle *h, const GemmProblem &P, cudaStream_t s) {
 
 // Dependent GEMMs of equal row count in one launch (bf16); fp32 runs them one
 // after the other on the CUDA cores.
-cudaError_t run_program(dflash_handle *h, const GemmProblem *P, int n, cudaStream_t s) {
+cudaError_t run_program(dflash_handle *h, const GemmProblem *P, int n, cudaStream_t s,
+                        const ProgramEmbed *embed = nullptr, const ProgramFinalize *fin = nullptr,
+                        const ProgramInject *inject = nullptr) {
   if (h->store == ST_F32) {
     for (int i = 0; i < n; ++i) {
       const cudaError_t e = launch_gemm_simt(ST_F32, P[i], s);
@@ -160,7 +162,7 @@ cudaError_t run_program(dflash_handle *h, const GemmProblem *P, int n, cudaStrea
   }
   return launch_gemm_program(P, n, at<float>(h, h->L.tc_partials), at<int>(h, h->L.tc_counters),
                              h->L.tc_max_tiles, at<unsigned int>(h, h->L.tc_grid_bar),
-                             at<unsigned int>(h, h->L.err), s);
+                             at<unsigned int>(h, h->L.err), s, nullptr, embed, fin, inject);
 }
 
 cudaError_t run_attention(dflash_handle *h, const AttnParams &a, cudaStream_t s) {
@@ -444,14 +446,19 @@ int dflash_inject_context(dflash_handle *h, const dflash_kv *kv, int32_t batch, 
   float *ssq_y = at<float>(h, h->L.ssq_y);
   const float2 *rope = at<const float2>(h, h->L.rope);
 
+  // fused bf16 path: the row map is computed inside the injection launch and,
+  // when that launch is the call's last, so is the kv_len update
+  const bool fused = h->store == ST_BF16 && h->fuse;
+  bool advanced = false;
   for (int64_t r0 = 0; r0 < total_rows; r0 += c.max_rows) {
     const int rows = (int)std::min<int64_t>(c.max_rows, total_rows - r0);
-    int st = timed(h, "inject_prep", s, [&] {
-      return launch_inject_prep(batch, (int)r0, rows, row_offset, n_rows, kv->kv_len,
-                                kv->page_table, kv->pages_per_req, kv->n_pages, c.page_size,
-                                c.max_position, slot, rpos, err, s);
-    });
-    if (st) return st;
+    int st = 0;
+    if (!fused && (st = timed(h, "inject_prep", s, [&] {
+                     return launch_inject_prep(batch, (int)r0, rows, row_offset, n_rows, kv->kv_len,
+                                               kv->page_table, kv->pages_per_req, kv->n_pages,
+                                               c.page_size, c.max_position, slot, rpos, err, s);
+                   })))
+      return st;
     // a1 + a2: concat (K-split over the selected layers) + fc; the epilogue
     // writes y * hidden_norm gain and the row sums of squares of y
     GemmProblem prog[2];
@@ -490,14 +497,34 @@ int dflash_inject_context(dflash_handle *h, const dflash_kv *kv, int32_t batch, 
       return Q;
     };
     prog[1] = kv_problem(0);
+    ProgramInject inj;
+    std::memset(&inj, 0, sizeof(inj));
+    inj.B = batch;
+    inj.row0 = (int)r0;
+    inj.rows = rows;
+    inj.row_offset = row_offset;
+    inj.n_rows = n_rows;
+    inj.kv_len = kv->kv_len;
+    inj.page_table = kv->page_table;
+    inj.pages_per_req = kv->pages_per_req;
+    inj.n_pages = kv->n_pages;
+    inj.page_size = c.page_size;
+    inj.max_position = c.max_position;
+    inj.row_slot = slot;
+    inj.row_pos = rpos;
+    inj.total_rows = total_rows;
+    inj.advance = r0 + rows >= total_rows && c.n_layers <= kMaxSeg;
+    advanced = fused && inj.advance;
     // fc and the first group of layers' K/V in one launch
-    if ((st = timed(h, "gemm_inject_program", s, [&] { return run_program(h, prog, 2, s); })))
+    if ((st = timed(h, "gemm_inject_program", s,
+                    [&] { return run_program(h, prog, 2, s, nullptr, nullptr, fused ? &inj : nullptr); })))
       return st;
     for (int l0 = kMaxSeg; l0 < c.n_layers; l0 += kMaxSeg) {
       GemmProblem Q = kv_problem(l0);
       if ((st = timed(h, "gemm_kv_inject", s, [&] { return run_gemm(h, Q, s); }))) return st;
     }
   }
+  if (advanced) return DFLASH_OK;
   return timed(h, "inject_finalize", s, [&] {
     return launch_inject_finalize(batch, total_rows, row_offset, n_rows, kv->kv_len,
                                   kv->pages_per_req * c.page_size, err, s);
@@ -529,13 +556,16 @@ int dflash_draft_block(dflash_handle *h, const dflash_kv *kv, int32_t batch, con
   const float2 *rope = at<const float2>(h, h->L.rope);
   int st;
 
+  // fused bf16 path: the embedding runs as the first phase of the layer-0
+  // QKV launch, the argmax ids are written by the last CTA of the final launch
+  const bool fused = h->store == ST_BF16 && h->fuse;
   // a4: block embedding [anchor, MASK x (S-1)] at positions kv_len + j, with the
   // first layer's input RMSNorm deferred into its QKV GEMM
-  if ((st = timed(h, "embed", s, [&] {
-         return launch_embed(h->store, h->embed, anchor, kv->kv_len, batch, S, H, c.vocab,
-                             c.mask_token_id, c.max_position, x, h->in_norm_g[0], xg, ssq, ldq,
-                             row_pos, keys, err, s);
-       })))
+  if (!fused && (st = timed(h, "embed", s, [&] {
+                   return launch_embed(h->store, h->embed, anchor, kv->kv_len, batch, S, H,
+                                       c.vocab, c.mask_token_id, c.max_position, x,
+                                       h->in_norm_g[0], xg, ssq, ldq, row_pos, keys, err, s);
+                 })))
     return st;
   // a5 of layer l: RMSNorm + QKV GEMM + q/k-norm + RoPE
   auto qkv_problem = [&](int l) {
@@ -555,7 +585,29 @@ int dflash_draft_block(dflash_handle *h, const dflash_kv *kv, int32_t batch, con
   };
   {
     GemmProblem P = qkv_problem(0);
-    if ((st = timed(h, "gemm_qkv", s, [&] { return run_gemm(h, P, s); }))) return st;
+    if (fused) {
+      ProgramEmbed em;
+      em.table = h->embed;
+      em.anchor = anchor;
+      em.kv_len = kv->kv_len;
+      em.M = M;
+      em.S = S;
+      em.H = H;
+      em.vocab = c.vocab;
+      em.mask_id = c.mask_token_id;
+      em.max_position = c.max_position;
+      em.x = x;
+      em.gain = h->in_norm_g[0];
+      em.xg = xg;
+      em.ssq = ssq;
+      em.ssq_ld = ldq;
+      em.row_pos = row_pos;
+      em.keys = keys;
+      if ((st = timed(h, "gemm_embed_qkv_program", s, [&] { return run_program(h, &P, 1, s, &em); })))
+        return st;
+    } else if ((st = timed(h, "gemm_qkv", s, [&] { return run_gemm(h, P, s); }))) {
+      return st;
+    }
   }
   for (int l = 0; l < c.n_layers; ++l) {
     // a6: non-causal block attention over [context ; block]
@@ -626,7 +678,14 @@ int dflash_draft_block(dflash_handle *h, const dflash_kv *kv, int32_t batch, con
       ea.N = c.vocab;
       ea.argmax_keys = keys;
       add_seg(prog[3], h->lm_head, H, c.vocab, ea);
-      if ((st = timed(h, "gemm_last_program", s, [&] { return run_program(h, prog, 4, s); })))
+      ProgramFinalize fin;
+      fin.keys = keys;
+      fin.anchor = anchor;
+      fin.M = M;
+      fin.S = S;
+      fin.draft_ids = draft_ids;
+      if ((st = timed(h, "gemm_last_program", s,
+                      [&] { return run_program(h, prog, 4, s, nullptr, fused ? &fin : nullptr); })))
         return st;
     }
   }
@@ -637,6 +696,7 @@ int dflash_draft_block(dflash_handle *h, const dflash_kv *kv, int32_t batch, con
                                nullptr, s);
        })))
     return st;
+  if (fused) return DFLASH_OK;   // the ids came with the last launch
   return timed(h, "argmax_finalize", s,
                [&] { return launch_argmax_finalize(keys, anchor, batch, S, draft_ids, s); });
 }

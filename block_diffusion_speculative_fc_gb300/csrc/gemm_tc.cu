@@ -43,6 +43,7 @@
 
 #include "common.cuh"
 #include "epilogue.cuh"
+#include "inject_rows.cuh"
 #include "kernels.h"
 
 namespace dflash {
@@ -74,6 +75,9 @@ struct Phase {
 struct Params {
   Phase ph[kMaxPhases];
   int nph;
+  ProgramEmbed emb;               // phase 0 is the embedding when emb.M > 0
+  ProgramFinalize fin;            // draft ids by the last CTA out when fin.M > 0
+  ProgramInject inj;              // injection row map in phase 0 when inj.rows > 0
   float *partials;                // [gridDim.x][2][<= 2*BN][128]
   int *counters;                  // tickets of every phase, zero between launches
   unsigned int *grid_bar;         // [2] phase arrivals, exits; zero between launches
@@ -468,6 +472,60 @@ __device__ __forceinline__ bool produce_phase(const Params &p, const Phase &ph,
   return true;
 }
 
+__device__ __forceinline__ InjectArgs inject_args(const ProgramInject &j) {
+  InjectArgs a;
+  a.B = j.B;
+  a.row_offset = j.row_offset;
+  a.n_rows = j.n_rows;
+  a.kv_len = j.kv_len;
+  a.page_table = j.page_table;
+  a.pages_per_req = j.pages_per_req;
+  a.n_pages = j.n_pages;
+  a.page_size = j.page_size;
+  a.max_position = j.max_position;
+  return a;
+}
+
+// The block embedding of a program's first phase ("Inside SGLang", Step 3:
+// input id = anchor at j = 0, else mask_token_id; position = prefix length +
+// j), with the first layer's deferred RMSNorm operand: x, x * g and the sum
+// of squares of every 128-feature part of x.  Work item = (row, part), one
+// per epilogue warp, spread over the grid.
+__device__ __forceinline__ void program_embed(const ProgramEmbed &e, unsigned int *err, int gwarp,
+                                              int nwarps, int lane) {
+  const int parts = e.H >> 7;
+  for (int item = gwarp; item < e.M * parts; item += nwarps) {
+    const int m = item / parts, t = item - m * parts;
+    const int b = m / e.S, j = m - b * e.S;
+    const int id = j == 0 ? e.anchor[b] : e.mask_id;
+    const bool bad_id = id < 0 || id >= e.vocab;
+    if (t == 0 && lane == 0) {
+      const int pos = e.kv_len[b] + j;
+      const bool bad_pos = pos < 0 || pos >= e.max_position;
+      if (bad_id) raise_error(err, DFLASH_DERR_TOKEN_RANGE);
+      if (bad_pos) raise_error(err, DFLASH_DERR_POSITION);
+      e.row_pos[m] = bad_pos ? 0 : pos;
+      e.keys[m] = 0ull;
+    }
+    const int c = t * 128 + lane * 4;
+    const bf16 *src = (const bf16 *)e.table + (int64_t)(bad_id ? 0 : id) * e.H + c;
+    const bf16 *gp = (const bf16 *)e.gain + c;
+    float v[4], g[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      v[k] = bad_id ? 0.f : __bfloat162float(src[k]);
+      g[k] = __bfloat162float(gp[k]);
+    }
+    float *xr = e.x + (int64_t)m * e.H + c;
+    bf16 *xgr = (bf16 *)e.xg + (int64_t)m * e.H + c;
+    *reinterpret_cast<float4 *>(xr) = make_float4(v[0], v[1], v[2], v[3]);
+    *reinterpret_cast<__nv_bfloat162 *>(xgr) = __floats2bfloat162_rn(v[0] * g[0], v[1] * g[1]);
+    *reinterpret_cast<__nv_bfloat162 *>(xgr + 2) = __floats2bfloat162_rn(v[2] * g[2], v[3] * g[3]);
+    const float ss = warp_sum((v[0] * v[0] + v[1] * v[1]) + (v[2] * v[2] + v[3] * v[3]));
+    if (lane == 0) e.ssq[(int64_t)t * e.ssq_ld + m] = ss;
+  }
+}
+
 template <int BN, bool PAIRABLE, typename T>
 __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_constant__ Params p) {
   using C = Cfg<BN, PAIRABLE>;
@@ -607,6 +665,20 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
         if (tid == 0) raise_error(p.err, DFLASH_DERR_TIMEOUT);
         alive = false;
         break;
+      }
+      if (ph_i == 0 && p.emb.M > 0)
+        program_embed(p.emb, p.err, cta * 4 + ew, G * 4, lane);
+      if (ph_i == 0 && p.inj.rows > 0) {
+        // the K/V phase's row map (read only after the grid barrier)
+        InjectArgs a = inject_args(p.inj);
+        for (int r = cta * 128 + tid; r < p.inj.rows; r += G * 128) {
+          int slot, pos;
+          inject_map_row(a, p.inj.row0 + r, [&](int b) { return a.kv_len[b]; },
+                         [&](int b) { return a.row_offset[b]; }, [&](int b) { return a.n_rows[b]; },
+                         slot, pos, p.err);
+          p.inj.row_slot[r] = slot;
+          p.inj.row_pos[r] = pos;
+        }
       }
       int rstd_m0 = -1, rstd_seg = -1;   // rows whose deferred-norm scales are in s_rstd
       const Range R = cta_range(ps.total, ps.G, cta);
@@ -760,14 +832,31 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
   if (warp == EPI_WARP0 && lane == 0) stamp(p, 7);
   tc_fence_before();
   __syncthreads();
-  if (p.nph > 1 && threadIdx.x == 0) {
-    // the last CTA out clears the barrier words for the next program
-    __threadfence();
-    const unsigned int old = atomicAdd(&p.grid_bar[1], 1u);
-    if (old == (unsigned int)G - 1) {
-      p.grid_bar[0] = 0;
-      p.grid_bar[1] = 0;
+  if (p.nph > 1 || p.fin.M > 0 || p.inj.advance) {
+    // the last CTA out clears the barrier words for the next program and
+    // turns the argmax keys every CTA has contributed to into draft ids
+    if (threadIdx.x == 0) {
       __threadfence();
+      const unsigned int old = atomicAdd(&p.grid_bar[1], 1u);
+      s_int[0] = old == (unsigned int)G - 1;
+      if (old == (unsigned int)G - 1) {
+        p.grid_bar[0] = 0;
+        p.grid_bar[1] = 0;
+        __threadfence();
+      }
+    }
+    __syncthreads();
+    if (s_int[0] && p.inj.advance) {
+      // every CTA has read the old lengths (row map, phase 0) and is done
+      const InjectArgs a = inject_args(p.inj);
+      for (int b = threadIdx.x; b < p.inj.B; b += blockDim.x)
+        inject_advance(a, b, p.inj.total_rows, (int64_t)a.pages_per_req * a.page_size, p.err);
+    }
+    if (s_int[0] && p.fin.M > 0) {
+      for (int m = threadIdx.x; m < p.fin.M; m += blockDim.x) {
+        const int j = m % p.fin.S;
+        p.fin.draft_ids[m] = j == 0 ? p.fin.anchor[m / p.fin.S] : argmax_key_index(__ldcg(p.fin.keys + m));
+      }
     }
   }
   pdl_trigger();   // every global write of this CTA is done
@@ -914,9 +1003,15 @@ cudaError_t prepare_gemm_tc() {
 
 cudaError_t launch_gemm_program(const GemmProblem *probs, int n, float *partials, int *counters,
                                 int max_tiles, unsigned int *grid_bar, unsigned int *err,
-                                cudaStream_t s, unsigned long long *trace) {
-  if (n <= 0 || n > kMaxPhases) return cudaErrorInvalidValue;
-  if (n > 1 && !grid_bar) return cudaErrorInvalidValue;
+                                cudaStream_t s, unsigned long long *trace,
+                                const ProgramEmbed *embed, const ProgramFinalize *fin,
+                                const ProgramInject *inject) {
+  const int lead = embed ? 1 : 0;   // the embedding phase comes first
+  if (n <= 0 || n + lead > kMaxPhases) return cudaErrorInvalidValue;
+  if ((n + lead > 1 || fin || inject) && !grid_bar) return cudaErrorInvalidValue;
+  if (inject && n + lead < 2) return cudaErrorInvalidValue;   // the map is read by a later phase
+  if (embed && (embed->M != probs[0].M || embed->H % 128 || embed->M <= 0))
+    return cudaErrorInvalidValue;
   const int M = probs[0].M;
   if (M <= 0) return cudaSuccess;
   bool any_pair = false;
@@ -929,12 +1024,22 @@ cudaError_t launch_gemm_program(const GemmProblem *probs, int n, float *partials
   memset(&p, 0, sizeof(p));
   int off = 0;
   long long most = 0;
+  if (lead) {
+    p.ph[0].nseg = 0;   // no GEMM work: the epilogue warps embed the block
+    p.ph[0].M = M;
+    p.ph[0].KB = 1;
+    p.ph[0].m_tiles = 1;
+    p.emb = *embed;
+  }
   for (int i = 0; i < n; ++i) {
-    if (!build_phase(p.ph[i], probs[i], BN, off)) return cudaErrorInvalidValue;
-    off += p.ph[i].tiles;
-    most = std::max(most, p.ph[i].total_iters);
+    if (!build_phase(p.ph[lead + i], probs[i], BN, off)) return cudaErrorInvalidValue;
+    off += p.ph[lead + i].tiles;
+    most = std::max(most, p.ph[lead + i].total_iters);
   }
   if (off > max_tiles) return cudaErrorInvalidValue;
+  if (fin) p.fin = *fin;
+  if (inject) p.inj = *inject;
+  n += lead;
   p.nph = n;
   p.partials = partials;
   p.counters = counters;

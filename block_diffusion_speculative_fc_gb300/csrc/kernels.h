@@ -109,11 +109,55 @@ constexpr int kMaxPhases = 4;     // dependent GEMMs fused into one tensor-core 
 // ---- launchers (return cudaGetLastError()) ----
 cudaError_t launch_gemm_tc(const GemmProblem &P, float *partials, int *counters, int max_tiles,
                            unsigned int *err, cudaStream_t s, unsigned long long *trace = nullptr);
+// Work a GEMM program can do besides its GEMMs (bf16 only).
+// ProgramEmbed: the block embedding, as a phase without GEMM work before the
+// first GEMM (rows M = B*S; writes x, x*g, the per-128-feature sums of
+// squares, the RoPE positions and clears the argmax keys -- what
+// launch_embed does).  ProgramFinalize: draft_ids from the argmax keys, done
+// by the last CTA to leave the launch.
+struct ProgramEmbed {
+  const void *table;            // [vocab, H]
+  const int *anchor, *kv_len;   // [B]
+  int M, S, H, vocab, mask_id, max_position;
+  float *x;                     // [M, H]
+  const void *gain;             // [H] first layer's input norm
+  void *xg;                     // [M, H]
+  float *ssq;                   // [H/128][ssq_ld]
+  int ssq_ld;
+  int *row_pos;                 // [M]
+  unsigned long long *keys;     // [M]
+};
+struct ProgramFinalize {
+  const unsigned long long *keys;
+  const int *anchor;            // [B]
+  int M, S;
+  int *draft_ids;               // [M]
+};
+
+// ProgramInject: the injection row map of feature rows row0 .. row0+rows-1
+// (into row_slot / row_pos), computed during the first phase for the K/V
+// phase that follows; with advance set, the last CTA out also advances kv_len
+// by n_rows (what launch_inject_prep / launch_inject_finalize do).
+struct ProgramInject {
+  int B, row0, rows;
+  const int *row_offset, *n_rows;
+  int *kv_len;
+  const int *page_table;
+  int pages_per_req, n_pages, page_size, max_position;
+  int *row_slot, *row_pos;
+  int advance, total_rows;
+};
+
 // Up to kMaxPhases dependent GEMMs of equal row count in one cooperative
-// launch, separated by grid barriers (grid_bar: two zeroed words).
+// launch, separated by grid barriers (grid_bar: two zeroed words); an
+// optional embedding phase first (it takes one of the kMaxPhases) and an
+// optional argmax finalisation at the end.
 cudaError_t launch_gemm_program(const GemmProblem *probs, int n, float *partials, int *counters,
                                 int max_tiles, unsigned int *grid_bar, unsigned int *err,
-                                cudaStream_t s, unsigned long long *trace = nullptr);
+                                cudaStream_t s, unsigned long long *trace = nullptr,
+                                const ProgramEmbed *embed = nullptr,
+                                const ProgramFinalize *fin = nullptr,
+                                const ProgramInject *inject = nullptr);
 size_t gemm_tc_partials_bytes();
 int gemm_tc_trace_slots();   // timestamps per CTA written by a traced launch
 int gemm_tc_tiles(int n_tiles, int M, bool pair);

@@ -1,6 +1,7 @@
 // Row-wise kernels around the GEMMs: block embedding, RMSNorm, argmax
 // finalisation, injection row mapping and the RoPE table.
 #include "common.cuh"
+#include "inject_rows.cuh"
 #include "kernels.h"
 
 namespace dflash {
@@ -158,12 +159,8 @@ cudaError_t launch_argmax_finalize(const unsigned long long *keys, const int *an
 }
 
 // ---------------------------------------------------------------------------
-// Injection row map ("Inside SGLang", Step 7: prefix-valid writes).  For the
-// feature rows row0 .. row0+rows-1 of this chunk: the owning request b is the
-// one with row_offset[b] <= r < row_offset[b] + n_rows[b]; its position is
-// kv_len[b] + (r - row_offset[b]) and its cache row is
-// page_table[b][pos / page] * page + pos % page.  Rows owned by no request,
-// or failing a capacity / page-range / position check, get slot -1.
+// Injection row map of the feature rows row0 .. row0+rows-1 of one chunk
+// (inject_rows.cuh states the map); request data staged in shared memory.
 // ---------------------------------------------------------------------------
 __global__ void inject_prep_kernel(int B, int row0, int rows, const int *__restrict__ row_offset,
                                    const int *__restrict__ n_rows, const int *__restrict__ kv_len,
@@ -182,28 +179,18 @@ __global__ void inject_prep_kernel(int B, int row0, int rows, const int *__restr
   __syncthreads();
   const int local = blockIdx.x * blockDim.x + threadIdx.x;
   if (local >= rows) return;
-  const int r = row0 + local;
-  int slot = -1, pos = 0;
-  for (int b = 0; b < B; ++b) {
-    const int i = r - s_off[b];
-    if (i < 0 || i >= s_n[b]) continue;
-    pos = s_len[b] + i;
-    const int64_t cap = (int64_t)pages_per_req * page_size;
-    if (pos >= cap || pos < 0) {
-      raise_error(err, DFLASH_DERR_KV_CAPACITY);
-    } else if (pos >= max_position) {
-      raise_error(err, DFLASH_DERR_POSITION);
-    } else {
-      const int page = page_table[(int64_t)b * pages_per_req + pos / page_size];
-      if (page < 0 || page >= n_pages)
-        raise_error(err, DFLASH_DERR_PAGE_RANGE);
-      else
-        slot = page * page_size + pos % page_size;
-    }
-    break;
-  }
+  InjectArgs a;
+  a.B = B;
+  a.page_table = page_table;
+  a.pages_per_req = pages_per_req;
+  a.n_pages = n_pages;
+  a.page_size = page_size;
+  a.max_position = max_position;
+  int slot, pos;
+  inject_map_row(a, row0 + local, [&](int b) { return s_len[b]; }, [&](int b) { return s_off[b]; },
+                 [&](int b) { return s_n[b]; }, slot, pos, err);
   row_slot[local] = slot;
-  row_pos[local] = slot < 0 ? 0 : pos;
+  row_pos[local] = pos;
 }
 
 cudaError_t launch_inject_prep(int B, int row0, int rows, const int *row_offset, const int *n_rows,
@@ -217,26 +204,19 @@ cudaError_t launch_inject_prep(int B, int row0, int rows, const int *row_offset,
                     pages_per_req, n_pages, page_size, max_position, row_slot, row_pos, err);
 }
 
-// kv_len[b] += n_rows[b].  A request whose rows do not lie inside the feature
-// buffers, or whose new length passes the page table's capacity, is flagged
-// and its length is not advanced past what was actually written.
+// kv_len[b] += n_rows[b] (inject_rows.cuh).
 __global__ void inject_finalize_kernel(int B, int total_rows, const int *__restrict__ row_offset,
                                        const int *__restrict__ n_rows, int *kv_len, int capacity,
                                        unsigned int *err) {
   pdl_wait();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= B) return;
-  const int n = n_rows[b], off = row_offset[b];
-  if (n <= 0) {
-    if (n < 0) raise_error(err, DFLASH_DERR_ROW_RANGE);
-    return;
-  }
-  if (off < 0 || (int64_t)off + n > total_rows) {
-    raise_error(err, DFLASH_DERR_ROW_RANGE);
-    return;
-  }
-  const int64_t v = (int64_t)kv_len[b] + n;
-  kv_len[b] = (int)(v > capacity ? capacity : v);
+  InjectArgs a;
+  a.B = B;
+  a.row_offset = row_offset;
+  a.n_rows = n_rows;
+  a.kv_len = kv_len;
+  inject_advance(a, b, total_rows, capacity, err);
 }
 
 cudaError_t launch_inject_finalize(int B, int total_rows, const int *row_offset, const int *n_rows,
