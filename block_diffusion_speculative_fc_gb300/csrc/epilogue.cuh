@@ -150,6 +150,92 @@ __device__ __forceinline__ void compute_rstd(const EpiParams &e, int m0, int row
   }
 }
 
+// Element-wise epilogues with wide accesses: a thread takes 8 consecutive
+// features of one row (16-byte stores of bf16, two float4 of fp32), and the
+// per-row sum of squares of the fused-norm ops reduces over the 16 lanes that
+// share the row.  Applies to whole 128-feature tiles whose rows are 16-byte
+// aligned; returns false (scalar path) otherwise.  Same arithmetic and output
+// as the scalar path.
+template <typename T>
+__device__ __forceinline__ bool elementwise_vec(const EpiParams &e, const float *t0,
+                                                const float *t1, int ldt, int m0, int rows,
+                                                int n0, int tid, int nthreads) {
+  const int op = e.op;
+  if (op != EPI_STORE_F32 && op != EPI_RESID && op != EPI_STORE_ACT && op != EPI_SWIGLU &&
+      op != EPI_RESID_NORM && op != EPI_STORE_NORM)
+    return false;
+  const int nvalid = op == EPI_SWIGLU ? e.N / 2 : e.N;
+  const bool f32_out = op == EPI_STORE_F32 || op == EPI_RESID || op == EPI_RESID_NORM;
+  const bool act_out = op == EPI_STORE_ACT || op == EPI_SWIGLU || op == EPI_RESID_NORM ||
+                       op == EPI_STORE_NORM;
+  const bool norm_out = op == EPI_RESID_NORM || op == EPI_STORE_NORM;
+  if (sizeof(T) != 2) return false;   // bf16 outputs (the tensor-core path)
+  if (n0 + 128 > nvalid || (e.ld & 7) || (nthreads & 31) || (ldt & 3)) return false;
+  if (f32_out && ((uintptr_t)e.out_f32 & 15)) return false;
+  if (act_out && ((uintptr_t)e.out_act & 15)) return false;
+  if (norm_out && ((uintptr_t)e.norm_gain & 15)) return false;
+  const int total = rows << 4;
+  const int lane = tid & 31;
+  // whole warps iterate together (the row reduction shuffles); an item past
+  // the end belongs to a 16-lane group that is past the end as a whole
+  for (int it = tid; it - lane < total; it += nthreads) {
+    const bool act = it < total;
+    const int r = it >> 4, c8 = (it & 15) << 3;
+    float ss = 0.f;
+    if (act) {
+      const float4 *src = reinterpret_cast<const float4 *>(t0 + r * ldt + c8);
+      const float4 a = src[0], b = src[1];
+      float y[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+      const int64_t o = (int64_t)(m0 + r) * e.ld + n0 + c8;
+      if (op == EPI_SWIGLU) {
+        const float4 *u = reinterpret_cast<const float4 *>(t1 + r * ldt + c8);
+        const float4 ua = u[0], ub = u[1];
+        const float up[8] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z, ub.w};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) y[k] = silu(y[k]) * up[k];
+      }
+      if (op == EPI_RESID || op == EPI_RESID_NORM) {
+        const float4 *old = reinterpret_cast<const float4 *>(e.out_f32 + o);
+        const float4 oa = old[0], ob = old[1];
+        y[0] += oa.x; y[1] += oa.y; y[2] += oa.z; y[3] += oa.w;
+        y[4] += ob.x; y[5] += ob.y; y[6] += ob.z; y[7] += ob.w;
+      }
+      if (f32_out) {
+        float4 *dst = reinterpret_cast<float4 *>(e.out_f32 + o);
+        dst[0] = make_float4(y[0], y[1], y[2], y[3]);
+        dst[1] = make_float4(y[4], y[5], y[6], y[7]);
+      }
+      if (act_out) {
+        float z[8];
+        if (norm_out) {
+          const uint4 graw = *reinterpret_cast<const uint4 *>((const T *)e.norm_gain + n0 + c8);
+          const T *g = reinterpret_cast<const T *>(&graw);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) z[k] = y[k] * to_f32(g[k]);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) z[k] = y[k];
+        }
+        uint4 packed;
+        T *pk = reinterpret_cast<T *>(&packed);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) pk[k] = from_f32<T>(z[k]);
+        *reinterpret_cast<uint4 *>((T *)e.out_act + o) = packed;
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) ss += y[k] * y[k];
+    }
+    if (norm_out) {
+      // sum of squares of this row's 128 features over the 16 lanes of the
+      // row (every lane of the warp takes part in the shuffles)
+#pragma unroll
+      for (int off = 8; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+      if (act && (it & 15) == 0) e.ssq_out[(int64_t)(n0 >> 7) * e.ssq_ld + m0 + r] = ss;
+    }
+  }
+  return true;
+}
+
 template <typename T, class Sync>
 __device__ void run_epilogue(const EpiParams &e, float *t0, float *t1, int ldt, int m0, int rows,
                              int n0, int tid, int nthreads, int *s_int, Sync sync,
@@ -172,6 +258,7 @@ __device__ void run_epilogue(const EpiParams &e, float *t0, float *t1, int ldt, 
     }
     sync();
   }
+  if (elementwise_vec<T>(e, t0, t1, ldt, m0, rows, n0, tid, nthreads)) return;
   switch (e.op) {
     case EPI_STORE_F32:
     case EPI_RESID:
