@@ -119,6 +119,91 @@ __device__ void head_ops(const EpiParams &e, const float *t0, int ldt, int m0, i
   (void)sync;
 }
 
+// The per-head epilogues for D = 128 with wide accesses: a tile is one head,
+// a half-warp takes a row, lane l owns elements 4l..4l+3 and their rotary
+// partners 64+4l..64+4l+3 (8-byte stores), and the head's RMSNorm reduces
+// over the 16 lanes.  Same arithmetic as head_epilogue.
+template <typename T>
+__device__ void head_ops_d128(const EpiParams &e, const float *t0, int ldt, int m0, int rows,
+                              int n0, int lane, int warp, int nwarps, const int *s_pos,
+                              const int *s_slot) {
+  if (n0 >= e.N) return;
+  const int kvd = e.n_kv_heads * 128;
+  const bool qkv = e.op == EPI_QKV;
+  const int hg = n0 >> 7;
+  int kind, head;
+  if (qkv) {
+    kind = hg < e.n_heads ? 0 : (hg < e.n_heads + e.n_kv_heads ? 1 : 2);
+    head = kind == 0 ? hg : (kind == 1 ? hg - e.n_heads : hg - e.n_heads - e.n_kv_heads);
+  } else {
+    kind = hg < e.n_kv_heads ? 1 : 2;
+    head = kind == 1 ? hg : hg - e.n_kv_heads;
+  }
+  const bool nr = kind != 2;
+  const int hl = lane & 15, hw = lane >> 4;
+  float glo[4] = {1.f, 1.f, 1.f, 1.f}, ghi[4] = {1.f, 1.f, 1.f, 1.f};
+  if (nr) {
+    const T *gain = (const T *)(kind == 0 ? e.q_gain : e.k_gain);
+    const uint2 a = *reinterpret_cast<const uint2 *>(gain + 4 * hl);
+    const uint2 b = *reinterpret_cast<const uint2 *>(gain + 64 + 4 * hl);
+    const T *pa = reinterpret_cast<const T *>(&a), *pb = reinterpret_cast<const T *>(&b);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      glo[k] = to_f32(pa[k]);
+      ghi[k] = to_f32(pb[k]);
+    }
+  }
+  // whole warps iterate together (the norm shuffles over 16 lanes)
+  for (int rb = 2 * warp; rb < rows; rb += 2 * nwarps) {
+    const int r = rb + hw;
+    const bool act = r < rows;
+    float lo[4] = {0.f, 0.f, 0.f, 0.f}, hi[4] = {0.f, 0.f, 0.f, 0.f};
+    if (act) {
+      const float4 a = *reinterpret_cast<const float4 *>(t0 + r * ldt + 4 * hl);
+      const float4 b = *reinterpret_cast<const float4 *>(t0 + r * ldt + 64 + 4 * hl);
+      lo[0] = a.x; lo[1] = a.y; lo[2] = a.z; lo[3] = a.w;
+      hi[0] = b.x; hi[1] = b.y; hi[2] = b.z; hi[3] = b.w;
+    }
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) ss += lo[k] * lo[k] + hi[k] * hi[k];
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    if (!act) continue;
+    const int m = m0 + r;
+    T *dst;
+    if (qkv) {
+      dst = kind == 0 ? (T *)e.q_out + (int64_t)m * e.n_heads * 128 + head * 128
+                      : (T *)(kind == 1 ? e.k_out : e.v_out) + (int64_t)m * kvd + head * 128;
+    } else {
+      const int slot = s_slot[r];
+      if (slot < 0) continue;
+      dst = (T *)(kind == 1 ? e.k_cache : e.v_cache) + (int64_t)slot * kvd + head * 128;
+    }
+    if (nr) {
+      const float rstd = rsqrtf(ss / 128.f + e.eps);
+      const float4 *rope = reinterpret_cast<const float4 *>(e.rope + (int64_t)s_pos[r] * 64 + 4 * hl);
+      const float4 c01 = rope[0], c23 = rope[1];   // (cos, sin) of elements 4l .. 4l+3
+      const float cs_c[4] = {c01.x, c01.z, c23.x, c23.z}, cs_s[4] = {c01.y, c01.w, c23.y, c23.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float a = lo[k] * rstd * glo[k], b = hi[k] * rstd * ghi[k];
+        lo[k] = a * cs_c[k] - b * cs_s[k];
+        hi[k] = b * cs_c[k] + a * cs_s[k];
+      }
+    }
+    uint2 plo, phi;
+    T *ql = reinterpret_cast<T *>(&plo), *qh = reinterpret_cast<T *>(&phi);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      ql[k] = from_f32<T>(lo[k]);
+      qh[k] = from_f32<T>(hi[k]);
+    }
+    *reinterpret_cast<uint2 *>(dst + 4 * hl) = plo;
+    *reinterpret_cast<uint2 *>(dst + 64 + 4 * hl) = phi;
+  }
+}
+
 // t0: fp32 tile [rows][ldt] (features n0 .. n0+127); t1: the "up" tile of a
 // SwiGLU pair.  All `nthreads` threads of the caller take part (a multiple of
 // 128); the caller synchronises before (tile complete) and after (tile reuse).
@@ -363,7 +448,11 @@ __device__ void run_epilogue(const EpiParams &e, float *t0, float *t1, int ldt, 
         s_slot[r] = e.op == EPI_KV_CACHE ? e.row_slot[m0 + r] : 0;
       }
       sync();
-      if (e.head_dim == 128)
+      const bool wide = sizeof(T) == 2 && (ldt & 3) == 0 && (nthreads & 31) == 0 &&
+                        ((uintptr_t)e.q_gain & 7) == 0 && ((uintptr_t)e.k_gain & 7) == 0;
+      if (e.head_dim == 128 && wide)
+        head_ops_d128<T>(e, t0, ldt, m0, rows, n0, lane, warp, nwarps, s_pos, s_slot);
+      else if (e.head_dim == 128)
         head_ops<T, 2>(e, t0, ldt, m0, rows, n0, lane, warp, nwarps, s_pos, s_slot, sync);
       else
         head_ops<T, 1>(e, t0, ldt, m0, rows, n0, lane, warp, nwarps, s_pos, s_slot, sync);
