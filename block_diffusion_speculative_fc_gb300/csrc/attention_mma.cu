@@ -288,14 +288,42 @@ __device__ __forceinline__ bool attend(const Params &p, uint8_t *smem, uint64_t 
     const bool whole = __all_sync(0xffffffffu, !blk && pos0 + KT <= kv && pos0 >= lo0 &&
                                                    pos0 >= lo1 && r1 < R);
     if (whole) {
+      // every score finite: the scale folds into the exponent (one FMA), and
+      // the accumulators are rescaled only when a row maximum of the warp moved
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) {
-        s[nt][0] *= p.scale_log2;
-        s[nt][1] *= p.scale_log2;
-        s[nt][2] *= p.scale_log2;
-        s[nt][3] *= p.scale_log2;
         mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
         mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
+      }
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+      const float mn0 = fmaxf(m0, mx0 * p.scale_log2), mn1 = fmaxf(m1, mx1 * p.scale_log2);
+      const bool moved = __any_sync(0xffffffffu, mn0 != m0 || mn1 != m1);
+      const float a0 = exp2f(m0 - mn0), a1 = exp2f(m1 - mn1);   // m = -inf at first: a = 0
+      m0 = mn0;
+      m1 = mn1;
+      float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+        s[nt][0] = exp2f(fmaf(s[nt][0], p.scale_log2, -mn0));
+        s[nt][1] = exp2f(fmaf(s[nt][1], p.scale_log2, -mn0));
+        s[nt][2] = exp2f(fmaf(s[nt][2], p.scale_log2, -mn1));
+        s[nt][3] = exp2f(fmaf(s[nt][3], p.scale_log2, -mn1));
+        ps0 += s[nt][0] + s[nt][1];
+        ps1 += s[nt][2] + s[nt][3];
+      }
+      l0 = l0 * a0 + ps0;
+      l1 = l1 * a1 + ps1;
+      if (moved) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          o[i][0] *= a0;
+          o[i][1] *= a0;
+          o[i][2] *= a1;
+          o[i][3] *= a1;
+        }
       }
     } else {
 #pragma unroll
@@ -317,34 +345,34 @@ __device__ __forceinline__ bool attend(const Params &p, uint8_t *smem, uint64_t 
           if (row1) mx1 = fmaxf(mx1, v); else mx0 = fmaxf(mx0, v);
         }
       }
-    }
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    const float a0 = mn0 == -INFINITY ? 1.f : exp2f(m0 - mn0);
-    const float a1 = mn1 == -INFINITY ? 1.f : exp2f(m1 - mn1);
-    m0 = mn0;
-    m1 = mn1;
-    float ps0 = 0.f, ps1 = 0.f;
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      const float a0 = mn0 == -INFINITY ? 1.f : exp2f(m0 - mn0);
+      const float a1 = mn1 == -INFINITY ? 1.f : exp2f(m1 - mn1);
+      m0 = mn0;
+      m1 = mn1;
+      float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      s[nt][0] = s[nt][0] == -INFINITY ? 0.f : exp2f(s[nt][0] - mn0);
-      s[nt][1] = s[nt][1] == -INFINITY ? 0.f : exp2f(s[nt][1] - mn0);
-      s[nt][2] = s[nt][2] == -INFINITY ? 0.f : exp2f(s[nt][2] - mn1);
-      s[nt][3] = s[nt][3] == -INFINITY ? 0.f : exp2f(s[nt][3] - mn1);
-      ps0 += s[nt][0] + s[nt][1];
-      ps1 += s[nt][2] + s[nt][3];
-    }
-    l0 = l0 * a0 + ps0;
-    l1 = l1 * a1 + ps1;
+      for (int nt = 0; nt < 8; ++nt) {
+        s[nt][0] = s[nt][0] == -INFINITY ? 0.f : exp2f(s[nt][0] - mn0);
+        s[nt][1] = s[nt][1] == -INFINITY ? 0.f : exp2f(s[nt][1] - mn0);
+        s[nt][2] = s[nt][2] == -INFINITY ? 0.f : exp2f(s[nt][2] - mn1);
+        s[nt][3] = s[nt][3] == -INFINITY ? 0.f : exp2f(s[nt][3] - mn1);
+        ps0 += s[nt][0] + s[nt][1];
+        ps1 += s[nt][2] + s[nt][3];
+      }
+      l0 = l0 * a0 + ps0;
+      l1 = l1 * a1 + ps1;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      o[i][0] *= a0;
-      o[i][1] *= a0;
-      o[i][2] *= a1;
-      o[i][3] *= a1;
+      for (int i = 0; i < 16; ++i) {
+        o[i][0] *= a0;
+        o[i][1] *= a0;
+        o[i][2] *= a1;
+        o[i][3] *= a1;
+      }
     }
     // ---- O += P V (P from the S accumulators, V via transposed ldmatrix)
 #pragma unroll
