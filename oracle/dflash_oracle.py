@@ -248,6 +248,50 @@ def accept_block(draft, posterior):
     return acc, bonus, acc + 1, out
 
 
+# ---------------------------------------------------------------------------
+# Lossless sampled verification ([P1] "Sampling: preserve the proposal
+# distribution the walk actually used"): a proposed token y is accepted with
+# probability min(1, p(y)/q(y)); at the first rejection the correction is drawn
+# from the normalised positive residual [p - q]+; after full acceptance the
+# target supplies a bonus token.  The plain DFlash drafter proposes argmax
+# tokens (same section), so q is a point mass at y: y is accepted iff
+# u < p(y), and [p - q]+ is p with y's entry set to 0 (p(y) - 1 <= 0).
+# Random numbers are inputs: accept_u [S-1] uniform on [0, 1) and exp_noise
+# [V] Exp(1) variates for the one draw the block needs.  A draw from weights
+# w is argmax_v w(v) / e_v (the exponential race: the smallest of independent
+# Exp(rate w_v) times e_v / w_v falls on v with probability w_v / sum w),
+# lowest id on ties.  Decisions are taken in float32 (probabilities, uniforms,
+# quotients), as the kernel takes them.
+# ---------------------------------------------------------------------------
+def exponential_race(weights, exp_noise):
+    w = np.asarray(weights, dtype=np.float32)
+    e = np.asarray(exp_noise, dtype=np.float32)
+    keys = w / e
+    return int(np.argmax(keys))
+
+
+def accept_block_sampled(draft, probs, accept_u, exp_noise):
+    """draft [S] int; probs [S, V] float32 target distribution at block
+    position i (the target's choice for the token after draft[i]); accept_u
+    [S-1]; exp_noise [V].  Returns (accept, bonus, commit, out_tokens) as
+    accept_block does."""
+    draft = np.asarray(draft, dtype=np.int64)
+    probs = np.asarray(probs, dtype=np.float32)
+    u = np.asarray(accept_u, dtype=np.float32)
+    S = draft.shape[0]
+    acc = 0
+    while acc < S - 1 and u[acc] < probs[acc, draft[acc + 1]]:
+        acc += 1
+    w = probs[acc].copy()
+    if acc < S - 1:
+        w[draft[acc + 1]] = 0.0          # [p - q]+ with q the point mass at the rejected token
+    bonus = exponential_race(w, exp_noise)
+    out = np.zeros(S, dtype=np.int64)
+    out[:acc] = draft[1:acc + 1]
+    out[acc] = bonus
+    return acc, bonus, acc + 1, out
+
+
 def commit_output(output_ids, start, draft, acc, bonus):
     """[P3] verify step: output_ids[start:start+acc+1] = block[:acc+1];
     output_ids[start+acc+1] = bonus; the new start (crop index) is start+acc+1."""

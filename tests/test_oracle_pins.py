@@ -450,3 +450,132 @@ def test_pins_catch_planted_mistakes(monkeypatch):
     with pytest.raises(AssertionError):
         test_rms_norm_hand_vector_and_invariants()
     monkeypatch.undo()
+
+
+# ------------------------------------------------ sampled (lossless) verification
+# [P1] "Sampling: preserve the proposal distribution the walk actually used":
+# accept y with probability min(1, p(y)/q(y)); at the first rejection draw from
+# the normalised residual [p - q]+; after full acceptance the target supplies a
+# bonus token.  The plain drafter proposes argmax tokens (q = point mass).
+def _chi2_pvalue(counts, probs):
+    from scipy.stats import chisquare
+    probs = np.asarray(probs, float)
+    keep = probs > 0
+    exp = probs[keep] / probs[keep].sum() * counts.sum()
+    assert counts[~keep].sum() == 0
+    return chisquare(counts[keep], exp).pvalue
+
+
+def test_sampled_reduces_to_greedy_for_a_deterministic_target():
+    """A one-hot target at the posterior tokens turns the sampled rule into the
+    greedy cumprod rule, for every uniform and every noise: the worked
+    examples of the pages carry over."""
+    rng = np.random.default_rng(5)
+    V, S = 11, 6
+    for _ in range(200):
+        draft = rng.integers(0, V, S)
+        post = np.where(rng.random(S) < 0.6, np.r_[draft[1:], 0], rng.integers(0, V, S))
+        probs = np.zeros((S, V), np.float32)
+        probs[np.arange(S), post] = 1.0
+        u = rng.random(S - 1).astype(np.float32)
+        e = rng.exponential(size=V).astype(np.float32)
+        assert O.accept_block_sampled(draft, probs, u, e)[:3] == O.accept_block(draft, post)[:3]
+    gd = _golden("accept_worked_example_p1.json")
+    voc, ex = gd["vocab"], gd["expected"]
+    d = [voc[t] for t in gd["block"]]
+    p = [voc[t] for t in gd["target_choices"]]
+    V = max(voc.values()) + 1
+    probs = np.zeros((len(d), V), np.float32)
+    probs[np.arange(len(d)), p] = 1.0
+    acc, bonus, commit, out = O.accept_block_sampled(d, probs, np.full(len(d) - 1, 0.99, np.float32),
+                                                     np.ones(V, np.float32))
+    assert (acc, bonus, commit) == (ex["accept_len"], voc[ex["bonus"]], ex["commit_len"])
+    assert list(out[:commit]) == [voc[t] for t in ex["out_tokens_valid"]]
+
+
+def test_sampled_zero_probability_rejects_and_is_excluded():
+    rng = np.random.default_rng(6)
+    V = 7
+    probs = np.full((3, V), 1.0 / (V - 1), np.float32)
+    probs[0, 4] = 0.0                       # the first proposed token is impossible
+    for _ in range(300):
+        acc, bonus, _, out = O.accept_block_sampled([1, 4, 2], probs, rng.random(2).astype(np.float32),
+                                                    rng.exponential(size=V).astype(np.float32))
+        assert acc == 0 and bonus != 4 and out[0] == bonus
+
+
+def test_exponential_race_samples_the_weights():
+    rng = np.random.default_rng(7)
+    w = np.array([0.05, 0.0, 0.4, 0.15, 0.3, 0.1], np.float32)
+    n = 30000
+    counts = np.zeros(len(w), np.int64)
+    for _ in range(n):
+        counts[O.exponential_race(w, rng.exponential(size=len(w)).astype(np.float32))] += 1
+    assert _chi2_pvalue(counts, w) > 1e-3
+    # unnormalised weights give the same distribution
+    counts2 = np.zeros(len(w), np.int64)
+    for _ in range(n):
+        counts2[O.exponential_race(7.0 * w, rng.exponential(size=len(w)).astype(np.float32))] += 1
+    assert _chi2_pvalue(counts2, w) > 1e-3
+
+
+@pytest.mark.parametrize("p_y", [0.0, 0.3, 0.9])
+def test_sampled_verification_is_lossless(p_y):
+    """The first emitted token (accepted draft or correction) follows the
+    target distribution p exactly, whatever the drafter proposed."""
+    rng = np.random.default_rng(int(p_y * 100) + 8)
+    V = 5
+    p0 = np.array([0.2, 0.15, 0.0, 0.25, 0.4], np.float64)
+    y = 2
+    p0 = p0 * (1 - p_y) / p0.sum()
+    p0[y] = p_y
+    probs = np.tile(p0.astype(np.float32), (3, 1))
+    n = 30000
+    counts = np.zeros(V, np.int64)
+    for _ in range(n):
+        _, _, _, out = O.accept_block_sampled([0, y, 1], probs, rng.random(2).astype(np.float32),
+                                              rng.exponential(size=V).astype(np.float32))
+        counts[out[0]] += 1
+    assert _chi2_pvalue(counts, probs[0]) > 1e-3
+
+
+def test_sampled_pins_catch_planted_mistakes(monkeypatch):
+    """Plausible mistakes in the sampled rule must trip a pin (CPU only)."""
+    orig = O.accept_block_sampled
+
+    # 1. the rejected token is not removed from the correction distribution
+    def no_residual(draft, probs, u, e):
+        draft = np.asarray(draft); probs = np.asarray(probs, np.float32); u = np.asarray(u, np.float32)
+        acc = 0
+        while acc < len(draft) - 1 and u[acc] < probs[acc, draft[acc + 1]]:
+            acc += 1
+        bonus = O.exponential_race(probs[acc], e)
+        out = np.zeros(len(draft), np.int64); out[:acc] = draft[1:acc + 1]; out[acc] = bonus
+        return acc, bonus, acc + 1, out
+    monkeypatch.setattr(O, "accept_block_sampled", no_residual)
+    with pytest.raises(AssertionError):
+        test_sampled_verification_is_lossless(0.3)
+    monkeypatch.undo()
+    # 2. acceptance with the complementary probability (accept iff u >= p)
+    def flipped(draft, probs, u, e):
+        draft = np.asarray(draft); probs = np.asarray(probs, np.float32); u = np.asarray(u, np.float32)
+        acc = 0
+        while acc < len(draft) - 1 and u[acc] >= probs[acc, draft[acc + 1]]:
+            acc += 1
+        w = probs[acc].copy()
+        if acc < len(draft) - 1:
+            w[draft[acc + 1]] = 0.0
+        bonus = O.exponential_race(w, e)
+        out = np.zeros(len(draft), np.int64); out[:acc] = draft[1:acc + 1]; out[acc] = bonus
+        return acc, bonus, acc + 1, out
+    monkeypatch.setattr(O, "accept_block_sampled", flipped)
+    with pytest.raises(AssertionError):
+        test_sampled_verification_is_lossless(0.9)
+    monkeypatch.undo()
+    # 3. the race taken as argmin instead of argmax of w / e
+    monkeypatch.setattr(O, "exponential_race",
+                        lambda w, e: int(np.argmin(np.where(np.asarray(w) > 0, np.asarray(w, np.float32) /
+                                                            np.asarray(e, np.float32), np.inf))))
+    with pytest.raises(AssertionError):
+        test_exponential_race_samples_the_weights()
+    monkeypatch.undo()
