@@ -10,6 +10,12 @@ Before every cycle kv_len / seq_len are restored to the workload's context
 length, so every timed cycle drafts against exactly that context.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+                  [--verify greedy|sampled]
+
+--verify sampled replaces the greedy acceptance with dflash_accept_commit_sampled
+(lossless rejection sampling): synthetic target rows (softmax of random
+logits, the proposed tokens given the workload's match probability, built
+outside the timed region) and per-step Exp(1) race noise.
 
 Under torchrun (N > 1) each rank runs an independent replica (requests are
 independent; no collective is on the path) and rank 0 prints the line.
@@ -46,6 +52,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="qwen8b-b1")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--verify", default="greedy", choices=["greedy", "sampled"],
+                    help="greedy: dflash_accept_commit; sampled: dflash_accept_commit_sampled "
+                         "(lossless rejection sampling against synthetic target rows)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-cycles", type=int, default=2)
@@ -85,6 +94,8 @@ def algorithmic(cfg, B, ctx_mean, commit_mean):
                                  + B * commit_mean * cfg.n_layers * 2 * kvd),
                            2 * rows * cfg.n_layers * 2 * kvd * H),
         "accept": (4 * (2 * B * S + B * (S + 4)), 0),
+        # target row at the stop position and the race noise, read once each
+        "accept_sampled": (4 * (2 * B * V + 2 * B * S + B * (S + 4)), 0),
     }
     add = lambda *names: tuple(sum(fam[n][i] for n in names) for i in range(2))  # noqa: E731
     fam["gemm_layer_program"] = add("gemm_o", "gemm_gate_up", "gemm_down", "gemm_qkv")
@@ -169,7 +180,7 @@ class ClockSampler:
 
 # ------------------------------------------------------------- our arm
 class Bench:
-    def __init__(self, wl, seed=0):
+    def __init__(self, wl, seed=0, verify="greedy"):
         import torch
         import block_diffusion_speculative_fc_gb300 as pkg
         self.torch, self.pkg = torch, pkg
@@ -223,6 +234,18 @@ class Bench:
             self.p = torch.as_tensor(r, dtype=torch.float32, device="cuda")[:, None]
         else:
             self.p = None
+        self.verify = verify
+        if verify == "sampled":
+            # target rows: softmax of random logits; each cycle the proposed
+            # tokens get the workload's match probability (outside the timed region)
+            V = cfg.vocab
+            logits = torch.randn((B, S, V), generator=g, device="cuda")
+            self.probs_base = torch.softmax(logits, dim=-1).contiguous()
+            del logits
+            self.probs = torch.empty_like(self.probs_base)
+            self.noise = [torch.empty((B, V), device="cuda").exponential_(generator=g) for _ in range(4)]
+            m = self.p if self.p is not None else torch.full((B, 1), 0.84, device="cuda")
+            self.match_val = m.expand(B, S - 1).contiguous().float()
 
     def posterior_randoms(self, n):
         torch, B, S, V = self.torch, self.B, self.S, self.cfg.vocab
@@ -257,10 +280,20 @@ class Bench:
         self.sess.draft(self.kv, anchor, self.draft)
         if ev:
             ev[1].record()
-        post = self.make_post(u, r, k)
+        if self.verify == "sampled":
+            self.probs.copy_(self.probs_base)
+            self.probs[:, :-1].scatter_(2, self.draft[:, 1:].long().unsqueeze(-1),
+                                        self.match_val.unsqueeze(-1))
+        else:
+            post = self.make_post(u, r, k)
         if ev:
             ev[2].record()
-        self.sess.accept(self.B, self.draft, post, self.seq, self.acc, self.com, self.bon, self.tok)
+        if self.verify == "sampled":
+            self.sess.accept_sampled(self.B, self.draft, self.probs, u, self.noise[c % 4], self.seq,
+                                     self.acc, self.com, self.bon, self.tok)
+        else:
+            self.sess.accept(self.B, self.draft, post, self.seq, self.acc, self.com, self.bon,
+                             self.tok)
         self.sess.inject(self.kv, self.pool[c % len(self.pool)], self.row_off, self.com)
         if ev:
             ev[3].record()
@@ -312,6 +345,11 @@ class Bench:
         h2d = feats_h[0].numel() * feats_h[0].element_size() + u_h[0].numel() * 4 + r_h[0].numel() * 4
         if k_h is not None:
             h2d += k_h[0].numel() * k_h.element_size()
+        sampled = self.verify == "sampled"
+        if sampled:   # the race noise of each step comes from the host as well
+            noise_h = [n.cpu().pin_memory() for n in self.noise]
+            noise_d = torch.empty_like(self.noise[0])
+            h2d += noise_h[0].numel() * 4
         d2h = out_h.numel() * 4
         torch.cuda.synchronize()
         t0 = torch.cuda.Event(enable_timing=True)
@@ -327,8 +365,17 @@ class Bench:
             self.seq.copy_(self.base_len)
             anchor = self.anchor if c == 0 else self.bon
             self.sess.draft(self.kv, anchor, self.draft)
-            post = self.make_post(u_d, r_d, k_d)
-            self.sess.accept(B, self.draft, post, self.seq, self.acc, self.com, self.bon, self.tok)
+            if sampled:
+                noise_d.copy_(noise_h[c % len(noise_h)], non_blocking=True)
+                self.probs.copy_(self.probs_base)
+                self.probs[:, :-1].scatter_(2, self.draft[:, 1:].long().unsqueeze(-1),
+                                            self.match_val.unsqueeze(-1))
+                self.sess.accept_sampled(B, self.draft, self.probs, u_d, noise_d, self.seq,
+                                         self.acc, self.com, self.bon, self.tok)
+            else:
+                post = self.make_post(u_d, r_d, k_d)
+                self.sess.accept(B, self.draft, post, self.seq, self.acc, self.com, self.bon,
+                                 self.tok)
             self.sess.inject(self.kv, feat_d, self.row_off, self.com)
             out_d[:, :S].copy_(self.tok)
             out_d[:, S].copy_(self.acc)
@@ -414,7 +461,7 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    bench = Bench(wl)
+    bench = Bench(wl, verify=a.verify)
     cs = ClockSampler(local)
     if dist:
         dist.barrier()
@@ -452,7 +499,7 @@ def main():
                        "layers": bench.cfg.n_layers, "hidden": bench.cfg.hidden,
                        "vocab": bench.cfg.vocab, "parallelism": f"replicas x{world}",
                        "l2": "inputs larger than L2 (weights streamed every step)",
-                       "kv_len_reset_each_cycle": True,
+                       "kv_len_reset_each_cycle": True, "verify": a.verify,
                        "mean_commit_len": mean_commit},
             "clocks": clocks, "e2e": e2e, "gpu_launches": launches,
             "roofline": roof, "cpu_baseline": cpu,

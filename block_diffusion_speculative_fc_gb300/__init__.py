@@ -23,6 +23,7 @@ DERR_BITS = {0x1: "KV_CAPACITY", 0x2: "PAGE_RANGE", 0x4: "TOKEN_RANGE", 0x8: "PO
              0x10: "OUTPUT_ROW", 0x20: "TIMEOUT", 0x40: "ROW_RANGE"}
 EXPORTED = ["dflash_create", "dflash_destroy", "dflash_workspace_size", "dflash_bind_workspace",
             "dflash_inject_context", "dflash_draft_block", "dflash_accept_commit",
+            "dflash_accept_commit_sampled",
             "dflash_get_error", "dflash_status_string", "dflash_last_error",
             "dflash_profile_enable", "dflash_profile_disable", "dflash_profile_collect"]
 
@@ -82,6 +83,9 @@ def load_library(path=LIB_PATH):
                                        c_void_p, c_void_p, c_void_p]
     lib.dflash_accept_commit.argtypes = [c_void_p, c_int32, c_void_p, c_void_p, c_void_p, c_void_p,
                                          c_void_p, c_void_p, c_void_p, c_void_p, c_int32, c_void_p]
+    lib.dflash_accept_commit_sampled.argtypes = [c_void_p, c_int32, c_void_p, c_void_p, c_void_p,
+                                                 c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                                 c_void_p, c_void_p, c_int32, c_void_p]
     lib.dflash_get_error.argtypes = [c_void_p, c_void_p, ctypes.POINTER(ctypes.c_uint32)]
     lib.dflash_profile_enable.argtypes = [c_void_p, c_int32]
     lib.dflash_profile_disable.argtypes = [c_void_p]
@@ -93,7 +97,7 @@ def load_library(path=LIB_PATH):
     lib.dflash_last_error.restype = ctypes.c_char_p
     for name in ["dflash_create", "dflash_workspace_size", "dflash_bind_workspace",
                  "dflash_inject_context", "dflash_draft_block", "dflash_accept_commit",
-                 "dflash_get_error", "dflash_profile_enable", "dflash_profile_disable",
+                 "dflash_accept_commit_sampled", "dflash_get_error", "dflash_profile_enable", "dflash_profile_disable",
                  "dflash_profile_collect"]:
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
@@ -158,6 +162,15 @@ def dflash_accept_commit(h, batch, draft_ids, posterior, seq_len, accept_len, co
     _check(load_library().dflash_accept_commit(h, batch, _p(draft_ids), _p(posterior), _p(seq_len),
                                                _p(accept_len), _p(commit_len), _p(bonus),
                                                _p(out_tokens), _p(output_ids), out_stride, stream))
+
+
+def dflash_accept_commit_sampled(h, batch, draft_ids, probs, accept_u, exp_noise, seq_len,
+                                 accept_len, commit_len, bonus, out_tokens, output_ids, out_stride,
+                                 stream):
+    _check(load_library().dflash_accept_commit_sampled(
+        h, batch, _p(draft_ids), _p(probs), _p(accept_u), _p(exp_noise), _p(seq_len),
+        _p(accept_len), _p(commit_len), _p(bonus), _p(out_tokens), _p(output_ids), out_stride,
+        stream))
 
 
 def dflash_get_error(h, stream):

@@ -15,6 +15,34 @@
 
 namespace dflash {
 
+// Commit of one request by one warp, lane = block position: out_tokens,
+// output_ids, accept/commit/bonus and the crop index (seq_len).  d / d_next:
+// this lane's draft id and the next lane's.
+__device__ __forceinline__ void commit_row(int b, int S, int lane, int acc, int bonus_id, int d,
+                                           int d_next, int *seq_len, int *accept_len,
+                                           int *commit_len, int *bonus, int *out_tokens,
+                                           int *output_ids, int out_stride, unsigned int *err) {
+  const bool live = lane < S;
+  const int start = seq_len[b];
+  const bool write_ids = output_ids != nullptr;
+  if (write_ids && (start < 0 || (int64_t)start + acc + 1 >= out_stride)) {
+    if (lane == 0) raise_error(err, DFLASH_DERR_OUTPUT_ROW);
+    return;
+  }
+  if (live) out_tokens[(int64_t)b * S + lane] = lane < acc ? d_next : (lane == acc ? bonus_id : 0);
+  if (write_ids) {
+    int *row = output_ids + (int64_t)b * out_stride + start;
+    if (lane <= acc) row[lane] = d;
+    if (lane == acc) row[acc + 1] = bonus_id;
+  }
+  if (lane == 0) {
+    accept_len[b] = acc;
+    commit_len[b] = acc + 1;
+    bonus[b] = bonus_id;
+    seq_len[b] = start + acc + 1;
+  }
+}
+
 __global__ void __launch_bounds__(128) accept_kernel(
     int B, int S, int vocab, const int *__restrict__ draft, const int *__restrict__ post,
     int *seq_len, int *accept_len, int *commit_len, int *bonus, int *out_tokens,
@@ -36,24 +64,8 @@ __global__ void __launch_bounds__(128) accept_kernel(
     if (lane == 0) raise_error(err, DFLASH_DERR_TOKEN_RANGE);
     return;
   }
-  const int start = seq_len[b];
-  const bool write_ids = output_ids != nullptr;
-  if (write_ids && (start < 0 || (int64_t)start + acc + 1 >= out_stride)) {
-    if (lane == 0) raise_error(err, DFLASH_DERR_OUTPUT_ROW);
-    return;
-  }
-  if (live) out_tokens[(int64_t)b * S + lane] = lane < acc ? d_next : (lane == acc ? bonus_id : 0);
-  if (write_ids) {
-    int *row = output_ids + (int64_t)b * out_stride + start;
-    if (lane <= acc) row[lane] = d;
-    if (lane == acc) row[acc + 1] = bonus_id;
-  }
-  if (lane == 0) {
-    accept_len[b] = acc;
-    commit_len[b] = acc + 1;
-    bonus[b] = bonus_id;
-    seq_len[b] = start + acc + 1;
-  }
+  commit_row(b, S, lane, acc, bonus_id, d, d_next, seq_len, accept_len, commit_len, bonus,
+             out_tokens, output_ids, out_stride, err);
 }
 
 cudaError_t launch_accept(int B, int S, int vocab, const int *draft, const int *post, int *seq_len,
@@ -63,6 +75,137 @@ cudaError_t launch_accept(int B, int S, int vocab, const int *draft, const int *
   const int warps = 4;
   return launch_pdl(accept_kernel, dim3((B + warps - 1) / warps), dim3(warps * 32), 0, s, B, S,
                     vocab, draft, post, seq_len, accept_len, commit_len, bonus, out_tokens,
+                    output_ids, out_stride, err);
+}
+
+// ---------------------------------------------------------------------------
+// Lossless sampled verification with the greedy drafter ("Inside SGLang",
+// "Sampling: preserve the proposal distribution the walk actually used"):
+// draft[i+1] is accepted with probability min(1, p(y)/q(y)) = p(y), as q is
+// the point mass of an argmax drafter, i.e. iff u[i] < p_i(y); at the first
+// rejection the correction comes from the residual [p - q]+ = p with y's
+// entry zeroed; after full acceptance the bonus comes from the target row of
+// the last position.  The draw is an exponential race, argmax_v w(v) / e_v
+// with e_v ~ Exp(1) given by the caller (lowest id on ties).
+// ---------------------------------------------------------------------------
+// Stop position of request b (accepted count) and the excluded id (-1 for
+// none); false if the stop position's proposed id lies outside the
+// vocabulary.  One warp, lane i decides block position i: every load is in
+// flight at once and a ballot finds the first rejection (S <= 32).
+__device__ __forceinline__ bool sampled_stop(int b, int S, int vocab, const int *draft,
+                                             const float *probs, const float *u, int lane,
+                                             int &acc, int &excl) {
+  const bool live = lane < S - 1;
+  const int y = live ? draft[(int64_t)b * S + lane + 1] : 0;
+  const bool bad = live && (y < 0 || y >= vocab);
+  const float py = (live && !bad) ? probs[((int64_t)b * S + lane) * vocab + y] : 0.f;
+  const float uu = live ? u[(int64_t)b * (S - 1) + lane] : 1.f;
+  const unsigned int taken = __ballot_sync(0xffffffffu, live && !bad && uu < py);
+  acc = __ffs(~taken) - 1;   // first position not accepted, <= S-1
+  const int ystop = __shfl_sync(0xffffffffu, y, acc);
+  const bool bad_stop = __shfl_sync(0xffffffffu, bad ? 1 : 0, acc) != 0;
+  excl = acc < S - 1 ? ystop : -1;
+  return !(acc < S - 1 && bad_stop);
+}
+
+// grid (blocks per request, B): each CTA races a slice of the vocabulary of
+// request b's stop row and folds its winner into keys[b]; the last CTA of the
+// request (ticket) commits it and clears keys[b] and the ticket.
+__global__ void __launch_bounds__(256) sampled_race_kernel(
+    int S, int vocab, const int *__restrict__ draft, const float *__restrict__ probs,
+    const float *__restrict__ u, const float *__restrict__ noise, unsigned long long *keys,
+    int *tickets, int *seq_len, int *accept_len, int *commit_len, int *bonus, int *out_tokens,
+    int *output_ids, int out_stride, unsigned int *err) {
+  pdl_wait();
+  __shared__ int s_acc, s_excl, s_ok, s_last;
+  __shared__ unsigned long long s_best[8];
+  const int b = blockIdx.y;
+  if (threadIdx.x < 32) {
+    int acc, excl;
+    const bool ok = sampled_stop(b, S, vocab, draft, probs, u, threadIdx.x, acc, excl);
+    if (threadIdx.x == 0) {
+      s_ok = ok;
+      s_acc = acc;
+      s_excl = excl;
+    }
+  }
+  __syncthreads();
+  const float *row = probs + ((int64_t)b * S + s_acc) * vocab;
+  const float *e = noise + (int64_t)b * vocab;
+  unsigned long long best = 0ull;
+  const int excl = s_excl;
+  const int stride = gridDim.x * blockDim.x;
+  if ((vocab & 3) == 0 && ((uintptr_t)row & 15) == 0 && ((uintptr_t)e & 15) == 0) {
+    // four entries per load (16-byte loads of the row and the noise)
+#pragma unroll 2
+    for (int v = 4 * (blockIdx.x * blockDim.x + threadIdx.x); v < vocab; v += 4 * stride) {
+      const float4 w4 = *reinterpret_cast<const float4 *>(row + v);
+      const float4 e4 = *reinterpret_cast<const float4 *>(e + v);
+      const float w[4] = {w4.x, w4.y, w4.z, w4.w}, en[4] = {e4.x, e4.y, e4.z, e4.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const unsigned long long k = argmax_key((v + j == excl ? 0.f : w[j]) / en[j], v + j);
+        best = k > best ? k : best;
+      }
+    }
+  } else {
+    for (int v = blockIdx.x * blockDim.x + threadIdx.x; v < vocab; v += stride) {
+      const float w = v == excl ? 0.f : row[v];
+      const unsigned long long k = argmax_key(w / e[v], v);
+      best = k > best ? k : best;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
+    best = other > best ? other : best;
+  }
+  if ((threadIdx.x & 31) == 0) s_best[threadIdx.x >> 5] = best;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int i = 1; i < (int)(blockDim.x >> 5); ++i) best = s_best[i] > best ? s_best[i] : best;
+    if (s_ok && best) atomicMax(keys + b, best);
+    // the last CTA of the request commits it
+    __threadfence();
+    s_last = atomicAdd(tickets + b, 1) == (int)gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!s_last || threadIdx.x >= 32) return;
+  __threadfence();
+  const int lane = threadIdx.x;
+  const bool live = lane < S;
+  const int d = live ? draft[(int64_t)b * S + lane] : -1;
+  const int d_next = __shfl_down_sync(0xffffffffu, d, 1);
+  const int acc = s_acc;
+  const unsigned long long k = __ldcg(keys + b);
+  const bool bad = !s_ok || k == 0ull || __any_sync(0xffffffffu, lane <= acc && (d < 0 || d >= vocab));
+  if (lane == 0) {
+    keys[b] = 0ull;     // ready for the next call
+    tickets[b] = 0;
+  }
+  if (bad) {
+    if (lane == 0) raise_error(err, DFLASH_DERR_TOKEN_RANGE);
+    return;
+  }
+  commit_row(b, S, lane, acc, argmax_key_index(k), d, d_next, seq_len, accept_len, commit_len,
+             bonus, out_tokens, output_ids, out_stride, err);
+}
+
+cudaError_t launch_accept_sampled(int B, int S, int vocab, const int *draft, const float *probs,
+                                  const float *u, const float *noise, unsigned long long *keys,
+                                  int *tickets, int *seq_len, int *accept_len, int *commit_len,
+                                  int *bonus, int *out_tokens, int *output_ids, int out_stride,
+                                  unsigned int *err, cudaStream_t s, int sms) {
+  if (B <= 0) return cudaSuccess;
+  if (S > 32) return cudaErrorInvalidValue;
+  // about two waves of 256-thread CTAs over all requests' rows, each thread
+  // taking at least four entries per pass
+  int per = (2 * sms * 4 + B - 1) / B;
+  per = per < 1 ? 1 : per;
+  const int need = (vocab + 1023) / 1024;
+  per = per > need ? need : per;
+  return launch_pdl(sampled_race_kernel, dim3(per, B), dim3(256), 0, s, S, vocab, draft, probs, u,
+                    noise, keys, tickets, seq_len, accept_len, commit_len, bonus, out_tokens,
                     output_ids, out_stride, err);
 }
 

@@ -24,6 +24,7 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct Layout {
   size_t err, rope, x, h, xg, ssq, qb, kb, vb, attn, act, row_pos, keys, yg, ssq_y, slot, rpos;
+  size_t skeys, stickets;   // race keys / tickets of sampled verification, zero between calls
   size_t tc_partials, tc_counters, tc_grid_bar;
   int tc_max_tiles;
   size_t att_item_start, att_pps, att_part_o, att_part_ml, att_tickets;
@@ -86,6 +87,8 @@ Layout plan(const dflash_config &c, size_t es) {
   L.ssq_y = take(4 * (H / 128) * R);
   L.slot = take(4 * R);
   L.rpos = take(4 * R);
+  L.skeys = take(8 * (size_t)c.max_batch);
+  L.stickets = take(4 * (size_t)c.max_batch);
   if (es == 2) {
     // tensor-core GEMM scratch: stream-K partial tiles and per-tile tickets
     const int Mb = (int)M, Mr = c.max_rows;
@@ -401,6 +404,11 @@ int dflash_bind_workspace(dflash_handle *h, void *dev_ptr, size_t bytes, dflash_
       (st = check_cuda(cudaMemsetAsync(h->ws + h->L.att_tickets, 0, 4 * (size_t)h->L.att_bg, s),
                        "clear attention tickets")))
     return st;
+  if ((st = check_cuda(cudaMemsetAsync(h->ws + h->L.skeys, 0, 8 * (size_t)h->cfg.max_batch, s),
+                       "clear sampled-verification keys")) ||
+      (st = check_cuda(cudaMemsetAsync(h->ws + h->L.stickets, 0, 4 * (size_t)h->cfg.max_batch, s),
+                       "clear sampled-verification tickets")))
+    return st;
   st = check_cuda(launch_rope_table(at<float2>(h, h->L.rope), h->cfg.max_position, h->cfg.head_dim,
                                     h->cfg.rope_theta, s), "rope table");
   if (st) return st;
@@ -699,6 +707,33 @@ int dflash_draft_block(dflash_handle *h, const dflash_kv *kv, int32_t batch, con
   if (fused) return DFLASH_OK;   // the ids came with the last launch
   return timed(h, "argmax_finalize", s,
                [&] { return launch_argmax_finalize(keys, anchor, batch, S, draft_ids, s); });
+}
+
+int dflash_accept_commit_sampled(dflash_handle *h, int32_t batch, const int32_t *draft_ids,
+                                 const float *probs, const float *accept_u, const float *exp_noise,
+                                 int32_t *seq_len, int32_t *accept_len, int32_t *commit_len,
+                                 int32_t *bonus, int32_t *out_tokens, int32_t *output_ids,
+                                 int32_t out_stride, dflash_stream_t stream) {
+  if (!h) return fail(DFLASH_EINVAL, "handle is NULL");
+  if (!h->ws) return fail(DFLASH_ESTATE, "no workspace bound");
+  if (batch < 0) return fail(DFLASH_EINVAL, "negative batch");
+  if (batch > h->cfg.max_batch) return fail(DFLASH_ECAPACITY, "batch > max_batch");
+  if (batch == 0) return DFLASH_OK;
+  if (!draft_ids || !probs || !accept_u || !exp_noise || !seq_len || !accept_len || !commit_len ||
+      !bonus || !out_tokens)
+    return fail(DFLASH_EINVAL, "a required pointer is NULL");
+  if (output_ids && out_stride <= 0) return fail(DFLASH_EINVAL, "out_stride must be positive");
+  cudaStream_t s = (cudaStream_t)stream;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return timed(h, "accept_sampled", s, [&] {
+    return launch_accept_sampled(batch, h->cfg.block_size, h->cfg.vocab, draft_ids, probs, accept_u,
+                                 exp_noise, at<unsigned long long>(h, h->L.skeys),
+                                 at<int>(h, h->L.stickets), seq_len,
+                                 accept_len, commit_len, bonus, out_tokens, output_ids, out_stride,
+                                 at<unsigned int>(h, h->L.err), s, sms > 0 ? sms : 1);
+  });
 }
 
 int dflash_test_set_fusion(dflash_handle *h, int32_t on) {

@@ -193,6 +193,14 @@ cudaError_t launch_accept(int B, int S, int vocab, const int *draft, const int *
                           int *out_tokens, int *output_ids, int out_stride, unsigned int *err,
                           cudaStream_t s);
 
+// Lossless sampled verification (accept.cu); keys, tickets: [B] zeroed
+// scratch that the launch leaves zeroed; sms: SM count (grid sizing).
+cudaError_t launch_accept_sampled(int B, int S, int vocab, const int *draft, const float *probs,
+                                  const float *u, const float *noise, unsigned long long *keys,
+                                  int *tickets, int *seq_len, int *accept_len, int *commit_len,
+                                  int *bonus, int *out_tokens, int *output_ids, int out_stride,
+                                  unsigned int *err, cudaStream_t s, int sms);
+
 // Host-side helpers implemented next to the handle (dflash_api.cu).
 int handle_lm_head(const dflash_handle *h, const void **lm_head, int *hidden, int *vocab,
                    int *dtype);

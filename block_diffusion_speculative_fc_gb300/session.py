@@ -11,7 +11,8 @@ import torch
 
 from . import (DFLASH_BF16, DFLASH_F32, DflashConfig, DflashKV, DflashWeights, _ptr_array,
                dflash_accept_commit, dflash_bind_workspace, dflash_create, dflash_destroy,
-               dflash_draft_block, dflash_get_error, dflash_inject_context, dflash_workspace_size,
+               dflash_accept_commit_sampled, dflash_draft_block, dflash_get_error,
+               dflash_inject_context, dflash_workspace_size,
                _check, load_library)
 
 
@@ -113,6 +114,15 @@ class DraftSession:
         stride = output_ids.shape[1] if output_ids is not None else 0
         dflash_accept_commit(self.h, batch, draft_ids, posterior, seq_len, accept_len, commit_len,
                              bonus, out_tokens, output_ids, stride, _stream())
+
+    def accept_sampled(self, batch, draft_ids, probs, accept_u, exp_noise, seq_len, accept_len,
+                       commit_len, bonus, out_tokens, output_ids=None):
+        """Lossless sampled verification (include/dflash.h); probs [B, S, V],
+        accept_u [B, S-1], exp_noise [B, V] float32 device tensors."""
+        stride = output_ids.shape[1] if output_ids is not None else 0
+        dflash_accept_commit_sampled(self.h, batch, draft_ids, probs, accept_u, exp_noise, seq_len,
+                                     accept_len, commit_len, bonus, out_tokens, output_ids, stride,
+                                     _stream())
 
     def set_fusion(self, on):
         """Dependent GEMMs as one fused launch (True) or one launch each (False)."""

@@ -240,6 +240,34 @@ int dflash_accept_commit(dflash_handle *h, int32_t batch, const int32_t *draft_i
                          int32_t *commit_len, int32_t *bonus, int32_t *out_tokens,
                          int32_t *output_ids, int32_t out_stride, dflash_stream_t stream);
 
+/*
+ * Step 3, sampled variant: lossless rejection-sampling verification with the
+ * argmax drafter ("Inside SGLang", "Sampling: preserve the proposal
+ * distribution the walk actually used": a proposed token y is accepted with
+ * probability min(1, p(y)/q(y)); at the first rejection the correction is
+ * drawn from the normalised residual [p - q]+; after full acceptance the
+ * target supplies a bonus token.  The plain drafter proposes argmax tokens,
+ * so q is the point mass at y.)  Random numbers are inputs:
+ *   probs      device float32 [batch, S, vocab]: the target's distribution at
+ *              block position i (over the token after draft[b][i])
+ *   accept_u   device float32 [batch, S-1], uniform on [0, 1):
+ *              draft[b][i+1] is accepted iff accept_u[b][i] < probs[b][i][draft[b][i+1]]
+ *   exp_noise  device float32 [batch, vocab], Exp(1) variates (> 0): the bonus
+ *              (correction or full-acceptance bonus) is the argmax over v of
+ *              w(v) / exp_noise[b][v], w the target row at the stop position
+ *              with the rejected token's entry set to 0, lowest id on ties
+ *              (the "exponential race", an exact draw from w / sum(w))
+ * Decisions are taken in float32 (IEEE division and comparison).  All other
+ * arguments and outputs as in dflash_accept_commit; a proposed id outside
+ * [0, vocab) sets DFLASH_DERR_TOKEN_RANGE and that request is not committed.
+ * Caller owns every buffer; the call allocates nothing.
+ */
+int dflash_accept_commit_sampled(dflash_handle *h, int32_t batch, const int32_t *draft_ids,
+                                 const float *probs, const float *accept_u, const float *exp_noise,
+                                 int32_t *seq_len, int32_t *accept_len, int32_t *commit_len,
+                                 int32_t *bonus, int32_t *out_tokens, int32_t *output_ids,
+                                 int32_t out_stride, dflash_stream_t stream);
+
 /* Synchronise `stream`, read the sticky device error word into *word (may be
  * NULL) and clear it.  Returns DFLASH_OK if it was zero, DFLASH_EDEVICE if
  * not. */
