@@ -294,7 +294,7 @@ struct Cfg {
   // stream-K merge area: shares of a (row chunk, half) of a split tile, one
   // bulk copy each
   static constexpr int CHUNK_BYTES = CH * 128 * 4;
-  static constexpr int MERGE_BYTES = BN >= 256 ? 16 * 1024 : 48 * 1024;
+  static constexpr int MERGE_BYTES = BN >= 128 ? 16 * 1024 : 48 * 1024;   // deeper ring at large tiles
   static constexpr int MERGE_SLOTS = MERGE_BYTES / CHUNK_BYTES;
   static constexpr int BAR_BYTES = 2048;   // mbarriers, TMEM slot, epilogue scratch, row scales
   static constexpr int BUDGET = 225 * 1024;
