@@ -447,6 +447,22 @@ def dominant_roofline(bench, prof, mean_commit, wl_name):
     return out
 
 
+def job_rate(ms, units, dist=None, device="cpu"):
+    """Whole-job rate of independent replicas: the units every rank processed,
+    summed, over the slowest rank's time (the job ends when its last replica
+    does).  Returns (units per second, max ms, total units); every rank gets
+    the same answer."""
+    if dist is None:
+        return units / (ms / 1e3), ms, units
+    import torch
+    t_max = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    t_sum = torch.tensor([float(units)], dtype=torch.float64, device=device)
+    dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
+    dist.all_reduce(t_sum, op=dist.ReduceOp.SUM)
+    ms_max, total = float(t_max.item()), float(t_sum.item())
+    return total / (ms_max / 1e3), ms_max, total
+
+
 def main():
     a = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -469,19 +485,13 @@ def main():
     cs.start()
     total_ms, ms, prof, mean_commit = bench.run(a.warmup, a.steps, min(a.steps, 50))
     clocks = cs.stop()
-    t = torch.tensor([total_ms], device="cuda")
-    if dist:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms = float(t.item())
-    tokens = world * a.steps * bench.B * (bench.S - 1)
-    value = tokens / (total_ms / 1e3)
+    tokens_here = a.steps * bench.B * (bench.S - 1)
+    value, total_ms, _ = job_rate(total_ms, tokens_here, dist, "cuda")
     e2e = None
     if not a.no_e2e:
         e_ms, h2d, d2h = bench.run_e2e(a.steps)
-        te = torch.tensor([e_ms], device="cuda")
-        if dist:
-            dist.all_reduce(te, op=dist.ReduceOp.MAX)
-        e2e = {"value": tokens / (float(te.item()) / 1e3), "unit": UNIT,
+        e_value, _, _ = job_rate(e_ms, tokens_here, dist, "cuda")
+        e2e = {"value": e_value, "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
     roof = dominant_roofline(bench, prof, mean_commit, a.workload)
     cpu = None
