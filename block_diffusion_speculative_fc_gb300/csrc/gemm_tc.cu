@@ -290,44 +290,48 @@ struct Cfg {
   static constexpr int A_BYTES = BN * BK * 2;
   static constexpr int SLOT_BYTES = W_BYTES + A_BYTES;
   static constexpr int CH = BN < 32 ? BN : 32;            // epilogue token chunk
-  static constexpr int STAGING_BYTES = P * CH * 128 * 4;
   // stream-K merge area: shares of a (row chunk, half) of a split tile, one
-  // bulk copy each
+  // bulk copy each.  The epilogue's fp32 staging tiles (one chunk per half)
+  // live in it too: the last slot holds the gate half of a paired tile while
+  // the up half's shares come into the slots before it, the first slot the up
+  // half (written once its merge is done); a tile's staging is consumed before
+  // the next merge starts.
   static constexpr int CHUNK_BYTES = CH * 128 * 4;
-  static constexpr int MERGE_BYTES = BN >= 128 ? 16 * 1024 : 48 * 1024;   // deeper ring at large tiles
+  static constexpr int MERGE_MIN = BN >= 128 ? 16 * 1024 : 48 * 1024;   // deeper ring at large tiles
+  static constexpr int MERGE_BYTES = MERGE_MIN > P * CHUNK_BYTES ? MERGE_MIN : P * CHUNK_BYTES;
   static constexpr int MERGE_SLOTS = MERGE_BYTES / CHUNK_BYTES;
   static constexpr int BAR_BYTES = 2048;   // mbarriers, TMEM slot, epilogue scratch, row scales
   static constexpr int BUDGET = 225 * 1024;
   static constexpr int SLOTS_RAW =
-      (BUDGET - 1024 - STAGING_BYTES - MERGE_BYTES - BAR_BYTES) / SLOT_BYTES;
+      (BUDGET - 1024 - MERGE_BYTES - BAR_BYTES) / SLOT_BYTES;
   static constexpr int SLOTS = SLOTS_RAW > 24 ? 24 : SLOTS_RAW;
-  static constexpr int SMEM = 1024 + SLOTS * SLOT_BYTES + STAGING_BYTES + MERGE_BYTES + BAR_BYTES;
+  static constexpr int SMEM = 1024 + SLOTS * SLOT_BYTES + MERGE_BYTES + BAR_BYTES;
   static constexpr int ACC_COLS = P * BN;                 // one accumulator buffer
   static constexpr int TMEM_COLS = 2 * ACC_COLS <= 32 ? 32 : (2 * ACC_COLS <= 64 ? 64 :
                                    (2 * ACC_COLS <= 128 ? 128 : (2 * ACC_COLS <= 256 ? 256 : 512)));
   static_assert(SLOTS >= (PAIRABLE ? 4 : 3), "two k-blocks (paired: two slots each) must fit");
-  static_assert(MERGE_SLOTS >= 1, "merge area");
+  static_assert(MERGE_SLOTS >= P, "merge area: the staging tiles and, paired, one share");
   static_assert(2 * ACC_COLS <= 512, "accumulators exceed TMEM");
   static_assert(2 * SLOTS * 8 + 6 * 8 <= 496, "barrier region");
 };
 
-// Bounded acquire-spin on a grid barrier word; false = gave up.
+// Bounded acquire-spin on a grid barrier word (no sleep between polls: the
+// wait is on the critical path of every phase change; one 4-byte L2 read per
+// poll and CTA); false = gave up after ~2^22 polls (seconds).
 __device__ __forceinline__ bool grid_wait(const unsigned int *bar, unsigned int target) {
-  for (uint32_t i = 0; i < 4 * WAIT_LIMIT; ++i) {
+  for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
     unsigned int v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(bar) : "memory");
     if (v >= target) return true;
-    __nanosleep(100);
   }
   return false;
 }
 // Bounded acquire-spin until a counter reaches `target`; false = gave up.
 __device__ __forceinline__ bool counter_wait(const int *ctr, int target) {
-  for (uint32_t i = 0; i < 4 * WAIT_LIMIT; ++i) {
+  for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
     int v;
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
     if (v >= target) return true;
-    __nanosleep(64);
   }
   return false;
 }
@@ -532,9 +536,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint8_t *slots = smem;
-  float *staging = (float *)(smem + C::SLOTS * C::SLOT_BYTES);
-  float *merge = (float *)(smem + C::SLOTS * C::SLOT_BYTES + C::STAGING_BYTES);
-  uint8_t *barbase = smem + C::SLOTS * C::SLOT_BYTES + C::STAGING_BYTES + C::MERGE_BYTES;
+  float *merge = (float *)(smem + C::SLOTS * C::SLOT_BYTES);
+  uint8_t *barbase = smem + C::SLOTS * C::SLOT_BYTES + C::MERGE_BYTES;
   uint64_t *bars = (uint64_t *)barbase;
   uint64_t *full = bars, *empty = bars + C::SLOTS;
   uint64_t *acc_full = bars + 2 * C::SLOTS, *acc_empty = acc_full + 2;
@@ -648,7 +651,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
     const int tid = ew * 32 + lane;                  // 0..127
     const int quarter = warp & 3;                    // TMEM lane quarter this warp may access
     const int f = quarter * 32 + lane;               // output feature row of this thread
-    float *st0 = staging, *st1 = staging + C::CH * 128;
+    // staging tiles in the merge area: gate (or only) half in its last slot, up half in its first
+    float *st0 = merge + (C::MERGE_SLOTS - 1) * (C::CHUNK_BYTES / 4), *st1 = merge;
     int seg_i = 0;
     uint32_t merge_phase = 0;   // completed phases of merge_bar
     bool alive = true;
@@ -773,10 +777,14 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
                 float acc[32];
                 tmem_ld16(tacc + q * BN + c0, acc);
                 if (C::CH == 32) tmem_ld16(tacc + q * BN + c0 + 16, acc + 16);
-                for (int k0 = 0; k0 < others; k0 += C::MERGE_SLOTS) {
-                  const int kn = min(C::MERGE_SLOTS, others - k0);
+                // the up half's shares keep clear of the gate half's staging tile
+                const int mslots = q ? C::MERGE_SLOTS - 1 : C::MERGE_SLOTS;
+                for (int k0 = 0; k0 < others; k0 += mslots) {
+                  const int kn = min(mslots, others - k0);
                   if (tid == 0) {
                     fence_proxy_async();   // the shares were written by generic stores
+                    // and this area was last written / read by generic accesses
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     mbar_expect_tx(merge_bar, kn * C::CHUNK_BYTES);
                     for (int k = 0; k < kn; ++k) {
                       const int c = c_first + 1 + k0 + k;
