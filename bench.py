@@ -217,11 +217,17 @@ class Bench:
         assert self.sess.error() == 0
         self.base_len = i32(self.T)
         self.anchor = i32(make_anchor(B, cfg, seed))
-        self.seq = i32(self.T)
         self.draft = torch.zeros((B, S), dtype=torch.int32, device="cuda")
-        self.acc = torch.zeros(B, dtype=torch.int32, device="cuda")
-        self.com, self.bon = torch.zeros_like(self.acc), torch.zeros_like(self.acc)
-        self.tok = torch.zeros((B, S), dtype=torch.int32, device="cuda")
+        # a step's results in one contiguous block (committed tokens [B, S], then
+        # accept length, bonus id and sequence length [B] each), so the end-to-end
+        # loop reads them back with a single copy
+        self.results = torch.zeros(B * (S + 3), dtype=torch.int32, device="cuda")
+        self.tok = self.results[:B * S].view(B, S)
+        self.acc = self.results[B * S:B * S + B]
+        self.bon = self.results[B * S + B:B * S + 2 * B]
+        self.seq = self.results[B * S + 2 * B:]
+        self.seq.copy_(i32(self.T))
+        self.com = torch.zeros(B, dtype=torch.int32, device="cuda")
         self.row_off = i32(np.arange(B) * S)
         self.pool = [make_features(cfg, B * S, seed, ("verify", i), device="cuda") for i in range(4)]
         g = torch.Generator(device="cuda")
@@ -331,7 +337,12 @@ class Bench:
 
     def run_e2e(self, steps):
         """Same cycles through the public API with host buffers: verify features
-        and verify randoms copied host->device each step, results device->host."""
+        and verify randoms copied host->device each step, results device->host.
+        The host->device copies of a step run on a second stream while that
+        step's draft block computes (only the acceptance and the injection read
+        them; the main stream waits on their event before the acceptance), and
+        the next step's copies wait for this step's injection to finish reading
+        the buffers.  The results come back with one device->host copy."""
         torch, B, S, cfg = self.torch, self.B, self.S, self.cfg
         u, r, k = self.posterior_randoms(steps)
         u_h, r_h = u.cpu().pin_memory(), r.cpu().pin_memory()
@@ -340,8 +351,7 @@ class Bench:
         feat_d = torch.empty_like(self.pool[0])
         u_d, r_d = torch.empty_like(u[0]), torch.empty_like(r[0])
         k_d = torch.empty_like(k[0]) if k is not None else None
-        out_h = torch.empty((B, S + 3), dtype=torch.int32).pin_memory()
-        out_d = torch.empty((B, S + 3), dtype=torch.int32, device="cuda")
+        out_h = torch.empty(B * (S + 3), dtype=torch.int32).pin_memory()
         h2d = feats_h[0].numel() * feats_h[0].element_size() + u_h[0].numel() * 4 + r_h[0].numel() * 4
         if k_h is not None:
             h2d += k_h[0].numel() * k_h.element_size()
@@ -351,22 +361,32 @@ class Bench:
             noise_d = torch.empty_like(self.noise[0])
             h2d += noise_h[0].numel() * 4
         d2h = out_h.numel() * 4
+        main = torch.cuda.current_stream()
+        side = torch.cuda.Stream()
+        copied = torch.cuda.Event()
+        consumed = torch.cuda.Event()
+        consumed.record(main)
         torch.cuda.synchronize()
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record()
         for c in range(steps):
-            feat_d.copy_(feats_h[c % len(feats_h)], non_blocking=True)
-            u_d.copy_(u_h[c], non_blocking=True)
-            r_d.copy_(r_h[c], non_blocking=True)
-            if k_d is not None:
-                k_d.copy_(k_h[c], non_blocking=True)
+            with torch.cuda.stream(side):
+                side.wait_event(consumed)      # the previous step's injection has read them
+                feat_d.copy_(feats_h[c % len(feats_h)], non_blocking=True)
+                u_d.copy_(u_h[c], non_blocking=True)
+                r_d.copy_(r_h[c], non_blocking=True)
+                if k_d is not None:
+                    k_d.copy_(k_h[c], non_blocking=True)
+                if sampled:
+                    noise_d.copy_(noise_h[c % len(noise_h)], non_blocking=True)
+                copied.record(side)
             self.kv.kv_len.copy_(self.base_len)
             self.seq.copy_(self.base_len)
             anchor = self.anchor if c == 0 else self.bon
             self.sess.draft(self.kv, anchor, self.draft)
+            main.wait_event(copied)
             if sampled:
-                noise_d.copy_(noise_h[c % len(noise_h)], non_blocking=True)
                 self.probs.copy_(self.probs_base)
                 self.probs[:, :-1].scatter_(2, self.draft[:, 1:].long().unsqueeze(-1),
                                             self.match_val.unsqueeze(-1))
@@ -377,11 +397,8 @@ class Bench:
                 self.sess.accept(B, self.draft, post, self.seq, self.acc, self.com, self.bon,
                                  self.tok)
             self.sess.inject(self.kv, feat_d, self.row_off, self.com)
-            out_d[:, :S].copy_(self.tok)
-            out_d[:, S].copy_(self.acc)
-            out_d[:, S + 1].copy_(self.bon)
-            out_d[:, S + 2].copy_(self.seq)
-            out_h.copy_(out_d, non_blocking=True)
+            consumed.record(main)
+            out_h.copy_(self.results, non_blocking=True)
         t1.record()
         torch.cuda.synchronize()
         ms = t0.elapsed_time(t1)
