@@ -30,6 +30,11 @@ Readings taken where the pages are silent (each is also pinned by a test):
 
 Parity status: every function below is pinned by ``tests/test_oracle_pins.py``
 (worked examples printed on the pages, closed forms, invariants, brute force).
+The DFlash 2 selector (compute_candidates, selector_walk,
+draft_block_selector) and the sampled verification with a real proposal
+(accept_block_sampled_q) are pinned by hand-built lattices, reductions to the
+plain drafter and rule, and distribution tests of the walk and of
+losslessness; the pages print no numeric selector example.
 The composition ``draft_forward`` has no printed numeric example on the pages;
 it is pinned through its pinned parts and through an independent loop-level
 restatement in the test suite ("parity unpinned by the pages" for the
@@ -285,6 +290,123 @@ def accept_block_sampled(draft, probs, accept_u, exp_noise):
     w = probs[acc].copy()
     if acc < S - 1:
         w[draft[acc + 1]] = 0.0          # [p - q]+ with q the point mass at the rejected token
+    bonus = exponential_race(w, exp_noise)
+    out = np.zeros(S, dtype=np.int64)
+    out[:acc] = draft[1:acc + 1]
+    out[acc] = bonus
+    return acc, bonus, acc + 1, out
+
+
+# ---------------------------------------------------------------------------
+# DFlash 2 candidate selector ([P1] "DFlash 2: replace selection, retain the
+# serving loop").  After the one backbone pass, every draft position j = 1..S-1
+# keeps the K highest lm_head logits as candidates (compute_candidates: ids
+# and their "unary" logits U).  A transition from predecessor token p to
+# candidate c at position j scores
+#     score_j(p, c) = U_j(c) + < A[p] * (W_h h_j), B[c] >
+# (the successor's unary logit plus a learned low-rank compatibility term;
+# A, B: [V, r] token factors, W_h: [r, H], h_j the final-normed hidden state
+# of position j).  The predecessor of the first prediction is the anchor; of
+# every later one, the candidate the walk chose at the position before.  The
+# walk goes left to right once, choosing greedily (highest score, earliest
+# candidate on ties) or by sampling from softmax(score_j(p, .)) over the K
+# candidates; it does not search for the best full path.  q_rows[j] is that
+# softmax for the predecessor actually chosen: the proposal distribution a
+# lossless sampled verification needs.
+# Readings where the pages are silent: candidates are ordered by logit,
+# highest first, lower id first among equal logits; no temperature (scores
+# are used as they are); h_j is the same final-normed hidden state the lm_head
+# reads; a sampled choice is the exponential race over q_rows[j] with one
+# Exp(1) variate per candidate, as in the verification above.
+# ---------------------------------------------------------------------------
+def compute_candidates(hidden_rows, lm_head, K):
+    """Top-K ids [R, K] (logit order, lower id first on ties) and their logits [R, K]."""
+    logits = _f64(hidden_rows) @ _f64(lm_head).T
+    V = logits.shape[1]
+    if not 1 <= K <= V:
+        raise ValueError("need 1 <= K <= vocab")
+    ids = np.empty((logits.shape[0], K), dtype=np.int64)
+    for r in range(logits.shape[0]):
+        ids[r] = np.argsort(-logits[r], kind="stable")[:K]
+    return ids, np.take_along_axis(logits, ids, axis=1)
+
+
+def selector_scores(unary_row, cand_row, pred, wh_row, A, B):
+    """score(pred, c) for the K candidates c of one position."""
+    return _f64(unary_row) + (_f64(A)[pred] * _f64(wh_row)) @ _f64(B)[np.asarray(cand_row)].T
+
+
+def softmax(x):
+    x = _f64(x)
+    e = np.exp(x - x.max())
+    return e / e.sum()
+
+
+def selector_walk(anchor, cand, unary, wh, A, B, exp_noise=None):
+    """cand, unary [S-1, K]; wh [S-1, r].  Greedy walk when exp_noise is None,
+    else sampled with exp_noise [S-1, K] Exp(1) variates.  Returns the chosen
+    ids [S-1], the chosen candidate slots [S-1] and q_rows [S-1, K] (float64)."""
+    cand = np.asarray(cand, dtype=np.int64)
+    n, K = cand.shape
+    ids = np.empty(n, dtype=np.int64)
+    slots = np.empty(n, dtype=np.int64)
+    q = np.empty((n, K))
+    pred = int(anchor)
+    for j in range(n):
+        sc = selector_scores(unary[j], cand[j], pred, wh[j], A, B)
+        q[j] = softmax(sc)
+        k = int(np.argmax(sc)) if exp_noise is None else exponential_race(q[j], exp_noise[j])
+        slots[j] = k
+        ids[j] = cand[j, k]
+        pred = int(ids[j])
+    return ids, slots, q
+
+
+def draft_block_selector(cfg, W, sel, anchor, ctx_kv_layers, kv_len, K, exp_noise=None):
+    """DFlash 2 draft pass for one request: ids [S] (col 0 = anchor), candidate
+    ids [S-1, K], their logits [S-1, K], q_rows [S-1, K], wh [S-1, r] and the
+    hidden states [S, H].  sel: {"A": [V, r], "B": [V, r], "W_h": [r, H]}."""
+    hid = draft_forward(cfg, W, anchor, ctx_kv_layers, kv_len)
+    cand, unary = compute_candidates(hid[1:], W["lm_head"], K)
+    wh = hid[1:] @ _f64(sel["W_h"]).T
+    ids, _, q = selector_walk(anchor, cand, unary, wh, sel["A"], sel["B"], exp_noise)
+    out = np.empty(cfg.block_size, dtype=np.int64)
+    out[0] = anchor
+    out[1:] = ids
+    return out, cand, unary, q, wh, hid
+
+
+# Sampled verification of a drafter with a real proposal distribution (the
+# selector's q_rows over its K candidates; zero elsewhere).  Proposed token y
+# at position i is accepted iff u_i < p(y) / q(y); at the first rejection the
+# correction is the exponential race over [p - q]+, after full acceptance over
+# the target's last row.  Decisions in float32, as the kernel takes them.
+def accept_block_sampled_q(draft, probs, cand, q_rows, accept_u, exp_noise):
+    """draft [S]; probs [S, V] float32; cand [S-1, K] ids with q_rows [S-1, K]
+    their proposal probabilities; accept_u [S-1]; exp_noise [V]."""
+    draft = np.asarray(draft, dtype=np.int64)
+    probs = np.asarray(probs, dtype=np.float32)
+    cand = np.asarray(cand, dtype=np.int64)
+    q = np.asarray(q_rows, dtype=np.float32)
+    u = np.asarray(accept_u, dtype=np.float32)
+    S = draft.shape[0]
+
+    def q_of(i, y):
+        hit = np.nonzero(cand[i] == y)[0]
+        return q[i, hit[0]] if len(hit) else np.float32(0.0)
+
+    acc = 0
+    while acc < S - 1:
+        y = draft[acc + 1]
+        qy = q_of(acc, y)
+        if not (qy > 0 and u[acc] < np.float32(probs[acc, y] / qy)):
+            break
+        acc += 1
+    w = probs[acc].copy()
+    if acc < S - 1:
+        for k in range(cand.shape[1]):
+            c = cand[acc, k]
+            w[c] = np.maximum(np.float32(w[c] - q[acc, k]), np.float32(0.0))
     bonus = exponential_race(w, exp_noise)
     out = np.zeros(S, dtype=np.int64)
     out[:acc] = draft[1:acc + 1]

@@ -579,3 +579,179 @@ def test_sampled_pins_catch_planted_mistakes(monkeypatch):
     with pytest.raises(AssertionError):
         test_exponential_race_samples_the_weights()
     monkeypatch.undo()
+
+
+# ------------------------------------------------ DFlash 2 candidate selector
+# [P1] "DFlash 2: replace selection, retain the serving loop": per position the
+# K best lm_head logits are candidates; score(p, c; h) = U(c) + <A[p] * W_h h,
+# B[c]>; the predecessor is the anchor, then the candidate chosen before; the
+# walk is greedy or sampled, never a search for the best full path; q_rows is
+# the softmax of the chosen predecessor's row.
+def _lm_rows(logit_rows):
+    """hidden rows = identity, lm_head = the logits transposed: logits come out as given."""
+    L = np.asarray(logit_rows, float)
+    return np.eye(L.shape[0]), L.T.copy()
+
+
+def test_candidates_order_ties_and_k1():
+    h, lm = _lm_rows([[1.0, 3.0, 3.0, 2.0, -1.0], [0.5, 0.5, 0.5, 0.5, 0.5]])
+    ids, u = O.compute_candidates(h, lm, 3)
+    assert ids.tolist() == [[1, 2, 3], [0, 1, 2]]
+    assert u.tolist() == [[3.0, 3.0, 2.0], [0.5, 0.5, 0.5]]
+    rng = np.random.default_rng(20)
+    hid, lmh = rng.normal(size=(6, 8)), rng.normal(size=(40, 8))
+    ids1, _ = O.compute_candidates(hid, lmh, 1)
+    assert ids1[:, 0].tolist() == O.lm_head_argmax(hid, lmh)[0].tolist()
+    idsV, _ = O.compute_candidates(hid, lmh, 40)     # K = V: a permutation of the vocabulary
+    assert all(sorted(r) == list(range(40)) for r in idsV.tolist())
+    with pytest.raises(ValueError):
+        O.compute_candidates(hid, lmh, 41)
+
+
+def _walk_example():
+    """Hand-built lattice, V = 4, r = 1, K = 2 (numbers chosen for the test).
+    position 1: candidates [0, 1], U = [0, 0], wh = 1; anchor 2 with A[2] = 1;
+                B[0] = 1, B[1] = -1: scores [1, -1] -> token 0.
+    position 2: candidates [1, 3], U = [0, 0.5], wh = 2; predecessor 0 with
+                A[0] = -1: scores [2, -1.5] -> token 1.
+    Using the anchor (A = 1) at position 2 would give [-2, 2.5] -> token 3;
+    the best full path is [1, 3] (-1 + 6.5 via A[1] = 3) -- the greedy walk
+    does not take it."""
+    A = np.array([[-1.0], [3.0], [1.0], [0.0]])
+    B = np.array([[1.0], [-1.0], [0.0], [1.0]])
+    cand = np.array([[0, 1], [1, 3]])
+    unary = np.array([[0.0, 0.0], [0.0, 0.5]])
+    wh = np.array([[1.0], [2.0]])
+    return A, B, cand, unary, wh
+
+
+def test_selector_walk_hand_lattice():
+    A, B, cand, unary, wh = _walk_example()
+    ids, slots, q = O.selector_walk(2, cand, unary, wh, A, B)
+    assert ids.tolist() == [0, 1] and slots.tolist() == [0, 0]
+    # a two-way softmax is the logistic of the score difference
+    assert q[0, 0] == pytest.approx(1.0 / (1.0 + math.exp(-2.0)), rel=1e-12)
+    assert q[1, 0] == pytest.approx(1.0 / (1.0 + math.exp(-3.5)), rel=1e-12)
+    assert np.allclose(q.sum(axis=1), 1.0)
+
+
+def test_selector_without_compatibility_is_plain_dflash():
+    """A = 0 (or W_h = 0) leaves only the unary logits: the greedy walk picks
+    every position's top candidate, i.e. the plain argmax draft."""
+    cfg = tiny_cfg()
+    rng = np.random.default_rng(21)
+    W = tiny_weights(cfg, rng)
+    ctx = O.DraftContext(cfg)
+    ctx.inject([rng.normal(size=(5, cfg.target_hidden)) for _ in range(cfg.n_sel)], W)
+    r = 3
+    for sel in ({"A": np.zeros((cfg.vocab, r)), "B": rng.normal(size=(cfg.vocab, r)),
+                 "W_h": rng.normal(size=(r, cfg.hidden))},
+                {"A": rng.normal(size=(cfg.vocab, r)), "B": rng.normal(size=(cfg.vocab, r)),
+                 "W_h": np.zeros((r, cfg.hidden))}):
+        ids, cand, unary, q, wh, _ = O.draft_block_selector(cfg, W, sel, 7, ctx.layers(), ctx.kv_len, 4)
+        plain, _, _ = O.draft_block(cfg, W, 7, ctx.layers(), ctx.kv_len)
+        assert ids.tolist() == plain.tolist()
+        assert np.allclose(q, np.exp(unary - unary.max(1, keepdims=True)) /
+                           np.exp(unary - unary.max(1, keepdims=True)).sum(1, keepdims=True))
+
+
+def test_selector_sampled_walk_follows_q_rows():
+    """Sampling at one position draws the candidates with the softmax of the
+    chosen predecessor's scores; a shift of all unary logits changes nothing."""
+    A, B, cand, unary, wh = _walk_example()
+    rng = np.random.default_rng(22)
+    n = 20000
+    counts = np.zeros(2, np.int64)
+    for _ in range(n):
+        _, slots, q = O.selector_walk(2, cand[:1], unary[:1] + 5.0, wh[:1], A, B,
+                                      rng.exponential(size=(1, 2)).astype(np.float32))
+        counts[slots[0]] += 1
+    assert _chi2_pvalue(counts, [1.0 / (1.0 + math.exp(-2.0)), 1.0 / (1.0 + math.exp(2.0))]) > 1e-3
+
+
+def test_sampled_q_point_mass_is_the_plain_rule():
+    """q = 1 on the proposed token (K = 1 candidate list of the draft) is the
+    argmax drafter's rule."""
+    rng = np.random.default_rng(23)
+    V, S = 9, 5
+    for _ in range(300):
+        draft = rng.integers(0, V, S)
+        probs = rng.dirichlet(np.ones(V), S).astype(np.float32)
+        u = rng.random(S - 1).astype(np.float32)
+        e = rng.exponential(size=V).astype(np.float32)
+        a = O.accept_block_sampled_q(draft, probs, draft[1:, None], np.ones((S - 1, 1)), u, e)
+        b = O.accept_block_sampled(draft, probs, u, e)
+        assert a[:3] == b[:3] and a[3].tolist() == b[3].tolist()
+
+
+def test_sampled_q_accepts_whenever_q_is_at_most_p():
+    probs = np.full((3, 4), 0.25, np.float32)
+    cand = np.array([[1, 2], [3, 0]])
+    q = np.array([[0.2, 0.8], [0.25, 0.75]], np.float32)      # q(1) = 0.2 <= p, q(3) = 0.25 <= p
+    for u in (0.0, 0.5, 0.999):
+        acc, _, _, out = O.accept_block_sampled_q([0, 1, 3], probs, cand, q, np.full(2, u, np.float32),
+                                                  np.ones(4, np.float32))
+        assert acc == 2 and out[:2].tolist() == [1, 3]
+    # a token outside the candidate list (q = 0) is rejected
+    acc, bonus, _, _ = O.accept_block_sampled_q([0, 2, 3], probs, np.array([[1, 3], [3, 0]]), q,
+                                                np.zeros(2, np.float32), np.ones(4, np.float32))
+    assert acc == 0
+
+
+def test_sampled_q_is_lossless():
+    """y drawn from q over K candidates, accepted with min(1, p/q), else the
+    correction from [p - q]+: the emitted token follows p exactly."""
+    rng = np.random.default_rng(24)
+    V = 6
+    p0 = np.array([0.3, 0.05, 0.25, 0.0, 0.15, 0.25])
+    cand = np.array([2, 4, 3, 1])
+    q0 = np.array([0.1, 0.5, 0.3, 0.1])          # over-proposes 4 and the impossible 3
+    probs = np.tile(p0.astype(np.float32), (2, 1))
+    n = 30000
+    counts = np.zeros(V, np.int64)
+    for _ in range(n):
+        k = O.exponential_race(q0, rng.exponential(size=4).astype(np.float32))
+        _, _, _, out = O.accept_block_sampled_q([0, cand[k]], probs, cand[None, :], q0[None, :],
+                                                rng.random(1).astype(np.float32),
+                                                rng.exponential(size=V).astype(np.float32))
+        counts[out[0]] += 1
+    assert _chi2_pvalue(counts, p0) > 1e-3
+
+
+def test_selector_pins_catch_planted_mistakes(monkeypatch):
+    """Plausible mistakes in the selector must trip a pin (CPU only)."""
+    # 1. the predecessor stays the anchor for every position
+    orig_scores = O.selector_scores
+
+    def anchor_always(unary_row, cand_row, pred, wh_row, A, B):
+        return orig_scores(unary_row, cand_row, 2, wh_row, A, B)
+    monkeypatch.setattr(O, "selector_scores", anchor_always)
+    with pytest.raises(AssertionError):
+        test_selector_walk_hand_lattice()
+    monkeypatch.undo()
+    # 2. the compatibility term with A and B swapped (successor factor on the predecessor)
+    monkeypatch.setattr(O, "selector_scores", lambda u, c, p, w, A, B: orig_scores(u, c, p, w, B, A))
+    with pytest.raises(AssertionError):
+        test_selector_walk_hand_lattice()
+    monkeypatch.undo()
+    # 3. candidates in ascending logit order
+    orig_cand = O.compute_candidates
+    monkeypatch.setattr(O, "compute_candidates",
+                        lambda h, lm, K: tuple(x[:, ::-1] for x in orig_cand(h, lm, K)))
+    with pytest.raises(AssertionError):
+        test_candidates_order_ties_and_k1()
+    monkeypatch.undo()
+    # 4. residual without subtracting q (the plain rule's [p - 1{y}]+ applied to a real q)
+    orig_acc = O.accept_block_sampled_q
+
+    def residual_point_mass(draft, probs, cand, q_rows, u, e):
+        draft = np.asarray(draft); probs = np.asarray(probs, np.float32)
+        acc, bonus, commit, out = orig_acc(draft, probs, cand, q_rows, u, e)
+        if acc < len(draft) - 1:
+            w = probs[acc].copy(); w[draft[acc + 1]] = 0.0
+            bonus = O.exponential_race(w, e); out[acc] = bonus
+        return acc, bonus, commit, out
+    monkeypatch.setattr(O, "accept_block_sampled_q", residual_point_mass)
+    with pytest.raises(AssertionError):
+        test_sampled_q_is_lossless()
+    monkeypatch.undo()
