@@ -52,6 +52,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="qwen8b-b1")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--draft", default="plain", choices=["plain", "selector"],
+                    help="plain: argmax drafter; selector: DFlash 2 candidate selector "
+                         "(K=8 candidates, rank 128, greedy walk, random factors)")
     ap.add_argument("--verify", default="greedy", choices=["greedy", "sampled"],
                     help="greedy: dflash_accept_commit; sampled: dflash_accept_commit_sampled "
                          "(lossless rejection sampling against synthetic target rows)")
@@ -180,7 +183,7 @@ class ClockSampler:
 
 # ------------------------------------------------------------- our arm
 class Bench:
-    def __init__(self, wl, seed=0, verify="greedy"):
+    def __init__(self, wl, seed=0, verify="greedy", draft="plain"):
         import torch
         import block_diffusion_speculative_fc_gb300 as pkg
         self.torch, self.pkg = torch, pkg
@@ -241,6 +244,17 @@ class Bench:
         else:
             self.p = None
         self.verify = verify
+        self.selector = draft == "selector"
+        if self.selector:
+            g2 = torch.Generator(device="cuda")
+            g2.manual_seed(seed + 29)
+            dt = torch.bfloat16 if cfg.dtype != "f32" else torch.float32
+            r = 128
+            self.sel_w = ((torch.randn((r, cfg.hidden), generator=g2, device="cuda") /
+                           cfg.hidden ** 0.5).to(dt),
+                          (r ** -0.25 * torch.randn((cfg.vocab, r), generator=g2, device="cuda")).to(dt),
+                          (r ** -0.25 * torch.randn((cfg.vocab, r), generator=g2, device="cuda")).to(dt))
+            self.sess.set_selector(8, *self.sel_w)
         if verify == "sampled":
             # target rows: softmax of random logits; each cycle the proposed
             # tokens get the workload's match probability (outside the timed region)
@@ -276,6 +290,12 @@ class Bench:
             post[:, :-1] = torch.where(take, nxt, torch.where(idx == k[:, None], miss, r[:, :-1]))
         return post
 
+    def draft_call(self, anchor):
+        if self.selector:
+            self.sess.draft_selector(self.kv, anchor, self.draft)
+        else:
+            self.sess.draft(self.kv, anchor, self.draft)
+
     def cycle(self, c, u, r, k, ev=None):
         torch = self.torch
         self.kv.kv_len.copy_(self.base_len)
@@ -283,7 +303,7 @@ class Bench:
         anchor = self.anchor if c == 0 else self.bon
         if ev:
             ev[0].record()
-        self.sess.draft(self.kv, anchor, self.draft)
+        self.draft_call(anchor)
         if ev:
             ev[1].record()
         if self.verify == "sampled":
@@ -384,7 +404,7 @@ class Bench:
             self.kv.kv_len.copy_(self.base_len)
             self.seq.copy_(self.base_len)
             anchor = self.anchor if c == 0 else self.bon
-            self.sess.draft(self.kv, anchor, self.draft)
+            self.draft_call(anchor)
             main.wait_event(copied)
             if sampled:
                 self.probs.copy_(self.probs_base)
@@ -494,7 +514,7 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    bench = Bench(wl, verify=a.verify)
+    bench = Bench(wl, verify=a.verify, draft=a.draft)
     cs = ClockSampler(local)
     if dist:
         dist.barrier()
@@ -526,7 +546,7 @@ def main():
                        "layers": bench.cfg.n_layers, "hidden": bench.cfg.hidden,
                        "vocab": bench.cfg.vocab, "parallelism": f"replicas x{world}",
                        "l2": "inputs larger than L2 (weights streamed every step)",
-                       "kv_len_reset_each_cycle": True, "verify": a.verify,
+                       "kv_len_reset_each_cycle": True, "verify": a.verify, "draft": a.draft,
                        "mean_commit_len": mean_commit},
             "clocks": clocks, "e2e": e2e, "gpu_launches": launches,
             "roofline": roof, "cpu_baseline": cpu,

@@ -24,6 +24,7 @@ DERR_BITS = {0x1: "KV_CAPACITY", 0x2: "PAGE_RANGE", 0x4: "TOKEN_RANGE", 0x8: "PO
 EXPORTED = ["dflash_create", "dflash_destroy", "dflash_workspace_size", "dflash_bind_workspace",
             "dflash_inject_context", "dflash_draft_block", "dflash_accept_commit",
             "dflash_accept_commit_sampled",
+            "dflash_selector_workspace_size", "dflash_set_selector", "dflash_draft_block_selector",
             "dflash_get_error", "dflash_status_string", "dflash_last_error",
             "dflash_profile_enable", "dflash_profile_disable", "dflash_profile_collect"]
 
@@ -48,6 +49,11 @@ class DflashWeights(ctypes.Structure):
 class DflashKV(ctypes.Structure):
     _fields_ = [("k_pages", P_VOID), ("v_pages", P_VOID), ("page_table", c_void_p),
                 ("pages_per_req", c_int32), ("n_pages", c_int32), ("kv_len", c_void_p)]
+
+
+class DflashSelector(ctypes.Structure):
+    _fields_ = [("K", c_int32), ("rank", c_int32), ("W_h", c_void_p), ("A", c_void_p),
+                ("B", c_void_p)]
 
 
 class DflashProfileEntry(ctypes.Structure):
@@ -86,6 +92,10 @@ def load_library(path=LIB_PATH):
     lib.dflash_accept_commit_sampled.argtypes = [c_void_p, c_int32, c_void_p, c_void_p, c_void_p,
                                                  c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                                  c_void_p, c_void_p, c_int32, c_void_p]
+    lib.dflash_selector_workspace_size.argtypes = [c_void_p, c_int32, c_int32, ctypes.POINTER(c_size_t)]
+    lib.dflash_set_selector.argtypes = [c_void_p, ctypes.POINTER(DflashSelector), c_void_p, c_size_t]
+    lib.dflash_draft_block_selector.argtypes = [c_void_p, ctypes.POINTER(DflashKV), c_int32, c_void_p,
+                                                c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]
     lib.dflash_get_error.argtypes = [c_void_p, c_void_p, ctypes.POINTER(ctypes.c_uint32)]
     lib.dflash_profile_enable.argtypes = [c_void_p, c_int32]
     lib.dflash_profile_disable.argtypes = [c_void_p]
@@ -97,7 +107,8 @@ def load_library(path=LIB_PATH):
     lib.dflash_last_error.restype = ctypes.c_char_p
     for name in ["dflash_create", "dflash_workspace_size", "dflash_bind_workspace",
                  "dflash_inject_context", "dflash_draft_block", "dflash_accept_commit",
-                 "dflash_accept_commit_sampled", "dflash_get_error", "dflash_profile_enable", "dflash_profile_disable",
+                 "dflash_accept_commit_sampled", "dflash_selector_workspace_size",
+                 "dflash_set_selector", "dflash_draft_block_selector", "dflash_get_error", "dflash_profile_enable", "dflash_profile_disable",
                  "dflash_profile_collect"]:
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
@@ -171,6 +182,25 @@ def dflash_accept_commit_sampled(h, batch, draft_ids, probs, accept_u, exp_noise
         h, batch, _p(draft_ids), _p(probs), _p(accept_u), _p(exp_noise), _p(seq_len),
         _p(accept_len), _p(commit_len), _p(bonus), _p(out_tokens), _p(output_ids), out_stride,
         stream))
+
+
+def dflash_selector_workspace_size(h, K, rank):
+    n = c_size_t()
+    _check(load_library().dflash_selector_workspace_size(h, K, rank, ctypes.byref(n)))
+    return n.value
+
+
+def dflash_set_selector(h, sel, workspace, nbytes):
+    """sel: DflashSelector or None (removes the selector)."""
+    _check(load_library().dflash_set_selector(h, ctypes.byref(sel) if sel is not None else None,
+                                              _p(workspace), nbytes))
+
+
+def dflash_draft_block_selector(h, kv: DflashKV, batch, anchor, exp_noise, draft_ids, cand_ids,
+                                q_rows, stream):
+    _check(load_library().dflash_draft_block_selector(h, ctypes.byref(kv), batch, _p(anchor),
+                                                      _p(exp_noise), _p(draft_ids), _p(cand_ids),
+                                                      _p(q_rows), stream))
 
 
 def dflash_get_error(h, stream):

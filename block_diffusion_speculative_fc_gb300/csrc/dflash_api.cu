@@ -45,6 +45,13 @@ struct dflash_handle {
   size_t ws_bytes = 0;
   int store;      // ST_F32 / ST_BF16
   bool fuse = true;   // dependent bf16 GEMMs as one cooperative launch
+  // DFlash 2 candidate selector (dflash_set_selector); K == 0: not set
+  struct Selector {
+    int K = 0, rank = 0;
+    const void *W_h = nullptr, *A = nullptr, *B = nullptr;
+    char *ws = nullptr;
+    size_t keys = 0, bound = 0, wh = 0;   // offsets into ws
+  } sel;
   size_t es;      // element size of the configured dtype
   // optional per-launch event timing
   struct ProfRec {
@@ -218,6 +225,24 @@ void add_seg(GemmProblem &P, const void *W, int64_t ldw, int N, const EpiParams 
   s.ldw = ldw;
   s.N = N;
   s.epi = e;
+}
+
+// Selector workspace: per-tile top-K keys [ceil(V/128)][max_rows][K], the
+// per-row bounds [max_rows] and W_h (x*g) [max_rows][rank] fp32.
+struct SelLayout {
+  size_t keys, bound, wh, total;
+};
+SelLayout sel_layout(const dflash_handle *h, int K, int rank) {
+  const dflash_config &c = h->cfg;
+  const size_t rows = (size_t)c.max_batch * c.block_size;
+  const size_t n_vt = ((size_t)c.vocab + 127) / 128;
+  auto up = [](size_t v) { return (v + 255) & ~(size_t)255; };
+  SelLayout L;
+  L.keys = 0;
+  L.bound = up(n_vt * rows * K * 8);
+  L.wh = L.bound + up(rows * 8);
+  L.total = L.wh + up(rows * rank * 4);
+  return L;
 }
 
 int check_kv(const dflash_handle *h, const dflash_kv *kv) {
@@ -539,8 +564,16 @@ int dflash_inject_context(dflash_handle *h, const dflash_kv *kv, int32_t batch, 
   });
 }
 
-int dflash_draft_block(dflash_handle *h, const dflash_kv *kv, int32_t batch, const int32_t *anchor,
-                       int32_t *draft_ids, void *hidden_out, dflash_stream_t stream) {
+// The draft pass; with `run` the final launch ends in the DFlash 2 candidate
+// selector instead of the argmax.
+struct SelRun {
+  const float *exp_noise;
+  int32_t *cand_ids;
+  float *q_rows;
+};
+static int draft_impl(dflash_handle *h, const dflash_kv *kv, int32_t batch,
+                      const int32_t *anchor, int32_t *draft_ids, void *hidden_out,
+                      dflash_stream_t stream, const SelRun *run) {
   if (!h) return fail(DFLASH_EINVAL, "handle is NULL");
   if (!h->ws) return fail(DFLASH_ESTATE, "no workspace bound");
   const dflash_config &c = h->cfg;
@@ -560,7 +593,9 @@ int dflash_draft_block(dflash_handle *h, const dflash_kv *kv, int32_t batch, con
   void *qb = h->ws + h->L.qb, *kb = h->ws + h->L.kb, *vb = h->ws + h->L.vb;
   void *attn = h->ws + h->L.attn, *act = h->ws + h->L.act;
   int *row_pos = at<int>(h, h->L.row_pos);
-  unsigned long long *keys = at<unsigned long long>(h, h->L.keys);
+  // argmax keys, or with the selector its per-row bounds (cleared by the embedding alike)
+  unsigned long long *keys = run ? (unsigned long long *)(h->sel.ws + h->sel.bound)
+                                 : at<unsigned long long>(h, h->L.keys);
   const float2 *rope = at<const float2>(h, h->L.rope);
   int st;
 
@@ -682,10 +717,25 @@ int dflash_draft_block(dflash_handle *h, const dflash_kv *kv, int32_t batch, con
       // unchanged by the row's positive RMSNorm scale, so the lm_head runs on
       // x * final gain directly.
       prog[3] = problem_1src(xg, H, M, H);
-      EpiParams ea = epi_base(h, EPI_ARGMAX);
+      EpiParams ea = epi_base(h, run ? EPI_TOPK : EPI_ARGMAX);
       ea.N = c.vocab;
       ea.argmax_keys = keys;
+      if (run) {
+        // DFlash 2: every row's K best tokens per vocabulary tile, and W_h of
+        // the same operand as a second segment of the launch
+        ea.topk_keys = (unsigned long long *)(h->sel.ws + h->sel.keys);
+        ea.topk_bound = keys;
+        ea.topk = h->sel.K;
+        ea.topk_ld = ldq;
+      }
       add_seg(prog[3], h->lm_head, H, c.vocab, ea);
+      if (run) {
+        EpiParams ew = epi_base(h, EPI_STORE_F32);
+        ew.N = h->sel.rank;
+        ew.ld = h->sel.rank;
+        ew.out_f32 = (float *)(h->sel.ws + h->sel.wh);
+        add_seg(prog[3], h->sel.W_h, H, h->sel.rank, ew);
+      }
       ProgramFinalize fin;
       fin.keys = keys;
       fin.anchor = anchor;
@@ -693,7 +743,10 @@ int dflash_draft_block(dflash_handle *h, const dflash_kv *kv, int32_t batch, con
       fin.S = S;
       fin.draft_ids = draft_ids;
       if ((st = timed(h, "gemm_last_program", s,
-                      [&] { return run_program(h, prog, 4, s, nullptr, fused ? &fin : nullptr); })))
+                      [&] {
+                        return run_program(h, prog, 4, s, nullptr,
+                                           fused && !run ? &fin : nullptr);
+                      })))
         return st;
     }
   }
@@ -704,9 +757,90 @@ int dflash_draft_block(dflash_handle *h, const dflash_kv *kv, int32_t batch, con
                                nullptr, s);
        })))
     return st;
+  if (run) {
+    SelectorParams sp;
+    std::memset(&sp, 0, sizeof(sp));
+    sp.topk_keys = (const unsigned long long *)(h->sel.ws + h->sel.keys);
+    sp.n_vt = (c.vocab + 127) / 128;
+    sp.topk_ld = ldq;
+    sp.wh = (const float *)(h->sel.ws + h->sel.wh);
+    sp.ssq = ssq;
+    sp.ssq_ld = ldq;
+    sp.H = H;
+    sp.eps = c.rms_eps;
+    sp.A = h->sel.A;
+    sp.Bf = h->sel.B;
+    sp.store = h->store;
+    sp.anchor = anchor;
+    sp.exp_noise = run->exp_noise;
+    sp.draft_ids = draft_ids;
+    sp.cand_ids = run->cand_ids;
+    sp.q_rows = run->q_rows;
+    sp.B = batch;
+    sp.S = S;
+    sp.K = h->sel.K;
+    sp.rank = h->sel.rank;
+    sp.vocab = c.vocab;
+    sp.err = err;
+    return timed(h, "selector_walk", s, [&] { return launch_selector_walk(sp, s); });
+  }
   if (fused) return DFLASH_OK;   // the ids came with the last launch
   return timed(h, "argmax_finalize", s,
                [&] { return launch_argmax_finalize(keys, anchor, batch, S, draft_ids, s); });
+}
+
+int dflash_draft_block(dflash_handle *h, const dflash_kv *kv, int32_t batch, const int32_t *anchor,
+                       int32_t *draft_ids, void *hidden_out, dflash_stream_t stream) {
+  return draft_impl(h, kv, batch, anchor, draft_ids, hidden_out, stream, nullptr);
+}
+
+int dflash_selector_workspace_size(const dflash_handle *h, int32_t K, int32_t rank,
+                                   size_t *bytes) {
+  if (!h || !bytes) return fail(DFLASH_EINVAL, "handle and bytes must be non-NULL");
+  if (K < 1 || K > kSelMaxK || K > h->cfg.vocab)
+    return fail(DFLASH_EUNSUPPORTED, "selector: K must be in [1, 8] and at most vocab");
+  if (rank < 1 || rank > kSelMaxRank) return fail(DFLASH_EUNSUPPORTED, "selector: rank must be in [1, 256]");
+  *bytes = sel_layout(h, K, rank).total;
+  return DFLASH_OK;
+}
+
+int dflash_set_selector(dflash_handle *h, const dflash_selector *sel, void *workspace,
+                        size_t bytes) {
+  if (!h) return fail(DFLASH_EINVAL, "handle is NULL");
+  if (!sel) {
+    h->sel = dflash_handle::Selector();
+    return DFLASH_OK;
+  }
+  size_t need = 0;
+  if (int st = dflash_selector_workspace_size(h, sel->K, sel->rank, &need)) return st;
+  if (!sel->W_h || !sel->A || !sel->B)
+    return fail(DFLASH_EINVAL, "selector: W_h, A and B must be non-NULL");
+  if (!workspace || bytes < need) return fail(DFLASH_ECAPACITY, "selector workspace too small");
+  if ((uintptr_t)workspace & 255) return fail(DFLASH_EINVAL, "selector workspace must be 256-byte aligned");
+  if (h->cfg.block_size - 1 > 32) return fail(DFLASH_EUNSUPPORTED, "selector: block_size above 33");
+  if (h->store == ST_BF16 && (((uintptr_t)sel->W_h & 15) || (h->cfg.hidden * 2) % 16))
+    return fail(DFLASH_EINVAL, "selector: W_h must be 16-byte aligned");
+  const SelLayout L = sel_layout(h, sel->K, sel->rank);
+  h->sel.K = sel->K;
+  h->sel.rank = sel->rank;
+  h->sel.W_h = sel->W_h;
+  h->sel.A = sel->A;
+  h->sel.B = sel->B;
+  h->sel.ws = (char *)workspace;
+  h->sel.keys = L.keys;
+  h->sel.bound = L.bound;
+  h->sel.wh = L.wh;
+  return DFLASH_OK;
+}
+
+int dflash_draft_block_selector(dflash_handle *h, const dflash_kv *kv, int32_t batch,
+                                const int32_t *anchor, const float *exp_noise,
+                                int32_t *draft_ids, int32_t *cand_ids, float *q_rows,
+                                dflash_stream_t stream) {
+  if (!h) return fail(DFLASH_EINVAL, "handle is NULL");
+  if (h->sel.K == 0) return fail(DFLASH_ESTATE, "no selector set (dflash_set_selector)");
+  SelRun run = {exp_noise, cand_ids, q_rows};
+  return draft_impl(h, kv, batch, anchor, draft_ids, nullptr, stream, &run);
 }
 
 int dflash_accept_commit_sampled(dflash_handle *h, int32_t batch, const int32_t *draft_ids,

@@ -12,6 +12,8 @@
 //                 for all layers, heads and tokens).
 //   EPI_SWIGLU    silu(gate) * up of a paired gate/up tile.
 //   EPI_ARGMAX    greedy token choice without materialising logits.
+//   EPI_TOPK      the K best tokens of every row, per 128-token tile (DFlash 2
+//                 candidates), again without materialising logits.
 //   EPI_RESID / EPI_STORE_*  residual add / plain stores.
 // The tile is tiny and sits on the critical path of short launches, so every
 // op issues its global loads in batches before using them (one memory round
@@ -437,6 +439,59 @@ __device__ void run_epilogue(const EpiParams &e, float *t0, float *t1, int ldt, 
           best = other > best ? other : best;
         }
         if (lane == 0 && best) atomicMax(e.argmax_keys + m0 + r, best);
+      }
+      break;
+    }
+    case EPI_TOPK: {
+      // per row: the tile's topk best keys by topk rounds of a warp max over
+      // the 128 features (four per lane, sorted first); a row whose best key in
+      // this tile is below its running bound contributes nothing, which after
+      // the first tiles is almost every row.  Keys are unique (the id is part
+      // of the key), so one lane wins each round.
+      const int K = e.topk;
+      unsigned long long *base = e.topk_keys + (size_t)(n0 >> 7) * e.topk_ld * K;
+      for (int r = warp; r < rows; r += nwarps) {
+        unsigned long long k0, k1, k2, k3;
+        {
+          const int n = n0 + lane;
+          k0 = n < e.N ? argmax_key(t0[r * ldt + lane], n) : 0ull;
+          k1 = n + 32 < e.N ? argmax_key(t0[r * ldt + lane + 32], n + 32) : 0ull;
+          k2 = n + 64 < e.N ? argmax_key(t0[r * ldt + lane + 64], n + 64) : 0ull;
+          k3 = n + 96 < e.N ? argmax_key(t0[r * ldt + lane + 96], n + 96) : 0ull;
+        }
+        auto order = [](unsigned long long &a, unsigned long long &b) {
+          if (a < b) {
+            const unsigned long long t = a;
+            a = b;
+            b = t;
+          }
+        };
+        order(k0, k1);
+        order(k2, k3);
+        order(k0, k2);
+        order(k1, k3);
+        order(k1, k2);
+        const int m = m0 + r;
+        const unsigned long long bound = *(volatile const unsigned long long *)(e.topk_bound + m);
+        unsigned long long mine_out = 0ull, kth = 0ull;
+        int head = 0;
+        for (int j = 0; j < K; ++j) {
+          const unsigned long long mine = head == 0 ? k0 : head == 1 ? k1 : head == 2 ? k2
+                                          : head == 3 ? k3 : 0ull;
+          unsigned long long best = mine;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            const unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
+            best = other > best ? other : best;
+          }
+          if (j == 0 && best < bound) break;   // uniform across the warp
+          if (best != 0ull && mine == best) ++head;
+          if (lane == j) mine_out = best;
+          kth = best;
+        }
+        // lanes below topk write the row's list (zeros past a short list or a skipped row)
+        if (lane < K) base[(size_t)m * K + lane] = mine_out;
+        if (lane == 0 && kth != 0ull) atomicMax(e.topk_bound + m, kth);
       }
       break;
     }

@@ -21,6 +21,7 @@ enum EpiOp {
   EPI_STORE_ACT = 6,  // out_act[m*ld + n] = y
   EPI_RESID_NORM = 7, // x = out_f32 += y; out_act = x * norm_gain; ssq_out += x^2 per row
   EPI_STORE_NORM = 8, // out_act = y * norm_gain; ssq_out = y^2 per row
+  EPI_TOPK = 9,       // topk_keys[n0/128][m][0..K) = the tile's K best keys of row m
 };
 
 // Deferred RMSNorm.  A producer of a tensor that feeds a normalised GEMM
@@ -56,6 +57,13 @@ struct EpiParams {
   // EPI_RESID_NORM / EPI_STORE_NORM outputs
   const void *norm_gain;         // [N] gain of the next RMSNorm
   float *ssq_out;                // [N / 128][ssq_ld]
+  // EPI_TOPK: per 128-feature tile and row, the tile's topk best argmax keys
+  // (descending; 0 = none) at topk_keys[((n0 / 128) * topk_ld + m) * topk + i],
+  // or a single 0 when even the tile's best key is below topk_bound[m] (a
+  // lower bound on the row's topk-th best key over all tiles, raised here)
+  unsigned long long *topk_keys;
+  unsigned long long *topk_bound;
+  int topk, topk_ld;
 };
 
 constexpr int kMaxSrc = 8;   // sources of the K-split A operand (selected layers)
@@ -102,6 +110,28 @@ struct AttnScratch {
   float *part_ml;    // [max_items][R][2]
   int *tickets;      // [max_batch * kvh], zero between launches
 };
+
+// DFlash 2 candidate selector: merge of the per-tile top-K keys and the walk.
+constexpr int kSelMaxK = 8;       // candidates per position
+constexpr int kSelMaxRank = 256;  // rank of the compatibility term
+struct SelectorParams {
+  const unsigned long long *topk_keys;  // [n_vt][topk_ld][K] (EPI_TOPK)
+  int n_vt, topk_ld;                    // 128-row vocabulary tiles; row stride
+  const float *wh;                      // [B*S, rank] W_h (x * g), before the row's rstd
+  const float *ssq;                     // [H / 128][ssq_ld] sums of squares of the final norm
+  int ssq_ld, H;
+  float eps;
+  const void *A, *Bf;                   // [V, rank] predecessor / successor factors (model dtype)
+  int store;                            // ST_F32 / ST_BF16: dtype of A and Bf
+  const int *anchor;                    // [B]
+  const float *exp_noise;               // [B, S-1, K] Exp(1) or NULL (greedy walk)
+  int *draft_ids;                       // [B, S]
+  int *cand_ids;                        // [B, S-1, K] or NULL
+  float *q_rows;                        // [B, S-1, K] or NULL
+  int B, S, K, rank, vocab;
+  unsigned int *err;
+};
+cudaError_t launch_selector_walk(const SelectorParams &p, cudaStream_t s);
 
 constexpr int kTcMaxCtas = 160;   // persistent tensor-core GEMM grid cap (>= SM count)
 constexpr int kMaxPhases = 4;     // dependent GEMMs fused into one tensor-core launch

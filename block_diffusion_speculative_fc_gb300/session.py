@@ -12,7 +12,8 @@ import torch
 from . import (DFLASH_BF16, DFLASH_F32, DflashConfig, DflashKV, DflashWeights, _ptr_array,
                dflash_accept_commit, dflash_bind_workspace, dflash_create, dflash_destroy,
                dflash_accept_commit_sampled, dflash_draft_block, dflash_get_error,
-               dflash_inject_context, dflash_workspace_size,
+               dflash_inject_context, dflash_workspace_size, DflashSelector,
+               dflash_selector_workspace_size, dflash_set_selector, dflash_draft_block_selector,
                _check, load_library)
 
 
@@ -123,6 +124,30 @@ class DraftSession:
         dflash_accept_commit_sampled(self.h, batch, draft_ids, probs, accept_u, exp_noise, seq_len,
                                      accept_len, commit_len, bonus, out_tokens, output_ids, stride,
                                      _stream())
+
+    def set_selector(self, K, W_h, A, B):
+        """DFlash 2 candidate selector (include/dflash.h): K candidates per
+        position; W_h [rank, hidden], A and B [vocab, rank] device tensors in
+        the model dtype (kept referenced here).  None for W_h removes it."""
+        if W_h is None:
+            dflash_set_selector(self.h, None, None, 0)
+            self._sel = None
+            return
+        rank = W_h.shape[0]
+        n = dflash_selector_workspace_size(self.h, K, rank)
+        ws = torch.empty(n + 256, dtype=torch.uint8, device="cuda")
+        ptr = (ws.data_ptr() + 255) // 256 * 256
+        sel = DflashSelector(K, rank, W_h.data_ptr(), A.data_ptr(), B.data_ptr())
+        dflash_set_selector(self.h, sel, ptr, n)
+        self._sel = (sel, ws, W_h, A, B)
+
+    def draft_selector(self, kv, anchor, draft_ids, exp_noise=None, cand_ids=None, q_rows=None,
+                       batch=None):
+        """Draft block with the selector walk: greedy (exp_noise None) or
+        sampled with exp_noise [B, S-1, K] Exp(1) float32."""
+        batch = kv.batch if batch is None else batch
+        dflash_draft_block_selector(self.h, kv.struct, batch, anchor, exp_noise, draft_ids,
+                                    cand_ids, q_rows, _stream())
 
     def set_fusion(self, on):
         """Dependent GEMMs as one fused launch (True) or one launch each (False)."""

@@ -268,6 +268,59 @@ int dflash_accept_commit_sampled(dflash_handle *h, int32_t batch, const int32_t 
                                  int32_t *bonus, int32_t *out_tokens, int32_t *output_ids,
                                  int32_t out_stride, dflash_stream_t stream);
 
+/*
+ * DFlash 2 candidate selector ("Inside SGLang", "DFlash 2: replace selection,
+ * retain the serving loop").  After the same backbone pass as
+ * dflash_draft_block, every draft position j = 1..S-1 keeps the K best
+ * lm_head tokens as candidates (their logits are the unary scores U), and a
+ * left-to-right walk from the anchor chooses one candidate per position.
+ * From predecessor p (the anchor, then the candidate chosen before) candidate
+ * c of position j scores
+ *     score(p, c) = U(c) + sum_i A[p][i] * (W_h h_j)[i] * B[c][i]
+ * with h_j the final-normed hidden state of position j.  Greedy walk: the
+ * highest score, earliest candidate on ties.  Sampled walk: the exponential
+ * race over q = softmax(score(p, .)) with caller-given Exp(1) noise (largest
+ * q_k / noise_k, earliest on ties).  The walk does not search for the best
+ * full path.  Logits are never stored: the lm_head launch keeps each
+ * 128-token tile's K best per row, a small kernel merges them and walks.
+ *
+ * dflash_selector:
+ *   K        candidates per position, 1..8 (<= vocab)
+ *   rank     width of the compatibility term, 1..256
+ *   W_h      device [rank, hidden], A and B device [vocab, rank], all in the
+ *            configured dtype; W_h 16-byte aligned.  Caller-owned; must
+ *            outlive their use.
+ * dflash_selector_workspace_size: device bytes the selector needs for this
+ * handle's max_batch and block size (per-tile candidate keys of every row,
+ * per-row bounds, W_h h_j).  dflash_set_selector binds the weights and that
+ * workspace (256-byte aligned, caller-owned, not shared with overlapping
+ * calls); NULL sel removes the selector.  block_size must be <= 33.
+ *
+ * dflash_draft_block_selector: as dflash_draft_block (same anchor, kv and
+ * draft_ids layout; column 0 = anchor), with
+ *   exp_noise  device float32 [batch, S-1, K] Exp(1) variates (> 0) for the
+ *              sampled walk, or NULL for the greedy walk
+ *   cand_ids   optional device int32 [batch, S-1, K]: the candidates of every
+ *              position in logit order (lower id first among equal logits)
+ *   q_rows     optional device float32 [batch, S-1, K]: softmax of the chosen
+ *              predecessor's scores: the walk's proposal distribution, which
+ *              a lossless sampled verification of this drafter needs
+ * Returns DFLASH_ESTATE when no selector is set.
+ */
+typedef struct {
+  int32_t K;
+  int32_t rank;
+  const void *W_h;
+  const void *A;
+  const void *B;
+} dflash_selector;
+
+int dflash_selector_workspace_size(const dflash_handle *h, int32_t K, int32_t rank, size_t *bytes);
+int dflash_set_selector(dflash_handle *h, const dflash_selector *sel, void *workspace, size_t bytes);
+int dflash_draft_block_selector(dflash_handle *h, const dflash_kv *kv, int32_t batch,
+                                const int32_t *anchor, const float *exp_noise, int32_t *draft_ids,
+                                int32_t *cand_ids, float *q_rows, dflash_stream_t stream);
+
 /* Synchronise `stream`, read the sticky device error word into *word (may be
  * NULL) and clear it.  Returns DFLASH_OK if it was zero, DFLASH_EDEVICE if
  * not. */
