@@ -50,7 +50,7 @@ struct dflash_handle {
     int K = 0, rank = 0;
     const void *W_h = nullptr, *A = nullptr, *B = nullptr;
     char *ws = nullptr;
-    size_t keys = 0, bound = 0, wh = 0;   // offsets into ws
+    size_t keys = 0, bound = 0, wh = 0, cand = 0;   // offsets into ws
   } sel;
   size_t es;      // element size of the configured dtype
   // optional per-launch event timing
@@ -228,9 +228,10 @@ void add_seg(GemmProblem &P, const void *W, int64_t ldw, int N, const EpiParams 
 }
 
 // Selector workspace: per-tile top-K keys [ceil(V/128)][max_rows][K], the
-// per-row bounds [max_rows] and W_h (x*g) [max_rows][rank] fp32.
+// per-row bounds [max_rows], W_h (x*g) [max_rows][rank] fp32 and the merged
+// candidates [max_rows][K].
 struct SelLayout {
-  size_t keys, bound, wh, total;
+  size_t keys, bound, wh, cand, total;
 };
 SelLayout sel_layout(const dflash_handle *h, int K, int rank) {
   const dflash_config &c = h->cfg;
@@ -241,7 +242,8 @@ SelLayout sel_layout(const dflash_handle *h, int K, int rank) {
   L.keys = 0;
   L.bound = up(n_vt * rows * K * 8);
   L.wh = L.bound + up(rows * 8);
-  L.total = L.wh + up(rows * rank * 4);
+  L.cand = L.wh + up(rows * rank * 4);
+  L.total = L.cand + up(rows * K * 8);
   return L;
 }
 
@@ -763,6 +765,7 @@ static int draft_impl(dflash_handle *h, const dflash_kv *kv, int32_t batch,
     sp.topk_keys = (const unsigned long long *)(h->sel.ws + h->sel.keys);
     sp.n_vt = (c.vocab + 127) / 128;
     sp.topk_ld = ldq;
+    sp.cand_keys = (unsigned long long *)(h->sel.ws + h->sel.cand);
     sp.wh = (const float *)(h->sel.ws + h->sel.wh);
     sp.ssq = ssq;
     sp.ssq_ld = ldq;
@@ -830,6 +833,7 @@ int dflash_set_selector(dflash_handle *h, const dflash_selector *sel, void *work
   h->sel.keys = L.keys;
   h->sel.bound = L.bound;
   h->sel.wh = L.wh;
+  h->sel.cand = L.cand;
   return DFLASH_OK;
 }
 

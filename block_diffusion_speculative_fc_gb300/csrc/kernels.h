@@ -116,6 +116,7 @@ constexpr int kSelMaxK = 8;       // candidates per position
 constexpr int kSelMaxRank = 256;  // rank of the compatibility term
 struct SelectorParams {
   const unsigned long long *topk_keys;  // [n_vt][topk_ld][K] (EPI_TOPK)
+  unsigned long long *cand_keys;        // [topk_ld][K] the merged candidates of every row
   int n_vt, topk_ld;                    // 128-row vocabulary tiles; row stride
   const float *wh;                      // [B*S, rank] W_h (x * g), before the row's rstd
   const float *ssq;                     // [H / 128][ssq_ld] sums of squares of the final norm
@@ -131,6 +132,7 @@ struct SelectorParams {
   int B, S, K, rank, vocab;
   unsigned int *err;
 };
+// Two launches: the per-row merge of the tiles' lists, then the walk.
 cudaError_t launch_selector_walk(const SelectorParams &p, cudaStream_t s);
 
 constexpr int kTcMaxCtas = 160;   // persistent tensor-core GEMM grid cap (>= SM count)
