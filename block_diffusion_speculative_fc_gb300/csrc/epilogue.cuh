@@ -450,7 +450,12 @@ __device__ void run_epilogue(const EpiParams &e, float *t0, float *t1, int ldt, 
       // of the key), so one lane wins each round.
       const int K = e.topk;
       unsigned long long *base = e.topk_keys + (size_t)(n0 >> 7) * e.topk_ld * K;
-      for (int r = warp; r < rows; r += nwarps) {
+      // the running bounds of this warp's rows, all read at once (lane i: the
+      // warp's i-th row; rows <= 32 per call)
+      const int r_l = warp + nwarps * lane;
+      const unsigned long long my_bound =
+          r_l < rows ? *(volatile const unsigned long long *)(e.topk_bound + m0 + r_l) : 0ull;
+      for (int r = warp, i_row = 0; r < rows; r += nwarps, ++i_row) {
         unsigned long long k0, k1, k2, k3;
         {
           const int n = n0 + lane;
@@ -472,7 +477,7 @@ __device__ void run_epilogue(const EpiParams &e, float *t0, float *t1, int ldt, 
         order(k1, k3);
         order(k1, k2);
         const int m = m0 + r;
-        const unsigned long long bound = *(volatile const unsigned long long *)(e.topk_bound + m);
+        const unsigned long long bound = __shfl_sync(0xffffffffu, my_bound, i_row & 31);
         unsigned long long mine_out = 0ull, kth = 0ull;
         int head = 0;
         for (int j = 0; j < K; ++j) {
