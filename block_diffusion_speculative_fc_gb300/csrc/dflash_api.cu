@@ -228,7 +228,7 @@ void add_seg(GemmProblem &P, const void *W, int64_t ldw, int N, const EpiParams 
 }
 
 // Selector workspace: per-tile top-K keys [ceil(V/128)][max_rows][K], the
-// per-row bounds [max_rows], W_h (x*g) [max_rows][rank] fp32 and the merged
+// per-row bound slots [K][max_rows], W_h (x*g) [max_rows][rank] fp32 and the merged
 // candidates [max_rows][K].
 struct SelLayout {
   size_t keys, bound, wh, cand, total;
@@ -241,7 +241,7 @@ SelLayout sel_layout(const dflash_handle *h, int K, int rank) {
   SelLayout L;
   L.keys = 0;
   L.bound = up(n_vt * rows * K * 8);
-  L.wh = L.bound + up(rows * 8);
+  L.wh = L.bound + up(rows * K * 8);
   L.cand = L.wh + up(rows * rank * 4);
   L.total = L.cand + up(rows * K * 8);
   return L;
@@ -595,9 +595,13 @@ static int draft_impl(dflash_handle *h, const dflash_kv *kv, int32_t batch,
   void *qb = h->ws + h->L.qb, *kb = h->ws + h->L.kb, *vb = h->ws + h->L.vb;
   void *attn = h->ws + h->L.attn, *act = h->ws + h->L.act;
   int *row_pos = at<int>(h, h->L.row_pos);
-  // argmax keys, or with the selector its per-row bounds (cleared by the embedding alike)
+  // argmax keys (cleared by the embedding), or with the selector the slots of
+  // its per-row bounds, cleared here
   unsigned long long *keys = run ? (unsigned long long *)(h->sel.ws + h->sel.bound)
                                  : at<unsigned long long>(h, h->L.keys);
+  if (run && check_cuda(cudaMemsetAsync(keys, 0, (size_t)h->sel.K * ldq * 8, s),
+                        "selector bound reset"))
+    return DFLASH_ECUDA;
   const float2 *rope = at<const float2>(h, h->L.rope);
   int st;
 

@@ -449,12 +449,27 @@ __device__ void run_epilogue(const EpiParams &e, float *t0, float *t1, int ldt, 
       // the first tiles is almost every row.  Keys are unique (the id is part
       // of the key), so one lane wins each round.
       const int K = e.topk;
-      unsigned long long *base = e.topk_keys + (size_t)(n0 >> 7) * e.topk_ld * K;
-      // the running bounds of this warp's rows, all read at once (lane i: the
-      // warp's i-th row; rows <= 32 per call)
+      const int tile = n0 >> 7;
+      unsigned long long *base = e.topk_keys + (size_t)tile * e.topk_ld * K;
+      // A row's running lower bound of its K-th best key over the whole
+      // vocabulary: K slots per row, slot s the best key of the tiles t with
+      // t % K == s seen so far; the smallest slot is reached by K distinct
+      // keys, so it bounds the K-th best (0 while a slot is empty).  The
+      // slots of this warp's rows are read at once (lane i: the warp's i-th
+      // row; rows <= 32 per call).
       const int r_l = warp + nwarps * lane;
-      const unsigned long long my_bound =
-          r_l < rows ? *(volatile const unsigned long long *)(e.topk_bound + m0 + r_l) : 0ull;
+      unsigned long long my_bound = 0ull;
+      if (r_l < rows) {
+        my_bound = ~0ull;
+#pragma unroll
+        for (int sl = 0; sl < 8; ++sl) {
+          if (sl < K) {
+            const unsigned long long v =
+                *(volatile const unsigned long long *)(e.topk_bound + (size_t)sl * e.topk_ld + m0 + r_l);
+            my_bound = v < my_bound ? v : my_bound;
+          }
+        }
+      }
       for (int r = warp, i_row = 0; r < rows; r += nwarps, ++i_row) {
         unsigned long long k0, k1, k2, k3;
         {
@@ -478,7 +493,7 @@ __device__ void run_epilogue(const EpiParams &e, float *t0, float *t1, int ldt, 
         order(k1, k2);
         const int m = m0 + r;
         const unsigned long long bound = __shfl_sync(0xffffffffu, my_bound, i_row & 31);
-        unsigned long long mine_out = 0ull, kth = 0ull;
+        unsigned long long mine_out = 0ull, top1 = 0ull;
         int head = 0;
         for (int j = 0; j < K; ++j) {
           const unsigned long long mine = head == 0 ? k0 : head == 1 ? k1 : head == 2 ? k2
@@ -492,11 +507,11 @@ __device__ void run_epilogue(const EpiParams &e, float *t0, float *t1, int ldt, 
           if (j == 0 && best < bound) break;   // uniform across the warp
           if (best != 0ull && mine == best) ++head;
           if (lane == j) mine_out = best;
-          kth = best;
+          if (j == 0) top1 = best;
         }
         // lanes below topk write the row's list (zeros past a short list or a skipped row)
         if (lane < K) base[(size_t)m * K + lane] = mine_out;
-        if (lane == 0 && kth != 0ull) atomicMax(e.topk_bound + m, kth);
+        if (lane == 0 && top1 != 0ull) atomicMax(e.topk_bound + (size_t)(tile % K) * e.topk_ld + m, top1);
       }
       break;
     }

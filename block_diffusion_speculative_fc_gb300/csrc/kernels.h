@@ -59,8 +59,10 @@ struct EpiParams {
   float *ssq_out;                // [N / 128][ssq_ld]
   // EPI_TOPK: per 128-feature tile and row, the tile's topk best argmax keys
   // (descending; 0 = none) at topk_keys[((n0 / 128) * topk_ld + m) * topk + i],
-  // or a single 0 when even the tile's best key is below topk_bound[m] (a
-  // lower bound on the row's topk-th best key over all tiles, raised here)
+  // or zeros when even the tile's best key is below the row's running bound:
+  // topk_bound[s * topk_ld + m], s < topk, holds the best key of the tiles
+  // t % topk == s so far (zeroed before the launch); the smallest slot is a
+  // lower bound on the row's topk-th best key
   unsigned long long *topk_keys;
   unsigned long long *topk_bound;
   int topk, topk_ld;
