@@ -25,6 +25,7 @@ EXPORTED = ["dflash_create", "dflash_destroy", "dflash_workspace_size", "dflash_
             "dflash_inject_context", "dflash_draft_block", "dflash_accept_commit",
             "dflash_accept_commit_sampled",
             "dflash_selector_workspace_size", "dflash_set_selector", "dflash_draft_block_selector",
+            "dflash_accept_commit_sampled_q",
             "dflash_get_error", "dflash_status_string", "dflash_last_error",
             "dflash_profile_enable", "dflash_profile_disable", "dflash_profile_collect"]
 
@@ -96,6 +97,10 @@ def load_library(path=LIB_PATH):
     lib.dflash_set_selector.argtypes = [c_void_p, ctypes.POINTER(DflashSelector), c_void_p, c_size_t]
     lib.dflash_draft_block_selector.argtypes = [c_void_p, ctypes.POINTER(DflashKV), c_int32, c_void_p,
                                                 c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]
+    lib.dflash_accept_commit_sampled_q.argtypes = [c_void_p, c_int32, c_void_p, c_void_p, c_int32,
+                                                   c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                                   c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                                   c_int32, c_void_p]
     lib.dflash_get_error.argtypes = [c_void_p, c_void_p, ctypes.POINTER(ctypes.c_uint32)]
     lib.dflash_profile_enable.argtypes = [c_void_p, c_int32]
     lib.dflash_profile_disable.argtypes = [c_void_p]
@@ -108,7 +113,8 @@ def load_library(path=LIB_PATH):
     for name in ["dflash_create", "dflash_workspace_size", "dflash_bind_workspace",
                  "dflash_inject_context", "dflash_draft_block", "dflash_accept_commit",
                  "dflash_accept_commit_sampled", "dflash_selector_workspace_size",
-                 "dflash_set_selector", "dflash_draft_block_selector", "dflash_get_error", "dflash_profile_enable", "dflash_profile_disable",
+                 "dflash_set_selector", "dflash_draft_block_selector",
+                 "dflash_accept_commit_sampled_q", "dflash_get_error", "dflash_profile_enable", "dflash_profile_disable",
                  "dflash_profile_collect"]:
         getattr(lib, name).restype = ctypes.c_int
     _lib = lib
@@ -201,6 +207,15 @@ def dflash_draft_block_selector(h, kv: DflashKV, batch, anchor, exp_noise, draft
     _check(load_library().dflash_draft_block_selector(h, ctypes.byref(kv), batch, _p(anchor),
                                                       _p(exp_noise), _p(draft_ids), _p(cand_ids),
                                                       _p(q_rows), stream))
+
+
+def dflash_accept_commit_sampled_q(h, batch, draft_ids, probs, K, cand_ids, q_rows, accept_u,
+                                   exp_noise, seq_len, accept_len, commit_len, bonus, out_tokens,
+                                   output_ids, out_stride, stream):
+    _check(load_library().dflash_accept_commit_sampled_q(
+        h, batch, _p(draft_ids), _p(probs), K, _p(cand_ids), _p(q_rows), _p(accept_u),
+        _p(exp_noise), _p(seq_len), _p(accept_len), _p(commit_len), _p(bonus), _p(out_tokens),
+        _p(output_ids), out_stride, stream))
 
 
 def dflash_get_error(h, stream):

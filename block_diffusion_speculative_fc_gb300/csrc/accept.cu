@@ -92,15 +92,29 @@ cudaError_t launch_accept(int B, int S, int vocab, const int *draft, const int *
 // none); false if the stop position's proposed id lies outside the
 // vocabulary.  One warp, lane i decides block position i: every load is in
 // flight at once and a ballot finds the first rejection (S <= 32).
+// With a real proposal (cand/qr: the K candidates of every position and their
+// probabilities) y is accepted iff q(y) > 0 and u < p(y) / q(y), q(y) the
+// probability of the first candidate equal to y (0 if none).
 __device__ __forceinline__ bool sampled_stop(int b, int S, int vocab, const int *draft,
                                              const float *probs, const float *u, int lane,
-                                             int &acc, int &excl) {
+                                             int &acc, int &excl, const int *cand = nullptr,
+                                             const float *qr = nullptr, int K = 0) {
   const bool live = lane < S - 1;
   const int y = live ? draft[(int64_t)b * S + lane + 1] : 0;
   const bool bad = live && (y < 0 || y >= vocab);
   const float py = (live && !bad) ? probs[((int64_t)b * S + lane) * vocab + y] : 0.f;
   const float uu = live ? u[(int64_t)b * (S - 1) + lane] : 1.f;
-  const unsigned int taken = __ballot_sync(0xffffffffu, live && !bad && uu < py);
+  bool take = live && !bad && uu < py;
+  if (cand) {
+    float qy = 0.f;
+    if (live && !bad) {
+      const int64_t o = ((int64_t)b * (S - 1) + lane) * K;
+      for (int k = K - 1; k >= 0; --k)   // the first match wins
+        if (cand[o + k] == y) qy = qr[o + k];
+    }
+    take = live && !bad && qy > 0.f && uu < py / qy;
+  }
+  const unsigned int taken = __ballot_sync(0xffffffffu, take);
   acc = __ffs(~taken) - 1;   // first position not accepted, <= S-1
   const int ystop = __shfl_sync(0xffffffffu, y, acc);
   const bool bad_stop = __shfl_sync(0xffffffffu, bad ? 1 : 0, acc) != 0;
@@ -111,22 +125,38 @@ __device__ __forceinline__ bool sampled_stop(int b, int S, int vocab, const int 
 // grid (blocks per request, B): each CTA races a slice of the vocabulary of
 // request b's stop row and folds its winner into keys[b]; the last CTA of the
 // request (ticket) commits it and clears keys[b] and the ticket.
+// QMODE: the proposal is a real distribution over K candidates per position
+// (cand/qr); the residual at a rejection is [p - q]+ on those candidates.
+constexpr int kMaxQ = 8;
+template <bool QMODE>
 __global__ void __launch_bounds__(256) sampled_race_kernel(
     int S, int vocab, const int *__restrict__ draft, const float *__restrict__ probs,
     const float *__restrict__ u, const float *__restrict__ noise, unsigned long long *keys,
     int *tickets, int *seq_len, int *accept_len, int *commit_len, int *bonus, int *out_tokens,
-    int *output_ids, int out_stride, unsigned int *err) {
+    int *output_ids, int out_stride, unsigned int *err, const int *__restrict__ cand,
+    const float *__restrict__ qr, int K) {
   pdl_wait();
   __shared__ int s_acc, s_excl, s_ok, s_last;
   __shared__ unsigned long long s_best[8];
+  __shared__ int s_cid[kMaxQ];
+  __shared__ float s_q[kMaxQ];
   const int b = blockIdx.y;
   if (threadIdx.x < 32) {
     int acc, excl;
-    const bool ok = sampled_stop(b, S, vocab, draft, probs, u, threadIdx.x, acc, excl);
+    const bool ok = QMODE ? sampled_stop(b, S, vocab, draft, probs, u, threadIdx.x, acc, excl,
+                                         cand, qr, K)
+                          : sampled_stop(b, S, vocab, draft, probs, u, threadIdx.x, acc, excl);
+    if (QMODE && threadIdx.x < kMaxQ) {
+      // the stop position's candidates; none after full acceptance
+      const bool have = acc < S - 1 && (int)threadIdx.x < K;
+      const int64_t o = ((int64_t)b * (S - 1) + (have ? acc : 0)) * K + threadIdx.x;
+      s_cid[threadIdx.x] = have ? cand[o] : -1;
+      s_q[threadIdx.x] = have ? qr[o] : 0.f;
+    }
     if (threadIdx.x == 0) {
       s_ok = ok;
       s_acc = acc;
-      s_excl = excl;
+      s_excl = QMODE ? -1 : excl;
     }
   }
   __syncthreads();
@@ -135,6 +165,15 @@ __global__ void __launch_bounds__(256) sampled_race_kernel(
   unsigned long long best = 0ull;
   const int excl = s_excl;
   const int stride = gridDim.x * blockDim.x;
+  // [p - q]+ on the candidates (QMODE); p elsewhere
+  auto resid = [&](int v, float w) {
+    if (QMODE) {
+#pragma unroll
+      for (int k = 0; k < kMaxQ; ++k)
+        if (v == s_cid[k]) w = fmaxf(w - s_q[k], 0.f);
+    }
+    return w;
+  };
   if ((vocab & 3) == 0 && ((uintptr_t)row & 15) == 0 && ((uintptr_t)e & 15) == 0) {
     // four entries per load (16-byte loads of the row and the noise)
 #pragma unroll 2
@@ -144,13 +183,14 @@ __global__ void __launch_bounds__(256) sampled_race_kernel(
       const float w[4] = {w4.x, w4.y, w4.z, w4.w}, en[4] = {e4.x, e4.y, e4.z, e4.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const unsigned long long k = argmax_key((v + j == excl ? 0.f : w[j]) / en[j], v + j);
+        const unsigned long long k =
+            argmax_key((v + j == excl ? 0.f : resid(v + j, w[j])) / en[j], v + j);
         best = k > best ? k : best;
       }
     }
   } else {
     for (int v = blockIdx.x * blockDim.x + threadIdx.x; v < vocab; v += stride) {
-      const float w = v == excl ? 0.f : row[v];
+      const float w = v == excl ? 0.f : resid(v, row[v]);
       const unsigned long long k = argmax_key(w / e[v], v);
       best = k > best ? k : best;
     }
@@ -195,18 +235,24 @@ cudaError_t launch_accept_sampled(int B, int S, int vocab, const int *draft, con
                                   const float *u, const float *noise, unsigned long long *keys,
                                   int *tickets, int *seq_len, int *accept_len, int *commit_len,
                                   int *bonus, int *out_tokens, int *output_ids, int out_stride,
-                                  unsigned int *err, cudaStream_t s, int sms) {
+                                  unsigned int *err, cudaStream_t s, int sms, const int *cand,
+                                  const float *qr, int K) {
   if (B <= 0) return cudaSuccess;
-  if (S > 32) return cudaErrorInvalidValue;
+  if (S > 32 || (cand && (K < 1 || K > kMaxQ || !qr))) return cudaErrorInvalidValue;
   // about two waves of 256-thread CTAs over all requests' rows, each thread
   // taking at least four entries per pass
   int per = (2 * sms * 4 + B - 1) / B;
   per = per < 1 ? 1 : per;
   const int need = (vocab + 1023) / 1024;
   per = per > need ? need : per;
-  return launch_pdl(sampled_race_kernel, dim3(per, B), dim3(256), 0, s, S, vocab, draft, probs, u,
-                    noise, keys, tickets, seq_len, accept_len, commit_len, bonus, out_tokens,
-                    output_ids, out_stride, err);
+  if (cand)
+    return launch_pdl(sampled_race_kernel<true>, dim3(per, B), dim3(256), 0, s, S, vocab, draft,
+                      probs, u, noise, keys, tickets, seq_len, accept_len, commit_len, bonus,
+                      out_tokens, output_ids, out_stride, err, cand, qr, K);
+  return launch_pdl(sampled_race_kernel<false>, dim3(per, B), dim3(256), 0, s, S, vocab, draft,
+                    probs, u, noise, keys, tickets, seq_len, accept_len, commit_len, bonus,
+                    out_tokens, output_ids, out_stride, err, (const int *)nullptr,
+                    (const float *)nullptr, 0);
 }
 
 }  // namespace dflash

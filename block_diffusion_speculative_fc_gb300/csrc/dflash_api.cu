@@ -878,6 +878,36 @@ int dflash_accept_commit_sampled(dflash_handle *h, int32_t batch, const int32_t 
   });
 }
 
+int dflash_accept_commit_sampled_q(dflash_handle *h, int32_t batch, const int32_t *draft_ids,
+                                   const float *probs, int32_t K, const int32_t *cand_ids,
+                                   const float *q_rows, const float *accept_u,
+                                   const float *exp_noise, int32_t *seq_len, int32_t *accept_len,
+                                   int32_t *commit_len, int32_t *bonus, int32_t *out_tokens,
+                                   int32_t *output_ids, int32_t out_stride,
+                                   dflash_stream_t stream) {
+  if (!h) return fail(DFLASH_EINVAL, "handle is NULL");
+  if (!h->ws) return fail(DFLASH_ESTATE, "no workspace bound");
+  if (batch < 0) return fail(DFLASH_EINVAL, "negative batch");
+  if (batch > h->cfg.max_batch) return fail(DFLASH_ECAPACITY, "batch > max_batch");
+  if (batch == 0) return DFLASH_OK;
+  if (K < 1 || K > kSelMaxK) return fail(DFLASH_EUNSUPPORTED, "K must be in [1, 8]");
+  if (!draft_ids || !probs || !cand_ids || !q_rows || !accept_u || !exp_noise || !seq_len ||
+      !accept_len || !commit_len || !bonus || !out_tokens)
+    return fail(DFLASH_EINVAL, "a required pointer is NULL");
+  if (output_ids && out_stride <= 0) return fail(DFLASH_EINVAL, "out_stride must be positive");
+  cudaStream_t s = (cudaStream_t)stream;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return timed(h, "accept_sampled_q", s, [&] {
+    return launch_accept_sampled(batch, h->cfg.block_size, h->cfg.vocab, draft_ids, probs, accept_u,
+                                 exp_noise, at<unsigned long long>(h, h->L.skeys),
+                                 at<int>(h, h->L.stickets), seq_len, accept_len, commit_len, bonus,
+                                 out_tokens, output_ids, out_stride, at<unsigned int>(h, h->L.err), s,
+                                 sms > 0 ? sms : 1, cand_ids, q_rows, K);
+  });
+}
+
 int dflash_test_set_fusion(dflash_handle *h, int32_t on) {
   if (!h) return fail(DFLASH_EINVAL, "handle is NULL");
   h->fuse = on != 0;

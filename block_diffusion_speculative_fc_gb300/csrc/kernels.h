@@ -233,7 +233,9 @@ cudaError_t launch_accept_sampled(int B, int S, int vocab, const int *draft, con
                                   const float *u, const float *noise, unsigned long long *keys,
                                   int *tickets, int *seq_len, int *accept_len, int *commit_len,
                                   int *bonus, int *out_tokens, int *output_ids, int out_stride,
-                                  unsigned int *err, cudaStream_t s, int sms);
+                                  unsigned int *err, cudaStream_t s, int sms,
+                                  const int *cand = nullptr, const float *qr = nullptr,
+                                  int K = 0);
 
 // Host-side helpers implemented next to the handle (dflash_api.cu).
 int handle_lm_head(const dflash_handle *h, const void **lm_head, int *hidden, int *vocab,

@@ -14,6 +14,7 @@ from . import (DFLASH_BF16, DFLASH_F32, DflashConfig, DflashKV, DflashWeights, _
                dflash_accept_commit_sampled, dflash_draft_block, dflash_get_error,
                dflash_inject_context, dflash_workspace_size, DflashSelector,
                dflash_selector_workspace_size, dflash_set_selector, dflash_draft_block_selector,
+               dflash_accept_commit_sampled_q,
                _check, load_library)
 
 
@@ -124,6 +125,16 @@ class DraftSession:
         dflash_accept_commit_sampled(self.h, batch, draft_ids, probs, accept_u, exp_noise, seq_len,
                                      accept_len, commit_len, bonus, out_tokens, output_ids, stride,
                                      _stream())
+
+    def accept_sampled_q(self, batch, draft_ids, probs, cand_ids, q_rows, accept_u, exp_noise,
+                         seq_len, accept_len, commit_len, bonus, out_tokens, output_ids=None):
+        """Sampled verification against a real proposal: cand_ids [B, S-1, K]
+        int32 with q_rows [B, S-1, K] float32 (e.g. the selector's)."""
+        stride = output_ids.shape[1] if output_ids is not None else 0
+        dflash_accept_commit_sampled_q(self.h, batch, draft_ids, probs, cand_ids.shape[-1],
+                                       cand_ids, q_rows, accept_u, exp_noise, seq_len, accept_len,
+                                       commit_len, bonus, out_tokens, output_ids, stride,
+                                       _stream())
 
     def set_selector(self, K, W_h, A, B):
         """DFlash 2 candidate selector (include/dflash.h): K candidates per

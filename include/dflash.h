@@ -269,6 +269,28 @@ int dflash_accept_commit_sampled(dflash_handle *h, int32_t batch, const int32_t 
                                  int32_t out_stride, dflash_stream_t stream);
 
 /*
+ * Step 3, sampled variant for a drafter with a real proposal distribution
+ * (the DFlash 2 selector's q_rows; "Inside SGLang", "Sampling: preserve the
+ * proposal distribution the walk actually used").  q is zero outside each
+ * position's K candidates:
+ *   cand_ids   device int32 [batch, S-1, K]: candidates of block position i+1
+ *   q_rows     device float32 [batch, S-1, K]: their proposal probabilities
+ * draft[b][i+1] = y is accepted iff q(y) > 0 and
+ * accept_u[b][i] < probs[b][i][y] / q(y) (float32 IEEE division), q(y) the
+ * probability of the first candidate equal to y (0 if none: rejected).  At
+ * the first rejection the correction is the exponential race over
+ * [p - q]+ (p minus q on the candidates, clipped at 0, float32); after full
+ * acceptance over the target's last row.  K in [1, 8].  Every other argument
+ * and output as in dflash_accept_commit_sampled.
+ */
+int dflash_accept_commit_sampled_q(dflash_handle *h, int32_t batch, const int32_t *draft_ids,
+                                   const float *probs, int32_t K, const int32_t *cand_ids,
+                                   const float *q_rows, const float *accept_u,
+                                   const float *exp_noise, int32_t *seq_len, int32_t *accept_len,
+                                   int32_t *commit_len, int32_t *bonus, int32_t *out_tokens,
+                                   int32_t *output_ids, int32_t out_stride, dflash_stream_t stream);
+
+/*
  * DFlash 2 candidate selector ("Inside SGLang", "DFlash 2: replace selection,
  * retain the serving loop").  After the same backbone pass as
  * dflash_draft_block, every draft position j = 1..S-1 keeps the K best
@@ -303,8 +325,8 @@ int dflash_accept_commit_sampled(dflash_handle *h, int32_t batch, const int32_t 
  *   cand_ids   optional device int32 [batch, S-1, K]: the candidates of every
  *              position in logit order (lower id first among equal logits)
  *   q_rows     optional device float32 [batch, S-1, K]: softmax of the chosen
- *              predecessor's scores: the walk's proposal distribution, which
- *              a lossless sampled verification of this drafter needs
+ *              predecessor's scores: the walk's proposal distribution, the
+ *              input of dflash_accept_commit_sampled_q
  * Returns DFLASH_ESTATE when no selector is set.
  */
 typedef struct {

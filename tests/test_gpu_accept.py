@@ -179,3 +179,53 @@ def test_sampled_accept_edge_cases():
     assert "TOKEN_RANGE" in pkg.decode_error(word)
     assert seq.cpu().numpy()[3] == 11 and acc.cpu().numpy()[3] == -1
     s.close()
+
+
+# ------------------------------------- sampled verification with a real proposal
+def _q_case(rng, B, S, V, K):
+    """K distinct candidates per position (the draft token among them in most
+    positions, absent in some), proposal probabilities q over them, target
+    rows p, uniforms and noise."""
+    draft, p, u, e = _sampled_case(rng, B, S, V)
+    cand = np.empty((B, S - 1, K), np.int64)
+    q = np.empty((B, S - 1, K), np.float32)
+    for b in range(B):
+        for i in range(S - 1):
+            c = rng.choice(V, size=K, replace=False)
+            if rng.random() < 0.85 and draft[b, i + 1] not in c:
+                c[rng.integers(K)] = draft[b, i + 1]
+            cand[b, i] = c
+            q[b, i] = rng.dirichlet(np.full(K, 0.7)).astype(np.float32)
+    return draft, p, cand, q, u, e
+
+
+@pytest.mark.parametrize("B,S,V,K", [(1, 16, 1000, 8), (29, 8, 3001, 3), (4, 16, 151936, 8),
+                                     (6, 4, 64, 1)])
+def test_sampled_q_accept_bit_exact(B, S, V, K):
+    """Acceptance u < p(y)/q(y), residual [p - q]+ and the race are float32
+    operations both sides take identically: outputs must match exactly."""
+    cfg = shrink(CFG, block_size=S, vocab=V, mask_token_id=V - 1)
+    W = make_weights(cfg, device="cuda")
+    s = pkg.DraftSession(cfg, W, max_batch=B, max_rows=16, max_position=4096)
+    rng = np.random.default_rng(B * 7 + K)
+    f32 = lambda a: torch.as_tensor(a, dtype=torch.float32, device="cuda")  # noqa: E731
+    for rep in range(3):
+        draft, p, cand, q, u, e = _q_case(rng, B, S, V, K)
+        start = rng.integers(0, 40, B)
+        out_ids = np.full((B, 64), 7, dtype=np.int64)
+        d_out = i32(out_ids)
+        seq = i32(start)
+        acc = torch.zeros(B, dtype=torch.int32, device="cuda")
+        com, bon = torch.zeros_like(acc), torch.zeros_like(acc)
+        tok = torch.zeros((B, S), dtype=torch.int32, device="cuda")
+        s.accept_sampled_q(B, i32(draft), f32(p), i32(cand), f32(q), f32(u), f32(e), seq, acc, com,
+                           bon, tok, d_out)
+        acc_g, com_g, bon_g = acc.cpu().numpy(), com.cpu().numpy(), bon.cpu().numpy()
+        tok_g, seq_g, ids_g = tok.cpu().numpy(), seq.cpu().numpy(), d_out.cpu().numpy()
+        for b in range(B):
+            a, bonus, commit, out = O.accept_block_sampled_q(draft[b], p[b], cand[b], q[b], u[b], e[b])
+            ref_ids, ref_start = O.commit_output(out_ids[b], int(start[b]), draft[b], a, bonus)
+            assert (acc_g[b], com_g[b], bon_g[b], seq_g[b]) == (a, commit, bonus, ref_start), (rep, b)
+            assert np.array_equal(tok_g[b], out) and np.array_equal(ids_g[b], ref_ids)
+    assert s.error() == 0
+    s.close()
