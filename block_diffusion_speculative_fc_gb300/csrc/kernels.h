@@ -136,6 +136,7 @@ struct SelectorParams {
 };
 // Two launches: the per-row merge of the tiles' lists, then the walk.
 cudaError_t launch_selector_walk(const SelectorParams &p, cudaStream_t s);
+cudaError_t prepare_selector();
 
 constexpr int kTcMaxCtas = 160;   // persistent tensor-core GEMM grid cap (>= SM count)
 constexpr int kMaxPhases = 4;     // dependent GEMMs fused into one tensor-core launch

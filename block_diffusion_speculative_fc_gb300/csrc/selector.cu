@@ -310,6 +310,8 @@ __global__ void __launch_bounds__(kSelThreads) selector_walk_kernel(const __grid
   }
 }
 
+constexpr size_t kSelWalkCacheBytes = 200 * 1024;   // staged factor rows at most
+
 size_t walk_smem(const SelectorParams &p, size_t elem, bool cached) {
   const size_t n = p.S - 1;
   size_t b = kSelMaxRows * kSelMaxK * 8 + kSelMaxRows * 4 + n * p.rank * 4;
@@ -319,6 +321,18 @@ size_t walk_smem(const SelectorParams &p, size_t elem, bool cached) {
 
 }  // namespace
 
+// Shared-memory opt-in of the walk kernels on the current device (kernel
+// attributes are per device; run once per handle with the others).
+cudaError_t prepare_selector() {
+  cudaError_t e = cudaFuncSetAttribute(selector_walk_kernel<bf16>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kSelWalkCacheBytes + 4096);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(selector_walk_kernel<float>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)kSelWalkCacheBytes + 4096);
+}
+
 cudaError_t launch_selector_walk(const SelectorParams &p, cudaStream_t s) {
   if (p.B <= 0) return cudaSuccess;
   if (p.K < 1 || p.K > kSelMaxK || p.rank < 1 || p.rank > kSelMaxRank || p.S < 2 ||
@@ -327,19 +341,9 @@ cudaError_t launch_selector_walk(const SelectorParams &p, cudaStream_t s) {
   cudaError_t e = launch_pdl(selector_merge_kernel, dim3(p.S - 1, p.B), dim3(kSelThreads), 0, s, p);
   if (e != cudaSuccess) return e;
   const size_t elem = p.store == ST_BF16 ? 2 : 4;
-  constexpr size_t kCacheLimit = 200 * 1024;
+  constexpr size_t kCacheLimit = kSelWalkCacheBytes;
   const bool cached = walk_smem(p, elem, true) <= kCacheLimit;
   const size_t smem = walk_smem(p, elem, cached);
-  static bool attr_set = false;
-  if (!attr_set) {
-    e = cudaFuncSetAttribute(selector_walk_kernel<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kCacheLimit + 4096);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(selector_walk_kernel<float>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCacheLimit + 4096);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
   if (p.store == ST_BF16)
     return launch_pdl(selector_walk_kernel<bf16>, dim3(p.B), dim3(kSelThreads), smem, s, p,
                       cached ? 1 : 0);
