@@ -669,6 +669,27 @@ def test_selector_sampled_walk_follows_q_rows():
     assert _chi2_pvalue(counts, [1.0 / (1.0 + math.exp(-2.0)), 1.0 / (1.0 + math.exp(2.0))]) > 1e-3
 
 
+def test_selector_sampled_walk_conditions_on_the_drawn_predecessor():
+    """Two sampled positions: P(y1, y2) = q1(y1) q2(y2 | y1), position 2's
+    softmax taken for the token actually drawn at position 1 (predecessor 0:
+    A = -1, predecessor 1: A = 3 in the hand lattice)."""
+    A, B, cand, unary, wh = _walk_example()
+    # position-2 scores for predecessor p: U + A[p] * 2 * B[c], c in [1, 3]
+    def q2(pred):
+        s = np.array([0.0 + A[pred, 0] * 2.0 * B[1, 0], 0.5 + A[pred, 0] * 2.0 * B[3, 0]])
+        e = np.exp(s - s.max())
+        return e / e.sum()
+    q1 = np.array([1.0 / (1.0 + math.exp(-2.0)), 1.0 / (1.0 + math.exp(2.0))])
+    expect = np.array([q1[0] * q2(0)[0], q1[0] * q2(0)[1], q1[1] * q2(1)[0], q1[1] * q2(1)[1]])
+    rng = np.random.default_rng(25)
+    counts = np.zeros(4, np.int64)
+    for _ in range(20000):
+        _, slots, _ = O.selector_walk(2, cand, unary, wh, A, B,
+                                      rng.exponential(size=(2, 2)).astype(np.float32))
+        counts[2 * slots[0] + slots[1]] += 1
+    assert _chi2_pvalue(counts, expect) > 1e-3
+
+
 def test_sampled_q_point_mass_is_the_plain_rule():
     """q = 1 on the proposed token (K = 1 candidate list of the draft) is the
     argmax drafter's rule."""
@@ -728,6 +749,8 @@ def test_selector_pins_catch_planted_mistakes(monkeypatch):
     monkeypatch.setattr(O, "selector_scores", anchor_always)
     with pytest.raises(AssertionError):
         test_selector_walk_hand_lattice()
+    with pytest.raises(AssertionError):
+        test_selector_sampled_walk_conditions_on_the_drawn_predecessor()
     monkeypatch.undo()
     # 2. the compatibility term with A and B swapped (successor factor on the predecessor)
     monkeypatch.setattr(O, "selector_scores", lambda u, c, p, w, A, B: orig_scores(u, c, p, w, B, A))
