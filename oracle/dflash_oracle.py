@@ -34,7 +34,10 @@ The DFlash 2 selector (compute_candidates, selector_walk,
 draft_block_selector) and the sampled verification with a real proposal
 (accept_block_sampled_q) are pinned by hand-built lattices, reductions to the
 plain drafter and rule, and distribution tests of the walk and of
-losslessness; the pages print no numeric selector example.
+losslessness; the pages print no numeric selector example.  The FP8 KV
+cache (e4m3_decode, e4m3_encode, fp8_kv) is pinned by the format's fixed
+values, exhaustive round trips, ties and saturation, and the card's 12 KiB
+per token.
 The composition ``draft_forward`` has no printed numeric example on the pages;
 it is pinned through its pinned parts and through an independent loop-level
 restatement in the test suite ("parity unpinned by the pages" for the
@@ -423,6 +426,52 @@ def commit_output(output_ids, start, draft, acc, bonus):
     return output_ids, start + acc + 1
 
 
+# ---------------------------------------------------------------------------
+# FP8 draft KV cache ([P3] Kimi-K2.6 draft card: "12 KiB / token (FP8)" for
+# 6 layers x 2 (K, V) x 8 KV heads x 128 dims -- one byte per element and no
+# per-token scale).  Readings where the pages are silent: the OCP 8-bit
+# floating-point format E4M3 (1 sign bit, 4 exponent bits with bias 7, 3
+# mantissa bits, subnormals, no infinities, S.1111.111 = NaN, largest finite
+# value 448); an element x is stored as the code nearest to x / scale (ties
+# to the code with an even mantissa, magnitudes beyond 448 saturate to 448,
+# the sign is kept, NaN -> 0x7F), with one caller-given scale per layer and
+# per tensor (K, V); attention reads code value * scale.
+# ---------------------------------------------------------------------------
+def e4m3_decode(code):
+    """Value of E4M3 codes 0..255 (NaN for 0x7F and 0xFF)."""
+    c = np.asarray(code, dtype=np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(F64)
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2((e - 7).astype(F64)))
+    mag = np.where((e == 15) & ((c & 0x7) == 7), np.nan, mag)
+    return sign * mag
+
+
+def e4m3_encode(x):
+    """Nearest E4M3 code of each element (see the readings above), by
+    comparing against every finite positive code."""
+    x = np.asarray(x, dtype=F64)
+    pos_codes = np.arange(0x7F)                       # 0x00 .. 0x7E, ascending values
+    vals = e4m3_decode(pos_codes)
+    a = np.minimum(np.abs(x), 448.0).reshape(-1, 1)
+    dist = np.abs(a - vals[None, :])
+    best = dist.min(axis=1, keepdims=True)
+    tie = dist == best
+    # among the (at most two) nearest codes prefer the even mantissa
+    pick = np.where(tie & (pos_codes[None, :] % 2 == 0), pos_codes[None, :], 10 ** 6).min(axis=1)
+    pick = np.where(pick == 10 ** 6, np.argmax(tie, axis=1), pick)
+    code = pick | np.where(np.signbit(x.reshape(-1)), 0x80, 0)
+    code = np.where(np.isnan(x.reshape(-1)), 0x7F, code)
+    return code.reshape(x.shape).astype(np.int64)
+
+
+def fp8_kv(k, v, k_scale, v_scale):
+    """K, V as an FP8 cache reads them back: decode(encode(x / scale)) * scale."""
+    dq = lambda t, sc: e4m3_decode(e4m3_encode(_f64(t) / sc)) * sc  # noqa: E731
+    return dq(k, k_scale), dq(v, v_scale)
+
+
 class DraftContext:
     """Committed draft K/V of one request: per layer K, V [rows, KVH, D].
 
@@ -442,6 +491,10 @@ class DraftContext:
 
     def layers(self):
         return list(zip(self.k, self.v))
+
+    def layers_fp8(self, k_scales, v_scales):
+        """The committed K/V as an FP8 cache with per-layer scales holds them."""
+        return [fp8_kv(k, v, ks, vs) for k, v, ks, vs in zip(self.k, self.v, k_scales, v_scales)]
 
     # [P1] Step 7: only the committed prefix rows of the verify features become
     # context (prefix-valid writes).

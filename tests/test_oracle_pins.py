@@ -778,3 +778,89 @@ def test_selector_pins_catch_planted_mistakes(monkeypatch):
     with pytest.raises(AssertionError):
         test_sampled_q_is_lossless()
     monkeypatch.undo()
+
+
+# ------------------------------------------------------------ FP8 draft KV cache
+# [P3] Kimi-K2.6 draft card: "12 KiB / token (FP8)".  Reading: OCP FP8 E4M3
+# (bias 7, 3 mantissa bits, subnormals, no infinities, S.1111.111 = NaN, max
+# 448), nearest code with ties to the even mantissa, saturation, one scale per
+# layer and tensor.
+def test_fp8_footprint_is_one_byte_per_element():
+    """The card's shape (6 layers, 8 KV heads, head_dim 128) and its 12 KiB per
+    token leave exactly one byte per K or V element: no per-token scales."""
+    layers, kv_heads, head_dim = 6, 8, 128
+    assert layers * 2 * kv_heads * head_dim * 1 == 12 * 1024
+
+
+def test_e4m3_decode_format_values():
+    v = O.e4m3_decode(np.arange(256))
+    # values fixed by the format: zero, smallest subnormal, largest subnormal,
+    # smallest normal, one, largest finite, NaN, negative zero, negative max
+    assert v[0x00] == 0.0 and v[0x01] == 2.0 ** -9 and v[0x07] == 7 * 2.0 ** -9
+    assert v[0x08] == 2.0 ** -6 and v[0x38] == 1.0 and v[0x7E] == 448.0
+    assert np.isnan(v[0x7F]) and np.isnan(v[0xFF])
+    assert v[0x80] == 0.0 and np.signbit(v[0x80]) and v[0xFE] == -448.0
+    # exponent field e >= 1: (1 + m/8) 2^(e-7); each binade holds 8 codes
+    assert v[0x40] == 2.0 and v[0x48] == 4.0 and v[0x30] == 0.5 and v[0x3C] == 1.5
+    pos = v[:0x7F]
+    assert np.all(np.diff(pos) > 0)                       # codes order like their values
+    assert np.array_equal(v[0x80:0xFF], -pos)             # sign bit mirrors
+
+
+def test_e4m3_encode_round_trip_ties_and_saturation():
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)])
+    assert np.array_equal(O.e4m3_encode(O.e4m3_decode(codes)), codes)
+    pos = O.e4m3_decode(np.arange(0x7F))
+    mid = (pos[:-1] + pos[1:]) / 2
+    got = O.e4m3_encode(mid)
+    even = np.where(np.arange(0x7E) % 2 == 0, np.arange(0x7E), np.arange(1, 0x7F))
+    assert np.array_equal(got, even)                      # ties go to the even mantissa
+    assert O.e4m3_encode(mid[10] * (1 + 1e-9)) == 11      # just above a midpoint: up
+    assert O.e4m3_encode(mid[10] * (1 - 1e-9)) == 10      # just below: down
+    assert list(O.e4m3_encode([1e6, -1e6, 464.0, 470.0])) == [0x7E, 0xFE, 0x7E, 0x7E]
+    assert O.e4m3_encode(np.nan) == 0x7F
+    rng = np.random.default_rng(30)
+    x = rng.uniform(2.0 ** -6, 448.0, 20000) * rng.choice([-1, 1], 20000)
+    err = np.abs(O.e4m3_decode(O.e4m3_encode(x)) - x) / np.abs(x)
+    assert err.max() <= 2.0 ** -4 + 1e-12                 # half a unit in the last place
+
+
+def test_fp8_cache_is_exact_for_representable_values_and_feeds_attention():
+    """Values that are codes times the scale survive the cache unchanged, so
+    attention over the FP8 cache equals attention over the originals; other
+    values move by at most half a code step."""
+    rng = np.random.default_rng(31)
+    codes = rng.integers(0, 0x7F, (20, 2, 8)) | (rng.integers(0, 2, (20, 2, 8)) << 7)
+    codes = np.where(codes == 0xFF, 0xFE, codes)
+    k = O.e4m3_decode(codes) * 0.25
+    v = O.e4m3_decode(np.flip(codes, 0)) * 2.0
+    kq, vq = O.fp8_kv(k, v, 0.25, 2.0)
+    assert np.array_equal(kq, k) and np.array_equal(vq, v)
+    q = rng.normal(size=(3, 4, 8))
+    a = O.block_attention(q, k, v, k[:3], v[:3], np.arange(20, 23), np.arange(20), 0)
+    b = O.block_attention(q, kq, vq, k[:3], v[:3], np.arange(20, 23), np.arange(20), 0)
+    assert np.array_equal(a, b)
+    x = rng.normal(size=(50, 2, 8))
+    xq, _ = O.fp8_kv(x, x, 0.01, 0.01)
+    assert np.all(np.abs(xq - x) <= np.maximum(np.abs(x) * 2.0 ** -4, 0.01 * 2.0 ** -10) + 1e-15)
+
+
+def test_fp8_pins_catch_planted_mistakes(monkeypatch):
+    orig = O.e4m3_decode
+    # exponent bias 8 instead of 7
+    monkeypatch.setattr(O, "e4m3_decode", lambda c: orig(c) / 2.0)
+    with pytest.raises(AssertionError):
+        test_e4m3_decode_format_values()
+    monkeypatch.undo()
+    # ties away from zero instead of to even
+    enc = O.e4m3_encode
+
+    def away(x):
+        x = np.asarray(x, float)
+        c = enc(x)
+        up = enc(x * (1 + 1e-12))
+        return np.where(c != up, up, c)
+    monkeypatch.setattr(O, "e4m3_encode", away)
+    with pytest.raises(AssertionError):
+        test_e4m3_encode_round_trip_ties_and_saturation()
+    monkeypatch.undo()
