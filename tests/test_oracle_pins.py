@@ -690,6 +690,29 @@ def test_selector_sampled_walk_conditions_on_the_drawn_predecessor():
     assert _chi2_pvalue(counts, expect) > 1e-3
 
 
+def test_selector_walk_with_sampled_verification_is_lossless():
+    """The sampled walk's q_rows, fed to the real-q verification: given the
+    first draft accepted, the second emitted token follows the target row of
+    position 1 -- which holds only if q_rows[1] is the distribution the walk
+    drew position 2 from, i.e. conditioned on the predecessor it chose."""
+    A, B, cand, unary, wh = _walk_example()
+    V = 4
+    p = np.array([[0.1, 0.6, 0.2, 0.1], [0.3, 0.2, 0.15, 0.35], [0.25, 0.25, 0.25, 0.25]],
+                 np.float32)
+    rng = np.random.default_rng(26)
+    counts = np.zeros(V, np.int64)
+    for _ in range(40000):
+        ids, _, q = O.selector_walk(2, cand, unary, wh, A, B,
+                                    rng.exponential(size=(2, 2)).astype(np.float32))
+        draft = np.array([2, ids[0], ids[1]])
+        acc, _, _, out = O.accept_block_sampled_q(draft, p, cand, q.astype(np.float32),
+                                                  rng.random(2).astype(np.float32),
+                                                  rng.exponential(size=V).astype(np.float32))
+        if acc >= 1:
+            counts[out[1]] += 1
+    assert _chi2_pvalue(counts, p[1]) > 1e-3
+
+
 def test_sampled_q_point_mass_is_the_plain_rule():
     """q = 1 on the proposed token (K = 1 candidate list of the draft) is the
     argmax drafter's rule."""
@@ -751,6 +774,18 @@ def test_selector_pins_catch_planted_mistakes(monkeypatch):
         test_selector_walk_hand_lattice()
     with pytest.raises(AssertionError):
         test_selector_sampled_walk_conditions_on_the_drawn_predecessor()
+    monkeypatch.undo()
+    # q_rows reported for the anchor's row while the draw used the true predecessor
+    orig_walk = O.selector_walk
+
+    def wrong_rows(anchor, cand, unary, wh, A, B, exp_noise=None):
+        ids, slots, q = orig_walk(anchor, cand, unary, wh, A, B, exp_noise)
+        for j in range(1, len(ids)):
+            q[j] = O.softmax(orig_scores(unary[j], cand[j], anchor, wh[j], A, B))
+        return ids, slots, q
+    monkeypatch.setattr(O, "selector_walk", wrong_rows)
+    with pytest.raises(AssertionError):
+        test_selector_walk_with_sampled_verification_is_lossless()
     monkeypatch.undo()
     # 2. the compatibility term with A and B swapped (successor factor on the predecessor)
     monkeypatch.setattr(O, "selector_scores", lambda u, c, p, w, A, B: orig_scores(u, c, p, w, B, A))
