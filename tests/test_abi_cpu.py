@@ -103,3 +103,47 @@ def test_null_arguments_are_refused(lib):
     assert lib.dflash_workspace_size(None, None) == -1
     assert lib.dflash_inject_context(None, None, 0, 0, None, None, None, None) == -1
     pkg.dflash_destroy(None)
+
+
+def test_selector_host_checks(lib):
+    """Selector sizes, workspace and state checks are host-side (no CUDA)."""
+    cfg = WORKLOADS["tiny"].cfg
+    c, w, keep = _session_structs(cfg)
+    h = pkg.dflash_create(c, w)
+    for K, r in [(0, 16), (9, 16), (4, 0), (4, 257)]:
+        with pytest.raises(pkg.DFlashError) as ei:
+            pkg.dflash_selector_workspace_size(h, K, r)
+        assert ei.value.status == -2, (K, r)
+    rows, n_vt = 4 * cfg.block_size, (cfg.vocab + 127) // 128   # max_batch 4
+    n1 = pkg.dflash_selector_workspace_size(h, 1, 16)
+    n8 = pkg.dflash_selector_workspace_size(h, 8, 16)
+    nr = pkg.dflash_selector_workspace_size(h, 8, 256)
+    # per-tile keys, K bound slots per row, W_h h rows, merged candidates
+    assert n8 >= n_vt * rows * 8 * 8 + rows * 8 * 8 + rows * 16 * 4 + rows * 8 * 8
+    assert n1 < n8 < nr
+    kvarr = (ctypes.c_void_p * cfg.n_layers)(*([0x10000] * cfg.n_layers))
+    P = ctypes.cast(kvarr, ctypes.POINTER(ctypes.c_void_p))
+    kv = pkg.DflashKV(P, P, 0x10000, 4, 16, 0x10000)
+    with pytest.raises(pkg.DFlashError) as ei:      # no selector set
+        pkg.dflash_draft_block_selector(h, kv, 1, 0x10000, None, 0x10000, None, None, None)
+    assert ei.value.status == -6
+    need = pkg.dflash_selector_workspace_size(h, 4, 16)
+    sel = pkg.DflashSelector(4, 16, 0x10000, 0x10000, 0x10000)
+    with pytest.raises(pkg.DFlashError) as ei:
+        pkg.dflash_set_selector(h, sel, 0x10000, need - 1)           # too small
+    assert ei.value.status == -3
+    with pytest.raises(pkg.DFlashError) as ei:
+        pkg.dflash_set_selector(h, sel, 0x10010, need)               # not 256-byte aligned
+    assert ei.value.status == -1
+    with pytest.raises(pkg.DFlashError) as ei:
+        pkg.dflash_set_selector(h, pkg.DflashSelector(4, 16, None, 0x10000, 0x10000), 0x10000, need)
+    assert ei.value.status == -1
+    pkg.dflash_set_selector(h, sel, 0x10000, need)
+    with pytest.raises(pkg.DFlashError) as ei:      # selector set, but no workspace bound
+        pkg.dflash_draft_block_selector(h, kv, 1, 0x10000, None, 0x10000, None, None, None)
+    assert ei.value.status == -6
+    pkg.dflash_set_selector(h, None, None, 0)       # removed again
+    with pytest.raises(pkg.DFlashError) as ei:
+        pkg.dflash_accept_commit_sampled_q(h, 1, 1, 1, 4, 1, 1, 1, 1, 1, 1, 1, 1, 1, None, 0, None)
+    assert ei.value.status == -6                    # no workspace
+    pkg.dflash_destroy(h)
