@@ -37,7 +37,8 @@ plain drafter and rule, and distribution tests of the walk and of
 losslessness; the pages print no numeric selector example.  The FP8 KV
 cache (e4m3_decode, e4m3_encode, fp8_kv) is pinned by the format's fixed
 values, exhaustive round trips, ties and saturation, and the card's 12 KiB
-per token.
+per token.  Draft KV windowing (DraftContext.window_layers,
+draft_block_windowed) is pinned against the full context masked per query.
 The composition ``draft_forward`` has no printed numeric example on the pages;
 it is pinned through its pinned parts and through an independent loop-level
 restatement in the test suite ("parity unpinned by the pages" for the
@@ -168,11 +169,12 @@ def silu(x):
     return x / (1.0 + np.exp(-x))
 
 
-def draft_layer(x, layer_w, k_ctx, v_ctx, positions, window, cfg):
+def draft_layer(x, layer_w, k_ctx, v_ctx, positions, window, cfg, ctx_pos=None):
     """One DFlashDecoderLayer on the block rows of one request.
 
     x [S, H] residual stream; returns the updated residual stream.  The
     block K/V computed here live only for this pass and are never committed.
+    ctx_pos: positions of the context rows (default 0, 1, ...).
     """
     S = x.shape[0]
     D = cfg.head_dim
@@ -183,7 +185,8 @@ def draft_layer(x, layer_w, k_ctx, v_ctx, positions, window, cfg):
     v = linear(h, wv).reshape(S, cfg.n_kv_heads, D)
     q = rope_neox(head_rms_norm(q, layer_w["q_norm"], cfg.rms_eps), positions, cfg.rope_theta)
     k = rope_neox(head_rms_norm(k, layer_w["k_norm"], cfg.rms_eps), positions, cfg.rope_theta)
-    ctx_pos = np.arange(k_ctx.shape[0], dtype=np.int64)
+    if ctx_pos is None:
+        ctx_pos = np.arange(k_ctx.shape[0], dtype=np.int64)
     a = block_attention(q, k_ctx, v_ctx, k, v, positions, ctx_pos, window)
     x = x + linear(a.reshape(S, cfg.n_heads * D), layer_w["o"])
     h2 = rms_norm(x, layer_w["post_norm"], cfg.rms_eps)
@@ -195,10 +198,11 @@ def draft_layer(x, layer_w, k_ctx, v_ctx, positions, window, cfg):
 
 # [P1] Step 3 (block_ids = [anchor, MASK...], positions = prefix + j) and
 # Step 4 (backbone, final norm); [P3] "draft model predict".
-def draft_forward(cfg, W, anchor, ctx_kv_layers, kv_len):
+def draft_forward(cfg, W, anchor, ctx_kv_layers, kv_len, ctx_pos=None):
     """Draft backbone for one request.
 
-    ctx_kv_layers: per layer (K [kv_len, KVH, D], V) of the committed context.
+    ctx_kv_layers: per layer (K [kv_len, KVH, D], V) of the committed context
+    (or, with ctx_pos, of the context rows at those positions).
     Returns the final-normed hidden states [S, H].
     """
     S = cfg.block_size
@@ -209,7 +213,7 @@ def draft_forward(cfg, W, anchor, ctx_kv_layers, kv_len):
     for l in range(cfg.n_layers):
         kc, vc = ctx_kv_layers[l]
         x = draft_layer(x, W["layers"][l], kc[:kv_len], vc[:kv_len], positions,
-                        cfg.sliding_window[l], cfg)
+                        cfg.sliding_window[l], cfg, ctx_pos)
     return rms_norm(x, W["final_norm"], cfg.rms_eps)
 
 
@@ -230,6 +234,17 @@ def lm_head_argmax(hidden_rows, lm_head):
 def draft_block(cfg, W, anchor, ctx_kv_layers, kv_len):
     """Full draft pass for one request: ids [S] (col 0 = anchor), hidden [S, H], margins [S-1]."""
     hid = draft_forward(cfg, W, anchor, ctx_kv_layers, kv_len)
+    ids, margin = lm_head_argmax(hid[1:], W["lm_head"])
+    out = np.empty(cfg.block_size, dtype=np.int64)
+    out[0] = anchor
+    out[1:] = ids
+    return out, hid, margin
+
+
+def draft_block_windowed(cfg, W, anchor, ctx, draft_window):
+    """draft_block over the compact store of the last draft_window rows."""
+    layers, pos = ctx.window_layers(draft_window)
+    hid = draft_forward(cfg, W, anchor, layers, ctx.kv_len, pos)
     ids, margin = lm_head_argmax(hid[1:], W["lm_head"])
     out = np.empty(cfg.block_size, dtype=np.int64)
     out[0] = anchor
@@ -491,6 +506,19 @@ class DraftContext:
 
     def layers(self):
         return list(zip(self.k, self.v))
+
+    # Draft KV windowing ([P1]: "with draft windowing enabled, the draft uses
+    # a private compact mapping over the shared global index space";
+    # --speculative-dflash-draft-window-size).  Reading: the draft keeps the
+    # most recent draft_window committed rows of a request, at their original
+    # positions (their K keeps the rotation of its position); every block
+    # query sees exactly those rows and the block, and a sliding layer still
+    # applies its own window on top.
+    def window_layers(self, draft_window):
+        """The compact store: per-layer (K, V) of the kept rows and their positions."""
+        lo = max(0, self.kv_len - int(draft_window))
+        return ([(k[lo:], v[lo:]) for k, v in zip(self.k, self.v)],
+                np.arange(lo, self.kv_len, dtype=np.int64))
 
     def layers_fp8(self, k_scales, v_scales):
         """The committed K/V as an FP8 cache with per-layer scales holds them."""

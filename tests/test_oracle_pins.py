@@ -899,3 +899,76 @@ def test_fp8_pins_catch_planted_mistakes(monkeypatch):
     with pytest.raises(AssertionError):
         test_e4m3_encode_round_trip_ties_and_saturation()
     monkeypatch.undo()
+
+
+# ----------------------------------------------------------- draft KV windowing
+# [P1]: "with draft windowing enabled, the draft uses a private compact mapping
+# over the shared global index space"; --speculative-dflash-draft-window-size.
+# Reading: keep the most recent W_d committed rows at their positions; every
+# block query sees exactly those rows (and the block); sliding layers still
+# apply their own window.
+def _masked_per_query(q, k, v, kb, vb, q_pos, kv_len, draft_window, layer_window):
+    """Attention over the full context with the rows before kv_len - W_d
+    hidden, one query at a time: for query j at kv_len + j a per-query window
+    of W_d + j + 1 hides exactly those rows (block keys are always seen); a
+    layer window W is the smaller of the two."""
+    out = []
+    for j in range(q.shape[0]):
+        w = draft_window + j + 1
+        if layer_window:
+            w = min(w, layer_window)
+        out.append(O.block_attention(q[j:j + 1], k, v, kb, vb, q_pos[j:j + 1],
+                                     np.arange(kv_len), w))
+    return np.concatenate(out, axis=0)
+
+
+@pytest.mark.parametrize("draft_window,layer_window", [(7, 0), (7, 4), (25, 0), (1, 0)])
+def test_compact_window_store_equals_masked_full_context(draft_window, layer_window):
+    rng = np.random.default_rng(40 + draft_window + layer_window)
+    kv_len, S, kvh, nh, D = 20, 4, 2, 4, 8
+    k, v = rng.normal(size=(kv_len, kvh, D)), rng.normal(size=(kv_len, kvh, D))
+    kb, vb = rng.normal(size=(S, kvh, D)), rng.normal(size=(S, kvh, D))
+    q = rng.normal(size=(S, nh, D))
+    q_pos = kv_len + np.arange(S)
+    lo = max(0, kv_len - draft_window)
+    compact = O.block_attention(q, k[lo:], v[lo:], kb, vb, q_pos, np.arange(lo, kv_len), layer_window)
+    masked = _masked_per_query(q, k, v, kb, vb, q_pos, kv_len, draft_window, layer_window)
+    assert np.allclose(compact, masked, rtol=1e-12, atol=1e-12)
+
+
+def test_window_store_keeps_the_newest_rows_at_their_positions():
+    cfg = tiny_cfg()
+    rng = np.random.default_rng(41)
+    W = tiny_weights(cfg, rng)
+    ctx = O.DraftContext(cfg)
+    ctx.inject([rng.normal(size=(9, cfg.target_hidden)) for _ in range(cfg.n_sel)], W)
+    layers, pos = ctx.window_layers(4)
+    assert pos.tolist() == [5, 6, 7, 8]
+    assert np.array_equal(layers[0][0], ctx.k[0][5:]) and np.array_equal(layers[1][1], ctx.v[1][5:])
+    # a window at least as long as the context changes nothing
+    full, hf, _ = O.draft_block(cfg, W, 3, ctx.layers(), ctx.kv_len)
+    same, hs, _ = O.draft_block_windowed(cfg, W, 3, ctx, 9)
+    assert np.array_equal(full, same) and np.allclose(hf, hs, rtol=0, atol=0)
+    # a short window does change the block's hidden states
+    _, hw, _ = O.draft_block_windowed(cfg, W, 3, ctx, 2)
+    assert not np.allclose(hw, hf)
+
+
+def test_window_pins_catch_planted_mistakes(monkeypatch):
+    """Re-basing the kept rows' positions to 0 breaks a layer window on top."""
+    orig = O.DraftContext.window_layers
+
+    def rebased(self, draft_window):
+        layers, pos = orig(self, draft_window)
+        return layers, np.arange(len(pos), dtype=np.int64)
+    rng = np.random.default_rng(42)
+    kv_len, S, kvh, nh, D = 20, 4, 2, 4, 8
+    k, v = rng.normal(size=(kv_len, kvh, D)), rng.normal(size=(kv_len, kvh, D))
+    kb, vb = rng.normal(size=(S, kvh, D)), rng.normal(size=(S, kvh, D))
+    q = rng.normal(size=(S, nh, D))
+    q_pos = kv_len + np.arange(S)
+    ctx = SimpleNamespace(k=[k], v=[v], kv_len=kv_len)
+    layers, pos = rebased(ctx, 7)
+    wrong = O.block_attention(q, layers[0][0], layers[0][1], kb, vb, q_pos, pos, 4)
+    right = _masked_per_query(q, k, v, kb, vb, q_pos, kv_len, 7, 4)
+    assert not np.allclose(wrong, right)
