@@ -147,3 +147,23 @@ def test_selector_host_checks(lib):
         pkg.dflash_accept_commit_sampled_q(h, 1, 1, 1, 4, 1, 1, 1, 1, 1, 1, 1, 1, 1, None, 0, None)
     assert ei.value.status == -6                    # no workspace
     pkg.dflash_destroy(h)
+
+
+def test_public_headers_compile_as_c_and_cpp():
+    """The boundary is a C ABI: its headers must compile as plain C99
+    (pedantic) and as C++, with no CUDA compiler involved."""
+    import shutil
+    import subprocess
+    cc, cxx = shutil.which("gcc"), shutil.which("g++")
+    if not cc or not cxx:
+        pytest.skip("no host C/C++ compiler")
+    inc = os.path.join(ROOT, "include")
+    cuda_inc = "/usr/local/cuda/include"
+    for h in sorted(f for f in os.listdir(inc) if f.endswith(".h")):
+        path = os.path.join(inc, h)
+        for cmd in ([cc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-fsyntax-only",
+                     "-x", "c", "-I", cuda_inc, path],
+                    [cxx, "-std=c++17", "-Wall", "-Werror", "-fsyntax-only", "-x", "c++", "-I",
+                     cuda_inc, path]):
+            r = subprocess.run(cmd, capture_output=True, text=True)
+            assert r.returncode == 0, (h, r.stderr)
