@@ -167,3 +167,22 @@ def test_public_headers_compile_as_c_and_cpp():
                      cuda_inc, path]):
             r = subprocess.run(cmd, capture_output=True, text=True)
             assert r.returncode == 0, (h, r.stderr)
+
+
+def test_plain_c_caller_links_and_runs(lib, tmp_path):
+    """tests/abi_example.c: a C program built with gcc against include/ and
+    linked to libdflash.so uses the host-side ABI (no GPU needed)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc")
+    if not cc:
+        pytest.skip("no host C compiler")
+    libdir = os.path.dirname(pkg.LIB_PATH)
+    exe = str(tmp_path / "abi_example")
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        os.path.join(ROOT, "tests", "abi_example.c"), "-L", libdir, "-ldflash",
+                        "-Wl,-rpath," + libdir, "-o", exe], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, (r.returncode, r.stdout, r.stderr)
+    assert r.stdout.startswith("ok workspace="), r.stdout
