@@ -146,6 +146,50 @@ def test_concat_column_blocks_reach_fc_in_list_order():
     assert np.allclose(yh / yh[:, :1], y / y[:, :1])
 
 
+def _check_projection_closed_form(project):
+    """fc + hidden_norm ("Inside SGLang", Step 1: project_target_hidden() is fc
+    then hidden_norm; CSDN article, "draft model predict": hidden_norm(fc(x))).
+    Inputs are built so that fc(X) has rows c_r * s with s a +-1 pattern: an
+    RMSNorm applied after fc sees a row of RMS |c_r|, so the output row is
+    exactly sign(c_r) * s * g (times |c_r| / sqrt(c_r^2 + eps)).  fc is dense
+    and the gain is not uniform."""
+    rng = np.random.default_rng(7)
+    rows, Ht, n_sel, H = 4, 24, 3, 16
+    fc = rng.normal(0, 0.3, (H, n_sel * Ht))
+    s = rng.choice([-1.0, 1.0], H)
+    c = np.array([0.7, -2.5, 11.0, 0.05])
+    Y = c[:, None] * s[None, :]
+    # X with X fc^T = Y: fc^T has full column rank, so pinv(fc^T) fc^T = I
+    X = Y @ np.linalg.pinv(fc.T)
+    assert np.allclose(X @ fc.T, Y, atol=1e-12)
+    feats = [X[:, j * Ht:(j + 1) * Ht] for j in range(n_sel)]
+    g = rng.uniform(0.5, 1.5, H)
+    for eps in (0.0, 1e-6, 0.3):
+        y = project(feats, fc, g, eps)
+        want = (c / np.sqrt(c * c + eps))[:, None] * s[None, :] * g[None, :]
+        assert np.allclose(y, want, rtol=1e-9, atol=1e-12), eps
+
+
+def test_project_target_hidden_is_fc_then_gained_rmsnorm():
+    _check_projection_closed_form(O.project_target_hidden)
+
+
+def test_projection_pin_catches_planted_mistakes():
+    def norm_before_fc(feats, fc, g, eps):
+        x = np.concatenate(feats, -1)
+        return O.linear(O.rms_norm(x, np.ones(x.shape[1]), eps), fc) * g
+
+    def gain_dropped(feats, fc, g, eps):
+        return O.rms_norm(O.linear(np.concatenate(feats, -1), fc), np.ones_like(g), eps)
+
+    def reversed_concat(feats, fc, g, eps):
+        return O.rms_norm(O.linear(np.concatenate(feats[::-1], -1), fc), g, eps)
+
+    for wrong in (norm_before_fc, gain_dropped, reversed_concat):
+        with pytest.raises(AssertionError):
+            _check_projection_closed_form(wrong)
+
+
 # ----------------------------------------------------------------- RMSNorm
 def test_rms_norm_hand_vector_and_invariants():
     y = O.rms_norm(np.array([[3.0, 4.0]]), np.ones(2), 0.0)
@@ -899,6 +943,53 @@ def test_fp8_pins_catch_planted_mistakes(monkeypatch):
     with pytest.raises(AssertionError):
         test_e4m3_encode_round_trip_ties_and_saturation()
     monkeypatch.undo()
+
+
+def _check_layers_fp8(layers_fp8):
+    """DraftContext.layers_fp8 with per-layer (K, V) scales: K/V values that
+    are E4M3 codes times their own layer's scale come back unchanged, and
+    values past 448 * scale saturate there.  The scales (0.3, 1.7, 0.11,
+    5.0) are unrelated by powers of two, so a value stored with another
+    layer's or the other tensor's scale is in general not representable and
+    changes."""
+    cfg = tiny_cfg(n_layers=2)
+    rng = np.random.default_rng(33)
+    ks, vs = [0.3, 0.11], [1.7, 5.0]
+    ctx = O.DraftContext(cfg)
+    shape = (30, cfg.n_kv_heads, cfg.head_dim)
+    for l in range(2):
+        codes_k = rng.integers(0x08, 0x7F, shape) | (rng.integers(0, 2, shape) << 7)
+        codes_v = rng.integers(0x08, 0x7F, shape) | (rng.integers(0, 2, shape) << 7)
+        ctx.k[l] = O.e4m3_decode(codes_k) * ks[l]
+        ctx.v[l] = O.e4m3_decode(codes_v) * vs[l]
+    ctx.k[1][0, 0, 0] = 1000.0 * ks[1]          # saturates at 448 * scale
+    ctx.v[0][1, 1, 1] = -900.0 * vs[0]
+    out = layers_fp8(ctx, ks, vs)
+    assert len(out) == 2
+    assert out[1][0][0, 0, 0] == 448.0 * ks[1] and out[0][1][1, 1, 1] == -448.0 * vs[0]
+    ctx.k[1][0, 0, 0] = 448.0 * ks[1]
+    ctx.v[0][1, 1, 1] = -448.0 * vs[0]
+    for l in range(2):
+        assert np.array_equal(out[l][0], ctx.k[l]) and np.array_equal(out[l][1], ctx.v[l]), l
+
+
+def test_layers_fp8_uses_each_layers_own_scales():
+    _check_layers_fp8(O.DraftContext.layers_fp8)
+
+
+def test_layers_fp8_pin_catches_planted_mistakes():
+    def swapped(self, ks, vs):
+        return [O.fp8_kv(k, v, b, a) for k, v, a, b in zip(self.k, self.v, ks, vs)]
+
+    def first_layer_scales(self, ks, vs):
+        return [O.fp8_kv(k, v, ks[0], vs[0]) for k, v in zip(self.k, self.v)]
+
+    def unscaled(self, ks, vs):
+        return [O.fp8_kv(k, v, 1.0, 1.0) for k, v in zip(self.k, self.v)]
+
+    for wrong in (swapped, first_layer_scales, unscaled):
+        with pytest.raises(AssertionError):
+            _check_layers_fp8(wrong)
 
 
 # ----------------------------------------------------------- draft KV windowing
