@@ -12,6 +12,12 @@ length, so every timed cycle drafts against exactly that context.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
                   [--verify greedy|sampled]
 
+The default workload is the largest one that fits one GPU, the stress sweep
+point stress-b128-s16 (Qwen3-8B-shaped bf16 draft, batch 128, block 16,
+lognormal contexts with median 2048 up to 32768, paged KV); the other named
+workloads (qwen8b-b1, qwen8b-b32, kimi-b8, stress-b{64,128}-s{8,16}) are
+selected with --workload.
+
 --verify sampled replaces the greedy acceptance with dflash_accept_commit_sampled
 (lossless rejection sampling): synthetic target rows (softmax of random
 logits, the proposed tokens given the workload's match probability, built
@@ -48,9 +54,9 @@ UNIT = "drafted tokens/s"
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="qwen8b-b1")
+    ap.add_argument("--workload", default="stress-b128-s16")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--draft", default="plain", choices=["plain", "selector"],
                     help="plain: argmax drafter; selector: DFlash 2 candidate selector "
@@ -425,21 +431,26 @@ class Bench:
         return ms, h2d, d2h
 
 
-def cpu_baseline(bench, cycles):
+def host_weights(W):
+    """float32 numpy copies of a weight dict (every bf16 value is exact in float32)."""
+    f = lambda t: t.float().cpu().numpy()  # noqa: E731
+    out = {k: f(v) for k, v in W.items() if k != "layers"}
+    out["layers"] = [{k: f(v) for k, v in L.items()} for L in W["layers"]]
+    return out
+
+
+def cpu_baseline(cfg, T, W, cycles):
     """The oracle, as it stands, timed on this host's cores for `cycles` cycles
-    of the same workload (request 0 only, scaled by batch)."""
-    import torch
+    of the same workload (one request at context T; W: host weights).  Its
+    inputs come from synth on the host: nothing here touches the GPU library."""
     from oracle import dflash_oracle as O
     from synth import make_posterior
-    cfg, T = bench.cfg, int(bench.T[0])
-    f = lambda t: t.float().cpu().numpy()  # noqa: E731
-    W = {k: f(v) for k, v in bench.W.items() if k != "layers"}
-    W["layers"] = [{k: f(v) for k, v in L.items()} for L in bench.W["layers"]]
-    feats = make_features(cfg, T, 99, "cpu-prefill", device="cuda")
+    T = int(T)
+    feats = make_features(cfg, T, 99, "cpu-prefill", device="cpu")
     ctx = O.DraftContext(cfg)
-    ctx.inject([feats[j].double().cpu().numpy() for j in range(cfg.n_sel)], W)
-    vfe = make_features(cfg, cfg.block_size, 99, "cpu-verify", device="cuda")
-    vf = [vfe[j].double().cpu().numpy() for j in range(cfg.n_sel)]
+    ctx.inject([feats[j].double().numpy() for j in range(cfg.n_sel)], W)
+    vfe = make_features(cfg, cfg.block_size, 99, "cpu-verify", device="cpu")
+    vf = [vfe[j].double().numpy() for j in range(cfg.n_sel)]
     anchor = 5
     t0 = time.perf_counter()
     for c in range(cycles):
@@ -458,7 +469,7 @@ def cpu_baseline(bench, cycles):
     value = cycles * (cfg.block_size - 1) / dt      # one request's drafted tokens per second
     return {"value": value, "unit": UNIT, "cores": blas or cores, "kind": "oracle",
             "sample": f"{cycles} full cycles (draft_block + accept + inject of the commit rows) "
-                      f"of request 0 at context {T}, float64 numpy, {cores} host cores"}, W
+                      f"of request 0 at context {T}, float64 numpy, {cores} host cores"}
 
 
 def dominant_roofline(bench, prof, mean_commit, wl_name):
@@ -533,7 +544,7 @@ def main():
     roof = dominant_roofline(bench, prof, mean_commit, a.workload)
     cpu = None
     if rank == 0 and world == 1 and not a.no_cpu_baseline:
-        cpu, _ = cpu_baseline(bench, a.cpu_cycles)
+        cpu = cpu_baseline(bench.cfg, bench.T[0], host_weights(bench.W), a.cpu_cycles)
     launches = int(round(sum(v[0] for v in prof.values()) * a.steps))
     if rank == 0:
         line = {
@@ -564,17 +575,17 @@ def reference_arm(a, wl, rank, world):
     """The oracle as it stands on the host cores: same workload, metric, unit."""
     if rank != 0:
         return
-    import torch
-    torch.cuda.set_device(0)
-    bench_like = Bench(wl)
+    # host-only inputs: the same workload drawn by synth on the CPU; no
+    # session, no device memory and no library call in this process
+    T = make_context_lengths(wl, 0)
+    W = host_weights(make_weights(wl.cfg, seed=0, device="cpu"))
     steps = max(1, a.steps)
     per = []
-    from oracle import dflash_oracle as O  # noqa: F401
     t_start = time.perf_counter()
-    cb, _ = cpu_baseline(bench_like, 1)       # warm-up / setup sample
+    cb = cpu_baseline(wl.cfg, T[0], W, 1)       # warm-up / setup sample
     done = 0
     for _ in range(steps):
-        r, _ = cpu_baseline(bench_like, 1)
+        r = cpu_baseline(wl.cfg, T[0], W, 1)
         per.append(r["value"])
         done += 1
         if time.perf_counter() - t_start > a.reference_budget_s:

@@ -155,7 +155,7 @@ cudaError_t run_gemm(dflash_handle *h, const GemmProblem &P, cudaStream_t s) {
 // after the other on the CUDA cores.
 cudaError_t run_program(dflash_handle *h, const GemmProblem *P, int n, cudaStream_t s,
                         const ProgramEmbed *embed = nullptr, const ProgramFinalize *fin = nullptr,
-                        const ProgramInject *inject = nullptr) {
+                        const ProgramInject *inject = nullptr, const ProgramNorm *norm = nullptr) {
   if (h->store == ST_F32) {
     for (int i = 0; i < n; ++i) {
       const cudaError_t e = launch_gemm_simt(ST_F32, P[i], s);
@@ -172,7 +172,7 @@ cudaError_t run_program(dflash_handle *h, const GemmProblem *P, int n, cudaStrea
   }
   return launch_gemm_program(P, n, at<float>(h, h->L.tc_partials), at<int>(h, h->L.tc_counters),
                              h->L.tc_max_tiles, at<unsigned int>(h, h->L.tc_grid_bar),
-                             at<unsigned int>(h, h->L.err), s, nullptr, embed, fin, inject);
+                             at<unsigned int>(h, h->L.err), s, nullptr, embed, fin, inject, norm);
 }
 
 cudaError_t run_attention(dflash_handle *h, const AttnParams &a, cudaStream_t s) {
@@ -719,9 +719,10 @@ static int draft_impl(dflash_handle *h, const dflash_kv *kv, int32_t batch,
       if ((st = timed(h, "gemm_layer_program", s, [&] { return run_program(h, prog, 4, s); })))
         return st;
     } else {
-      // a9: lm_head + argmax (logits never stored).  The argmax of a row is
-      // unchanged by the row's positive RMSNorm scale, so the lm_head runs on
-      // x * final gain directly.
+      // a9: final norm, lm_head + argmax (logits never stored).  The lm_head
+      // reads the final-normed rows rounded to the store type -- the same
+      // values hidden_out receives -- so the drafted ids are exactly the
+      // argmax of the hidden states the caller sees.
       prog[3] = problem_1src(xg, H, M, H);
       EpiParams ea = epi_base(h, run ? EPI_TOPK : EPI_ARGMAX);
       ea.N = c.vocab;
@@ -748,21 +749,38 @@ static int draft_impl(dflash_handle *h, const dflash_kv *kv, int32_t batch,
       fin.M = M;
       fin.S = S;
       fin.draft_ids = draft_ids;
-      if ((st = timed(h, "gemm_last_program", s,
-                      [&] {
-                        return run_program(h, prog, 4, s, nullptr,
-                                           fused && !run ? &fin : nullptr);
-                      })))
-        return st;
+      if (fused && H % 256 == 0) {
+        // O, gate/up, down, the final norm (a GEMM-free phase) and the lm_head
+        ProgramNorm nm;
+        nm.x = x;
+        nm.ssq = ssq;
+        nm.ssq_ld = ldq;
+        nm.gain = h->final_norm_g;
+        nm.out = xg;
+        nm.out2 = hidden_out;
+        nm.M = M;
+        nm.H = H;
+        nm.eps = c.rms_eps;
+        if ((st = timed(h, "gemm_last_program", s, [&] {
+               return run_program(h, prog, 4, s, nullptr, run ? nullptr : &fin, nullptr, &nm);
+             })))
+          return st;
+      } else {
+        if ((st = timed(h, "gemm_last_layer_program", s, [&] { return run_program(h, prog, 3, s); })))
+          return st;
+        if ((st = timed(h, "rmsnorm_final", s, [&] {
+               return launch_rmsnorm(1, h->store, x, h->final_norm_g, M, H, c.rms_eps, xg,
+                                     hidden_out, s);
+             })))
+          return st;
+        if ((st = timed(h, "gemm_lm_head", s, [&] {
+               return fused ? run_program(h, &prog[3], 1, s, nullptr, run ? nullptr : &fin)
+                            : run_gemm(h, prog[3], s);
+             })))
+          return st;
+      }
     }
   }
-  // the normalised hidden states are formed only when the caller asks for them
-  if (hidden_out &&
-      (st = timed(h, "rmsnorm_hidden_out", s, [&] {
-         return launch_rmsnorm(1, h->store, x, h->final_norm_g, M, H, c.rms_eps, hidden_out,
-                               nullptr, s);
-       })))
-    return st;
   if (run) {
     SelectorParams sp;
     std::memset(&sp, 0, sizeof(sp));
@@ -771,7 +789,7 @@ static int draft_impl(dflash_handle *h, const dflash_kv *kv, int32_t batch,
     sp.topk_ld = ldq;
     sp.cand_keys = (unsigned long long *)(h->sel.ws + h->sel.cand);
     sp.wh = (const float *)(h->sel.ws + h->sel.wh);
-    sp.ssq = ssq;
+    sp.ssq = nullptr;   // the lm_head operand is already the normalised hidden state
     sp.ssq_ld = ldq;
     sp.H = H;
     sp.eps = c.rms_eps;
@@ -791,7 +809,7 @@ static int draft_impl(dflash_handle *h, const dflash_kv *kv, int32_t batch,
     sp.err = err;
     return timed(h, "selector_walk", s, [&] { return launch_selector_walk(sp, s); });
   }
-  if (fused) return DFLASH_OK;   // the ids came with the last launch
+  if (fused && !run) return DFLASH_OK;   // the ids came with the last launch
   return timed(h, "argmax_finalize", s,
                [&] { return launch_argmax_finalize(keys, anchor, batch, S, draft_ids, s); });
 }

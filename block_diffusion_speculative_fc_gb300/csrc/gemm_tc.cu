@@ -78,12 +78,15 @@ struct Params {
   ProgramEmbed emb;               // phase 0 is the embedding when emb.M > 0
   ProgramFinalize fin;            // draft ids by the last CTA out when fin.M > 0
   ProgramInject inj;              // injection row map in phase 0 when inj.rows > 0
+  ProgramNorm nrm;                // GEMM-free phase nrm_phase normalises rows when nrm.M > 0
+  int nrm_phase;
   float *partials;                // [gridDim.x][2][<= 2*BN][128]
   int *counters;                  // tickets of every phase, zero between launches
   unsigned int *grid_bar;         // [2] phase arrivals, exits; zero between launches
   unsigned int *err;
   unsigned long long *trace;      // optional [gridDim.x][kTraceSlots] timestamps (ns), test entries only
 };
+static_assert(sizeof(Params) <= 32000, "kernel parameter block limit");
 
 // ------------------------------------------------------------------ PTX
 __device__ __forceinline__ uint32_t su32(const void *p) {
@@ -412,6 +415,9 @@ __device__ __forceinline__ bool produce_phase(const Params &p, const Phase &ph,
                                               uint32_t &it, uint8_t *slots, uint64_t *full,
                                               uint64_t *empty, int *pend_s, int *pend_k,
                                               int *pend_m, uint64_t pol_w, uint64_t pol_a) {
+  // a GEMM-free phase (embedding, normalisation) loads nothing: its inputs
+  // are never needed here, and the next phase's weights may stream at once
+  if (ps.total == 0) return true;
   const Range R = cta_range(ps.total, ps.G, cta);
   const uint32_t it0 = it;
   bool ready = false;
@@ -527,6 +533,35 @@ __device__ __forceinline__ void program_embed(const ProgramEmbed &e, unsigned in
     *reinterpret_cast<__nv_bfloat162 *>(xgr + 2) = __floats2bfloat162_rn(v[2] * g[2], v[3] * g[3]);
     const float ss = warp_sum((v[0] * v[0] + v[1] * v[1]) + (v[2] * v[2] + v[3] * v[3]));
     if (lane == 0) e.ssq[(int64_t)t * e.ssq_ld + m] = ss;
+  }
+}
+
+// The final RMSNorm as a GEMM-free phase of the program ("Inside SGLang",
+// Step 4: the lm_head reads the draft's final-normed hidden state): the
+// rows are rounded to bf16 after the row scale, so the lm_head's operand is
+// exactly the normalised hidden state the caller may receive.  Work item =
+// (row, 256-feature chunk), one per epilogue warp; each lane 8 features.
+__device__ __forceinline__ void program_norm(const ProgramNorm &q, int gwarp, int nwarps, int lane) {
+  const int chunks = q.H >> 8, parts = q.H >> 7;
+  for (int item = gwarp; item < q.M * chunks; item += nwarps) {
+    const int m = item / chunks, c0 = (item - m * chunks) * 256 + lane * 8;
+    float ss = 0.f;
+    for (int t = lane; t < parts; t += 32) ss += __ldcg(q.ssq + (int64_t)t * q.ssq_ld + m);
+    const float r = rsqrtf(warp_sum(ss) / (float)q.H + q.eps);
+    const float4 *xr = reinterpret_cast<const float4 *>(q.x + (int64_t)m * q.H + c0);
+    const float4 a = __ldcg(xr), b = __ldcg(xr + 1);
+    const uint4 gw = *reinterpret_cast<const uint4 *>((const bf16 *)q.gain + c0);
+    const __nv_bfloat162 *g2 = reinterpret_cast<const __nv_bfloat162 *>(&gw);
+    const float2 g0 = __bfloat1622float2(g2[0]), g1 = __bfloat1622float2(g2[1]);
+    const float2 g2f = __bfloat1622float2(g2[2]), g3 = __bfloat1622float2(g2[3]);
+    uint4 o;
+    __nv_bfloat162 *o2 = reinterpret_cast<__nv_bfloat162 *>(&o);
+    o2[0] = __floats2bfloat162_rn(a.x * r * g0.x, a.y * r * g0.y);
+    o2[1] = __floats2bfloat162_rn(a.z * r * g1.x, a.w * r * g1.y);
+    o2[2] = __floats2bfloat162_rn(b.x * r * g2f.x, b.y * r * g2f.y);
+    o2[3] = __floats2bfloat162_rn(b.z * r * g3.x, b.w * r * g3.y);
+    *reinterpret_cast<uint4 *>((bf16 *)q.out + (int64_t)m * q.H + c0) = o;
+    if (q.out2) *reinterpret_cast<uint4 *>((bf16 *)q.out2 + (int64_t)m * q.H + c0) = o;
   }
 }
 
@@ -672,6 +707,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
       }
       if (ph_i == 0 && p.emb.M > 0)
         program_embed(p.emb, p.err, cta * 4 + ew, G * 4, lane);
+      if (ph_i == p.nrm_phase && p.nrm.M > 0) program_norm(p.nrm, cta * 4 + ew, G * 4, lane);
       if (ph_i == 0 && p.inj.rows > 0) {
         // the K/V phase's row map (read only after the grid barrier)
         InjectArgs a = inject_args(p.inj);
@@ -1013,10 +1049,14 @@ cudaError_t launch_gemm_program(const GemmProblem *probs, int n, float *partials
                                 int max_tiles, unsigned int *grid_bar, unsigned int *err,
                                 cudaStream_t s, unsigned long long *trace,
                                 const ProgramEmbed *embed, const ProgramFinalize *fin,
-                                const ProgramInject *inject) {
+                                const ProgramInject *inject, const ProgramNorm *norm) {
   const int lead = embed ? 1 : 0;   // the embedding phase comes first
-  if (n <= 0 || n + lead > kMaxPhases) return cudaErrorInvalidValue;
-  if ((n + lead > 1 || fin || inject) && !grid_bar) return cudaErrorInvalidValue;
+  const int extra = norm ? 1 : 0;   // the normalisation phase comes before the last GEMM
+  if (n <= 0 || n > kMaxGemmPhases || n + lead + extra > kMaxPhases) return cudaErrorInvalidValue;
+  if ((n + lead + extra > 1 || fin || inject) && !grid_bar) return cudaErrorInvalidValue;
+  if (norm && (norm->M != probs[0].M || norm->H % 256 || norm->H <= 0 || !norm->x || !norm->ssq ||
+               !norm->gain || !norm->out))
+    return cudaErrorInvalidValue;
   if (inject && n + lead < 2) return cudaErrorInvalidValue;   // the map is read by a later phase
   if (embed && (embed->M != probs[0].M || embed->H % 128 || embed->M <= 0))
     return cudaErrorInvalidValue;
@@ -1039,15 +1079,27 @@ cudaError_t launch_gemm_program(const GemmProblem *probs, int n, float *partials
     p.ph[0].m_tiles = 1;
     p.emb = *embed;
   }
+  p.nrm_phase = -1;
   for (int i = 0; i < n; ++i) {
-    if (!build_phase(p.ph[lead + i], probs[i], BN, off)) return cudaErrorInvalidValue;
-    off += p.ph[lead + i].tiles;
-    most = std::max(most, p.ph[lead + i].total_iters);
+    int k = lead + i;
+    if (norm && i == n - 1) {
+      // GEMM-free: no tiles, the epilogue warps normalise the rows
+      p.ph[k].nseg = 0;
+      p.ph[k].M = M;
+      p.ph[k].KB = 1;
+      p.ph[k].m_tiles = 1;
+      p.nrm = *norm;
+      p.nrm_phase = k;
+      ++k;
+    }
+    if (!build_phase(p.ph[k], probs[i], BN, off)) return cudaErrorInvalidValue;
+    off += p.ph[k].tiles;
+    most = std::max(most, p.ph[k].total_iters);
   }
   if (off > max_tiles) return cudaErrorInvalidValue;
   if (fin) p.fin = *fin;
   if (inject) p.inj = *inject;
-  n += lead;
+  n += lead + extra;
   p.nph = n;
   p.partials = partials;
   p.counters = counters;

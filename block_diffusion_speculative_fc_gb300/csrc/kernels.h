@@ -122,6 +122,7 @@ struct SelectorParams {
   int n_vt, topk_ld;                    // 128-row vocabulary tiles; row stride
   const float *wh;                      // [B*S, rank] W_h (x * g), before the row's rstd
   const float *ssq;                     // [H / 128][ssq_ld] sums of squares of the final norm
+                                        // (NULL: the lm_head operand was already normalised)
   int ssq_ld, H;
   float eps;
   const void *A, *Bf;                   // [V, rank] predecessor / successor factors (model dtype)
@@ -139,7 +140,8 @@ cudaError_t launch_selector_walk(const SelectorParams &p, cudaStream_t s);
 cudaError_t prepare_selector();
 
 constexpr int kTcMaxCtas = 160;   // persistent tensor-core GEMM grid cap (>= SM count)
-constexpr int kMaxPhases = 4;     // dependent GEMMs fused into one tensor-core launch
+constexpr int kMaxPhases = 5;     // phases of one fused tensor-core launch (GEMMs and GEMM-free ones)
+constexpr int kMaxGemmPhases = 4; // dependent GEMMs a caller may chain in one launch
 
 // ---- launchers (return cudaGetLastError()) ----
 cudaError_t launch_gemm_tc(const GemmProblem &P, float *partials, int *counters, int max_tiles,
@@ -183,16 +185,33 @@ struct ProgramInject {
   int advance, total_rows;
 };
 
-// Up to kMaxPhases dependent GEMMs of equal row count in one cooperative
+// ProgramNorm: a GEMM-free phase placed just before a program's last GEMM.
+// Every row m of the fp32 residual x is normalised with the sums of squares
+// the previous phase wrote (ssq[t * ssq_ld + m], one per 128-feature part):
+// out[m, :] = x[m, :] * rsqrt(sum_t ssq / H + eps) * gain, rounded to the
+// store type, into out (the last GEMM's operand) and, when non-NULL, out2.
+struct ProgramNorm {
+  const float *x;               // [M, H]
+  const float *ssq;             // [H/128][ssq_ld]
+  int ssq_ld;
+  const void *gain;             // [H]
+  void *out, *out2;             // [M, H] bf16
+  int M, H;
+  float eps;
+};
+
+// Up to kMaxGemmPhases dependent GEMMs of equal row count in one cooperative
 // launch, separated by grid barriers (grid_bar: two zeroed words); an
-// optional embedding phase first (it takes one of the kMaxPhases) and an
-// optional argmax finalisation at the end.
+// optional embedding phase first, an optional normalisation phase before the
+// last GEMM (each takes one of the kMaxPhases) and an optional argmax
+// finalisation at the end.
 cudaError_t launch_gemm_program(const GemmProblem *probs, int n, float *partials, int *counters,
                                 int max_tiles, unsigned int *grid_bar, unsigned int *err,
                                 cudaStream_t s, unsigned long long *trace = nullptr,
                                 const ProgramEmbed *embed = nullptr,
                                 const ProgramFinalize *fin = nullptr,
-                                const ProgramInject *inject = nullptr);
+                                const ProgramInject *inject = nullptr,
+                                const ProgramNorm *norm = nullptr);
 size_t gemm_tc_partials_bytes();
 int gemm_tc_trace_slots();   // timestamps per CTA written by a traced launch
 int gemm_tc_tiles(int n_tiles, int M, bool pair);

@@ -44,12 +44,17 @@ constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
 unsigned char *g_scratch_ptr[kMaxDevices] = {};
 
-// keys -> token ids
+// keys -> token ids.  A call whose bounded waits gave up (its status word is
+// non-zero) reports -1 ids rather than ids built from unmerged partial tiles,
+// and copies the word to the caller's status.
 __global__ void keys_to_ids_kernel(const unsigned long long *__restrict__ keys, int rows,
-                                   int *__restrict__ ids) {
+                                   const unsigned int *__restrict__ err, int *__restrict__ ids,
+                                   unsigned int *__restrict__ status) {
   pdl_wait();
+  const unsigned int word = __ldcg(err);
   const int r = blockIdx.x * blockDim.x + threadIdx.x;
-  if (r < rows) ids[r] = argmax_key_index(keys[r]);
+  if (r < rows) ids[r] = word ? -1 : argmax_key_index(keys[r]);
+  if (status && r == 0) *status = word;
 }
 
 int noalloc_fail(int st, const char *msg) {
@@ -58,8 +63,8 @@ int noalloc_fail(int st, const char *msg) {
 }
 
 // Once per device, with that device current: the device address of the
-// scratch, the tensor-core kernels' shared-memory limits, zeroed tickets.
-int setup_device(cudaStream_t s, unsigned char **out) {
+// scratch and the tensor-core kernels' shared-memory limits.
+int setup_device(unsigned char **out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return noalloc_fail(DFLASH_ECUDA, "cudaGetDevice failed");
   if (dev < 0 || dev >= kMaxDevices) return noalloc_fail(DFLASH_EUNSUPPORTED, "device index too large");
@@ -70,8 +75,6 @@ int setup_device(cudaStream_t s, unsigned char **out) {
       return noalloc_fail(DFLASH_ECUDA, "cudaGetSymbolAddress of the no-alloc scratch failed");
     if (prepare_gemm_tc() != cudaSuccess)
       return noalloc_fail(DFLASH_ECUDA, "setting tensor-core GEMM attributes failed");
-    if (cudaMemsetAsync(ptr, 0, kPartialsOff, s) != cudaSuccess)
-      return noalloc_fail(DFLASH_ECUDA, "clearing the no-alloc scratch failed");
     g_scratch_ptr[dev] = (unsigned char *)ptr;
   }
   *out = g_scratch_ptr[dev];
@@ -81,7 +84,8 @@ int setup_device(cudaStream_t s, unsigned char **out) {
 }  // namespace
 
 extern "C" int dflash_select_tokens_noalloc(dflash_handle *h, int32_t rows, const void *hidden,
-                                            int32_t *ids, dflash_stream_t stream) {
+                                            int32_t *ids, uint32_t *status,
+                                            dflash_stream_t stream) {
   if (!h || !hidden || !ids) return noalloc_fail(DFLASH_EINVAL, "handle, hidden and ids must be non-NULL");
   const void *lm_head = nullptr;
   int H = 0, V = 0, dtype = 0;
@@ -91,14 +95,23 @@ extern "C" int dflash_select_tokens_noalloc(dflash_handle *h, int32_t rows, cons
   if (rows < 0) return noalloc_fail(DFLASH_EINVAL, "negative rows");
   if (rows == 0) return DFLASH_OK;
   if (rows > kNoAllocMaxRows) return noalloc_fail(DFLASH_ECAPACITY, "rows > 32");
-  if ((V + 127) / 128 > kNoAllocMaxTiles) return noalloc_fail(DFLASH_ECAPACITY, "vocab > 262144");
+  const int tiles = (V + 127) / 128;
+  if (tiles > kNoAllocMaxTiles) return noalloc_fail(DFLASH_ECAPACITY, "vocab > 262144");
+  // the GEMM reads hidden through a tensor map (16-byte aligned rows) in
+  // k-blocks of 64 features
+  if ((uintptr_t)hidden % 16 != 0) return noalloc_fail(DFLASH_EINVAL, "hidden must be 16-byte aligned");
+  if (H % 64 != 0) return noalloc_fail(DFLASH_EUNSUPPORTED, "hidden size must be a multiple of 64");
   cudaStream_t s = (cudaStream_t)stream;
   unsigned char *scratch = nullptr;
-  if (int st = setup_device(s, &scratch)) return st;
+  if (int st = setup_device(&scratch)) return st;
   unsigned long long *keys = (unsigned long long *)(scratch + kKeysOff);
-  // the keys of the previous call are still there: start from zero
-  if (cudaMemsetAsync(keys, 0, 8 * (size_t)rows, s) != cudaSuccess)
-    return noalloc_fail(DFLASH_ECUDA, "clearing the argmax keys failed");
+  unsigned int *err = (unsigned int *)(scratch + kErrOff);
+  // The array keeps the previous call's contents: the status word, the argmax
+  // keys and the per-tile tickets (a call whose waits gave up can leave a
+  // ticket non-zero) all start from zero.  They are contiguous.
+  static_assert(kErrOff == 0 && kKeysOff < kTicketsOff, "cleared region layout");
+  if (cudaMemsetAsync(scratch, 0, kTicketsOff + 4 * (size_t)tiles, s) != cudaSuccess)
+    return noalloc_fail(DFLASH_ECUDA, "clearing the no-alloc scratch failed");
   GemmProblem P;
   std::memset(&P, 0, sizeof(P));
   P.A.ptr[0] = hidden;
@@ -116,10 +129,11 @@ extern "C" int dflash_select_tokens_noalloc(dflash_handle *h, int32_t rows, cons
   g.epi.N = V;
   g.epi.argmax_keys = keys;
   if (launch_gemm_tc(P, (float *)(scratch + kPartialsOff), (int *)(scratch + kTicketsOff),
-                     kNoAllocMaxTiles, (unsigned int *)(scratch + kErrOff), s) != cudaSuccess)
+                     kNoAllocMaxTiles, err, s) != cudaSuccess)
     return noalloc_fail(DFLASH_ECUDA, "lm_head GEMM launch failed");
   if (launch_pdl(keys_to_ids_kernel, dim3((rows + 127) / 128), dim3(128), 0, s,
-                 (const unsigned long long *)keys, (int)rows, (int *)ids) != cudaSuccess)
+                 (const unsigned long long *)keys, (int)rows, (const unsigned int *)err, (int *)ids,
+                 (unsigned int *)status) != cudaSuccess)
     return noalloc_fail(DFLASH_ECUDA, "argmax id kernel launch failed");
   return DFLASH_OK;
 }

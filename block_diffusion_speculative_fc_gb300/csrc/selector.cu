@@ -155,14 +155,19 @@ __global__ void __launch_bounds__(kSelThreads) selector_walk_kernel(const __grid
     s_key[i] = __ldcg(p.cand_keys + (size_t)(b * S + 1) * K + i);
   for (int j = tid; j < n; j += blockDim.x) s_rstd[j] = 0.f;
   __syncthreads();
-  // row scales of the final RMSNorm: every (row, 128-feature part) sum at once
-  const int parts = p.H / 128;
-  for (int idx = tid; idx < n * parts; idx += blockDim.x) {
-    const int j = idx / parts, part = idx - j * parts;
-    atomicAdd(&s_rstd[j], p.ssq[(size_t)part * p.ssq_ld + b * S + 1 + j]);
+  // row scales of the final RMSNorm when the lm_head read unnormalised rows
+  // (every (row, 128-feature part) sum at once); 1 when its operand is
+  // already the normalised hidden state (ssq NULL)
+  if (p.ssq) {
+    const int parts = p.H / 128;
+    for (int idx = tid; idx < n * parts; idx += blockDim.x) {
+      const int j = idx / parts, part = idx - j * parts;
+      atomicAdd(&s_rstd[j], p.ssq[(size_t)part * p.ssq_ld + b * S + 1 + j]);
+    }
+    __syncthreads();
   }
-  __syncthreads();
-  for (int j = tid; j < n; j += blockDim.x) s_rstd[j] = rsqrtf(s_rstd[j] / (float)p.H + p.eps);
+  for (int j = tid; j < n; j += blockDim.x)
+    s_rstd[j] = p.ssq ? rsqrtf(s_rstd[j] / (float)p.H + p.eps) : 1.f;
   __syncthreads();
   const T *A = (const T *)p.A, *Bf = (const T *)p.Bf;
   int anchor = p.anchor[b];

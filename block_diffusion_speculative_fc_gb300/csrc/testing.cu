@@ -79,7 +79,7 @@ int program_tiles(int n, int32_t M, const int32_t *N, const int32_t *op) {
 
 extern "C" size_t dflash_test_program_scratch(int32_t n_phases, int32_t M, const int32_t *N,
                                               const int32_t *op) {
-  if (n_phases <= 0 || n_phases > kMaxPhases || M <= 0 || !N || !op) return 0;
+  if (n_phases <= 0 || n_phases > kMaxGemmPhases || M <= 0 || !N || !op) return 0;
   return 256 + gemm_tc_partials_bytes() + 4 * (size_t)program_tiles(n_phases, M, N, op) + 256;
 }
 
@@ -100,7 +100,7 @@ extern "C" int dflash_test_gemm_program_traced(int32_t n_phases, int32_t M, cons
                                                void *const *out, void *scratch,
                                                size_t scratch_bytes, unsigned long long *trace,
                                                dflash_stream_t stream) {
-  if (n_phases <= 0 || n_phases > kMaxPhases || M <= 0 || !N || !K || !A || !W || !op || !out ||
+  if (n_phases <= 0 || n_phases > kMaxGemmPhases || M <= 0 || !N || !K || !A || !W || !op || !out ||
       !scratch)
     return DFLASH_EINVAL;
   for (int i = 0; i < n_phases; ++i) {
@@ -111,7 +111,7 @@ extern "C" int dflash_test_gemm_program_traced(int32_t n_phases, int32_t M, cons
   }
   if (scratch_bytes < dflash_test_program_scratch(n_phases, M, N, op)) return DFLASH_ECAPACITY;
   cudaStream_t s = (cudaStream_t)stream;
-  GemmProblem P[kMaxPhases];
+  GemmProblem P[kMaxGemmPhases];
   for (int i = 0; i < n_phases; ++i) {
     std::memset(&P[i], 0, sizeof(P[i]));
     P[i].A.ptr[0] = A[i];

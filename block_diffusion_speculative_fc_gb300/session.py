@@ -41,15 +41,6 @@ class KVCache:
                                self.page_table.data_ptr(), pages_per_req, self.n_pages,
                                self.kv_len.data_ptr())
 
-    def gather(self, layer, b, n=None):
-        """Host copy of the first n committed rows of request b: (K, V) [n, KVH, D]."""
-        n = int(self.kv_len[b].item()) if n is None else n
-        pos = torch.arange(n, device=self.page_table.device)
-        rows = self.page_table[b, pos // 64].long() * 64 + pos % 64
-        kf = self.k[layer].reshape(-1, *self.k[layer].shape[2:])[rows]
-        vf = self.v[layer].reshape(-1, *self.v[layer].shape[2:])[rows]
-        return kf.float().cpu(), vf.float().cpu()
-
 
 class DraftSession:
     """One draft model bound to libdflash.

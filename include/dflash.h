@@ -374,22 +374,30 @@ int dflash_profile_collect(dflash_handle *h, dflash_profile_entry *out, int32_t 
  * memory, or code that may not call cudaMalloc at all).
  *   ids[r] = argmax_v <hidden[r], lm_head[v]>   (lowest id among equal maxima)
  *   rows    1 .. 32
- *   hidden  device [rows, hidden] in the configured dtype (bf16 only), e.g.
- *           rows 1..S-1 of dflash_draft_block's hidden_out
- *   ids     device int32 [rows]
+ *   hidden  device [rows, hidden] in the configured dtype (bf16 only), rows
+ *           contiguous, 16-byte aligned (e.g. rows 1..S-1 of
+ *           dflash_draft_block's hidden_out); the hidden size must be a
+ *           multiple of 64
+ *   ids     device int32 [rows]; all -1 when the call's status is non-zero
+ *   status  optional device uint32 (NULL: not reported): written when the
+ *           call's last kernel runs with the call's device error bits, 0 on
+ *           success, DFLASH_DERR_TIMEOUT if a bounded wait inside the GEMM
+ *           gave up.  Read it after synchronising the stream.
  * Needs a handle (host memory) but no bound workspace.  Its scratch (argmax
- * keys, GEMM partial tiles and tickets, about 5.3 MB) is one static device
- * array of the library, held by every GPU that loads it until the process
- * exits.  The first call on a device sets that device up (looks up the
- * array's address, sets kernel attributes, zeroes the tickets on `stream`):
- * make that first call before any stream capture.  All calls share the one
- * array, so calls that may overlap on the GPU (other streams, other threads)
- * race; serialise them.  No cudaMalloc/cudaFree is made.
- * Returns DFLASH_ECAPACITY for rows > 32 or vocab > 262144,
- * DFLASH_EUNSUPPORTED for fp32 handles.
+ * keys, GEMM partial tiles and tickets, a status word; about 5.3 MB) is one
+ * static device array of the library, held by every GPU that loads it until
+ * the process exits.  The first call on a device sets that device up (looks
+ * up the array's address and sets kernel attributes): make that first call
+ * before any stream capture.  Every call clears the status word, the keys and
+ * the tickets on `stream` before its GEMM.  All calls share the one array, so
+ * calls that may overlap on the GPU (other streams, other threads) race;
+ * serialise them.  No cudaMalloc/cudaFree is made.
+ * Returns DFLASH_ECAPACITY for rows > 32 or vocab > 262144, DFLASH_EINVAL
+ * for a misaligned hidden, DFLASH_EUNSUPPORTED for fp32 handles or a hidden
+ * size that is not a multiple of 64.
  */
 int dflash_select_tokens_noalloc(dflash_handle *h, int32_t rows, const void *hidden, int32_t *ids,
-                                 dflash_stream_t stream);
+                                 uint32_t *status, dflash_stream_t stream);
 
 /* Static description of a status code. */
 const char *dflash_status_string(int status);

@@ -35,7 +35,7 @@ def _run(name, cycles, pool=64, max_rows=65536):
                    check=_checked(T), match=wl.match, max_rows=max_rows, pool=pool)
     st = run.run()
     print(name, "hidden_rel", max(st["hidden_rel"]), "kv_rel", max(st["kv_rel"]),
-          "ids", st["ids"], "near-tie", st["id_mismatch_near_tie"],
+          "ids", st["ids"], "near-tie", st["id_near_tie"], "e2e flips", len(st["e2e_flips"]),
           "mean accept", float(np.mean(st["accept"])))
     return st
 
@@ -54,3 +54,15 @@ def test_kimi_b8_full():
 
 def test_stress_b128_s16_full():
     _run("stress-b128-s16", cycles=1)
+
+
+def test_stress_b128_s8_full():
+    _run("stress-b128-s8", cycles=1)
+
+
+def test_stress_b64_s8_full():
+    _run("stress-b64-s8", cycles=1)
+
+
+def test_stress_b64_s16_full():
+    _run("stress-b64-s16", cycles=1)

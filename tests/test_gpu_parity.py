@@ -30,8 +30,9 @@ KIMI_MINI = shrink(KIMI, name="kimi-mini", target_hidden=256, target_layer_ids=(
 
 
 def _report(stats):
-    print({k: (max(v) if isinstance(v, list) and v and k not in ("accept", "mismatch") else v)
-           for k, v in stats.items() if k != "accept"},
+    print({k: (max(v) if isinstance(v, list) and v else v)
+           for k, v in stats.items() if k not in ("accept", "e2e_flips")},
+          "e2e flips", len(stats["e2e_flips"]),
           "mean accept", float(np.mean(stats["accept"])) if stats["accept"] else None)
 
 
