@@ -464,18 +464,19 @@ def e4m3_decode(code):
 
 
 def e4m3_encode(x):
-    """Nearest E4M3 code of each element (see the readings above), by
-    comparing against every finite positive code."""
+    """Nearest E4M3 code of each element (see the readings above): the two
+    finite codes whose values bracket |x| (found by bisection over the
+    ascending values of codes 0x00..0x7E), the nearer of the two, the one with
+    the even mantissa when both are equally near."""
     x = np.asarray(x, dtype=F64)
-    pos_codes = np.arange(0x7F)                       # 0x00 .. 0x7E, ascending values
-    vals = e4m3_decode(pos_codes)
-    a = np.minimum(np.abs(x), 448.0).reshape(-1, 1)
-    dist = np.abs(a - vals[None, :])
-    best = dist.min(axis=1, keepdims=True)
-    tie = dist == best
-    # among the (at most two) nearest codes prefer the even mantissa
-    pick = np.where(tie & (pos_codes[None, :] % 2 == 0), pos_codes[None, :], 10 ** 6).min(axis=1)
-    pick = np.where(pick == 10 ** 6, np.argmax(tie, axis=1), pick)
+    vals = e4m3_decode(np.arange(0x7F))               # 0x00 .. 0x7E, ascending values
+    a = np.minimum(np.abs(x), 448.0).reshape(-1)
+    hi = np.clip(np.searchsorted(vals, a, side="left"), 0, 0x7E)
+    lo = np.clip(hi - 1, 0, 0x7E)
+    d_lo, d_hi = a - vals[lo], vals[hi] - a
+    even = np.where(lo % 2 == 0, lo, hi)              # the mantissa's last bit is the code's
+    pick = np.where(d_lo < d_hi, lo, np.where(d_hi < d_lo, hi, even))
+    pick = np.where(np.isnan(a), 0, pick)
     code = pick | np.where(np.signbit(x.reshape(-1)), 0x80, 0)
     code = np.where(np.isnan(x.reshape(-1)), 0x7F, code)
     return code.reshape(x.shape).astype(np.int64)
