@@ -64,6 +64,14 @@ def parse():
     ap.add_argument("--verify", default="greedy", choices=["greedy", "sampled"],
                     help="greedy: dflash_accept_commit; sampled: dflash_accept_commit_sampled "
                          "(lossless rejection sampling against synthetic target rows)")
+    ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"],
+                    help="draft KV cache: bf16, or one-byte FP8 E4M3 codes with per-layer scales")
+    ap.add_argument("--draft-window", type=int, default=0,
+                    help="draft KV windowing: keep the newest W committed rows per request "
+                         "(a ring of ceil(W/64)+1 pages); 0 = off")
+    ap.add_argument("--profile-case", action="store_true",
+                    help="counter captures only: two layers and a 32,768-token vocabulary "
+                         "(same per-layer kernels and batch shape); not a benchmark value")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-cycles", type=int, default=2)
@@ -81,34 +89,59 @@ def peaks():
 
 
 # ------------------------------------------------------------- roofline model
-def algorithmic(cfg, B, ctx_mean, commit_mean):
-    """Per-launch algorithmic bytes and flops of each kernel family."""
+def visible_keys(cfg, ctx, draft_window=0):
+    """Context keys one attention launch reads, summed over the requests and
+    averaged over the layers: min(T_b, the layer's sliding window, the draft
+    window) -- the pages the kernel stages (a window's first page may be
+    partial; that slack is not counted)."""
+    T = np.atleast_1d(np.asarray(ctx, dtype=np.float64))
+    per_layer = []
+    for w in cfg.sliding_window:
+        v = T.copy()
+        if w:
+            v = np.minimum(v, w)
+        if draft_window:
+            v = np.minimum(v, draft_window)
+        per_layer.append(v.sum())
+    return float(np.mean(per_layer))
+
+
+def algorithmic(cfg, B, ctx, commit_mean, kv_fp8=False, draft_window=0):
+    """Per-launch algorithmic bytes and flops of each kernel family; ctx is
+    the mean context length or the per-request lengths."""
     S, H, D = cfg.block_size, cfg.hidden, cfg.head_dim
     M = B * S
     es = 2 if cfg.dtype == "bf16" else 4
+    kvb = 1 if kv_fp8 else es             # bytes per cached K/V element
     qkv = cfg.qkv_rows
     qd, kvd, I, V = cfg.n_heads * D, cfg.n_kv_heads * D, cfg.intermediate, cfg.vocab
     K_fc = cfg.n_sel * cfg.target_hidden
     rows = B * S  # dense verify block; commit rows are written
-    keys = B * (ctx_mean + S)
+    if np.ndim(ctx) == 0:
+        ctx = np.full(B, float(ctx))
+    ctx_keys = visible_keys(cfg, ctx, draft_window)          # summed over the batch
     fam = {
         "gemm_qkv": (es * (qkv * H + M * H + M * qkv), 2 * M * qkv * H),
         "gemm_o": (es * (H * qd + M * qd) + 8 * M * H, 2 * M * H * qd),
         "gemm_gate_up": (es * (2 * I * H + M * H + M * I), 2 * M * 2 * I * H),
         "gemm_down": (es * (H * I + M * I) + 8 * M * H, 2 * M * H * I),
         "gemm_lm_head_argmax": (es * (V * H + M * H) + 8 * M, 2 * M * V * H),
-        "attention": (es * (2 * keys * kvd + 2 * M * qd), 4 * M * qd * (ctx_mean + S)),
+        "attention": (kvb * 2 * ctx_keys * kvd + es * (2 * B * S * kvd + 2 * M * qd),
+                      4 * S * qd * (ctx_keys + B * S)),
         "gemm_fc": (es * (H * K_fc + rows * K_fc) + 4 * rows * H, 2 * rows * H * K_fc),
-        "gemm_kv_inject": (es * (cfg.n_layers * 2 * kvd * H + rows * H
-                                 + B * commit_mean * cfg.n_layers * 2 * kvd),
+        "gemm_kv_inject": (es * (cfg.n_layers * 2 * kvd * H + rows * H)
+                           + kvb * B * commit_mean * cfg.n_layers * 2 * kvd,
                            2 * rows * cfg.n_layers * 2 * kvd * H),
+        # the final RMSNorm phase: x (fp32) read, the normalised rows written
+        "final_norm": ((4 + es) * M * H + 4 * M * (H // 128), 0),
         "accept": (4 * (2 * B * S + B * (S + 4)), 0),
         # target row at the stop position and the race noise, read once each
         "accept_sampled": (4 * (2 * B * V + 2 * B * S + B * (S + 4)), 0),
     }
     add = lambda *names: tuple(sum(fam[n][i] for n in names) for i in range(2))  # noqa: E731
     fam["gemm_layer_program"] = add("gemm_o", "gemm_gate_up", "gemm_down", "gemm_qkv")
-    fam["gemm_last_program"] = add("gemm_o", "gemm_gate_up", "gemm_down", "gemm_lm_head_argmax")
+    fam["gemm_last_program"] = add("gemm_o", "gemm_gate_up", "gemm_down", "final_norm",
+                                   "gemm_lm_head_argmax")
     fam["gemm_inject_program"] = add("gemm_fc", "gemm_kv_inject")
     # block embedding (table rows read; x fp32, x*g bf16 and row sums of squares written)
     fam["embed"] = (es * M * H + (4 + es) * M * H + 4 * M * (H // 128), 0)
@@ -189,7 +222,7 @@ class ClockSampler:
 
 # ------------------------------------------------------------- our arm
 class Bench:
-    def __init__(self, wl, seed=0, verify="greedy", draft="plain"):
+    def __init__(self, wl, seed=0, verify="greedy", draft="plain", kv="bf16", draft_window=0):
         import torch
         import block_diffusion_speculative_fc_gb300 as pkg
         self.torch, self.pkg = torch, pkg
@@ -199,12 +232,20 @@ class Bench:
         self.B, self.S = B, S
         self.T = make_context_lengths(wl, seed)
         self.W = make_weights(cfg, seed=seed, device="cuda")
-        self.ppr = (int(self.T.max()) + 2 * S + 63) // 64 + 1
+        self.kv_fp8 = kv == "fp8"
+        self.draft_window = int(draft_window)
+        full_ppr = (int(self.T.max()) + 2 * S + 63) // 64 + 1
+        # a draft window keeps a ring of ceil(W / 64) + 1 pages per request
+        self.ppr = (self.draft_window + 63) // 64 + 1 if self.draft_window else full_ppr
         self.page_table = make_page_table(B, self.ppr, wl.permuted_pages, seed)
         self.sess = pkg.DraftSession(cfg, self.W, max_batch=B,
                                      max_rows=max(B * S, min(int(self.T.sum()), 65536)),
-                                     max_position=self.ppr * 64 + S)
-        self.kv = self.sess.new_kv(B, self.ppr, self.page_table)
+                                     max_position=full_ppr * 64 + S, kv_fp8=self.kv_fp8)
+        # FP8 scales: the magnitude k-normed K and hidden_norm(y) W_v^T reach, over 448
+        ks = [4.5 / 448.0] * cfg.n_layers if self.kv_fp8 else None
+        vs = [4.0 * 0.02 * cfg.hidden ** 0.5 / 448.0] * cfg.n_layers if self.kv_fp8 else None
+        self.kv = self.sess.new_kv(B, self.ppr, self.page_table, ks, vs,
+                                   draft_window=self.draft_window)
         i32 = lambda a: torch.as_tensor(np.asarray(a), dtype=torch.int32, device="cuda")  # noqa
         self.i32 = i32
         offs = np.concatenate([[0], np.cumsum(self.T)[:-1]])
@@ -474,7 +515,8 @@ def cpu_baseline(cfg, T, W, cycles):
 
 def dominant_roofline(bench, prof, mean_commit, wl_name):
     hbm, tf, tf_sus, src = peaks()
-    fam = algorithmic(bench.cfg, bench.B, float(np.mean(bench.T)), mean_commit)
+    fam = algorithmic(bench.cfg, bench.B, bench.T, mean_commit, getattr(bench, "kv_fp8", False),
+                      getattr(bench, "draft_window", 0))
     total = sum(v[1] for v in prof.values())
     name = max(prof, key=lambda n: prof[n][1])
     launches, ms = prof[name]          # per cycle
@@ -517,6 +559,15 @@ def main():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     wl = WORKLOADS[a.workload]
+    if a.profile_case:
+        # for counter captures only: the same per-layer kernels and batch
+        # shape on two layers and a 32,768-token vocabulary, so the capture
+        # holds a few GB; the line is marked and is not a benchmark value
+        from dataclasses import replace
+        from synth.configs import shrink
+        cfg = shrink(wl.cfg, name=wl.cfg.name + "-profile-case", n_layers=2,
+                     vocab=32768, mask_token_id=32767)
+        wl = replace(wl, name=wl.name + "-profile-case", cfg=cfg)
     if a.impl == "reference":
         return reference_arm(a, wl, rank, world)
     import torch
@@ -525,7 +576,7 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    bench = Bench(wl, verify=a.verify, draft=a.draft)
+    bench = Bench(wl, verify=a.verify, draft=a.draft, kv=a.kv, draft_window=a.draft_window)
     cs = ClockSampler(local)
     if dist:
         dist.barrier()
@@ -558,6 +609,8 @@ def main():
                        "vocab": bench.cfg.vocab, "parallelism": f"replicas x{world}",
                        "l2": "inputs larger than L2 (weights streamed every step)",
                        "kv_len_reset_each_cycle": True, "verify": a.verify, "draft": a.draft,
+                       "kv_cache": a.kv, "draft_window": a.draft_window,
+                       "profile_case": bool(a.profile_case),
                        "mean_commit_len": mean_commit},
             "clocks": clocks, "e2e": e2e, "gpu_launches": launches,
             "roofline": roof, "cpu_baseline": cpu,

@@ -37,7 +37,7 @@ class DflashConfig(ctypes.Structure):
                 ("vocab", c_int32), ("mask_token_id", c_int32), ("block_size", c_int32),
                 ("page_size", c_int32), ("sliding_window", ctypes.POINTER(c_int32)),
                 ("rms_eps", c_float), ("rope_theta", c_float), ("max_batch", c_int32),
-                ("max_rows", c_int32), ("max_position", c_int32)]
+                ("max_rows", c_int32), ("max_position", c_int32), ("kv_fp8", c_int32)]
 
 
 class DflashWeights(ctypes.Structure):
@@ -49,7 +49,9 @@ class DflashWeights(ctypes.Structure):
 
 class DflashKV(ctypes.Structure):
     _fields_ = [("k_pages", P_VOID), ("v_pages", P_VOID), ("page_table", c_void_p),
-                ("pages_per_req", c_int32), ("n_pages", c_int32), ("kv_len", c_void_p)]
+                ("pages_per_req", c_int32), ("n_pages", c_int32), ("kv_len", c_void_p),
+                ("draft_window", c_int32), ("k_scale", ctypes.POINTER(c_float)),
+                ("v_scale", ctypes.POINTER(c_float))]
 
 
 class DflashSelector(ctypes.Structure):

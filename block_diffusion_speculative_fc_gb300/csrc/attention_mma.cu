@@ -18,12 +18,23 @@
 // online softmax in registers with quad shuffles.  A split that is not alone
 // writes (O, m, l) to scratch; the last split of a (b, g) to finish (atomic
 // ticket) merges the splits in split order and writes the output.
+// FP8 cache (CSDN article, Kimi-K2.6 draft card: one byte per K/V element):
+// a context tile is one 8 KB box of E4M3 codes per tensor; all threads widen
+// it into a 16-bit staging tile before the MMAs.  An E4M3 byte shifted into
+// the bit layout of an f16 is exactly that code's value times 2^-8
+// (subnormals and zero included), so the widening is a few integer ops and
+// the MMAs run in f16 (Q rounded to f16 once per item); the factors 2^8 *
+// k_scale and 2^8 * v_scale fold into the softmax scale and into P.  The S
+// block keys stay bf16 (16-row boxes), widened to f16 the same way.
+// Draft KV windowing: the page table is a ring (page of logical page lp is
+// page_table[b][lp % pages_per_req]) and keys below kv_len - W are hidden.
 #include <cuda.h>
 
 #include <algorithm>
 #include <cstring>
 
 #include <cooperative_groups.h>
+#include <cuda_fp16.h>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -39,6 +50,18 @@ constexpr int TILE_BYTES = KT * 128 * 2;   // K (or V) tile: 64 keys x 128 dims
 constexpr int STAGE_BYTES = 2 * TILE_BYTES;
 constexpr int MAX_SPLITS = 16;  // splits of one (request, KV head) at most
 constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 64 + (MAX_SPLITS + 1) * 128 * 4;
+// FP8 layout: STAGES stages of [K codes 8 KB | V codes 8 KB], the 16-bit
+// staging tile [K 16 KB | V 16 KB], the block keys [K 4 KB | V 4 KB] (16 rows
+// of bf16), then the barriers; the split-merge weights reuse the staging tile.
+constexpr int F8_TILE = KT * 128;
+constexpr int F8_STAGE = 2 * F8_TILE;
+constexpr int F8_STAGING = STAGES * F8_STAGE;
+constexpr int F8_BLOCK = F8_STAGING + STAGE_BYTES;
+constexpr int F8_BLK_ROWS = 16;
+constexpr int F8_BARS = F8_BLOCK + 2 * F8_BLK_ROWS * 256;
+constexpr int SMEM_F8 = 1024 + F8_BARS + 64;
+static_assert(SMEM_F8 <= SMEM, "the FP8 layout fits the bf16 kernel's shared memory");
+static_assert((MAX_SPLITS + 1) * 128 * 4 <= STAGE_BYTES, "merge weights fit the staging tile");
 constexpr uint32_t WAIT_LIMIT = 1u << 22;
 constexpr int kMaxCluster = 16;  // CTAs per (request, KV head) in the cluster kernel
 
@@ -57,7 +80,26 @@ struct Params {
   unsigned int *err;
   int B, S, n_heads, kvh, pages_per_req, n_pages, window, R, max_items;
   float scale_log2;              // log2(e) / sqrt(D)
+  int draft_window;              // 0 = off; W > 0: ring page table, keys below kv_len - W hidden
+  float k_mul, v_mul;            // FP8: 2^8 * k_scale, 2^8 * v_scale
 };
+
+// First visible context position of query row j (of a request with kv
+// committed rows): the draft window's bound and, on a sliding layer, the
+// layer's own window (pq - pk < W).
+__device__ __forceinline__ int first_visible(const Params &p, int kv, int j) {
+  const int lw = p.draft_window > 0 ? max(0, kv - p.draft_window) : 0;
+  return p.window > 0 ? max(lw, kv + j - p.window + 1) : lw;
+}
+// Cache page of logical page lp of request b.
+__device__ __forceinline__ int page_of(const Params &p, int b, int lp) {
+  return p.page_table[(size_t)b * p.pages_per_req + (p.draft_window > 0 ? lp % p.pages_per_req : lp)];
+}
+// kv_len clamped to the page table's capacity (no limit for a ring).
+__device__ __forceinline__ int clamp_kv(const Params &p, int kv) {
+  const int cap = p.pages_per_req * KT;
+  return kv < 0 ? 0 : (p.draft_window == 0 && kv > cap ? cap : kv);
+}
 
 __device__ __forceinline__ uint32_t su32(const void *p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -111,6 +153,29 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&v);
 }
+__device__ __forceinline__ void mma16816_f16(float *c, const uint32_t *a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+// Two E4M3 codes (bytes 0, 1 of w, or bytes 2, 3 with hi) as an f16 pair
+// whose values are the codes' values times 2^-8: the sign bit moves to bit
+// 15 and the 7 exponent/mantissa bits to bits 7..13 of each half.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2_scaled(uint32_t w, bool hi) {
+  const uint32_t t = __byte_perm(w, 0u, hi ? 0x3424u : 0x1404u);   // bytes at 8..15 and 24..31
+  return (t & 0x80008000u) | ((t >> 1) & 0x3F803F80u);
+}
+// bf16 pair -> f16 pair (round to nearest)
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+  const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w));
+  return pack_f16(f.x, f.y);
+}
 // Byte address of (row, 16-byte chunk c) in a tile of rows of 128 bytes with
 // the 128-byte swizzle TMA applies (chunk index XOR row % 8).
 __device__ __forceinline__ uint32_t swz(uint32_t base, int row, int c) {
@@ -118,9 +183,17 @@ __device__ __forceinline__ uint32_t swz(uint32_t base, int row, int c) {
 }
 
 // ---------------------------------------------------------------- work list
+// Visible context range of a request with kv rows: [lo, kv), lo from the
+// draft window and the layer window (the earliest query of the block sees
+// the most); its pages.
+__device__ __forceinline__ int visible_lo(int kv, int window, int draft_window) {
+  const int lw = draft_window > 0 ? max(0, kv - draft_window) : 0;
+  return window > 0 ? max(lw, kv - window + 1) : lw;
+}
+
 __global__ void attn_prep_kernel(const int *__restrict__ kv_len, int B, int kvh, int cap,
-                                 int window, int target_items, int max_items, int *item_start,
-                                 int *pps_out, unsigned int *err) {
+                                 int window, int draft_window, int target_items, int max_items,
+                                 int *item_start, int *pps_out, unsigned int *err) {
   pdl_wait();
   __shared__ int s_total;
   if (threadIdx.x == 0) s_total = 0;
@@ -129,7 +202,7 @@ __global__ void attn_prep_kernel(const int *__restrict__ kv_len, int B, int kvh,
   for (int b = threadIdx.x; b < B; b += blockDim.x) {
     int kv = kv_len[b];
     kv = kv < 0 ? 0 : (kv > cap ? cap : kv);
-    const int lo = window > 0 ? max(0, kv - window + 1) : 0;
+    const int lo = visible_lo(kv, window, draft_window);
     const int pages = kv > lo ? (kv - 1) / KT - lo / KT + 1 : 0;
     local += pages;
   }
@@ -140,7 +213,7 @@ __global__ void attn_prep_kernel(const int *__restrict__ kv_len, int B, int kvh,
   for (int b = threadIdx.x; b < B; b += blockDim.x) {
     int kv = kv_len[b];
     kv = kv < 0 ? 0 : (kv > cap ? cap : kv);
-    const int lo = window > 0 ? max(0, kv - window + 1) : 0;
+    const int lo = visible_lo(kv, window, draft_window);
     atomicMax(&s_maxpages, kv > lo ? (kv - 1) / KT - lo / KT + 1 : 0);
   }
   __syncthreads();
@@ -157,7 +230,7 @@ __global__ void attn_prep_kernel(const int *__restrict__ kv_len, int B, int kvh,
       int kv = kv_len[b];
       if (kv < 0 || kv > cap) raise_error(err, DFLASH_DERR_KV_CAPACITY);
       kv = kv < 0 ? 0 : (kv > cap ? cap : kv);
-      const int lo = window > 0 ? max(0, kv - window + 1) : 0;
+      const int lo = visible_lo(kv, window, draft_window);
       const int pages = kv > lo ? (kv - 1) / KT - lo / KT + 1 : 0;
       const int nsplit = max(1, (pages + pps - 1) / pps);
       for (int g = 0; g < kvh; ++g) {
@@ -180,16 +253,33 @@ struct Acc {
 };
 
 // One 64-key tile into ring stage u: context page `lp` of request b, head g
-// (its cache page looked up in the page table), or the S block keys.
+// (its cache page looked up in the page table), or the S block keys.  FP8:
+// a context tile is one box of codes per tensor; the block keys go to their
+// own 16-row region (barrier full[STAGES]) and are issued by issue_block.
+template <bool FP8>
 __device__ __forceinline__ void issue_tile(const Params &p, uint8_t *smem, uint64_t *full,
                                            uint32_t u, int b, int g, int lp, bool block) {
-  uint8_t *st = smem + (u % STAGES) * STAGE_BYTES;
   uint64_t *bar = &full[u % STAGES];
+  if (FP8) {
+    uint8_t *st = smem + (u % STAGES) * F8_STAGE;
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(bar)),
+                 "r"(F8_STAGE)
+                 : "memory");
+    int page = page_of(p, b, lp);
+    if (page < 0 || page >= p.n_pages) {
+      raise_error(p.err, DFLASH_DERR_PAGE_RANGE);
+      page = 0;
+    }
+    tma3(st, &p.tmK, bar, 0, g, page * KT);
+    tma3(st + F8_TILE, &p.tmV, bar, 0, g, page * KT);
+    return;
+  }
+  uint8_t *st = smem + (u % STAGES) * STAGE_BYTES;
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(bar)),
                "r"(STAGE_BYTES)
                : "memory");
   if (!block) {
-    int page = p.page_table[(size_t)b * p.pages_per_req + lp];
+    int page = page_of(p, b, lp);
     if (page < 0 || page >= p.n_pages) {
       raise_error(p.err, DFLASH_DERR_PAGE_RANGE);
       page = 0;
@@ -205,16 +295,75 @@ __device__ __forceinline__ void issue_tile(const Params &p, uint8_t *smem, uint6
     tma3(st + TILE_BYTES + TILE_BYTES / 2, &p.tmVb, bar, 64, g, b * p.S);
   }
 }
+// FP8 layout: the S block keys of (b, g) as bf16, 16 rows per box.
+__device__ __forceinline__ void issue_block_f8(const Params &p, uint8_t *smem, uint64_t *full, int b,
+                                               int g) {
+  uint64_t *bar = &full[STAGES];
+  uint8_t *st = smem + F8_BLOCK;
+  constexpr int BOX = F8_BLK_ROWS * 128;   // 16 rows x 64 dims of bf16
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(bar)),
+               "r"(4 * BOX)
+               : "memory");
+  tma3(st, &p.tmKb, bar, 0, g, b * p.S);
+  tma3(st + BOX, &p.tmKb, bar, 64, g, b * p.S);
+  tma3(st + 2 * BOX, &p.tmVb, bar, 0, g, b * p.S);
+  tma3(st + 3 * BOX, &p.tmVb, bar, 64, g, b * p.S);
+}
+
+// FP8: E4M3 codes of stage `st` (K and V, 64 rows of 128 bytes, 128-byte
+// swizzle) -> the f16 staging tile (two boxes of 64 dims per tensor, the same
+// layout as a bf16 tile), values times 2^-8.  A 16-byte chunk of codes (dims
+// 16c .. 16c+15 of one row) becomes two 16-byte chunks in box c / 4.
+__device__ __forceinline__ void widen_f8(const uint8_t *st, uint8_t *staging) {
+  for (int idx = threadIdx.x; idx < 2 * KT * 8; idx += blockDim.x) {
+    const int tensor = idx >> 9, row = (idx >> 3) & 63, c = idx & 7;
+    const uint4 w = *reinterpret_cast<const uint4 *>(st + tensor * F8_TILE + row * 128 +
+                                                      (((c ^ row) & 7) << 4));
+    uint4 lo, hi;
+    lo.x = e4m3x2_to_f16x2_scaled(w.x, false);
+    lo.y = e4m3x2_to_f16x2_scaled(w.x, true);
+    lo.z = e4m3x2_to_f16x2_scaled(w.y, false);
+    lo.w = e4m3x2_to_f16x2_scaled(w.y, true);
+    hi.x = e4m3x2_to_f16x2_scaled(w.z, false);
+    hi.y = e4m3x2_to_f16x2_scaled(w.z, true);
+    hi.z = e4m3x2_to_f16x2_scaled(w.w, false);
+    hi.w = e4m3x2_to_f16x2_scaled(w.w, true);
+    uint8_t *box = staging + tensor * TILE_BYTES + (c >> 2) * (TILE_BYTES / 2) + row * 128;
+    const int c0 = (c & 3) * 2;
+    *reinterpret_cast<uint4 *>(box + (((c0 ^ row) & 7) << 4)) = lo;
+    *reinterpret_cast<uint4 *>(box + ((((c0 + 1) ^ row) & 7) << 4)) = hi;
+  }
+}
+// FP8: the bf16 block keys (16 rows) -> rows 0..15 of the f16 staging tile.
+// Box rows of 128 bytes keep their 128-byte swizzle position (row % 8).
+__device__ __forceinline__ void widen_block_f8(const uint8_t *blk, uint8_t *staging) {
+  constexpr int BOX = F8_BLK_ROWS * 128;
+  for (int idx = threadIdx.x; idx < 4 * F8_BLK_ROWS * 8; idx += blockDim.x) {
+    const int box = idx >> 7, within = idx & 127;   // box: K lo, K hi, V lo, V hi
+    const uint4 w = *reinterpret_cast<const uint4 *>(blk + box * BOX + within * 16);
+    uint4 o;
+    o.x = bf16x2_to_f16x2(w.x);
+    o.y = bf16x2_to_f16x2(w.y);
+    o.z = bf16x2_to_f16x2(w.z);
+    o.w = bf16x2_to_f16x2(w.w);
+    *reinterpret_cast<uint4 *>(staging + (box >> 1) * TILE_BYTES + (box & 1) * (TILE_BYTES / 2) +
+                               within * 16) = o;
+  }
+}
 
 // `pre`: tiles 0..pre-1 were already issued by the caller (context tiles,
-// issued before the predecessor kernel finished).
+// issued before the predecessor kernel finished).  FP8: the caller has also
+// issued the block keys (issue_block_f8) when has_block; `buse` counts the
+// block region's uses (its barrier phase).
+template <bool FP8>
 __device__ __forceinline__ bool attend(const Params &p, uint8_t *smem, uint64_t *full, uint32_t &use,
-                                       int b, int g, int kv, int first_page, int pg0, int pg1,
-                                       bool has_block, Acc &a, int pre = 0) {
+                                       uint32_t &buse, int b, int g, int kv, int first_page, int pg0,
+                                       int pg1, bool has_block, Acc &a, int pre = 0) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int grp = lane >> 2, tig = lane & 3;
   const int S = p.S, R = p.R, G = p.n_heads / p.kvh;
-  const int ntiles = max(0, pg1 - pg0) + (has_block ? 1 : 0);
+  const int nctx = max(0, pg1 - pg0);
+  const int ntiles = nctx + (has_block ? 1 : 0);
   float(&o)[16][4] = a.o;
   float &m0 = a.m0, &m1 = a.m1, &l0 = a.l0, &l1 = a.l1;
   // query rows of this warp: r = warp*16 + grp (+8); row r -> head g*G + r/S, position j = r%S
@@ -234,6 +383,7 @@ __device__ __forceinline__ bool attend(const Params &p, uint8_t *smem, uint64_t 
           if (r < R) {
             const int h = g * G + r / S, j = r % S;
             v = *reinterpret_cast<const uint32_t *>(q + ((size_t)(b * S + j) * p.n_heads + h) * 128 + d);
+            if (FP8) v = bf16x2_to_f16x2(v);
           }
           qa[ks][half * 2 + hh] = v;
         }
@@ -247,23 +397,44 @@ __device__ __forceinline__ bool attend(const Params &p, uint8_t *smem, uint64_t 
   l0 = 0.f;
   l1 = 0.f;
   const int j0 = r0 % S, j1 = r1 % S;
-  const int lo0 = p.window > 0 ? kv + j0 - p.window + 1 : 0;   // first visible ctx position
-  const int lo1 = p.window > 0 ? kv + j1 - p.window + 1 : 0;
+  const int lo0 = first_visible(p, kv, j0), lo1 = first_visible(p, kv, j1);
+  uint8_t *staging = smem + F8_STAGING;
 
   auto issue = [&](int t, uint32_t u) {
-    issue_tile(p, smem, full, u, b, g, first_page + pg0 + t, t >= pg1 - pg0);
+    issue_tile<FP8>(p, smem, full, u, b, g, first_page + pg0 + t, t >= pg1 - pg0);
   };
+  // FP8: the ring carries only the context tiles; the block keys come last
+  const int nring = FP8 ? nctx : ntiles;
   if (threadIdx.x == 0)
-    for (int t = pre; t < STAGES && t < ntiles; ++t) issue(t, use + t);
+    for (int t = pre; t < STAGES && t < nring; ++t) issue(t, use + t);
 
   bool ok = true;
   for (int t = 0; t < ntiles; ++t) {
+    const bool blk = t >= nctx;
     const uint32_t u = use + t;
-    const bool got = mbar_wait(&full[u % STAGES], (u / STAGES) & 1);
-    if (!got) ok = false;
-    const uint32_t kbase = su32(smem + (u % STAGES) * STAGE_BYTES);
-    const uint32_t vbase = kbase + TILE_BYTES;
-    const bool blk = t >= pg1 - pg0;
+    uint32_t kbase, vbase;
+    float sl = p.scale_log2, vm = 1.f;   // logit scale (log2 units), P factor
+    if (FP8) {
+      if (!blk) {
+        if (!mbar_wait(&full[u % STAGES], (u / STAGES) & 1)) ok = false;
+        widen_f8(smem + (u % STAGES) * F8_STAGE, staging);
+        sl = p.scale_log2 * p.k_mul;
+        vm = p.v_mul;
+      } else {
+        if (!mbar_wait(&full[STAGES], buse & 1)) ok = false;
+        ++buse;
+        widen_block_f8(smem + F8_BLOCK, staging);
+      }
+      __syncthreads();   // staging complete; the stage is free again
+      if (!blk && threadIdx.x == 0 && t + STAGES < nring) issue(t + STAGES, u + STAGES);
+      kbase = su32(staging);
+    } else {
+      if (!mbar_wait(&full[u % STAGES], (u / STAGES) & 1)) ok = false;
+      kbase = su32(smem + (u % STAGES) * STAGE_BYTES);
+    }
+    vbase = kbase + TILE_BYTES;
+    // FP8 block tile: only its 16 rows are in the staging tile
+    const bool short_tile = FP8 && blk;
     const int pos0 = (first_page + pg0 + t) * KT;   // position of key 0 of a context tile
     // ---- S = Q K^T (16 rows x 64 keys per warp)
     float s[8][4];
@@ -271,6 +442,7 @@ __device__ __forceinline__ bool attend(const Params &p, uint8_t *smem, uint64_t 
     for (int nt = 0; nt < 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
+      if (short_tile && nt >= F8_BLK_ROWS / 8) continue;
 #pragma unroll
       for (int kc = 0; kc < 4; ++kc) {          // 32 dims per ldmatrix.x4
         const int key = nt * 8 + (lane & 7);
@@ -278,12 +450,17 @@ __device__ __forceinline__ bool attend(const Params &p, uint8_t *smem, uint64_t 
         const uint32_t addr = swz(kbase + (d >> 6) * (TILE_BYTES / 2), key, (d & 63) >> 3);
         uint32_t b0, b1, b2, b3;
         ldsm_x4(addr, b0, b1, b2, b3);
-        mma16816(s[nt], qa[kc * 2], b0, b1);
-        mma16816(s[nt], qa[kc * 2 + 1], b2, b3);
+        if (FP8) {
+          mma16816_f16(s[nt], qa[kc * 2], b0, b1);
+          mma16816_f16(s[nt], qa[kc * 2 + 1], b2, b3);
+        } else {
+          mma16816(s[nt], qa[kc * 2], b0, b1);
+          mma16816(s[nt], qa[kc * 2 + 1], b2, b3);
+        }
       }
     }
     // ---- mask, online softmax.  A context tile that every row of the warp
-    // sees whole (all but the last tile and the window edge) needs no mask.
+    // sees whole (all but the last tile and the window edges) needs no mask.
     float mx0 = -INFINITY, mx1 = -INFINITY;
     const bool whole = __all_sync(0xffffffffu, !blk && pos0 + KT <= kv && pos0 >= lo0 &&
                                                    pos0 >= lo1 && r1 < R);
@@ -299,7 +476,7 @@ __device__ __forceinline__ bool attend(const Params &p, uint8_t *smem, uint64_t 
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-      const float mn0 = fmaxf(m0, mx0 * p.scale_log2), mn1 = fmaxf(m1, mx1 * p.scale_log2);
+      const float mn0 = fmaxf(m0, mx0 * sl), mn1 = fmaxf(m1, mx1 * sl);
       const bool moved = __any_sync(0xffffffffu, mn0 != m0 || mn1 != m1);
       const float a0 = exp2f(m0 - mn0), a1 = exp2f(m1 - mn1);   // m = -inf at first: a = 0
       m0 = mn0;
@@ -307,10 +484,10 @@ __device__ __forceinline__ bool attend(const Params &p, uint8_t *smem, uint64_t 
       float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) {
-        s[nt][0] = exp2f(fmaf(s[nt][0], p.scale_log2, -mn0));
-        s[nt][1] = exp2f(fmaf(s[nt][1], p.scale_log2, -mn0));
-        s[nt][2] = exp2f(fmaf(s[nt][2], p.scale_log2, -mn1));
-        s[nt][3] = exp2f(fmaf(s[nt][3], p.scale_log2, -mn1));
+        s[nt][0] = exp2f(fmaf(s[nt][0], sl, -mn0));
+        s[nt][1] = exp2f(fmaf(s[nt][1], sl, -mn0));
+        s[nt][2] = exp2f(fmaf(s[nt][2], sl, -mn1));
+        s[nt][3] = exp2f(fmaf(s[nt][3], sl, -mn1));
         ps0 += s[nt][0] + s[nt][1];
         ps1 += s[nt][2] + s[nt][3];
       }
@@ -340,7 +517,7 @@ __device__ __forceinline__ bool attend(const Params &p, uint8_t *smem, uint64_t 
             vis = pos < kv && pos >= (row1 ? lo1 : lo0);
           }
           if ((row1 ? r1 : r0) >= R) vis = false;
-          const float v = vis ? s[nt][e] * p.scale_log2 : -INFINITY;
+          const float v = vis ? s[nt][e] * sl : -INFINITY;
           s[nt][e] = v;
           if (row1) mx1 = fmaxf(mx1, v); else mx0 = fmaxf(mx0, v);
         }
@@ -374,14 +551,23 @@ __device__ __forceinline__ bool attend(const Params &p, uint8_t *smem, uint64_t 
         o[i][3] *= a1;
       }
     }
-    // ---- O += P V (P from the S accumulators, V via transposed ldmatrix)
+    // ---- O += P V (P from the S accumulators, V via transposed ldmatrix);
+    // FP8 context tiles: P carries the V factor, f16 operands
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {              // 16 keys per step
+      if (short_tile && kk >= F8_BLK_ROWS / 16) continue;
       uint32_t pa[4];
-      pa[0] = pack_bf16(s[2 * kk][0], s[2 * kk][1]);
-      pa[1] = pack_bf16(s[2 * kk][2], s[2 * kk][3]);
-      pa[2] = pack_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-      pa[3] = pack_bf16(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+      if (FP8) {
+        pa[0] = pack_f16(s[2 * kk][0] * vm, s[2 * kk][1] * vm);
+        pa[1] = pack_f16(s[2 * kk][2] * vm, s[2 * kk][3] * vm);
+        pa[2] = pack_f16(s[2 * kk + 1][0] * vm, s[2 * kk + 1][1] * vm);
+        pa[3] = pack_f16(s[2 * kk + 1][2] * vm, s[2 * kk + 1][3] * vm);
+      } else {
+        pa[0] = pack_bf16(s[2 * kk][0], s[2 * kk][1]);
+        pa[1] = pack_bf16(s[2 * kk][2], s[2 * kk][3]);
+        pa[2] = pack_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1]);
+        pa[3] = pack_bf16(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+      }
 #pragma unroll
       for (int np = 0; np < 8; ++np) {            // pairs of 8-dim n-tiles
         const int key = kk * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
@@ -389,14 +575,19 @@ __device__ __forceinline__ bool attend(const Params &p, uint8_t *smem, uint64_t 
         const uint32_t addr = swz(vbase + (d >> 6) * (TILE_BYTES / 2), key, (d & 63) >> 3);
         uint32_t b0, b1, b2, b3;
         ldsm_x4_t(addr, b0, b1, b2, b3);
-        mma16816(o[2 * np], pa, b0, b1);
-        mma16816(o[2 * np + 1], pa, b2, b3);
+        if (FP8) {
+          mma16816_f16(o[2 * np], pa, b0, b1);
+          mma16816_f16(o[2 * np + 1], pa, b2, b3);
+        } else {
+          mma16816(o[2 * np], pa, b0, b1);
+          mma16816(o[2 * np + 1], pa, b2, b3);
+        }
       }
     }
-    __syncthreads();   // every warp is done with this stage
-    if (threadIdx.x == 0 && t + STAGES < ntiles) issue(t + STAGES, u + STAGES);
+    __syncthreads();   // every warp is done with this stage (FP8: with the staging tile)
+    if (!FP8 && threadIdx.x == 0 && t + STAGES < ntiles) issue(t + STAGES, u + STAGES);
   }
-  use += ntiles;
+  use += nring;
   if (!ok && lane == 0) raise_error(p.err, DFLASH_DERR_TIMEOUT);
 
   // ---- finish: row sums across the quad
@@ -411,14 +602,15 @@ __device__ __forceinline__ bool attend(const Params &p, uint8_t *smem, uint64_t 
 // MAXT: threads per CTA this instantiation is built for; up to 128 threads
 // (G*S <= 64 query rows) three CTAs share an SM, which is what hides the
 // latency of the per-tile MMA/softmax chain.
-template <int MAXT>
+template <int MAXT, bool FP8>
 __global__ void __launch_bounds__(MAXT, MAXT <= 128 ? 3 : 1) attn_mma_kernel(const __grid_constant__ Params p) {
   pdl_wait();
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  uint64_t *full = (uint64_t *)(smem + STAGES * STAGE_BYTES);
-  int *s_flag = (int *)(full + STAGES);
-  float *s_w = (float *)(smem + STAGES * STAGE_BYTES + 64);   // [MAX_SPLITS + 1][R]
+  uint64_t *full = (uint64_t *)(smem + (FP8 ? F8_BARS : STAGES * STAGE_BYTES));
+  int *s_flag = (int *)(full + STAGES + 1);
+  // [MAX_SPLITS + 1][R] merge weights (FP8: in the staging tile, free between items)
+  float *s_w = (float *)(smem + (FP8 ? F8_STAGING : STAGES * STAGE_BYTES + 64));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nwarps = blockDim.x >> 5;
   const int grp = lane >> 2, tig = lane & 3;
@@ -426,15 +618,14 @@ __global__ void __launch_bounds__(MAXT, MAXT <= 128 ? 3 : 1) attn_mma_kernel(con
   const int pps = *p.pps_ptr;
   const int n_bg = p.B * p.kvh;
   const int total_items = p.item_start[n_bg];
-  const int cap = p.pages_per_req * KT;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < STAGES; ++i)
+    for (int i = 0; i < STAGES + (FP8 ? 1 : 0); ++i)
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&full[i])));
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  uint32_t use = 0;   // stage uses so far (ring position and phase)
+  uint32_t use = 0, buse = 0;   // stage uses so far (ring position and phase), block uses
 
   for (int item = blockIdx.x; item < total_items; item += gridDim.x) {
     // item -> (b, g, split)
@@ -446,16 +637,16 @@ __global__ void __launch_bounds__(MAXT, MAXT <= 128 ? 3 : 1) attn_mma_kernel(con
     const int bg = lo_i, b = bg / p.kvh, g = bg % p.kvh;
     const int split = item - p.item_start[bg];
     const int nsplit = p.item_start[bg + 1] - p.item_start[bg];
-    int kv = p.kv_len[b];
-    kv = kv < 0 ? 0 : (kv > cap ? cap : kv);
-    const int lo = p.window > 0 ? max(0, kv - p.window + 1) : 0;
+    const int kv = clamp_kv(p, p.kv_len[b]);
+    const int lo = visible_lo(kv, p.window, p.draft_window);
     const int first_page = lo / KT;
     const int pages = kv > lo ? (kv - 1) / KT - first_page + 1 : 0;
     const int pg0 = split * pps, pg1 = min(pages, pg0 + pps);
     const bool has_block = split == nsplit - 1;
 
+    if (FP8 && has_block && threadIdx.x == 0) issue_block_f8(p, smem, full, b, g);
     Acc acc;
-    attend(p, smem, full, use, b, g, kv, first_page, pg0, pg1, has_block, acc);
+    attend<FP8>(p, smem, full, use, buse, b, g, kv, first_page, pg0, pg1, has_block, acc);
     const int r0 = warp * 16 + grp, r1 = r0 + 8;
     float(&o)[16][4] = acc.o;
     const float m0 = acc.m0, m1 = acc.m1, l0 = acc.l0, l1 = acc.l1;
@@ -542,10 +733,11 @@ __global__ void __launch_bounds__(MAXT, MAXT <= 128 ? 3 : 1) attn_mma_kernel(con
 // the r-th of C equal slices of the context pages (the last rank also the
 // block keys), then the C partial results are merged through distributed
 // shared memory -- no scratch in global memory, no tickets, no prep kernel.
+template <bool FP8>
 __global__ void __launch_bounds__(256) attn_cluster_kernel(const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  uint64_t *full = (uint64_t *)(smem + STAGES * STAGE_BYTES);
+  uint64_t *full = (uint64_t *)(smem + (FP8 ? F8_BARS : STAGES * STAGE_BYTES));
   cg::cluster_group cl = cg::this_cluster();
   const int C = (int)cl.num_blocks();
   const int rank = (int)cl.block_rank();
@@ -553,19 +745,16 @@ __global__ void __launch_bounds__(256) attn_cluster_kernel(const __grid_constant
   const int grp = lane >> 2, tig = lane & 3;
   const int S = p.S, R = p.R, G = p.n_heads / p.kvh;
   const int bg = blockIdx.x / C, b = bg / p.kvh, g = bg % p.kvh;
-  const int cap = p.pages_per_req * KT;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < STAGES; ++i)
+    for (int i = 0; i < STAGES + (FP8 ? 1 : 0); ++i)
       asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&full[i])));
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  int kv = p.kv_len[b];
-  if (kv < 0 || kv > cap) {
-    if (threadIdx.x == 0 && rank == 0) raise_error(p.err, DFLASH_DERR_KV_CAPACITY);
-    kv = kv < 0 ? 0 : cap;
-  }
-  const int lo = p.window > 0 ? max(0, kv - p.window + 1) : 0;
+  const int kv_raw = p.kv_len[b];
+  const int kv = clamp_kv(p, kv_raw);
+  if (kv != kv_raw && threadIdx.x == 0 && rank == 0) raise_error(p.err, DFLASH_DERR_KV_CAPACITY);
+  const int lo = visible_lo(kv, p.window, p.draft_window);
   const int first_page = lo / KT;
   const int pages = kv > lo ? (kv - 1) / KT - first_page + 1 : 0;
   const int pg0 = pages * rank / C, pg1 = pages * (rank + 1) / C;
@@ -574,11 +763,12 @@ __global__ void __launch_bounds__(256) attn_cluster_kernel(const __grid_constant
   // first tiles go out before waiting for it.
   const int pre = min(STAGES, pg1 - pg0);
   if (threadIdx.x == 0)
-    for (int t = 0; t < pre; ++t) issue_tile(p, smem, full, t, b, g, first_page + pg0 + t, false);
+    for (int t = 0; t < pre; ++t) issue_tile<FP8>(p, smem, full, t, b, g, first_page + pg0 + t, false);
   pdl_wait();
-  uint32_t use = 0;
+  if (FP8 && rank == C - 1 && threadIdx.x == 0) issue_block_f8(p, smem, full, b, g);
+  uint32_t use = 0, buse = 0;
   Acc acc;
-  attend(p, smem, full, use, b, g, kv, first_page, pg0, pg1, rank == C - 1, acc, pre);
+  attend<FP8>(p, smem, full, use, buse, b, g, kv, first_page, pg0, pg1, rank == C - 1, acc, pre);
   // this CTA's partial (unnormalised O, row max, row sum) into its own shared memory;
   // the stage ring is free: attend() ends every tile with a CTA barrier
   float *po = reinterpret_cast<float *>(smem);                    // [R][128]
@@ -657,15 +847,28 @@ EncodeTiledFn att_encoder() {
   }
   return fn;
 }
-// [rows, kvh, 128] bf16 viewed as dims {128, kvh, rows}; box {64, 1, 64}.
-bool encode_kv(CUtensorMap *tm, const void *base, uint64_t rows, int kvh) {
+// [rows, kvh, 128] bf16 viewed as dims {128, kvh, rows}; box {64, 1, box_rows}.
+bool encode_kv(CUtensorMap *tm, const void *base, uint64_t rows, int kvh, uint32_t box_rows = 64) {
   EncodeTiledFn fn = att_encoder();
   if (!fn) return false;
   cuuint64_t dims[3] = {128, (cuuint64_t)kvh, rows};
   cuuint64_t strides[2] = {128 * 2, (cuuint64_t)kvh * 128 * 2};
-  cuuint32_t box[3] = {64, 1, 64};
+  cuuint32_t box[3] = {64, 1, box_rows};
   cuuint32_t estr[3] = {1, 1, 1};
   return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+// FP8 cache [rows, kvh, 128] bytes viewed as dims {128, kvh, rows}; box {128, 1, 64}:
+// one 128-byte swizzle row per key.
+bool encode_kv_f8(CUtensorMap *tm, const void *base, uint64_t rows, int kvh) {
+  EncodeTiledFn fn = att_encoder();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {128, (cuuint64_t)kvh, rows};
+  cuuint64_t strides[2] = {128, (cuuint64_t)kvh * 128};
+  cuuint32_t box[3] = {128, 1, 64};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -676,16 +879,21 @@ size_t attention_mma_scratch_items(int max_batch, int kvh) {
 }
 
 cudaError_t prepare_attention_mma() {
-  cudaError_t e = cudaFuncSetAttribute(att::attn_mma_kernel<128>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, att::SMEM);
+  const void *kernels[] = {(const void *)att::attn_mma_kernel<128, false>,
+                           (const void *)att::attn_mma_kernel<256, false>,
+                           (const void *)att::attn_mma_kernel<128, true>,
+                           (const void *)att::attn_mma_kernel<256, true>,
+                           (const void *)att::attn_cluster_kernel<false>,
+                           (const void *)att::attn_cluster_kernel<true>};
+  for (const void *k : kernels) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, att::SMEM);
+    if (e != cudaSuccess) return e;
+  }
+  cudaError_t e = cudaFuncSetAttribute((const void *)att::attn_cluster_kernel<false>,
+                                       cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(att::attn_mma_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           att::SMEM);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(att::attn_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           att::SMEM);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(att::attn_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return cudaFuncSetAttribute((const void *)att::attn_cluster_kernel<true>,
+                              cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
 }
 
 namespace {
@@ -707,7 +915,7 @@ bool cluster_fits(int C, int warps) {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int n = 0;
-    k = (cudaOccupancyMaxActiveClusters(&n, att::attn_cluster_kernel, &cfg) == cudaSuccess && n > 0)
+    k = (cudaOccupancyMaxActiveClusters(&n, att::attn_cluster_kernel<false>, &cfg) == cudaSuccess && n > 0)
             ? 1 : -1;
     cudaGetLastError();
   }
@@ -721,13 +929,20 @@ cudaError_t launch_attention_mma(const AttnParams &a, const AttnScratch &w, cuda
   const int R = (a.n_heads / a.n_kv_heads) * a.S;
   const int warps = (R + 15) / 16;
   if (warps > 8) return cudaErrorInvalidValue;
+  if (a.fp8 && a.S > att::F8_BLK_ROWS) return cudaErrorInvalidValue;
   att::Params p;
   memset(&p, 0, sizeof(p));
-  if (!encode_kv(&p.tmK, a.k_cache, (uint64_t)a.n_pages * att::KT, a.n_kv_heads) ||
-      !encode_kv(&p.tmV, a.v_cache, (uint64_t)a.n_pages * att::KT, a.n_kv_heads) ||
-      !encode_kv(&p.tmKb, a.kb, (uint64_t)a.B * a.S, a.n_kv_heads) ||
-      !encode_kv(&p.tmVb, a.vb, (uint64_t)a.B * a.S, a.n_kv_heads))
-    return cudaErrorInvalidValue;
+  const uint64_t cache_rows = (uint64_t)a.n_pages * att::KT;
+  const bool maps_ok =
+      a.fp8 ? encode_kv_f8(&p.tmK, a.k_cache, cache_rows, a.n_kv_heads) &&
+                  encode_kv_f8(&p.tmV, a.v_cache, cache_rows, a.n_kv_heads) &&
+                  encode_kv(&p.tmKb, a.kb, (uint64_t)a.B * a.S, a.n_kv_heads, att::F8_BLK_ROWS) &&
+                  encode_kv(&p.tmVb, a.vb, (uint64_t)a.B * a.S, a.n_kv_heads, att::F8_BLK_ROWS)
+            : encode_kv(&p.tmK, a.k_cache, cache_rows, a.n_kv_heads) &&
+                  encode_kv(&p.tmV, a.v_cache, cache_rows, a.n_kv_heads) &&
+                  encode_kv(&p.tmKb, a.kb, (uint64_t)a.B * a.S, a.n_kv_heads) &&
+                  encode_kv(&p.tmVb, a.vb, (uint64_t)a.B * a.S, a.n_kv_heads);
+  if (!maps_ok) return cudaErrorInvalidValue;
   int sms = 0, dev = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -746,6 +961,9 @@ cudaError_t launch_attention_mma(const AttnParams &a, const AttnScratch &w, cuda
   p.window = a.window;
   p.R = R;
   p.scale_log2 = 1.4426950408889634f * a.scale;
+  p.draft_window = a.draft_window;
+  p.k_mul = 256.f * a.k_scale;   // widened codes carry a factor 2^-8
+  p.v_mul = 256.f * a.v_scale;
   // Few (request, head) pairs: a cluster of C CTAs per pair, merged on chip.
   const int pairs = a.B * a.n_kv_heads;
   if (4 * pairs <= 2 * sms) {
@@ -767,12 +985,14 @@ cudaError_t launch_attention_mma(const AttnParams &a, const AttnScratch &w, cuda
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, att::attn_cluster_kernel, p);
+    return a.fp8 ? cudaLaunchKernelEx(&cfg, att::attn_cluster_kernel<true>, p)
+                 : cudaLaunchKernelEx(&cfg, att::attn_cluster_kernel<false>, p);
   }
   const int max_items = (int)attention_mma_scratch_items(a.B, a.n_kv_heads);
   const int per_sm = warps <= 4 ? 3 : 1;   // resident CTAs per SM (shared memory / registers)
+  const int cap = a.draft_window > 0 ? INT32_MAX : a.pages_per_req * att::KT;
   cudaError_t e = launch_pdl(att::attn_prep_kernel, dim3(1), dim3(256), 0, s, a.kv_len, a.B,
-                             a.n_kv_heads, a.pages_per_req * att::KT, a.window, per_sm * sms,
+                             a.n_kv_heads, cap, a.window, a.draft_window, per_sm * sms,
                              max_items, w.item_start, w.pps, a.err);
   if (e != cudaSuccess) return e;
   p.item_start = w.item_start;
@@ -781,9 +1001,12 @@ cudaError_t launch_attention_mma(const AttnParams &a, const AttnScratch &w, cuda
   p.part_ml = (float2 *)w.part_ml;
   p.tickets = w.tickets;
   p.max_items = max_items;
-  if (warps <= 4)
-    return launch_pdl(att::attn_mma_kernel<128>, dim3(per_sm * sms), dim3(warps * 32), att::SMEM, s, p);
-  return launch_pdl(att::attn_mma_kernel<256>, dim3(per_sm * sms), dim3(warps * 32), att::SMEM, s, p);
+  const dim3 grid(per_sm * sms), block(warps * 32);
+  if (a.fp8)
+    return warps <= 4 ? launch_pdl(att::attn_mma_kernel<128, true>, grid, block, att::SMEM, s, p)
+                      : launch_pdl(att::attn_mma_kernel<256, true>, grid, block, att::SMEM, s, p);
+  return warps <= 4 ? launch_pdl(att::attn_mma_kernel<128, false>, grid, block, att::SMEM, s, p)
+                    : launch_pdl(att::attn_mma_kernel<256, false>, grid, block, att::SMEM, s, p);
 }
 
 }  // namespace dflash

@@ -51,12 +51,15 @@ __global__ void __launch_bounds__(THREADS) attn_simt_kernel(const __grid_constan
     lrow[r] = 0.f;
   }
   const int cap = p.pages_per_req * p.page_size;
+  const bool ring = p.draft_window > 0;   // draft KV windowing: ring page table, no capacity
   int kv = p.kv_len[b];
-  if (kv > cap || kv < 0) {
+  if ((!ring && kv > cap) || kv < 0) {
     if (tid == 0) raise_error(p.err, DFLASH_DERR_KV_CAPACITY);
     kv = kv < 0 ? 0 : cap;
   }
-  const int lo = p.window > 0 ? max(0, kv - p.window + 1) : 0;  // first key query j=0 can see
+  // first key query j=0 can see: the draft window's newest W rows, the layer window
+  const int lw = ring ? max(0, kv - p.draft_window) : 0;
+  const int lo = p.window > 0 ? max(lw, kv - p.window + 1) : lw;
   const int nctx = kv - lo, total = nctx + S;
   const T *kc = (const T *)p.k_cache, *vc = (const T *)p.v_cache;
   const T *kb = (const T *)p.kb, *vb = (const T *)p.vb;
@@ -68,7 +71,8 @@ __global__ void __launch_bounds__(THREADS) attn_simt_kernel(const __grid_constan
       float kv_k = 0.f, kv_v = 0.f;
       if (kk < nctx) {
         const int pos = lo + kk;
-        const int page = p.page_table[(int64_t)b * p.pages_per_req + pos / p.page_size];
+        const int lp = pos / p.page_size;
+        const int page = p.page_table[(int64_t)b * p.pages_per_req + (ring ? lp % p.pages_per_req : lp)];
         if (page >= 0 && page < p.n_pages) {
           const int64_t row = (int64_t)page * p.page_size + pos % p.page_size;
           kv_k = to_f32(kc[row * kvd + g * D + d]);

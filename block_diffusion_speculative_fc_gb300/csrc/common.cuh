@@ -50,6 +50,17 @@ __device__ __forceinline__ int argmax_key_index(unsigned long long k) {
 
 __device__ __forceinline__ float silu(float x) { return x / (1.0f + expf(-x)); }
 
+// Two OCP FP8 E4M3 codes of lo / scale and hi / scale (IEEE float32 division)
+// packed little-endian (lo in the low byte): nearest code, ties to the even
+// code, magnitudes beyond 448 saturate to +-448 (the hardware conversion's
+// round-to-nearest-even with .satfinite).
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi, float scale) {
+  const float a = __fdiv_rn(lo, scale), b = __fdiv_rn(hi, scale);
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(b), "f"(a));
+  return r;
+}
+
 // Programmatic dependent launch.  Every kernel is launched so that it may be
 // scheduled before its predecessor in the stream has exited.  A kernel waits
 // for its predecessor (griddepcontrol.wait) right before it first reads what

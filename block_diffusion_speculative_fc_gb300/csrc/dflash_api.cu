@@ -1,6 +1,7 @@
 // C-ABI runtime of the DFlash draft-pass library: handle, validation,
 // workspace plan and the launch sequence of each entry point.
 #include <algorithm>
+#include <cmath>
 #include <cstring>
 #include <string>
 #include <vector>
@@ -256,7 +257,23 @@ int check_kv(const dflash_handle *h, const dflash_kv *kv) {
   for (int l = 0; l < h->cfg.n_layers; ++l)
     if (!kv->k_pages[l] || !kv->v_pages[l])
       return fail(DFLASH_EINVAL, "kv: NULL page pointer for layer " + std::to_string(l));
+  if (kv->draft_window < 0) return fail(DFLASH_EINVAL, "kv: negative draft_window");
+  if (kv->draft_window > 0 &&
+      (int64_t)kv->pages_per_req * h->cfg.page_size < (int64_t)kv->draft_window + h->cfg.page_size)
+    return fail(DFLASH_EINVAL, "kv: a draft window of W rows needs a ring of at least "
+                               "ceil(W / page_size) + 1 pages per request");
+  if (h->cfg.kv_fp8) {
+    if (!kv->k_scale || !kv->v_scale) return fail(DFLASH_EINVAL, "kv: FP8 cache without k_scale/v_scale");
+    for (int l = 0; l < h->cfg.n_layers; ++l)
+      if (!(kv->k_scale[l] > 0.f) || !(kv->v_scale[l] > 0.f) || std::isinf(kv->k_scale[l]) ||
+          std::isinf(kv->v_scale[l]))
+        return fail(DFLASH_EINVAL, "kv: FP8 scales must be positive and finite");
+  }
   return DFLASH_OK;
+}
+// Capacity of a request's page table in rows (no limit for a draft-window ring).
+int64_t kv_capacity(const dflash_handle *h, const dflash_kv *kv) {
+  return kv->draft_window > 0 ? (int64_t)INT32_MAX : (int64_t)kv->pages_per_req * h->cfg.page_size;
 }
 
 }  // namespace
@@ -313,6 +330,9 @@ int dflash_create(const dflash_config *cfg, const dflash_weights *w, dflash_hand
   if (c.page_size != 64) return fail(DFLASH_EUNSUPPORTED, "page_size must be 64");
   if (c.dtype == DFLASH_BF16 && c.head_dim != 128)
     return fail(DFLASH_EUNSUPPORTED, "bf16 configurations need head_dim 128");
+  if (c.kv_fp8 != 0 && c.kv_fp8 != 1) return fail(DFLASH_EINVAL, "kv_fp8 must be 0 or 1");
+  if (c.kv_fp8 && (c.dtype != DFLASH_BF16 || c.head_dim != 128 || c.block_size > 16))
+    return fail(DFLASH_EUNSUPPORTED, "an FP8 KV cache needs bf16, head_dim 128 and block_size <= 16");
   if (c.mask_token_id < 0 || c.mask_token_id >= c.vocab) return fail(DFLASH_EINVAL, "mask_token_id outside the vocabulary");
   if (!(c.rms_eps >= 0.f) || !(c.rope_theta > 0.f)) return fail(DFLASH_EINVAL, "rms_eps >= 0 and rope_theta > 0 required");
   if (c.max_position < c.block_size) return fail(DFLASH_EINVAL, "max_position < block_size");
@@ -327,6 +347,11 @@ int dflash_create(const dflash_config *cfg, const dflash_weights *w, dflash_hand
     if (!w->qkv_w[l] || !w->o_w[l] || !w->gate_up_w[l] || !w->down_w[l] || !w->in_norm_g[l] ||
         !w->post_norm_g[l] || !w->q_norm_g[l] || !w->k_norm_g[l])
       return fail(DFLASH_EINVAL, "a per-layer weight pointer is NULL (layer " + std::to_string(l) + ")");
+  // the FP8 store runs in the per-head epilogue that reads gains 8 bytes at a time
+  if (c.kv_fp8)
+    for (int l = 0; l < c.n_layers; ++l)
+      if ((uintptr_t)w->k_norm_g[l] % 8 || (uintptr_t)w->q_norm_g[l] % 8)
+        return fail(DFLASH_EINVAL, "q/k norm gains must be 8-byte aligned with an FP8 KV cache");
 
   dflash_handle *h = new dflash_handle();
   h->cfg = c;
@@ -491,7 +516,8 @@ int dflash_inject_context(dflash_handle *h, const dflash_kv *kv, int32_t batch, 
     if (!fused && (st = timed(h, "inject_prep", s, [&] {
                      return launch_inject_prep(batch, (int)r0, rows, row_offset, n_rows, kv->kv_len,
                                                kv->page_table, kv->pages_per_req, kv->n_pages,
-                                               c.page_size, c.max_position, slot, rpos, err, s);
+                                               c.page_size, c.max_position, kv->draft_window, slot,
+                                               rpos, err, s);
                    })))
       return st;
     // a1 + a2: concat (K-split over the selected layers) + fc; the epilogue
@@ -526,6 +552,11 @@ int dflash_inject_context(dflash_handle *h, const dflash_kv *kv, int32_t batch, 
         k.row_pos = rpos;
         k.row_slot = slot;
         k.rope = rope;
+        if (c.kv_fp8) {
+          k.kv_fp8 = 1;
+          k.k_scale = kv->k_scale[l];
+          k.v_scale = kv->v_scale[l];
+        }
         set_norm_in(h, k, ssq_y, c.max_rows);
         add_seg(Q, (const char *)h->qkv_w[l] + (size_t)q_rows * H * h->es, H, 2 * kvd, k);
       }
@@ -548,6 +579,7 @@ int dflash_inject_context(dflash_handle *h, const dflash_kv *kv, int32_t batch, 
     inj.row_slot = slot;
     inj.row_pos = rpos;
     inj.total_rows = total_rows;
+    inj.draft_window = kv->draft_window;
     inj.advance = r0 + rows >= total_rows && c.n_layers <= kMaxSeg;
     advanced = fused && inj.advance;
     // fc and the first group of layers' K/V in one launch
@@ -562,7 +594,7 @@ int dflash_inject_context(dflash_handle *h, const dflash_kv *kv, int32_t batch, 
   if (advanced) return DFLASH_OK;
   return timed(h, "inject_finalize", s, [&] {
     return launch_inject_finalize(batch, total_rows, row_offset, n_rows, kv->kv_len,
-                                  kv->pages_per_req * c.page_size, err, s);
+                                  (int)kv_capacity(h, kv), err, s);
   });
 }
 
@@ -681,6 +713,12 @@ static int draft_impl(dflash_handle *h, const dflash_kv *kv, int32_t batch,
     a.window = h->window[l];
     a.scale = 1.0f / sqrtf((float)D);
     a.err = err;
+    a.draft_window = kv->draft_window;
+    if (c.kv_fp8) {
+      a.fp8 = 1;
+      a.k_scale = kv->k_scale[l];
+      a.v_scale = kv->v_scale[l];
+    }
     if ((st = timed(h, "attention", s, [&] { return run_attention(h, a, s); }))) return st;
     // One launch for the rest of the layer and the start of the next:
     // a7 O-proj + residual (+ deferred post-attention norm), a8 gate/up with

@@ -174,13 +174,15 @@ __device__ void head_ops_d128(const EpiParams &e, const float *t0, int ldt, int 
     if (!act) continue;
     const int m = m0 + r;
     T *dst;
+    int64_t cache_off = 0;   // element offset of this head row in the cache
     if (qkv) {
       dst = kind == 0 ? (T *)e.q_out + (int64_t)m * e.n_heads * 128 + head * 128
                       : (T *)(kind == 1 ? e.k_out : e.v_out) + (int64_t)m * kvd + head * 128;
     } else {
       const int slot = s_slot[r];
       if (slot < 0) continue;
-      dst = (T *)(kind == 1 ? e.k_cache : e.v_cache) + (int64_t)slot * kvd + head * 128;
+      cache_off = (int64_t)slot * kvd + head * 128;
+      dst = (T *)(kind == 1 ? e.k_cache : e.v_cache) + cache_off;
     }
     if (nr) {
       const float rstd = rsqrtf(ss / 128.f + e.eps);
@@ -193,6 +195,17 @@ __device__ void head_ops_d128(const EpiParams &e, const float *t0, int ldt, int 
         lo[k] = a * cs_c[k] - b * cs_s[k];
         hi[k] = b * cs_c[k] + a * cs_s[k];
       }
+    }
+    if (!qkv && e.kv_fp8) {
+      // FP8 E4M3 cache (CSDN article, Kimi-K2.6 draft card: one byte per
+      // K/V element): the code of x / scale, four bytes per store
+      const float sc = kind == 1 ? e.k_scale : e.v_scale;
+      uint8_t *d8 = (uint8_t *)(kind == 1 ? e.k_cache : e.v_cache) + cache_off;
+      *reinterpret_cast<uint32_t *>(d8 + 4 * hl) =
+          e4m3x2(lo[0], lo[1], sc) | (e4m3x2(lo[2], lo[3], sc) << 16);
+      *reinterpret_cast<uint32_t *>(d8 + 64 + 4 * hl) =
+          e4m3x2(hi[0], hi[1], sc) | (e4m3x2(hi[2], hi[3], sc) << 16);
+      continue;
     }
     uint2 plo, phi;
     T *ql = reinterpret_cast<T *>(&plo), *qh = reinterpret_cast<T *>(&phi);

@@ -493,6 +493,7 @@ __device__ __forceinline__ InjectArgs inject_args(const ProgramInject &j) {
   a.n_pages = j.n_pages;
   a.page_size = j.page_size;
   a.max_position = j.max_position;
+  a.draft_window = j.draft_window;
   return a;
 }
 
@@ -894,7 +895,9 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
       // every CTA has read the old lengths (row map, phase 0) and is done
       const InjectArgs a = inject_args(p.inj);
       for (int b = threadIdx.x; b < p.inj.B; b += blockDim.x)
-        inject_advance(a, b, p.inj.total_rows, (int64_t)a.pages_per_req * a.page_size, p.err);
+        inject_advance(a, b, p.inj.total_rows,
+                       a.draft_window > 0 ? (int64_t)INT32_MAX : (int64_t)a.pages_per_req * a.page_size,
+                       p.err);
     }
     if (s_int[0] && p.fin.M > 0) {
       for (int m = threadIdx.x; m < p.fin.M; m += blockDim.x) {

@@ -66,6 +66,9 @@ struct EpiParams {
   unsigned long long *topk_keys;
   unsigned long long *topk_bound;
   int topk, topk_ld;
+  // EPI_KV_CACHE into an FP8 E4M3 cache: code of x / scale, one byte per element
+  int kv_fp8;
+  float k_scale, v_scale;
 };
 
 constexpr int kMaxSrc = 8;   // sources of the K-split A operand (selected layers)
@@ -103,6 +106,9 @@ struct AttnParams {
   int window;          // 0 = full
   float scale;
   unsigned int *err;
+  int draft_window;    // 0 = off; W > 0: the page table is a ring, keys below kv_len - W hidden
+  int fp8;             // context pages hold E4M3 codes: value = code * k_scale / v_scale
+  float k_scale, v_scale;
 };
 
 struct AttnScratch {
@@ -183,6 +189,7 @@ struct ProgramInject {
   int pages_per_req, n_pages, page_size, max_position;
   int *row_slot, *row_pos;
   int advance, total_rows;
+  int draft_window;             // 0: off; W > 0: ring page table (inject_rows.cuh)
 };
 
 // ProgramNorm: a GEMM-free phase placed just before a program's last GEMM.
@@ -233,8 +240,8 @@ cudaError_t launch_argmax_finalize(const unsigned long long *keys, const int *an
                                    int *draft_ids, cudaStream_t s);
 cudaError_t launch_inject_prep(int B, int row0, int rows, const int *row_offset, const int *n_rows,
                                const int *kv_len, const int *page_table, int pages_per_req,
-                               int n_pages, int page_size, int max_position, int *row_slot,
-                               int *row_pos, unsigned int *err, cudaStream_t s);
+                               int n_pages, int page_size, int max_position, int draft_window,
+                               int *row_slot, int *row_pos, unsigned int *err, cudaStream_t s);
 cudaError_t launch_inject_finalize(int B, int total_rows, const int *row_offset,
                                    const int *n_rows, int *kv_len, int capacity,
                                    unsigned int *err, cudaStream_t s);

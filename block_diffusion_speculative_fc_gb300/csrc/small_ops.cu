@@ -165,7 +165,7 @@ cudaError_t launch_argmax_finalize(const unsigned long long *keys, const int *an
 __global__ void inject_prep_kernel(int B, int row0, int rows, const int *__restrict__ row_offset,
                                    const int *__restrict__ n_rows, const int *__restrict__ kv_len,
                                    const int *__restrict__ page_table, int pages_per_req,
-                                   int n_pages, int page_size, int max_position,
+                                   int n_pages, int page_size, int max_position, int draft_window,
                                    int *__restrict__ row_slot, int *__restrict__ row_pos,
                                    unsigned int *err) {
   pdl_wait();
@@ -186,6 +186,7 @@ __global__ void inject_prep_kernel(int B, int row0, int rows, const int *__restr
   a.n_pages = n_pages;
   a.page_size = page_size;
   a.max_position = max_position;
+  a.draft_window = draft_window;
   int slot, pos;
   inject_map_row(a, row0 + local, [&](int b) { return s_len[b]; }, [&](int b) { return s_off[b]; },
                  [&](int b) { return s_n[b]; }, slot, pos, err);
@@ -195,13 +196,14 @@ __global__ void inject_prep_kernel(int B, int row0, int rows, const int *__restr
 
 cudaError_t launch_inject_prep(int B, int row0, int rows, const int *row_offset, const int *n_rows,
                                const int *kv_len, const int *page_table, int pages_per_req,
-                               int n_pages, int page_size, int max_position, int *row_slot,
-                               int *row_pos, unsigned int *err, cudaStream_t s) {
+                               int n_pages, int page_size, int max_position, int draft_window,
+                               int *row_slot, int *row_pos, unsigned int *err, cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
   const int thr = 256;
   return launch_pdl(inject_prep_kernel, dim3((rows + thr - 1) / thr), dim3(thr),
                     3 * B * sizeof(int), s, B, row0, rows, row_offset, n_rows, kv_len, page_table,
-                    pages_per_req, n_pages, page_size, max_position, row_slot, row_pos, err);
+                    pages_per_req, n_pages, page_size, max_position, draft_window, row_slot,
+                    row_pos, err);
 }
 
 // kv_len[b] += n_rows[b] (inject_rows.cuh).

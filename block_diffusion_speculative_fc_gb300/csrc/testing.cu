@@ -1,7 +1,9 @@
-// Test-only entry point: the tensor-core GEMM on its own (include/dflash_testing.h).
+// Test-only entry points: the tensor-core GEMM on its own, the FP8 encoder of
+// the K/V cache epilogue (include/dflash_testing.h).
 #include <cstring>
 
 #include "../../include/dflash_testing.h"
+#include "common.cuh"
 #include "kernels.h"
 
 using namespace dflash;
@@ -144,4 +146,25 @@ extern "C" int dflash_test_gemm_program_traced(int32_t n_phases, int32_t M, cons
       cudaSuccess)
     return DFLASH_ECUDA;
   return DFLASH_OK;
+}
+
+namespace {
+// The K/V cache epilogue's encoder (e4m3x2 in common.cuh) on n given values.
+__global__ void e4m3_encode_kernel(const float *__restrict__ x, int n, float scale,
+                                   uint8_t *__restrict__ codes) {
+  const int i = 2 * (blockIdx.x * blockDim.x + threadIdx.x);
+  if (i >= n) return;
+  const uint32_t c = e4m3x2(x[i], i + 1 < n ? x[i + 1] : 0.f, scale);
+  codes[i] = (uint8_t)(c & 0xFF);
+  if (i + 1 < n) codes[i + 1] = (uint8_t)(c >> 8);
+}
+}  // namespace
+
+extern "C" int dflash_test_e4m3_encode(const float *x, int32_t n, float scale, uint8_t *codes,
+                                       dflash_stream_t stream) {
+  if (n < 0 || (n > 0 && (!x || !codes)) || !(scale > 0.f)) return DFLASH_EINVAL;
+  if (n == 0) return DFLASH_OK;
+  const int pairs = (n + 1) / 2;
+  e4m3_encode_kernel<<<(pairs + 255) / 256, 256, 0, (cudaStream_t)stream>>>(x, n, scale, codes);
+  return cudaGetLastError() == cudaSuccess ? DFLASH_OK : DFLASH_ECUDA;
 }

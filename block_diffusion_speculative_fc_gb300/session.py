@@ -23,23 +23,40 @@ def _stream():
 
 
 class KVCache:
-    """Paged draft KV cache: per layer K and V pages [n_pages, 64, KVH, D]."""
+    """Paged draft KV cache: per layer K and V pages [n_pages, 64, KVH, D].
 
-    def __init__(self, cfg, batch, pages_per_req, page_table, dtype, device="cuda"):
+    fp8: the pages hold one-byte E4M3 codes (uint8 tensors) with the per-layer
+    scales k_scale / v_scale (sequences of n_layers floats).  draft_window W >
+    0: the page table is a ring of pages_per_req pages keeping the newest W
+    committed rows of each request (include/dflash.h, dflash_kv).
+    """
+
+    def __init__(self, cfg, batch, pages_per_req, page_table, dtype, device="cuda", fp8=False,
+                 k_scale=None, v_scale=None, draft_window=0):
         self.batch = batch
         self.pages_per_req = pages_per_req
         self.page_table = torch.as_tensor(page_table, dtype=torch.int32).to(device).contiguous()
         self.n_pages = int(self.page_table.max().item()) + 1 if self.page_table.numel() else 1
+        self.fp8 = bool(fp8)
+        self.draft_window = int(draft_window)
         shape = (self.n_pages, cfg.page_size, cfg.n_kv_heads, cfg.head_dim)
-        self.k = [torch.zeros(shape, dtype=dtype, device=device) for _ in range(cfg.n_layers)]
-        self.v = [torch.zeros(shape, dtype=dtype, device=device) for _ in range(cfg.n_layers)]
+        dt = torch.uint8 if self.fp8 else dtype
+        self.k = [torch.zeros(shape, dtype=dt, device=device) for _ in range(cfg.n_layers)]
+        self.v = [torch.zeros(shape, dtype=dt, device=device) for _ in range(cfg.n_layers)]
         self.kv_len = torch.zeros(batch, dtype=torch.int32, device=device)
         self._kp = _ptr_array(self.k)
         self._vp = _ptr_array(self.v)
+        n = cfg.n_layers
+        self.k_scale = list(k_scale) if k_scale is not None else [1.0] * n
+        self.v_scale = list(v_scale) if v_scale is not None else [1.0] * n
+        self._ks = (ctypes.c_float * n)(*self.k_scale)
+        self._vs = (ctypes.c_float * n)(*self.v_scale)
         self.struct = DflashKV(ctypes.cast(self._kp, ctypes.POINTER(ctypes.c_void_p)),
                                ctypes.cast(self._vp, ctypes.POINTER(ctypes.c_void_p)),
                                self.page_table.data_ptr(), pages_per_req, self.n_pages,
-                               self.kv_len.data_ptr())
+                               self.kv_len.data_ptr(), self.draft_window,
+                               ctypes.cast(self._ks, ctypes.POINTER(ctypes.c_float)),
+                               ctypes.cast(self._vs, ctypes.POINTER(ctypes.c_float)))
 
 
 class DraftSession:
@@ -49,9 +66,10 @@ class DraftSession:
     the layout of include/dflash.h (see synth.make_weights).
     """
 
-    def __init__(self, cfg, W, max_batch, max_rows, max_position):
+    def __init__(self, cfg, W, max_batch, max_rows, max_position, kv_fp8=False):
         self.cfg = cfg
         self.W = W
+        self.kv_fp8 = bool(kv_fp8)
         self.dtype = torch.float32 if cfg.dtype == "f32" else torch.bfloat16
         self._win = (ctypes.c_int32 * cfg.n_layers)(*cfg.sliding_window)
         self.c = DflashConfig(DFLASH_F32 if cfg.dtype == "f32" else DFLASH_BF16, cfg.target_hidden,
@@ -59,7 +77,8 @@ class DraftSession:
                               cfg.head_dim, cfg.intermediate, cfg.vocab, cfg.mask_token_id,
                               cfg.block_size, cfg.page_size,
                               ctypes.cast(self._win, ctypes.POINTER(ctypes.c_int32)),
-                              cfg.rms_eps, cfg.rope_theta, max_batch, max_rows, max_position)
+                              cfg.rms_eps, cfg.rope_theta, max_batch, max_rows, max_position,
+                              1 if self.kv_fp8 else 0)
         Ls = W["layers"]
         self._arrs = {k: _ptr_array([L[k] for L in Ls]) for k in
                       ["qkv", "o", "gate_up", "down", "in_norm", "post_norm", "q_norm", "k_norm"]}
@@ -88,8 +107,10 @@ class DraftSession:
         except Exception:
             pass
 
-    def new_kv(self, batch, pages_per_req, page_table):
-        return KVCache(self.cfg, batch, pages_per_req, page_table, self.dtype)
+    def new_kv(self, batch, pages_per_req, page_table, k_scale=None, v_scale=None,
+               draft_window=0):
+        return KVCache(self.cfg, batch, pages_per_req, page_table, self.dtype, fp8=self.kv_fp8,
+                       k_scale=k_scale, v_scale=v_scale, draft_window=draft_window)
 
     def inject(self, kv, feats, row_offset, n_rows, batch=None):
         """feats: [n_sel, rows, H_t] device tensor (or a list of n_sel [rows, H_t])."""

@@ -34,7 +34,8 @@
  *  - Matrices are row-major.  Weight matrices use the [out, in] layout of a
  *    linear layer (y = x W^T), i.e. the reduction dimension is contiguous.
  *  - Storage type of weights, features, K/V pages and the optional hidden
- *    output is the configured dtype (fp32 or bf16); ids are int32.
+ *    output is the configured dtype (fp32 or bf16); ids are int32.  With
+ *    kv_fp8 set, the K/V pages hold one-byte FP8 E4M3 codes instead.
  */
 #ifndef DFLASH_H
 #define DFLASH_H
@@ -86,6 +87,16 @@ typedef enum { DFLASH_F32 = 0, DFLASH_BF16 = 1 } dflash_dtype;
  *                  (larger calls are chunked); also bounds workspace size.
  *   max_position   positions (context + block) must stay below this; sizes
  *                  the RoPE table.
+ *   kv_fp8         0: the K/V pages hold the configured dtype.  1: they hold
+ *                  one-byte OCP FP8 E4M3 codes (CSDN article, Kimi-K2.6 draft
+ *                  card: "KV cache per token (FP8)" of 6 x 2 x 8 x 128 bytes =
+ *                  12 KiB, i.e. one byte per element and no per-token scale):
+ *                  element x of layer l's K (V) is stored as the E4M3 code
+ *                  nearest to x / k_scale[l] (x / v_scale[l]) -- IEEE float32
+ *                  division, ties to the even code, magnitudes beyond 448
+ *                  saturate to 448 -- and attention reads code value * scale.
+ *                  The scales are given per call in dflash_kv.  bf16
+ *                  configurations with head_dim 128 and block_size <= 16 only.
  * Supported: head_dim in {64, 128}; hidden, target_hidden, intermediate and
  * n_heads*head_dim multiples of 128; n_heads a multiple of n_kv_heads;
  * block_size in [2, 32]; (n_heads/n_kv_heads)*block_size <= 128.
@@ -110,6 +121,7 @@ typedef struct {
   int32_t max_batch;
   int32_t max_rows;
   int32_t max_position;
+  int32_t kv_fp8;
 } dflash_config;
 
 /*
@@ -148,13 +160,29 @@ typedef struct {
  * from projected target features, never from draft hidden states ("Inside
  * SGLang", Step 4: two K/V sources).
  *   k_pages/v_pages  HOST arrays [n_layers] of device pointers, each to
- *                    [n_pages, page_size, n_kv_heads, head_dim].
+ *                    [n_pages, page_size, n_kv_heads, head_dim] elements of
+ *                    the configured dtype (one byte each with kv_fp8).
  *   page_table       device int32 [batch, pages_per_req]: page of logical
  *                    position p of request b is page_table[b][p / page_size]
  *                    (logical positions and physical slots are distinct,
- *                    "Inside SGLang", Step 3).
+ *                    "Inside SGLang", Step 3); with a draft window, the page
+ *                    of p is page_table[b][(p / page_size) % pages_per_req].
  *   kv_len           device int32 [batch]: committed context rows.  Context
  *                    row i of request b has position i.
+ *   draft_window     0: every committed row is kept.  W > 0: draft KV
+ *                    windowing ("Inside SGLang", worker/memory section: "a
+ *                    private compact mapping over the shared global index
+ *                    space"; CSDN article, --speculative-dflash-draft-window-size):
+ *                    the cache keeps only the most recent W committed rows of
+ *                    each request, at their original positions, in a ring of
+ *                    pages_per_req pages (at least ceil(W / page_size) + 1);
+ *                    every block query sees exactly those rows and the block
+ *                    (a sliding layer still applies its own window on top);
+ *                    dflash_inject_context skips rows that fall out of the
+ *                    window within the same call.
+ *   k_scale/v_scale  HOST float arrays [n_layers] (read during the call),
+ *                    kv_fp8 only (else ignored, may be NULL): the per-layer
+ *                    scales of the FP8 codes (positive, finite).
  */
 typedef struct {
   void *const *k_pages;
@@ -163,6 +191,9 @@ typedef struct {
   int32_t pages_per_req;
   int32_t n_pages;
   int32_t *kv_len;
+  int32_t draft_window;
+  const float *k_scale;
+  const float *v_scale;
 } dflash_kv;
 
 typedef struct dflash_handle dflash_handle;

@@ -2,7 +2,8 @@
  * dflash_testing.h -- test-only entry point of libdflash.
  *
  * Runs the tensor-core GEMM of the library on its own so that it can be
- * compared with a plain matrix product; the draft pass never calls it.
+ * compared with a plain matrix product, and the FP8 encoder of the K/V cache
+ * on given values; the draft pass never calls these entries.
  */
 #ifndef DFLASH_TESTING_H
 #define DFLASH_TESTING_H
@@ -67,6 +68,13 @@ int dflash_test_gemm_program_traced(int32_t n_phases, int32_t M, const int32_t *
                                     const void *const *A, const void *const *W, const int32_t *op,
                                     void *const *out, void *scratch, size_t scratch_bytes,
                                     unsigned long long *trace, dflash_stream_t stream);
+
+/* The FP8 encoder of the K/V cache epilogue on its own: codes[i] = the OCP
+ * E4M3 code of x[i] / scale (IEEE float32 division, nearest code, ties to the
+ * even code, saturation at +-448), the same device function the injection
+ * epilogue calls.  x: device float32 [n]; codes: device uint8 [n]. */
+int dflash_test_e4m3_encode(const float *x, int32_t n, float scale, uint8_t *codes,
+                            dflash_stream_t stream);
 
 /* Fused launches of dependent GEMMs in the draft pass on (1) or off (0, one
  * launch per GEMM) for this handle. */

@@ -30,16 +30,53 @@ from synth import make_anchor, make_features, make_page_table, make_posterior, \
 MARGIN = 1e-2
 
 
-def gather_kv(kv, layer, b, n=None):
-    """Host copy of the first n committed rows of request b through the page
-    table: (K, V) [n, KVH, D] as float32."""
-    n = int(kv.kv_len[b].item()) if n is None else n
+def gather_kv(kv, layer, b, lo=0, hi=None):
+    """Host copy of the committed rows lo .. hi-1 of request b through the page
+    table (a ring when the cache has a draft window): (K, V) [n, KVH, D] --
+    float32 values, or the raw uint8 codes of an FP8 cache."""
+    hi = int(kv.kv_len[b].item()) if hi is None else hi
     page = kv.k[layer].shape[1]
-    pos = torch.arange(n, device=kv.page_table.device)
-    rows = kv.page_table[b, pos // page].long() * page + pos % page
+    pos = torch.arange(lo, hi, device=kv.page_table.device)
+    lp = pos // page
+    if kv.draft_window > 0:
+        lp = lp % kv.pages_per_req
+    rows = kv.page_table[b, lp].long() * page + pos % page
     kf = kv.k[layer].reshape(-1, *kv.k[layer].shape[2:])[rows]
     vf = kv.v[layer].reshape(-1, *kv.v[layer].shape[2:])[rows]
+    if kv.fp8:
+        return kf.cpu().numpy().astype(np.int64), vf.cpu().numpy().astype(np.int64)
     return kf.float().cpu(), vf.float().cpu()
+
+
+def fp8_scales(cfg):
+    """Per-layer FP8 scales of the tests: the magnitude each tensor reaches
+    (k-normed K is O(1); V has the spread of hidden_norm(y) W_v^T with
+    N(0, 0.02) weights) over the E4M3 maximum 448, different per layer and
+    not powers of two."""
+    vstd = 0.02 * np.sqrt(cfg.hidden)
+    k = [(4.5 + 0.37 * l) / 448.0 for l in range(cfg.n_layers)]
+    v = [(4.0 + 0.29 * l) * vstd / 448.0 for l in range(cfg.n_layers)]
+    return k, v
+
+
+def check_fp8_codes(codes, x_ref, scale, rel=0.02, max_rows=4096):
+    """GPU codes of a tensor whose oracle values are x_ref: every code must be
+    the E4M3 code of some value within rel * (row RMS) of x_ref / scale
+    (encode is monotone, so the allowed codes lie between the codes of the
+    interval's ends); returns the share of codes that differ from the
+    oracle's own code.  Long contexts are checked on max_rows evenly spaced
+    rows."""
+    if len(codes) > max_rows:
+        pick = np.linspace(0, len(codes) - 1, max_rows).astype(np.int64)
+        codes, x_ref = codes[pick], np.asarray(x_ref)[pick]
+    x = np.asarray(x_ref, dtype=np.float64) / scale
+    d = rel * np.sqrt(np.mean(x * x, axis=-1, keepdims=True)) + 1e-9
+    got = O.e4m3_decode(codes)
+    lo, hi = O.e4m3_decode(O.e4m3_encode(x - d)), O.e4m3_decode(O.e4m3_encode(x + d))
+    bad = ~((got >= lo) & (got <= hi))
+    assert not bad.any(), ("FP8 code outside the rounding interval", int(bad.sum()),
+                           np.argwhere(bad)[:5].tolist())
+    return float(np.mean(codes != O.e4m3_encode(x)))
 
 
 def to_numpy_weights(W):
@@ -65,7 +102,8 @@ def i32(a):
 class CycleRun:
     def __init__(self, cfg, batch, ctx_lens, cycles, seed=0, gains="unit", permuted=False,
                  check=None, match=("bernoulli", 0.85), tol=None, max_rows=None,
-                 extra_pages=2, W=None, Wn=None, pool=None, fused=None):
+                 extra_pages=2, W=None, Wn=None, pool=None, fused=None, fp8=False,
+                 draft_window=0):
         self.cfg, self.B, self.cycles, self.seed = cfg, batch, cycles, seed
         self.pool = pool   # prefill rows drawn from this many distinct feature rows
         self.ctx_lens = np.asarray(ctx_lens, dtype=np.int64)
@@ -76,15 +114,25 @@ class CycleRun:
         self.W = W if W is not None else make_weights(cfg, seed=seed, device="cuda", gains=gains)
         self.Wn = Wn if Wn is not None else to_numpy_weights(self.W)
         max_ctx = int(self.ctx_lens.max()) + (cycles + 1) * S
-        self.ppr = (max_ctx + 63) // 64 + extra_pages
+        self.fp8, self.draft_window = fp8, int(draft_window)
+        if self.draft_window > 0:
+            # a ring of ceil(W / 64) + 1 pages per request (+ extra) keeps the newest W rows
+            self.ppr = (self.draft_window + 63) // 64 + 1 + extra_pages
+        else:
+            self.ppr = (max_ctx + 63) // 64 + extra_pages
         self.page_table = make_page_table(batch, self.ppr, permuted, seed)
         rows_total = int(self.ctx_lens.sum())
         self.sess = pkg.DraftSession(cfg, self.W, max_batch=batch,
                                      max_rows=max_rows or max(rows_total, batch * S),
-                                     max_position=self.ppr * 64 + S)
+                                     max_position=((max_ctx + 63) // 64 + extra_pages) * 64 + S,
+                                     kv_fp8=fp8)
         if fused is not None:
             self.sess.set_fusion(fused)
-        self.kv = self.sess.new_kv(batch, self.ppr, self.page_table)
+        self.k_scale, self.v_scale = fp8_scales(cfg) if fp8 else (None, None)
+        self.kv = self.sess.new_kv(batch, self.ppr, self.page_table, self.k_scale, self.v_scale,
+                                   draft_window=self.draft_window)
+        self.stats_fp8 = []
+        self.ctx_q = {}
         self.ctx = {b: O.DraftContext(cfg) for b in self.check}
         self.stats = {"hidden_rel": [], "kv_rel": [], "id_near_tie": 0, "ids": 0,
                       "accept": [], "e2e_flips": []}
@@ -122,12 +170,67 @@ class CycleRun:
 
     def compare_kv(self, layers=None):
         for b in self.check:
+            if self.fp8:
+                self._sync_fp8(b)
+            n = self.ctx[b].kv_len
+            lo = max(0, n - self.draft_window) if self.draft_window > 0 else 0
             for l in (range(self.cfg.n_layers) if layers is None else layers):
-                k, v = gather_kv(self.kv, l, b)
-                rk = rel_l2(k.numpy(), self.ctx[b].k[l])
-                rv = rel_l2(v.numpy(), self.ctx[b].v[l])
+                k, v = gather_kv(self.kv, l, b, lo, n)
+                kr, vr = self.ctx[b].k[l][lo:n], self.ctx[b].v[l][lo:n]
+                if self.fp8:
+                    fk = check_fp8_codes(k, kr, self.k_scale[l])
+                    fv = check_fp8_codes(v, vr, self.v_scale[l])
+                    self.stats_fp8.append(max(fk, fv))
+                    k = O.e4m3_decode(k) * self.k_scale[l]
+                    v = O.e4m3_decode(v) * self.v_scale[l]
+                    kq, vq = self.ctx_q[b][l][0][lo:n], self.ctx_q[b][l][1][lo:n]
+                    rk, rv = rel_l2(k, kq), rel_l2(v, vq)
+                else:
+                    rk, rv = rel_l2(k.numpy(), kr), rel_l2(v.numpy(), vr)
                 self.stats["kv_rel"].append(max(rk, rv))
                 assert rk <= self.tol and rv <= self.tol, (b, l, rk, rv)
+
+    def _oracle_draft(self, b, anchor, own_fp8=False):
+        """The oracle's draft block of request b as the GPU's cache holds the
+        context: only the newest draft_window rows with a draft window, and
+        with an FP8 cache the stored codes times the per-layer scales.  The
+        codes are integers decided by floating point, so the lock-step run
+        takes the GPU's codes (checked against the oracle's encoder by
+        compare_kv); own_fp8 uses the oracle's own codes instead (reported)."""
+        ctx = self.ctx[b]
+        if self.fp8:
+            view = O.DraftContext(self.cfg)
+            if own_fp8:
+                self._sync_fp8(b)
+                view.k, view.v = [k for k, _ in self.ctx_q[b]], [v for _, v in self.ctx_q[b]]
+            else:
+                n = ctx.kv_len
+                lo = max(0, n - self.draft_window) if self.draft_window > 0 else 0
+                for l in range(self.cfg.n_layers):
+                    ck, cv = gather_kv(self.kv, l, b, lo, n)
+                    k = np.zeros((n,) + ck.shape[1:])
+                    v = np.zeros((n,) + cv.shape[1:])
+                    k[lo:] = O.e4m3_decode(ck) * self.k_scale[l]
+                    v[lo:] = O.e4m3_decode(cv) * self.v_scale[l]
+                    view.k[l], view.v[l] = k, v
+            ctx = view
+        if self.draft_window > 0:
+            return O.draft_block_windowed(self.cfg, self.Wn, anchor, ctx, self.draft_window)
+        return O.draft_block(self.cfg, self.Wn, anchor, ctx.layers(), ctx.kv_len)
+
+    def _sync_fp8(self, b):
+        """The oracle's FP8 cache of request b (DraftContext.layers_fp8 is
+        elementwise, so rows are quantised once, as they are appended)."""
+        ctx, q = self.ctx[b], self.ctx_q.setdefault(b, [])
+        if not q:
+            q.extend([np.zeros((0,) + k.shape[1:]), np.zeros((0,) + k.shape[1:])] for k in ctx.k)
+        n0 = q[0][0].shape[0]
+        if n0 == ctx.kv_len:
+            return
+        for l in range(self.cfg.n_layers):
+            kq, vq = O.fp8_kv(ctx.k[l][n0:], ctx.v[l][n0:], self.k_scale[l], self.v_scale[l])
+            q[l][0] = np.concatenate([q[l][0], kq])
+            q[l][1] = np.concatenate([q[l][1], vq])
 
     def run(self):
         cfg, B, S = self.cfg, self.B, self.cfg.block_size
@@ -148,11 +251,13 @@ class CycleRun:
             got = draft_d.cpu().numpy().astype(np.int64)
             draft_used = got.copy()
             for b in self.check:
-                ids, hid, margin = O.draft_block(cfg, self.Wn, int(anchor[b]), self.ctx[b].layers(),
-                                                 self.ctx[b].kv_len)
+                ids, hid, margin = self._oracle_draft(b, int(anchor[b]))
                 h_gpu = hid_d[b].double().cpu().numpy()
                 r = rel_l2(h_gpu, hid)
                 self.stats["hidden_rel"].append(r)
+                if self.fp8:
+                    _, hid_own, _ = self._oracle_draft(b, int(anchor[b]), own_fp8=True)
+                    self.stats.setdefault("hidden_rel_own_fp8", []).append(rel_l2(h_gpu, hid_own))
                 assert r <= self.tol, (c, b, r)
                 assert got[b, 0] == anchor[b]
                 # the argmax on the GPU's own operand, decided by the oracle
