@@ -66,6 +66,7 @@ struct Phase {
   int seg_half[kMaxSeg];          // pair: row offset of the "up" half
   int nseg, pair;
   int M, K, KB, m_tiles, tiles;
+  int bnt;                        // token rows per tile in this phase
   int k_per_src;
   int counter_off;                // this phase's tickets start here
   int G;                          // CTAs sharing this phase (<= gridDim.x, <= total_iters)
@@ -252,7 +253,7 @@ __device__ __forceinline__ int cta_of_iter(long long it, long long total, int G)
 // The scalars of a phase that the inner loops use, read once per phase into
 // registers.
 struct PhaseScalars {
-  int KB, k_per_src, m_tiles, nseg, pair, M, G;
+  int KB, k_per_src, m_tiles, nseg, pair, M, G, bnt;
   long long total;
   int seg_ntiles[kMaxSeg];
 };
@@ -265,6 +266,7 @@ __device__ __forceinline__ PhaseScalars load_scalars(const Phase &ph) {
   ps.pair = ph.pair;
   ps.M = ph.M;
   ps.G = ph.G;
+  ps.bnt = ph.bnt;
   ps.total = ph.total_iters;
 #pragma unroll
   for (int i = 0; i < kMaxSeg; ++i) ps.seg_ntiles[i] = ph.seg_ntiles[i];
@@ -274,7 +276,7 @@ __device__ __forceinline__ PhaseScalars load_scalars(const Phase &ph) {
 template <int BN>
 __device__ __forceinline__ void locate(const PhaseScalars &ps, int tile, int &seg, int &n0, int &m0) {
   int nt = tile / ps.m_tiles;
-  m0 = (tile - nt * ps.m_tiles) * BN;
+  m0 = (tile - nt * ps.m_tiles) * ps.bnt;
   seg = 0;
 #pragma unroll
   for (int i = 0; i < kMaxSeg - 1; ++i) {
@@ -292,7 +294,14 @@ struct Cfg {
   static constexpr int W_BYTES = 128 * BK * 2;
   static constexpr int A_BYTES = BN * BK * 2;
   static constexpr int SLOT_BYTES = W_BYTES + A_BYTES;
-  static constexpr int CH = BN < 32 ? BN : 32;            // epilogue token chunk
+  // SPLIT (256-token tiles with pairs in the program): a paired k-block takes
+  // one slot, [W_gate | W_up | activations of PT = 128 tokens], and its two
+  // 128-column accumulators fill one 256-column buffer; plain phases keep
+  // [W | activations of 256 tokens].  Smaller tiles pair two slots (the
+  // activation tile rides in the first).
+  static constexpr bool SPLIT = PAIRABLE && BN == 256;
+  static constexpr int PT = SPLIT ? BN / 2 : BN;          // token rows of a paired tile
+  static constexpr int CH = SPLIT ? 16 : (BN < 32 ? BN : 32);   // epilogue token chunk
   // stream-K merge area: shares of a (row chunk, half) of a split tile, one
   // bulk copy each.  The epilogue's fp32 staging tiles (one chunk per half)
   // live in it too: the last slot holds the gate half of a paired tile while
@@ -309,10 +318,10 @@ struct Cfg {
       (BUDGET - 1024 - MERGE_BYTES - BAR_BYTES) / SLOT_BYTES;
   static constexpr int SLOTS = SLOTS_RAW > 24 ? 24 : SLOTS_RAW;
   static constexpr int SMEM = 1024 + SLOTS * SLOT_BYTES + MERGE_BYTES + BAR_BYTES;
-  static constexpr int ACC_COLS = P * BN;                 // one accumulator buffer
+  static constexpr int ACC_COLS = SPLIT ? BN : P * BN;    // one accumulator buffer
   static constexpr int TMEM_COLS = 2 * ACC_COLS <= 32 ? 32 : (2 * ACC_COLS <= 64 ? 64 :
                                    (2 * ACC_COLS <= 128 ? 128 : (2 * ACC_COLS <= 256 ? 256 : 512)));
-  static_assert(SLOTS >= (PAIRABLE ? 4 : 3), "two k-blocks (paired: two slots each) must fit");
+  static_assert(SLOTS >= (PAIRABLE && !SPLIT ? 4 : 3), "two k-blocks (paired: two slots each) must fit");
   static_assert(MERGE_SLOTS >= P, "merge area: the staging tiles and, paired, one share");
   static_assert(2 * ACC_COLS <= 512, "accumulators exceed TMEM");
   static_assert(2 * SLOTS * 8 + 6 * 8 <= 496, "barrier region");
@@ -343,14 +352,37 @@ __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
-// MMAs of k-blocks kb0..kb1-1 of one tile into the accumulator at d0; NS
-// slots per k-block (2: a gate/up pair sharing the activation tile).  The
-// pair count is a compile-time constant so that the MMAs of a k-block issue
-// back to back (a run-time choice here measurably slowed every GEMM).
+// MMAs of k-blocks kb0..kb1-1 of one tile into the accumulator at d0.  NS
+// 1: one weight tile per slot; 2: a gate/up pair in two slots sharing the
+// activation tile of the first; 3: a gate/up pair in one slot (SPLIT
+// layout).  The pair layout is a compile-time constant so that the MMAs of a
+// k-block issue back to back (a run-time choice here measurably slowed every
+// GEMM).
 template <class C, int NS, int BN>
 __device__ __forceinline__ bool mma_kblocks(uint32_t &it, int kb0, int kb1, uint32_t d0,
                                             uint8_t *slots, uint64_t *full, uint64_t *empty,
                                             const Params &p) {
+  if constexpr (NS == 3) {
+    constexpr uint32_t idesc = idesc_bf16(128, C::PT);
+    for (int kb = kb0; kb < kb1; ++kb) {
+      const int s0 = it % C::SLOTS;
+      if (!mbar_wait(&full[s0], (it / C::SLOTS) & 1)) return false;
+      if (it == 0) stamp(p, 4);
+      tc_fence_after();
+      const uint32_t st0 = su32(slots + s0 * C::SLOT_BYTES);
+      const uint64_t gdesc = sw128_desc(st0), udesc = sw128_desc(st0 + C::W_BYTES);
+      const uint64_t adesc = sw128_desc(st0 + 2 * C::W_BYTES);
+#pragma unroll
+      for (int kk = 0; kk < BK / 16; ++kk) {
+        const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
+        umma_bf16(d0, gdesc + 2 * kk, adesc + 2 * kk, idesc, acc);
+        umma_bf16(d0 + C::PT, udesc + 2 * kk, adesc + 2 * kk, idesc, acc);
+      }
+      umma_commit(&empty[s0]);
+      it += 1;
+    }
+    return true;
+  }
   constexpr uint32_t idesc = idesc_bf16(128, BN);
   for (int kb = kb0; kb < kb1; ++kb) {
     const int s0 = it % C::SLOTS;
@@ -379,12 +411,13 @@ __device__ __forceinline__ bool mma_kblocks(uint32_t &it, int kb0, int kb1, uint
   return true;
 }
 // Activation tile of one k-block into slot s (K-split over the A sources).
-template <class C>
+template <class C, int NS>
 __device__ __forceinline__ void issue_a(const Phase &ph, const PhaseScalars &ps, uint8_t *slots,
                                         int s, int k, int m0, uint64_t *full, uint64_t pol) {
   const int src = k / ps.k_per_src;
-  tma_load_2d(slots + s * C::SLOT_BYTES + C::W_BYTES, &ph.tmA[src], &full[s],
-              k - src * ps.k_per_src, m0, pol);
+  constexpr int off = NS == 3 ? 2 * C::W_BYTES : C::W_BYTES;   // after the weight tile(s)
+  tma_load_2d(slots + s * C::SLOT_BYTES + off, &ph.tmA[src], &full[s], k - src * ps.k_per_src, m0,
+              pol);
 }
 // The activations of phase ph_i may be read: the preceding kernel (phase 0)
 // or every CTA's previous phase has written them.  false = the grid barrier
@@ -429,7 +462,7 @@ __device__ __forceinline__ bool produce_phase(const Params &p, const Phase &ph,
   if (left > 0) {
     locate<BN>(ps, tile, seg, n0, m0);
     tmw = &ph.tmW[seg];
-    if (NS == 2) half = ph.seg_half[seg];
+    if (NS >= 2) half = ph.seg_half[seg];
   }
   while (left > 0) {
     --left;
@@ -438,13 +471,14 @@ __device__ __forceinline__ bool produce_phase(const Params &p, const Phase &ph,
       ++tile;
       locate<BN>(ps, tile, seg, n0, m0);
       tmw = &ph.tmW[seg];
-      if (NS == 2) half = ph.seg_half[seg];
+      if (NS >= 2) half = ph.seg_half[seg];
     }
     const int k = kb * BK;
-    if (!ready && it + NS - it0 > (uint32_t)C::SLOTS) {
+    constexpr int SPK = NS == 2 ? 2 : 1;   // slots per k-block
+    if (!ready && it + SPK - it0 > (uint32_t)C::SLOTS) {
       const bool ok = phase_inputs_ready(p, ph_i, gridDim.x);
       for (int j = 0; j < npend; ++j)
-        issue_a<C>(ph, ps, slots, pend_s[j], pend_k[j], pend_m[j], full, pol_a);
+        issue_a<C, NS>(ph, ps, slots, pend_s[j], pend_k[j], pend_m[j], full, pol_a);
       npend = 0;
       ready = true;
       if (!ok) return false;
@@ -456,27 +490,34 @@ __device__ __forceinline__ bool produce_phase(const Params &p, const Phase &ph,
         !mbar_wait(&empty[(it + 1) % C::SLOTS], (((it + 1) / C::SLOTS) & 1) ^ 1))
       return false;
     const int s0 = it % C::SLOTS;
-    mbar_expect_tx(&full[s0], NS * C::W_BYTES + C::A_BYTES);
-    tma_load_2d(slots + s0 * C::SLOT_BYTES, tmw, &full[s0], k, n0, pol_w);
+    if (NS == 3) {
+      // [W_gate | W_up | activations of PT tokens] in one slot
+      mbar_expect_tx(&full[s0], 2 * C::W_BYTES + C::PT * BK * 2);
+      tma_load_2d(slots + s0 * C::SLOT_BYTES, tmw, &full[s0], k, n0, pol_w);
+      tma_load_2d(slots + s0 * C::SLOT_BYTES + C::W_BYTES, tmw, &full[s0], k, half + n0, pol_w);
+    } else {
+      mbar_expect_tx(&full[s0], NS * C::W_BYTES + C::A_BYTES);
+      tma_load_2d(slots + s0 * C::SLOT_BYTES, tmw, &full[s0], k, n0, pol_w);
+    }
     if (NS == 2) {
       const int s1 = (it + 1) % C::SLOTS;
       tma_load_2d(slots + s1 * C::SLOT_BYTES, tmw, &full[s0], k, half + n0, pol_w);
       mbar_arrive(&full[s1]);   // keeps the second slot's phase count in step
     }
     if (ready) {
-      issue_a<C>(ph, ps, slots, s0, k, m0, full, pol_a);
+      issue_a<C, NS>(ph, ps, slots, s0, k, m0, full, pol_a);
     } else {
       pend_s[npend] = s0;
       pend_k[npend] = k;
       pend_m[npend] = m0;
       ++npend;
     }
-    it += NS;
+    it += SPK;
   }
   if (!ready) {
     const bool ok = phase_inputs_ready(p, ph_i, gridDim.x);
     for (int j = 0; j < npend; ++j)
-      issue_a<C>(ph, ps, slots, pend_s[j], pend_k[j], pend_m[j], full, pol_a);
+      issue_a<C, NS>(ph, ps, slots, pend_s[j], pend_k[j], pend_m[j], full, pol_a);
     if (!ok) return false;
   }
   return true;
@@ -627,8 +668,9 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
         const Phase &ph = p.ph[ph_i];
         const PhaseScalars ps = load_scalars(ph);
         if constexpr (PAIRABLE)
-          ok = ps.pair ? produce_phase<C, 2, BN>(p, ph, ps, ph_i, cta, it, slots, full, empty,
-                                                 pend_s, pend_k, pend_m, pol_w, pol_a)
+          ok = ps.pair ? produce_phase<C, C::SPLIT ? 3 : 2, BN>(p, ph, ps, ph_i, cta, it, slots,
+                                                                full, empty, pend_s, pend_k,
+                                                                pend_m, pol_w, pol_a)
                        : produce_phase<C, 1, BN>(p, ph, ps, ph_i, cta, it, slots, full, empty,
                                                  pend_s, pend_k, pend_m, pol_w, pol_a);
         else
@@ -664,7 +706,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
           tc_fence_after();
           const uint32_t d0 = tmem + buf * C::ACC_COLS;
           if constexpr (PAIRABLE)
-            ok = ns == 2 ? mma_kblocks<C, 2, BN>(it, kb0, kb1, d0, slots, full, empty, p)
+            ok = ns == 2 ? mma_kblocks<C, C::SPLIT ? 3 : 2, BN>(it, kb0, kb1, d0, slots, full,
+                                                                 empty, p)
                          : mma_kblocks<C, 1, BN>(it, kb0, kb1, d0, slots, full, empty, p);
           else
             ok = mma_kblocks<C, 1, BN>(it, kb0, kb1, d0, slots, full, empty, p);
@@ -731,7 +774,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
         int seg, n0, m0;
         locate<BN>(ps, tile, seg, n0, m0);
         const EpiParams e = ph.epi[seg];
-        const int rows = min(BN, ps.M - m0);
+        const int bnt = ps.bnt;   // token rows of this phase's tiles
+        const int rows = min(bnt, ps.M - m0);
         const int buf = seg_i & 1;
         const uint32_t aph = (seg_i >> 1) & 1;
         // row scales of a deferred RMSNorm, computed while the MMAs still run
@@ -752,11 +796,11 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
         const uint32_t tacc = tmem + ((uint32_t)(quarter * 32) << 16) + buf * C::ACC_COLS;
         const bool whole = kb0 == 0 && kb1 == ps.KB;
         if (whole) {
-          for (int c0 = 0; c0 < BN; c0 += C::CH) {
+          for (int c0 = 0; c0 < bnt; c0 += C::CH) {
             float v[32];
             for (int q = 0; q < np; ++q) {
-              tmem_ld16(tacc + q * BN + c0, v);
-              if (C::CH == 32) tmem_ld16(tacc + q * BN + c0 + 16, v + 16);
+              tmem_ld16(tacc + q * bnt + c0, v);
+              if (C::CH == 32) tmem_ld16(tacc + q * bnt + c0 + 16, v + 16);
               float *dst = q ? st1 : st0;
 #pragma unroll
               for (int t = 0; t < C::CH; ++t) dst[t * 128 + f] = v[t];
@@ -781,14 +825,14 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
           if (cta != c_first) {
             const long long first_tile = R.b / ps.KB;
             const int which = tile == first_tile ? 0 : 1;
-            float *mine = p.partials + ((size_t)cta * 2 + which) * (C::P * BN * 128);
-            for (int c0 = 0; c0 < BN; c0 += C::CH) {
+            float *mine = p.partials + ((size_t)cta * 2 + which) * (C::ACC_COLS * 128);
+            for (int c0 = 0; c0 < bnt; c0 += C::CH) {
               float v[32];
               for (int q = 0; q < np; ++q) {
-                tmem_ld16(tacc + q * BN + c0, v);
-                if (C::CH == 32) tmem_ld16(tacc + q * BN + c0 + 16, v + 16);
+                tmem_ld16(tacc + q * bnt + c0, v);
+                if (C::CH == 32) tmem_ld16(tacc + q * bnt + c0 + 16, v + 16);
 #pragma unroll
-                for (int t = 0; t < C::CH; ++t) mine[(q * BN + c0 + t) * 128 + f] = v[t];
+                for (int t = 0; t < C::CH; ++t) mine[(q * bnt + c0 + t) * 128 + f] = v[t];
               }
             }
             tc_fence_before();
@@ -809,11 +853,11 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
             const int others = c_last - c_first;
             if (!epi_all(tid == 0 ? counter_wait(ticket, others) : true) && tid == 0)
               raise_error(p.err, DFLASH_DERR_TIMEOUT);
-            for (int c0 = 0; c0 < BN; c0 += C::CH) {
+            for (int c0 = 0; c0 < bnt; c0 += C::CH) {
               for (int q = 0; q < np; ++q) {
                 float acc[32];
-                tmem_ld16(tacc + q * BN + c0, acc);
-                if (C::CH == 32) tmem_ld16(tacc + q * BN + c0 + 16, acc + 16);
+                tmem_ld16(tacc + q * bnt + c0, acc);
+                if (C::CH == 32) tmem_ld16(tacc + q * bnt + c0 + 16, acc + 16);
                 // the up half's shares keep clear of the gate half's staging tile
                 const int mslots = q ? C::MERGE_SLOTS - 1 : C::MERGE_SLOTS;
                 for (int k0 = 0; k0 < others; k0 += mslots) {
@@ -828,8 +872,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
                       const long long cfirst_tile = (ps.total * c / ps.G) / ps.KB;
                       const int w = tile == cfirst_tile ? 0 : 1;
                       bulk_g2s(merge + k * (C::CHUNK_BYTES / 4),
-                               p.partials + ((size_t)c * 2 + w) * (C::P * BN * 128) +
-                                   (size_t)(q * BN + c0) * 128,
+                               p.partials + ((size_t)c * 2 + w) * (C::ACC_COLS * 128) +
+                                   (size_t)(q * bnt + c0) * 128,
                                C::CHUNK_BYTES, merge_bar);
                     }
                   }
@@ -977,19 +1021,21 @@ cudaError_t set_attr() {
                               cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
 }
 
-int pick_bn(int M, bool pair) {
-  int BN = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
-  if (pair && BN > 128) BN = 128;
-  return BN;
+int pick_bn(int M, bool) {
+  return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
 }
+// Token rows of a tile: a paired phase of a 256-token program uses the SPLIT
+// layout's 128-token tiles.
+int tile_rows(int BN, bool pair) { return pair && BN == 256 ? 128 : BN; }
 
 // One phase of a program from a problem description; returns its tile count.
 bool build_phase(tc::Phase &ph, const GemmProblem &P, int BN, int counter_off) {
   memset(&ph, 0, sizeof(ph));
   if (P.K % tc::BK || P.A.k_per_src % tc::BK) return false;
   const bool pair = P.seg[0].epi.op == EPI_SWIGLU;
+  const int bnt = tile_rows(BN, pair);
   for (int j = 0; j < P.A.n_src; ++j)
-    if (!encode_2d(&ph.tmA[j], P.A.ptr[j], (uint64_t)P.M, (uint64_t)P.A.k_per_src, (uint64_t)P.A.ld, BN))
+    if (!encode_2d(&ph.tmA[j], P.A.ptr[j], (uint64_t)P.M, (uint64_t)P.A.k_per_src, (uint64_t)P.A.ld, bnt))
       return false;
   int ntiles = 0;
   for (int i = 0; i < P.nseg; ++i) {
@@ -1007,7 +1053,8 @@ bool build_phase(tc::Phase &ph, const GemmProblem &P, int BN, int counter_off) {
   ph.M = P.M;
   ph.K = P.K;
   ph.KB = P.K / tc::BK;
-  ph.m_tiles = (P.M + BN - 1) / BN;
+  ph.bnt = bnt;
+  ph.m_tiles = (P.M + bnt - 1) / bnt;
   ph.tiles = ntiles * ph.m_tiles;
   ph.k_per_src = P.A.k_per_src;
   ph.counter_off = counter_off;
@@ -1023,8 +1070,8 @@ int gemm_tc_trace_slots() { return tc::kTraceSlots; }
 size_t gemm_tc_partials_bytes() { return (size_t)kTcMaxCtas * 2 * 256 * 128 * 4; }
 
 int gemm_tc_tiles(int n_tiles, int M, bool pair) {
-  const int BN = pick_bn(M, pair);
-  return n_tiles * ((M + BN - 1) / BN);
+  const int bnt = tile_rows(pick_bn(M, pair), pair);
+  return n_tiles * ((M + bnt - 1) / bnt);
 }
 
 int gemm_tc_num_sms() {
@@ -1044,6 +1091,7 @@ cudaError_t prepare_gemm_tc() {
   DFLASH_TC_ATTR(16, false) DFLASH_TC_ATTR(32, false) DFLASH_TC_ATTR(64, false)
   DFLASH_TC_ATTR(128, false) DFLASH_TC_ATTR(256, false) DFLASH_TC_ATTR(16, true)
   DFLASH_TC_ATTR(32, true) DFLASH_TC_ATTR(64, true) DFLASH_TC_ATTR(128, true)
+  DFLASH_TC_ATTR(256, true)
 #undef DFLASH_TC_ATTR
   return cudaSuccess;
 }
@@ -1118,6 +1166,7 @@ cudaError_t launch_gemm_program(const GemmProblem *probs, int n, float *partials
       case 32: return launch_cfg<32, true>(p, G, coop, s);
       case 64: return launch_cfg<64, true>(p, G, coop, s);
       case 128: return launch_cfg<128, true>(p, G, coop, s);
+      case 256: return launch_cfg<256, true>(p, G, coop, s);
     }
   } else {
     switch (BN) {

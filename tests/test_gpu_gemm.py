@@ -80,7 +80,7 @@ def test_gemm_k_split_sources(M):
     assert np.abs(out.cpu().numpy() - ref).max() / np.abs(ref).max() < 1e-5
 
 
-@pytest.mark.parametrize("M", [16, 48, 130])
+@pytest.mark.parametrize("M", [16, 48, 130, 385])
 def test_gemm_swiglu_pairs(M):
     g = torch.Generator(device="cuda").manual_seed(100 + M)
     I, K = 768, 1024
@@ -146,7 +146,7 @@ def _rel(got, ref):
     return np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30)
 
 
-@pytest.mark.parametrize("M", [1, 16, 37, 130])
+@pytest.mark.parametrize("M", [1, 16, 37, 130, 300, 600])
 def test_program_four_dependent_phases(M):
     """x -> bf16 y1 -> swiglu act -> bf16 y3 -> fp32 out, one cooperative launch;
     each phase is checked against a float64 product of the GPU's own input of
