@@ -197,6 +197,19 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
+// Each thread of the warp writes 16 consecutive 32-bit columns of its own TMEM lane.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float *v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15]))
+      : "memory");
+}
 __device__ __forceinline__ void stamp(const Params &p, int slot) {
   if (p.trace) {
     unsigned long long t;
@@ -302,6 +315,10 @@ struct Cfg {
   static constexpr bool SPLIT = PAIRABLE && BN == 256;
   static constexpr int PT = SPLIT ? BN / 2 : BN;          // token rows of a paired tile
   static constexpr int CH = SPLIT ? 16 : (BN < 32 ? BN : 32);   // epilogue token chunk
+  static constexpr int CH_PLAIN = SPLIT ? 32 : CH;        // ... of a plain phase
+  // large tiles: an owner adds the other shares into its TMEM accumulator
+  // with direct loads (a 256-token share does not fit the merge area)
+  static constexpr bool TMEM_MERGE = BN >= 128;
   // stream-K merge area: shares of a (row chunk, half) of a split tile, one
   // bulk copy each.  The epilogue's fp32 staging tiles (one chunk per half)
   // live in it too: the last slot holds the gate half of a paired tile while
@@ -607,6 +624,74 @@ __device__ __forceinline__ void program_norm(const ProgramNorm &q, int gwarp, in
   }
 }
 
+// The epilogue of a finished tile read from TMEM: CHc tokens at a time
+// through the fp32 staging tiles (the gate or only half at the end of the
+// merge area, the up half at its start).
+template <class C, int CHc, typename T>
+__device__ __forceinline__ void finish_tile(const EpiParams &e, uint32_t tacc, int bnt, int np,
+                                            int rows, int m0, int n0, int tid, int f, float *merge,
+                                            int *s_int, float *s_rstd) {
+  float *st0 = merge + (C::MERGE_BYTES - CHc * 128 * 4) / 4, *st1 = merge;
+  for (int c0 = 0; c0 < bnt; c0 += CHc) {
+    float v[CHc];
+    for (int q = 0; q < np; ++q) {
+      tmem_ld16(tacc + q * bnt + c0, v);
+      if (CHc == 32) tmem_ld16(tacc + q * bnt + c0 + 16, v + 16);
+      float *dst = q ? st1 : st0;
+#pragma unroll
+      for (int t = 0; t < CHc; ++t) dst[t * 128 + f] = v[t];
+    }
+    epi_bar();
+    if (c0 < rows)
+      run_epilogue<T>(e, st0, np == 2 ? st1 : nullptr, 128, m0 + c0, min(CHc, rows - c0), n0, tid,
+                      128, s_int, [] { epi_bar(); }, s_rstd + c0);
+    epi_bar();
+  }
+}
+
+// Owner of a split tile, large tiles: the other contributors' fp32 shares
+// are added, in CTA order (deterministic), to this CTA's accumulator in
+// TMEM -- 32 tokens and up to two shares per batch of loads, all in flight
+// together -- so the tile then finishes like an unsplit one.
+template <class C>
+__device__ __forceinline__ void tmem_merge(const Params &p, const PhaseScalars &ps, int tile,
+                                           int c_first, int others, uint32_t tacc, int bnt, int np,
+                                           int f) {
+  constexpr int GT = 32, KMAX = 2;
+  for (int q = 0; q < np; ++q) {
+    for (int g0 = 0; g0 < bnt; g0 += GT) {
+      float acc[GT];
+      tmem_ld16(tacc + q * bnt + g0, acc);
+      tmem_ld16(tacc + q * bnt + g0 + 16, acc + 16);
+      for (int k0 = 0; k0 < others; k0 += KMAX) {
+        float v[KMAX][GT];
+#pragma unroll
+        for (int kk = 0; kk < KMAX; ++kk) {
+          if (k0 + kk < others) {
+            const int c = c_first + 1 + k0 + kk;
+            const long long cfirst_tile = (ps.total * c / ps.G) / ps.KB;
+            const int w = tile == cfirst_tile ? 0 : 1;
+            const float *sh = p.partials + ((size_t)c * 2 + w) * (C::ACC_COLS * 128) +
+                              (size_t)(q * bnt + g0) * 128 + f;
+#pragma unroll
+            for (int t = 0; t < GT; ++t) v[kk][t] = __ldcg(sh + t * 128);
+          }
+        }
+#pragma unroll
+        for (int kk = 0; kk < KMAX; ++kk) {
+          if (k0 + kk < others) {
+#pragma unroll
+            for (int t = 0; t < GT; ++t) acc[t] += v[kk][t];
+          }
+        }
+      }
+      tmem_st16(tacc + q * bnt + g0, acc);
+      tmem_st16(tacc + q * bnt + g0 + 16, acc + 16);
+    }
+  }
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 template <int BN, bool PAIRABLE, typename T>
 __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_constant__ Params p) {
   using C = Cfg<BN, PAIRABLE>;
@@ -795,26 +880,9 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
         if (tid == 0 && seg_i == 0) stamp(p, 6);
         const uint32_t tacc = tmem + ((uint32_t)(quarter * 32) << 16) + buf * C::ACC_COLS;
         const bool whole = kb0 == 0 && kb1 == ps.KB;
-        if (whole) {
-          for (int c0 = 0; c0 < bnt; c0 += C::CH) {
-            float v[32];
-            for (int q = 0; q < np; ++q) {
-              tmem_ld16(tacc + q * bnt + c0, v);
-              if (C::CH == 32) tmem_ld16(tacc + q * bnt + c0 + 16, v + 16);
-              float *dst = q ? st1 : st0;
-#pragma unroll
-              for (int t = 0; t < C::CH; ++t) dst[t * 128 + f] = v[t];
-            }
-            epi_bar();
-            if (c0 < rows)
-              run_epilogue<T>(e, st0, np == 2 ? st1 : nullptr, 128, m0 + c0, min(C::CH, rows - c0),
-                              n0, tid, 128, s_int, [] { epi_bar(); }, s_rstd + c0);
-            epi_bar();
-          }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&acc_empty[buf]);
-        } else {
+        bool finish = whole;            // this CTA runs the tile's epilogue from TMEM
+        int *owner_ticket = nullptr;    // reset after that epilogue (merged in TMEM)
+        if (!whole) {
           // Split tile.  Its owner is the CTA holding the tile's first k-block:
           // the tile is the last segment of that CTA's range, so the owner
           // merges after all its other work.  Every other contributor
@@ -845,6 +913,16 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
               __threadfence();
               atomicAdd(ticket, 1);
             }
+          } else if (C::TMEM_MERGE) {
+            // Owner, large tiles: the other shares (every CTA is resident)
+            // are added into this CTA's accumulator, then the tile finishes
+            // like an unsplit one.
+            const int others = c_last - c_first;
+            if (!epi_all(tid == 0 ? counter_wait(ticket, others) : true) && tid == 0)
+              raise_error(p.err, DFLASH_DERR_TIMEOUT);
+            tmem_merge<C>(p, ps, tile, c_first, others, tacc, bnt, np, f);
+            finish = true;
+            owner_ticket = ticket;
           } else {
             // Owner: the other shares (every CTA is resident) come into the
             // merge area by bulk copy -- one memory round trip for up to
@@ -903,6 +981,17 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
             if (tid == 0) *ticket = 0;   // ready for the next launch
           }
           epi_bar();
+        }
+        if (finish) {
+          if (C::SPLIT && !ps.pair)
+            finish_tile<C, C::CH_PLAIN, T>(e, tacc, bnt, np, rows, m0, n0, tid, f, merge, s_int,
+                                           s_rstd);
+          else
+            finish_tile<C, C::CH, T>(e, tacc, bnt, np, rows, m0, n0, tid, f, merge, s_int, s_rstd);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[buf]);
+          if (owner_ticket && tid == 0) *owner_ticket = 0;   // ready for the next launch
         }
       }
       if (!alive) break;
