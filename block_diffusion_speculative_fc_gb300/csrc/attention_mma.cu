@@ -355,13 +355,21 @@ __device__ __forceinline__ void widen_block_f8(const uint8_t *blk, uint8_t *stag
 // issued before the predecessor kernel finished).  FP8: the caller has also
 // issued the block keys (issue_block_f8) when has_block; `buse` counts the
 // block region's uses (its barrier phase).
-template <bool FP8>
+// KS key groups: with KS = 2 (at most 32 query rows, i.e. two warps of
+// rows) the CTA runs twice the warps and warp group kg takes keys
+// 32 kg .. 32 kg + 31 of every tile; the two groups' partial softmax states
+// are merged at the end, so the caller sees the result in warps 0 .. RW-1.
+template <bool FP8, int KS>
 __device__ __forceinline__ bool attend(const Params &p, uint8_t *smem, uint64_t *full, uint32_t &use,
                                        uint32_t &buse, int b, int g, int kv, int first_page, int pg0,
                                        int pg1, bool has_block, Acc &a, int pre = 0) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int NT = 8 / KS;                 // 8-key n-tiles of a tile per warp
+  const int lane = threadIdx.x & 31;
   const int grp = lane >> 2, tig = lane & 3;
   const int S = p.S, R = p.R, G = p.n_heads / p.kvh;
+  const int RW = (R + 15) >> 4;              // warps of query rows
+  const int warp = (threadIdx.x >> 5) % RW, kg = (threadIdx.x >> 5) / RW;
+  const int key0 = kg * (KT / KS);           // first key of this warp's part of a tile
   const int nctx = max(0, pg1 - pg0);
   const int ntiles = nctx + (has_block ? 1 : 0);
   float(&o)[16][4] = a.o;
@@ -436,16 +444,16 @@ __device__ __forceinline__ bool attend(const Params &p, uint8_t *smem, uint64_t 
     // FP8 block tile: only its 16 rows are in the staging tile
     const bool short_tile = FP8 && blk;
     const int pos0 = (first_page + pg0 + t) * KT;   // position of key 0 of a context tile
-    // ---- S = Q K^T (16 rows x 64 keys per warp)
-    float s[8][4];
+    // ---- S = Q K^T (16 rows x 64 / KS keys per warp)
+    float s[NT][4];
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+    for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      if (short_tile && nt >= F8_BLK_ROWS / 8) continue;
+    for (int nt = 0; nt < NT; ++nt) {
+      if (short_tile && key0 + nt * 8 >= F8_BLK_ROWS) continue;
 #pragma unroll
       for (int kc = 0; kc < 4; ++kc) {          // 32 dims per ldmatrix.x4
-        const int key = nt * 8 + (lane & 7);
+        const int key = key0 + nt * 8 + (lane & 7);
         const int d = kc * 32 + (lane >> 3) * 8;
         const uint32_t addr = swz(kbase + (d >> 6) * (TILE_BYTES / 2), key, (d & 63) >> 3);
         uint32_t b0, b1, b2, b3;
@@ -468,7 +476,7 @@ __device__ __forceinline__ bool attend(const Params &p, uint8_t *smem, uint64_t 
       // every score finite: the scale folds into the exponent (one FMA), and
       // the accumulators are rescaled only when a row maximum of the warp moved
 #pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
+      for (int nt = 0; nt < NT; ++nt) {
         mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
         mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
       }
@@ -483,7 +491,7 @@ __device__ __forceinline__ bool attend(const Params &p, uint8_t *smem, uint64_t 
       m1 = mn1;
       float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
+      for (int nt = 0; nt < NT; ++nt) {
         s[nt][0] = exp2f(fmaf(s[nt][0], sl, -mn0));
         s[nt][1] = exp2f(fmaf(s[nt][1], sl, -mn0));
         s[nt][2] = exp2f(fmaf(s[nt][2], sl, -mn1));
@@ -504,10 +512,10 @@ __device__ __forceinline__ bool attend(const Params &p, uint8_t *smem, uint64_t 
       }
     } else {
 #pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
+      for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int key = nt * 8 + tig * 2 + (e & 1);
+          const int key = key0 + nt * 8 + tig * 2 + (e & 1);
           const bool row1 = e >= 2;
           bool vis;
           if (blk) {
@@ -533,7 +541,7 @@ __device__ __forceinline__ bool attend(const Params &p, uint8_t *smem, uint64_t 
       m1 = mn1;
       float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
+      for (int nt = 0; nt < NT; ++nt) {
         s[nt][0] = s[nt][0] == -INFINITY ? 0.f : exp2f(s[nt][0] - mn0);
         s[nt][1] = s[nt][1] == -INFINITY ? 0.f : exp2f(s[nt][1] - mn0);
         s[nt][2] = s[nt][2] == -INFINITY ? 0.f : exp2f(s[nt][2] - mn1);
@@ -554,8 +562,8 @@ __device__ __forceinline__ bool attend(const Params &p, uint8_t *smem, uint64_t 
     // ---- O += P V (P from the S accumulators, V via transposed ldmatrix);
     // FP8 context tiles: P carries the V factor, f16 operands
 #pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {              // 16 keys per step
-      if (short_tile && kk >= F8_BLK_ROWS / 16) continue;
+    for (int kk = 0; kk < NT / 2; ++kk) {         // 16 keys per step
+      if (short_tile && key0 + kk * 16 >= F8_BLK_ROWS) continue;
       uint32_t pa[4];
       if (FP8) {
         pa[0] = pack_f16(s[2 * kk][0] * vm, s[2 * kk][1] * vm);
@@ -570,7 +578,7 @@ __device__ __forceinline__ bool attend(const Params &p, uint8_t *smem, uint64_t 
       }
 #pragma unroll
       for (int np = 0; np < 8; ++np) {            // pairs of 8-dim n-tiles
-        const int key = kk * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+        const int key = key0 + kk * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
         const int d = np * 16 + (lane >> 4) * 8;
         const uint32_t addr = swz(vbase + (d >> 6) * (TILE_BYTES / 2), key, (d & 63) >> 3);
         uint32_t b0, b1, b2, b3;
@@ -595,6 +603,37 @@ __device__ __forceinline__ bool attend(const Params &p, uint8_t *smem, uint64_t 
   l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+  if (KS == 2) {
+    // the second key group's (O, m, l) through shared memory (the stage
+    // ring is idle: every issued tile has been consumed) into the first's
+    float *x = reinterpret_cast<float *>(smem) + ((size_t)warp * 32 + lane) * 68;
+    if (kg == 1) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        *reinterpret_cast<float4 *>(x + 4 * i) = make_float4(o[i][0], o[i][1], o[i][2], o[i][3]);
+      *reinterpret_cast<float4 *>(x + 64) = make_float4(m0, m1, l0, l1);
+    }
+    __syncthreads();
+    if (kg == 0) {
+      const float4 ml = *reinterpret_cast<const float4 *>(x + 64);
+      const float n0 = fmaxf(m0, ml.x), n1 = fmaxf(m1, ml.y);
+      const float a0 = n0 == -INFINITY ? 0.f : exp2f(m0 - n0), b0 = n0 == -INFINITY ? 0.f : exp2f(ml.x - n0);
+      const float a1 = n1 == -INFINITY ? 0.f : exp2f(m1 - n1), b1 = n1 == -INFINITY ? 0.f : exp2f(ml.y - n1);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float4 w = *reinterpret_cast<const float4 *>(x + 4 * i);
+        o[i][0] = o[i][0] * a0 + w.x * b0;
+        o[i][1] = o[i][1] * a0 + w.y * b0;
+        o[i][2] = o[i][2] * a1 + w.z * b1;
+        o[i][3] = o[i][3] * a1 + w.w * b1;
+      }
+      l0 = l0 * a0 + ml.z * b0;
+      l1 = l1 * a1 + ml.w * b1;
+      m0 = n0;
+      m1 = n1;
+    }
+    __syncthreads();   // the exchange area may be reused
+  }
   return ok;
 }
 
@@ -602,7 +641,7 @@ __device__ __forceinline__ bool attend(const Params &p, uint8_t *smem, uint64_t 
 // MAXT: threads per CTA this instantiation is built for; up to 128 threads
 // (G*S <= 64 query rows) three CTAs share an SM, which is what hides the
 // latency of the per-tile MMA/softmax chain.
-template <int MAXT, bool FP8>
+template <int MAXT, bool FP8, int KS>
 __global__ void __launch_bounds__(MAXT, MAXT <= 128 ? 3 : 1) attn_mma_kernel(const __grid_constant__ Params p) {
   pdl_wait();
   extern __shared__ uint8_t smem_raw[];
@@ -646,7 +685,7 @@ __global__ void __launch_bounds__(MAXT, MAXT <= 128 ? 3 : 1) attn_mma_kernel(con
 
     if (FP8 && has_block && threadIdx.x == 0) issue_block_f8(p, smem, full, b, g);
     Acc acc;
-    attend<FP8>(p, smem, full, use, buse, b, g, kv, first_page, pg0, pg1, has_block, acc);
+    attend<FP8, KS>(p, smem, full, use, buse, b, g, kv, first_page, pg0, pg1, has_block, acc);
     const int r0 = warp * 16 + grp, r1 = r0 + 8;
     float(&o)[16][4] = acc.o;
     const float m0 = acc.m0, m1 = acc.m1, l0 = acc.l0, l1 = acc.l1;
@@ -733,7 +772,7 @@ __global__ void __launch_bounds__(MAXT, MAXT <= 128 ? 3 : 1) attn_mma_kernel(con
 // the r-th of C equal slices of the context pages (the last rank also the
 // block keys), then the C partial results are merged through distributed
 // shared memory -- no scratch in global memory, no tickets, no prep kernel.
-template <bool FP8>
+template <bool FP8, int KS>
 __global__ void __launch_bounds__(256) attn_cluster_kernel(const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -768,7 +807,7 @@ __global__ void __launch_bounds__(256) attn_cluster_kernel(const __grid_constant
   if (FP8 && rank == C - 1 && threadIdx.x == 0) issue_block_f8(p, smem, full, b, g);
   uint32_t use = 0, buse = 0;
   Acc acc;
-  attend<FP8>(p, smem, full, use, buse, b, g, kv, first_page, pg0, pg1, rank == C - 1, acc, pre);
+  attend<FP8, KS>(p, smem, full, use, buse, b, g, kv, first_page, pg0, pg1, rank == C - 1, acc, pre);
   // this CTA's partial (unnormalised O, row max, row sum) into its own shared memory;
   // the stage ring is free: attend() ends every tile with a CTA barrier
   float *po = reinterpret_cast<float *>(smem);                    // [R][128]
@@ -879,21 +918,26 @@ size_t attention_mma_scratch_items(int max_batch, int kvh) {
 }
 
 cudaError_t prepare_attention_mma() {
-  const void *kernels[] = {(const void *)att::attn_mma_kernel<128, false>,
-                           (const void *)att::attn_mma_kernel<256, false>,
-                           (const void *)att::attn_mma_kernel<128, true>,
-                           (const void *)att::attn_mma_kernel<256, true>,
-                           (const void *)att::attn_cluster_kernel<false>,
-                           (const void *)att::attn_cluster_kernel<true>};
+  const void *kernels[] = {(const void *)att::attn_mma_kernel<128, false, 1>,
+                           (const void *)att::attn_mma_kernel<128, false, 2>,
+                           (const void *)att::attn_mma_kernel<256, false, 1>,
+                           (const void *)att::attn_mma_kernel<128, true, 1>,
+                           (const void *)att::attn_mma_kernel<128, true, 2>,
+                           (const void *)att::attn_mma_kernel<256, true, 1>};
   for (const void *k : kernels) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, att::SMEM);
     if (e != cudaSuccess) return e;
   }
-  cudaError_t e = cudaFuncSetAttribute((const void *)att::attn_cluster_kernel<false>,
-                                       cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute((const void *)att::attn_cluster_kernel<true>,
-                              cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  const void *clusters[] = {(const void *)att::attn_cluster_kernel<false, 1>,
+                            (const void *)att::attn_cluster_kernel<false, 2>,
+                            (const void *)att::attn_cluster_kernel<true, 1>,
+                            (const void *)att::attn_cluster_kernel<true, 2>};
+  for (const void *k : clusters) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, att::SMEM);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 namespace {
@@ -915,7 +959,7 @@ bool cluster_fits(int C, int warps) {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int n = 0;
-    k = (cudaOccupancyMaxActiveClusters(&n, att::attn_cluster_kernel<false>, &cfg) == cudaSuccess && n > 0)
+    k = (cudaOccupancyMaxActiveClusters(&n, att::attn_cluster_kernel<false, 1>, &cfg) == cudaSuccess && n > 0)
             ? 1 : -1;
     cudaGetLastError();
   }
@@ -927,7 +971,9 @@ cudaError_t launch_attention_mma(const AttnParams &a, const AttnScratch &w, cuda
   if (a.B <= 0) return cudaSuccess;
   if (a.head_dim != 128 || a.page_size != att::KT) return cudaErrorInvalidValue;
   const int R = (a.n_heads / a.n_kv_heads) * a.S;
-  const int warps = (R + 15) / 16;
+  // at most 32 query rows: two key groups per CTA (twice the warps)
+  const int ks = R <= 32 ? 2 : 1;
+  const int warps = (R + 15) / 16 * ks;
   if (warps > 8) return cudaErrorInvalidValue;
   if (a.fp8 && a.S > att::F8_BLK_ROWS) return cudaErrorInvalidValue;
   att::Params p;
@@ -985,8 +1031,11 @@ cudaError_t launch_attention_mma(const AttnParams &a, const AttnScratch &w, cuda
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return a.fp8 ? cudaLaunchKernelEx(&cfg, att::attn_cluster_kernel<true>, p)
-                 : cudaLaunchKernelEx(&cfg, att::attn_cluster_kernel<false>, p);
+    if (a.fp8)
+      return ks == 2 ? cudaLaunchKernelEx(&cfg, att::attn_cluster_kernel<true, 2>, p)
+                     : cudaLaunchKernelEx(&cfg, att::attn_cluster_kernel<true, 1>, p);
+    return ks == 2 ? cudaLaunchKernelEx(&cfg, att::attn_cluster_kernel<false, 2>, p)
+                   : cudaLaunchKernelEx(&cfg, att::attn_cluster_kernel<false, 1>, p);
   }
   const int max_items = (int)attention_mma_scratch_items(a.B, a.n_kv_heads);
   const int per_sm = warps <= 4 ? 3 : 1;   // resident CTAs per SM (shared memory / registers)
@@ -1002,11 +1051,14 @@ cudaError_t launch_attention_mma(const AttnParams &a, const AttnScratch &w, cuda
   p.tickets = w.tickets;
   p.max_items = max_items;
   const dim3 grid(per_sm * sms), block(warps * 32);
-  if (a.fp8)
-    return warps <= 4 ? launch_pdl(att::attn_mma_kernel<128, true>, grid, block, att::SMEM, s, p)
-                      : launch_pdl(att::attn_mma_kernel<256, true>, grid, block, att::SMEM, s, p);
-  return warps <= 4 ? launch_pdl(att::attn_mma_kernel<128, false>, grid, block, att::SMEM, s, p)
-                    : launch_pdl(att::attn_mma_kernel<256, false>, grid, block, att::SMEM, s, p);
+  if (a.fp8) {
+    if (ks == 2) return launch_pdl(att::attn_mma_kernel<128, true, 2>, grid, block, att::SMEM, s, p);
+    return warps <= 4 ? launch_pdl(att::attn_mma_kernel<128, true, 1>, grid, block, att::SMEM, s, p)
+                      : launch_pdl(att::attn_mma_kernel<256, true, 1>, grid, block, att::SMEM, s, p);
+  }
+  if (ks == 2) return launch_pdl(att::attn_mma_kernel<128, false, 2>, grid, block, att::SMEM, s, p);
+  return warps <= 4 ? launch_pdl(att::attn_mma_kernel<128, false, 1>, grid, block, att::SMEM, s, p)
+                    : launch_pdl(att::attn_mma_kernel<256, false, 1>, grid, block, att::SMEM, s, p);
 }
 
 }  // namespace dflash
