@@ -20,12 +20,11 @@
 // ticket) merges the splits in split order and writes the output.
 // FP8 cache (CSDN article, Kimi-K2.6 draft card: one byte per K/V element):
 // a context tile is one 8 KB box of E4M3 codes per tensor; all threads widen
-// it into a 16-bit staging tile before the MMAs.  An E4M3 byte shifted into
-// the bit layout of an f16 is exactly that code's value times 2^-8
-// (subnormals and zero included), so the widening is a few integer ops and
-// the MMAs run in f16 (Q rounded to f16 once per item); the factors 2^8 *
-// k_scale and 2^8 * v_scale fold into the softmax scale and into P.  The S
-// block keys stay bf16 (16-row boxes), widened to f16 the same way.
+// it into a 16-bit staging tile before the MMAs: every E4M3 value is exact
+// in f16 (the hardware conversion, two codes per instruction), so the MMAs
+// run in f16 (Q rounded to f16 once per item) and k_scale / v_scale fold
+// into the softmax scale and into P.  The S block keys stay bf16 (16-row
+// boxes), converted to f16 in the staging tile.
 // Draft KV windowing: the page table is a ring (page of logical page lp is
 // page_table[b][lp % pages_per_req]) and keys below kv_len - W are hidden.
 #include <cuda.h>
@@ -81,7 +80,7 @@ struct Params {
   int B, S, n_heads, kvh, pages_per_req, n_pages, window, R, max_items;
   float scale_log2;              // log2(e) / sqrt(D)
   int draft_window;              // 0 = off; W > 0: ring page table, keys below kv_len - W hidden
-  float k_mul, v_mul;            // FP8: 2^8 * k_scale, 2^8 * v_scale
+  float k_mul, v_mul;            // FP8: k_scale, v_scale
 };
 
 // First visible context position of query row j (of a request with kv
@@ -164,12 +163,14 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&v);
 }
-// Two E4M3 codes (bytes 0, 1 of w, or bytes 2, 3 with hi) as an f16 pair
-// whose values are the codes' values times 2^-8: the sign bit moves to bit
-// 15 and the 7 exponent/mantissa bits to bits 7..13 of each half.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2_scaled(uint32_t w, bool hi) {
-  const uint32_t t = __byte_perm(w, 0u, hi ? 0x3424u : 0x1404u);   // bytes at 8..15 and 24..31
-  return (t & 0x80008000u) | ((t >> 1) & 0x3F803F80u);
+// Two E4M3 codes (bytes 0, 1 of w, or bytes 2, 3 with hi) as the f16 pair
+// of their values (exact: every E4M3 value is an f16), lower byte in the
+// lower half.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w, bool hi) {
+  const uint16_t pair = (uint16_t)(hi ? (w >> 16) : (w & 0xFFFFu));
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(pair));
+  return r;
 }
 // bf16 pair -> f16 pair (round to nearest)
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
@@ -312,7 +313,7 @@ __device__ __forceinline__ void issue_block_f8(const Params &p, uint8_t *smem, u
 
 // FP8: E4M3 codes of stage `st` (K and V, 64 rows of 128 bytes, 128-byte
 // swizzle) -> the f16 staging tile (two boxes of 64 dims per tensor, the same
-// layout as a bf16 tile), values times 2^-8.  A 16-byte chunk of codes (dims
+// layout as a bf16 tile).  A 16-byte chunk of codes (dims
 // 16c .. 16c+15 of one row) becomes two 16-byte chunks in box c / 4.
 __device__ __forceinline__ void widen_f8(const uint8_t *st, uint8_t *staging) {
   for (int idx = threadIdx.x; idx < 2 * KT * 8; idx += blockDim.x) {
@@ -320,14 +321,14 @@ __device__ __forceinline__ void widen_f8(const uint8_t *st, uint8_t *staging) {
     const uint4 w = *reinterpret_cast<const uint4 *>(st + tensor * F8_TILE + row * 128 +
                                                       (((c ^ row) & 7) << 4));
     uint4 lo, hi;
-    lo.x = e4m3x2_to_f16x2_scaled(w.x, false);
-    lo.y = e4m3x2_to_f16x2_scaled(w.x, true);
-    lo.z = e4m3x2_to_f16x2_scaled(w.y, false);
-    lo.w = e4m3x2_to_f16x2_scaled(w.y, true);
-    hi.x = e4m3x2_to_f16x2_scaled(w.z, false);
-    hi.y = e4m3x2_to_f16x2_scaled(w.z, true);
-    hi.z = e4m3x2_to_f16x2_scaled(w.w, false);
-    hi.w = e4m3x2_to_f16x2_scaled(w.w, true);
+    lo.x = e4m3x2_to_f16x2(w.x, false);
+    lo.y = e4m3x2_to_f16x2(w.x, true);
+    lo.z = e4m3x2_to_f16x2(w.y, false);
+    lo.w = e4m3x2_to_f16x2(w.y, true);
+    hi.x = e4m3x2_to_f16x2(w.z, false);
+    hi.y = e4m3x2_to_f16x2(w.z, true);
+    hi.z = e4m3x2_to_f16x2(w.w, false);
+    hi.w = e4m3x2_to_f16x2(w.w, true);
     uint8_t *box = staging + tensor * TILE_BYTES + (c >> 2) * (TILE_BYTES / 2) + row * 128;
     const int c0 = (c & 3) * 2;
     *reinterpret_cast<uint4 *>(box + (((c0 ^ row) & 7) << 4)) = lo;
@@ -1008,8 +1009,8 @@ cudaError_t launch_attention_mma(const AttnParams &a, const AttnScratch &w, cuda
   p.R = R;
   p.scale_log2 = 1.4426950408889634f * a.scale;
   p.draft_window = a.draft_window;
-  p.k_mul = 256.f * a.k_scale;   // widened codes carry a factor 2^-8
-  p.v_mul = 256.f * a.v_scale;
+  p.k_mul = a.k_scale;
+  p.v_mul = a.v_scale;
   // Few (request, head) pairs: a cluster of C CTAs per pair, merged on chip.
   const int pairs = a.B * a.n_kv_heads;
   if (4 * pairs <= 2 * sms) {

@@ -26,6 +26,13 @@ namespace dflash {
 
 constexpr int kEpiMaxRows = 32;
 
+// Bring a line into L1 ahead of its use: the epilogues touch a row of global
+// memory per item, and issuing every line of a chunk first turns one memory
+// round trip per item into one per chunk, with no registers held meanwhile.
+__device__ __forceinline__ void prefetch_l1(const void *p) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+
 // Rotate-half RoPE on one head held by a warp (component i pairs with
 // i + D/2), optionally preceded by a per-head RMSNorm.  g_lo/g_hi: this lane's
 // gains for i = lane + 32k and i + D/2; cs: this lane's (cos, sin).
@@ -155,6 +162,11 @@ __device__ void head_ops_d128(const EpiParams &e, const float *t0, int ldt, int 
       ghi[k] = to_f32(pb[k]);
     }
   }
+  // the RoPE rows of this warp's rows (512 bytes each, four lines) go to L1
+  // before any is used
+  if (nr && (hl & 3) == 0)
+    for (int r = 2 * warp + hw; r < rows; r += 2 * nwarps)
+      prefetch_l1(e.rope + (int64_t)s_pos[r] * 64 + 4 * hl);
   // whole warps iterate together (the norm shuffles over 16 lanes)
   for (int rb = 2 * warp; rb < rows; rb += 2 * nwarps) {
     const int r = rb + hw;
@@ -276,6 +288,10 @@ __device__ __forceinline__ bool elementwise_vec(const EpiParams &e, const float 
   if (norm_out && ((uintptr_t)e.norm_gain & 15)) return false;
   const int total = rows << 4;
   const int lane = tid & 31;
+  if (op == EPI_RESID || op == EPI_RESID_NORM)   // residual rows to L1 first (4 items a line)
+    for (int it = tid; it < total; it += nthreads)
+      if ((it & 3) == 0)
+        prefetch_l1(e.out_f32 + (int64_t)(m0 + (it >> 4)) * e.ld + n0 + ((it & 15) << 3));
   // whole warps iterate together (the row reduction shuffles); an item past
   // the end belongs to a 16-lane group that is past the end as a whole
   for (int it = tid; it - lane < total; it += nthreads) {
