@@ -239,26 +239,23 @@ __device__ void head_ops_d128(const EpiParams &e, const float *t0, int ldt, int 
 constexpr int kEpiScratchInts = 3 * kEpiMaxRows;
 
 // Row scales 1/sqrt(sum_t ssq[t][m] / H + eps) of the deferred RMSNorm for
-// rows m0 .. m0+rows-1 into rstd[0..rows): one warp per row, lanes over the
-// slots, every load of a warp issued before the reductions.
+// rows m0 .. m0+rows-1 into rstd[0..rows): a thread per row, the slots of a
+// row summed in four interleaved chains, every load issued before the sums
+// (consecutive threads read consecutive rows of a slot: coalesced).
 __device__ __forceinline__ void compute_rstd(const EpiParams &e, int m0, int rows, float *rstd,
                                              int lane, int warp, int nwarps) {
-  constexpr int U = 8;
-  for (int r0 = warp; r0 < rows; r0 += U * nwarps) {
-    float acc[U];
+  const int nthr = nwarps * 32;
+  for (int r = warp * 32 + lane; r < rows; r += nthr) {
+    const float *p = e.ssq_in + m0 + r;
+    float a[4] = {0.f, 0.f, 0.f, 0.f};
+    int q = 0;
+#pragma unroll 8
+    for (; q + 4 <= e.ssq_parts; q += 4) {
 #pragma unroll
-    for (int k = 0; k < U; ++k) {
-      const int r = r0 + k * nwarps;
-      acc[k] = 0.f;
-      if (r < rows)
-        for (int q = lane; q < e.ssq_parts; q += 32) acc[k] += e.ssq_in[(int64_t)q * e.ssq_ld + m0 + r];
+      for (int k = 0; k < 4; ++k) a[k] += p[(int64_t)(q + k) * e.ssq_ld];
     }
-#pragma unroll
-    for (int k = 0; k < U; ++k) {
-      const int r = r0 + k * nwarps;
-      const float t = warp_sum(acc[k]);
-      if (lane == 0 && r < rows) rstd[r] = rsqrtf(t * e.inv_h + e.norm_eps);
-    }
+    for (; q < e.ssq_parts; ++q) a[0] += p[(int64_t)q * e.ssq_ld];
+    rstd[r] = rsqrtf(((a[0] + a[1]) + (a[2] + a[3])) * e.inv_h + e.norm_eps);
   }
 }
 
