@@ -135,7 +135,7 @@ __device__ void head_ops(const EpiParams &e, const float *t0, int ldt, int m0, i
 template <typename T>
 __device__ void head_ops_d128(const EpiParams &e, const float *t0, int ldt, int m0, int rows,
                               int n0, int lane, int warp, int nwarps, const int *s_pos,
-                              const int *s_slot) {
+                              const int *s_slot, const float *rs) {
   if (n0 >= e.N) return;
   const int kvd = e.n_kv_heads * 128;
   const bool qkv = e.op == EPI_QKV;
@@ -175,8 +175,9 @@ __device__ void head_ops_d128(const EpiParams &e, const float *t0, int ldt, int 
     if (act) {
       const float4 a = *reinterpret_cast<const float4 *>(t0 + r * ldt + 4 * hl);
       const float4 b = *reinterpret_cast<const float4 *>(t0 + r * ldt + 64 + 4 * hl);
-      lo[0] = a.x; lo[1] = a.y; lo[2] = a.z; lo[3] = a.w;
-      hi[0] = b.x; hi[1] = b.y; hi[2] = b.z; hi[3] = b.w;
+      const float sc = rs ? rs[r] : 1.f;   // the deferred RMSNorm's row scale
+      lo[0] = a.x * sc; lo[1] = a.y * sc; lo[2] = a.z * sc; lo[3] = a.w * sc;
+      hi[0] = b.x * sc; hi[1] = b.y * sc; hi[2] = b.z * sc; hi[3] = b.w * sc;
     }
     float ss = 0.f;
 #pragma unroll
@@ -268,7 +269,7 @@ __device__ __forceinline__ void compute_rstd(const EpiParams &e, int m0, int row
 template <typename T>
 __device__ __forceinline__ bool elementwise_vec(const EpiParams &e, const float *t0,
                                                 const float *t1, int ldt, int m0, int rows,
-                                                int n0, int tid, int nthreads) {
+                                                int n0, int tid, int nthreads, const float *rs) {
   const int op = e.op;
   if (op != EPI_STORE_F32 && op != EPI_RESID && op != EPI_STORE_ACT && op != EPI_SWIGLU &&
       op != EPI_RESID_NORM && op != EPI_STORE_NORM)
@@ -299,13 +300,16 @@ __device__ __forceinline__ bool elementwise_vec(const EpiParams &e, const float 
       const float4 *src = reinterpret_cast<const float4 *>(t0 + r * ldt + c8);
       const float4 a = src[0], b = src[1];
       float y[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+      const float sc = rs ? rs[r] : 1.f;   // the deferred RMSNorm's row scale
+#pragma unroll
+      for (int k = 0; k < 8; ++k) y[k] *= sc;
       const int64_t o = (int64_t)(m0 + r) * e.ld + n0 + c8;
       if (op == EPI_SWIGLU) {
         const float4 *u = reinterpret_cast<const float4 *>(t1 + r * ldt + c8);
         const float4 ua = u[0], ub = u[1];
         const float up[8] = {ua.x, ua.y, ua.z, ua.w, ub.x, ub.y, ub.z, ub.w};
 #pragma unroll
-        for (int k = 0; k < 8; ++k) y[k] = silu(y[k]) * up[k];
+        for (int k = 0; k < 8; ++k) y[k] = silu(y[k]) * (up[k] * sc);
       }
       if (op == EPI_RESID || op == EPI_RESID_NORM) {
         const float4 *old = reinterpret_cast<const float4 *>(e.out_f32 + o);
@@ -354,16 +358,26 @@ __device__ void run_epilogue(const EpiParams &e, float *t0, float *t1, int ldt, 
                              int n0, int tid, int nthreads, int *s_int, Sync sync,
                              const float *rstd_pre = nullptr) {
   const int lane = tid & 31, warp = tid >> 5, nwarps = nthreads >> 5;
+  // deferred RMSNorm of the A operand: every row scales by its rstd
+  // (rstd_pre: row scales the caller already computed, indexed from m0).
+  // The wide element-wise and per-head paths apply it as they read the tile;
+  // the others scale the tile in place first.
+  const float *rs = nullptr;
   if (e.ssq_in) {
-    // deferred RMSNorm of the A operand: scale every row by its rstd first
-    // (rstd_pre: row scales the caller already computed, indexed from m0)
-    const float *rs = rstd_pre;
+    rs = rstd_pre;
     if (!rs) {
       float *s_rstd = reinterpret_cast<float *>(s_int + 2 * kEpiMaxRows);
       compute_rstd(e, m0, rows, s_rstd, lane, warp, nwarps);
       sync();
       rs = s_rstd;
     }
+  }
+  if (elementwise_vec<T>(e, t0, t1, ldt, m0, rows, n0, tid, nthreads, rs)) return;
+  const bool heads = e.op == EPI_QKV || e.op == EPI_KV_CACHE;
+  const bool wide = sizeof(T) == 2 && (ldt & 3) == 0 && (nthreads & 31) == 0 &&
+                    ((uintptr_t)e.q_gain & 7) == 0 && ((uintptr_t)e.k_gain & 7) == 0;
+  const bool heads_wide = heads && e.head_dim == 128 && wide;
+  if (rs && !heads_wide) {
     for (int idx = tid; idx < rows * 128; idx += nthreads) {
       const int r = idx >> 7, c = idx & 127;
       t0[r * ldt + c] *= rs[r];
@@ -371,7 +385,6 @@ __device__ void run_epilogue(const EpiParams &e, float *t0, float *t1, int ldt, 
     }
     sync();
   }
-  if (elementwise_vec<T>(e, t0, t1, ldt, m0, rows, n0, tid, nthreads)) return;
   switch (e.op) {
     case EPI_STORE_F32:
     case EPI_RESID:
@@ -549,10 +562,8 @@ __device__ void run_epilogue(const EpiParams &e, float *t0, float *t1, int ldt, 
         s_slot[r] = e.op == EPI_KV_CACHE ? e.row_slot[m0 + r] : 0;
       }
       sync();
-      const bool wide = sizeof(T) == 2 && (ldt & 3) == 0 && (nthreads & 31) == 0 &&
-                        ((uintptr_t)e.q_gain & 7) == 0 && ((uintptr_t)e.k_gain & 7) == 0;
-      if (e.head_dim == 128 && wide)
-        head_ops_d128<T>(e, t0, ldt, m0, rows, n0, lane, warp, nwarps, s_pos, s_slot);
+      if (heads_wide)
+        head_ops_d128<T>(e, t0, ldt, m0, rows, n0, lane, warp, nwarps, s_pos, s_slot, rs);
       else if (e.head_dim == 128)
         head_ops<T, 2>(e, t0, ldt, m0, rows, n0, lane, warp, nwarps, s_pos, s_slot, sync);
       else
