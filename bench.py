@@ -567,7 +567,7 @@ def main():
         from synth.configs import shrink
         cfg = shrink(wl.cfg, name=wl.cfg.name + "-profile-case", n_layers=2,
                      vocab=32768, mask_token_id=32767)
-        wl = replace(wl, name=wl.name + "-profile-case", cfg=cfg)
+        wl = replace(wl, cfg=cfg)   # same name: the same seeded context lengths
     if a.impl == "reference":
         return reference_arm(a, wl, rank, world)
     import torch

@@ -71,6 +71,7 @@ struct Phase {
   int counter_off;                // this phase's tickets start here
   int G;                          // CTAs sharing this phase (<= gridDim.x, <= total_iters)
   long long total_iters;
+  int nfull;                      // whole tiles per CTA in full waves (see cta_sched)
 };
 
 struct Params {
@@ -250,24 +251,31 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
 }
 
 // ------------------------------------------------------------------ schedule
+// A phase's work is the (tile, k-block) space.  With several token tiles
+// (m_tiles > 1) and at least G tiles, it starts with nfull full waves of
+// whole tiles: wave w gives tile w*G + c to CTA c, so the m_tiles CTAs that
+// share a weight tile (consecutive tiles in the raster order
+// tile = feature tile * m_tiles + token tile) stream the same weight
+// k-blocks at the same time and all but the first read them from L2.  The
+// remaining tiles (the tail) are split stream-K: their flattened (tile,
+// k-block) iterations are cut into Gt = min(G, tail iterations) equal
+// contiguous ranges, so every CTA that takes part holds at least one
+// iteration (a split tile's contributors are exactly the CTAs between its
+// first and last).  In the
+// schedule's own numbering CTA c's whole tiles are contiguous: schedule tile
+// s < nfull*G is tile (s % nfull) * G + s / nfull; tail tiles keep their
+// index.  Only tail tiles are ever split.
 struct Range {
   long long b, e;
 };
-// CTA c's share of a phase spread over its first G CTAs (G <= total, so
-// every share of a participating CTA is non-empty); other CTAs sit it out.
-__device__ __forceinline__ Range cta_range(long long total, int G, int c) {
-  if (c >= G) return {0, 0};
-  return {total * c / G, total * (c + 1) / G};
-}
-__device__ __forceinline__ int cta_of_iter(long long it, long long total, int G) {
-  return (int)(((it + 1) * G - 1) / total);
-}
-
+struct Sched {
+  Range whole, tail;   // schedule iterations (tile * KB + k-block) of this CTA
+};
 // The scalars of a phase that the inner loops use, read once per phase into
 // registers.
 struct PhaseScalars {
-  int KB, k_per_src, m_tiles, nseg, pair, M, G, bnt;
-  long long total;
+  int KB, k_per_src, m_tiles, nseg, pair, M, G, bnt, nfull, Gt;
+  long long total, tail_base, tail_total;
   int seg_ntiles[kMaxSeg];
 };
 __device__ __forceinline__ PhaseScalars load_scalars(const Phase &ph) {
@@ -280,11 +288,44 @@ __device__ __forceinline__ PhaseScalars load_scalars(const Phase &ph) {
   ps.M = ph.M;
   ps.G = ph.G;
   ps.bnt = ph.bnt;
+  ps.nfull = ph.nfull;
   ps.total = ph.total_iters;
+  ps.tail_base = (long long)ph.nfull * ph.G * ph.KB;
+  ps.tail_total = ps.total - ps.tail_base;
+  ps.Gt = (int)(ps.tail_total < ps.G ? (ps.tail_total > 0 ? ps.tail_total : 1) : ps.G);
 #pragma unroll
   for (int i = 0; i < kMaxSeg; ++i) ps.seg_ntiles[i] = ph.seg_ntiles[i];
   return ps;
 }
+// CTA c's whole tiles and its share of the tail (empty ranges for CTAs
+// that sit the phase out).
+__device__ __forceinline__ Sched cta_sched(const PhaseScalars &ps, int c) {
+  Sched s;
+  if (c >= ps.G) {
+    s.whole = {0, 0};
+    s.tail = {0, 0};
+    return s;
+  }
+  s.whole.b = (long long)c * ps.nfull * ps.KB;
+  s.whole.e = s.whole.b + (long long)ps.nfull * ps.KB;
+  if (c < ps.Gt) {
+    s.tail.b = ps.tail_base + ps.tail_total * c / ps.Gt;
+    s.tail.e = ps.tail_base + ps.tail_total * (c + 1) / ps.Gt;
+  } else {
+    s.tail = {0, 0};
+  }
+  return s;
+}
+// The tile a schedule tile stands for.
+__device__ __forceinline__ int sched_tile(const PhaseScalars &ps, int s) {
+  if (s >= ps.nfull * ps.G) return s;
+  return (s % ps.nfull) * ps.G + s / ps.nfull;
+}
+// The CTA whose tail range holds tail iteration it (it >= tail_base).
+__device__ __forceinline__ int cta_of_tail_iter(const PhaseScalars &ps, long long it) {
+  return (int)(((it - ps.tail_base + 1) * ps.Gt - 1) / ps.tail_total);
+}
+
 // tile -> (segment, feature tile, token tile), with register-only indexing
 template <int BN>
 __device__ __forceinline__ void locate(const PhaseScalars &ps, int tile, int &seg, int &n0, int &m0) {
@@ -468,16 +509,18 @@ __device__ __forceinline__ bool produce_phase(const Params &p, const Phase &ph,
   // a GEMM-free phase (embedding, normalisation) loads nothing: its inputs
   // are never needed here, and the next phase's weights may stream at once
   if (ps.total == 0) return true;
-  const Range R = cta_range(ps.total, ps.G, cta);
+  const Sched S = cta_sched(ps, cta);
   const uint32_t it0 = it;
   bool ready = false;
   int npend = 0;
+  for (int part = 0; part < 2; ++part) {
+  const Range R = part ? S.tail : S.whole;
   long long left = R.e - R.b;
   int tile = (int)(R.b / ps.KB), kb = (int)(R.b - (long long)tile * ps.KB) - 1;
   int seg = 0, n0 = 0, m0 = 0, half = 0;
   const CUtensorMap *tmw = &ph.tmW[0];
   if (left > 0) {
-    locate<BN>(ps, tile, seg, n0, m0);
+    locate<BN>(ps, sched_tile(ps, tile), seg, n0, m0);
     tmw = &ph.tmW[seg];
     if (NS >= 2) half = ph.seg_half[seg];
   }
@@ -486,7 +529,7 @@ __device__ __forceinline__ bool produce_phase(const Params &p, const Phase &ph,
     if (++kb == ps.KB) {
       kb = 0;
       ++tile;
-      locate<BN>(ps, tile, seg, n0, m0);
+      locate<BN>(ps, sched_tile(ps, tile), seg, n0, m0);
       tmw = &ph.tmW[seg];
       if (NS >= 2) half = ph.seg_half[seg];
     }
@@ -530,6 +573,7 @@ __device__ __forceinline__ bool produce_phase(const Params &p, const Phase &ph,
       ++npend;
     }
     it += SPK;
+  }
   }
   if (!ready) {
     const bool ok = phase_inputs_ready(p, ph_i, gridDim.x);
@@ -669,7 +713,7 @@ __device__ __forceinline__ void tmem_merge(const Params &p, const PhaseScalars &
         for (int kk = 0; kk < KMAX; ++kk) {
           if (k0 + kk < others) {
             const int c = c_first + 1 + k0 + kk;
-            const long long cfirst_tile = (ps.total * c / ps.G) / ps.KB;
+            const long long cfirst_tile = (ps.tail_base + ps.tail_total * c / ps.Gt) / ps.KB;
             const int w = tile == cfirst_tile ? 0 : 1;
             const float *sh = p.partials + ((size_t)c * 2 + w) * (C::ACC_COLS * 128) +
                               (size_t)(q * bnt + g0) * 128 + f;
@@ -777,8 +821,10 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
       bool ok = true;
       for (int ph_i = 0; ph_i < p.nph && ok; ++ph_i) {
         const PhaseScalars ps = load_scalars(p.ph[ph_i]);
-        const Range R = cta_range(ps.total, ps.G, cta);
+        const Sched S = cta_sched(ps, cta);
         const int ns = ps.pair ? 2 : 1;
+        for (int part = 0; part < 2 && ok; ++part) {
+        const Range R = part ? S.tail : S.whole;
         for (long long i = R.b; i < R.e && ok; ++seg_i) {
           const int kb0 = (int)(i % ps.KB);
           const int kb1 = (int)(kb0 + (R.e - i) < ps.KB ? kb0 + (R.e - i) : ps.KB);
@@ -798,10 +844,12 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
             ok = mma_kblocks<C, 1, BN>(it, kb0, kb1, d0, slots, full, empty, p);
           if (!ok) break;
           umma_commit(&acc_full[buf]);
-          if (i == R.b) stamp(p, 9 + 4 * ph_i);   // first segment's MMAs issued
+          if (i == R.b && part == (S.whole.e > S.whole.b ? 0 : 1))
+            stamp(p, 9 + 4 * ph_i);   // first segment's MMAs issued
           i += kb1 - kb0;
         }
-        if (R.e > R.b) stamp(p, 10 + 4 * ph_i);
+        }
+        if (S.whole.e > S.whole.b || S.tail.e > S.tail.b) stamp(p, 10 + 4 * ph_i);
       }
       if (!ok) raise_error(p.err, DFLASH_DERR_TIMEOUT);
       // every MMA issued by this thread must be complete before TMEM is freed
@@ -850,10 +898,13 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
         }
       }
       int rstd_m0 = -1, rstd_seg = -1;   // rows whose deferred-norm scales are in s_rstd
-      const Range R = cta_range(ps.total, ps.G, cta);
+      const Sched S = cta_sched(ps, cta);
+      for (int part = 0; part < 2 && alive; ++part) {
+      const Range R = part ? S.tail : S.whole;
       for (long long i = R.b; i < R.e; ++seg_i) {
-        const int tile = (int)(i / ps.KB);
-        const int kb0 = (int)(i - (long long)tile * ps.KB);
+        const int stile = (int)(i / ps.KB);          // schedule tile
+        const int tile = sched_tile(ps, stile);
+        const int kb0 = (int)(i - (long long)stile * ps.KB);
         const int kb1 = (int)(kb0 + (R.e - i) < ps.KB ? kb0 + (R.e - i) : ps.KB);
         i += kb1 - kb0;
         int seg, n0, m0;
@@ -887,8 +938,9 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
           // the tile is the last segment of that CTA's range, so the owner
           // merges after all its other work.  Every other contributor
           // publishes its fp32 share and moves on.
-          const int c_first = cta_of_iter((long long)tile * ps.KB, ps.total, ps.G);
-          const int c_last = cta_of_iter((long long)(tile + 1) * ps.KB - 1, ps.total, ps.G);
+          // (only tail tiles are split, and they keep their index)
+          const int c_first = cta_of_tail_iter(ps, (long long)tile * ps.KB);
+          const int c_last = cta_of_tail_iter(ps, (long long)(tile + 1) * ps.KB - 1);
           int *ticket = p.counters + ph.counter_off + tile;   // shares published so far
           if (cta != c_first) {
             const long long first_tile = R.b / ps.KB;
@@ -947,7 +999,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
                     mbar_expect_tx(merge_bar, kn * C::CHUNK_BYTES);
                     for (int k = 0; k < kn; ++k) {
                       const int c = c_first + 1 + k0 + k;
-                      const long long cfirst_tile = (ps.total * c / ps.G) / ps.KB;
+                      const long long cfirst_tile =
+                          (ps.tail_base + ps.tail_total * c / ps.Gt) / ps.KB;
                       const int w = tile == cfirst_tile ? 0 : 1;
                       bulk_g2s(merge + k * (C::CHUNK_BYTES / 4),
                                p.partials + ((size_t)c * 2 + w) * (C::ACC_COLS * 128) +
@@ -993,6 +1046,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
           if (lane == 0) mbar_arrive(&acc_empty[buf]);
           if (owner_ticket && tid == 0) *owner_ticket = 0;   // ready for the next launch
         }
+      }
       }
       if (!alive) break;
       if (tid == 0) stamp(p, 11 + 4 * ph_i);
@@ -1247,7 +1301,12 @@ cudaError_t launch_gemm_program(const GemmProblem *probs, int n, float *partials
   p.err = err;
   p.trace = trace;
   const int G = (int)std::min<long long>(std::min(gemm_tc_num_sms(), kTcMaxCtas), most);
-  for (int i = 0; i < n; ++i) p.ph[i].G = (int)std::max<long long>(1, std::min<long long>(G, p.ph[i].total_iters));
+  for (int i = 0; i < n; ++i) {
+    tc::Phase &ph = p.ph[i];
+    ph.G = (int)std::max<long long>(1, std::min<long long>(G, ph.total_iters));
+    // full waves of whole tiles when several token tiles share each weight tile
+    ph.nfull = ph.m_tiles > 1 && ph.nseg > 0 ? ph.tiles / ph.G : 0;
+  }
   const bool coop = n > 1;
   if (any_pair) {
     switch (BN) {
