@@ -159,7 +159,8 @@ def source_hash():
 
 
 def traffic_for(kernel, workload):
-    """DRAM bytes per launch from a committed ncu summary, if it matches the source."""
+    """DRAM bytes per launch from a committed ncu summary, if it matches the
+    source (workload keys carry "+fp8" / "+w<W>" for the cache options)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
@@ -530,7 +531,9 @@ def dominant_roofline(bench, prof, mean_commit, wl_name):
     else:
         out = {"bound": "hbm", "achieved": bytes_ / avg_s / 1e9, "peak": hbm, "unit": "GB/s"}
     out["frac"] = out["achieved"] / out["peak"]
-    out["traffic"] = traffic_for(name, wl_name)
+    key = wl_name + ("+fp8" if getattr(bench, "kv_fp8", False) else "") + \
+        (f"+w{bench.draft_window}" if getattr(bench, "draft_window", 0) else "")
+    out["traffic"] = traffic_for(name, key)
     out["kernel"] = name
     out["share"] = ms / total if total else None
     out["peak_source"] = src
@@ -592,7 +595,8 @@ def main():
         e_value, _, _ = job_rate(e_ms, tokens_here, dist, "cuda")
         e2e = {"value": e_value, "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
-    roof = dominant_roofline(bench, prof, mean_commit, a.workload)
+    roof = dominant_roofline(bench, prof, mean_commit,
+                             a.workload + ("+profile-case" if a.profile_case else ""))
     cpu = None
     if rank == 0 and world == 1 and not a.no_cpu_baseline:
         cpu = cpu_baseline(bench.cfg, bench.T[0], host_weights(bench.W), a.cpu_cycles)

@@ -513,14 +513,16 @@ __device__ __forceinline__ bool produce_phase(const Params &p, const Phase &ph,
   const uint32_t it0 = it;
   bool ready = false;
   int npend = 0;
-  for (int part = 0; part < 2; ++part) {
+  // full waves exist only with 256-token tiles (smaller tiles hold every row)
+  constexpr bool FW = BN == 256;
+  for (int part = FW ? 0 : 1; part < 2; ++part) {
   const Range R = part ? S.tail : S.whole;
   long long left = R.e - R.b;
   int tile = (int)(R.b / ps.KB), kb = (int)(R.b - (long long)tile * ps.KB) - 1;
   int seg = 0, n0 = 0, m0 = 0, half = 0;
   const CUtensorMap *tmw = &ph.tmW[0];
   if (left > 0) {
-    locate<BN>(ps, sched_tile(ps, tile), seg, n0, m0);
+    locate<BN>(ps, FW ? sched_tile(ps, tile) : tile, seg, n0, m0);
     tmw = &ph.tmW[seg];
     if (NS >= 2) half = ph.seg_half[seg];
   }
@@ -529,7 +531,7 @@ __device__ __forceinline__ bool produce_phase(const Params &p, const Phase &ph,
     if (++kb == ps.KB) {
       kb = 0;
       ++tile;
-      locate<BN>(ps, sched_tile(ps, tile), seg, n0, m0);
+      locate<BN>(ps, FW ? sched_tile(ps, tile) : tile, seg, n0, m0);
       tmw = &ph.tmW[seg];
       if (NS >= 2) half = ph.seg_half[seg];
     }
@@ -823,7 +825,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
         const PhaseScalars ps = load_scalars(p.ph[ph_i]);
         const Sched S = cta_sched(ps, cta);
         const int ns = ps.pair ? 2 : 1;
-        for (int part = 0; part < 2 && ok; ++part) {
+        for (int part = BN == 256 ? 0 : 1; part < 2 && ok; ++part) {
         const Range R = part ? S.tail : S.whole;
         for (long long i = R.b; i < R.e && ok; ++seg_i) {
           const int kb0 = (int)(i % ps.KB);
@@ -899,11 +901,11 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
       }
       int rstd_m0 = -1, rstd_seg = -1;   // rows whose deferred-norm scales are in s_rstd
       const Sched S = cta_sched(ps, cta);
-      for (int part = 0; part < 2 && alive; ++part) {
+      for (int part = BN == 256 ? 0 : 1; part < 2 && alive; ++part) {
       const Range R = part ? S.tail : S.whole;
       for (long long i = R.b; i < R.e; ++seg_i) {
         const int stile = (int)(i / ps.KB);          // schedule tile
-        const int tile = sched_tile(ps, stile);
+        const int tile = BN == 256 ? sched_tile(ps, stile) : stile;
         const int kb0 = (int)(i - (long long)stile * ps.KB);
         const int kb1 = (int)(kb0 + (R.e - i) < ps.KB ? kb0 + (R.e - i) : ps.KB);
         i += kb1 - kb0;
