@@ -915,7 +915,15 @@ bool encode_kv_f8(CUtensorMap *tm, const void *base, uint64_t rows, int kvh) {
 }  // namespace
 
 size_t attention_mma_scratch_items(int max_batch, int kvh) {
-  return (size_t)max_batch * kvh + 3 * (size_t)kTcMaxCtas + 8;
+  return (size_t)max_batch * kvh + 8 * (size_t)kTcMaxCtas + 8;
+}
+
+bool attention_mma_uses_cluster(const AttnParams &a) {
+  int sms = 0, dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (sms <= 0) sms = 1;
+  return 4 * a.B * a.n_kv_heads <= 2 * sms;
 }
 
 cudaError_t prepare_attention_mma() {

@@ -151,6 +151,7 @@ cudaError_t prepare_kernels() {
   cudaError_t e = prepare_attention_simt();
   if (e == cudaSuccess) e = prepare_gemm_tc();
   if (e == cudaSuccess) e = prepare_attention_mma();
+  if (e == cudaSuccess) e = prepare_attention_tc();
   if (e == cudaSuccess) e = prepare_selector();
   return e;
 }

@@ -28,7 +28,7 @@ struct Layout {
   size_t skeys, stickets;   // race keys / tickets of sampled verification, zero between calls
   size_t tc_partials, tc_counters, tc_grid_bar;
   int tc_max_tiles;
-  size_t att_item_start, att_pps, att_part_o, att_part_ml, att_tickets;
+  size_t att_item_start, att_pps, att_order, att_part_o, att_part_ml, att_tickets;
   int att_bg;
   size_t total;
 };
@@ -46,6 +46,7 @@ struct dflash_handle {
   size_t ws_bytes = 0;
   int store;      // ST_F32 / ST_BF16
   bool fuse = true;   // dependent bf16 GEMMs as one cooperative launch
+  bool attn_tc = true;  // tcgen05 attention where it applies (else the mma.sync kernel)
   // DFlash 2 candidate selector (dflash_set_selector); K == 0: not set
   struct Selector {
     int K = 0, rank = 0;
@@ -117,7 +118,8 @@ Layout plan(const dflash_config &c, size_t es) {
     const size_t items = attention_mma_scratch_items(c.max_batch, c.n_kv_heads);
     L.att_bg = c.max_batch * c.n_kv_heads;
     L.att_item_start = take(4 * ((size_t)L.att_bg + 1));
-    L.att_pps = take(4);
+    L.att_pps = take(8);
+    L.att_order = take(4 * items);
     L.att_part_o = take(4 * items * R * 128);
     L.att_part_ml = take(8 * items * R);
     L.att_tickets = take(4 * (size_t)L.att_bg);
@@ -184,6 +186,9 @@ cudaError_t run_attention(dflash_handle *h, const AttnParams &a, cudaStream_t s)
   w.part_o = at<float>(h, h->L.att_part_o);
   w.part_ml = at<float>(h, h->L.att_part_ml);
   w.tickets = at<int>(h, h->L.att_tickets);
+  w.order = at<int>(h, h->L.att_order);
+  if (h->attn_tc && attention_tc_eligible(a) && !attention_mma_uses_cluster(a))
+    return launch_attention_tc(a, w, s);
   return launch_attention_mma(a, w, s);
 }
 
@@ -967,6 +972,13 @@ int dflash_accept_commit_sampled_q(dflash_handle *h, int32_t batch, const int32_
 int dflash_test_set_fusion(dflash_handle *h, int32_t on) {
   if (!h) return fail(DFLASH_EINVAL, "handle is NULL");
   h->fuse = on != 0;
+  return DFLASH_OK;
+}
+
+int dflash_test_set_attention(dflash_handle *h, int32_t kernel) {
+  if (!h) return fail(DFLASH_EINVAL, "handle is NULL");
+  if (kernel != 0 && kernel != 1) return fail(DFLASH_EINVAL, "attention kernel must be 0 or 1");
+  h->attn_tc = kernel == 0;
   return DFLASH_OK;
 }
 

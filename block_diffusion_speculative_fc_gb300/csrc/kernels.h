@@ -113,7 +113,8 @@ struct AttnParams {
 
 struct AttnScratch {
   int *item_start;   // [max_batch * kvh + 1]
-  int *pps;          // [1]
+  int *pps;          // [2]: pages per split; the tensor-core kernel's work-queue position
+  int *order;        // [max_items] the tensor-core kernel's work queue
   float *part_o;     // [max_items][R][128]
   float *part_ml;    // [max_items][R][2]
   int *tickets;      // [max_batch * kvh], zero between launches
@@ -226,6 +227,13 @@ cudaError_t prepare_gemm_tc();
 cudaError_t launch_attention_mma(const AttnParams &p, const AttnScratch &w, cudaStream_t s);
 size_t attention_mma_scratch_items(int max_batch, int kvh);
 cudaError_t prepare_attention_mma();
+// Whether launch_attention_mma takes its cluster path (few (request, head) pairs).
+bool attention_mma_uses_cluster(const AttnParams &p);
+// tcgen05 attention: bf16 cache, head_dim 128, 64-row pages, at most 64 query
+// rows per (request, KV head), batch <= 1024.
+bool attention_tc_eligible(const AttnParams &p);
+cudaError_t launch_attention_tc(const AttnParams &p, const AttnScratch &w, cudaStream_t s);
+cudaError_t prepare_attention_tc();
 cudaError_t launch_gemm_simt(int store, const GemmProblem &P, cudaStream_t s);
 cudaError_t launch_attention_simt(int store, const AttnParams &p, cudaStream_t s);
 

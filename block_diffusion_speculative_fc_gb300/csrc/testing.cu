@@ -1,5 +1,8 @@
 // Test-only entry points: the tensor-core GEMM on its own, the FP8 encoder of
-// the K/V cache epilogue (include/dflash_testing.h).
+// the K/V cache epilogue, the bf16 attention kernels on their own
+// (include/dflash_testing.h).
+#include <algorithm>
+#include <cmath>
 #include <cstring>
 
 #include "../../include/dflash_testing.h"
@@ -167,4 +170,92 @@ extern "C" int dflash_test_e4m3_encode(const float *x, int32_t n, float scale, u
   const int pairs = (n + 1) / 2;
   e4m3_encode_kernel<<<(pairs + 255) / 256, 256, 0, (cudaStream_t)stream>>>(x, n, scale, codes);
   return cudaGetLastError() == cudaSuccess ? DFLASH_OK : DFLASH_ECUDA;
+}
+
+// ------------------------------------------------------------ attention
+namespace {
+struct AttnScratchLayout {
+  size_t item_start, pps, order, part_o, part_ml, tickets, total;
+};
+AttnScratchLayout attn_scratch_layout(int B, int n_heads, int kvh, int S) {
+  AttnScratchLayout L;
+  const size_t items = attention_mma_scratch_items(B, kvh);
+  const size_t R = (size_t)(n_heads / kvh) * S;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = (o + std::max<size_t>(bytes, 1) + 255) & ~(size_t)255;
+    return at;
+  };
+  L.item_start = take(4 * ((size_t)B * kvh + 1));
+  L.pps = take(8);
+  L.order = take(4 * items);
+  L.part_o = take(4 * items * R * 128);
+  L.part_ml = take(8 * items * R);
+  L.tickets = take(4 * (size_t)B * kvh);
+  L.total = o;
+  return L;
+}
+}  // namespace
+
+extern "C" size_t dflash_test_attention_scratch(int32_t B, int32_t n_heads, int32_t n_kv_heads,
+                                                int32_t S) {
+  if (B <= 0 || n_kv_heads <= 0 || n_heads % n_kv_heads != 0 || S <= 0) return 0;
+  return attn_scratch_layout(B, n_heads, n_kv_heads, S).total;
+}
+
+extern "C" int dflash_test_attention(int32_t kernel, int32_t B, int32_t S, int32_t n_heads,
+                                     int32_t n_kv_heads, int32_t pages_per_req, int32_t n_pages,
+                                     int32_t window, int32_t draft_window, const void *q,
+                                     const void *kb, const void *vb, const void *k_cache,
+                                     const void *v_cache, const int32_t *page_table,
+                                     const int32_t *kv_len, void *out, void *scratch,
+                                     size_t scratch_bytes, uint32_t *err, dflash_stream_t stream) {
+  if (B <= 0 || S <= 0 || n_kv_heads <= 0 || n_heads % n_kv_heads != 0 || !q || !kb || !vb ||
+      !k_cache || !v_cache || !page_table || !kv_len || !out || !scratch || !err)
+    return DFLASH_EINVAL;
+  if (kernel != 0 && kernel != 1) return DFLASH_EINVAL;
+  const AttnScratchLayout L = attn_scratch_layout(B, n_heads, n_kv_heads, S);
+  if (scratch_bytes < L.total) return DFLASH_ECAPACITY;
+  AttnParams a;
+  memset(&a, 0, sizeof(a));
+  a.q = q;
+  a.kb = kb;
+  a.vb = vb;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.page_table = page_table;
+  a.kv_len = kv_len;
+  a.out = out;
+  a.B = B;
+  a.S = S;
+  a.n_heads = n_heads;
+  a.n_kv_heads = n_kv_heads;
+  a.head_dim = 128;
+  a.page_size = 64;
+  a.pages_per_req = pages_per_req;
+  a.n_pages = n_pages;
+  a.window = window;
+  a.scale = 1.0f / sqrtf(128.0f);
+  a.err = (unsigned int *)err;
+  a.draft_window = draft_window;
+  uint8_t *base = (uint8_t *)scratch;
+  AttnScratch w;
+  w.item_start = (int *)(base + L.item_start);
+  w.pps = (int *)(base + L.pps);
+  w.order = (int *)(base + L.order);
+  w.part_o = (float *)(base + L.part_o);
+  w.part_ml = (float *)(base + L.part_ml);
+  w.tickets = (int *)(base + L.tickets);
+  cudaStream_t s = (cudaStream_t)stream;
+  if (prepare_kernels() != cudaSuccess) return DFLASH_ECUDA;
+  if (cudaMemsetAsync(w.tickets, 0, 4 * (size_t)B * n_kv_heads, s) != cudaSuccess) return DFLASH_ECUDA;
+  cudaError_t e;
+  if (kernel == 0) {
+    if (!attention_tc_eligible(a)) return DFLASH_EUNSUPPORTED;
+    e = launch_attention_tc(a, w, s);
+  } else {
+    e = launch_attention_mma(a, w, s);
+  }
+  return e == cudaSuccess ? DFLASH_OK : DFLASH_ECUDA;
 }

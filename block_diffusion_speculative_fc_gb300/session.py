@@ -179,5 +179,13 @@ class DraftSession:
         lib.dflash_test_set_fusion.restype = ctypes.c_int
         _check(lib.dflash_test_set_fusion(self.h, 1 if on else 0))
 
+    def set_attention(self, kernel):
+        """Attention kernel: "tc" (tcgen05 where it applies, the default) or
+        "mma" (the mma.sync kernels only)."""
+        lib = load_library()
+        lib.dflash_test_set_attention.argtypes = [ctypes.c_void_p, ctypes.c_int32]
+        lib.dflash_test_set_attention.restype = ctypes.c_int
+        _check(lib.dflash_test_set_attention(self.h, {"tc": 0, "mma": 1}[kernel]))
+
     def error(self):
         return dflash_get_error(self.h, _stream())

@@ -2,8 +2,9 @@
  * dflash_testing.h -- test-only entry point of libdflash.
  *
  * Runs the tensor-core GEMM of the library on its own so that it can be
- * compared with a plain matrix product, and the FP8 encoder of the K/V cache
- * on given values; the draft pass never calls these entries.
+ * compared with a plain matrix product, the FP8 encoder of the K/V cache on
+ * given values, and the attention kernels on given inputs; the draft pass
+ * never calls these entries.
  */
 #ifndef DFLASH_TESTING_H
 #define DFLASH_TESTING_H
@@ -76,9 +77,43 @@ int dflash_test_gemm_program_traced(int32_t n_phases, int32_t M, const int32_t *
 int dflash_test_e4m3_encode(const float *x, int32_t n, float scale, uint8_t *codes,
                             dflash_stream_t stream);
 
+/*
+ * The bf16 attention step of the draft block on its own: for every request b
+ * and query head h, out[b*S + j, h, :] = softmax over the visible keys of
+ * q[b*S + j, h, :] . k / sqrt(128), weighted sum of the values.  The keys are
+ * the request's committed context (kv_len[b] rows, paged: row r of request b
+ * is row r % 64 of cache page page_table[b * pages_per_req + r / 64], or of
+ * page page_table[b * pages_per_req + (r / 64) % pages_per_req] when
+ * draft_window > 0) followed by the S block keys kb/vb[b*S .. b*S + S - 1].
+ * A context key at position r is visible to block query j when
+ * r >= kv_len[b] - draft_window (draft_window > 0) and, when window > 0,
+ * kv_len[b] + j - r < window; block keys are always visible.
+ *   kernel   0: the tcgen05 kernel (DFLASH_EUNSUPPORTED where it does not
+ *            apply: more than 64 query rows per (request, KV head), batch
+ *            above 1024); 1: the mma.sync kernels (cluster or split-KV)
+ *   q, out   device bf16 [B*S, n_heads, 128]; kb, vb device bf16 [B*S, n_kv_heads, 128]
+ *   k_cache, v_cache device bf16 [n_pages*64, n_kv_heads, 128]
+ *   page_table, kv_len device int32 [B * pages_per_req], [B]
+ *   scratch  device, at least dflash_test_attention_scratch(B, n_heads, n_kv_heads, S) bytes
+ *   err      device uint32 error word (bits of dflash.h's device errors are OR-ed in)
+ */
+size_t dflash_test_attention_scratch(int32_t B, int32_t n_heads, int32_t n_kv_heads, int32_t S);
+int dflash_test_attention(int32_t kernel, int32_t B, int32_t S, int32_t n_heads, int32_t n_kv_heads,
+                          int32_t pages_per_req, int32_t n_pages, int32_t window,
+                          int32_t draft_window, const void *q, const void *kb, const void *vb,
+                          const void *k_cache, const void *v_cache, const int32_t *page_table,
+                          const int32_t *kv_len, void *out, void *scratch, size_t scratch_bytes,
+                          uint32_t *err, dflash_stream_t stream);
+
 /* Fused launches of dependent GEMMs in the draft pass on (1) or off (0, one
  * launch per GEMM) for this handle. */
 int dflash_test_set_fusion(dflash_handle *h, int32_t on);
+
+/* Attention kernel of the bf16 draft pass for this handle: 0 (default) the
+ * tcgen05 kernel wherever it applies (head_dim 128, at most 64 query rows
+ * per (request, KV head), more (request, KV head) pairs than half the SMs,
+ * bf16 cache), else the mma.sync kernels; 1 the mma.sync kernels only. */
+int dflash_test_set_attention(dflash_handle *h, int32_t kernel);
 
 #ifdef __cplusplus
 }
