@@ -26,10 +26,15 @@
 //   O^T = V^T P^T tcgen05.mma M=128 N=64 K=64: A = the V tile read
 //                 dims-major (MN-major operand: the staged [key][dim] rows as
 //                 they are), B = P; lane = dim, column = slot.
-//   accumulate    thread d (lane d) keeps O[q][d] for every slot q in
-//                 registers: O = O * alpha_t[q] + O_t, alpha_t = exp2(m_{t-1} - m_t).
-// The MMA of tile t+1's S overlaps the softmax of tile t; the accumulation of
-// tile t overlaps the softmax of tile t+1 (double-buffered S, P and O^T).
+//                 The PVs of an item accumulate in one TMEM O^T.  A row's
+//                 running maximum m is raised only when a tile's maximum
+//                 exceeds it by more than 8 (log2 units), so P <= 2^8; then,
+//                 between the PVs of tiles t-1 and t, the four warps rescale
+//                 the O^T columns of the rows that moved by exp2(m_old - m_new)
+//                 (one vote per tile decides whether that pass runs).  The
+//                 end result O / l does not depend on which m was used.
+// The MMA of tile t+1's S overlaps the softmax of tile t (double-buffered S
+// and P).
 //
 // Warp roles (192 threads, two CTAs per SM so that each scheduler has two
 // softmax warps to switch between): warps 0-3 softmax and accumulation, warp
@@ -70,12 +75,16 @@ constexpr int OFF_ALPHA = OFF_ST + NST * STAGE;              // [3][NSLOT] float
 constexpr int OFF_ML = OFF_ALPHA + 3 * NSLOT * 4;            // [NSLOT] float2
 constexpr int OFF_W = OFF_ML + NSLOT * 8;                    // [MAX_SPLITS + 1][NSLOT] float
 constexpr int OFF_MISC = OFF_W + (MAX_SPLITS + 1) * NSLOT * 4;
-// barriers: full[NST], empty[NST], s_full[2], s_free[2], p_full[2], o_full[2],
-// o_free[2], q_full, done, item_full[NQ], item_empty[NQ]
-constexpr int N_BARS = 2 * NST + 10 + 2 * NQ + 2;
+// barriers: full[NST], empty[NST], s_full[2], s_free[2], p_full[2], p_free[2],
+// o_full[2], corr_done, o_read, q_full, done, item_full[NQ], item_empty[NQ]
+constexpr int N_BARS = 2 * NST + 14 + 2 * NQ;
 constexpr int SMEM = 1024 + OFF_MISC + N_BARS * 8 + 64;
 static_assert(2 * (SMEM + 1024) <= 228 * 1024, "two CTAs per SM");
-constexpr uint32_t TMEM_COLS = 256;       // S[2] at 0 / 64, O^T[2] at 128 / 192
+constexpr uint32_t TMEM_COLS = 256;       // S[2] at 0 / 64, the O^T accumulator at 128
+// A row's running maximum is raised only when a tile's maximum exceeds it by
+// more than TAU (log2 units): P <= 2^TAU otherwise, and the O^T column is
+// rescaled (a correction between two PV MMAs) only when the maximum moves.
+constexpr float TAU = 8.f;
 constexpr uint32_t WAIT_LIMIT = 1u << 22;
 constexpr int kThreads = 192;
 
@@ -241,6 +250,26 @@ __device__ __forceinline__ void tmem_ld_halves32(uint32_t taddr, float *v) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Each thread of the warp writes 32 consecutive columns of its own TMEM lane.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float *v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31, %32};" ::"r"(taddr),
+      "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]),
+      "f"(v[8]), "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]),
+      "f"(v[15]), "f"(v[16]), "f"(v[17]), "f"(v[18]), "f"(v[19]), "f"(v[20]), "f"(v[21]),
+      "f"(v[22]), "f"(v[23]), "f"(v[24]), "f"(v[25]), "f"(v[26]), "f"(v[27]), "f"(v[28]),
+      "f"(v[29]), "f"(v[30]), "f"(v[31])
+      : "memory");
+}
+// 2^x by the hardware approximation (ex2.approx.ftz; results below 2^-126 flush to 0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // Shared-memory matrix descriptors (128-byte swizzle).  K-major: rows of 128
@@ -423,11 +452,13 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
   uint64_t *bars = (uint64_t *)(smem + OFF_MISC);
   uint64_t *full = bars, *empty = bars + NST;
   uint64_t *s_full = bars + 2 * NST, *s_free = s_full + 2, *p_full = s_free + 2;
-  uint64_t *o_full = p_full + 2, *o_free = o_full + 2, *q_full = o_free + 2, *done = q_full + 1;
+  uint64_t *p_free = p_full + 2, *o_full = p_free + 2, *corr_done = o_full + 2;
+  uint64_t *o_read = corr_done + 1, *q_full = o_read + 1, *done = q_full + 1;
   uint64_t *item_full = done + 1, *item_empty = item_full + NQ;
   int *s_items = (int *)(item_empty + NQ);          // [NQ]
   uint32_t *s_tmem = (uint32_t *)(s_items + NQ);
   int *s_flag = (int *)(s_tmem + 1);
+  int *s_corr = s_flag + 2;                         // [2] tile needs an O^T correction
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = p.S, R = p.R, G = p.n_heads / p.kvh;
@@ -441,9 +472,11 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
       mbar_init(&s_full[i], 1);
       mbar_init(&s_free[i], 128);
       mbar_init(&p_full[i], 128);
+      mbar_init(&p_free[i], 1);
       mbar_init(&o_full[i], 1);
-      mbar_init(&o_free[i], 128);
     }
+    mbar_init(corr_done, 128);
+    mbar_init(o_read, 128);
     mbar_init(q_full, 128);
     mbar_init(done, 1);
     for (int i = 0; i < NQ; ++i) {
@@ -538,18 +571,21 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
                       desc_kmajor(kb + kblk * (TILE / 2)) + 2 * kk, ID_S, (kblk | kk) ? 1u : 0u);
         umma_commit(&s_full[uu & 1]);
       };
-      auto issue_pv = [&](uint32_t v) {
+      // O^T += V^T P^T of tile v into the one accumulator (tile 0 of an item
+      // overwrites it); the stage and the P buffer are free once it is done
+      auto issue_pv = [&](uint32_t v, bool first) {
         tc_fence_after();
         const uint32_t vb = su32(sST + (v % NST) * STAGE + TILE);
         const uint32_t pb = qa + ((v & 1) ? P_OFF1 : P_OFF0);
 #pragma unroll
         for (int kk = 0; kk < KT / 16; ++kk)
-          umma_bf16(tmem + 128 + (v & 1) * 64, desc_mnmajor(vb + kk * 2048, TILE / 2),
-                    desc_kmajor(pb, P_SBO) + 2 * kk, ID_PV, kk > 0 ? 1u : 0u);
+          umma_bf16(tmem + 128, desc_mnmajor(vb + kk * 2048, TILE / 2),
+                    desc_kmajor(pb, P_SBO) + 2 * kk, ID_PV, (first && kk == 0) ? 0u : 1u);
         umma_commit(&o_full[v & 1]);
         umma_commit(&empty[v % NST]);
+        umma_commit(&p_free[v & 1]);
       };
-      uint32_t u = 0, ni = 0;
+      uint32_t u = 0, ni = 0, ncorr = 0;
       for (uint32_t k = 0;; ++k) {
         const int item = get_item(k);
         if (item < 0) break;
@@ -572,12 +608,19 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
               did = true;
             }
           }
+          // PV of tile np: its P written; then the O^T correction the softmax
+          // asked for, or (tile 0) the previous item's O^T read out
           const uint32_t v = u + np;
-          if (mbar_test(&p_full[v & 1], (v >> 1) & 1) &&
-              mbar_test(&o_free[v & 1], ((v >> 1) & 1) ^ 1)) {
-            issue_pv(v);
-            ++np;
-            did = true;
+          if (mbar_test(&p_full[v & 1], (v >> 1) & 1)) {
+            const bool corr = *(volatile int *)&s_corr[v & 1] != 0;
+            const bool ready = np == 0 ? mbar_test(o_read, (ni & 1) ^ 1)
+                                       : (!corr || mbar_test(corr_done, ncorr & 1));
+            if (ready) {
+              if (np > 0 && corr) ++ncorr;
+              issue_pv(v, np == 0);
+              ++np;
+              did = true;
+            }
           }
           if (did) {
             idle = 0;
@@ -606,6 +649,19 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
     const bool live = warp * 16 < R;           // the warp's slots hold queries
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     auto bar_math = [] { asm volatile("bar.sync 1, 128;" ::: "memory"); };
+    // barrier of the 128 math threads returning the OR of `v` over them
+    auto bar_math_or = [](bool v) -> bool {
+      uint32_t r;
+      asm volatile(
+          "{\n\t.reg .pred p, q;\n\t"
+          "setp.ne.u32 p, %1, 0;\n\t"
+          "bar.red.or.pred q, 1, 128, p;\n\t"
+          "selp.u32 %0, 1, 0, q;\n\t}"
+          : "=r"(r)
+          : "r"((uint32_t)v)
+          : "memory");
+      return r != 0;
+    };
 
     // A row `arow` of Q, K-block kh <- dims 64 kh .. 64 kh + 63 of the query
     // in `slot` (zeros past R)
@@ -651,37 +707,15 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
       // producer publishes it only after issuing all of this item's tiles)
       int nitem = -1;
       const int lo_q = first_visible(p, it.kv, slot % S);
-      float o[NSLOT];
-#pragma unroll
-      for (int i = 0; i < NSLOT; ++i) o[i] = 0.f;
       float m = -INFINITY, l = 0.f;
       const float sl = p.scale_log2;
 
-      auto accumulate = [&](uint32_t v) {
-        role_wait(ok, &o_full[v & 1], (v >> 1) & 1);
-        tc_fence_after();
-        const float4 *al4 = reinterpret_cast<const float4 *>(s_alpha + (v % 3) * NSLOT);
-#pragma unroll
-        for (int c0 = 0; c0 < NSLOT; c0 += 32) {
-          float ov[32];
-          tmem_ld<32>(tmem + lane_base + 128 + (v & 1) * 64 + c0, ov);
-#pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            const float4 al = al4[(c0 + i) >> 2];
-            o[c0 + i] = fmaf(o[c0 + i], al.x, ov[i]);
-            o[c0 + i + 1] = fmaf(o[c0 + i + 1], al.y, ov[i + 1]);
-            o[c0 + i + 2] = fmaf(o[c0 + i + 2], al.z, ov[i + 2]);
-            o[c0 + i + 3] = fmaf(o[c0 + i + 3], al.w, ov[i + 3]);
-          }
-        }
-        tc_fence_before();
-        mbar_arrive(&o_free[v & 1]);
-      };
       for (int t = 0; t < it.ntiles; ++t) {
         const uint32_t uu = u + t;
         // ---- softmax of tile t
         role_wait(ok, &s_full[uu & 1], (uu >> 1) & 1);
         tc_fence_after();
+        bool need = false;   // this row's O^T column must be rescaled before PV of tile t
         if (live) {
           float sv[32];
           tmem_ld_halves32(tmem + lane_base + (uu & 1) * 64, sv);
@@ -708,20 +742,29 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
             if ((vis >> i) & 1u) mx = fmaxf(mx, sv[i]);
           mx *= sl;
           mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-          const float mn = fmaxf(m, mx);
-          const float alpha = mn == -INFINITY ? 1.f : exp2f(m - mn);
-          m = mn;
+          // the running maximum moves only by more than TAU; before the first
+          // visible key of the row its O^T column is still zero
+          float alpha = 1.f;
+          if (mx > m + TAU) {
+            if (m != -INFINITY) {
+              alpha = ex2(m - mx);
+              need = true;
+            }
+            m = mx;
+          }
           float ps = 0.f;
           uint32_t packed[16];
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
-            const float p0 = (vis >> i) & 1u ? exp2f(fmaf(sv[i], sl, -mn)) : 0.f;
-            const float p1 = (vis >> (i + 1)) & 1u ? exp2f(fmaf(sv[i + 1], sl, -mn)) : 0.f;
+            const float p0 = (vis >> i) & 1u ? ex2(fmaf(sv[i], sl, -m)) : 0.f;
+            const float p1 = (vis >> (i + 1)) & 1u ? ex2(fmaf(sv[i + 1], sl, -m)) : 0.f;
             ps += p0 + p1;
             __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
             packed[i / 2] = *reinterpret_cast<uint32_t *>(&h2);
           }
           l = fmaf(l, alpha, ps);
+          // P buffer of this tile parity free again: PV of tile uu - 2 done
+          role_wait(ok, &p_free[uu & 1], ((uu >> 1) & 1) ^ 1);
           // P row `slot`, keys key0 .. key0 + 31: 16-byte chunks 4 kh .. 4 kh + 3
           uint8_t *prow = sQ + ((uu & 1) ? P_OFF1 : P_OFF0) + (slot >> 3) * P_SBO + (slot & 7) * 128;
 #pragma unroll
@@ -730,16 +773,18 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
             *reinterpret_cast<uint4 *>(prow + ((chunk ^ (slot & 7)) << 4)) =
                 make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
           }
-          if (kh == 0) s_alpha[(uu % 3) * NSLOT + slot] = alpha;
+          if (kh == 0) s_alpha[(uu & 1) * NSLOT + slot] = alpha;
           fence_async_smem();
         } else {
           tc_fence_before();
           mbar_arrive(&s_free[uu & 1]);
         }
+        // one vote over the 128 threads (also publishes alpha of tile t)
+        const bool any = bar_math_or(need);
+        if (threadIdx.x == 0) s_corr[uu & 1] = any ? 1 : 0;
         mbar_arrive(&p_full[uu & 1]);
         if (t == it.ntiles - 1) {
           // the last S of the item has been read: the next item's Q may go in
-          // (the barrier inside also publishes alpha of tile t)
           nitem = get_item_all(k + 1);
           if (nitem >= 0) {
             // (request, KV head) of the next item: item_start is ordered
@@ -750,12 +795,42 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
             }
             write_q(lo_i / p.kvh, lo_i % p.kvh);
           }
-        } else {
-          bar_math();   // alpha of tile t visible; every thread is past accumulate(t - 2)
         }
-        if (t > 0) accumulate(uu - 1);
+        if (any) {
+          // O^T column q *= alpha_t[q] once PV of tile t - 1 is done (thread a: dim a)
+          role_wait(ok, &o_full[(uu - 1) & 1], ((uu - 1) >> 1) & 1);
+          tc_fence_after();
+          const float4 *al4 = reinterpret_cast<const float4 *>(s_alpha + (uu & 1) * NSLOT);
+#pragma unroll
+          for (int c0 = 0; c0 < NSLOT; c0 += 32) {
+            float ov[32];
+            tmem_ld<32>(tmem + lane_base + 128 + c0, ov);
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+              const float4 al = al4[(c0 + i) >> 2];
+              ov[i] *= al.x;
+              ov[i + 1] *= al.y;
+              ov[i + 2] *= al.z;
+              ov[i + 3] *= al.w;
+            }
+            tmem_st32(tmem + lane_base + 128 + c0, ov);
+          }
+          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+          tc_fence_before();
+          mbar_arrive(corr_done);
+        }
       }
-      accumulate(u + it.ntiles - 1);
+      // ---- O^T of the item (thread a: dim a, every slot) once its last PV is done
+      float o[NSLOT];
+      {
+        const uint32_t v = u + it.ntiles - 1;
+        role_wait(ok, &o_full[v & 1], (v >> 1) & 1);
+        tc_fence_after();
+        tmem_ld<32>(tmem + lane_base + 128, o);
+        tmem_ld<32>(tmem + lane_base + 128 + 32, o + 32);
+        tc_fence_before();
+        mbar_arrive(o_read);
+      }
       // ---- row sums over the two key halves of each slot; (m, l) per slot
       l += __shfl_xor_sync(0xffffffffu, l, 16);
       if (live && kh == 0) s_ml[slot] = make_float2(m, l);
