@@ -56,9 +56,8 @@ namespace dflash {
 namespace atc {
 
 constexpr int KT = 64;                    // keys per tile (one page)
-constexpr int NST = 2;                    // K/V stages (two CTAs share an SM)
+constexpr int NST = 2;                    // K slots and V slots (two CTAs share an SM)
 constexpr int TILE = KT * 128 * 2;        // K (or V) of one tile: two boxes of 64 keys x 64 dims
-constexpr int STAGE = 2 * TILE;           // K then V
 constexpr int Q_KBLK = 128 * 128;         // one 64-dim K-block of the 128-row Q operand
 constexpr int NSLOT = 64;                 // query slots: lanes 0-15 of each TMEM lane quarter
 constexpr int MAX_SPLITS = 16;
@@ -71,14 +70,16 @@ constexpr int P_SBO = 4096;
 constexpr int P_OFF0 = 2048, P_OFF1 = 3072;
 constexpr int OFF_Q = 0;
 constexpr int OFF_ST = OFF_Q + 2 * Q_KBLK;
-constexpr int OFF_ALPHA = OFF_ST + NST * STAGE;              // [3][NSLOT] float
+constexpr int OFF_V = OFF_ST + NST * TILE;                   // the V ring after the K ring
+constexpr int OFF_ALPHA = OFF_V + NST * TILE;                // [2][NSLOT] float
 constexpr int OFF_ML = OFF_ALPHA + 3 * NSLOT * 4;            // [NSLOT] float2
 constexpr int OFF_W = OFF_ML + NSLOT * 8;                    // [MAX_SPLITS + 1][NSLOT] float
 constexpr int OFF_MISC = OFF_W + (MAX_SPLITS + 1) * NSLOT * 4;
-// barriers: full[NST], empty[NST], s_full[2], s_free[2], p_full[2], p_free[2],
-// o_full[2], corr_done, o_read, q_full, done, item_full[NQ], item_empty[NQ]
-constexpr int N_BARS = 2 * NST + 14 + 2 * NQ;
-constexpr int SMEM = 1024 + OFF_MISC + N_BARS * 8 + 64;
+// barriers: fullK[NST], fullV[NST], emptyK[NST], emptyV[NST], s_full[2],
+// s_free[2], p_full[2], p_free[2], o_full[2], corr_done, o_read, q_full, done,
+// item_full[NQ], item_empty[NQ]; then the queue entries [NQ][8] and a few words
+constexpr int N_BARS = 4 * NST + 14 + 2 * NQ;
+constexpr int SMEM = 1024 + OFF_MISC + N_BARS * 8 + NQ * 32 + 64;
 static_assert(2 * (SMEM + 1024) <= 228 * 1024, "two CTAs per SM");
 constexpr uint32_t TMEM_COLS = 256;       // S[2] at 0 / 64, the O^T accumulator at 128
 // A row's running maximum is raised only when a tile's maximum exceeds it by
@@ -98,7 +99,7 @@ struct Params {
   const int *item_start;         // [B*KVH + 1] prefix of splits per (b, g)
   const int *pps_ptr;            // [0] pages per split, [1] work-queue counter
   int *counter;                  // work-queue position (reset by the prep kernel)
-  const int *order;              // [items] the queue: item indices, largest first
+  const int4 *queue;             // [items][2] the work queue, largest first (see Item)
   float *part_o;                 // [max_items][R][D]
   float2 *part_ml;               // [max_items][R]
   int *tickets;                  // [B*KVH]
@@ -314,28 +315,24 @@ __device__ __forceinline__ int clamp_kv(const Params &p, int kv) {
   const int cap = p.pages_per_req * KT;
   return kv < 0 ? 0 : (p.draft_window == 0 && kv > cap ? cap : kv);
 }
+// A work item as the prep kernel lays it out in the queue (two int4):
+// {item, b * kvh + g, split, nsplit}, {kv, first visible page, first page of
+// the split (relative), context pages of the split}.
 struct Item {
-  int b, g, bg, split, nsplit, kv, first_page, pg0, nctx, ntiles;
+  int item, b, g, bg, split, nsplit, kv, first_page, pg0, nctx, ntiles;
 };
-__device__ __forceinline__ Item decode(const Params &p, int item, int pps) {
-  const int n_bg = p.B * p.kvh;
-  int lo_i = 0, hi_i = n_bg - 1;
-  while (lo_i < hi_i) {
-    const int mid = (lo_i + hi_i + 1) >> 1;
-    if (__ldg(&p.item_start[mid]) <= item) lo_i = mid; else hi_i = mid - 1;
-  }
+__device__ __forceinline__ Item unpack_item(const int *e, int kvh) {
   Item it;
-  it.bg = lo_i;
-  it.b = lo_i / p.kvh;
-  it.g = lo_i % p.kvh;
-  it.split = item - __ldg(&p.item_start[lo_i]);
-  it.nsplit = __ldg(&p.item_start[lo_i + 1]) - __ldg(&p.item_start[lo_i]);
-  it.kv = clamp_kv(p, __ldg(&p.kv_len[it.b]));
-  const int lo = visible_lo(it.kv, p.window, p.draft_window);
-  it.first_page = lo / KT;
-  const int pages = it.kv > lo ? (it.kv - 1) / KT - it.first_page + 1 : 0;
-  it.pg0 = it.split * pps;
-  it.nctx = max(0, min(pages, it.pg0 + pps) - it.pg0);
+  it.item = e[0];
+  it.bg = e[1];
+  it.split = e[2];
+  it.nsplit = e[3];
+  it.kv = e[4];
+  it.first_page = e[5];
+  it.pg0 = e[6];
+  it.nctx = e[7];
+  it.b = it.bg / kvh;
+  it.g = it.bg % kvh;
   it.ntiles = it.nctx + (it.split == it.nsplit - 1 ? 1 : 0);
   return it;
 }
@@ -384,7 +381,7 @@ __device__ __forceinline__ int2 block_scan2(int2 v, int2 *s_warp, int2 &total) {
 
 __global__ void __launch_bounds__(kPrepThreads) attn_tc_prep_kernel(
     const int *__restrict__ kv_len, int B, int kvh, int cap, int window, int draft_window,
-    int target_items, int max_items, int *item_start, int *pps_out, int *order, unsigned int *err) {
+    int target_items, int max_items, int *item_start, int *pps_out, int4 *queue, unsigned int *err) {
   pdl_wait();
   __shared__ int s_rem[kPrepThreads];
   __shared__ int2 s_warp[32];
@@ -395,13 +392,14 @@ __global__ void __launch_bounds__(kPrepThreads) attn_tc_prep_kernel(
     s_max = 0;
   }
   __syncthreads();
-  int pages = 0;
+  int pages = 0, kv = 0, first_page = 0;
   if (b < B) {
-    int kv = kv_len[b];
+    kv = kv_len[b];
     if (kv < 0 || kv > cap) raise_error(err, DFLASH_DERR_KV_CAPACITY);
     kv = kv < 0 ? 0 : (kv > cap ? cap : kv);
     const int lo = visible_lo(kv, window, draft_window);
-    pages = kv > lo ? (kv - 1) / KT - lo / KT + 1 : 0;
+    first_page = lo / KT;
+    pages = kv > lo ? (kv - 1) / KT - first_page + 1 : 0;
     atomicAdd(&s_total, pages * kvh);
     atomicMax(&s_max, pages);
   }
@@ -425,17 +423,22 @@ __global__ void __launch_bounds__(kPrepThreads) attn_tc_prep_kernel(
   if (b < B) {
     for (int g = 0; g < kvh; ++g) item_start[b * kvh + g] = ex.x + g * nsplit;
     if (b == B - 1) item_start[B * kvh] = ex.x + nsplit * kvh;
+    auto put = [&](int at, int g, int sp) {
+      const int pg0 = sp * pps;
+      queue[2 * at] = make_int4(ex.x + g * nsplit + sp, b * kvh + g, sp, nsplit);
+      queue[2 * at + 1] = make_int4(kv, first_page, pg0, max(0, min(pages, pg0 + pps) - pg0));
+    };
     // full splits: queue positions [0, tot.y) in request order
     int pos = ex.y;
     for (int g = 0; g < kvh; ++g)
-      for (int sp = 0; sp + 1 < nsplit; ++sp) order[pos++] = ex.x + g * nsplit + sp;
+      for (int sp = 0; sp + 1 < nsplit; ++sp) put(pos++, g, sp);
     // last splits: by decreasing size (ties: lower request first)
     int rank = 0;
     for (int o = 0; o < B; ++o) {
       const int r = s_rem[o];
       rank += (r > rem || (r == rem && o < b)) ? 1 : 0;
     }
-    for (int g = 0; g < kvh; ++g) order[tot.y + rank * kvh + g] = ex.x + g * nsplit + nsplit - 1;
+    for (int g = 0; g < kvh; ++g) put(tot.y + rank * kvh + g, g, nsplit - 1);
   }
   if (b == 0) pps_out[1] = 0;   // queue position
 }
@@ -449,14 +452,15 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
   float *s_alpha = (float *)(smem + OFF_ALPHA);
   float2 *s_ml = (float2 *)(smem + OFF_ML);
   float *s_w = (float *)(smem + OFF_W);
+  uint8_t *sV = smem + OFF_V;
   uint64_t *bars = (uint64_t *)(smem + OFF_MISC);
-  uint64_t *full = bars, *empty = bars + NST;
-  uint64_t *s_full = bars + 2 * NST, *s_free = s_full + 2, *p_full = s_free + 2;
+  uint64_t *fullK = bars, *fullV = bars + NST, *emptyK = bars + 2 * NST, *emptyV = bars + 3 * NST;
+  uint64_t *s_full = bars + 4 * NST, *s_free = s_full + 2, *p_full = s_free + 2;
   uint64_t *p_free = p_full + 2, *o_full = p_free + 2, *corr_done = o_full + 2;
   uint64_t *o_read = corr_done + 1, *q_full = o_read + 1, *done = q_full + 1;
   uint64_t *item_full = done + 1, *item_empty = item_full + NQ;
-  int *s_items = (int *)(item_empty + NQ);          // [NQ]
-  uint32_t *s_tmem = (uint32_t *)(s_items + NQ);
+  int *s_items = (int *)(item_empty + NQ);          // [NQ][8] queue entries
+  uint32_t *s_tmem = (uint32_t *)(s_items + NQ * 8);
   int *s_flag = (int *)(s_tmem + 1);
   int *s_corr = s_flag + 2;                         // [2] tile needs an O^T correction
 
@@ -465,8 +469,10 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < NST; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
+      mbar_init(&fullK[i], 1);
+      mbar_init(&fullV[i], 1);
+      mbar_init(&emptyK[i], 1);
+      mbar_init(&emptyV[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
@@ -495,60 +501,130 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
   pdl_wait();   // Q, the block K/V and the work list come from the predecessors
-  const int pps = __ldg(&p.pps_ptr[0]);
   const int total_items = __ldg(&p.item_start[p.B * p.kvh]);
   bool ok = true;
 
-  // consumers: the item of queue entry k (-1: no more work or a timeout)
-  auto get_item = [&](uint32_t k) -> int {
+  // consumers: queue entry k (item -1: no more work or a timeout)
+  auto get_item = [&](uint32_t k) -> Item {
     role_wait(ok, &item_full[k % NQ], (k / NQ) & 1);
-    return ok ? *(volatile int *)&s_items[k % NQ] : -1;
+    Item it = unpack_item((const int *)&s_items[(k % NQ) * 8], p.kvh);
+    if (!ok) it.item = -1;
+    return it;
   };
 
   if (warp == 4) {
     // ------------------------------------------------------------ producer
+    // Two cursors over the same sequence of tiles: K tiles go out as soon as
+    // a K slot is free (after that tile's S), V tiles as soon as a V slot is
+    // free (after that tile's PV), the V cursor never ahead of the K cursor.
+    // The K cursor also takes the queue entries, which stay in place until
+    // the consumers have finished their items.
     if (lane == 0) {
-      uint32_t u = 0;
-      for (uint32_t k = 0;; ++k) {
-        role_wait(ok, &item_empty[k % NQ], ((k / NQ) & 1) ^ 1);
-        const int idx = atomicAdd(p.counter, 1);
-        const int item = ok && idx < total_items ? __ldg(&p.order[idx]) : -1;
-        s_items[k % NQ] = item;
-        mbar_arrive(&item_full[k % NQ]);
-        if (item < 0) break;
-        const Item it = decode(p, item, pps);
-        for (int t = 0; t < it.ntiles; ++t, ++u) {
-          const int s = u % NST;
-          role_wait(ok, &empty[s], ((u / NST) & 1) ^ 1);
-          uint64_t *bar = &full[s];
-          uint8_t *st = sST + s * STAGE;
-          asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(bar)),
-                       "r"(STAGE)
-                       : "memory");
-          if (t < it.nctx) {
-            const int lp = it.first_page + it.pg0 + t;
-            int page = __ldg(&p.page_table[(size_t)it.b * p.pages_per_req +
-                                           (p.draft_window > 0 ? lp % p.pages_per_req : lp)]);
-            if (page < 0 || page >= p.n_pages) {
-              raise_error(p.err, DFLASH_DERR_PAGE_RANGE);
-              page = 0;
+      auto tile_page = [&](const Item &it, int t) {
+        const int lp = it.first_page + it.pg0 + t;
+        int page = __ldg(&p.page_table[(size_t)it.b * p.pages_per_req +
+                                       (p.draft_window > 0 ? lp % p.pages_per_req : lp)]);
+        if (page < 0 || page >= p.n_pages) {
+          raise_error(p.err, DFLASH_DERR_PAGE_RANGE);
+          page = 0;
+        }
+        return page;
+      };
+      auto issue = [&](const CUtensorMap *tm, const CUtensorMap *tmb, uint8_t *dst, uint64_t *bar,
+                       const Item &it, int t) {
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(bar)),
+                     "r"(TILE)
+                     : "memory");
+        if (t < it.nctx) {
+          const int page = tile_page(it, t);
+          tma3(dst, tm, bar, 0, it.g, page * KT);
+          tma3(dst + TILE / 2, tm, bar, 64, it.g, page * KT);
+        } else {
+          tma3(dst, tmb, bar, 0, it.g, it.b * S);
+          tma3(dst + TILE / 2, tmb, bar, 64, it.g, it.b * S);
+        }
+      };
+      uint32_t nf = 0;             // queue entries taken
+      uint32_t kq = 0, vq = 0;     // entries of the K and V cursors
+      int kt = 0, vt = 0;          // next tile of those entries
+      uint32_t uK = 0, uV = 0;     // K and V tiles issued
+      bool endK = false, endV = false, hasK = false, hasV = false;
+      Item ik, iv;
+      uint32_t idle = 0;
+      while (ok && !(endK && endV)) {
+        bool did = false;
+        if (!endK && !hasK) {
+          if (kq == nf && mbar_test(&item_empty[nf % NQ], ((nf / NQ) & 1) ^ 1)) {
+            const int idx = atomicAdd(p.counter, 1);
+            int *e = &s_items[(nf % NQ) * 8];
+            if (idx < total_items) {
+              const int4 d0 = __ldg(&p.queue[2 * idx]), d1 = __ldg(&p.queue[2 * idx + 1]);
+              e[0] = d0.x; e[1] = d0.y; e[2] = d0.z; e[3] = d0.w;
+              e[4] = d1.x; e[5] = d1.y; e[6] = d1.z; e[7] = d1.w;
+            } else {
+              e[0] = -1;
             }
-            tma3(st, &p.tmK, bar, 0, it.g, page * KT);
-            tma3(st + TILE / 2, &p.tmK, bar, 64, it.g, page * KT);
-            tma3(st + TILE, &p.tmV, bar, 0, it.g, page * KT);
-            tma3(st + TILE + TILE / 2, &p.tmV, bar, 64, it.g, page * KT);
-          } else {
-            tma3(st, &p.tmKb, bar, 0, it.g, it.b * S);
-            tma3(st + TILE / 2, &p.tmKb, bar, 64, it.g, it.b * S);
-            tma3(st + TILE, &p.tmVb, bar, 0, it.g, it.b * S);
-            tma3(st + TILE + TILE / 2, &p.tmVb, bar, 64, it.g, it.b * S);
+            mbar_arrive(&item_full[nf % NQ]);
+            ++nf;
+            did = true;
+          }
+          if (kq < nf) {
+            ik = unpack_item(&s_items[(kq % NQ) * 8], p.kvh);
+            if (ik.item < 0) {
+              endK = true;
+            } else {
+              hasK = true;
+              kt = 0;
+            }
           }
         }
+        if (hasK && mbar_test(&emptyK[uK % NST], ((uK / NST) & 1) ^ 1)) {
+          issue(&p.tmK, &p.tmKb, sST + (uK % NST) * TILE, &fullK[uK % NST], ik, kt);
+          ++uK;
+          did = true;
+          if (++kt == ik.ntiles) {
+            hasK = false;
+            ++kq;
+          }
+        }
+        if (!endV && !hasV && vq < nf) {
+          iv = unpack_item(&s_items[(vq % NQ) * 8], p.kvh);
+          if (iv.item < 0) {
+            endV = true;
+          } else {
+            hasV = true;
+            vt = 0;
+          }
+        }
+        if (hasV && uV < uK && mbar_test(&emptyV[uV % NST], ((uV / NST) & 1) ^ 1)) {
+          issue(&p.tmV, &p.tmVb, sV + (uV % NST) * TILE, &fullV[uV % NST], iv, vt);
+          ++uV;
+          did = true;
+          if (++vt == iv.ntiles) {
+            hasV = false;
+            ++vq;
+          }
+        }
+        if (did) {
+          idle = 0;
+        } else if (++idle > WAIT_LIMIT) {
+          ok = false;
+        } else if (idle > 64) {
+          __nanosleep(32);
+        }
       }
-      if (!ok) raise_error(p.err, DFLASH_DERR_TIMEOUT);
+      if (!ok) {
+        raise_error(p.err, DFLASH_DERR_TIMEOUT);
+        // the consumers learn of the end through the queue
+        if (!endK && kq == nf && mbar_wait(&item_empty[nf % NQ], ((nf / NQ) & 1) ^ 1)) {
+          s_items[(nf % NQ) * 8] = -1;
+          mbar_arrive(&item_full[nf % NQ]);
+        }
+      }
       // every copy this CTA issued has landed before it exits (the normal
       // path consumed them all already)
-      for (uint32_t v = u > (uint32_t)NST ? u - NST : 0; v < u; ++v) mbar_wait(&full[v % NST], (v / NST) & 1);
+      for (uint32_t v = uK > (uint32_t)NST ? uK - NST : 0; v < uK; ++v) mbar_wait(&fullK[v % NST], (v / NST) & 1);
+      for (uint32_t v = uV > (uint32_t)NST ? uV - NST : 0; v < uV; ++v) mbar_wait(&fullV[v % NST], (v / NST) & 1);
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
@@ -562,7 +638,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
       const uint32_t qa = su32(sQ);
       auto issue_s = [&](uint32_t uu) {
         tc_fence_after();
-        const uint32_t kb = su32(sST + (uu % NST) * STAGE);
+        const uint32_t kb = su32(sST + (uu % NST) * TILE);
 #pragma unroll
         for (int kblk = 0; kblk < 2; ++kblk)
 #pragma unroll
@@ -570,29 +646,29 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
             umma_bf16(tmem + (uu & 1) * 64, desc_kmajor(qa + kblk * Q_KBLK) + 2 * kk,
                       desc_kmajor(kb + kblk * (TILE / 2)) + 2 * kk, ID_S, (kblk | kk) ? 1u : 0u);
         umma_commit(&s_full[uu & 1]);
+        umma_commit(&emptyK[uu % NST]);
       };
       // O^T += V^T P^T of tile v into the one accumulator (tile 0 of an item
       // overwrites it); the stage and the P buffer are free once it is done
       auto issue_pv = [&](uint32_t v, bool first) {
         tc_fence_after();
-        const uint32_t vb = su32(sST + (v % NST) * STAGE + TILE);
+        const uint32_t vb = su32(sV + (v % NST) * TILE);
         const uint32_t pb = qa + ((v & 1) ? P_OFF1 : P_OFF0);
 #pragma unroll
         for (int kk = 0; kk < KT / 16; ++kk)
           umma_bf16(tmem + 128, desc_mnmajor(vb + kk * 2048, TILE / 2),
                     desc_kmajor(pb, P_SBO) + 2 * kk, ID_PV, (first && kk == 0) ? 0u : 1u);
         umma_commit(&o_full[v & 1]);
-        umma_commit(&empty[v % NST]);
+        umma_commit(&emptyV[v % NST]);
         umma_commit(&p_free[v & 1]);
       };
       uint32_t u = 0, ni = 0, ncorr = 0;
       for (uint32_t k = 0;; ++k) {
-        const int item = get_item(k);
-        if (item < 0) break;
-        const Item it = decode(p, item, pps);
+        const Item it = get_item(k);
+        if (it.item < 0) break;
         mbar_arrive(&item_empty[k % NQ]);
         role_wait(ok, q_full, ni & 1);
-        role_wait(ok, &full[u % NST], (u / NST) & 1);
+        role_wait(ok, &fullK[u % NST], (u / NST) & 1);
         role_wait(ok, &s_free[u & 1], ((u >> 1) & 1) ^ 1);
         issue_s(u);
         int ns = 1, np = 0;   // tiles of this item with S issued / with PV issued
@@ -601,7 +677,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
           bool did = false;
           if (ns < it.ntiles) {
             const uint32_t uu = u + ns;
-            if (mbar_test(&full[uu % NST], (uu / NST) & 1) &&
+            if (mbar_test(&fullK[uu % NST], (uu / NST) & 1) &&
                 mbar_test(&s_free[uu & 1], ((uu >> 1) & 1) ^ 1)) {
               issue_s(uu);
               ++ns;
@@ -611,7 +687,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
           // PV of tile np: its P written; then the O^T correction the softmax
           // asked for, or (tile 0) the previous item's O^T read out
           const uint32_t v = u + np;
-          if (mbar_test(&p_full[v & 1], (v >> 1) & 1)) {
+          if (mbar_test(&p_full[v & 1], (v >> 1) & 1) && mbar_test(&fullV[v % NST], (v / NST) & 1)) {
             const bool corr = *(volatile int *)&s_corr[v & 1] != 0;
             const bool ready = np == 0 ? mbar_test(o_read, (ni & 1) ^ 1)
                                        : (!corr || mbar_test(corr_done, ncorr & 1));
@@ -688,24 +764,22 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
     // queue entry k for all 128 threads: one thread waits, a barrier
     // broadcasts (the loop bounds of every thread come from it)
     int *s_bcast = s_flag + 1;
-    auto get_item_all = [&](uint32_t k) -> int {
-      if (threadIdx.x == 0) *s_bcast = get_item(k);
+    auto get_item_all = [&](uint32_t kk) -> Item {
+      if (threadIdx.x == 0) *s_bcast = get_item(kk).item;
       bar_math();
-      return *(volatile int *)s_bcast;
+      Item e = unpack_item(&s_items[(kk % NQ) * 8], p.kvh);
+      e.item = *(volatile int *)s_bcast;
+      return e;
     };
 
     uint32_t u = 0;
     uint32_t k = 0;
-    int item = get_item_all(0);
-    if (item >= 0) {
-      const Item it0 = decode(p, item, pps);
-      write_q(it0.b, it0.g);
-    }
-    while (item >= 0) {
-      const Item it = decode(p, item, pps);
-      // the next queue entry, taken once this item's last S has been read (the
-      // producer publishes it only after issuing all of this item's tiles)
-      int nitem = -1;
+    Item it = get_item_all(0);
+    if (it.item >= 0) write_q(it.b, it.g);
+    while (it.item >= 0) {
+      // the next queue entry, taken once this item's last S has been read
+      Item nit;
+      nit.item = -1;
       const int lo_q = first_visible(p, it.kv, slot % S);
       float m = -INFINITY, l = 0.f;
       const float sl = p.scale_log2;
@@ -785,16 +859,8 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
         mbar_arrive(&p_full[uu & 1]);
         if (t == it.ntiles - 1) {
           // the last S of the item has been read: the next item's Q may go in
-          nitem = get_item_all(k + 1);
-          if (nitem >= 0) {
-            // (request, KV head) of the next item: item_start is ordered
-            int lo_i = 0, hi_i = p.B * p.kvh - 1;
-            while (lo_i < hi_i) {
-              const int mid = (lo_i + hi_i + 1) >> 1;
-              if (__ldg(&p.item_start[mid]) <= nitem) lo_i = mid; else hi_i = mid - 1;
-            }
-            write_q(lo_i / p.kvh, lo_i % p.kvh);
-          }
+          nit = get_item_all(k + 1);
+          if (nit.item >= 0) write_q(nit.b, nit.g);
         }
         if (any) {
           // O^T column q *= alpha_t[q] once PV of tile t - 1 is done (thread a: dim a)
@@ -845,13 +911,13 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
           p.out[((size_t)(it.b * S + jq) * p.n_heads + h) * 128 + d] = __float2bfloat16_rn(o[q] * inv);
         }
       } else {
-        float *po = p.part_o + (size_t)item * R * 128;
+        float *po = p.part_o + (size_t)it.item * R * 128;
 #pragma unroll
         for (int q = 0; q < NSLOT; ++q) {
           if (q >= R) break;
           po[q * 128 + d] = o[q];
         }
-        if (d < R) p.part_ml[(size_t)item * R + d] = s_ml[d];
+        if (d < R) p.part_ml[(size_t)it.item * R + d] = s_ml[d];
         __threadfence();
         bar_math();
         if (threadIdx.x == 0) *s_flag = atomicAdd(&p.tickets[it.bg], 1) == it.nsplit - 1;
@@ -899,7 +965,7 @@ __global__ void __launch_bounds__(kThreads, 2) attn_tc_kernel(const __grid_const
       mbar_arrive(&item_empty[k % NQ]);
       u += it.ntiles;
       ++k;
-      item = nitem;
+      it = nit;
     }
     if (!ok && lane == 0) raise_error(p.err, DFLASH_DERR_TIMEOUT);
   }
@@ -977,7 +1043,7 @@ cudaError_t launch_attention_tc(const AttnParams &a, const AttnScratch &w, cudaS
   const int cap = a.draft_window > 0 ? INT32_MAX : a.pages_per_req * atc::KT;
   cudaError_t e = launch_pdl(atc::attn_tc_prep_kernel, dim3(1), dim3(atc::kPrepThreads), 0, s,
                              a.kv_len, a.B, a.n_kv_heads, cap, a.window, a.draft_window,
-                             8 * sms, max_items, w.item_start, w.pps, w.order, a.err);
+                             8 * sms, max_items, w.item_start, w.pps, reinterpret_cast<int4 *>(w.order), a.err);
   if (e != cudaSuccess) return e;
   p.q = (const bf16 *)a.q;
   p.out = (bf16 *)a.out;
@@ -986,7 +1052,7 @@ cudaError_t launch_attention_tc(const AttnParams &a, const AttnScratch &w, cudaS
   p.item_start = w.item_start;
   p.pps_ptr = w.pps;
   p.counter = w.pps + 1;
-  p.order = w.order;
+  p.queue = reinterpret_cast<const int4 *>(w.order);
   p.part_o = w.part_o;
   p.part_ml = (float2 *)w.part_ml;
   p.tickets = w.tickets;

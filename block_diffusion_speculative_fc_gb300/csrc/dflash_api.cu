@@ -119,7 +119,7 @@ Layout plan(const dflash_config &c, size_t es) {
     L.att_bg = c.max_batch * c.n_kv_heads;
     L.att_item_start = take(4 * ((size_t)L.att_bg + 1));
     L.att_pps = take(8);
-    L.att_order = take(4 * items);
+    L.att_order = take(32 * items);   // the tensor-core kernel's queue: two int4 per item
     L.att_part_o = take(4 * items * R * 128);
     L.att_part_ml = take(8 * items * R);
     L.att_tickets = take(4 * (size_t)L.att_bg);

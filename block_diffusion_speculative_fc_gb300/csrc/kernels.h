@@ -114,7 +114,7 @@ struct AttnParams {
 struct AttnScratch {
   int *item_start;   // [max_batch * kvh + 1]
   int *pps;          // [2]: pages per split; the tensor-core kernel's work-queue position
-  int *order;        // [max_items] the tensor-core kernel's work queue
+  int *order;        // [max_items][8] the tensor-core kernel's work queue (two int4 per item)
   float *part_o;     // [max_items][R][128]
   float *part_ml;    // [max_items][R][2]
   int *tickets;      // [max_batch * kvh], zero between launches

@@ -189,7 +189,7 @@ AttnScratchLayout attn_scratch_layout(int B, int n_heads, int kvh, int S) {
   };
   L.item_start = take(4 * ((size_t)B * kvh + 1));
   L.pps = take(8);
-  L.order = take(4 * items);
+  L.order = take(32 * items);
   L.part_o = take(4 * items * R * 128);
   L.part_ml = take(8 * items * R);
   L.tickets = take(4 * (size_t)B * kvh);
