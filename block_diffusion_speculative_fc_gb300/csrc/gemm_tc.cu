@@ -257,7 +257,8 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
 // share a weight tile (consecutive tiles in the raster order
 // tile = feature tile * m_tiles + token tile) stream the same weight
 // k-blocks at the same time and all but the first read them from L2.  The
-// remaining tiles (the tail) are split stream-K: their flattened (tile,
+// remaining tiles (the tail: at least half a wave when there are full waves)
+// are split stream-K: their flattened (tile,
 // k-block) iterations are cut into Gt = min(G, tail iterations) equal
 // contiguous ranges, so every CTA that takes part holds at least one
 // iteration (a split tile's contributors are exactly the CTAs between its
@@ -1306,8 +1307,12 @@ cudaError_t launch_gemm_program(const GemmProblem *probs, int n, float *partials
   for (int i = 0; i < n; ++i) {
     tc::Phase &ph = p.ph[i];
     ph.G = (int)std::max<long long>(1, std::min<long long>(G, ph.total_iters));
-    // full waves of whole tiles when several token tiles share each weight tile
+    // full waves of whole tiles when several token tiles share each weight tile;
+    // a tail of fewer than half a wave of tiles would be split many ways
+    // (every tail tile merged from many shares at the end of the phase), so
+    // the last full wave joins the tail then
     ph.nfull = ph.m_tiles > 1 && ph.nseg > 0 ? ph.tiles / ph.G : 0;
+    if (ph.nfull > 0 && 2 * (ph.tiles - ph.nfull * ph.G) < ph.G) --ph.nfull;
   }
   const bool coop = n > 1;
   if (any_pair) {
