@@ -678,6 +678,49 @@ template <class C, int CHc, typename T>
 __device__ __forceinline__ void finish_tile(const EpiParams &e, uint32_t tacc, int bnt, int np,
                                             int rows, int m0, int n0, int tid, int f, float *merge,
                                             int *s_int, float *s_rstd) {
+  if (e.op == EPI_ARGMAX && e.ssq_in == nullptr && np == 1 && (bnt & 31) == 0) {
+    // lm_head argmax straight from TMEM: thread f holds vocabulary row n0 + f
+    // for 32 tokens at a time; a transpose-reduce over the warp's lanes (at
+    // offset s every lane keeps half of its 2s candidates and trades the other
+    // half with lane ^ s) leaves lane l with the warp's best key of token
+    // c0 + l; the four warps meet in shared memory, one atomic per token.
+    unsigned long long *xk = reinterpret_cast<unsigned long long *>(merge);   // [4][32]
+    const int lane = tid & 31, ew = tid >> 5;
+    const int n = n0 + f;
+    const bool fvalid = n < e.N;
+    for (int c0 = 0; c0 < bnt; c0 += 32) {
+      float v[32];
+      tmem_ld16(tacc + c0, v);
+      tmem_ld16(tacc + c0 + 16, v + 16);
+      unsigned long long k[32];
+#pragma unroll
+      for (int t = 0; t < 32; ++t) k[t] = fvalid ? argmax_key(v[t], n) : 0ull;
+#pragma unroll
+      for (int sft = 16; sft >= 1; sft >>= 1) {
+        const bool up = (lane & sft) != 0;
+#pragma unroll
+        for (int i = 0; i < sft; ++i) {
+          const unsigned long long send = up ? k[i] : k[i + sft];
+          const unsigned long long keep = up ? k[i + sft] : k[i];
+          const unsigned long long got = __shfl_xor_sync(0xffffffffu, send, sft);
+          k[i] = got > keep ? got : keep;
+        }
+      }
+      xk[ew * 32 + lane] = k[0];
+      epi_bar();
+      if (ew == 0) {
+        unsigned long long b = xk[lane];
+#pragma unroll
+        for (int w = 1; w < 4; ++w) {
+          const unsigned long long o = xk[w * 32 + lane];
+          b = o > b ? o : b;
+        }
+        if (c0 + lane < rows && b) atomicMax(e.argmax_keys + m0 + c0 + lane, b);
+      }
+      epi_bar();
+    }
+    return;
+  }
   float *st0 = merge + (C::MERGE_BYTES - CHc * 128 * 4) / 4, *st1 = merge;
   for (int c0 = 0; c0 < bnt; c0 += CHc) {
     float v[CHc];
