@@ -721,6 +721,59 @@ __device__ __forceinline__ void finish_tile(const EpiParams &e, uint32_t tacc, i
     }
     return;
   }
+  if (e.op == EPI_RESID_NORM && e.ssq_in == nullptr && np == 1 && (bnt & 31) == 0 &&
+      sizeof(T) == 2 && n0 + 128 <= e.N) {
+    // residual + next norm's operand straight from TMEM (no staging through
+    // shared memory, which the tensor cores and TMA keep busy): thread f owns
+    // feature n0 + f for 32 tokens at a time -- every residual load of the
+    // chunk first, then coalesced stores of x and x * g (a warp writes 32
+    // consecutive features of a row); the per-token sum of squares of the 128
+    // features by a warp transpose-reduce and the four warps in shared memory.
+    float *red = merge;   // [4][32]
+    const int lane = tid & 31, ew = tid >> 5;
+    const int n = n0 + f;
+    const float g = to_f32(((const T *)e.norm_gain)[n]);
+    for (int c0 = 0; c0 < bnt; c0 += 32) {
+      float v[32];
+      tmem_ld16(tacc + c0, v);
+      tmem_ld16(tacc + c0 + 16, v + 16);
+      const int nr = min(32, rows - c0);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {   // 16 tokens at a time: every load before any store
+        float *xr = e.out_f32 + (int64_t)(m0 + c0 + 16 * h) * e.ld + n;
+        T *ar = (T *)e.out_act + (int64_t)(m0 + c0 + 16 * h) * e.ld + n;
+        float xo[16];
+#pragma unroll
+        for (int t = 0; t < 16; ++t) xo[t] = 16 * h + t < nr ? xr[(int64_t)t * e.ld] : 0.f;
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+          const float y = v[16 * h + t] + xo[t];
+          if (16 * h + t < nr) {
+            xr[(int64_t)t * e.ld] = y;
+            ar[(int64_t)t * e.ld] = from_f32<T>(y * g);
+          }
+          v[16 * h + t] = y * y;
+        }
+      }
+#pragma unroll
+      for (int sft = 16; sft >= 1; sft >>= 1) {
+        const bool up = (lane & sft) != 0;
+#pragma unroll
+        for (int i = 0; i < sft; ++i) {
+          const float send = up ? v[i] : v[i + sft];
+          const float keep = up ? v[i + sft] : v[i];
+          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, sft);
+        }
+      }
+      red[ew * 32 + lane] = v[0];
+      epi_bar();
+      if (ew == 0 && lane < nr)
+        e.ssq_out[(int64_t)(n0 >> 7) * e.ssq_ld + m0 + c0 + lane] =
+            (red[lane] + red[32 + lane]) + (red[64 + lane] + red[96 + lane]);
+      epi_bar();
+    }
+    return;
+  }
   float *st0 = merge + (C::MERGE_BYTES - CHc * 128 * 4) / 4, *st1 = merge;
   for (int c0 = 0; c0 < bnt; c0 += CHc) {
     float v[CHc];
