@@ -723,36 +723,49 @@ __device__ __forceinline__ void finish_tile(const EpiParams &e, uint32_t tacc, i
   }
   if (e.op == EPI_RESID_NORM && e.ssq_in == nullptr && np == 1 && (bnt & 31) == 0 &&
       sizeof(T) == 2 && n0 + 128 <= e.N) {
-    // residual + next norm's operand straight from TMEM (no staging through
-    // shared memory, which the tensor cores and TMA keep busy): thread f owns
-    // feature n0 + f for 32 tokens at a time -- every residual load of the
-    // chunk first, then coalesced stores of x and x * g (a warp writes 32
-    // consecutive features of a row); the per-token sum of squares of the 128
-    // features by a warp transpose-reduce and the four warps in shared memory.
+    // Residual + next norm's operand straight from TMEM (no staging through
+    // shared memory): thread f owns feature n0 + f.  The tile goes in units of
+    // 16 tokens; the residual rows of the next unit are loaded into registers
+    // before this unit's stores and the unit after that is prefetched into L1,
+    // so the loads' latency (long while the TMA stream keeps L2 busy) overlaps
+    // the stores.  Per 32 tokens the sums of squares of the 128 features come
+    // from a warp transpose-reduce and the four warps in shared memory.
     float *red = merge;   // [4][32]
     const int lane = tid & 31, ew = tid >> 5;
     const int n = n0 + f;
     const float g = to_f32(((const T *)e.norm_gain)[n]);
-    for (int c0 = 0; c0 < bnt; c0 += 32) {
-      float v[32];
-      tmem_ld16(tacc + c0, v);
-      tmem_ld16(tacc + c0 + 16, v + 16);
-      const int nr = min(32, rows - c0);
+    const int units = bnt >> 4;
+    auto row = [&](int u, int t) { return (int64_t)(m0 + 16 * u + t) * e.ld + n; };
+    auto load_unit = [&](int u, float *x) {
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {   // 16 tokens at a time: every load before any store
-        float *xr = e.out_f32 + (int64_t)(m0 + c0 + 16 * h) * e.ld + n;
-        T *ar = (T *)e.out_act + (int64_t)(m0 + c0 + 16 * h) * e.ld + n;
+      for (int t = 0; t < 16; ++t) x[t] = 16 * u + t < rows ? e.out_f32[row(u, t)] : 0.f;
+    };
+    auto prefetch_unit = [&](int u) {   // lane t < 16: row t of the unit (one line per warp)
+      if (u < units && lane < 16 && 16 * u + lane < rows) prefetch_l1(e.out_f32 + row(u, lane));
+    };
+    float xn[16];
+    prefetch_unit(1);
+    load_unit(0, xn);
+    for (int c0 = 0; c0 < bnt; c0 += 32) {
+      float sq[32];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int u = (c0 >> 4) + h;
         float xo[16];
 #pragma unroll
-        for (int t = 0; t < 16; ++t) xo[t] = 16 * h + t < nr ? xr[(int64_t)t * e.ld] : 0.f;
+        for (int t = 0; t < 16; ++t) xo[t] = xn[t];
+        prefetch_unit(u + 2);
+        if (u + 1 < units) load_unit(u + 1, xn);
+        float v[16];
+        tmem_ld16(tacc + 16 * u, v);
 #pragma unroll
         for (int t = 0; t < 16; ++t) {
-          const float y = v[16 * h + t] + xo[t];
-          if (16 * h + t < nr) {
-            xr[(int64_t)t * e.ld] = y;
-            ar[(int64_t)t * e.ld] = from_f32<T>(y * g);
+          const float y = v[t] + xo[t];
+          if (16 * u + t < rows) {
+            e.out_f32[row(u, t)] = y;
+            ((T *)e.out_act)[row(u, t)] = from_f32<T>(y * g);
           }
-          v[16 * h + t] = y * y;
+          sq[16 * h + t] = y * y;
         }
       }
 #pragma unroll
@@ -760,14 +773,14 @@ __device__ __forceinline__ void finish_tile(const EpiParams &e, uint32_t tacc, i
         const bool up = (lane & sft) != 0;
 #pragma unroll
         for (int i = 0; i < sft; ++i) {
-          const float send = up ? v[i] : v[i + sft];
-          const float keep = up ? v[i + sft] : v[i];
-          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, sft);
+          const float send = up ? sq[i] : sq[i + sft];
+          const float keep = up ? sq[i + sft] : sq[i];
+          sq[i] = keep + __shfl_xor_sync(0xffffffffu, send, sft);
         }
       }
-      red[ew * 32 + lane] = v[0];
+      red[ew * 32 + lane] = sq[0];
       epi_bar();
-      if (ew == 0 && lane < nr)
+      if (ew == 0 && c0 + lane < rows)
         e.ssq_out[(int64_t)(n0 >> 7) * e.ssq_ld + m0 + c0 + lane] =
             (red[lane] + red[32 + lane]) + (red[64 + lane] + red[96 + lane]);
       epi_bar();
