@@ -350,8 +350,9 @@ struct Cfg {
   static constexpr int A_BYTES = BN * BK * 2;
   static constexpr int SLOT_BYTES = W_BYTES + A_BYTES;
   // SPLIT (256-token tiles with pairs in the program): a paired k-block takes
-  // one slot, [W_gate | W_up | activations of PT = 128 tokens], and its two
-  // 128-column accumulators fill one 256-column buffer; plain phases keep
+  // one slot, [W_gate | W_up | activations of PT = 128 tokens], and its
+  // accumulator (tokens in lanes, gate then up features in 256 columns) fills
+  // one 256-column buffer; plain phases keep
   // [W | activations of 256 tokens].  Smaller tiles pair two slots (the
   // activation tile rides in the first).
   static constexpr bool SPLIT = PAIRABLE && BN == 256;
@@ -422,20 +423,23 @@ __device__ __forceinline__ bool mma_kblocks(uint32_t &it, int kb0, int kb1, uint
                                             uint8_t *slots, uint64_t *full, uint64_t *empty,
                                             const Params &p) {
   if constexpr (NS == 3) {
-    constexpr uint32_t idesc = idesc_bf16(128, C::PT);
+    // [W_gate | W_up] is one 256-row operand (the up rows follow the gate rows
+    // 16 KB on, 8-row groups 1 KB apart): one M=128 (tokens) x N=256 MMA per
+    // k-step reads the token tile once; D lanes are tokens, columns 0..127
+    // the gate features and 128..255 the up features
+    constexpr uint32_t idesc = idesc_bf16(128, 2 * C::PT);
     for (int kb = kb0; kb < kb1; ++kb) {
       const int s0 = it % C::SLOTS;
       if (!mbar_wait(&full[s0], (it / C::SLOTS) & 1)) return false;
       if (it == 0) stamp(p, 4);
       tc_fence_after();
       const uint32_t st0 = su32(slots + s0 * C::SLOT_BYTES);
-      const uint64_t gdesc = sw128_desc(st0), udesc = sw128_desc(st0 + C::W_BYTES);
+      const uint64_t wdesc = sw128_desc(st0);
       const uint64_t adesc = sw128_desc(st0 + 2 * C::W_BYTES);
 #pragma unroll
       for (int kk = 0; kk < BK / 16; ++kk) {
         const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
-        umma_bf16(d0, gdesc + 2 * kk, adesc + 2 * kk, idesc, acc);
-        umma_bf16(d0 + C::PT, udesc + 2 * kk, adesc + 2 * kk, idesc, acc);
+        umma_bf16(d0, adesc + 2 * kk, wdesc + 2 * kk, idesc, acc);
       }
       umma_commit(&empty[s0]);
       it += 1;
@@ -678,6 +682,33 @@ template <class C, int CHc, typename T>
 __device__ __forceinline__ void finish_tile(const EpiParams &e, uint32_t tacc, int bnt, int np,
                                             int rows, int m0, int n0, int tid, int f, float *merge,
                                             int *s_int, float *s_rstd) {
+  if (C::SPLIT && np == 2) {
+    // gate/up pair tile of the 256-token layout: TMEM lane f is token m0 + f,
+    // columns 0..127 the gate and bnt.. the up features n0 .. n0+127; each
+    // thread writes its token's 128 outputs (16-byte stores), scaled by the
+    // token's deferred-RMSNorm factor
+    const bool live = f < rows;
+    const float sc = e.ssq_in && live ? s_rstd[f] : 1.f;
+    const int nvalid = e.N / 2;
+    T *dst = (T *)e.out_act + (int64_t)(m0 + (live ? f : 0)) * e.ld + n0;
+    for (int c0 = 0; c0 < 128; c0 += 16) {
+      float gv[16], uv[16];
+      tmem_ld16(tacc + c0, gv);
+      tmem_ld16(tacc + bnt + c0, uv);
+      uint4 pk[2];
+      T *pt = reinterpret_cast<T *>(pk);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) pt[k] = from_f32<T>(silu(gv[k] * sc) * (uv[k] * sc));
+      if (live && n0 + c0 + 16 <= nvalid) {
+        reinterpret_cast<uint4 *>(dst + c0)[0] = pk[0];
+        reinterpret_cast<uint4 *>(dst + c0)[1] = pk[1];
+      } else if (live) {
+        for (int k = 0; k < 16; ++k)
+          if (n0 + c0 + k < nvalid) dst[c0 + k] = pt[k];
+      }
+    }
+    return;
+  }
   if (e.op == EPI_ARGMAX && e.ssq_in == nullptr && np == 1 && (bnt & 31) == 0) {
     // lm_head argmax straight from TMEM: thread f holds vocabulary row n0 + f
     // for 32 tokens at a time; a transpose-reduce over the warp's lanes (at
