@@ -1041,9 +1041,12 @@ cudaError_t launch_attention_tc(const AttnParams &a, const AttnScratch &w, cudaS
   if (sms <= 0) sms = 1;
   const int max_items = (int)attention_mma_scratch_items(a.B, a.n_kv_heads);
   const int cap = a.draft_window > 0 ? INT32_MAX : a.pages_per_req * atc::KT;
+  // about one item per CTA (two CTAs per SM): measured against four and eight
+  // per SM, fewer items cut the per-item start and the split merges; one per
+  // SM left large items that unbalanced the CTAs at block size 8
   cudaError_t e = launch_pdl(atc::attn_tc_prep_kernel, dim3(1), dim3(atc::kPrepThreads), 0, s,
                              a.kv_len, a.B, a.n_kv_heads, cap, a.window, a.draft_window,
-                             8 * sms, max_items, w.item_start, w.pps, reinterpret_cast<int4 *>(w.order), a.err);
+                             2 * sms, max_items, w.item_start, w.pps, reinterpret_cast<int4 *>(w.order), a.err);
   if (e != cudaSuccess) return e;
   p.q = (const bf16 *)a.q;
   p.out = (bf16 *)a.out;
