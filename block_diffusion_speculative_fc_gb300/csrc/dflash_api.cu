@@ -982,6 +982,12 @@ int dflash_test_set_attention(dflash_handle *h, int32_t kernel) {
   return DFLASH_OK;
 }
 
+int dflash_test_set_head_pairs(int32_t on) {
+  if (on != 0 && on != 1) return fail(DFLASH_EINVAL, "head pairs must be 0 or 1");
+  gemm_tc_set_head_pairs(on == 1);
+  return DFLASH_OK;
+}
+
 int dflash_accept_commit(dflash_handle *h, int32_t batch, const int32_t *draft_ids,
                          const int32_t *posterior, int32_t *seq_len, int32_t *accept_len,
                          int32_t *commit_len, int32_t *bonus, int32_t *out_tokens,

@@ -63,8 +63,9 @@ struct Phase {
   CUtensorMap tmW[kMaxSeg];       // weights, box {BK, 128}
   EpiParams epi[kMaxSeg];
   int seg_ntiles[kMaxSeg];        // 128-feature tiles per segment (pairs count once)
-  int seg_half[kMaxSeg];          // pair: row offset of the "up" half
+  int seg_half[kMaxSeg];          // pair: row offset of the second half
   int nseg, pair;
+  int nstep;                      // features between consecutive tiles of a segment
   int M, K, KB, m_tiles, tiles;
   int bnt;                        // token rows per tile in this phase
   int k_per_src;
@@ -275,7 +276,7 @@ struct Sched {
 // The scalars of a phase that the inner loops use, read once per phase into
 // registers.
 struct PhaseScalars {
-  int KB, k_per_src, m_tiles, nseg, pair, M, G, bnt, nfull, Gt;
+  int KB, k_per_src, m_tiles, nseg, pair, M, G, bnt, nfull, Gt, nstep;
   long long total, tail_base, tail_total;
   int seg_ntiles[kMaxSeg];
 };
@@ -290,6 +291,7 @@ __device__ __forceinline__ PhaseScalars load_scalars(const Phase &ph) {
   ps.G = ph.G;
   ps.bnt = ph.bnt;
   ps.nfull = ph.nfull;
+  ps.nstep = ph.nstep;
   ps.total = ph.total_iters;
   ps.tail_base = (long long)ph.nfull * ph.G * ph.KB;
   ps.tail_total = ps.total - ps.tail_base;
@@ -340,7 +342,7 @@ __device__ __forceinline__ void locate(const PhaseScalars &ps, int tile, int &se
       seg = i + 1;
     }
   }
-  n0 = nt * 128;
+  n0 = nt * ps.nstep;
 }
 
 template <int BN, bool PAIRABLE>
@@ -682,6 +684,99 @@ template <class C, int CHc, typename T>
 __device__ __forceinline__ void finish_tile(const EpiParams &e, uint32_t tacc, int bnt, int np,
                                             int rows, int m0, int n0, int tid, int f, float *merge,
                                             int *s_int, float *s_rstd) {
+  if (C::SPLIT && np == 2 && e.op == EPI_QKV) {
+    // Head-pair tile of the 256-token layout (QKV, 128-wide heads): TMEM lane
+    // f is token m0 + f, columns 0..127 head n0 / 128 and bnt.. the next head.
+    // A thread holds its token's whole head rows, so the per-head RMSNorm
+    // needs no exchange between threads and the rotary partners (d, d + 64)
+    // are the thread's own columns; each head row leaves in 16-byte stores.
+    // The arithmetic is head_ops_d128's: the deferred norm's row scale, the
+    // head RMSNorm and its gain, then the rotation.
+    const bool live = f < rows;
+    const int m = m0 + (live ? f : 0);
+    const float sc = e.ssq_in && live ? s_rstd[f] : 1.f;
+    const float4 *rope =
+        reinterpret_cast<const float4 *>(e.rope + (int64_t)(live ? e.row_pos[m] : 0) * 64);
+    // the token's (cos, sin) row (512 bytes) comes into L1 while the sums of
+    // squares are formed
+#pragma unroll
+    for (int j = 0; j < 4; ++j) prefetch_l1(rope + 8 * j);
+    const int kvd = e.n_kv_heads * 128;
+    float rstd[2];
+    T *dst[2];
+    const T *gain[2];
+    bool nr[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      float ss[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int c0 = 0; c0 < 128; c0 += 32) {
+        float v[32];
+        tmem_ld16(tacc + h * bnt + c0, v);
+        tmem_ld16(tacc + h * bnt + c0 + 16, v + 16);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const float x = v[k] * sc;
+          ss[k & 3] += x * x;
+        }
+      }
+      const int hg = (n0 >> 7) + h;
+      const int kind = hg < e.n_heads ? 0 : (hg < e.n_heads + e.n_kv_heads ? 1 : 2);
+      const int head = kind == 0 ? hg : (kind == 1 ? hg - e.n_heads : hg - e.n_heads - e.n_kv_heads);
+      nr[h] = kind != 2;
+      rstd[h] = rsqrtf(((ss[0] + ss[1]) + (ss[2] + ss[3])) / 128.f + e.eps);
+      gain[h] = (const T *)(kind == 0 ? e.q_gain : e.k_gain);
+      dst[h] = kind == 0 ? (T *)e.q_out + (int64_t)m * e.n_heads * 128 + head * 128
+                         : (T *)(kind == 1 ? e.k_out : e.v_out) + (int64_t)m * kvd + head * 128;
+    }
+    for (int c0 = 0; c0 < 64; c0 += 16) {
+      // (cos, sin) of elements c0 .. c0+15: two per float4
+      float4 cs[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) cs[j] = rope[(c0 >> 1) + j];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float lo[16], hi[16];
+        tmem_ld16(tacc + h * bnt + c0, lo);
+        tmem_ld16(tacc + h * bnt + 64 + c0, hi);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          lo[k] *= sc;
+          hi[k] *= sc;
+        }
+        if (nr[h]) {
+          // the gains are the same for every thread (broadcast loads)
+          uint4 gw[4];
+          gw[0] = reinterpret_cast<const uint4 *>(gain[h] + c0)[0];
+          gw[1] = reinterpret_cast<const uint4 *>(gain[h] + c0)[1];
+          gw[2] = reinterpret_cast<const uint4 *>(gain[h] + 64 + c0)[0];
+          gw[3] = reinterpret_cast<const uint4 *>(gain[h] + 64 + c0)[1];
+          const T *gl = reinterpret_cast<const T *>(gw), *gh = gl + 16;
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const float c = (k & 1) ? cs[k >> 1].z : cs[k >> 1].x;
+            const float sn = (k & 1) ? cs[k >> 1].w : cs[k >> 1].y;
+            const float a = lo[k] * rstd[h] * to_f32(gl[k]), b = hi[k] * rstd[h] * to_f32(gh[k]);
+            lo[k] = a * c - b * sn;
+            hi[k] = b * c + a * sn;
+          }
+        }
+        uint4 pk[4];
+        T *pt = reinterpret_cast<T *>(pk);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          pt[k] = from_f32<T>(lo[k]);
+          pt[16 + k] = from_f32<T>(hi[k]);
+        }
+        if (live) {
+          reinterpret_cast<uint4 *>(dst[h] + c0)[0] = pk[0];
+          reinterpret_cast<uint4 *>(dst[h] + c0)[1] = pk[1];
+          reinterpret_cast<uint4 *>(dst[h] + 64 + c0)[0] = pk[2];
+          reinterpret_cast<uint4 *>(dst[h] + 64 + c0)[1] = pk[3];
+        }
+      }
+    }
+    return;
+  }
   if (C::SPLIT && np == 2) {
     // gate/up pair tile of the 256-token layout: TMEM lane f is token m0 + f,
     // columns 0..127 the gate and bnt.. the up features n0 .. n0+127; each
@@ -1307,18 +1402,31 @@ cudaError_t set_attr() {
                               cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
 }
 
-int pick_bn(int M, bool) {
+int pick_bn(int M) {
   return M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
 }
 // Token rows of a tile: a paired phase of a 256-token program uses the SPLIT
 // layout's 128-token tiles.
 int tile_rows(int BN, bool pair) { return pair && BN == 256 ? 128 : BN; }
 
+bool g_head_pairs = true;
+
+// A QKV GEMM of 128-wide heads in a 256-token program runs as head pairs:
+// tiles of two consecutive heads (256 features) by 128 tokens in the SPLIT
+// layout, so that the epilogue finds whole head rows in each TMEM lane.
+bool head_pairs(const GemmProblem &P, int BN) {
+  const EpiParams &e = P.seg[0].epi;
+  return g_head_pairs && BN == 256 && P.nseg == 1 && e.op == EPI_QKV && e.head_dim == 128 &&
+         P.seg[0].N == e.N && e.N % 256 == 0;
+}
+
 // One phase of a program from a problem description; returns its tile count.
 bool build_phase(tc::Phase &ph, const GemmProblem &P, int BN, int counter_off) {
   memset(&ph, 0, sizeof(ph));
   if (P.K % tc::BK || P.A.k_per_src % tc::BK) return false;
-  const bool pair = P.seg[0].epi.op == EPI_SWIGLU;
+  const bool swiglu = P.seg[0].epi.op == EPI_SWIGLU;
+  const bool hp = head_pairs(P, BN);
+  const bool pair = swiglu || hp;
   const int bnt = tile_rows(BN, pair);
   for (int j = 0; j < P.A.n_src; ++j)
     if (!encode_2d(&ph.tmA[j], P.A.ptr[j], (uint64_t)P.M, (uint64_t)P.A.k_per_src, (uint64_t)P.A.ld, bnt))
@@ -1329,13 +1437,16 @@ bool build_phase(tc::Phase &ph, const GemmProblem &P, int BN, int counter_off) {
     if (!encode_2d(&ph.tmW[i], g.W, (uint64_t)g.N, (uint64_t)P.K, (uint64_t)g.ldw, 128))
       return false;
     ph.epi[i] = g.epi;
+    // a gate/up pair: gate rows n0.., up rows N/2 + n0..; a head pair: rows
+    // n0 .. n0+255 (tiles 256 features apart)
     const int n = pair ? g.N / 2 : g.N;
     ph.seg_ntiles[i] = (n + 127) / 128;
-    ph.seg_half[i] = pair ? g.N / 2 : 0;
+    ph.seg_half[i] = swiglu ? g.N / 2 : hp ? 128 : 0;
     ntiles += ph.seg_ntiles[i];
   }
   ph.nseg = P.nseg;
   ph.pair = pair ? 1 : 0;
+  ph.nstep = hp ? 256 : 128;
   ph.M = P.M;
   ph.K = P.K;
   ph.KB = P.K / tc::BK;
@@ -1353,10 +1464,12 @@ bool build_phase(tc::Phase &ph, const GemmProblem &P, int BN, int counter_off) {
 // Partial-tile scratch: per CTA two slots of (pair ? 2 : 1) * BN * 128 fp32, at most 256 * 128.
 int gemm_tc_trace_slots() { return tc::kTraceSlots; }
 
+void gemm_tc_set_head_pairs(bool on) { g_head_pairs = on; }
+
 size_t gemm_tc_partials_bytes() { return (size_t)kTcMaxCtas * 2 * 256 * 128 * 4; }
 
 int gemm_tc_tiles(int n_tiles, int M, bool pair) {
-  const int bnt = tile_rows(pick_bn(M, pair), pair);
+  const int bnt = tile_rows(pick_bn(M), pair);
   return n_tiles * ((M + bnt - 1) / bnt);
 }
 
@@ -1399,12 +1512,12 @@ cudaError_t launch_gemm_program(const GemmProblem *probs, int n, float *partials
     return cudaErrorInvalidValue;
   const int M = probs[0].M;
   if (M <= 0) return cudaSuccess;
+  const int BN = pick_bn(M);
   bool any_pair = false;
   for (int i = 0; i < n; ++i) {
     if (probs[i].M != M || probs[i].nseg <= 0) return cudaErrorInvalidValue;
-    any_pair |= probs[i].seg[0].epi.op == EPI_SWIGLU;
+    any_pair |= probs[i].seg[0].epi.op == EPI_SWIGLU || head_pairs(probs[i], BN);
   }
-  const int BN = pick_bn(M, any_pair);
   tc::Params p;
   memset(&p, 0, sizeof(p));
   int off = 0;

@@ -223,6 +223,7 @@ cudaError_t launch_gemm_program(const GemmProblem *probs, int n, float *partials
 size_t gemm_tc_partials_bytes();
 int gemm_tc_trace_slots();   // timestamps per CTA written by a traced launch
 int gemm_tc_tiles(int n_tiles, int M, bool pair);
+void gemm_tc_set_head_pairs(bool on);   // QKV head-pair tiles (default on)
 cudaError_t prepare_gemm_tc();
 cudaError_t launch_attention_mma(const AttnParams &p, const AttnScratch &w, cudaStream_t s);
 size_t attention_mma_scratch_items(int max_batch, int kvh);

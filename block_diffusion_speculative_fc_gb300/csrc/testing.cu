@@ -163,6 +163,82 @@ __global__ void e4m3_encode_kernel(const float *__restrict__ x, int n, float sca
 }
 }  // namespace
 
+// ------------------------------------------------------------------ QKV GEMM
+namespace {
+size_t align256(size_t n) { return (n + 255) & ~(size_t)255; }
+size_t qkv_tiles(int32_t M, int32_t N) { return (size_t)gemm_tc_tiles((N + 127) / 128, M, false); }
+}  // namespace
+
+extern "C" size_t dflash_test_qkv_scratch(int32_t M, int32_t N, int32_t max_position) {
+  if (M <= 0 || N <= 0 || max_position <= 0) return 0;
+  return 256 + gemm_tc_partials_bytes() + align256(4 * qkv_tiles(M, N)) +
+         (size_t)max_position * 64 * sizeof(float2);
+}
+
+extern "C" int dflash_test_qkv(int32_t M, int32_t K, int32_t n_heads, int32_t n_kv_heads,
+                               int32_t head_dim, int32_t max_position, float rope_theta, float eps,
+                               const void *A, const void *W, const float *ssq, const void *q_gain,
+                               const void *k_gain, const int32_t *row_pos, void *q_out,
+                               void *k_out, void *v_out, void *scratch, size_t scratch_bytes,
+                               dflash_stream_t stream) {
+  if (M <= 0 || K <= 0 || n_heads <= 0 || n_kv_heads <= 0 || max_position <= 0 || !A || !W ||
+      !q_gain || !k_gain || !row_pos || !q_out || !k_out || !v_out || !scratch)
+    return DFLASH_EINVAL;
+  if (head_dim != 128 && head_dim != 64) return DFLASH_EUNSUPPORTED;
+  if (K % 128 || !(rope_theta > 0.f) || !(eps >= 0.f)) return DFLASH_EINVAL;
+  const int N = (n_heads + 2 * n_kv_heads) * head_dim;
+  if (N % 128) return DFLASH_EUNSUPPORTED;
+  if (scratch_bytes < dflash_test_qkv_scratch(M, N, max_position)) return DFLASH_ECAPACITY;
+  cudaStream_t s = (cudaStream_t)stream;
+  GemmProblem P;
+  std::memset(&P, 0, sizeof(P));
+  P.A.ptr[0] = A;
+  P.A.ld = K;
+  P.A.k_per_src = K;
+  P.A.n_src = 1;
+  P.M = M;
+  P.K = K;
+  GemmSeg &g = P.seg[P.nseg++];
+  g.W = W;
+  g.ldw = K;
+  g.N = N;
+  char *base = (char *)scratch;
+  unsigned int *err = (unsigned int *)base;
+  float *partials = (float *)(base + 256);
+  int *counters = (int *)(base + 256 + gemm_tc_partials_bytes());
+  float2 *rope = (float2 *)(base + 256 + gemm_tc_partials_bytes() + align256(4 * qkv_tiles(M, N)));
+  EpiParams &e = g.epi;
+  std::memset(&e, 0, sizeof(e));
+  e.op = EPI_QKV;
+  e.N = N;
+  e.n_heads = n_heads;
+  e.n_kv_heads = n_kv_heads;
+  e.head_dim = head_dim;
+  e.eps = eps;
+  e.q_out = q_out;
+  e.k_out = k_out;
+  e.v_out = v_out;
+  e.q_gain = q_gain;
+  e.k_gain = k_gain;
+  e.row_pos = row_pos;
+  e.rope = rope;
+  if (ssq) {
+    e.ssq_in = ssq;
+    e.ssq_parts = K / 128;
+    e.ssq_ld = M;
+    e.norm_eps = eps;
+    e.inv_h = 1.0f / (float)K;
+  }
+  if (cudaMemsetAsync(base, 0, 256, s) != cudaSuccess) return DFLASH_ECUDA;
+  if (cudaMemsetAsync(counters, 0, 4 * qkv_tiles(M, N), s) != cudaSuccess) return DFLASH_ECUDA;
+  if (prepare_gemm_tc() != cudaSuccess) return DFLASH_ECUDA;
+  if (launch_rope_table(rope, max_position, head_dim, rope_theta, s) != cudaSuccess)
+    return DFLASH_ECUDA;
+  if (launch_gemm_tc(P, partials, counters, (int)qkv_tiles(M, N), err, s) != cudaSuccess)
+    return DFLASH_ECUDA;
+  return DFLASH_OK;
+}
+
 extern "C" int dflash_test_e4m3_encode(const float *x, int32_t n, float scale, uint8_t *codes,
                                        dflash_stream_t stream) {
   if (n < 0 || (n > 0 && (!x || !codes)) || !(scale > 0.f)) return DFLASH_EINVAL;

@@ -70,6 +70,35 @@ int dflash_test_gemm_program_traced(int32_t n_phases, int32_t M, const int32_t *
                                     void *const *out, void *scratch, size_t scratch_bytes,
                                     unsigned long long *trace, dflash_stream_t stream);
 
+/*
+ * The QKV projection of a draft layer on its own (the tensor-core GEMM with
+ * its EPI_QKV epilogue): Y = r[m] * (A W^T) with r[m] = 1 / sqrt(sum_t
+ * ssq[t*M + m] / K + eps) when ssq is non-NULL (the deferred input RMSNorm:
+ * A holds x * g, ssq the sums of squares of x's 128-column parts), else 1.
+ * Column blocks of Y: n_heads query heads, then n_kv_heads key heads, then
+ * n_kv_heads value heads, head_dim wide each.  Query and key heads get the
+ * per-head RMSNorm (gain q_gain or k_gain, head_dim bf16 values, epsilon
+ * eps), then rotate-half RoPE at position row_pos[m] with frequencies
+ * rope_theta^(-2i/head_dim); value heads are stored as they are.
+ *   A        device bf16 [M, K];  W device bf16 [N, K], N = (n_heads +
+ *            2 n_kv_heads) * head_dim, a multiple of 128
+ *   ssq      device float32 [K/128, M] or NULL
+ *   row_pos  device int32 [M], every value in [0, max_position)
+ *   q_out    device bf16 [M, n_heads * head_dim]; k_out, v_out device bf16
+ *            [M, n_kv_heads * head_dim]
+ *   scratch  device, at least dflash_test_qkv_scratch(M, N, max_position)
+ *            bytes; its first 4 bytes are the device error word after the call
+ * head_dim is 64 or 128; K a multiple of 128.  Returns DFLASH_EINVAL,
+ * DFLASH_EUNSUPPORTED or DFLASH_ECAPACITY (scratch too small) on bad
+ * arguments, DFLASH_ECUDA when a launch fails; nothing is launched then.
+ */
+size_t dflash_test_qkv_scratch(int32_t M, int32_t N, int32_t max_position);
+int dflash_test_qkv(int32_t M, int32_t K, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
+                    int32_t max_position, float rope_theta, float eps, const void *A,
+                    const void *W, const float *ssq, const void *q_gain, const void *k_gain,
+                    const int32_t *row_pos, void *q_out, void *k_out, void *v_out, void *scratch,
+                    size_t scratch_bytes, dflash_stream_t stream);
+
 /* The FP8 encoder of the K/V cache epilogue on its own: codes[i] = the OCP
  * E4M3 code of x[i] / scale (IEEE float32 division, nearest code, ties to the
  * even code, saturation at +-448), the same device function the injection
@@ -114,6 +143,13 @@ int dflash_test_set_fusion(dflash_handle *h, int32_t on);
  * per (request, KV head), more (request, KV head) pairs than half the SMs,
  * bf16 cache), else the mma.sync kernels; 1 the mma.sync kernels only. */
 int dflash_test_set_attention(dflash_handle *h, int32_t kernel);
+
+/* Tiling of the QKV GEMM (128-wide heads, more than 128 rows) for every
+ * later launch of this process: 1 (default) tiles of two consecutive heads
+ * by 128 tokens, whose epilogue reads whole head rows from the tensor-memory
+ * accumulator; 0 tiles of 128 features by 256 tokens with the staged
+ * epilogue.  Returns DFLASH_EINVAL for other values. */
+int dflash_test_set_head_pairs(int32_t on);
 
 #ifdef __cplusplus
 }
