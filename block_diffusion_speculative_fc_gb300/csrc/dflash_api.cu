@@ -26,6 +26,7 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 struct Layout {
   size_t err, rope, x, h, xg, ssq, qb, kb, vb, attn, act, row_pos, keys, yg, ssq_y, slot, rpos;
   size_t skeys, stickets;   // race keys / tickets of sampled verification, zero between calls
+  size_t cfeat, coff, crows, ccount;   // prefix-valid compaction of injected rows (bf16)
   size_t tc_partials, tc_counters, tc_grid_bar;
   int tc_max_tiles;
   size_t att_item_start, att_pps, att_order, att_part_o, att_part_ml, att_tickets;
@@ -98,6 +99,14 @@ Layout plan(const dflash_config &c, size_t es) {
   L.rpos = take(4 * R);
   L.skeys = take(8 * (size_t)c.max_batch);
   L.stickets = take(4 * (size_t)c.max_batch);
+  if (es == 2) {
+    // the committed rows of a verify block, gathered: up to max_batch *
+    // block_size rows of the concatenated target features
+    L.cfeat = take(es * std::min(M, R) * (size_t)c.n_sel * c.target_hidden);
+    L.coff = take(4 * (size_t)c.max_batch);
+    L.crows = take(4 * (size_t)c.max_batch);
+    L.ccount = take(4);
+  }
   if (es == 2) {
     // tensor-core GEMM scratch: stream-K partial tiles and per-tile tickets
     const int Mb = (int)M, Mr = c.max_rows;
@@ -515,6 +524,35 @@ int dflash_inject_context(dflash_handle *h, const dflash_kv *kv, int32_t batch, 
   // when that launch is the call's last, so is the kv_len update
   const bool fused = h->store == ST_BF16 && h->fuse;
   bool advanced = false;
+  // Prefix-valid compaction ("Inside SGLang", Step 7: only the accepted rows
+  // of a verify block are written): when the feature rows fit one chunk of
+  // the dense [max_batch, block_size] bound, the rows of some request are
+  // gathered first and fc and the K/V projections run on them alone; the
+  // launches read the row count from the device.  At most 128 rows are one
+  // token tile whatever the count, so there it would only add a launch.
+  const int64_t gather_cap = std::min<int64_t>(c.max_rows, (int64_t)c.max_batch * c.block_size);
+  bool aligned = true;   // the gather copies 16-byte vectors
+  for (int j = 0; j < c.n_sel; ++j) aligned = aligned && ((uintptr_t)target_feats[j] & 15) == 0;
+  const bool compact =
+      fused && aligned && total_rows > 128 && total_rows <= gather_cap && c.n_sel <= kMaxSrc;
+  const int32_t *map_off = row_offset, *map_rows = n_rows;
+  const int *count = nullptr;
+  void *cfeat = h->ws + h->L.cfeat;
+  if (compact) {
+    FeatPtrs fp;
+    std::memset(&fp, 0, sizeof(fp));
+    for (int j = 0; j < c.n_sel; ++j) fp.p[j] = target_feats[j];
+    int *coff = at<int>(h, h->L.coff), *crows = at<int>(h, h->L.crows);
+    int *ccount = at<int>(h, h->L.ccount);
+    if (int st = timed(h, "inject_compact", s, [&] {
+          return launch_inject_compact(batch, total_rows, fp, c.n_sel, c.target_hidden, row_offset,
+                                       n_rows, cfeat, coff, crows, ccount, err, s);
+        }))
+      return st;
+    map_off = coff;
+    map_rows = crows;
+    count = ccount;
+  }
   for (int64_t r0 = 0; r0 < total_rows; r0 += c.max_rows) {
     const int rows = (int)std::min<int64_t>(c.max_rows, total_rows - r0);
     int st = 0;
@@ -530,11 +568,20 @@ int dflash_inject_context(dflash_handle *h, const dflash_kv *kv, int32_t batch, 
     GemmProblem prog[2];
     GemmProblem &P = prog[0];
     std::memset(&P, 0, sizeof(P));
-    for (int j = 0; j < c.n_sel; ++j)
-      P.A.ptr[j] = (const char *)target_feats[j] + (size_t)r0 * c.target_hidden * h->es;
-    P.A.ld = c.target_hidden;
-    P.A.k_per_src = c.target_hidden;
-    P.A.n_src = c.n_sel;
+    if (compact) {
+      // one source: the gathered rows hold the selected layers side by side
+      P.A.ptr[0] = cfeat;
+      P.A.ld = (int64_t)c.n_sel * c.target_hidden;
+      P.A.k_per_src = c.n_sel * c.target_hidden;
+      P.A.n_src = 1;
+      P.M_dev = count;
+    } else {
+      for (int j = 0; j < c.n_sel; ++j)
+        P.A.ptr[j] = (const char *)target_feats[j] + (size_t)r0 * c.target_hidden * h->es;
+      P.A.ld = c.target_hidden;
+      P.A.k_per_src = c.target_hidden;
+      P.A.n_src = c.n_sel;
+    }
     P.M = rows;
     P.K = c.n_sel * c.target_hidden;
     EpiParams e = epi_base(h, EPI_STORE_NORM);
@@ -548,6 +595,7 @@ int dflash_inject_context(dflash_handle *h, const dflash_kv *kv, int32_t batch, 
     // a3: every layer's K/V projection of hidden_norm(y) + k-norm + RoPE + paged scatter
     auto kv_problem = [&](int l0) {
       GemmProblem Q = problem_1src(yg, H, rows, H);
+      Q.M_dev = count;
       for (int l = l0; l < std::min(c.n_layers, l0 + kMaxSeg); ++l) {
         EpiParams k = epi_base(h, EPI_KV_CACHE);
         k.N = 2 * kvd;
@@ -573,8 +621,8 @@ int dflash_inject_context(dflash_handle *h, const dflash_kv *kv, int32_t batch, 
     inj.B = batch;
     inj.row0 = (int)r0;
     inj.rows = rows;
-    inj.row_offset = row_offset;
-    inj.n_rows = n_rows;
+    inj.row_offset = map_off;
+    inj.n_rows = map_rows;
     inj.kv_len = kv->kv_len;
     inj.page_table = kv->page_table;
     inj.pages_per_req = kv->pages_per_req;

@@ -73,6 +73,10 @@ struct Phase {
   int G;                          // CTAs sharing this phase (<= gridDim.x, <= total_iters)
   long long total_iters;
   int nfull;                      // whole tiles per CTA in full waves (see cta_sched)
+  // M_dev: row count on the device (<= M); the schedule fields above are then
+  // recomputed in the kernel from it (nfeat feature tiles per token tile)
+  const int *M_dev;
+  int nfeat;
 };
 
 struct Params {
@@ -293,7 +297,19 @@ __device__ __forceinline__ PhaseScalars load_scalars(const Phase &ph) {
   ps.nfull = ph.nfull;
   ps.nstep = ph.nstep;
   ps.total = ph.total_iters;
-  ps.tail_base = (long long)ph.nfull * ph.G * ph.KB;
+  if (ph.M_dev) {
+    // row count written by the previous kernel (the caller has waited for
+    // it): the same schedule the host computes for a known M
+    const int M = min(ph.M, max(0, __ldcg(ph.M_dev)));
+    ps.M = M;
+    ps.m_tiles = (M + ph.bnt - 1) / ph.bnt;
+    const int tiles = ph.nfeat * ps.m_tiles;
+    ps.total = (long long)tiles * ph.KB;
+    ps.G = (int)max(1LL, min((long long)gridDim.x, ps.total));
+    ps.nfull = ps.m_tiles > 1 && ph.nseg > 0 ? tiles / ps.G : 0;
+    if (ps.nfull > 0 && 2 * (tiles - ps.nfull * ps.G) < ps.G) --ps.nfull;
+  }
+  ps.tail_base = (long long)ps.nfull * ps.G * ph.KB;
   ps.tail_total = ps.total - ps.tail_base;
   ps.Gt = (int)(ps.tail_total < ps.G ? (ps.tail_total > 0 ? ps.tail_total : 1) : ps.G);
 #pragma unroll
@@ -1033,6 +1049,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
       int pend_s[C::SLOTS], pend_k[C::SLOTS], pend_m[C::SLOTS];
       for (int ph_i = 0; ph_i < p.nph && ok; ++ph_i) {
         const Phase &ph = p.ph[ph_i];
+        if (ph.M_dev) pdl_wait();   // the row count comes from the previous kernel
         const PhaseScalars ps = load_scalars(ph);
         if constexpr (PAIRABLE)
           ok = ps.pair ? produce_phase<C, C::SPLIT ? 3 : 2, BN>(p, ph, ps, ph_i, cta, it, slots,
@@ -1058,6 +1075,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
       int seg_i = 0;
       bool ok = true;
       for (int ph_i = 0; ph_i < p.nph && ok; ++ph_i) {
+        if (p.ph[ph_i].M_dev) pdl_wait();
         const PhaseScalars ps = load_scalars(p.ph[ph_i]);
         const Sched S = cta_sched(ps, cta);
         const int ns = ps.pair ? 2 : 1;
@@ -1108,14 +1126,13 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
     bool alive = true;
     for (int ph_i = 0; ph_i < p.nph && alive; ++ph_i) {
       const Phase &ph = p.ph[ph_i];
+      if (ph_i == 0 || ph.M_dev) pdl_wait();
       const PhaseScalars ps = load_scalars(ph);
       const int np = ps.pair ? 2 : 1;
       // this phase reads what the previous kernel / every CTA's previous phase
       // wrote; for the latter one thread spins with acquire semantics and the
       // named barrier orders the other epilogue threads after it
-      if (ph_i == 0) {
-        pdl_wait();
-      } else if (!epi_all(tid == 0 ? grid_wait(p.grid_bar, (unsigned)(ph_i * G)) : true)) {
+      if (ph_i > 0 && !epi_all(tid == 0 ? grid_wait(p.grid_bar, (unsigned)(ph_i * G)) : true)) {
         if (tid == 0) raise_error(p.err, DFLASH_DERR_TIMEOUT);
         alive = false;
         break;
@@ -1447,6 +1464,8 @@ bool build_phase(tc::Phase &ph, const GemmProblem &P, int BN, int counter_off) {
   ph.nseg = P.nseg;
   ph.pair = pair ? 1 : 0;
   ph.nstep = hp ? 256 : 128;
+  ph.M_dev = P.M_dev;
+  ph.nfeat = ntiles;
   ph.M = P.M;
   ph.K = P.K;
   ph.KB = P.K / tc::BK;

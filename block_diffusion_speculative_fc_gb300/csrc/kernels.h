@@ -93,6 +93,10 @@ struct GemmProblem {
   int M, K;
   int nseg;
   GemmSeg seg[kMaxSeg];
+  // optional device row count (<= M), read by the launch after its
+  // predecessor finished: tiles past it are not scheduled (M bounds the
+  // schedule and the scratch)
+  const int *M_dev;
 };
 
 struct AttnParams {
@@ -223,6 +227,7 @@ cudaError_t launch_gemm_program(const GemmProblem *probs, int n, float *partials
 size_t gemm_tc_partials_bytes();
 int gemm_tc_trace_slots();   // timestamps per CTA written by a traced launch
 int gemm_tc_tiles(int n_tiles, int M, bool pair);
+int gemm_tc_num_sms();   // SMs of the current device (cached)
 void gemm_tc_set_head_pairs(bool on);   // QKV head-pair tiles (default on)
 cudaError_t prepare_gemm_tc();
 cudaError_t launch_attention_mma(const AttnParams &p, const AttnScratch &w, cudaStream_t s);
@@ -251,6 +256,17 @@ cudaError_t launch_inject_prep(int B, int row0, int rows, const int *row_offset,
                                const int *kv_len, const int *page_table, int pages_per_req,
                                int n_pages, int page_size, int max_position, int draft_window,
                                int *row_slot, int *row_pos, unsigned int *err, cudaStream_t s);
+// Prefix-valid compaction of the injection's feature rows: the rows of every
+// request (row_offset[b] .. + n_rows[b] - 1 of the n_sel buffers [total_rows,
+// th]) go, in request order, to rows coff[b] .. coff[b] + crows[b] - 1 of x
+// [rows, n_sel * th] (bf16); crows[b] = n_rows[b], or 0 (flagged) when those
+// rows are not inside the buffers; *count = the rows kept.
+struct FeatPtrs {
+  const void *p[kMaxSrc];
+};
+cudaError_t launch_inject_compact(int B, int total_rows, const FeatPtrs &src, int n_sel, int th,
+                                  const int *row_offset, const int *n_rows, void *x, int *coff,
+                                  int *crows, int *count, unsigned int *err, cudaStream_t s);
 cudaError_t launch_inject_finalize(int B, int total_rows, const int *row_offset,
                                    const int *n_rows, int *kv_len, int capacity,
                                    unsigned int *err, cudaStream_t s);

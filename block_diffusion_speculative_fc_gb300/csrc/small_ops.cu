@@ -1,5 +1,7 @@
 // Row-wise kernels around the GEMMs: block embedding, RMSNorm, argmax
 // finalisation, injection row mapping and the RoPE table.
+#include <algorithm>
+
 #include "common.cuh"
 #include "inject_rows.cuh"
 #include "kernels.h"
@@ -226,6 +228,74 @@ cudaError_t launch_inject_finalize(int B, int total_rows, const int *row_offset,
   if (B <= 0) return cudaSuccess;
   return launch_pdl(inject_finalize_kernel, dim3((B + 127) / 128), dim3(128), 0, s, B, total_rows,
                     row_offset, n_rows, kv_len, capacity, err);
+}
+
+// Prefix-valid compaction ("Inside SGLang", Step 7: of a verify block only
+// the accepted rows reach the draft cache).  Every block scans the (few)
+// requests itself in shared memory; then compact row r of request b (the
+// last request whose compact offset is <= r) is copied from feature row
+// row_offset[b] + r - coff[b] of each of the n_sel buffers, 16 bytes per
+// thread and step.  A request with negative n_rows, or rows outside
+// [0, total_rows), keeps none (flagged, as the length update would).
+__global__ void inject_compact_kernel(int B, int total_rows, FeatPtrs src, int n_sel, int th,
+                                      const int *__restrict__ row_offset,
+                                      const int *__restrict__ n_rows, bf16 *__restrict__ x,
+                                      int *__restrict__ coff, int *__restrict__ crows,
+                                      int *__restrict__ count, unsigned int *err) {
+  pdl_wait();
+  extern __shared__ int sm[];
+  int *s_off = sm, *s_n = sm + B, *s_c = sm + 2 * B;   // s_c: B + 1 entries
+  for (int b = threadIdx.x; b < B; b += blockDim.x) {
+    const int n = n_rows[b], off = row_offset[b];
+    const bool inside = off >= 0 && (int64_t)off + n <= (int64_t)total_rows;
+    const bool keep = n > 0 && inside;
+    if (blockIdx.x == 0 && (n < 0 || (n > 0 && !inside))) raise_error(err, DFLASH_DERR_ROW_RANGE);
+    s_off[b] = off;
+    s_n[b] = keep ? n : 0;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int b = 0; b < B; ++b) {
+      s_c[b] = acc;
+      acc += s_n[b];
+    }
+    s_c[B] = acc;
+  }
+  __syncthreads();
+  if (blockIdx.x == 0) {
+    for (int b = threadIdx.x; b < B; b += blockDim.x) {
+      coff[b] = s_c[b];
+      crows[b] = s_n[b];
+    }
+    if (threadIdx.x == 0) *count = s_c[B];
+  }
+  const int total = s_c[B];
+  const int vecs = th >> 3;   // 16-byte vectors per source row
+  for (int r = blockIdx.x; r < total; r += gridDim.x) {
+    int lo = 0, hi = B - 1;   // last b with s_c[b] <= r (it has s_n[b] > 0)
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_c[mid] <= r) lo = mid;
+      else hi = mid - 1;
+    }
+    const int64_t row = (int64_t)s_off[lo] + (r - s_c[lo]);
+    uint4 *dst = reinterpret_cast<uint4 *>(x + (int64_t)r * n_sel * th);
+    for (int j = 0; j < n_sel; ++j) {
+      const uint4 *sp = reinterpret_cast<const uint4 *>((const bf16 *)src.p[j] + row * th);
+      for (int v = threadIdx.x; v < vecs; v += blockDim.x) dst[j * vecs + v] = __ldg(sp + v);
+    }
+  }
+}
+
+cudaError_t launch_inject_compact(int B, int total_rows, const FeatPtrs &src, int n_sel, int th,
+                                  const int *row_offset, const int *n_rows, void *x, int *coff,
+                                  int *crows, int *count, unsigned int *err, cudaStream_t s) {
+  if (B <= 0 || n_sel <= 0 || n_sel > kMaxSrc || th % 8) return cudaErrorInvalidValue;
+  const int grid = std::max(1, std::min(std::max(total_rows, 1), 2 * gemm_tc_num_sms()));
+  const size_t smem = sizeof(int) * (3 * (size_t)B + 1);
+  return launch_pdl(inject_compact_kernel, dim3(grid), dim3(256), smem, s, B, total_rows, src, n_sel,
+                    th, row_offset, n_rows, (bf16 *)x, coff, crows, count, err);
 }
 
 // ---------------------------------------------------------------------------
