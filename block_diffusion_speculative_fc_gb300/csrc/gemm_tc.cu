@@ -624,27 +624,97 @@ __device__ __forceinline__ InjectArgs inject_args(const ProgramInject &j) {
   return a;
 }
 
+// Row bookkeeping of the block embedding (once per row): its position,
+// range checks and the cleared argmax key.
+__device__ __forceinline__ void embed_row_setup(const ProgramEmbed &e, unsigned int *err, int m,
+                                                bool bad_id) {
+  const int b = m / e.S, j = m - b * e.S;
+  const int pos = e.kv_len[b] + j;
+  const bool bad_pos = pos < 0 || pos >= e.max_position;
+  if (bad_id) raise_error(err, DFLASH_DERR_TOKEN_RANGE);
+  if (bad_pos) raise_error(err, DFLASH_DERR_POSITION);
+  e.row_pos[m] = bad_pos ? 0 : pos;
+  e.keys[m] = 0ull;
+}
+
 // The block embedding of a program's first phase ("Inside SGLang", Step 3:
 // input id = anchor at j = 0, else mask_token_id; position = prefix length +
 // j), with the first layer's deferred RMSNorm operand: x, x * g and the sum
-// of squares of every 128-feature part of x.  Work item = (row, part), one
-// per epilogue warp, spread over the grid.
+// of squares of every 128-feature part of x.  Work item = (row, 256-feature
+// chunk): a lane holds 8 features (16-byte loads of the table row and the
+// gain) and a warp takes four items per step, issuing all of their loads
+// before using any -- the loads' latency, not bandwidth, bounds this phase.
+// Lanes 0-15 hold the chunk's first 128-feature part, 16-31 its second.
+// (Feature counts that are not a multiple of 256, or unaligned buffers:
+// one (row, 128-feature part) item per warp and step.)
 __device__ __forceinline__ void program_embed(const ProgramEmbed &e, unsigned int *err, int gwarp,
                                               int nwarps, int lane) {
+  const bool vec = (e.H & 255) == 0 && (((uintptr_t)e.table | (uintptr_t)e.gain |
+                                          (uintptr_t)e.x | (uintptr_t)e.xg) & 15) == 0;
+  if (vec) {
+    constexpr int U = 4;
+    const int chunks = e.H >> 8, items = e.M * chunks;
+    for (int base = gwarp; base < items; base += nwarps * U) {
+      int m[U], t[U], id[U];
+#pragma unroll
+      for (int k = 0; k < U; ++k) {
+        const int item = base + k * nwarps;
+        const bool live = item < items;
+        m[k] = live ? item / chunks : 0;
+        t[k] = live ? item - m[k] * chunks : 0;
+        const int b = m[k] / e.S, j = m[k] - b * e.S;
+        id[k] = !live ? 0 : (j == 0 ? e.anchor[b] : e.mask_id);
+      }
+      uint4 tv[U], gv[U];
+#pragma unroll
+      for (int k = 0; k < U; ++k) {
+        const bool live = base + k * nwarps < items;
+        const bool bad = id[k] < 0 || id[k] >= e.vocab;
+        const int c = t[k] * 256 + lane * 8;
+        tv[k] = make_uint4(0u, 0u, 0u, 0u);
+        gv[k] = tv[k];
+        if (live && !bad)
+          tv[k] = *reinterpret_cast<const uint4 *>((const bf16 *)e.table + (int64_t)id[k] * e.H + c);
+        if (live) gv[k] = *reinterpret_cast<const uint4 *>((const bf16 *)e.gain + c);
+      }
+#pragma unroll
+      for (int k = 0; k < U; ++k) {
+        if (base + k * nwarps >= items) continue;   // the same for the whole warp
+        if (t[k] == 0 && lane == 0) embed_row_setup(e, err, m[k], id[k] < 0 || id[k] >= e.vocab);
+        const int c = t[k] * 256 + lane * 8;
+        const bf16 *vb = reinterpret_cast<const bf16 *>(&tv[k]);
+        const bf16 *gb = reinterpret_cast<const bf16 *>(&gv[k]);
+        float v[8];
+        uint4 o;
+        __nv_bfloat162 *o2 = reinterpret_cast<__nv_bfloat162 *>(&o);
+        float ss = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          v[i] = __bfloat162float(vb[i]);
+          ss += v[i] * v[i];
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          o2[i] = __floats2bfloat162_rn(v[2 * i] * __bfloat162float(gb[2 * i]),
+                                        v[2 * i + 1] * __bfloat162float(gb[2 * i + 1]));
+        float *xr = e.x + (int64_t)m[k] * e.H + c;
+        reinterpret_cast<float4 *>(xr)[0] = make_float4(v[0], v[1], v[2], v[3]);
+        reinterpret_cast<float4 *>(xr)[1] = make_float4(v[4], v[5], v[6], v[7]);
+        *reinterpret_cast<uint4 *>((bf16 *)e.xg + (int64_t)m[k] * e.H + c) = o;
+#pragma unroll
+        for (int off = 8; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        if ((lane & 15) == 0) e.ssq[(int64_t)(2 * t[k] + (lane >> 4)) * e.ssq_ld + m[k]] = ss;
+      }
+    }
+    return;
+  }
   const int parts = e.H >> 7;
   for (int item = gwarp; item < e.M * parts; item += nwarps) {
     const int m = item / parts, t = item - m * parts;
     const int b = m / e.S, j = m - b * e.S;
     const int id = j == 0 ? e.anchor[b] : e.mask_id;
     const bool bad_id = id < 0 || id >= e.vocab;
-    if (t == 0 && lane == 0) {
-      const int pos = e.kv_len[b] + j;
-      const bool bad_pos = pos < 0 || pos >= e.max_position;
-      if (bad_id) raise_error(err, DFLASH_DERR_TOKEN_RANGE);
-      if (bad_pos) raise_error(err, DFLASH_DERR_POSITION);
-      e.row_pos[m] = bad_pos ? 0 : pos;
-      e.keys[m] = 0ull;
-    }
+    if (t == 0 && lane == 0) embed_row_setup(e, err, m, bad_id);
     const int c = t * 128 + lane * 4;
     const bf16 *src = (const bf16 *)e.table + (int64_t)(bad_id ? 0 : id) * e.H + c;
     const bf16 *gp = (const bf16 *)e.gain + c;
@@ -668,28 +738,52 @@ __device__ __forceinline__ void program_embed(const ProgramEmbed &e, unsigned in
 // Step 4: the lm_head reads the draft's final-normed hidden state): the
 // rows are rounded to bf16 after the row scale, so the lm_head's operand is
 // exactly the normalised hidden state the caller may receive.  Work item =
-// (row, 256-feature chunk), one per epilogue warp; each lane 8 features.
+// (row, 256-feature chunk), each lane 8 features; a warp takes four items
+// per step and issues all their loads (sums of squares, x, gains) before
+// using any, since the loads' latency bounds this phase.
 __device__ __forceinline__ void program_norm(const ProgramNorm &q, int gwarp, int nwarps, int lane) {
-  const int chunks = q.H >> 8, parts = q.H >> 7;
-  for (int item = gwarp; item < q.M * chunks; item += nwarps) {
-    const int m = item / chunks, c0 = (item - m * chunks) * 256 + lane * 8;
-    float ss = 0.f;
-    for (int t = lane; t < parts; t += 32) ss += __ldcg(q.ssq + (int64_t)t * q.ssq_ld + m);
-    const float r = rsqrtf(warp_sum(ss) / (float)q.H + q.eps);
-    const float4 *xr = reinterpret_cast<const float4 *>(q.x + (int64_t)m * q.H + c0);
-    const float4 a = __ldcg(xr), b = __ldcg(xr + 1);
-    const uint4 gw = *reinterpret_cast<const uint4 *>((const bf16 *)q.gain + c0);
-    const __nv_bfloat162 *g2 = reinterpret_cast<const __nv_bfloat162 *>(&gw);
-    const float2 g0 = __bfloat1622float2(g2[0]), g1 = __bfloat1622float2(g2[1]);
-    const float2 g2f = __bfloat1622float2(g2[2]), g3 = __bfloat1622float2(g2[3]);
-    uint4 o;
-    __nv_bfloat162 *o2 = reinterpret_cast<__nv_bfloat162 *>(&o);
-    o2[0] = __floats2bfloat162_rn(a.x * r * g0.x, a.y * r * g0.y);
-    o2[1] = __floats2bfloat162_rn(a.z * r * g1.x, a.w * r * g1.y);
-    o2[2] = __floats2bfloat162_rn(b.x * r * g2f.x, b.y * r * g2f.y);
-    o2[3] = __floats2bfloat162_rn(b.z * r * g3.x, b.w * r * g3.y);
-    *reinterpret_cast<uint4 *>((bf16 *)q.out + (int64_t)m * q.H + c0) = o;
-    if (q.out2) *reinterpret_cast<uint4 *>((bf16 *)q.out2 + (int64_t)m * q.H + c0) = o;
+  constexpr int U = 4;
+  const int chunks = q.H >> 8, parts = q.H >> 7, items = q.M * chunks;
+  for (int base = gwarp; base < items; base += nwarps * U) {
+    float ss[U];
+    float4 xa[U], xb[U];
+    uint4 gw[U];
+#pragma unroll
+    for (int k = 0; k < U; ++k) {
+      const int item = base + k * nwarps;
+      const bool live = item < items;
+      const int m = live ? item / chunks : 0;
+      const int c0 = (item - m * chunks) * 256 + lane * 8;
+      ss[k] = 0.f;
+      xa[k] = xb[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      gw[k] = make_uint4(0u, 0u, 0u, 0u);
+      if (live) {
+        for (int t = lane; t < parts; t += 32) ss[k] += __ldcg(q.ssq + (int64_t)t * q.ssq_ld + m);
+        const float4 *xr = reinterpret_cast<const float4 *>(q.x + (int64_t)m * q.H + c0);
+        xa[k] = __ldcg(xr);
+        xb[k] = __ldcg(xr + 1);
+        gw[k] = *reinterpret_cast<const uint4 *>((const bf16 *)q.gain + c0);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < U; ++k) {
+      const int item = base + k * nwarps;
+      if (item >= items) continue;   // the same for the whole warp
+      const int m = item / chunks, c0 = (item - m * chunks) * 256 + lane * 8;
+      const float r = rsqrtf(warp_sum(ss[k]) / (float)q.H + q.eps);
+      const __nv_bfloat162 *g2 = reinterpret_cast<const __nv_bfloat162 *>(&gw[k]);
+      const float2 g0 = __bfloat1622float2(g2[0]), g1 = __bfloat1622float2(g2[1]);
+      const float2 g2f = __bfloat1622float2(g2[2]), g3 = __bfloat1622float2(g2[3]);
+      const float4 a = xa[k], b = xb[k];
+      uint4 o;
+      __nv_bfloat162 *o2 = reinterpret_cast<__nv_bfloat162 *>(&o);
+      o2[0] = __floats2bfloat162_rn(a.x * r * g0.x, a.y * r * g0.y);
+      o2[1] = __floats2bfloat162_rn(a.z * r * g1.x, a.w * r * g1.y);
+      o2[2] = __floats2bfloat162_rn(b.x * r * g2f.x, b.y * r * g2f.y);
+      o2[3] = __floats2bfloat162_rn(b.z * r * g3.x, b.w * r * g3.y);
+      *reinterpret_cast<uint4 *>((bf16 *)q.out + (int64_t)m * q.H + c0) = o;
+      if (q.out2) *reinterpret_cast<uint4 *>((bf16 *)q.out2 + (int64_t)m * q.H + c0) = o;
+    }
   }
 }
 
