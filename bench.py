@@ -116,7 +116,7 @@ def algorithmic(cfg, B, ctx, commit_mean, kv_fp8=False, draft_window=0):
     qkv = cfg.qkv_rows
     qd, kvd, I, V = cfg.n_heads * D, cfg.n_kv_heads * D, cfg.intermediate, cfg.vocab
     K_fc = cfg.n_sel * cfg.target_hidden
-    rows = B * S  # dense verify block; commit rows are written
+    rows = B * commit_mean  # the committed rows are projected and written
     if np.ndim(ctx) == 0:
         ctx = np.full(B, float(ctx))
     ctx_keys = visible_keys(cfg, ctx, draft_window)          # summed over the batch
@@ -130,7 +130,7 @@ def algorithmic(cfg, B, ctx, commit_mean, kv_fp8=False, draft_window=0):
                       4 * S * qd * (ctx_keys + B * S)),
         "gemm_fc": (es * (H * K_fc + rows * K_fc) + 4 * rows * H, 2 * rows * H * K_fc),
         "gemm_kv_inject": (es * (cfg.n_layers * 2 * kvd * H + rows * H)
-                           + kvb * B * commit_mean * cfg.n_layers * 2 * kvd,
+                           + kvb * rows * cfg.n_layers * 2 * kvd,
                            2 * rows * cfg.n_layers * 2 * kvd * H),
         # the final RMSNorm phase: x (fp32) read, the normalised rows written
         "final_norm": ((4 + es) * M * H + 4 * M * (H // 128), 0),

@@ -41,7 +41,8 @@ def test_program_bytes_are_the_streamed_weights_plus_activations():
     # the figures of the design notes (MB per launch)
     assert fam["gemm_layer_program"][0] / 1e6 == pytest.approx(388.3, abs=0.1)
     assert fam["gemm_last_program"][0] / 1e6 == pytest.approx(1582.8, abs=0.1)
-    assert fam["gemm_inject_program"][0] / 1e6 == pytest.approx(252.8, abs=0.1)
+    # (the injection projects the committed rows only: 6.4 of the block's 16)
+    assert fam["gemm_inject_program"][0] / 1e6 == pytest.approx(252.2, abs=0.1)
     # a program is the sum of its GEMMs
     parts = [fam[n] for n in ("gemm_o", "gemm_gate_up", "gemm_down", "gemm_qkv")]
     assert fam["gemm_layer_program"] == tuple(sum(p[i] for p in parts) for i in range(2))
