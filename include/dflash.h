@@ -222,7 +222,12 @@ int dflash_bind_workspace(dflash_handle *h, void *dev_ptr, size_t bytes, dflash_
  * positions kv_len[b] .. kv_len[b]+n_rows[b]-1 (k-normed and rotated K,
  * plain V); then kv_len[b] += n_rows[b].  Rows of the feature buffers that
  * belong to no request (e.g. rejected rows of a dense [B, S] verify block)
- * are never written: this is the prefix-valid commit of Step 7.
+ * are never written: this is the prefix-valid commit of Step 7.  In bf16
+ * with fused launches (the default), when total_rows is above 128 and at
+ * most min(max_rows, max_batch * block_size), they are not projected either:
+ * the rows of the requests are first gathered into the workspace (16-byte
+ * aligned feature pointers).  Results do not depend on which way a call
+ * goes beyond float rounding.
  *   batch        <= max_batch
  *   total_rows   rows in each feature buffer (an upper bound of every row
  *                index used); processed in chunks of max_rows
