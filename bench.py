@@ -149,10 +149,23 @@ def algorithmic(cfg, B, ctx, commit_mean, kv_fp8=False, draft_window=0):
     return fam
 
 
-def source_hash():
+# the sources a kernel family's launches are built from (its kernels, the
+# headers they include, and the host code that sets the launches up)
+KERNEL_SOURCES = {
+    "gemm": ("gemm_tc.cu", "epilogue.cuh", "inject_rows.cuh", "common.cuh", "kernels.h",
+             "dflash_api.cu"),
+    "attention": ("attention_tc.cu", "attention_mma.cu", "attention_simt.cu", "common.cuh",
+                  "kernels.h", "dflash_api.cu"),
+}
+
+
+def source_hash(kernel=None):
+    """Hash of the sources of a kernel family (launch names starting with
+    "gemm" or "attention"); of every source file when kernel is None."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "block_diffusion_speculative_fc_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    fam = next((v for k, v in KERNEL_SOURCES.items() if kernel and kernel.startswith(k)), None)
+    for f in sorted(fam if fam else os.listdir(csrc)):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
@@ -168,7 +181,7 @@ def traffic_for(kernel, workload):
     except Exception:
         return None
     e = t.get(workload, {}).get(kernel)
-    if not e or e.get("source_hash") != source_hash():
+    if not e or e.get("source_hash") != source_hash(kernel):
         return None
     return e.get("dram_bytes_per_launch")
 
