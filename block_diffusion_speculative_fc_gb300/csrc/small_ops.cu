@@ -237,6 +237,9 @@ cudaError_t launch_inject_finalize(int B, int total_rows, const int *row_offset,
 // row_offset[b] + r - coff[b] of each of the n_sel buffers, 16 bytes per
 // thread and step.  A request with negative n_rows, or rows outside
 // [0, total_rows), keeps none (flagged, as the length update would).
+// Requests may share feature rows; the compact rows never exceed
+// total_rows (the operand's size): rows past it are dropped from the last
+// requests and flagged.
 __global__ void inject_compact_kernel(int B, int total_rows, FeatPtrs src, int n_sel, int th,
                                       const int *__restrict__ row_offset,
                                       const int *__restrict__ n_rows, bf16 *__restrict__ x,
@@ -256,11 +259,16 @@ __global__ void inject_compact_kernel(int B, int total_rows, FeatPtrs src, int n
   __syncthreads();
   if (threadIdx.x == 0) {
     int acc = 0;
+    bool trimmed = false;
     for (int b = 0; b < B; ++b) {
       s_c[b] = acc;
-      acc += s_n[b];
+      const int keep = min(s_n[b], total_rows - acc);
+      trimmed |= keep < s_n[b];
+      s_n[b] = keep;
+      acc += keep;
     }
     s_c[B] = acc;
+    if (trimmed && blockIdx.x == 0) raise_error(err, DFLASH_DERR_ROW_RANGE);
   }
   __syncthreads();
   if (blockIdx.x == 0) {

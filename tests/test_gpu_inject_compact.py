@@ -47,3 +47,28 @@ def test_dense_block_injection(fused):
     assert np.array_equal(run.kv.kv_len.cpu().numpy(), expect)
     run.compare_kv()
     assert run.sess.error() == 0
+
+
+def test_gathered_rows_never_exceed_the_feature_rows():
+    """Requests may share feature rows, but the gathered rows stop at the
+    buffer's row count: here the commits sum to 208 of 192 rows, so the last
+    request keeps its first 16 rows (flagged); every written row is checked."""
+    cfg = QWEN_MINI
+    B, S = 12, cfg.block_size
+    ctx = np.random.default_rng(37).integers(10, 200, B)
+    run = CycleRun(cfg, B, ctx, cycles=0, seed=37, gains="random", permuted=True, fused=True)
+    run.prefill()
+    assert run.sess.error() == 0
+    offs = np.arange(B) * S
+    n = np.full(B, S)
+    offs[-1], n[-1] = 0, 2 * S                      # rows 0 .. 31, shared with request 0
+    feats = make_features(cfg, B * S, 37, "shared-rows", device="cuda")
+    run.sess.inject(run.kv, feats, i32(offs), i32(n))
+    assert run.sess.error() & ROW_RANGE
+    kept = n.copy()
+    kept[-1] = B * S - int(n[:-1].sum())            # 16
+    for b in range(B):
+        run.ctx[b].inject(run._feat_rows(feats, slice(int(offs[b]), int(offs[b] + kept[b]))), run.Wn)
+    assert np.array_equal(run.kv.kv_len.cpu().numpy(), ctx + kept)
+    run.compare_kv()
+    assert run.sess.error() == 0
