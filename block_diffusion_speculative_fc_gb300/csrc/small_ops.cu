@@ -289,9 +289,25 @@ __global__ void inject_compact_kernel(int B, int total_rows, FeatPtrs src, int n
     }
     const int64_t row = (int64_t)s_off[lo] + (r - s_c[lo]);
     uint4 *dst = reinterpret_cast<uint4 *>(x + (int64_t)r * n_sel * th);
-    for (int j = 0; j < n_sel; ++j) {
-      const uint4 *sp = reinterpret_cast<const uint4 *>((const bf16 *)src.p[j] + row * th);
-      for (int v = threadIdx.x; v < vecs; v += blockDim.x) dst[j * vecs + v] = __ldg(sp + v);
+    // the row's n_sel * vecs vectors, U per thread in flight at a time (all
+    // loads of a batch issued before its stores)
+    constexpr int U = 8;
+    const int total = n_sel * vecs, step = blockDim.x * U;
+    for (int v0 = threadIdx.x; v0 < total; v0 += step) {
+      uint4 t[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int v = v0 + u * blockDim.x;
+        if (v < total) {
+          const int j = v / vecs;
+          t[u] = __ldg(reinterpret_cast<const uint4 *>((const bf16 *)src.p[j] + row * th) + (v - j * vecs));
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int v = v0 + u * blockDim.x;
+        if (v < total) dst[v] = t[u];
+      }
     }
   }
 }
