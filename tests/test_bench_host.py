@@ -88,3 +88,21 @@ def test_attention_bytes_follow_the_cache_type_and_the_windows():
     keys = bench.visible_keys(kimi, np.full(8, 8192.0))
     assert keys == pytest.approx(8 * (5 * 2048 + 8192) / 6)
     assert S == 16
+
+
+def test_traffic_entries_follow_their_kernel_sources():
+    """The DRAM bytes of a committed capture stay valid only while the sources
+    of that kernel family are unchanged: every listed file exists, the GEMM
+    and attention families differ, and a launch name outside them hashes all
+    sources."""
+    import os
+    csrc = os.path.join(os.path.dirname(os.path.abspath(bench.__file__)),
+                        "block_diffusion_speculative_fc_gb300", "csrc")
+    for files in bench.KERNEL_SOURCES.values():
+        for f in files:
+            assert os.path.exists(os.path.join(csrc, f)), f
+    assert "gemm_tc.cu" in bench.KERNEL_SOURCES["gemm"]
+    assert "attention_tc.cu" in bench.KERNEL_SOURCES["attention"]
+    g, a = bench.source_hash("gemm_layer_program"), bench.source_hash("attention")
+    assert g != a and bench.source_hash("gemm_inject_program") == g
+    assert bench.source_hash() not in (g, a)
